@@ -1,0 +1,532 @@
+"""Benchmark: LoopVQ 0.5-bit decode attention, Ouro-1.4B-shaped serving step on one GB300.
+
+One step = one generated token through the whole looped stack: 4 loop steps x 24 layers =
+96 kvq_decode_attn calls, batch 64, 16 heads, context 6144 (8 sink + 759 index pages + 64
+recent per request), each layer with its own cache. Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload loopvq_b64_6k|loopvq_b8_32k|kivi_b16_4k|encode_32k|kivi_quant_32k]
+
+Under torchrun each rank runs its own replica on its own GPU (requests shard across GPUs
+with no collective on the data path); rank 0 prints the max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized-KV decode attn: effective HBM GB/s (% of GB300 peak), µs/step @B64 6K"
+D = 128
+
+
+# ------------------------------------------------------------------------------ workloads
+
+WORKLOADS = {
+    "loopvq_b64_6k": dict(kind="loopvq", B=64, H=16, L=6144, layers=24, T=4, Tc=2, G=16, recent=64,
+                          rho=(0.69, 0.94), n_splits=0,
+                          name="LoopVQ 0.5-bit serving decode, Ouro-1.4B-shaped: 24 layers x 4 loop steps, "
+                               "16 heads, D=128, Tc=2, G=16, batch 64, context 6144"),
+    "loopvq_b8_32k": dict(kind="loopvq", B=8, H=16, L=32768, layers=1, T=4, Tc=4, G=32, recent=256,
+                          rho=(0.85, 0.85), n_splits=0,
+                          name="LoopVQ 0.25-bit long-context decode: 16 heads, D=128, Tc=4, G=32, batch 8, "
+                               "context 32768, 4 loop steps"),
+    "kivi_b16_4k": dict(kind="kivi", B=16, H=32, n_quant=3968, n_resid=128, layers=32,
+                        name="KIVI 2-bit decode attention, Llama-2-7B-shaped: 32 layers, 32 heads, batch 16, "
+                             "context 4096 = 3968 quantized + 128 fp16"),
+    "encode_32k": dict(kind="encode", H=16, L=32768, T=4, Tc=2, G=16, groups=8,
+                       name="LoopVQ prefill encode: 16 heads x 8 groups x 2 loop blocks x 32768 tokens"),
+    "kivi_quant_32k": dict(kind="kivi_quant", H=16, L=32768,
+                           name="KIVI 2-bit quantize of K and V: 16 heads x 32768 tokens"),
+}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.p:
+            self.p.terminate()
+            try:
+                out, _ = self.p.communicate(timeout=5)
+            except Exception:
+                self.p.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ CPU oracle leg
+
+def _oracle_vq_job(args):
+    seed, n_pairs, L, T, Tc, G, recent = args
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    import numpy as np
+    import synth
+    from oracle import loopvq as olv
+    g = synth.rng(seed)
+    _, n_pages, _ = olv.prefill_split(L, 8, recent)
+    rhos = synth.rho_schedule(T)
+    pool = synth.loop_correlated(g, T, 512, D, rhos)
+    NG = D // (G // Tc)
+    cb_k = synth.sample_codebooks(g, pool, Tc, G)[0]
+    cb_v = synth.sample_codebooks(g, pool, Tc, G)[0]
+    inputs = []
+    for _ in range(n_pairs):
+        wk = np.zeros((L, D))
+        wv = np.zeros((L, D))
+        bf = olv.cache_positions(L, n_pages)[0]
+        wk[bf] = synth.bf16_round(g.standard_normal((len(bf), D)))
+        wv[bf] = synth.bf16_round(g.standard_normal((len(bf), D)))
+        inputs.append((synth.bf16_round(g.standard_normal(D)), synth.random_indices(g, (8 * n_pages, NG)),
+                       synth.random_indices(g, (8 * n_pages, NG)), wk, wv))
+    t0 = time.perf_counter()
+    for q, ik, iv, wk, wv in inputs:
+        olv.decode_attention(q, 1, Tc, L, n_pages, ik, iv, cb_k, cb_v, wk, wv)
+    return time.perf_counter() - t0
+
+
+def _oracle_kivi_job(args):
+    seed, n_pairs, nq, nr = args
+    import numpy as np
+    import synth
+    from oracle import kivi as okivi
+    g = synth.rng(seed)
+    inputs = []
+    for _ in range(n_pairs):
+        inputs.append((g.standard_normal(D), g.integers(0, 4, (nq, D)),
+                       (np.abs(g.standard_normal((nq // 32, D))) + 0.05).astype(np.float16),
+                       g.standard_normal((nq // 32, D)).astype(np.float16), g.integers(0, 4, (nq, D)),
+                       (np.abs(g.standard_normal((nq, D // 32))) + 0.05).astype(np.float16),
+                       g.standard_normal((nq, D // 32)).astype(np.float16),
+                       g.standard_normal((nr, D)).astype(np.float16), g.standard_normal((nr, D)).astype(np.float16)))
+    t0 = time.perf_counter()
+    for q, kc, ks, kz, vc, vs, vz, kr, vr in inputs:
+        okivi.decode_attention(q, kc, ks, kz, vc, vs, vz, kr, vr)
+    return time.perf_counter() - t0
+
+
+def cpu_oracle(wl, bytes_per_unit, unit_pairs_total, n_pairs, pool=None):
+    """Time the oracle on ``n_pairs`` (request, head) units on all host cores.
+    Returns (GB/s, cores, wall seconds)."""
+    cores = os.cpu_count() or 1
+    per = max(1, math.ceil(n_pairs / cores))
+    jobs = []
+    done = 0
+    k = 0
+    while done < n_pairs:
+        n = min(per, n_pairs - done)
+        if wl["kind"] == "loopvq":
+            jobs.append((1000 + k, n, wl["L"], wl["T"], wl["Tc"], wl["G"], wl["recent"]))
+        else:
+            jobs.append((1000 + k, n, wl["n_quant"], wl["n_resid"]))
+        done += n
+        k += 1
+    fn = _oracle_vq_job if wl["kind"] == "loopvq" else _oracle_kivi_job
+    own = pool is None
+    if own:
+        pool = mp.get_context("spawn").Pool(min(cores, len(jobs)))
+    secs = pool.map(fn, jobs)
+    if own:
+        pool.close()
+    # the jobs run side by side, one per core: the sample takes as long as the slowest job
+    wall = max(secs)
+    gbs = bytes_per_unit * n_pairs / wall / 1e9
+    return gbs, min(cores, len(jobs)), wall
+
+
+# ------------------------------------------------------------------------------ GPU legs
+
+def vq_call_bytes(B, H, n_pages, n_win, NB_unused=None):
+    """Algorithmic bytes of one LoopVQ decode-attention call (one layer, one loop step):
+    K and V index pages, bf16 window K and V, both fp32 codebook slices, the cos/sin rows the
+    call needs (one per page start and per window token), query and bf16 output."""
+    idx = B * H * n_pages * 128 * 2
+    win = B * H * n_win * D * 2 * 2
+    bt = H * 256 * D * 4 * 2
+    rope = (n_pages + n_win) * (D // 2) * 4 * 2
+    qo = B * H * D * 2 * 2
+    return idx + win + bt + rope + qo
+
+
+def setup_loopvq(wl, dev, seed):
+    import torch
+    import synth
+    from sub_bit_quantized_gb300 import kvq
+    B, H, L, NL, T, Tc, G, W = wl["B"], wl["H"], wl["L"], wl["layers"], wl["T"], wl["Tc"], wl["G"], wl["recent"]
+    n_pages = max(0, (L - 8 - W) // 8)
+    cfg = kvq.VqConfig(T=T, Tc=Tc, G=G, n_layers=NL, n_heads=H, recent=W, max_pages=n_pages, max_batch=B,
+                       max_ctx=L)
+    cache = kvq.VqCache(cfg, dev)
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    rhos = synth.rho_schedule(T, *wl["rho"])
+    cbk = torch.empty_like(cache.cb_k)
+    cbv = torch.empty_like(cache.cb_v)
+    chunk = max(1, min(B, (1 << 30) // (T * H * L * D * 4)))
+    for layer in range(NL):
+        outl = torch.randperm(D, generator=gen, device=dev)[:4]
+        # codebooks: sampled from one request's synthetic K/V of this layer, per head
+        xk = synth.torch_loop_correlated(gen, T, (H, L, D), rhos, dev)
+        xk[..., outl] *= 15.0
+        xv = synth.torch_loop_correlated(gen, T, (H, L, D), rhos, dev)
+        for h in range(H):
+            cbk[layer, :, h] = synth.torch_sample_codebooks(gen, xk[:, h], Tc, G)
+            cbv[layer, :, h] = synth.torch_sample_codebooks(gen, xv[:, h], Tc, G)
+        del xk, xv
+    cache.load_codebooks(cbk, cbv)
+    del cbk, cbv
+    for layer in range(NL):
+        outl = torch.randperm(D, generator=gen, device=dev)[:4]
+        for b0 in range(0, B, chunk):
+            nb = min(chunk, B - b0)
+            xk = synth.torch_loop_correlated(gen, T, (nb, H, L, D), rhos, dev)
+            xk[..., outl] *= 15.0
+            xk = xk.to(torch.bfloat16).contiguous()
+            xv = synth.torch_loop_correlated(gen, T, (nb, H, L, D), rhos, dev).to(torch.bfloat16).contiguous()
+            kvq.kvq_prefill_vq(cfg, cache, layer, xk, xv, b0, L)
+            del xk, xv
+    torch.cuda.synchronize(dev)
+    assert kvq.device_error() == 0
+    return cfg, cache, n_pages, (L - 8 * n_pages)
+
+
+def setup_kivi(wl, dev, seed):
+    import torch
+    from sub_bit_quantized_gb300 import kvq
+    B, H, NQ, NR, NL = wl["B"], wl["H"], wl["n_quant"], wl["n_resid"], wl["layers"]
+    cfg = kvq.KiviConfig(n_heads=H, residual=NR, max_batch=B, max_tokens=NQ)
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    caches = []
+    for layer in range(NL):
+        c = kvq.KiviCache(cfg, dev)
+        outl = torch.randperm(D, generator=gen, device=dev)[:6]
+        K = torch.randn((B, H, NQ + NR, D), generator=gen, device=dev)
+        K[..., outl] *= 20.0
+        K = K.half()
+        V = torch.randn((B, H, NQ + NR, D), generator=gen, device=dev).half()
+        kvq.kvq_quantize_kivi(cfg, kvq.PER_CHANNEL, K[:, :, :NQ].contiguous(), c.k_codes, c.k_scale, c.k_zero)
+        kvq.kvq_quantize_kivi(cfg, kvq.PER_TOKEN, V[:, :, :NQ].contiguous(), c.v_codes, c.v_scale, c.v_zero)
+        c.k_resid.copy_(K[:, :, NQ:])
+        c.v_resid.copy_(V[:, :, NQ:])
+        c.n_quant.fill_(NQ)
+        c.n_resid.fill_(NR)
+        caches.append(c)
+    torch.cuda.synchronize(dev)
+    return cfg, caches
+
+
+def kivi_call_bytes(B, H, NQ, NR):
+    codes = B * H * NQ * D // 4 * 2
+    ksz = B * H * (NQ // 32) * D * 2 * 2
+    vsz = B * H * NQ * (D // 32) * 2 * 2
+    res = B * H * NR * D * 2 * 2
+    qo = B * H * D * 2 * 2
+    return codes + ksz + vsz + res + qo
+
+
+def time_region(fn, steps, stream, dist):
+    import torch
+    if dist:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+    return ms
+
+
+def run_ours(args, wl, rank, world, dist, pool):
+    import torch
+    from sub_bit_quantized_gb300 import kvq
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    gpu_index = dev.index
+    hbm_peak, peak_src = peaks()
+    result = {}
+
+    if wl["kind"] in ("loopvq", "kivi"):
+        if wl["kind"] == "loopvq":
+            cfg, cache, n_pages, n_win = setup_loopvq(wl, dev, 1234 + rank)
+            B, H, NL, T = wl["B"], wl["H"], wl["layers"], wl["T"]
+            calls = [(l, t) for t in range(1, T + 1) for l in range(NL)]
+            call_bytes = vq_call_bytes(B, H, n_pages, n_win)
+            caches = None
+        else:
+            cfg, caches = setup_kivi(wl, dev, 1234 + rank)
+            B, H, NL = wl["B"], wl["H"], wl["layers"]
+            calls = [(l, 1) for l in range(NL)]
+            call_bytes = kivi_call_bytes(B, H, wl["n_quant"], wl["n_resid"])
+        n_calls = len(calls)
+        gen = torch.Generator(device=dev).manual_seed(99 + rank)
+        q = torch.randn((n_calls, B, H, D), generator=gen, device=dev).to(torch.bfloat16)
+        out = torch.empty((n_calls, B, H, D), dtype=torch.bfloat16, device=dev)
+        n_splits = kvq.kvq_decode_auto_splits(cfg, B)
+        ws = kvq.make_workspace(cfg, B, 0, dev)
+        dcalls = [kvq.DecodeCall(cfg, cache if caches is None else caches[l], l, t, q[i], out[i], 0, ws, stream)
+                  for i, (l, t) in enumerate(calls)]
+
+        def step():
+            for c in dcalls:
+                c()
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        assert kvq.device_error() == 0
+        with ClockSampler(gpu_index) as cs:
+            ms = time_region(step, args.steps, stream, dist)
+        clocks = cs.summary()
+        ms_step = ms / args.steps
+        step_bytes = call_bytes * n_calls
+        gbs = step_bytes / (ms_step * 1e-3) / 1e9 * world
+        per_launch_us = ms_step * 1e3 / n_calls
+        achieved = call_bytes / (per_launch_us * 1e-6) / 1e9
+
+        # end to end through the public API with host buffers: H2D of the step's queries from
+        # pinned memory, the 96 calls, D2H of the outputs
+        q_host = q.cpu().pin_memory()
+        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+        def step_e2e():
+            q.copy_(q_host, non_blocking=True)
+            step()
+            out_host.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            step_e2e()
+        e2e_steps = max(3, args.steps // 4)
+        ms_e2e = time_region(step_e2e, e2e_steps, stream, dist) / e2e_steps
+        e2e = {"value": round(step_bytes / (ms_e2e * 1e-3) / 1e9 * world, 1), "unit": "GB/s",
+               "h2d_bytes_per_step": q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2,
+               "ms_per_step": round(ms_e2e, 4)}
+        result.update(dict(value=round(gbs, 1), unit="GB/s", ms_per_step=round(ms_step, 4),
+                           us_per_call=round(per_launch_us, 2), gpu_launches=args.steps * n_calls,
+                           tokens_per_s=round(B * world / (ms_step * 1e-3), 1), e2e=e2e, clocks=clocks,
+                           roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                                     "traffic": None, "peak_source": peak_src,
+                                     "kernel": "vq_attn_kernel" if wl["kind"] == "loopvq" else "kivi_attn_kernel",
+                                     "bytes_per_launch": call_bytes},
+                           n_splits=n_splits))
+        if rank == 0 and not args.no_cpu_baseline:
+            n_pairs = 256 if wl["kind"] == "loopvq" else 128
+            unit_bytes = call_bytes / (B * H)
+            cgbs, cores, wall = cpu_oracle(wl, unit_bytes, B * H, n_pairs, pool)
+            result["cpu_baseline"] = {"value": round(cgbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                      "sample": f"{n_pairs} (request, head) units of one call, fp64 NumPy oracle, "
+                                                f"{wall:.1f} s wall on {cores} processes"}
+        return result
+
+    if wl["kind"] == "encode":
+        import synth
+        H, L, T, Tc, G = wl["H"], wl["L"], wl["T"], wl["Tc"], wl["G"]
+        cfg = kvq.VqConfig(T=T, Tc=Tc, G=G, n_heads=H, max_pages=L // 8, max_batch=1, max_ctx=L + 80)
+        gen = torch.Generator(device=dev).manual_seed(5)
+        x = synth.torch_loop_correlated(gen, T, (1, H, L, D), synth.rho_schedule(T), dev).to(torch.bfloat16)
+        cb = torch.stack([synth.torch_sample_codebooks(gen, x[:, 0, h].float(), Tc, G) for h in range(H)], 1)
+        idx = torch.zeros((cfg.NB, 1, H, L // 8, 128), dtype=torch.uint8, device=dev)
+        ties = torch.zeros(1, dtype=torch.int32, device=dev)
+        strides = (H * L * D, H * L * D, L * D)
+
+        def step():
+            kvq.kvq_encode_vq(cfg, x, strides, 0, 1, L, cb, idx, 0, 0, wl["groups"], ties, stream)
+
+        for _ in range(args.warmup):
+            step()
+        with ClockSampler(gpu_index) as cs:
+            ms = time_region(step, args.steps, stream, dist) / args.steps
+        n_vec = H * wl["groups"] * (T // Tc) * L
+        flops = 2.0 * n_vec * 256 * G
+        byts = n_vec * G * 2 + H * (T // Tc) * wl["groups"] * 256 * G * 4 + n_vec
+        result.update(dict(value=round(byts / (ms * 1e-3) / 1e9 * world, 1), unit="GB/s", ms_per_step=round(ms, 4),
+                           gpu_launches=args.steps, clocks=cs.summary(),
+                           vectors_per_s=round(n_vec / (ms * 1e-3), 1),
+                           roofline={"bound": "alu", "achieved": round(flops / (ms * 1e-3) / 1e12, 2),
+                                     "peak": round(152 * 128 * 2 * 2.07e9 / 1e12, 1), "unit": "TFLOP/s",
+                                     "frac": round(flops / (ms * 1e-3) / (152 * 128 * 2 * 2.07e9), 4),
+                                     "traffic": None, "kernel": "encode_kernel"}))
+        return result
+
+    if wl["kind"] == "kivi_quant":
+        H, L = wl["H"], wl["L"]
+        cfg = kvq.KiviConfig(n_heads=H, max_batch=1, max_tokens=L)
+        gen = torch.Generator(device=dev).manual_seed(6)
+        K = torch.randn((1, H, L, D), generator=gen, device=dev).half()
+        V = torch.randn((1, H, L, D), generator=gen, device=dev).half()
+        c = kvq.KiviCache(cfg, dev)
+
+        def step():
+            kvq.kvq_quantize_kivi(cfg, kvq.PER_CHANNEL, K, c.k_codes, c.k_scale, c.k_zero, 0, stream)
+            kvq.kvq_quantize_kivi(cfg, kvq.PER_TOKEN, V, c.v_codes, c.v_scale, c.v_zero, 0, stream)
+
+        for _ in range(args.warmup):
+            step()
+        with ClockSampler(gpu_index) as cs:
+            ms = time_region(step, args.steps, stream, dist) / args.steps
+        byts = 2 * H * L * D * 2 + 2 * H * L * D // 4 + H * (L // 32) * D * 4 + H * L * (D // 32) * 4
+        gbs = byts / (ms * 1e-3) / 1e9
+        result.update(dict(value=round(gbs * world, 1), unit="GB/s", ms_per_step=round(ms, 4),
+                           gpu_launches=2 * args.steps, clocks=cs.summary(),
+                           roofline={"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                                     "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                                     "kernel": "kivi_quant_*_kernel"}))
+        return result
+    raise ValueError(wl["kind"])
+
+
+def run_reference(args, wl, pool):
+    """The CPU oracle as the reference arm: each step is a bounded sample of the workload."""
+    if wl["kind"] == "loopvq":
+        n_pages = max(0, (wl["L"] - 8 - wl["recent"]) // 8)
+        call_bytes = vq_call_bytes(wl["B"], wl["H"], n_pages, wl["L"] - 8 * n_pages)
+        units = wl["B"] * wl["H"]
+    elif wl["kind"] == "kivi":
+        call_bytes = kivi_call_bytes(wl["B"], wl["H"], wl["n_quant"], wl["n_resid"])
+        units = wl["B"] * wl["H"]
+    else:
+        raise SystemExit(json.dumps({"impl": "reference", "unavailable": "the CPU oracle arm covers the decode "
+                                     "attention workloads only"}))
+    unit_bytes = call_bytes / units
+    n_pairs = 64
+    for _ in range(args.warmup):
+        cpu_oracle(wl, unit_bytes, units, 16, pool)
+    total = 0.0
+    cores = 1
+    for _ in range(args.steps):
+        _, cores, wall = cpu_oracle(wl, unit_bytes, units, n_pairs, pool)
+        total += wall
+    wall = total
+    gbs = unit_bytes * n_pairs * args.steps / wall / 1e9
+    return dict(value=round(gbs, 4), unit="GB/s", ms_per_step=round(wall / args.steps * 1e3, 3),
+                cpu_baseline={"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                              "sample": f"{n_pairs} (request, head) units of one call per step"},
+                e2e={"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                gpu_launches=0)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="loopvq_b64_6k", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    wl = dict(WORKLOADS[args.workload])
+    if args.layers > 0 and "layers" in wl:
+        wl["layers"] = args.layers
+        wl["name"] += f" [profiling subset: {args.layers} layer(s)]"
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    pool = None
+    if rank == 0 and (args.impl == "reference" or not args.no_cpu_baseline) and wl["kind"] in ("loopvq", "kivi"):
+        # the oracle's process pool starts (spawn) before any GPU work
+        pool = mp.get_context("spawn").Pool(os.cpu_count() or 1)
+    base = {"metric": METRIC, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "data": "synthetic"}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        res = run_reference(args, wl, pool)
+        line = dict(base, impl="reference", dtype="f64", **res)
+        line["config"] = {"workload": wl["name"], "sample_units": "(request, head) pairs"}
+        print(json.dumps(line))
+        pool.close()
+        return
+    dist = world > 1
+    if dist:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, wl, rank, world, dist, pool)
+    if rank == 0:
+        cfgd = {"workload": wl["name"], "parallelism": f"replicas x{world} (requests shard, no collective)",
+                "l2": "inputs larger than L2: each call reads its own layer's cache (~240 MB)"
+                if wl["kind"] == "loopvq" else "inputs larger than L2"}
+        for k in ("B", "H", "L", "layers", "T", "Tc", "G", "recent", "n_quant", "n_resid"):
+            if k in wl:
+                cfgd[k] = wl[k]
+        if "n_splits" in res:
+            cfgd["n_splits"] = res.pop("n_splits")
+        line = dict(base, dtype="f32" if wl["kind"] != "kivi_quant" else "f32->u8", config=cfgd, **res)
+        print(json.dumps(line))
+    if pool is not None:
+        pool.close()
+    if dist:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,285 @@
+/*
+ * kvq.h - C ABI of libkvq: decode attention over quantized KV caches on one NVIDIA GB300
+ * (sm_103a). Two cache formats:
+ *
+ *   LoopVQ  "LoopVQ: Sub 1-bit KV Cache Quantization for Looped Transformers" (paper
+ *           digest): one 8-bit codeword covers c = G/Tc channels over Tc consecutive loop
+ *           steps (method step 1, Figure 3); 256-entry codebooks per (loop block, layer,
+ *           head, channel group); keys quantized before RoPE; 8 sink and W recent tokens
+ *           kept in bf16 at every loop step, the rest in 8-token index pages (method
+ *           step 4, Figure 5); decode attention looks codewords up through the per-step
+ *           slice B_t, applies RoPE and merges the bf16 and quantized partials exactly
+ *           (method step 5, Algorithm 1).
+ *   KIVI    "KIVI 完全拆解：非对称 2-bit KV Cache 量化": asymmetric 2-bit quantization
+ *           q = clamp(round(X/s + z), 0, 2^b - 1) with fp16 scale and zero-point per group
+ *           (section on per-token / per-channel quantization); keys per channel over 32
+ *           tokens, values per token over 32 channels, an fp16 residual window, and one
+ *           softmax over both segments (core design, eq. (3)).
+ *
+ * Conventions for every call:
+ *   - Pointers are CUDA device pointers unless stated otherwise, owned by the caller; the
+ *     library never allocates, frees or keeps them. Device pointers must be 16-byte
+ *     aligned (checked: KVQ_ERR_INVALID_ARG).
+ *   - bf16 and fp16 values are passed as uint16_t bit patterns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *     and return a status at once. KVQ_ERR_CUDA means a launch failed; kvq_last_error()
+ *     gives the detail. Argument errors are detected on the host before anything is
+ *     launched, so an error return leaves all buffers untouched.
+ *   - Device-side waits (the TMA completion barrier) are bounded; a timed-out wait sets a
+ *     device error word that kvq_device_error() reads after the stream has drained.
+ *   - Loop steps are 1-based (t = 1..T) as on the LoopVQ page; layers and heads 0-based.
+ *   - Head dimension D = 128 and page size 8; c = G/Tc must be 8 (so that D/c = 16
+ *     index groups per token) in this version; other shapes return KVQ_ERR_UNSUPPORTED.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int kvq_status;
+enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, inconsistent shape            */
+  KVQ_ERR_CAPACITY = 2,     /* more tokens, pages or requests than the buffers hold      */
+  KVQ_ERR_UNSUPPORTED = 3,  /* a valid shape this build has no kernel for               */
+  KVQ_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed                     */
+  KVQ_ERR_WORKSPACE = 5,    /* workspace smaller than kvq_decode_workspace_size()       */
+  KVQ_ERR_TIMEOUT = 6       /* a device-side wait ran out of time (device error word)   */
+};
+
+enum { KVQ_FMT_LOOPVQ = 0, KVQ_FMT_KIVI = 1 };
+enum { KVQ_OUT_BF16 = 0, KVQ_OUT_FP32 = 1 };
+enum { KVQ_PER_CHANNEL = 0, KVQ_PER_TOKEN = 1 };
+
+typedef void* kvq_stream; /* cudaStream_t */
+
+/* ---------------------------------------------------------------------------------- */
+/* LoopVQ                                                                              */
+/* ---------------------------------------------------------------------------------- */
+
+/* Shape of a LoopVQ cache. NB = T/Tc loop blocks, c = G/Tc, NG = D/c index groups, a page
+ * holds 8 tokens and is 8*NG bytes. `recent` is W, the bf16 recent window (64, or 256
+ * for long contexts). */
+typedef struct {
+  int D;            /* head dimension (128)                                  */
+  int T;            /* loop steps                                            */
+  int Tc;           /* loop steps per block; divides T and G                 */
+  int G;            /* coupled dimensions per codeword                      */
+  int K;            /* codebook entries (256: 8-bit indices)                 */
+  int n_layers;
+  int n_heads;      /* KV heads (= query heads: dense multi-head attention) */
+  int sink;         /* bf16 sink tokens (8)                                  */
+  int recent;       /* W                                                     */
+  int max_pages;    /* index pages per (layer, block, request, head)         */
+  int max_batch;    /* requests the buffers hold                             */
+  int max_ctx;      /* rows of the RoPE table (largest position + 1)         */
+  float rope_base;  /* RoPE base (1e4)                                       */
+} kvq_vq_cfg;
+
+/* Device buffers of a LoopVQ cache (all caller-owned, sizes from kvq_vq_cache_sizes).
+ *
+ * idx_k, idx_v  uint8  [n_layers][NB][max_batch][n_heads][max_pages][8*NG]
+ *     Index page p of (layer, block, request, head) holds the 8 tokens at positions
+ *     sink + 8p .. sink + 8p + 7. In-page byte order pairs the RoPE partner groups
+ *     s and s + NG/2 (channels s*c.. and D/2 + s*c..): byte (s*8 + j)*2 + 0 is the index
+ *     of group s for token j, byte (s*8 + j)*2 + 1 that of group s + NG/2.
+ * win_k, win_v  bf16   [n_layers][T][max_batch][n_heads][sink + recent + 8][D]
+ *     Pre-RoPE keys / values of the bf16 tokens at each loop step. Position p < sink sits
+ *     in slot p; a recent position p in slot sink + (p - sink) mod (recent + 8).
+ * bt_k, bt_v    fp32   [n_layers][T][n_heads][K][D]
+ *     Per-loop-step codebook slices B_t, cut once by kvq_slice_codebooks:
+ *     bt[l][t][h][r][g*c + i] = cb[l][beta][h][g][r][i*Tc + m], beta = (t-1)/Tc,
+ *     m = (t-1)%Tc.
+ * cb_k, cb_v    fp32   [n_layers][NB][n_heads][NG][K][G]   full codebooks (encode, roll)
+ * rope_cos, rope_sin fp32 [max_ctx][D/2]: cos / sin(p * base^(-2i/D)) (kvq_rope_table)
+ * seq_len       int32  [max_batch]: tokens cached per request, including the newest one
+ *                      (the query position is seq_len - 1)
+ * n_pages       int32  [max_batch]: index pages in use per request
+ */
+typedef struct {
+  uint8_t* idx_k;
+  uint8_t* idx_v;
+  uint16_t* win_k;
+  uint16_t* win_v;
+  float* bt_k;
+  float* bt_v;
+  const float* cb_k;
+  const float* cb_v;
+  const float* rope_cos;
+  const float* rope_sin;
+  int32_t* seq_len;
+  int32_t* n_pages;
+} kvq_vq_cache;
+
+/* Byte sizes of each buffer of kvq_vq_cache for `cfg` (host-only, no device work).
+ * Order: idx (each of k, v), win (each), bt (each), cb (each), rope (each of cos, sin),
+ * per-request int32 arrays (each). Returns KVQ_ERR_INVALID_ARG for an invalid cfg. */
+typedef struct {
+  size_t idx, win, bt, cb, rope, per_request;
+} kvq_vq_sizes;
+kvq_status kvq_vq_cache_sizes(const kvq_vq_cfg* cfg, kvq_vq_sizes* out /* host */);
+
+/* RoPE table: cos/sin(p * theta_i), theta_i = base^(-2i/D), p < max_ctx, i < D/2, computed
+ * in fp64 and rounded to fp32 (LoopVQ page, background "RoPE" and method step 5:
+ * reconstructed keys are rotated with a precomputed cos/sin table). The pairing is
+ * rotate-half: channel i with channel i + D/2 (a reading; the page names no convention). */
+kvq_status kvq_rope_table(const kvq_vq_cfg* cfg, float* rope_cos, float* rope_sin, kvq_stream stream);
+
+/* Cut the per-loop-step slices B_t out of the full codebooks, once at load time
+ * (LoopVQ method step 5 and Figure 3: step t reads the shared indices through its own
+ * slice). cb: [n_layers][NB][n_heads][NG][K][G]; bt: [n_layers][T][n_heads][K][D]
+ * (layout in kvq_vq_cache). */
+kvq_status kvq_slice_codebooks(const kvq_vq_cfg* cfg, const float* cb, float* bt, kvq_stream stream);
+
+/* Nearest-codeword encode of coupled vectors (LoopVQ background: a(z) = argmin_r
+ * ||z - e_r||^2; method step 1 for the coupling, method step 4 for prefill encoding).
+ *
+ * x: bf16 pre-RoPE keys (or values) of ONE layer, element (t, b, h, j, ch) at
+ *    x[t*x_stride_t + b*x_stride_b + h*x_stride_h + j*D + ch], t the 0-based loop step,
+ *    b < n_seq, j < n_tok (n_tok a multiple of 8: whole pages).
+ * cb: fp32 [NB][n_heads][NG][K][G] codebooks of this layer.
+ * idx: this layer's index pages, [NB][max_batch][n_heads][max_pages][8*NG] (in-page order
+ *    as in kvq_vq_cache); token j of request b goes to page page_begin + j/8 of request
+ *    seq_begin + b. Only groups [g_begin, g_begin + g_count) are written.
+ * n_ties: optional device int32 counter (may be NULL); incremented once per (vector) whose
+ *    two best distances lie within 1e-6 relative of each other, where either index is a
+ *    correct encoding. The arithmetic is exact enough that any other decision equals the
+ *    exact-arithmetic argmin with the lowest index on ties.
+ * Errors: KVQ_ERR_CAPACITY if pages or requests exceed max_pages / max_batch. */
+kvq_status kvq_encode_vq(const kvq_vq_cfg* cfg, const uint16_t* x, int64_t x_stride_t,
+                         int64_t x_stride_b, int64_t x_stride_h, int seq_begin, int n_seq,
+                         int n_tok, const float* cb, uint8_t* idx, int page_begin,
+                         int g_begin, int g_count, int32_t* n_ties, kvq_stream stream);
+
+/* Prefill of one layer (LoopVQ method step 4, Figure 5): for requests
+ * [seq_begin, seq_begin + n_seq), each with L prompt tokens, keep positions [0, sink) and
+ * the last recent + ((L - sink - recent) mod 8) positions in bf16 at every loop step, and
+ * encode the positions in between into index pages (K and V, every loop block). Sets
+ * seq_len = L and n_pages = max(0, (L - sink - recent) / 8) for those requests.
+ * xk, xv: bf16 pre-RoPE keys / values of the layer, strides as in kvq_encode_vq, j < L.
+ * Errors: KVQ_ERR_CAPACITY if L needs more than max_pages pages or L > max_ctx. */
+kvq_status kvq_prefill_vq(const kvq_vq_cfg* cfg, const kvq_vq_cache* cache, int layer,
+                          const uint16_t* xk, const uint16_t* xv, int64_t x_stride_t,
+                          int64_t x_stride_b, int64_t x_stride_h, int seq_begin, int n_seq,
+                          int L, int32_t* n_ties, kvq_stream stream);
+
+/* Decode-time cache write (LoopVQ Figure 5: new keys and values are written in bf16; every
+ * 8 generated tokens the oldest recent page is encoded into indices).
+ * Call once per (layer, loop step) with that step's new pre-RoPE key and value, bf16
+ * [n_seq][n_heads][D] for requests [0, n_seq). The first call of a token (layer 0,
+ * loop_step 1) advances seq_len by one; when that makes the recent window hold
+ * recent + 8 tokens, the same call first encodes the oldest recent page for every layer,
+ * block, head, K and V (its tokens are complete at that point), adds it as page n_pages
+ * and increments n_pages. Other calls only write the bf16 slot of the newest token.
+ * Errors: KVQ_ERR_CAPACITY is reported through kvq_device_error() (the lengths live on the
+ * device) if a request would exceed max_pages or max_ctx; such a request is left as is. */
+kvq_status kvq_append_page(const kvq_vq_cfg* cfg, const kvq_vq_cache* cache, int layer,
+                           int loop_step, const uint16_t* k_new, const uint16_t* v_new,
+                           int n_seq, kvq_stream stream);
+
+/* ---------------------------------------------------------------------------------- */
+/* KIVI                                                                                */
+/* ---------------------------------------------------------------------------------- */
+
+typedef struct {
+  int D;            /* head dimension (128)                                     */
+  int n_heads;      /* KV heads (= query heads)                                 */
+  int bits;         /* 2                                                        */
+  int group;        /* 32: tokens per key group, channels per value group       */
+  int residual;     /* R: fp16 residual window capacity (128)                   */
+  int max_batch;
+  int max_tokens;   /* quantized-token capacity per (request, head), multiple of group */
+} kvq_kivi_cfg;
+
+/* Device buffers of a KIVI cache (caller-owned).
+ * k_codes, v_codes uint8 [max_batch][n_heads][max_tokens][D/4]: 4 codes per byte along
+ *     channels, channel 4k + i in bits [2i, 2i + 2).
+ * k_scale, k_zero  fp16 [max_batch][n_heads][max_tokens/group][D]   (per channel)
+ * v_scale, v_zero  fp16 [max_batch][n_heads][max_tokens][D/group]   (per token)
+ * k_resid, v_resid fp16 [max_batch][n_heads][residual][D]            (newest tokens)
+ * n_quant  int32 [max_batch]: quantized tokens per request (a multiple of group)
+ * n_resid  int32 [max_batch]: residual tokens per request (<= residual)
+ */
+typedef struct {
+  uint8_t* k_codes;
+  uint16_t* k_scale;
+  uint16_t* k_zero;
+  uint8_t* v_codes;
+  uint16_t* v_scale;
+  uint16_t* v_zero;
+  uint16_t* k_resid;
+  uint16_t* v_resid;
+  int32_t* n_quant;
+  int32_t* n_resid;
+} kvq_kivi_cache;
+
+/* Group quantization (KIVI page, quantization-direction section and the group-quant
+ * kernel of the implementation section). In fp32 per group: s = (max - min)/(2^b - 1),
+ * s16 = fp16(s) (1 if that is 0), z16 = fp16(-min/s16),
+ * q = clamp(rint(x/s16 + z16), 0, 2^b - 1) with IEEE division and no fused multiply-add,
+ * so codes, scales and zero-points are reproducible bit for bit.
+ * axis = KVQ_PER_CHANNEL: keys, groups of `group` tokens per channel; n_tok and
+ *        tok_begin multiples of group; writes k-style codes/scale/zero.
+ * axis = KVQ_PER_TOKEN:   values, groups of `group` channels per token.
+ * x: fp16, element (b, h, j, ch) at x[b*x_stride_b + h*x_stride_h + j*D + ch], b < B.
+ * codes / scale / zero: cache arrays (layouts in kvq_kivi_cache); token j of request b is
+ *    written at token tok_begin + j.
+ * Errors: KVQ_ERR_CAPACITY if tok_begin + n_tok > max_tokens or B > max_batch. */
+kvq_status kvq_quantize_kivi(const kvq_kivi_cfg* cfg, int axis, const uint16_t* x,
+                             int64_t x_stride_b, int64_t x_stride_h, int B, int n_tok,
+                             uint8_t* codes, uint16_t* scale, uint16_t* zero, int tok_begin,
+                             kvq_stream stream);
+
+/* ---------------------------------------------------------------------------------- */
+/* Decode attention (both formats)                                                     */
+/* ---------------------------------------------------------------------------------- */
+
+/* One decode attention call: every request b < B attends with its query (bf16
+ * [B][n_heads][D], pre-RoPE for LoopVQ) to its whole cache, split-K over the quantized
+ * pages with partial softmax per split and an exact logsumexp merge (LoopVQ page:
+ * Flash-Decoding background and method step 5; KIVI page: eq. (3), one softmax over the
+ * quantized and residual segments). Scale 1/sqrt(D).
+ *
+ * format KVQ_FMT_LOOPVQ: cfg is kvq_vq_cfg*, cache kvq_vq_cache*; layer and loop_step
+ *   select the cache slice. The query sits at position seq_len[b] - 1; every key and the
+ *   query are rotated by RoPE at their positions.
+ * format KVQ_FMT_KIVI: cfg is kvq_kivi_cfg*, cache kvq_kivi_cache*; layer and loop_step
+ *   are ignored; no RoPE (KIVI caches post-RoPE keys).
+ * out: [B][n_heads][D], bf16 (KVQ_OUT_BF16) or fp32 (KVQ_OUT_FP32).
+ * n_splits: quantized-page splits per (request, head); 0 picks one for the GPU.
+ * ws: device workspace of at least kvq_decode_workspace_size() bytes (may be NULL when
+ *   that size is 0). Its first use needs it zero-filled; every call leaves it reusable.
+ *   Two calls that run at the same time need two workspaces.
+ * Errors: KVQ_ERR_WORKSPACE, KVQ_ERR_CAPACITY (B > max_batch). */
+kvq_status kvq_decode_attn(int format, const void* cfg, const void* cache, int layer,
+                           int loop_step, const uint16_t* q, int B, void* out, int out_dtype,
+                           int n_splits, void* ws, size_t ws_bytes, kvq_stream stream);
+
+/* Workspace bytes kvq_decode_attn needs for these arguments (0 if none). */
+size_t kvq_decode_workspace_size(int format, const void* cfg, int B, int n_splits);
+
+/* The split count kvq_decode_attn uses when n_splits = 0. */
+int kvq_decode_auto_splits(int format, const void* cfg, int B);
+
+/* ---------------------------------------------------------------------------------- */
+/* Diagnostics                                                                         */
+/* ---------------------------------------------------------------------------------- */
+
+const char* kvq_status_string(kvq_status s);
+/* Detail of the last error on the calling host thread ("" if none). */
+const char* kvq_last_error(void);
+/* Reads and clears the device error word of the current device (synchronizes the device).
+ * 0 = no device-side error; otherwise a KVQ_ERR_* code. */
+int kvq_device_error(void);
+/* Library version, major*10000 + minor*100 + patch. */
+int kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H */

@@ -1,0 +1,113 @@
+// Internal launch interface between the C ABI layer (kvq_api.cu) and the kernel files.
+// Not exported; no validation here (kvq_api.cu checks every argument first).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvq {
+
+constexpr int kD = 128;        // head dimension
+constexpr int kPage = 8;       // tokens per index page
+constexpr int kNG = 16;        // index groups per token (c = 8)
+constexpr int kC = 8;          // channels per group
+constexpr int kCB = 256;       // codebook entries
+constexpr int kPageBytes = kPage * kNG;
+
+// ---------------------------------------------------------------- LoopVQ decode attention
+struct VqAttnArgs {
+  const uint8_t* idx_k;      // [max_batch][H][max_pages][128] of (layer, block)
+  const uint8_t* idx_v;
+  const uint16_t* win_k;     // [max_batch][H][win_slots][D] of (layer, step)
+  const uint16_t* win_v;
+  const float* bt_k;         // [H][256][D] of (layer, step)
+  const float* bt_v;
+  const float* rope_cos;     // [max_ctx][D/2]
+  const float* rope_sin;
+  const int32_t* seq_len;    // [max_batch]
+  const int32_t* n_pages;
+  const uint16_t* q;         // [B][H][D] bf16
+  void* out;                 // [B][H][D]
+  int out_fp32;
+  float* part;               // [B][H][n_split][D + 2] partials (n_split > 1)
+  int* counters;             // [ceil(B/2)][H] arrival counters (n_split > 1)
+  int* err;
+  int B, H, max_pages, max_ctx, sink, recent, win_slots;
+  int n_split, pages_per_split;
+};
+size_t vq_attn_smem_bytes(int pages_per_split, int win_slots);
+int vq_attn_max_pages_per_split(int win_slots);
+cudaError_t launch_vq_attn(const VqAttnArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- LoopVQ encode and friends
+struct VqEncodeArgs {
+  const uint16_t* x;               // bf16, element (t, b, h, j, ch)
+  int64_t st, sb, sh;              // element strides of t, b, h (token stride D)
+  const float* cb;                 // [NB][H][NG][256][G] of one layer
+  uint8_t* idx;                    // [NB][max_batch][H][max_pages][128] of one layer
+  int32_t* n_ties;
+  int* err;
+  int T, Tc, G, NB, H, max_batch, max_pages;
+  int seq_begin, n_seq, n_tok, page_begin, g_begin, g_count;
+};
+cudaError_t launch_vq_encode(const VqEncodeArgs& a, cudaStream_t s);
+
+cudaError_t launch_rope_table(float* cos_t, float* sin_t, int max_ctx, int D, float base, cudaStream_t s);
+cudaError_t launch_slice_codebooks(const float* cb, float* bt, int L, int T, int Tc, int G, int H,
+                                   cudaStream_t s);
+
+struct VqWindowArgs {              // copy prefill tokens into the bf16 windows
+  const uint16_t* xk; const uint16_t* xv;
+  int64_t st, sb, sh;
+  uint16_t* win_k; uint16_t* win_v;  // [T][max_batch][H][win_slots][D] of one layer
+  int32_t* seq_len; int32_t* n_pages;  // set for the requests (may be null)
+  int T, H, max_batch, win_slots, sink, recent;
+  int seq_begin, n_seq, L, n_pages_val;
+};
+cudaError_t launch_vq_prefill_window(const VqWindowArgs& a, cudaStream_t s);
+
+struct VqAppendArgs {
+  const uint16_t* k_new; const uint16_t* v_new;   // [n_seq][H][D]
+  uint16_t* win_k; uint16_t* win_v;               // of (layer, step): [max_batch][H][win_slots][D]
+  int32_t* seq_len; int32_t* n_pages;
+  int* err;
+  int H, n_seq, win_slots, sink, recent, max_pages, max_ctx;
+  int advance;                                    // first (layer, step) of the token
+};
+cudaError_t launch_vq_append(const VqAppendArgs& a, cudaStream_t s);
+
+struct VqRollArgs {                // encode the oldest recent page where the ring is full
+  const uint16_t* win_k; const uint16_t* win_v;   // full [L][T][max_batch][H][win_slots][D]
+  const float* cb_k; const float* cb_v;           // [L][NB][H][NG][256][G]
+  uint8_t* idx_k; uint8_t* idx_v;                 // [L][NB][max_batch][H][max_pages][128]
+  int32_t* seq_len; int32_t* n_pages;
+  int* err;
+  int L, T, Tc, G, NB, H, n_seq, max_batch, max_pages, win_slots, sink, recent;
+};
+cudaError_t launch_vq_roll(const VqRollArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- KIVI
+struct KiviQuantArgs {
+  const uint16_t* x;               // fp16 (b, h, j, ch)
+  int64_t sb, sh;
+  uint8_t* codes; uint16_t* scale; uint16_t* zero;
+  int axis, B, H, n_tok, tok_begin, max_tokens, group;
+};
+cudaError_t launch_kivi_quantize(const KiviQuantArgs& a, cudaStream_t s);
+
+struct KiviAttnArgs {
+  const uint8_t* k_codes; const uint16_t* k_scale; const uint16_t* k_zero;
+  const uint8_t* v_codes; const uint16_t* v_scale; const uint16_t* v_zero;
+  const uint16_t* k_resid; const uint16_t* v_resid;
+  const int32_t* n_quant; const int32_t* n_resid;
+  const uint16_t* q;
+  void* out; int out_fp32;
+  float* part; int* counters; int* err;
+  int B, H, max_tokens, residual, group;
+  int n_split, tok_per_split;
+};
+size_t kivi_attn_smem_bytes(int tok_per_split, int residual);
+int kivi_attn_max_tok_per_split(int residual);
+cudaError_t launch_kivi_attn(const KiviAttnArgs& a, cudaStream_t s);
+
+}  // namespace kvq

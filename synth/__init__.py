@@ -150,3 +150,32 @@ def bf16_round(x) -> np.ndarray:
 def fp16_round(x) -> np.ndarray:
     """``x`` rounded to fp16, returned as float64."""
     return np.asarray(x, dtype=np.float64).astype(np.float16).astype(np.float64)
+
+
+# ---- device-side generation for full-size workloads (same recipe, torch generator) ------
+
+def torch_loop_correlated(gen, T: int, shape, rhos, device="cuda"):
+    """Float32 tensor [T, *shape]: the loop-axis AR(1) chain of ``loop_correlated``, drawn
+    with a seeded ``torch.Generator`` on ``device``."""
+    import torch
+
+    rhos = [float(r) for r in rhos]
+    x = torch.empty((T, *shape), dtype=torch.float32, device=device)
+    x[0].normal_(generator=gen)
+    for t in range(1, T):
+        r = rhos[t - 1]
+        x[t] = r * x[t - 1] + (1.0 - r * r) ** 0.5 * torch.randn(shape, generator=gen, device=device)
+    return x
+
+
+def torch_sample_codebooks(gen, x, Tc: int, G: int, K: int = 256, noise_var: float = 0.01):
+    """Device version of ``sample_codebooks``: x float [T][n][D] (one head) ->
+    float32 [NB][NG][K][G], K tokens drawn with ``gen`` plus N(0, noise_var) noise."""
+    import torch
+
+    T, n, D = x.shape
+    c = G // Tc
+    NB, NG = T // Tc, D // c
+    toks = torch.randint(0, n, (K,), generator=gen, device=x.device)
+    s = x[:, toks, :].float().reshape(NB, Tc, K, NG, c).permute(0, 3, 2, 4, 1).reshape(NB, NG, K, G)
+    return (s + noise_var ** 0.5 * torch.randn(s.shape, generator=gen, device=x.device)).contiguous()

@@ -1,0 +1,158 @@
+"""CPU checks of the C ABI: the library builds, loads and exports every function the header
+declares, and host-side validation rejects bad arguments before anything is launched.
+No call here reaches a kernel (there is no GPU in this suite)."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import synth
+from sub_bit_quantized_gb300 import _build, kvq
+from tests import _layout
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return kvq.lib()
+
+
+def test_exports_every_declared_function(L):
+    names = kvq.header_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(kvq._SIGS) == set(names)
+
+
+def test_version_and_status_strings(L):
+    assert L.kvq_version() >= 100
+    for code, text in [(0, b"ok"), (1, b"invalid argument"), (2, b"capacity exceeded"),
+                       (3, b"unsupported shape"), (4, b"CUDA error"), (5, b"workspace too small"),
+                       (6, b"device wait timed out")]:
+        assert L.kvq_status_string(code) == text
+
+
+def cfg2(**kw):
+    base = dict(D=128, T=4, Tc=2, G=16, K=256, n_layers=24, n_heads=16, sink=8, recent=64,
+                max_pages=759, max_batch=64, max_ctx=6144)
+    base.update(kw)
+    return kvq.VqConfig(**base)
+
+
+def test_cache_sizes_formula(L):
+    c = cfg2()
+    s = kvq.vq_cache_sizes(c)
+    assert s.idx == 24 * 2 * 64 * 16 * 759 * 128
+    assert s.win == 24 * 4 * 64 * 16 * 80 * 128 * 2
+    assert s.bt == 24 * 4 * 16 * 256 * 128 * 4
+    assert s.cb == 24 * 2 * 16 * 16 * 256 * 16 * 4
+    assert s.rope == 6144 * 64 * 4 and s.per_request == 64 * 4
+    # one call reads one (layer, block) of each index array: 199.0 MB at B=64, 6K
+    assert s.idx / 24 / 2 * 2 == pytest.approx(199.0e6, rel=1e-3)
+
+
+@pytest.mark.parametrize("kw,code", [(dict(Tc=3), 1), (dict(G=12), 1), (dict(G=32), 3),
+                                     (dict(D=64), 3), (dict(K=16), 3), (dict(max_ctx=1), 1),
+                                     (dict(T=8, Tc=8, G=64), 3), (dict(max_batch=0), 1)])
+def test_bad_configs_rejected(L, kw, code):
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.vq_cache_sizes(cfg2(**kw))
+    assert e.value.status == code
+
+
+FAKE = 0x10000  # aligned, never dereferenced: every call below fails validation first
+
+
+def fake_cache():
+    return kvq.VqCacheC(*([FAKE] * 12))
+
+
+def test_decode_attn_argument_checks(L):
+    c = cfg2().to_c()
+    kc = fake_cache()
+    f = L.kvq_decode_attn
+    B = ctypes.byref
+    assert f(0, B(c), B(kc), 0, 1, None, 64, FAKE, 0, 0, None, 0, None) == 1   # null q
+    assert f(0, B(c), B(kc), 0, 1, FAKE + 2, 64, FAKE, 0, 0, None, 0, None) == 1  # misaligned
+    assert f(0, B(c), B(kc), 0, 1, FAKE, 64, FAKE, 7, 0, None, 0, None) == 1   # out dtype
+    assert f(0, B(c), B(kc), 24, 1, FAKE, 64, FAKE, 0, 0, None, 0, None) == 1  # layer
+    assert f(0, B(c), B(kc), 0, 5, FAKE, 64, FAKE, 0, 0, None, 0, None) == 1   # loop step 5 > T
+    assert f(0, B(c), B(kc), 0, 0, FAKE, 64, FAKE, 0, 0, None, 0, None) == 1   # steps are 1-based
+    assert f(0, B(c), B(kc), 0, 1, FAKE, 65, FAKE, 0, 0, None, 0, None) == 2   # B > max_batch
+    assert f(0, B(c), B(kc), 0, 1, FAKE, 64, FAKE, 0, 3, None, 0, None) == 5   # split needs ws
+    assert f(9, B(c), B(kc), 0, 1, FAKE, 64, FAKE, 0, 0, None, 0, None) == 1   # format
+    assert b"workspace" in L.kvq_last_error() or b"format" in L.kvq_last_error()
+    kc.seq_len = None
+    assert f(0, B(c), B(kc), 0, 1, FAKE, 64, FAKE, 0, 0, None, 0, None) == 1   # cache pointer
+
+
+def test_workspace_size_and_split_plan(L):
+    c = cfg2()
+    assert kvq.kvq_decode_workspace_size(c, 64, 1) == 0
+    n = kvq.kvq_decode_workspace_size(c, 64, 4)
+    assert n >= 64 * 16 * 4 * 130 * 4 + 32 * 16 * 4
+    auto = kvq.kvq_decode_auto_splits(c, 64)
+    assert 1 <= auto <= 64
+    # a split that would not fit in shared memory is refused
+    big = cfg2(max_pages=40000, max_ctx=400000)
+    assert kvq.kvq_decode_auto_splits(big, 1) >= 40000 // 1000
+
+
+def test_encode_and_prefill_argument_checks(L):
+    c = cfg2().to_c()
+    B = ctypes.byref
+    f = L.kvq_encode_vq
+    # n_tok not a whole number of pages
+    assert f(B(c), FAKE, 0, 0, 0, 0, 1, 12, FAKE, FAKE, 0, 0, 16, None, None) == 1
+    # pages beyond max_pages
+    assert f(B(c), FAKE, 0, 0, 0, 0, 1, 8 * 760, FAKE, FAKE, 0, 0, 16, None, None) == 2
+    # groups outside [0, 16)
+    assert f(B(c), FAKE, 0, 0, 0, 0, 1, 8, FAKE, FAKE, 0, 10, 8, None, None) == 1
+    # stride not a multiple of 8 elements
+    assert f(B(c), FAKE, 3, 0, 0, 0, 1, 8, FAKE, FAKE, 0, 0, 16, None, None) == 1
+    kc = fake_cache()
+    g = L.kvq_prefill_vq
+    assert g(B(c), B(kc), 0, FAKE, FAKE, 0, 0, 0, 0, 1, 6145, None, None) == 2   # L > max_ctx
+    big = cfg2(max_ctx=1 << 20).to_c()
+    assert g(B(big), B(kc), 0, FAKE, FAKE, 0, 0, 0, 0, 1, 8 * 800, None, None) == 2  # pages
+    assert g(B(c), B(kc), 0, FAKE, FAKE, 0, 0, 0, 60, 5, 100, None, None) == 2  # requests
+    a = L.kvq_append_page
+    assert a(B(c), B(kc), 0, 0, FAKE, FAKE, 1, None) == 1                        # step 0
+    assert a(B(c), B(kc), 0, 1, FAKE, FAKE, 65, None) == 2                       # n_seq
+
+
+def test_kivi_argument_checks(L):
+    k = kvq.KiviConfig(n_heads=32, max_batch=16, max_tokens=3968).to_c()
+    B = ctypes.byref
+    f = L.kvq_quantize_kivi
+    assert f(B(k), 0, FAKE, 0, 0, 16, 31, FAKE, FAKE, FAKE, 0, None) == 1   # keys need 32-token groups
+    assert f(B(k), 0, FAKE, 0, 0, 16, 64, FAKE, FAKE, FAKE, 3936, None) == 2  # past capacity
+    assert f(B(k), 2, FAKE, 0, 0, 16, 64, FAKE, FAKE, FAKE, 0, None) == 1   # axis
+    k4 = kvq.KiviConfig(bits=4, max_tokens=64).to_c()
+    assert f(B(k4), 1, FAKE, 0, 0, 1, 1, FAKE, FAKE, FAKE, 0, None) == 3    # 4-bit not built
+
+
+def test_library_missing_fails_loudly(monkeypatch):
+    monkeypatch.setattr(kvq, "_lib", None)
+    monkeypatch.setattr(kvq, "LIB_PATH", "/nonexistent/libkvq.so")
+    with pytest.raises(RuntimeError, match="libkvq.so not found"):
+        kvq.lib()
+
+
+def test_page_layout_round_trip():
+    g = synth.rng(5)
+    idx = synth.random_indices(g, (3, 40, 16))
+    pages = _layout.pack_pages(idx)
+    assert pages.shape == (3, 5, 128)
+    assert np.array_equal(_layout.unpack_pages(pages), idx)
+    # byte (s*8 + j)*2 + 1 holds group s + 8 of token j
+    assert pages[0, 0, (3 * 8 + 5) * 2 + 1] == idx[0, 5, 11]
+
+
+def test_code_packing_round_trip():
+    g = synth.rng(6)
+    codes = g.integers(0, 4, size=(7, 128))
+    b = _layout.pack_codes(codes)
+    assert b.shape == (7, 32) and np.array_equal(_layout.unpack_codes(b), codes)
+    assert b[0, 0] == codes[0, 0] | (codes[0, 1] << 2) | (codes[0, 2] << 4) | (codes[0, 3] << 6)

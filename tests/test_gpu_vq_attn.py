@@ -1,0 +1,109 @@
+"""GPU parity of LoopVQ decode attention (kvq_decode_attn, format LoopVQ) against the fp64
+oracle, on the same seeded inputs. Tolerance: max-abs 2e-3 and relative L2 1e-3 on the
+fp32-output mode; the bf16 output must be the bf16 rounding of the fp32 result."""
+import numpy as np
+import pytest
+import torch
+
+from sub_bit_quantized_gb300 import kvq
+from tests import _cases as C
+
+pytestmark = pytest.mark.gpu
+
+
+def run_attn(case, cache, t, n_splits=0, out_dtype=torch.float32):
+    c = case.cfg
+    B = len(case.lens)
+    q = C.bf16_tensor(case.q)
+    out = torch.empty((B, c.n_heads, 128), dtype=out_dtype, device="cuda")
+    ws = kvq.make_workspace(c, B, n_splits)
+    kvq.kvq_decode_attn(c, cache, 0, t, q, out, n_splits, ws)
+    torch.cuda.synchronize()
+    assert kvq.device_error() == 0
+    return out
+
+
+def check_all(case, cache, steps=(1, 2, 3, 4), n_splits=0, pairs=None):
+    errs = []
+    for t in steps:
+        out = run_attn(case, cache, t, n_splits).cpu().numpy().astype(np.float64)
+        sel = pairs or [(b, h) for b in range(len(case.lens)) for h in range(case.cfg.n_heads)]
+        got = np.stack([out[b, h] for b, h in sel])
+        ref = np.stack([C.oracle_vq(case, b, h, t) for b, h in sel])
+        errs.append(C.check_close(got, ref))
+    return errs
+
+
+def test_tiny_config_every_loop_step():
+    # 1 layer, 1 head, T=4, Tc=2, G=16, batch 1, context 512: 55 pages + 8 sink + 64 recent
+    case = C.make_vq_case(100, B=1, H=1, lens=[512])
+    assert case.n_pages == [55]
+    cache = C.fill_vq_cache(case)
+    check_all(case, cache)
+
+
+@pytest.mark.parametrize("n_splits", [0, 1, 2, 3, 7, 64])
+def test_split_counts_and_odd_batch(n_splits):
+    # ragged batch of 3 (one request pairs with nothing); lengths give 0, 1 and 55 pages
+    case = C.make_vq_case(101, B=3, H=2, lens=[73, 80, 513])
+    assert case.n_pages == [0, 1, 55]
+    cache = C.fill_vq_cache(case)
+    check_all(case, cache, steps=(1, 4), n_splits=n_splits)
+
+
+@pytest.mark.parametrize("lens", [[1], [5], [8], [72], [79], [80], [81], [8 + 64 + 8 * 7 + 7]])
+def test_short_and_boundary_contexts(lens):
+    case = C.make_vq_case(102, B=1, H=1, lens=lens)
+    cache = C.fill_vq_cache(case)
+    check_all(case, cache, steps=(1, 3))
+
+
+def test_bf16_output_is_rounded_fp32_output():
+    case = C.make_vq_case(103, B=2, H=2, lens=[300, 301])
+    cache = C.fill_vq_cache(case)
+    o32 = run_attn(case, cache, 2, out_dtype=torch.float32)
+    o16 = run_attn(case, cache, 2, out_dtype=torch.bfloat16)
+    assert torch.equal(o32.to(torch.bfloat16), o16)
+    ref = np.stack([C.oracle_vq(case, b, h, 2) for b in range(2) for h in range(2)])
+    got = o16.float().cpu().numpy().reshape(4, 128)
+    ulp = np.maximum(2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7), 2.0 ** -133)
+    assert np.all(np.abs(got - ref) <= ulp * 1.01 + 2e-3)
+
+
+def test_quarter_bit_long_context_layout():
+    # Tc=4, G=32 (0.25 bit), recent 256: shape of the long-context workload, smaller context
+    case = C.make_vq_case(104, B=2, H=2, lens=[8 + 256 + 8 * 300 + 5, 8 + 256 + 8 * 123], T=4, Tc=4, G=32,
+                          recent=256, rho=(0.85, 0.85))
+    cache = C.fill_vq_cache(case)
+    check_all(case, cache, steps=(1, 2, 3, 4), n_splits=64)
+    check_all(case, cache, steps=(3,), n_splits=0)
+
+
+def test_repeated_calls_reuse_workspace():
+    case = C.make_vq_case(105, B=4, H=3, lens=[600, 1000, 999, 1500])
+    cache = C.fill_vq_cache(case)
+    outs = [run_attn(case, cache, 1, n_splits=5) for _ in range(3)]
+    # the value histogram accumulates with shared-memory atomics, whose order varies from
+    # call to call: repeated calls agree to fp32 rounding, not bit for bit
+    for o in outs[1:]:
+        assert torch.allclose(o, outs[0], rtol=1e-5, atol=1e-6)
+    check_all(case, cache, steps=(1,), n_splits=5)
+
+
+@pytest.mark.parametrize("cfgname", ["b64_ctx6144_half_bit", "b8_ctx32768_quarter_bit"])
+def test_full_size_sampled(cfgname):
+    # full workload sizes in the launch configuration the bench uses (automatic split);
+    # the oracle evaluates a sample of (request, head) pairs one by one
+    if cfgname == "b64_ctx6144_half_bit":
+        case = C.make_vq_case(106, B=64, H=16, lens=[6144] * 64)
+        steps = (1, 2, 3, 4)
+    else:
+        case = C.make_vq_case(107, B=8, H=16, lens=[32768] * 8, Tc=4, G=32, recent=256, rho=(0.85, 0.85))
+        steps = (1, 4)
+    cache = C.fill_vq_cache(case)
+    rng = np.random.default_rng(7)
+    pairs = [(int(b), int(h)) for b, h in zip(rng.integers(0, len(case.lens), 6), rng.integers(0, 16, 6))]
+    pairs += [(0, 0), (len(case.lens) - 1, 15)]
+    check_all(case, cache, steps=steps, pairs=pairs)
+    if cfgname == "b8_ctx32768_quarter_bit":
+        check_all(case, cache, steps=(2,), n_splits=64, pairs=pairs[:3])

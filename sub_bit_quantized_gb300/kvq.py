@@ -387,5 +387,8 @@ class DecodeCall:
 
 def kvq_decode_attn(cfg, cache, layer: int, loop_step: int, q, out, n_splits: int = 0, ws=None,
                     stream=None):
-    """q: bf16 [B][H][D]; out: bf16 or fp32 [B][H][D]."""
+    """q: bf16 [B][H][D]; out: bf16 or fp32 [B][H][D]. When the split plan needs a workspace
+    and none is given, a zero-filled one is allocated for this call (through PyTorch)."""
+    if ws is None:
+        ws = make_workspace(cfg, q.shape[0], n_splits, q.device)
     DecodeCall(cfg, cache, layer, loop_step, q, out, n_splits, ws, stream)()

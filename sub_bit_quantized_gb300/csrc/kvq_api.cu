@@ -104,7 +104,8 @@ VqPlan plan_vq(const kvq_vq_cfg* c, int B, int n_splits) {
   const double overhead = 48.0;  // staging cost in page-equivalents per block
   double best = 1e300;
   const int n_lo = std::max(1, (c->max_pages + pmax - 1) / pmax);
-  for (int n = n_lo; n <= std::min(64, c->max_pages); ++n) {
+  const int n_hi = std::max(n_lo, std::min(64, c->max_pages));
+  for (int n = n_lo; n <= n_hi; ++n) {
     const int pps = (c->max_pages + n - 1) / n;
     const long long blocks = (long long)pairs * c->n_heads * n;
     const long long waves = (blocks + sms - 1) / sms;

@@ -260,6 +260,26 @@ kvq_status kvq_decode_attn(int format, const void* cfg, const void* cache, int l
                            int loop_step, const uint16_t* q, int B, void* out, int out_dtype,
                            int n_splits, void* ws, size_t ws_bytes, kvq_stream stream);
 
+/* Decode attention for callers that cannot allocate device memory: a serving engine that
+ * gives all device memory to its own pool at start-up and forbids later allocations, or code
+ * running inside another framework's callback that only sees the tensors it is handed.
+ * The pages have no counterpart of this call; it is kvq_decode_attn with the workspace taken
+ * from an array the library reserves on every device it is loaded on
+ * (KVQ_NOALLOC_SCRATCH_BYTES, held until the process exits) instead of from the caller.
+ * - Arguments and results are those of kvq_decode_attn without ws / ws_bytes.
+ * - The first call on a device looks the array's device address up (cudaGetSymbolAddress);
+ *   make that first call before any stream capture on that device.
+ * - Each call clears the part of the array it uses (cudaMemsetAsync on `stream`) and then
+ *   launches; it never calls cudaMalloc or cudaFree.
+ * - All calls on a device share the one array: calls that can run at the same time on the
+ *   GPU (other streams, other host threads) race and must be serialised by the caller.
+ * - A call that would need more scratch than the array holds returns KVQ_ERR_WORKSPACE
+ *   without launching anything; use kvq_decode_attn with a workspace for it. */
+#define KVQ_NOALLOC_SCRATCH_BYTES (8u << 20)
+kvq_status kvq_decode_attn_noalloc(int format, const void* cfg, const void* cache, int layer,
+                                   int loop_step, const uint16_t* q, int B, void* out,
+                                   int out_dtype, int n_splits, kvq_stream stream);
+
 /* Workspace bytes kvq_decode_attn needs for these arguments (0 if none). */
 size_t kvq_decode_workspace_size(int format, const void* cfg, int B, int n_splits);
 

@@ -178,6 +178,8 @@ size_t kivi_ws_bytes(const kvq_kivi_cfg* c, int B, const KiviPlan& p) {
 
 }  // namespace
 
+void kvq::set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+
 // ======================================================================================
 // Exported entry points
 // ======================================================================================

@@ -7,6 +7,9 @@
 
 namespace kvq {
 
+// stores the detail message kvq_last_error() returns on this host thread
+void set_last_error(const char* msg);
+
 constexpr int kD = 128;        // head dimension
 constexpr int kPage = 8;       // tokens per index page
 constexpr int kNG = 16;        // index groups per token (c = 8)

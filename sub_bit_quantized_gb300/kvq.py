@@ -78,6 +78,7 @@ _SIGS = {
     "kvq_append_page": (_I, [_P, _P, _I, _I, _P, _P, _I, _P]),
     "kvq_quantize_kivi": (_I, [_P, _I, _P, _I64, _I64, _I, _I, _P, _P, _P, _I, _P]),
     "kvq_decode_attn": (_I, [_I, _P, _P, _I, _I, _P, _I, _P, _I, _I, _P, _SZ, _P]),
+    "kvq_decode_attn_noalloc": (_I, [_I, _P, _P, _I, _I, _P, _I, _P, _I, _I, _P]),
     "kvq_decode_workspace_size": (_SZ, [_I, _P, _I, _I]),
     "kvq_decode_auto_splits": (_I, [_I, _P, _I]),
 }

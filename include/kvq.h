@@ -91,10 +91,11 @@ typedef struct {
  * win_k, win_v  bf16   [n_layers][T][max_batch][n_heads][sink + recent + 8][D]
  *     Pre-RoPE keys / values of the bf16 tokens at each loop step. Position p < sink sits
  *     in slot p; a recent position p in slot sink + (p - sink) mod (recent + 8).
- * bt_k, bt_v    fp32   [n_layers][T][n_heads][K][D]
- *     Per-loop-step codebook slices B_t, cut once by kvq_slice_codebooks:
- *     bt[l][t][h][r][g*c + i] = cb[l][beta][h][g][r][i*Tc + m], beta = (t-1)/Tc,
- *     m = (t-1)%Tc.
+ * bt_k, bt_v    fp32   [n_layers][T][n_heads][2][K][D/2]
+ *     Per-loop-step codebook slices B_t, cut once by kvq_slice_codebooks. Channel
+ *     ch = g*c + i of codeword r sits in half ch / (D/2) at column ch % (D/2):
+ *     bt[l][t][h][ch/(D/2)][r][ch%(D/2)] = cb[l][beta][h][g][r][i*Tc + m],
+ *     beta = (t-1)/Tc, m = (t-1)%Tc. (The halves hold the RoPE partner channels.)
  * cb_k, cb_v    fp32   [n_layers][NB][n_heads][NG][K][G]   full codebooks (encode, roll)
  * rope_cos, rope_sin fp32 [max_ctx][D/2]: cos / sin(p * base^(-2i/D)) (kvq_rope_table)
  * seq_len       int32  [max_batch]: tokens cached per request, including the newest one
@@ -132,7 +133,7 @@ kvq_status kvq_rope_table(const kvq_vq_cfg* cfg, float* rope_cos, float* rope_si
 
 /* Cut the per-loop-step slices B_t out of the full codebooks, once at load time
  * (LoopVQ method step 5 and Figure 3: step t reads the shared indices through its own
- * slice). cb: [n_layers][NB][n_heads][NG][K][G]; bt: [n_layers][T][n_heads][K][D]
+ * slice). cb: [n_layers][NB][n_heads][NG][K][G]; bt: [n_layers][T][n_heads][2][K][D/2]
  * (layout in kvq_vq_cache). */
 kvq_status kvq_slice_codebooks(const kvq_vq_cfg* cfg, const float* cb, float* bt, kvq_stream stream);
 

@@ -23,7 +23,7 @@ struct VqAttnArgs {
   const uint8_t* idx_v;
   const uint16_t* win_k;     // [max_batch][H][win_slots][D] of (layer, step)
   const uint16_t* win_v;
-  const float* bt_k;         // [H][256][D] of (layer, step)
+  const float* bt_k;         // [H][2][256][D/2] of (layer, step)
   const float* bt_v;
   const float* rope_cos;     // [max_ctx][D/2]
   const float* rope_sin;

@@ -3,35 +3,35 @@
 //
 // Follows "LoopVQ: Sub 1-bit KV Cache Quantization for Looped Transformers", method
 // step 5, Algorithm 1 and Figure 5: the step's codebook slice B_t is staged in shared
-// memory once per thread block, keys are rebuilt from D/c = 16 indices per token, rotated
-// by RoPE and dotted with the query; the bf16 sink/recent tokens are attended directly and
-// the partials of every split are merged exactly. Two requests of the same head share a
-// thread block and its B_t load.
+// memory once per thread block, keys and values are rebuilt from D/c = 16 indices per
+// token, keys are rotated by RoPE and dotted with the query, the bf16 sink/recent tokens are
+// attended directly, and the partials of every split are merged exactly. Two requests of
+// the same head share a thread block and its B_t load.
 //
-// GB300 design (differs from the page's Triton kernel):
-//  * B_t is copied into shared memory with TMA bulk copies; the index pages stream through
-//    a 4-stage shared-memory ring (32 pages of each request per stage) filled by TMA bulk
-//    copies, with full/empty mbarriers, so no warp waits on HBM latency per page. Every
+// GB300 design (differs from the page's Triton kernel). On this GPU each codeword lookup
+// costs shared-memory bandwidth (32 B per fp32 group), and that, not HBM, bounds the
+// kernel; the structure keeps every lookup a conflict-free 128-bit shared load and moves
+// no other data through shared memory per token:
+//  * Both slices stay resident: keys in fp32 (128 KB, TMA bulk copy; channels 0..63 and
+//    64..127 as two [256][64] tables), values in fp16 ([256][128], converted while
+//    staging; value rounding error ~1e-4 of the output). A codeword's shared-memory address
+//    is one byte permute: (index << 8) | lane offset.
+//  * Index pages stream through a 2-stage shared-memory ring (32 key and 32 value pages of
+//    each request per stage) filled by TMA bulk copies with full/empty mbarriers. Every
 //    wait is bounded and reports a timeout through the device error word.
-//  * Keys: 8 lanes per page, lane s owns the RoPE partner groups s and s+8 (channels
-//    8s..8s+7 and 64+8s..64+8s+7). The rotated query u = R(p_q - p) q satisfies
-//    <R(p_q) q, R(p) k> = <u, k>, so the key is never rotated: u is built once from the
-//    cos/sin table at the lane-group's first page, advanced one position per token by a
-//    fixed rotation R(-theta) and 256 positions per chunk by R(-256 theta), and re-read
-//    from the table every 16 chunks (a few ulp of drift at most). Rotation and dot
-//    product use packed fp32x2 FMAs. Codeword rows are read with 128-bit shared loads in a
-//    lane-dependent half order so the 8 lanes of a phase hit 8 distinct bank quads, and a
-//    transposing shuffle reduction (7 shuffles per 8 tokens) leaves lane s with token s.
-//  * Values: scores stay in shared memory (two-pass softmax) and, instead of rebuilding
-//    value vectors, each token adds its softmax weight to w[g][r] for its 16 codewords;
-//    o_g = sum_r w[g][r] B_t,V[g][r] is formed once per split (the same sum,
-//    re-associated), reading B_t,V from L2. The histogram is laid out
-//    [codeword][request*16 + group] so the 32 lanes of a warp (2 requests x 16 groups) hit
-//    32 distinct banks. Once the key pass is done, the value pages of the whole split are
-//    fetched by one bulk copy per request into the (then free) codebook buffer, and the
-//    bf16 window values are read by all warps at once.
-//  * The last thread block of a (request pair, head) to finish merges the split partials
-//    (arrival counter, no spin-wait) and resets the counter for the next call.
+//  * 8 lanes per page, lane s owns the RoPE partner groups s and s+8 (channels 8s..8s+7 and
+//    64+8s..64+8s+7). The rotated query u = R(p_q - p) q satisfies <R(p_q) q, R(p) k> =
+//    <u, k>, so keys are never rotated: u is built from the cos/sin table at a lane-group's
+//    first page, advanced one position per token by R(-theta) and one chunk (256
+//    positions) by R(-256 theta), and re-read from the table every 16 chunks. Packed fp32x2
+//    FMAs. A transposing shuffle reduction leaves lane s with the score of token s.
+//  * One pass with an online softmax per lane-group (running max, rescale on increase):
+//    the 8 softmax weights of a page are broadcast by shuffles and each lane accumulates
+//    its 16 value channels directly from the fp16 value table.
+//  * Lane-groups merge in registers (shuffles), warps through shared memory, splits in the
+//    last block of a (request pair, head) to finish (arrival counter, no spin-wait).
+#include <cuda_fp16.h>
+
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
 #include "../../include/kvq.h"
@@ -42,43 +42,56 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kLaneGroups = kThreads / 8;
-constexpr int kChunk = 32;                               // pages of each request per ring stage
-constexpr int kStages = 4;
-constexpr int kResync = 16;                              // chunks between cos/sin table reloads
-constexpr uint32_t kSliceBytes = kCB * kD * 4;           // 128 KB fp32 B_t slice
-constexpr uint32_t kStageBytes = 2 * kChunk * kPageBytes;  // 8 KB
+constexpr int kChunk = 32;                                // pages of each request per ring stage
+constexpr int kStages = 2;
+constexpr int kResync = 16;                               // chunks between cos/sin table reloads
+constexpr uint32_t kKSliceBytes = kCB * kD * 4;           // fp32 key codebook slice
+constexpr uint32_t kVSliceBytes = kCB * kD * 2;           // fp16 value codebook slice
+constexpr uint32_t kPart = kChunk * kPageBytes;           // 4 KB: one request's pages of one kind
+constexpr uint32_t kStageBytes = 4 * kPart;               // [K r0 | K r1 | V r0 | V r1]
 
 // shared-memory layout (bytes)
-constexpr int kOffCb = 0;
-constexpr int kOffHist = kOffCb + kSliceBytes;           // float [256][32]
-constexpr int kOffRing = kOffHist + kCB * 32 * 4;        // kStages x [2][kChunk][128] bytes
-constexpr int kOffQ = kOffRing + kStages * kStageBytes;  // float [2][128]
-constexpr int kOffOw = kOffQ + 2 * kD * 4;               // float [2][128] bf16-window V sums
-constexpr int kOffComb = kOffOw + 2 * kD * 4;            // float [2][128]
-constexpr int kOffRed = kOffComb + 2 * kD * 4;           // float [2][kWarps]
-constexpr int kOffBar = kOffRed + 256;                   // mbarriers + flags
-constexpr int kOffScores = kOffBar + 128;                // float [2][sc_stride]
-constexpr int kSmemLimit = 232448;                       // 227 KB opt-in per block
-
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kKSliceBytes;
+constexpr int kOffRing = kOffV + kVSliceBytes;
+constexpr int kOffQ = kOffRing + kStages * kStageBytes;    // float [2][128]
+constexpr int kOffJ = kOffQ + 2 * kD * 4;                  // float [8 slots][16]: cos, sin(256 theta)
+constexpr int kOffBar = kOffJ + 8 * 16 * 4;                // mbarriers + flags
+constexpr int kSmemBytes = kOffBar + 128;
+static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kOffBar % 8 == 0 && kOffRing % 128 == 0, "alignment");
 
-__device__ __forceinline__ void load8_perm(const float* p, int o0, float (&v)[8]) {
-  const float4 a = *reinterpret_cast<const float4*>(p + o0);
-  const float4 b = *reinterpret_cast<const float4*>(p + (4 - o0));
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
 __device__ __forceinline__ void ldg8_perm(const float* p, int o0, float (&v)[8]) {
   const float4 a = __ldg(reinterpret_cast<const float4*>(p + o0));
   const float4 b = __ldg(reinterpret_cast<const float4*>(p + (4 - o0)));
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
+__device__ __forceinline__ void load8_perm(const float* p, int o0, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p + o0);
+  const float4 b = *reinterpret_cast<const float4*>(p + (4 - o0));
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+// 8 consecutive bf16 values in the lane's half order
 __device__ __forceinline__ void ldg8_bf16_perm(const uint16_t* p, int o0, float (&v)[8]) {
   const uint2 a = __ldg(reinterpret_cast<const uint2*>(p + o0));
   const uint2 b = __ldg(reinterpret_cast<const uint2*>(p + (4 - o0)));
   v[0] = bf16_lo(a.x); v[1] = bf16_hi(a.x); v[2] = bf16_lo(a.y); v[3] = bf16_hi(a.y);
   v[4] = bf16_lo(b.x); v[5] = bf16_hi(b.x); v[6] = bf16_lo(b.y); v[7] = bf16_hi(b.y);
+}
+// 8 consecutive fp16 values (one 128-bit shared load), natural order
+__device__ __forceinline__ void lds8_fp16(const unsigned char* p, float2 (&v)[4]) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  v[0] = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+  v[1] = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+  v[2] = __half22float2(*reinterpret_cast<const __half2*>(&w.z));
+  v[3] = __half22float2(*reinterpret_cast<const __half2*>(&w.w));
+}
+// byte offset (index << 8) | lane_byte, the index being byte k of w (lane_byte < 256)
+template <int K>
+__device__ __forceinline__ uint32_t row_off(uint32_t w, uint32_t lane_byte) {
+  return __byte_perm(w, lane_byte, 0x5504u | (K << 4));
 }
 
 __device__ __forceinline__ void transpose_reduce8(float (&p)[8], int s, unsigned mask) {
@@ -116,6 +129,23 @@ __device__ __forceinline__ void rotate8(float2 (&ul)[4], float2 (&uh)[4], const 
   }
 }
 
+// rotated query u = R(d) q for the lane's 8 pairs (lane half order), q from shared memory
+__device__ __forceinline__ void rotated_query(const float* rc, const float* rs, int d, int s, int o0,
+                                              const float* q, float2 (&ul)[4], float2 (&uh)[4]) {
+  float c8[8], s8[8], ql[8], qh[8];
+  ldg8_perm(rc + (size_t)d * (kD / 2) + 8 * s, o0, c8);
+  ldg8_perm(rs + (size_t)d * (kD / 2) + 8 * s, o0, s8);
+  load8_perm(q + 8 * s, o0, ql);
+  load8_perm(q + 64 + 8 * s, o0, qh);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    ul[k] = make_float2(ql[2 * k] * c8[2 * k] - qh[2 * k] * s8[2 * k],
+                        ql[2 * k + 1] * c8[2 * k + 1] - qh[2 * k + 1] * s8[2 * k + 1]);
+    uh[k] = make_float2(qh[2 * k] * c8[2 * k] + ql[2 * k] * s8[2 * k],
+                        qh[2 * k + 1] * c8[2 * k + 1] + ql[2 * k + 1] * s8[2 * k + 1]);
+  }
+}
+
 // A timed-out wait marks the block as failed; every later wait then returns at once so
 // that all threads reach the same barriers and leave together.
 __device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, volatile int* failed, int* err) {
@@ -126,26 +156,51 @@ __device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, volat
   return false;
 }
 
-struct Req {
-  int L, NP, pend, nq, nsink, nwin;
+// running softmax state of one lane (the max is shared by its lane-group)
+struct Acc {
+  float M, l;
+  float2 ol[4], oh[4];
 };
 
-__global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a, const float scale_log2,
-                                                                const int sc_stride) {
+// Fold the 8 scores of a page (lane s holds token s; -inf for a missing token) into the
+// running state: raise the shared max if needed (rescaling the sums), return this lane's
+// token weight.
+__device__ __forceinline__ float online_weights(Acc& A, float sc, unsigned mask) {
+  float mp = sc;
+  mp = fmaxf(mp, __shfl_xor_sync(mask, mp, 4));
+  mp = fmaxf(mp, __shfl_xor_sync(mask, mp, 2));
+  mp = fmaxf(mp, __shfl_xor_sync(mask, mp, 1));
+  if (mp > A.M) {  // uniform within the lane-group
+    const float f = (A.M == -INFINITY) ? 0.f : exp2f(A.M - mp);
+    const float2 f2 = make_float2(f, f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      A.ol[k] = __fmul2_rn(A.ol[k], f2);
+      A.oh[k] = __fmul2_rn(A.oh[k], f2);
+    }
+    A.l *= f;
+    A.M = mp;
+  }
+  const float p = (sc == -INFINITY) ? 0.f : exp2f(sc - A.M);
+  A.l += p;
+  return p;
+}
+
+struct Req {
+  int L, NP, pend, nsink, nwin;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a, const float scale_log2) {
   extern __shared__ __align__(128) unsigned char smem[];
-  float* cbs = reinterpret_cast<float*>(smem + kOffCb);
-  float* hist = reinterpret_cast<float*>(smem + kOffHist);
+  float* ks = reinterpret_cast<float*>(smem + kOffK);
+  __half* vs = reinterpret_cast<__half*>(smem + kOffV);
   unsigned char* ring = smem + kOffRing;
   float* qs = reinterpret_cast<float*>(smem + kOffQ);
-  float* ow = reinterpret_cast<float*>(smem + kOffOw);
-  float* comb = reinterpret_cast<float*>(smem + kOffComb);
-  float* red = reinterpret_cast<float*>(smem + kOffRed);
-  uint64_t* cbar = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* full = cbar + 1;
+  uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* full = kbar + 1;
   uint64_t* empty = full + kStages;
   int* sflag = reinterpret_cast<int*>(empty + kStages);  // [0] merge, [1] failed
   volatile int* failed = sflag + 1;
-  float* sc = reinterpret_cast<float*>(smem + kOffScores);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int split = blockIdx.x, pair = blockIdx.y, h = blockIdx.z;
@@ -174,33 +229,35 @@ __global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a
     rq[r].L = L;
     rq[r].NP = NP;
     rq[r].pend = min(NP, pg0 + a.pages_per_split);
-    rq[r].nq = max(0, rq[r].pend - pg0) * kPage;
     rq[r].nsink = min(a.sink, L);
     rq[r].nwin = (split == 0 && L > 0) ? (rq[r].nsink + max(0, L - a.sink - kPage * NP)) : 0;
   }
-  const int n_items = max(rq[0].nq, rq[1].nq) / kPage;  // pages of the longer request
+  const int n_items = max(max(0, rq[0].pend - pg0), max(0, rq[1].pend - pg0));
   const int n_chunks = (n_items + kChunk - 1) / kChunk;
-  const int total_chunks = n_chunks;                     // key pages through the ring
-
   const size_t bh0 = ((size_t)b0 * H + h) * (size_t)a.max_pages * kPageBytes;
   const size_t bh1 = ((size_t)(b0 + (nreq > 1 ? 1 : 0)) * H + h) * (size_t)a.max_pages * kPageBytes;
 
-  // producer (thread 0): chunk c of the key pages into ring stage c % kStages
+  // producer (thread 0): key and value pages of chunk c into ring stage c % kStages
   auto produce = [&](int c) {
     const int st = c % kStages;
-    const uint8_t* base = a.idx_k;
     const int p_first = pg0 + c * kChunk;
     const int n0 = min(kChunk, max(0, rq[0].pend - p_first));
     const int n1 = min(kChunk, max(0, rq[1].pend - p_first));
-    mbar_arrive_expect_tx(&full[st], (uint32_t)(n0 + n1) * kPageBytes);
+    mbar_arrive_expect_tx(&full[st], (uint32_t)(n0 + n1) * 2 * kPageBytes);
     unsigned char* dst = ring + st * kStageBytes;
-    if (n0 > 0) bulk_g2s(dst, base + bh0 + (size_t)p_first * kPageBytes, n0 * kPageBytes, &full[st]);
-    if (n1 > 0)
-      bulk_g2s(dst + kChunk * kPageBytes, base + bh1 + (size_t)p_first * kPageBytes, n1 * kPageBytes, &full[st]);
+    const size_t off = (size_t)p_first * kPageBytes;
+    if (n0 > 0) {
+      bulk_g2s(dst, a.idx_k + bh0 + off, n0 * kPageBytes, &full[st]);
+      bulk_g2s(dst + 2 * kPart, a.idx_v + bh0 + off, n0 * kPageBytes, &full[st]);
+    }
+    if (n1 > 0) {
+      bulk_g2s(dst + kPart, a.idx_k + bh1 + off, n1 * kPageBytes, &full[st]);
+      bulk_g2s(dst + 3 * kPart, a.idx_v + bh1 + off, n1 * kPageBytes, &full[st]);
+    }
   };
 
   if (tid == 0) {
-    mbar_init(cbar, 1);
+    mbar_init(kbar, 1);
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -211,73 +268,115 @@ __global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a
     fence_mbar_init();
   }
   __syncthreads();
-  const float* btk = a.bt_k + (size_t)h * kCB * kD;
-  const float* btv = a.bt_v + (size_t)h * kCB * kD;
   if (tid == 0 && n_items > 0) {
-    mbar_arrive_expect_tx(cbar, kSliceBytes);
+    const float* btk = a.bt_k + (size_t)h * kCB * kD;
+    mbar_arrive_expect_tx(kbar, kKSliceBytes);
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      bulk_g2s(cbs + k * (kSliceBytes / 16), btk + k * (kSliceBytes / 16), kSliceBytes / 4, cbar);
-    for (int gc = 0; gc < min(kStages, total_chunks); ++gc) produce(gc);
+      bulk_g2s(ks + k * (kKSliceBytes / 16), btk + k * (kKSliceBytes / 16), kKSliceBytes / 4, kbar);
+    for (int c = 0; c < min(kStages, n_chunks); ++c) produce(c);
   }
-  for (int i = tid; i < kCB * 32 / 4; i += kThreads)
-    reinterpret_cast<float4*>(hist)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (n_items > 0) {  // value slice: fp32 [2][256][64] in L2 -> fp16 [256][128] in shared memory
+    const float4* src = reinterpret_cast<const float4*>(a.bt_v + (size_t)h * kCB * kD);
+    for (int i = tid; i < kCB * kD / 4; i += kThreads) {
+      const float4 v = __ldg(src + i);
+      const int half = i / (kCB * kD / 8), rem = i % (kCB * kD / 8);
+      const int row = rem / (kD / 8), c4 = rem % (kD / 8);
+      __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
+      uint2 w;
+      w.x = *reinterpret_cast<uint32_t*>(&lo);
+      w.y = *reinterpret_cast<uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(vs + row * kD + half * (kD / 2))[c4] = w;
+    }
+  }
   if (tid < 2 * kD) {
     const int r = tid >> 7;
-    const uint16_t* qp = a.q + ((size_t)(b0 + min(r, nreq - 1)) * H + h) * kD;
-    qs[tid] = bf16_to_f32(qp[tid & 127]);
-    ow[tid] = 0.f;
+    qs[tid] = bf16_to_f32(a.q[((size_t)(b0 + min(r, nreq - 1)) * H + h) * kD + (tid & 127)]);
+  }
+  if (tid < 8 && n_chunks > 1) {  // cos/sin(256 theta_i) for slot tid, in that slot's half order
+    float* jt = reinterpret_cast<float*>(smem + kOffJ) + tid * 16;
+    const int jo0 = (tid & 4) ? 4 : 0;
+    float c8[8], s8[8];
+    ldg8_perm(a.rope_cos + (size_t)(kChunk * kPage) * (kD / 2) + 8 * tid, jo0, c8);
+    ldg8_perm(a.rope_sin + (size_t)(kChunk * kPage) * (kD / 2) + 8 * tid, jo0, s8);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      jt[k] = c8[k];
+      jt[8 + k] = s8[k];
+    }
   }
   __syncthreads();
 
   const int s = tid & 7;                 // slot: groups s and s + 8
-  const int o0 = (s & 4) ? 4 : 0;        // half order (bank-quad spreading)
+  const int o0 = (s & 4) ? 4 : 0;        // key half order (bank-quad spreading)
   const unsigned gmask = 0xFFu << (lane & 24);
   const int lg = tid >> 3;
+  const int r = lg >> 5, po = lg & 31;   // this lane-group's request and page slot
+  const Req R = r ? rq[1] : rq[0];
+  const float* qr = qs + r * kD;
 
-  float mloc0 = -INFINITY, mloc1 = -INFINITY;
-
-  // ---- bf16 window scores (split 0 only) ------------------------------------------------
-  for (int wi = lg; wi < rq[0].nwin + rq[1].nwin; wi += kLaneGroups) {
-    const bool r1 = wi >= rq[0].nwin;
-    const Req R = r1 ? rq[1] : rq[0];
-    const int r = r1 ? 1 : 0;
-    const int w = r1 ? wi - rq[0].nwin : wi;
-    const int p = (w < R.nsink) ? w : a.sink + kPage * R.NP + (w - R.nsink);
-    const int slot = (p < a.sink) ? p : a.sink + (p - a.sink) % (a.recent + kPage);
-    const uint16_t* kr = a.win_k + (((size_t)(b0 + r) * H + h) * a.win_slots + slot) * kD;
-    float klo[8], khi[8], c[8], sn[8], ql[8], qh[8];
-    ldg8_bf16_perm(kr + 8 * s, o0, klo);
-    ldg8_bf16_perm(kr + 64 + 8 * s, o0, khi);
-    const int dl = R.L - 1 - p;
-    ldg8_perm(a.rope_cos + (size_t)dl * (kD / 2) + 8 * s, o0, c);
-    ldg8_perm(a.rope_sin + (size_t)dl * (kD / 2) + 8 * s, o0, sn);
-    load8_perm(qs + r * kD + 8 * s, o0, ql);
-    load8_perm(qs + r * kD + 64 + 8 * s, o0, qh);
-    float acc = 0.f;
+  // value accumulators in natural channel order: ol = channels 8s..8s+7, oh = 64+8s..
+  Acc A;
+  A.M = -INFINITY;
+  A.l = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float ul = ql[k] * c[k] - qh[k] * sn[k];
-      const float uh = qh[k] * c[k] + ql[k] * sn[k];
-      acc = fmaf(ul, klo[k], acc);
-      acc = fmaf(uh, khi[k], acc);
+  for (int k = 0; k < 4; ++k) {
+    A.ol[k] = make_float2(0.f, 0.f);
+    A.oh[k] = make_float2(0.f, 0.f);
+  }
+  const uint16_t* wk = a.win_k + ((size_t)(b0 + r) * H + h) * a.win_slots * kD;
+  const uint16_t* wv = a.win_v + ((size_t)(b0 + r) * H + h) * a.win_slots * kD;
+
+  // ---- bf16 window (split 0): lane-group po takes window tokens [8 wp, 8 wp + 8) ----------
+  for (int wp = po; wp * kPage < R.nwin; wp += kLaneGroups / 2) {
+    float part[8];
+    int slots[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int w = wp * kPage + j;
+      part[j] = 0.f;
+      slots[j] = 0;
+      if (w < R.nwin) {
+        const int p = (w < R.nsink) ? w : a.sink + kPage * R.NP + (w - R.nsink);
+        const int slot = (p < a.sink) ? p : a.sink + (p - a.sink) % (a.recent + kPage);
+        slots[j] = slot;
+        float kl[8], kh[8];
+        ldg8_bf16_perm(wk + (size_t)slot * kD + 8 * s, o0, kl);
+        ldg8_bf16_perm(wk + (size_t)slot * kD + 64 + 8 * s, o0, kh);
+        float2 ul[4], uh[4];
+        rotated_query(a.rope_cos, a.rope_sin, R.L - 1 - p, s, o0, qr, ul, uh);
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc = __ffma2_rn(ul[k], make_float2(kl[2 * k], kl[2 * k + 1]), acc);
+          acc = __ffma2_rn(uh[k], make_float2(kh[2 * k], kh[2 * k + 1]), acc);
+        }
+        part[j] = acc.x + acc.y;
+      }
     }
-    acc += __shfl_xor_sync(gmask, acc, 4);
-    acc += __shfl_xor_sync(gmask, acc, 2);
-    acc += __shfl_xor_sync(gmask, acc, 1);
-    if (s == 0) {
-      const float v = acc * scale_log2;
-      sc[r * sc_stride + R.nq + w] = v;
-      if (r1) mloc1 = fmaxf(mloc1, v);
-      else mloc0 = fmaxf(mloc0, v);
+    transpose_reduce8(part, s, gmask);
+    const float sc = (wp * kPage + s < R.nwin) ? part[0] * scale_log2 : -INFINITY;
+    const float p = online_weights(A, sc, gmask);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float pj = __shfl_sync(gmask, p, (lane & 24) + j);
+      if (wp * kPage + j < R.nwin) {
+        float vl[8], vh[8];
+        ldg8_bf16_perm(wv + (size_t)slots[j] * kD + 8 * s, 0, vl);
+        ldg8_bf16_perm(wv + (size_t)slots[j] * kD + 64 + 8 * s, 0, vh);
+        const float2 p2 = make_float2(pj, pj);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          A.ol[k] = __ffma2_rn(p2, make_float2(vl[2 * k], vl[2 * k + 1]), A.ol[k]);
+          A.oh[k] = __ffma2_rn(p2, make_float2(vh[2 * k], vh[2 * k + 1]), A.oh[k]);
+        }
+      }
     }
   }
 
-  // ---- key pages: lane-group lg takes request lg/32, page lg%32 of every chunk ----------
+  // ---- quantized pages -------------------------------------------------------------------
   {
-    const int r = lg >> 5, po = lg & 31;
-    const Req R = (r == 0) ? rq[0] : rq[1];
-    float2 cth[4], sth[4], nsth[4], cj[4], sj[4], nsj[4];
+    float2 cth[4], sth[4], nsth[4];
     {
       float c8[8], s8[8];
       ldg8_perm(a.rope_cos + (kD / 2) + 8 * s, o0, c8);
@@ -288,51 +387,42 @@ __global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a
         sth[k] = make_float2(s8[2 * k], s8[2 * k + 1]);
         nsth[k] = make_float2(-s8[2 * k], -s8[2 * k + 1]);
       }
-      const int jrow = kChunk * kPage;  // one chunk further: 256 positions
-      if (n_chunks > 1 && jrow < a.max_ctx) {
-        ldg8_perm(a.rope_cos + (size_t)jrow * (kD / 2) + 8 * s, o0, c8);
-        ldg8_perm(a.rope_sin + (size_t)jrow * (kD / 2) + 8 * s, o0, s8);
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        cj[k] = make_float2(c8[2 * k], c8[2 * k + 1]);
-        sj[k] = make_float2(s8[2 * k], s8[2 * k + 1]);
-        nsj[k] = make_float2(-s8[2 * k], -s8[2 * k + 1]);
-      }
     }
-    float ql8[8], qh8[8];
-    load8_perm(qs + r * kD + 8 * s, o0, ql8);
-    load8_perm(qs + r * kD + 64 + 8 * s, o0, qh8);
-    float2 u0l[4], u0h[4];  // rotated query at this lane-group's current page start
+    float2 u0l[4], u0h[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       u0l[k] = make_float2(0.f, 0.f);
       u0h[k] = make_float2(0.f, 0.f);
     }
+    // lane byte offsets inside a 256-byte table row: key halves swapped for s >= 4 so the 8
+    // lanes of a phase hit 8 bank quads; value lanes read 16 natural bytes each
+    const uint32_t kb0 = 32 * s + 4 * o0, kb1 = kb0 ^ 16u;
+    const uint32_t vb0 = 16 * s, vb1 = 128 + 16 * s;
+    const unsigned char* ksb = reinterpret_cast<const unsigned char*>(ks);
+    const unsigned char* vsb = reinterpret_cast<const unsigned char*>(vs);
+    const float* jt = reinterpret_cast<const float*>(smem + kOffJ) + s * 16;
 
-    if (n_items > 0) wait_stage(cbar, 0, failed, a.err);
+    if (n_items > 0) wait_stage(kbar, 0, failed, a.err);
     for (int c = 0; c < n_chunks; ++c) {
       const int st = c % kStages;
       wait_stage(&full[st], (c / kStages) & 1, failed, a.err);
       const int pg = pg0 + c * kChunk + po;
       if (!*failed && pg < R.pend) {
         if (c % kResync == 0) {
-          const int d0 = R.L - 1 - (a.sink + kPage * pg);
-          float c8[8], s8[8];
-          ldg8_perm(a.rope_cos + (size_t)d0 * (kD / 2) + 8 * s, o0, c8);
-          ldg8_perm(a.rope_sin + (size_t)d0 * (kD / 2) + 8 * s, o0, s8);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            u0l[k] = make_float2(ql8[2 * k] * c8[2 * k] - qh8[2 * k] * s8[2 * k],
-                                 ql8[2 * k + 1] * c8[2 * k + 1] - qh8[2 * k + 1] * s8[2 * k + 1]);
-            u0h[k] = make_float2(qh8[2 * k] * c8[2 * k] + ql8[2 * k] * s8[2 * k],
-                                 qh8[2 * k + 1] * c8[2 * k + 1] + ql8[2 * k + 1] * s8[2 * k + 1]);
-          }
-        } else {
-          rotate8(u0l, u0h, cj, sj, nsj);  // 256 positions later
+          rotated_query(a.rope_cos, a.rope_sin, R.L - 1 - (a.sink + kPage * pg), s, o0, qr, u0l, u0h);
+        } else {  // 256 positions later
+          const float4 c0 = *reinterpret_cast<const float4*>(jt), c1 = *reinterpret_cast<const float4*>(jt + 4);
+          const float4 s0 = *reinterpret_cast<const float4*>(jt + 8), s1 = *reinterpret_cast<const float4*>(jt + 12);
+          const float2 cj[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w), make_float2(c1.x, c1.y),
+                                make_float2(c1.z, c1.w)};
+          const float2 sj[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
+                                make_float2(s1.z, s1.w)};
+          const float2 nsj[4] = {make_float2(-s0.x, -s0.y), make_float2(-s0.z, -s0.w), make_float2(-s1.x, -s1.y),
+                                 make_float2(-s1.z, -s1.w)};
+          rotate8(u0l, u0h, cj, sj, nsj);
         }
-        const uint4 row =
-            *reinterpret_cast<const uint4*>(ring + st * kStageBytes + (r * kChunk + po) * kPageBytes + 16 * s);
+        const unsigned char* stage = ring + st * kStageBytes;
+        const uint4 rowk = *reinterpret_cast<const uint4*>(stage + r * kPart + po * kPageBytes + 16 * s);
         float2 ul[4], uh[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -342,190 +432,120 @@ __global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a
         float part[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const uint32_t wd = (j < 2) ? row.x : (j < 4) ? row.y : (j < 6) ? row.z : row.w;
-          const uint32_t sh = (j & 1) * 16;
-          const uint32_t rlo = (wd >> sh) & 0xFFu;
-          const uint32_t rhi = (wd >> (sh + 8)) & 0xFFu;
-          const float* pl = cbs + rlo * kD + 8 * s;
-          const float* ph = cbs + rhi * kD + 64 + 8 * s;
-          const float4 la = *reinterpret_cast<const float4*>(pl + o0);
-          const float4 lb = *reinterpret_cast<const float4*>(pl + (4 - o0));
-          const float4 ha = *reinterpret_cast<const float4*>(ph + o0);
-          const float4 hb = *reinterpret_cast<const float4*>(ph + (4 - o0));
-          float2 acc = __fmul2_rn(ul[0], make_float2(la.x, la.y));
-          acc = __ffma2_rn(ul[1], make_float2(la.z, la.w), acc);
-          acc = __ffma2_rn(ul[2], make_float2(lb.x, lb.y), acc);
-          acc = __ffma2_rn(ul[3], make_float2(lb.z, lb.w), acc);
-          acc = __ffma2_rn(uh[0], make_float2(ha.x, ha.y), acc);
-          acc = __ffma2_rn(uh[1], make_float2(ha.z, ha.w), acc);
-          acc = __ffma2_rn(uh[2], make_float2(hb.x, hb.y), acc);
-          acc = __ffma2_rn(uh[3], make_float2(hb.z, hb.w), acc);
+          const uint32_t wd = (j < 2) ? rowk.x : (j < 4) ? rowk.y : (j < 6) ? rowk.z : rowk.w;
+          uint32_t al0, al1, ah0, ah1;
+          if (j & 1) {
+            al0 = row_off<2>(wd, kb0); al1 = row_off<2>(wd, kb1);
+            ah0 = row_off<3>(wd, kb0); ah1 = row_off<3>(wd, kb1);
+          } else {
+            al0 = row_off<0>(wd, kb0); al1 = row_off<0>(wd, kb1);
+            ah0 = row_off<1>(wd, kb0); ah1 = row_off<1>(wd, kb1);
+          }
+          const float4 la = *reinterpret_cast<const float4*>(ksb + al0);
+          const float4 lb = *reinterpret_cast<const float4*>(ksb + al1);
+          const float4 ha = *reinterpret_cast<const float4*>(ksb + kKSliceBytes / 2 + ah0);
+          const float4 hb = *reinterpret_cast<const float4*>(ksb + kKSliceBytes / 2 + ah1);
+          float2 acc0 = __fmul2_rn(ul[0], make_float2(la.x, la.y));
+          float2 acc1 = __fmul2_rn(uh[0], make_float2(ha.x, ha.y));
+          acc0 = __ffma2_rn(ul[1], make_float2(la.z, la.w), acc0);
+          acc1 = __ffma2_rn(uh[1], make_float2(ha.z, ha.w), acc1);
+          acc0 = __ffma2_rn(ul[2], make_float2(lb.x, lb.y), acc0);
+          acc1 = __ffma2_rn(uh[2], make_float2(hb.x, hb.y), acc1);
+          acc0 = __ffma2_rn(ul[3], make_float2(lb.z, lb.w), acc0);
+          acc1 = __ffma2_rn(uh[3], make_float2(hb.z, hb.w), acc1);
+          const float2 acc = __fadd2_rn(acc0, acc1);
           part[j] = acc.x + acc.y;
           if (j < 7) rotate8(ul, uh, cth, sth, nsth);  // next token: one position later
         }
         transpose_reduce8(part, s, gmask);
-        const float v = part[0] * scale_log2;
-        sc[r * sc_stride + (c * kChunk + po) * kPage + s] = v;
-        if (r) mloc1 = fmaxf(mloc1, v);
-        else mloc0 = fmaxf(mloc0, v);
+        const float p = online_weights(A, part[0] * scale_log2, gmask);
+        const uint4 rowv = *reinterpret_cast<const uint4*>(stage + (2 + r) * kPart + po * kPageBytes + 16 * s);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float pj = __shfl_sync(gmask, p, (lane & 24) + j);
+          const uint32_t wd = (j < 2) ? rowv.x : (j < 4) ? rowv.y : (j < 6) ? rowv.z : rowv.w;
+          const uint32_t avl = (j & 1) ? row_off<2>(wd, vb0) : row_off<0>(wd, vb0);
+          const uint32_t avh = (j & 1) ? row_off<3>(wd, vb1) : row_off<1>(wd, vb1);
+          float2 vl[4], vh[4];
+          lds8_fp16(vsb + avl, vl);
+          lds8_fp16(vsb + avh, vh);
+          const float2 p2 = make_float2(pj, pj);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            A.ol[k] = __ffma2_rn(p2, vl[k], A.ol[k]);
+            A.oh[k] = __ffma2_rn(p2, vh[k], A.oh[k]);
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
-      if (tid == 0 && c + kStages < total_chunks) {
+      if (tid == 0 && c + kStages < n_chunks) {
         if (wait_stage(&empty[st], (c / kStages) & 1, failed, a.err)) produce(c + kStages);
       }
     }
   }
 
-  // ---- B_t(K) no longer read: fetch this split's value pages into the same buffer -------
-  // (request r's pages at byte offset r * pages_per_split * 128; at most 128 KB in all)
-  unsigned char* vpages = reinterpret_cast<unsigned char*>(cbs);
-  fence_proxy_async_smem();
+  // ---- merge: lanes of a group (l), lane-groups of a warp (shuffles), warps (smem) -------
+  A.l += __shfl_xor_sync(0xFFFFFFFFu, A.l, 1);
+  A.l += __shfl_xor_sync(0xFFFFFFFFu, A.l, 2);
+  A.l += __shfl_xor_sync(0xFFFFFFFFu, A.l, 4);
+#pragma unroll
+  for (int off = 8; off <= 16; off <<= 1) {
+    const float Mo = __shfl_xor_sync(0xFFFFFFFFu, A.M, off);
+    const float lo = __shfl_xor_sync(0xFFFFFFFFu, A.l, off);
+    const float Mn = fmaxf(A.M, Mo);
+    const float f = (A.M == -INFINITY) ? 0.f : exp2f(A.M - Mn);
+    const float fo = (Mo == -INFINITY) ? 0.f : exp2f(Mo - Mn);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 xl = make_float2(__shfl_xor_sync(0xFFFFFFFFu, A.ol[k].x, off),
+                                    __shfl_xor_sync(0xFFFFFFFFu, A.ol[k].y, off));
+      const float2 xh = make_float2(__shfl_xor_sync(0xFFFFFFFFu, A.oh[k].x, off),
+                                    __shfl_xor_sync(0xFFFFFFFFu, A.oh[k].y, off));
+      A.ol[k] = __ffma2_rn(A.ol[k], make_float2(f, f), __fmul2_rn(xl, make_float2(fo, fo)));
+      A.oh[k] = __ffma2_rn(A.oh[k], make_float2(f, f), __fmul2_rn(xh, make_float2(fo, fo)));
+    }
+    A.l = A.l * f + lo * fo;
+    A.M = Mn;
+  }
+  // per-warp partials in the (now idle) ring: [warp][130] = o[128], M, l
+  __syncthreads();  // every warp is done with the ring
+  float* wpart = reinterpret_cast<float*>(ring);
+  if (lane < 8) {
+    float* wp = wpart + warp * (kD + 2);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      reinterpret_cast<float2*>(wp + 8 * s)[k] = A.ol[k];
+      reinterpret_cast<float2*>(wp + 64 + 8 * s)[k] = A.oh[k];
+    }
+    if (lane == 0) {
+      wp[kD] = A.M;
+      wp[kD + 1] = A.l;
+    }
+  }
   __syncthreads();
-  if (tid == 0 && n_items > 0 && !*failed) {
-    const int n0 = max(0, rq[0].pend - pg0), n1 = max(0, rq[1].pend - pg0);
-    mbar_arrive_expect_tx(cbar, (uint32_t)(n0 + n1) * kPageBytes);
-    if (n0 > 0) bulk_g2s(vpages, a.idx_v + bh0 + (size_t)pg0 * kPageBytes, n0 * kPageBytes, cbar);
-    if (n1 > 0)
-      bulk_g2s(vpages + (size_t)a.pages_per_split * kPageBytes, a.idx_v + bh1 + (size_t)pg0 * kPageBytes,
-               n1 * kPageBytes, cbar);
-  }
+  if (*failed) return;  // uniform: every thread read the flag after the barrier
 
-  // ---- softmax statistics per request ---------------------------------------------------
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    mloc0 = fmaxf(mloc0, __shfl_xor_sync(0xFFFFFFFFu, mloc0, off));
-    mloc1 = fmaxf(mloc1, __shfl_xor_sync(0xFFFFFFFFu, mloc1, off));
-  }
-  if (lane == 0) {
-    red[warp] = mloc0;
-    red[kWarps + warp] = mloc1;
-  }
-  __syncthreads();
-  float M0 = -INFINITY, M1 = -INFINITY;
-  for (int w = 0; w < kWarps; ++w) {
-    M0 = fmaxf(M0, red[w]);
-    M1 = fmaxf(M1, red[kWarps + w]);
-  }
-  __syncthreads();  // red is reused below
-  float ls0 = 0.f, ls1 = 0.f;
-  if (M0 != -INFINITY) {
-    for (int i = tid; i < rq[0].nq + rq[0].nwin; i += kThreads) {
-      const float e = exp2f(sc[i] - M0);
-      sc[i] = e;
-      ls0 += e;
-    }
-  }
-  if (M1 != -INFINITY) {
-    for (int i = tid; i < rq[1].nq + rq[1].nwin; i += kThreads) {
-      const float e = exp2f(sc[sc_stride + i] - M1);
-      sc[sc_stride + i] = e;
-      ls1 += e;
-    }
-  }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    ls0 += __shfl_xor_sync(0xFFFFFFFFu, ls0, off);
-    ls1 += __shfl_xor_sync(0xFFFFFFFFu, ls1, off);
-  }
-  if (lane == 0) {
-    red[warp] = ls0;
-    red[kWarps + warp] = ls1;
-  }
-  __syncthreads();  // weights in sc are final
-  float L0s = 0.f, L1s = 0.f;
-  for (int w = 0; w < kWarps; ++w) {
-    L0s += red[w];
-    L1s += red[kWarps + w];
-  }
-
-  // ---- bf16 window values: warp w takes window tokens w, w+16, ...; lane = 4 channels ----
-  {
-    float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-    const int nw = rq[0].nwin + rq[1].nwin;
-#pragma unroll 4
-    for (int wi = warp; wi < nw; wi += kWarps) {
-      const bool r1 = wi >= rq[0].nwin;
-      const Req R = r1 ? rq[1] : rq[0];
-      const int r = r1 ? 1 : 0;
-      const int w = r1 ? wi - rq[0].nwin : wi;
-      const int p = (w < R.nsink) ? w : a.sink + kPage * R.NP + (w - R.nsink);
-      const int slot = (p < a.sink) ? p : a.sink + (p - a.sink) % (a.recent + kPage);
-      const uint2 v = __ldg(reinterpret_cast<const uint2*>(
-          a.win_v + (((size_t)(b0 + r) * H + h) * a.win_slots + slot) * kD + 4 * lane));
-      const float pw = sc[r * sc_stride + R.nq + w];
-      const float p0 = r1 ? 0.f : pw, p1 = r1 ? pw : 0.f;
-      const float v0 = bf16_lo(v.x), v1 = bf16_hi(v.x), v2 = bf16_lo(v.y), v3 = bf16_hi(v.y);
-      acc0.x = fmaf(p0, v0, acc0.x); acc0.y = fmaf(p0, v1, acc0.y);
-      acc0.z = fmaf(p0, v2, acc0.z); acc0.w = fmaf(p0, v3, acc0.w);
-      acc1.x = fmaf(p1, v0, acc1.x); acc1.y = fmaf(p1, v1, acc1.y);
-      acc1.z = fmaf(p1, v2, acc1.z); acc1.w = fmaf(p1, v3, acc1.w);
-    }
-    // per-warp partial sums into the ring buffer (free now): [warp][request][128]
-    float* wpart = reinterpret_cast<float*>(ring);
-    reinterpret_cast<float4*>(wpart + (warp * 2 + 0) * kD)[lane] = acc0;
-    reinterpret_cast<float4*>(wpart + (warp * 2 + 1) * kD)[lane] = acc1;
-  }
-
-  // ---- value pages (now in shared memory): warp w takes pages w, w+16, ...; lane =
-  //      (request, group) column of the histogram ----------------------------------------
-  if (n_items > 0) wait_stage(cbar, 1, failed, a.err);
-  {
-    const int r = lane >> 4, g = lane & 15;
-    const int sl = g & 7, hb = (g >> 3) * 8;
-    const int np_r = max(0, (r ? rq[1].pend : rq[0].pend) - pg0);
-    const unsigned char* vp = vpages + (size_t)r * a.pages_per_split * kPageBytes + 16 * sl;
-    if (!*failed) {
-      for (int pi = warp; pi < np_r; pi += kWarps) {
-        const uint4 row = *reinterpret_cast<const uint4*>(vp + (size_t)pi * kPageBytes);
-        const float* pw = sc + r * sc_stride + pi * kPage;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t wd = (j < 2) ? row.x : (j < 4) ? row.y : (j < 6) ? row.z : row.w;
-          const uint32_t bin = (wd >> ((j & 1) * 16 + hb)) & 0xFFu;
-          atomicAdd(&hist[bin * 32 + lane], pw[j]);
-        }
+  // threads (request rr, channel ch) merge the 8 warps of their request
+  const int rr = tid >> 7, ch = tid & 127;
+  float Mr = -INFINITY, Lr = 0.f, o = 0.f;
+  if (tid < 2 * kD) {
+    for (int w = rr * 8; w < rr * 8 + 8; ++w) Mr = fmaxf(Mr, wpart[w * (kD + 2) + kD]);
+    if (Mr != -INFINITY) {
+      for (int w = rr * 8; w < rr * 8 + 8; ++w) {
+        const float mw = wpart[w * (kD + 2) + kD];
+        if (mw == -INFINITY) continue;
+        const float f = exp2f(mw - Mr);
+        Lr = fmaf(f, wpart[w * (kD + 2) + kD + 1], Lr);
+        o = fmaf(f, wpart[w * (kD + 2) + ch], o);
       }
     }
   }
-  __syncthreads();
-  if (tid < 2 * kD) {  // window value sums of the 16 warps
-    const float* wpart = reinterpret_cast<const float*>(ring);
-    const int r = tid >> 7, ch = tid & 127;
-    float acc = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) acc += wpart[(w * 2 + r) * kD + ch];
-    ow[tid] = acc;
-  }
 
-  // ---- o_g = sum_r w[g][r] * B_t,V[g][r], B_t,V read from L2 ---------------------------
-  if (*failed) return;  // uniform: every thread read the flag after the last barrier
-  float o = 0.f;
-  const int rr = (tid >> 7) & 1, ch = tid & 127, half = tid >> 8;
-  if (n_items > 0) {
-    const int col = rr * 16 + (ch >> 3);
-    const int b_lo = half * 128;
-    float o1 = 0.f, o2 = 0.f, o3 = 0.f;
-#pragma unroll 4
-    for (int bin = b_lo; bin < b_lo + 128; bin += 4) {
-      o = fmaf(hist[bin * 32 + col], __ldg(btv + bin * kD + ch), o);
-      o1 = fmaf(hist[(bin + 1) * 32 + col], __ldg(btv + (bin + 1) * kD + ch), o1);
-      o2 = fmaf(hist[(bin + 2) * 32 + col], __ldg(btv + (bin + 2) * kD + ch), o2);
-      o3 = fmaf(hist[(bin + 3) * 32 + col], __ldg(btv + (bin + 3) * kD + ch), o3);
-    }
-    o = (o + o1) + (o2 + o3);
-  }
-  if (half) comb[rr * kD + ch] = o;
-  __syncthreads();
-
-  const float Mr = rr ? M1 : M0;
-  const float Lr = rr ? L1s : L0s;
   if (a.n_split == 1) {
-    if (!half && rr < nreq) {
-      const int b = b0 + rr;
-      o += comb[rr * kD + ch] + ow[rr * kD + ch];
+    if (tid < 2 * kD && rr < nreq) {
       const float val = (Lr > 0.f) ? o / Lr : 0.f;
-      const size_t oi = ((size_t)b * H + h) * kD + ch;
+      const size_t oi = ((size_t)(b0 + rr) * H + h) * kD + ch;
       if (a.out_fp32) reinterpret_cast<float*>(a.out)[oi] = val;
       else reinterpret_cast<uint16_t*>(a.out)[oi] = f32_to_bf16(val);
     }
@@ -533,10 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a
   }
 
   // ---- split partial, then the last block of this (pair, head) merges -------------------
-  if (!half && rr < nreq) {
-    const int b = b0 + rr;
-    float* pp = a.part + (((size_t)b * H + h) * a.n_split + split) * (kD + 2);
-    pp[2 + ch] = o + comb[rr * kD + ch] + ow[rr * kD + ch];
+  if (tid < 2 * kD && rr < nreq) {
+    float* pp = a.part + (((size_t)(b0 + rr) * H + h) * a.n_split + split) * (kD + 2);
+    pp[2 + ch] = o;
     if (ch == 0) {
       pp[0] = Mr;
       pp[1] = Lr;
@@ -551,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a
   __syncthreads();
   if (!sflag[0]) return;
   __threadfence();
-  if (!half && rr < nreq) {
+  if (tid < 2 * kD && rr < nreq) {
     const int b = b0 + rr;
     const float* pp = a.part + ((size_t)b * H + h) * a.n_split * (kD + 2);
     float Mx = -INFINITY;
@@ -576,23 +595,16 @@ __global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a
 
 }  // namespace
 
-int vq_attn_max_pages_per_split(int win_slots) {
-  const int per_req = (kSmemLimit - kOffScores) / (2 * 4);
-  return (per_req - win_slots) / kPage;
-}
+int vq_attn_max_pages_per_split(int) { return 1 << 20; }  // one pass: no per-split storage
 
-size_t vq_attn_smem_bytes(int pages_per_split, int win_slots) {
-  return kOffScores + (size_t)2 * 4 * (pages_per_split * kPage + win_slots);
-}
+size_t vq_attn_smem_bytes(int, int) { return kSmemBytes; }
 
 cudaError_t launch_vq_attn(const VqAttnArgs& a, cudaStream_t st) {
-  const int sc_stride = a.pages_per_split * kPage + a.win_slots;
-  const size_t smem = vq_attn_smem_bytes(a.pages_per_split, a.win_slots);
-  cudaError_t e = cudaFuncSetAttribute(vq_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(vq_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)kD);
   dim3 grid(a.n_split, (a.B + 1) / 2, a.H);
-  vq_attn_kernel<<<grid, kThreads, smem, st>>>(a, scale_log2, sc_stride);
+  vq_attn_kernel<<<grid, kThreads, kSmemBytes, st>>>(a, scale_log2);
   return cudaGetLastError();
 }
 

@@ -36,18 +36,20 @@ __global__ void rope_table_kernel(float* cos_t, float* sin_t, int max_ctx, int D
 }
 
 // ---------------------------------------------------------------- B_t slices
-// bt[l][t][h][r][g*c + i] = cb[l][beta][h][g][r][i*Tc + m]
+// bt[l][t][h][ch / 64][r][ch % 64] = cb[l][beta][h][g][r][i*Tc + m], ch = g*c + i
 __global__ void slice_kernel(const float* __restrict__ cb, float* __restrict__ bt, int L, int T, int Tc,
                              int G, int H) {
   const int c = G / Tc, NG = kD / c, NB = T / Tc;
   const long long n = (long long)L * T * H * kCB * kD;
   for (long long k = blockIdx.x * (long long)blockDim.x + threadIdx.x; k < n; k += (long long)gridDim.x * blockDim.x) {
     long long q = k;
-    const int ch = (int)(q % kD); q /= kD;
+    const int col = (int)(q % (kD / 2)); q /= (kD / 2);
     const int r = (int)(q % kCB); q /= kCB;
+    const int half = (int)(q % 2); q /= 2;
     const int h = (int)(q % H); q /= H;
     const int t0 = (int)(q % T); q /= T;  // 0-based step
     const int l = (int)q;
+    const int ch = half * (kD / 2) + col;
     const int beta = t0 / Tc, m = t0 % Tc, g = ch / c, i = ch % c;
     bt[k] = cb[((((size_t)l * NB + beta) * H + h) * NG + g) * (size_t)kCB * G + (size_t)r * G + i * Tc + m];
   }

@@ -205,7 +205,7 @@ class VqCache:
         self.idx_v = torch.zeros_like(self.idx_k)
         self.win_k = torch.zeros((L, c.T, B, H, c.win_slots, c.D), dtype=torch.bfloat16, device=dev)
         self.win_v = torch.zeros_like(self.win_k)
-        self.bt_k = torch.zeros((L, c.T, H, c.K, c.D), dtype=torch.float32, device=dev)
+        self.bt_k = torch.zeros((L, c.T, H, 2, c.K, c.D // 2), dtype=torch.float32, device=dev)
         self.bt_v = torch.zeros_like(self.bt_k)
         self.cb_k = torch.zeros((L, NB, H, c.NG, c.K, c.G), dtype=torch.float32, device=dev)
         self.cb_v = torch.zeros_like(self.cb_k)

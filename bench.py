@@ -279,7 +279,33 @@ def kivi_call_bytes(B, H, NQ, NR):
     return codes + ksz + vsz + res + qo
 
 
-def time_region(fn, steps, stream, dist):
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch from an ncu capture,
+# valid only for the kernel source it was taken on (profiles/ holds the capture summary)
+PROFILED_TRAFFIC = {
+    "vq_attn_kernel": ("sub_bit_quantized_gb300/csrc/vq_attn.cu",
+                       "9e910cd57d5faf028a3fd8ec3a160f7d712d48f834152d31620f156237467a3c", 245971200),
+}
+
+
+def profiled_traffic(kernel):
+    """Per-launch DRAM bytes of ``kernel`` if its source is unchanged since the capture, else None."""
+    import hashlib
+    entry = PROFILED_TRAFFIC.get(kernel)
+    if entry is None:
+        return None
+    path, digest, nbytes = entry
+    try:
+        with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), path), "rb") as f:
+            ok = hashlib.sha256(f.read()).hexdigest() == digest
+    except OSError:
+        return None
+    return nbytes if ok else None
+
+
+def time_region(fn, steps, stream, dist, nvtx_name=None):
+    """Device time of ``steps`` calls of ``fn`` (CUDA events on ``stream``), max over ranks.
+    ``nvtx_name`` marks the launches with an NVTX range so that a profiler can be limited to
+    them (ncu --nvtx --nvtx-include "<name>/")."""
     import torch
     if dist:
         torch.distributed.barrier()
@@ -287,8 +313,12 @@ def time_region(fn, steps, stream, dist):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    if nvtx_name:
+        torch.cuda.nvtx.range_push(nvtx_name)
     for _ in range(steps):
         fn()
+    if nvtx_name:
+        torch.cuda.nvtx.range_pop()
     e1.record(stream)
     e1.synchronize()
     torch.cuda.synchronize()
@@ -341,7 +371,7 @@ def run_ours(args, wl, rank, world, dist, pool):
         torch.cuda.synchronize()
         assert kvq.device_error() == 0
         with ClockSampler(gpu_index) as cs:
-            ms = time_region(step, args.steps, stream, dist)
+            ms = time_region(step, args.steps, stream, dist, nvtx_name="timed")
         clocks = cs.summary()
         ms_step = ms / args.steps
         step_bytes = call_bytes * n_calls
@@ -371,17 +401,20 @@ def run_ours(args, wl, rank, world, dist, pool):
                            tokens_per_s=round(B * world / (ms_step * 1e-3), 1), e2e=e2e, clocks=clocks,
                            roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                                     "traffic": None, "peak_source": peak_src,
+                                     "traffic": profiled_traffic("vq_attn_kernel" if wl["kind"] == "loopvq"
+                                                                 else "kivi_attn_kernel"),
+                                     "peak_source": peak_src,
                                      "kernel": "vq_attn_kernel" if wl["kind"] == "loopvq" else "kivi_attn_kernel",
                                      "bytes_per_launch": call_bytes},
                            n_splits=n_splits))
         if rank == 0 and not args.no_cpu_baseline:
-            n_pairs = 256 if wl["kind"] == "loopvq" else 128
+            # eight calls' worth of (request, head) units: about 10 s on 16 host cores
+            n_pairs = 8 * B * H
             unit_bytes = call_bytes / (B * H)
             cgbs, cores, wall = cpu_oracle(wl, unit_bytes, B * H, n_pairs, pool)
             result["cpu_baseline"] = {"value": round(cgbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                      "sample": f"{n_pairs} (request, head) units of one call, fp64 NumPy oracle, "
-                                                f"{wall:.1f} s wall on {cores} processes"}
+                                      "sample": f"{n_pairs} (request, head) units (8 calls' worth), fp64 NumPy "
+                                                f"oracle, {wall:.1f} s wall on {cores} processes"}
         return result
 
     if wl["kind"] == "encode":

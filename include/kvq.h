@@ -252,10 +252,16 @@ kvq_status kvq_quantize_kivi(const kvq_kivi_cfg* cfg, int axis, const uint16_t* 
  * format KVQ_FMT_KIVI: cfg is kvq_kivi_cfg*, cache kvq_kivi_cache*; layer and loop_step
  *   are ignored; no RoPE (KIVI caches post-RoPE keys).
  * out: [B][n_heads][D], bf16 (KVQ_OUT_BF16) or fp32 (KVQ_OUT_FP32).
- * n_splits: quantized-page splits per (request, head); 0 picks one for the GPU.
+ * n_splits: how the quantized pages are split, 0 picks for the GPU.
+ *   LoopVQ: thread blocks of the page kernel. The units (head, request pair, 32 index
+ *   pages), head-major, are cut into n_splits equal contiguous shares, one per block; each
+ *   block writes a partial softmax for every piece of a (request, head) it covers and a
+ *   second kernel merges them with the bf16 window tokens. 0 = one block per SM.
+ *   KIVI: token splits per (request, head), merged by the last block of each.
  * ws: device workspace of at least kvq_decode_workspace_size() bytes (may be NULL when
- *   that size is 0). Its first use needs it zero-filled; every call leaves it reusable.
- *   Two calls that run at the same time need two workspaces.
+ *   that size is 0; LoopVQ always needs one). A KIVI workspace must be zero-filled before
+ *   its first use; every call leaves it reusable. Two calls that run at the same time need
+ *   two workspaces.
  * Errors: KVQ_ERR_WORKSPACE, KVQ_ERR_CAPACITY (B > max_batch). */
 kvq_status kvq_decode_attn(int format, const void* cfg, const void* cache, int layer,
                            int loop_step, const uint16_t* q, int B, void* out, int out_dtype,
@@ -284,7 +290,7 @@ kvq_status kvq_decode_attn_noalloc(int format, const void* cfg, const void* cach
 /* Workspace bytes kvq_decode_attn needs for these arguments (0 if none). */
 size_t kvq_decode_workspace_size(int format, const void* cfg, int B, int n_splits);
 
-/* The split count kvq_decode_attn uses when n_splits = 0. */
+/* The split count kvq_decode_attn uses when n_splits = 0 (LoopVQ: the number of SMs). */
 int kvq_decode_auto_splits(int format, const void* cfg, int B);
 
 /* ---------------------------------------------------------------------------------- */

@@ -84,47 +84,13 @@ kvq_status check_vq_cfg(const kvq_vq_cfg* c, const char* fn) {
 
 int win_slots(const kvq_vq_cfg* c) { return c->sink + c->recent + kvq::kPage; }
 
-struct VqPlan {
-  int n_split, pps;
-};
-
-// Choose the page split: fill whole waves of blocks, keep each block's staging cost
-// (two 128 KB codebook slices) small against its share of pages.
-VqPlan plan_vq(const kvq_vq_cfg* c, int B, int n_splits) {
-  const int pmax = kvq::vq_attn_max_pages_per_split(win_slots(c));
-  const int pairs = (B + 1) / 2;
-  VqPlan p{1, c->max_pages};
-  if (n_splits > 0) {
-    p.n_split = n_splits;
-    p.pps = (c->max_pages + n_splits - 1) / n_splits;
-    return p;
-  }
-  if (c->max_pages == 0) return VqPlan{1, 0};
-  const int sms = sm_count();
-  const double overhead = 48.0;  // staging cost in page-equivalents per block
-  double best = 1e300;
-  const int n_lo = std::max(1, (c->max_pages + pmax - 1) / pmax);
-  const int n_hi = std::max(n_lo, std::min(64, c->max_pages));
-  for (int n = n_lo; n <= n_hi; ++n) {
-    const int pps = (c->max_pages + n - 1) / n;
-    const long long blocks = (long long)pairs * c->n_heads * n;
-    const long long waves = (blocks + sms - 1) / sms;
-    const double cost = (double)waves * (pps + overhead + (n > 1 ? 4.0 : 0.0));
-    if (cost < best * 0.999) {
-      best = cost;
-      p = VqPlan{n, pps};
-    }
-  }
-  return p;
-}
+// Blocks of the LoopVQ page kernel: one per SM unless the caller names a count (every block
+// takes an equal contiguous share of the units, so any count is correct).
+int plan_vq_blocks(int n_splits) { return n_splits > 0 ? n_splits : sm_count(); }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-size_t vq_ws_bytes(const kvq_vq_cfg* c, int B, const VqPlan& p) {
-  if (p.n_split <= 1) return 0;
-  return align256((size_t)B * c->n_heads * p.n_split * (kvq::kD + 2) * sizeof(float)) +
-         align256((size_t)((B + 1) / 2) * c->n_heads * sizeof(int));
-}
+size_t vq_ws_bytes(const kvq_vq_cfg* c, int B, int blocks) { return kvq::vq_attn_ws_bytes(B, c->n_heads, blocks); }
 
 // ---- KIVI config -----------------------------------------------------------------------
 kvq_status check_kivi_cfg(const kvq_kivi_cfg* c, const char* fn) {
@@ -397,7 +363,7 @@ KVQ_API size_t kvq_decode_workspace_size(int format, const void* cfg, int B, int
   if (format == KVQ_FMT_LOOPVQ) {
     const kvq_vq_cfg* c = static_cast<const kvq_vq_cfg*>(cfg);
     if (check_vq_cfg(c, __func__) != KVQ_OK) return 0;
-    return vq_ws_bytes(c, B, plan_vq(c, B, n_splits));
+    return vq_ws_bytes(c, B, plan_vq_blocks(n_splits));
   }
   if (format == KVQ_FMT_KIVI) {
     const kvq_kivi_cfg* c = static_cast<const kvq_kivi_cfg*>(cfg);
@@ -412,7 +378,7 @@ KVQ_API int kvq_decode_auto_splits(int format, const void* cfg, int B) {
   if (format == KVQ_FMT_LOOPVQ) {
     const kvq_vq_cfg* c = static_cast<const kvq_vq_cfg*>(cfg);
     if (check_vq_cfg(c, __func__) != KVQ_OK) return 0;
-    return plan_vq(c, B, 0).n_split;
+    return plan_vq_blocks(0);
   }
   if (format == KVQ_FMT_KIVI) {
     const kvq_kivi_cfg* c = static_cast<const kvq_kivi_cfg*>(cfg);
@@ -440,12 +406,13 @@ KVQ_API kvq_status kvq_decode_attn(int format, const void* cfg, const void* cach
     if (layer < 0 || layer >= c->n_layers || loop_step < 1 || loop_step > c->T || B < 1)
       return fail(KVQ_ERR_INVALID_ARG, "%s: layer/loop_step/B out of range", __func__);
     if (B > c->max_batch) return fail(KVQ_ERR_CAPACITY, "%s: B=%d > max_batch=%d", __func__, B, c->max_batch);
-    const VqPlan p = plan_vq(c, B, n_splits);
-    if (p.pps > kvq::vq_attn_max_pages_per_split(win_slots(c)))
-      return fail(KVQ_ERR_UNSUPPORTED, "%s: %d pages per split exceed the shared-memory limit of %d; use more splits",
-                  __func__, p.pps, kvq::vq_attn_max_pages_per_split(win_slots(c)));
-    const size_t need = vq_ws_bytes(c, B, p);
-    if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws)))
+    if ((B + 1) / 2 > kvq::vq_attn_max_pairs())
+      return fail(KVQ_ERR_UNSUPPORTED, "%s: B=%d exceeds %d requests", __func__, B, 2 * kvq::vq_attn_max_pairs());
+    const long long units = (long long)c->n_heads * ((B + 1) / 2) * ((c->max_pages + kvq::kVqChunk - 1) / kvq::kVqChunk);
+    if (units >= (1ll << 31)) return fail(KVQ_ERR_UNSUPPORTED, "%s: too many page units for one call", __func__);
+    const int blocks = plan_vq_blocks(n_splits);
+    const size_t need = vq_ws_bytes(c, B, blocks);
+    if (!ws || ws_bytes < need || !aligned16(ws))
       return fail(KVQ_ERR_WORKSPACE, "%s: workspace needs %zu bytes (got %zu)", __func__, need, ws_bytes);
     const int NB = c->T / c->Tc, NG = c->D / (c->G / c->Tc);
     const int beta = (loop_step - 1) / c->Tc;
@@ -463,15 +430,10 @@ KVQ_API kvq_status kvq_decode_attn(int format, const void* cfg, const void* cach
     a.rope_cos = k->rope_cos; a.rope_sin = k->rope_sin;
     a.seq_len = k->seq_len; a.n_pages = k->n_pages;
     a.q = q; a.out = out; a.out_fp32 = (out_dtype == KVQ_OUT_FP32);
-    if (p.n_split > 1) {
-      a.part = static_cast<float*>(ws);
-      a.counters = reinterpret_cast<int*>(static_cast<char*>(ws) +
-                                          align256((size_t)B * c->n_heads * p.n_split * (kvq::kD + 2) * sizeof(float)));
-    }
     a.err = device_error_ptr();
     a.B = B; a.H = c->n_heads; a.max_pages = c->max_pages; a.max_ctx = c->max_ctx; a.sink = c->sink;
-    a.recent = c->recent; a.win_slots = win_slots(c); a.n_split = p.n_split; a.pages_per_split = p.pps;
-    return cuda_status(kvq::launch_vq_attn(a, s), __func__);
+    a.recent = c->recent; a.win_slots = win_slots(c); a.G = blocks;
+    return cuda_status(kvq::launch_vq_attn(a, ws, s), __func__);
   }
   if (format == KVQ_FMT_KIVI) {
     const kvq_kivi_cfg* c = static_cast<const kvq_kivi_cfg*>(cfg);

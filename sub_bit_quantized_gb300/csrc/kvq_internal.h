@@ -18,6 +18,16 @@ constexpr int kCB = 256;       // codebook entries
 constexpr int kPageBytes = kPage * kNG;
 
 // ---------------------------------------------------------------- LoopVQ decode attention
+// Two launches per call. The page kernel runs G persistent blocks over the work units
+// (head, request pair, chunk of 32 index pages), head-major; block k takes the contiguous
+// units [k U / G, (k + 1) U / G). It writes one partial softmax (M, l, o[128]) per request
+// for every piece of a (pair, head) segment it covers: to part_whole[seg] when the whole
+// segment lies in its share, else to part_slot[k][0] (the piece holding the block's first
+// unit) or part_slot[k][1] (the piece holding its last). The window kernel attends the bf16
+// sink/recent tokens of every (request, head) and merges them with the pieces.
+constexpr int kVqChunk = 32;   // index pages of each request per work unit
+constexpr int kVqPartFloats = 2 * (kD + 2);  // one piece: [request][M, l, o[128]]
+
 struct VqAttnArgs {
   const uint8_t* idx_k;      // [max_batch][H][max_pages][128] of (layer, block)
   const uint8_t* idx_v;
@@ -32,15 +42,16 @@ struct VqAttnArgs {
   const uint16_t* q;         // [B][H][D] bf16
   void* out;                 // [B][H][D]
   int out_fp32;
-  float* part;               // [B][H][n_split][D + 2] partials (n_split > 1)
-  int* counters;             // [ceil(B/2)][H] arrival counters (n_split > 1)
+  int32_t* pref;             // [n_pairs + 1] unit prefix over pairs (written by page block 0)
+  float* part_whole;         // [H * n_pairs][kVqPartFloats]
+  float* part_slot;          // [G][2][kVqPartFloats]
   int* err;
   int B, H, max_pages, max_ctx, sink, recent, win_slots;
-  int n_split, pages_per_split;
+  int G;                     // page-kernel blocks
 };
-size_t vq_attn_smem_bytes(int pages_per_split, int win_slots);
-int vq_attn_max_pages_per_split(int win_slots);
-cudaError_t launch_vq_attn(const VqAttnArgs& a, cudaStream_t s);
+size_t vq_attn_ws_bytes(int B, int H, int G);
+int vq_attn_max_pairs();
+cudaError_t launch_vq_attn(const VqAttnArgs& a, void* ws, cudaStream_t s);
 
 // ---------------------------------------------------------------- LoopVQ encode and friends
 struct VqEncodeArgs {

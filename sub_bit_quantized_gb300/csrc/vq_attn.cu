@@ -1,35 +1,44 @@
 // LoopVQ decode attention over the bf16 window and the 8-token index pages of one
-// (layer, loop step), split-K over pages with an exact logsumexp merge.
+// (layer, loop step), with an exact logsumexp merge of partial softmaxes.
 //
 // Follows "LoopVQ: Sub 1-bit KV Cache Quantization for Looped Transformers", method
 // step 5, Algorithm 1 and Figure 5: the step's codebook slice B_t is staged in shared
-// memory once per thread block, keys and values are rebuilt from D/c = 16 indices per
-// token, keys are rotated by RoPE and dotted with the query, the bf16 sink/recent tokens are
-// attended directly, and the partials of every split are merged exactly. Two requests of
-// the same head share a thread block and its B_t load.
+// memory, keys and values are rebuilt from D/c = 16 indices per token, keys are rotated by
+// RoPE and dotted with the query, the bf16 sink/recent tokens are attended directly, and
+// the partial results are merged exactly (the Flash-Decoding merge the page builds on).
 //
-// GB300 design (differs from the page's Triton kernel). On this GPU each codeword lookup
-// costs shared-memory bandwidth (32 B per fp32 group), and that, not HBM, bounds the
-// kernel; the structure keeps every lookup a conflict-free 128-bit shared load and moves
-// no other data through shared memory per token:
+// GB300 design (differs from the page's Triton kernel, which gives every (request, head,
+// split) its own program). On this GPU a codeword lookup costs shared-memory bandwidth and
+// every key 6 FMAs per channel pair, so the work is bound on chip, not by HBM. Two kernels:
+//
+// vq_pages_kernel: persistent, one 512-thread block per SM. The work units (head, request
+// pair, chunk of 32 index pages), head-major, are cut into G equal contiguous shares, one
+// per block, so every SM gets the same number of pages whatever the batch mix, and a block
+// restages the codebook slices only when its share crosses into the next head (at most
+// twice for the usual shapes).
 //  * Both slices stay resident: keys in fp32 (128 KB, TMA bulk copy; channels 0..63 and
 //    64..127 as two [256][64] tables), values in fp16 ([256][128], converted while
 //    staging; value rounding error ~1e-4 of the output). A codeword's shared-memory address
-//    is one byte permute: (index << 8) | lane offset.
-//  * Index pages stream through a 2-stage shared-memory ring (32 key and 32 value pages of
-//    each request per stage) filled by TMA bulk copies with full/empty mbarriers. Every
-//    wait is bounded and reports a timeout through the device error word.
+//    is one byte permute: (index << 8) | lane offset, and every lookup is a 128-bit load.
+//  * Thread 0 streams the units through a 2-stage ring with TMA bulk copies: 32 key and 32
+//    value pages of each request, the two bf16 queries and a header naming the unit. Full
+//    and empty mbarriers; every wait is bounded and reports a timeout through the device
+//    error word instead of hanging.
 //  * 8 lanes per page, lane s owns the RoPE partner groups s and s+8 (channels 8s..8s+7 and
 //    64+8s..64+8s+7). The rotated query u = R(p_q - p) q satisfies <R(p_q) q, R(p) k> =
 //    <u, k>, so keys are never rotated: u is built from the cos/sin table at a lane-group's
-//    first page, advanced one position per token by R(-theta) and one chunk (256
-//    positions) by R(-256 theta), and re-read from the table every 16 chunks. Packed fp32x2
-//    FMAs. A transposing shuffle reduction leaves lane s with the score of token s.
-//  * One pass with an online softmax per lane-group (running max, rescale on increase):
-//    the 8 softmax weights of a page are broadcast by shuffles and each lane accumulates
-//    its 16 value channels directly from the fp16 value table.
-//  * Lane-groups merge in registers (shuffles), warps through shared memory, splits in the
-//    last block of a (request pair, head) to finish (arrival counter, no spin-wait).
+//    first page of a piece, advanced one position per token by R(-theta) and one unit (256
+//    positions) by R(-256 theta), and re-read from the table every 16 units. A transposing
+//    shuffle reduction leaves lane s with the score of token s.
+//  * One pass with an online softmax per lane-group; the 8 weights of a page are broadcast
+//    by shuffles and each lane accumulates its 16 value channels from the fp16 table.
+//  * At the end of each piece of a (pair, head) segment the lane-groups merge (shuffles,
+//    then warps through the stage's shared memory) and the block writes the piece's partial
+//    (M, l, o) per request to the workspace.
+//
+// vq_window_kernel: one 128-thread block per (request, head) attends the bf16 sink and
+// recent tokens (one token per lane-group step, online softmax) and merges the result with
+// every page piece of its segment, found from the same share arithmetic.
 #include <cuda_fp16.h>
 
 #include "kvq_common.cuh"
@@ -41,25 +50,29 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kLaneGroups = kThreads / 8;
-constexpr int kChunk = 32;                                // pages of each request per ring stage
+constexpr int kChunk = kVqChunk;                          // pages of each request per unit
 constexpr int kStages = 2;
-constexpr int kResync = 16;                               // chunks between cos/sin table reloads
+constexpr int kResync = 16;                               // units between cos/sin table reloads
+constexpr int kJump = kChunk * kPage;                     // positions between a lane-group's pages
 constexpr uint32_t kKSliceBytes = kCB * kD * 4;           // fp32 key codebook slice
 constexpr uint32_t kVSliceBytes = kCB * kD * 2;           // fp16 value codebook slice
 constexpr uint32_t kPart = kChunk * kPageBytes;           // 4 KB: one request's pages of one kind
-constexpr uint32_t kStageBytes = 4 * kPart;               // [K r0 | K r1 | V r0 | V r1]
+constexpr uint32_t kOffHdr = 4 * kPart;                   // unit header within a stage
+constexpr uint32_t kOffQs = kOffHdr + 64;                 // bf16 queries [2][128] within a stage
+constexpr uint32_t kStageBytes = kOffQs + 2 * kD * 2 + 64;  // [K r0|K r1|V r0|V r1|hdr|q r0|q r1]
 
 // shared-memory layout (bytes)
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kKSliceBytes;
 constexpr int kOffRing = kOffV + kVSliceBytes;
-constexpr int kOffQ = kOffRing + kStages * kStageBytes;    // float [2][128]
-constexpr int kOffJ = kOffQ + 2 * kD * 4;                  // float [8 slots][16]: cos, sin(256 theta)
-constexpr int kOffBar = kOffJ + 8 * 16 * 4;                // mbarriers + flags
+constexpr int kOffJ = kOffRing + kStages * kStageBytes;   // float [8 slots][16]: cos, sin(256 theta)
+constexpr int kOffProd = kOffJ + 8 * 16 * 4;              // producer state (thread 0)
+constexpr int kOffBar = kOffProd + 64;                    // mbarriers + flags
 constexpr int kSmemBytes = kOffBar + 128;
 static_assert(kSmemBytes <= 232448, "shared memory");
-static_assert(kOffBar % 8 == 0 && kOffRing % 128 == 0, "alignment");
+static_assert(kOffBar % 8 == 0 && kOffRing % 128 == 0 && kStageBytes % 128 == 0, "alignment");
+static_assert(kWarps * (kD + 2) * 4 <= (int)kOffHdr, "piece merge scratch fits in a stage");
+constexpr int kMaxPairs = (int)(kVSliceBytes / 4) - 1;    // unit scan runs in the value-slice area
 
 __device__ __forceinline__ void ldg8_perm(const float* p, int o0, float (&v)[8]) {
   const float4 a = __ldg(reinterpret_cast<const float4*>(p + o0));
@@ -146,8 +159,33 @@ __device__ __forceinline__ void rotated_query(const float* rc, const float* rs, 
   }
 }
 
-// A timed-out wait marks the block as failed; every later wait then returns at once so
-// that all threads reach the same barriers and leave together.
+// 8 consecutive bf16 values from shared memory in the lane's half order
+__device__ __forceinline__ void lds8_bf16_perm(const uint16_t* p, int o0, float (&v)[8]) {
+  const uint2 a = *reinterpret_cast<const uint2*>(p + o0);
+  const uint2 b = *reinterpret_cast<const uint2*>(p + (4 - o0));
+  v[0] = bf16_lo(a.x); v[1] = bf16_hi(a.x); v[2] = bf16_lo(a.y); v[3] = bf16_hi(a.y);
+  v[4] = bf16_lo(b.x); v[5] = bf16_hi(b.x); v[6] = bf16_lo(b.y); v[7] = bf16_hi(b.y);
+}
+
+// rotated query u = R(d) q from a bf16 query in shared memory (lane half order)
+__device__ __forceinline__ void rotated_query_bf16(const float* rc, const float* rs, int d, int s, int o0,
+                                                   const uint16_t* q, float2 (&ul)[4], float2 (&uh)[4]) {
+  float c8[8], s8[8], ql[8], qh[8];
+  ldg8_perm(rc + (size_t)d * (kD / 2) + 8 * s, o0, c8);
+  ldg8_perm(rs + (size_t)d * (kD / 2) + 8 * s, o0, s8);
+  lds8_bf16_perm(q + 8 * s, o0, ql);
+  lds8_bf16_perm(q + 64 + 8 * s, o0, qh);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    ul[k] = make_float2(ql[2 * k] * c8[2 * k] - qh[2 * k] * s8[2 * k],
+                        ql[2 * k + 1] * c8[2 * k + 1] - qh[2 * k + 1] * s8[2 * k + 1]);
+    uh[k] = make_float2(qh[2 * k] * c8[2 * k] + ql[2 * k] * s8[2 * k],
+                        qh[2 * k + 1] * c8[2 * k + 1] + ql[2 * k + 1] * s8[2 * k + 1]);
+  }
+}
+
+// A timed-out wait marks the block as failed; every later wait then returns at once, so a
+// block that lost a copy finishes (with the error word set) instead of hanging.
 __device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, volatile int* failed, int* err) {
   if (*failed) return false;
   if (mbar_wait_bounded(bar, parity)) return true;
@@ -156,11 +194,30 @@ __device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, volat
   return false;
 }
 
+// Block-wide barrier on an mbarrier that every thread arrives on, with a bounded wait. Used
+// inside the unit loop instead of __syncthreads so that a failed wait elsewhere can never
+// leave threads parked at a barrier.
+__device__ __forceinline__ void block_sync(uint64_t* bar, uint32_t& phase, volatile int* failed, int* err) {
+  mbar_arrive(bar);
+  wait_stage(bar, phase, failed, err);
+  phase ^= 1u;
+}
+
 // running softmax state of one lane (the max is shared by its lane-group)
 struct Acc {
   float M, l;
   float2 ol[4], oh[4];
 };
+
+__device__ __forceinline__ void acc_reset(Acc& A) {
+  A.M = -INFINITY;
+  A.l = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    A.ol[k] = make_float2(0.f, 0.f);
+    A.oh[k] = make_float2(0.f, 0.f);
+  }
+}
 
 // Fold the 8 scores of a page (lane s holds token s; -inf for a missing token) into the
 // running state: raise the shared max if needed (rescaling the sums), return this lane's
@@ -186,309 +243,9 @@ __device__ __forceinline__ float online_weights(Acc& A, float sc, unsigned mask)
   return p;
 }
 
-struct Req {
-  int L, NP, pend, nsink, nwin;
-};
-
-__global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a, const float scale_log2) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  float* ks = reinterpret_cast<float*>(smem + kOffK);
-  __half* vs = reinterpret_cast<__half*>(smem + kOffV);
-  unsigned char* ring = smem + kOffRing;
-  float* qs = reinterpret_cast<float*>(smem + kOffQ);
-  uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* full = kbar + 1;
-  uint64_t* empty = full + kStages;
-  int* sflag = reinterpret_cast<int*>(empty + kStages);  // [0] merge, [1] failed
-  volatile int* failed = sflag + 1;
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int split = blockIdx.x, pair = blockIdx.y, h = blockIdx.z;
-  const int H = a.H;
-  const int b0 = pair * 2;
-  const int nreq = min(2, a.B - b0);
-
-  // ---- lengths of the two requests; pages of this split -------------------------------
-  Req rq[2];
-  const int pg0 = split * a.pages_per_split;
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    int L = 0, NP = 0;
-    if (r < nreq) {
-      L = a.seq_len[b0 + r];
-      NP = a.n_pages[b0 + r];
-      // lengths that do not describe a valid cache are reported and attended as empty
-      const bool bad = L < 0 || L > a.max_ctx || NP < 0 || NP > a.max_pages ||
-                       (NP > 0 && a.sink + kPage * NP > L) || L - a.sink - kPage * NP > a.recent + kPage;
-      if (bad) {
-        if (split == 0 && tid == 0) set_error(a.err, KVQ_ERR_CAPACITY);
-        L = 0;
-        NP = 0;
-      }
-    }
-    rq[r].L = L;
-    rq[r].NP = NP;
-    rq[r].pend = min(NP, pg0 + a.pages_per_split);
-    rq[r].nsink = min(a.sink, L);
-    rq[r].nwin = (split == 0 && L > 0) ? (rq[r].nsink + max(0, L - a.sink - kPage * NP)) : 0;
-  }
-  const int n_items = max(max(0, rq[0].pend - pg0), max(0, rq[1].pend - pg0));
-  const int n_chunks = (n_items + kChunk - 1) / kChunk;
-  const size_t bh0 = ((size_t)b0 * H + h) * (size_t)a.max_pages * kPageBytes;
-  const size_t bh1 = ((size_t)(b0 + (nreq > 1 ? 1 : 0)) * H + h) * (size_t)a.max_pages * kPageBytes;
-
-  // producer (thread 0): key and value pages of chunk c into ring stage c % kStages
-  auto produce = [&](int c) {
-    const int st = c % kStages;
-    const int p_first = pg0 + c * kChunk;
-    const int n0 = min(kChunk, max(0, rq[0].pend - p_first));
-    const int n1 = min(kChunk, max(0, rq[1].pend - p_first));
-    mbar_arrive_expect_tx(&full[st], (uint32_t)(n0 + n1) * 2 * kPageBytes);
-    unsigned char* dst = ring + st * kStageBytes;
-    const size_t off = (size_t)p_first * kPageBytes;
-    if (n0 > 0) {
-      bulk_g2s(dst, a.idx_k + bh0 + off, n0 * kPageBytes, &full[st]);
-      bulk_g2s(dst + 2 * kPart, a.idx_v + bh0 + off, n0 * kPageBytes, &full[st]);
-    }
-    if (n1 > 0) {
-      bulk_g2s(dst + kPart, a.idx_k + bh1 + off, n1 * kPageBytes, &full[st]);
-      bulk_g2s(dst + 3 * kPart, a.idx_v + bh1 + off, n1 * kPageBytes, &full[st]);
-    }
-  };
-
-  if (tid == 0) {
-    mbar_init(kbar, 1);
-#pragma unroll
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kWarps);
-    }
-    sflag[0] = 0;
-    sflag[1] = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (tid == 0 && n_items > 0) {
-    const float* btk = a.bt_k + (size_t)h * kCB * kD;
-    mbar_arrive_expect_tx(kbar, kKSliceBytes);
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      bulk_g2s(ks + k * (kKSliceBytes / 16), btk + k * (kKSliceBytes / 16), kKSliceBytes / 4, kbar);
-    for (int c = 0; c < min(kStages, n_chunks); ++c) produce(c);
-  }
-  if (n_items > 0) {  // value slice: fp32 [2][256][64] in L2 -> fp16 [256][128] in shared memory
-    const float4* src = reinterpret_cast<const float4*>(a.bt_v + (size_t)h * kCB * kD);
-    for (int i = tid; i < kCB * kD / 4; i += kThreads) {
-      const float4 v = __ldg(src + i);
-      const int half = i / (kCB * kD / 8), rem = i % (kCB * kD / 8);
-      const int row = rem / (kD / 8), c4 = rem % (kD / 8);
-      __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
-      uint2 w;
-      w.x = *reinterpret_cast<uint32_t*>(&lo);
-      w.y = *reinterpret_cast<uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(vs + row * kD + half * (kD / 2))[c4] = w;
-    }
-  }
-  if (tid < 2 * kD) {
-    const int r = tid >> 7;
-    qs[tid] = bf16_to_f32(a.q[((size_t)(b0 + min(r, nreq - 1)) * H + h) * kD + (tid & 127)]);
-  }
-  if (tid < 8 && n_chunks > 1) {  // cos/sin(256 theta_i) for slot tid, in that slot's half order
-    float* jt = reinterpret_cast<float*>(smem + kOffJ) + tid * 16;
-    const int jo0 = (tid & 4) ? 4 : 0;
-    float c8[8], s8[8];
-    ldg8_perm(a.rope_cos + (size_t)(kChunk * kPage) * (kD / 2) + 8 * tid, jo0, c8);
-    ldg8_perm(a.rope_sin + (size_t)(kChunk * kPage) * (kD / 2) + 8 * tid, jo0, s8);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      jt[k] = c8[k];
-      jt[8 + k] = s8[k];
-    }
-  }
-  __syncthreads();
-
-  const int s = tid & 7;                 // slot: groups s and s + 8
-  const int o0 = (s & 4) ? 4 : 0;        // key half order (bank-quad spreading)
-  const unsigned gmask = 0xFFu << (lane & 24);
-  const int lg = tid >> 3;
-  const int r = lg >> 5, po = lg & 31;   // this lane-group's request and page slot
-  const Req R = r ? rq[1] : rq[0];
-  const float* qr = qs + r * kD;
-
-  // value accumulators in natural channel order: ol = channels 8s..8s+7, oh = 64+8s..
-  Acc A;
-  A.M = -INFINITY;
-  A.l = 0.f;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    A.ol[k] = make_float2(0.f, 0.f);
-    A.oh[k] = make_float2(0.f, 0.f);
-  }
-  const uint16_t* wk = a.win_k + ((size_t)(b0 + r) * H + h) * a.win_slots * kD;
-  const uint16_t* wv = a.win_v + ((size_t)(b0 + r) * H + h) * a.win_slots * kD;
-
-  // ---- bf16 window (split 0): lane-group po takes window tokens [8 wp, 8 wp + 8) ----------
-  for (int wp = po; wp * kPage < R.nwin; wp += kLaneGroups / 2) {
-    float part[8];
-    int slots[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int w = wp * kPage + j;
-      part[j] = 0.f;
-      slots[j] = 0;
-      if (w < R.nwin) {
-        const int p = (w < R.nsink) ? w : a.sink + kPage * R.NP + (w - R.nsink);
-        const int slot = (p < a.sink) ? p : a.sink + (p - a.sink) % (a.recent + kPage);
-        slots[j] = slot;
-        float kl[8], kh[8];
-        ldg8_bf16_perm(wk + (size_t)slot * kD + 8 * s, o0, kl);
-        ldg8_bf16_perm(wk + (size_t)slot * kD + 64 + 8 * s, o0, kh);
-        float2 ul[4], uh[4];
-        rotated_query(a.rope_cos, a.rope_sin, R.L - 1 - p, s, o0, qr, ul, uh);
-        float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          acc = __ffma2_rn(ul[k], make_float2(kl[2 * k], kl[2 * k + 1]), acc);
-          acc = __ffma2_rn(uh[k], make_float2(kh[2 * k], kh[2 * k + 1]), acc);
-        }
-        part[j] = acc.x + acc.y;
-      }
-    }
-    transpose_reduce8(part, s, gmask);
-    const float sc = (wp * kPage + s < R.nwin) ? part[0] * scale_log2 : -INFINITY;
-    const float p = online_weights(A, sc, gmask);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float pj = __shfl_sync(gmask, p, (lane & 24) + j);
-      if (wp * kPage + j < R.nwin) {
-        float vl[8], vh[8];
-        ldg8_bf16_perm(wv + (size_t)slots[j] * kD + 8 * s, 0, vl);
-        ldg8_bf16_perm(wv + (size_t)slots[j] * kD + 64 + 8 * s, 0, vh);
-        const float2 p2 = make_float2(pj, pj);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          A.ol[k] = __ffma2_rn(p2, make_float2(vl[2 * k], vl[2 * k + 1]), A.ol[k]);
-          A.oh[k] = __ffma2_rn(p2, make_float2(vh[2 * k], vh[2 * k + 1]), A.oh[k]);
-        }
-      }
-    }
-  }
-
-  // ---- quantized pages -------------------------------------------------------------------
-  {
-    float2 cth[4], sth[4], nsth[4];
-    {
-      float c8[8], s8[8];
-      ldg8_perm(a.rope_cos + (kD / 2) + 8 * s, o0, c8);
-      ldg8_perm(a.rope_sin + (kD / 2) + 8 * s, o0, s8);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        cth[k] = make_float2(c8[2 * k], c8[2 * k + 1]);
-        sth[k] = make_float2(s8[2 * k], s8[2 * k + 1]);
-        nsth[k] = make_float2(-s8[2 * k], -s8[2 * k + 1]);
-      }
-    }
-    float2 u0l[4], u0h[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      u0l[k] = make_float2(0.f, 0.f);
-      u0h[k] = make_float2(0.f, 0.f);
-    }
-    // lane byte offsets inside a 256-byte table row: key halves swapped for s >= 4 so the 8
-    // lanes of a phase hit 8 bank quads; value lanes read 16 natural bytes each
-    const uint32_t kb0 = 32 * s + 4 * o0, kb1 = kb0 ^ 16u;
-    const uint32_t vb0 = 16 * s, vb1 = 128 + 16 * s;
-    const unsigned char* ksb = reinterpret_cast<const unsigned char*>(ks);
-    const unsigned char* vsb = reinterpret_cast<const unsigned char*>(vs);
-    const float* jt = reinterpret_cast<const float*>(smem + kOffJ) + s * 16;
-
-    if (n_items > 0) wait_stage(kbar, 0, failed, a.err);
-    for (int c = 0; c < n_chunks; ++c) {
-      const int st = c % kStages;
-      wait_stage(&full[st], (c / kStages) & 1, failed, a.err);
-      const int pg = pg0 + c * kChunk + po;
-      if (!*failed && pg < R.pend) {
-        if (c % kResync == 0) {
-          rotated_query(a.rope_cos, a.rope_sin, R.L - 1 - (a.sink + kPage * pg), s, o0, qr, u0l, u0h);
-        } else {  // 256 positions later
-          const float4 c0 = *reinterpret_cast<const float4*>(jt), c1 = *reinterpret_cast<const float4*>(jt + 4);
-          const float4 s0 = *reinterpret_cast<const float4*>(jt + 8), s1 = *reinterpret_cast<const float4*>(jt + 12);
-          const float2 cj[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w), make_float2(c1.x, c1.y),
-                                make_float2(c1.z, c1.w)};
-          const float2 sj[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
-                                make_float2(s1.z, s1.w)};
-          const float2 nsj[4] = {make_float2(-s0.x, -s0.y), make_float2(-s0.z, -s0.w), make_float2(-s1.x, -s1.y),
-                                 make_float2(-s1.z, -s1.w)};
-          rotate8(u0l, u0h, cj, sj, nsj);
-        }
-        const unsigned char* stage = ring + st * kStageBytes;
-        const uint4 rowk = *reinterpret_cast<const uint4*>(stage + r * kPart + po * kPageBytes + 16 * s);
-        float2 ul[4], uh[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          ul[k] = u0l[k];
-          uh[k] = u0h[k];
-        }
-        float part[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t wd = (j < 2) ? rowk.x : (j < 4) ? rowk.y : (j < 6) ? rowk.z : rowk.w;
-          uint32_t al0, al1, ah0, ah1;
-          if (j & 1) {
-            al0 = row_off<2>(wd, kb0); al1 = row_off<2>(wd, kb1);
-            ah0 = row_off<3>(wd, kb0); ah1 = row_off<3>(wd, kb1);
-          } else {
-            al0 = row_off<0>(wd, kb0); al1 = row_off<0>(wd, kb1);
-            ah0 = row_off<1>(wd, kb0); ah1 = row_off<1>(wd, kb1);
-          }
-          const float4 la = *reinterpret_cast<const float4*>(ksb + al0);
-          const float4 lb = *reinterpret_cast<const float4*>(ksb + al1);
-          const float4 ha = *reinterpret_cast<const float4*>(ksb + kKSliceBytes / 2 + ah0);
-          const float4 hb = *reinterpret_cast<const float4*>(ksb + kKSliceBytes / 2 + ah1);
-          float2 acc0 = __fmul2_rn(ul[0], make_float2(la.x, la.y));
-          float2 acc1 = __fmul2_rn(uh[0], make_float2(ha.x, ha.y));
-          acc0 = __ffma2_rn(ul[1], make_float2(la.z, la.w), acc0);
-          acc1 = __ffma2_rn(uh[1], make_float2(ha.z, ha.w), acc1);
-          acc0 = __ffma2_rn(ul[2], make_float2(lb.x, lb.y), acc0);
-          acc1 = __ffma2_rn(uh[2], make_float2(hb.x, hb.y), acc1);
-          acc0 = __ffma2_rn(ul[3], make_float2(lb.z, lb.w), acc0);
-          acc1 = __ffma2_rn(uh[3], make_float2(hb.z, hb.w), acc1);
-          const float2 acc = __fadd2_rn(acc0, acc1);
-          part[j] = acc.x + acc.y;
-          if (j < 7) rotate8(ul, uh, cth, sth, nsth);  // next token: one position later
-        }
-        transpose_reduce8(part, s, gmask);
-        const float p = online_weights(A, part[0] * scale_log2, gmask);
-        const uint4 rowv = *reinterpret_cast<const uint4*>(stage + (2 + r) * kPart + po * kPageBytes + 16 * s);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float pj = __shfl_sync(gmask, p, (lane & 24) + j);
-          const uint32_t wd = (j < 2) ? rowv.x : (j < 4) ? rowv.y : (j < 6) ? rowv.z : rowv.w;
-          const uint32_t avl = (j & 1) ? row_off<2>(wd, vb0) : row_off<0>(wd, vb0);
-          const uint32_t avh = (j & 1) ? row_off<3>(wd, vb1) : row_off<1>(wd, vb1);
-          float2 vl[4], vh[4];
-          lds8_fp16(vsb + avl, vl);
-          lds8_fp16(vsb + avh, vh);
-          const float2 p2 = make_float2(pj, pj);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            A.ol[k] = __ffma2_rn(p2, vl[k], A.ol[k]);
-            A.oh[k] = __ffma2_rn(p2, vh[k], A.oh[k]);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-      if (tid == 0 && c + kStages < n_chunks) {
-        if (wait_stage(&empty[st], (c / kStages) & 1, failed, a.err)) produce(c + kStages);
-      }
-    }
-  }
-
-  // ---- merge: lanes of a group (l), lane-groups of a warp (shuffles), warps (smem) -------
-  A.l += __shfl_xor_sync(0xFFFFFFFFu, A.l, 1);
-  A.l += __shfl_xor_sync(0xFFFFFFFFu, A.l, 2);
-  A.l += __shfl_xor_sync(0xFFFFFFFFu, A.l, 4);
+// Merge the running states of the lane-groups 8 and 16 lanes apart (all lanes end with the
+// merged state of their warp half pair, i.e. of the whole warp after both steps).
+__device__ __forceinline__ void merge_lane_groups(Acc& A) {
 #pragma unroll
   for (int off = 8; off <= 16; off <<= 1) {
     const float Mo = __shfl_xor_sync(0xFFFFFFFFu, A.M, off);
@@ -508,11 +265,488 @@ __global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a
     A.l = A.l * f + lo * fo;
     A.M = Mn;
   }
-  // per-warp partials in the (now idle) ring: [warp][130] = o[128], M, l
-  __syncthreads();  // every warp is done with the ring
-  float* wpart = reinterpret_cast<float*>(ring);
+}
+
+// Lengths of request b, or zeros when b >= B or when they do not describe a valid cache
+// (returns false then; the window kernel reports it).
+__device__ __forceinline__ bool req_len(const VqAttnArgs& a, int b, int& L, int& NP) {
+  L = 0;
+  NP = 0;
+  if (b >= a.B) return true;
+  const int l = a.seq_len[b], np = a.n_pages[b];
+  const bool ok = !(l < 0 || l > a.max_ctx || np < 0 || np > a.max_pages || (np > 0 && a.sink + kPage * np > l) ||
+                    l - a.sink - kPage * np > a.recent + kPage);
+  if (ok) {
+    L = l;
+    NP = np;
+  }
+  return ok;
+}
+
+__device__ __forceinline__ int pair_units(int NP0, int NP1) { return (max(NP0, NP1) + kChunk - 1) / kChunk; }
+
+// share k of U units among G blocks starts at unit floor(k U / G)
+__device__ __forceinline__ long long share_lo(long long U, int k, int G) { return U * k / G; }
+// the block whose share holds unit u (0 <= u < U)
+__device__ __forceinline__ int share_of(long long u, long long U, int G) { return (int)(((u + 1) * G - 1) / U); }
+
+// header of a unit in its ring stage
+struct UnitHdr {
+  int h, pair, c, flags;   // flags: 1 first unit of a piece, 2 last unit, (dest << 2)
+  int L0, NP0, L1, NP1;    // dest: 0 whole segment, 1 block's first piece, 2 block's last piece
+};
+
+// producer (thread 0) state, in shared memory so it costs the consumers no registers
+struct ProdState {
+  long long i;  // next unit to issue
+  int h, pair, c, nu;
+  int L0, NP0, L1, NP1;
+  int issued;   // units issued by this block
+  int k_loads;  // key-slice copies issued
+};
+
+__device__ __forceinline__ void prod_load_pair(const VqAttnArgs& a, ProdState& P) {
+  req_len(a, 2 * P.pair, P.L0, P.NP0);
+  req_len(a, 2 * P.pair + 1, P.L1, P.NP1);
+  P.nu = pair_units(P.NP0, P.NP1);
+}
+
+// Issue unit P.i into its ring stage (header, index pages, queries), then step to the next
+// unit of the share (skipping request pairs without pages).
+__device__ void prod_next(const VqAttnArgs& a, ProdState& P, unsigned char* ring, uint64_t* full, long long lo,
+                          long long hi, int n_pairs) {
+  const int st = P.issued % kStages;
+  unsigned char* dst = ring + st * kStageBytes;
+  UnitHdr* hd = reinterpret_cast<UnitHdr*>(dst + kOffHdr);
+  const long long seg0 = P.i - P.c, seg1 = seg0 + P.nu;
+  int flags = 0;
+  if (P.i == lo || P.c == 0) flags |= 1;
+  if (P.i == hi - 1 || P.c == P.nu - 1) flags |= 2;
+  const int dest = (seg0 >= lo && seg1 <= hi) ? 0 : (seg0 <= lo ? 1 : 2);
+  hd->h = P.h;
+  hd->pair = P.pair;
+  hd->c = P.c;
+  hd->flags = flags | (dest << 2);
+  hd->L0 = P.L0;
+  hd->NP0 = P.NP0;
+  hd->L1 = P.L1;
+  hd->NP1 = P.NP1;
+  const int p_first = P.c * kChunk;
+  const int n0 = min(kChunk, max(0, P.NP0 - p_first));
+  const int n1 = min(kChunk, max(0, P.NP1 - p_first));
+  const int b0 = 2 * P.pair;
+  const bool two = b0 + 1 < a.B;
+  // the header stores above are released to the consumers by this arrive
+  mbar_arrive_expect_tx(&full[st], (uint32_t)(n0 + n1) * 2 * kPageBytes + (two ? 2u : 1u) * kD * 2);
+  const size_t off = (size_t)p_first * kPageBytes;
+  const size_t bh0 = ((size_t)b0 * a.H + P.h) * (size_t)a.max_pages * kPageBytes;
+  if (n0 > 0) {
+    bulk_g2s(dst, a.idx_k + bh0 + off, n0 * kPageBytes, &full[st]);
+    bulk_g2s(dst + 2 * kPart, a.idx_v + bh0 + off, n0 * kPageBytes, &full[st]);
+  }
+  if (n1 > 0) {
+    const size_t bh1 = ((size_t)(b0 + 1) * a.H + P.h) * (size_t)a.max_pages * kPageBytes;
+    bulk_g2s(dst + kPart, a.idx_k + bh1 + off, n1 * kPageBytes, &full[st]);
+    bulk_g2s(dst + 3 * kPart, a.idx_v + bh1 + off, n1 * kPageBytes, &full[st]);
+  }
+  bulk_g2s(dst + kOffQs, a.q + ((size_t)b0 * a.H + P.h) * kD, kD * 2, &full[st]);
+  if (two) bulk_g2s(dst + kOffQs + kD * 2, a.q + ((size_t)(b0 + 1) * a.H + P.h) * kD, kD * 2, &full[st]);
+  ++P.issued;
+  if (P.i + 1 >= hi) {
+    ++P.i;
+    return;
+  }
+  ++P.i;
+  if (++P.c < P.nu) return;
+  P.c = 0;
+  do {
+    if (++P.pair == n_pairs) {
+      P.pair = 0;
+      ++P.h;
+    }
+    prod_load_pair(a, P);
+  } while (P.nu == 0 && P.h < a.H);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs a, const float scale_log2) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  float* ks = reinterpret_cast<float*>(smem + kOffK);
+  __half* vs = reinterpret_cast<__half*>(smem + kOffV);
+  unsigned char* ring = smem + kOffRing;
+  ProdState* ps = reinterpret_cast<ProdState*>(smem + kOffProd);
+  uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* full = kbar + 1;
+  uint64_t* empty = full + kStages;
+  uint64_t* bsync = empty + kStages;
+  volatile int* failed = reinterpret_cast<volatile int*>(bsync + 1);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = gridDim.x, blk = blockIdx.x;
+  const int n_pairs = (a.B + 1) / 2;
+
+  // ---- units per request pair and their exclusive prefix (every block; block 0 publishes
+  //      it for the window kernel). Runs in the value-slice area before the slice is staged.
+  int* scan = reinterpret_cast<int*>(smem + kOffV);
+  {
+    int* wsum = reinterpret_cast<int*>(ring);
+    for (int p = tid; p < n_pairs; p += kThreads) {
+      int L0, NP0, L1, NP1;
+      req_len(a, 2 * p, L0, NP0);
+      req_len(a, 2 * p + 1, L1, NP1);
+      scan[p] = pair_units(NP0, NP1);
+    }
+    __syncthreads();
+    const int per = (n_pairs + kThreads - 1) / kThreads;
+    const int beg = min(n_pairs, tid * per), end = min(n_pairs, beg + per);
+    int local = 0;
+    for (int p = beg; p < end; ++p) local += scan[p];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int run = incl - local;
+    for (int w = 0; w < warp; ++w) run += wsum[w];
+    for (int p = beg; p < end; ++p) {
+      const int u = scan[p];
+      scan[p] = run;
+      run += u;
+    }
+    if (tid == kThreads - 1) scan[n_pairs] = run;  // the last thread ends on the total
+    __syncthreads();
+  }
+  if (blk == 0)
+    for (int p = tid; p <= n_pairs; p += kThreads) a.pref[p] = scan[p];
+  const int Up = scan[n_pairs];
+  const long long U = (long long)a.H * Up;
+  const long long lo = share_lo(U, blk, G), hi = share_lo(U, blk + 1, G);
+  if (lo >= hi) return;  // uniform: an empty share
+
+  if (tid == 0) {
+    mbar_init(kbar, 1);
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
+    mbar_init(bsync, kThreads);
+    *failed = 0;
+    fence_mbar_init();
+    // first unit of the share: head, then the last pair whose prefix is <= the remainder
+    ProdState& P = *ps;
+    P.i = lo;
+    P.issued = 0;
+    P.k_loads = 0;
+    P.h = (int)(lo / Up);
+    const int rem = (int)(lo - (long long)P.h * Up);
+    int pl = 0, ph = n_pairs - 1;
+    while (pl < ph) {
+      const int mid = (pl + ph + 1) >> 1;
+      if (scan[mid] <= rem) pl = mid;
+      else ph = mid - 1;
+    }
+    P.pair = pl;
+    P.c = rem - scan[pl];
+    prod_load_pair(a, P);
+  }
+  if (tid < 8 && a.max_ctx > kJump) {  // cos/sin(kJump theta_i) for slot tid, in that slot's half order
+    float* jt = reinterpret_cast<float*>(smem + kOffJ) + tid * 16;
+    const int jo0 = (tid & 4) ? 4 : 0;
+    float c8[8], s8[8];
+    ldg8_perm(a.rope_cos + (size_t)kJump * (kD / 2) + 8 * tid, jo0, c8);
+    ldg8_perm(a.rope_sin + (size_t)kJump * (kD / 2) + 8 * tid, jo0, s8);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      jt[k] = c8[k];
+      jt[8 + k] = s8[k];
+    }
+  }
+  __syncthreads();  // barriers initialised, scan read by thread 0: the value area is free
+  if (tid == 0)
+    for (int s = 0; s < kStages && ps->i < hi; ++s) prod_next(a, *ps, ring, full, lo, hi, n_pairs);
+
+  const int s = tid & 7;                 // slot: groups s and s + 8
+  const int o0 = (s & 4) ? 4 : 0;        // key half order (bank-quad spreading)
+  const unsigned gmask = 0xFFu << (lane & 24);
+  const int lg = tid >> 3;
+  const int r = lg >> 5, po = lg & 31;   // this lane-group's request and page slot
+
+  float2 cth[4], sth[4], nsth[4];
+  {
+    float c8[8], s8[8];
+    const int row = (a.max_ctx > 1) ? 1 : 0;
+    ldg8_perm(a.rope_cos + (size_t)row * (kD / 2) + 8 * s, o0, c8);
+    ldg8_perm(a.rope_sin + (size_t)row * (kD / 2) + 8 * s, o0, s8);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      cth[k] = make_float2(c8[2 * k], c8[2 * k + 1]);
+      sth[k] = make_float2(s8[2 * k], s8[2 * k + 1]);
+      nsth[k] = make_float2(-s8[2 * k], -s8[2 * k + 1]);
+    }
+  }
+  float2 u0l[4], u0h[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    u0l[k] = make_float2(0.f, 0.f);
+    u0h[k] = make_float2(0.f, 0.f);
+  }
+  Acc A;
+  acc_reset(A);
+  // lane byte offsets inside a 256-byte table row: key halves swapped for s >= 4 so the 8
+  // lanes of a phase hit 8 bank quads; value lanes read 16 natural bytes each
+  const uint32_t kb0 = 32 * s + 4 * o0, kb1 = kb0 ^ 16u;
+  const uint32_t vb0 = 16 * s, vb1 = 128 + 16 * s;
+  const unsigned char* ksb = reinterpret_cast<const unsigned char*>(ks);
+  const unsigned char* vsb = reinterpret_cast<const unsigned char*>(vs);
+  const float* jt = reinterpret_cast<const float*>(smem + kOffJ) + s * 16;
+
+  const int n_units = (int)(hi - lo);
+  int cur_head = -1;
+  uint32_t kphase = 0, sphase = 0;
+  for (int i = 0; i < n_units; ++i) {
+    const int st = i % kStages;
+    wait_stage(&full[st], (i / kStages) & 1, failed, a.err);
+    unsigned char* stage = ring + st * kStageBytes;
+    const int4 hv0 = *reinterpret_cast<const int4*>(stage + kOffHdr);
+    const int4 hv1 = *reinterpret_cast<const int4*>(stage + kOffHdr + 16);
+    const int uh = hv0.x, upair = hv0.y, uc = hv0.z, uflags = hv0.w;
+
+    if (uh != cur_head) {  // uniform: every thread read the same header
+      // ---- stage the codebook slices of head uh ----
+      block_sync(bsync, sphase, failed, a.err);  // every warp is done with the old slices
+      if (tid == 0 && !*failed) {
+        const float* btk = a.bt_k + (size_t)uh * kCB * kD;
+        mbar_arrive_expect_tx(kbar, kKSliceBytes);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          bulk_g2s(ks + k * (kKSliceBytes / 16), btk + k * (kKSliceBytes / 16), kKSliceBytes / 4, kbar);
+        ++ps->k_loads;
+      }
+      {  // value slice: fp32 [2][256][64] in L2 -> fp16 [256][128] in shared memory
+        const float4* src = reinterpret_cast<const float4*>(a.bt_v + (size_t)uh * kCB * kD);
+        for (int j = tid; j < kCB * kD / 4; j += kThreads) {
+          const float4 v = __ldg(src + j);
+          const int half = j / (kCB * kD / 8), rem = j % (kCB * kD / 8);
+          const int row = rem / (kD / 8), c4 = rem % (kD / 8);
+          __half2 lo2 = __floats2half2_rn(v.x, v.y), hi2 = __floats2half2_rn(v.z, v.w);
+          uint2 w;
+          w.x = *reinterpret_cast<uint32_t*>(&lo2);
+          w.y = *reinterpret_cast<uint32_t*>(&hi2);
+          reinterpret_cast<uint2*>(vs + row * kD + half * (kD / 2))[c4] = w;
+        }
+      }
+      block_sync(bsync, sphase, failed, a.err);  // value slice complete
+      wait_stage(kbar, kphase, failed, a.err);
+      kphase ^= 1u;
+      cur_head = uh;
+    }
+    if (uflags & 1) acc_reset(A);  // a new piece
+
+    const int L = r ? hv1.z : hv1.x, NP = r ? hv1.w : hv1.y;
+    const int pg = uc * kChunk + po;
+    if (!*failed && pg < NP) {
+      if ((uflags & 1) || uc % kResync == 0) {
+        const uint16_t* qr = reinterpret_cast<const uint16_t*>(stage + kOffQs) + r * kD;
+        rotated_query_bf16(a.rope_cos, a.rope_sin, L - 1 - (a.sink + kPage * pg), s, o0, qr, u0l, u0h);
+      } else {  // kJump positions later
+        const float4 c0 = *reinterpret_cast<const float4*>(jt), c1 = *reinterpret_cast<const float4*>(jt + 4);
+        const float4 s0 = *reinterpret_cast<const float4*>(jt + 8), s1 = *reinterpret_cast<const float4*>(jt + 12);
+        const float2 cj[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w), make_float2(c1.x, c1.y),
+                              make_float2(c1.z, c1.w)};
+        const float2 sj[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
+                              make_float2(s1.z, s1.w)};
+        const float2 nsj[4] = {make_float2(-s0.x, -s0.y), make_float2(-s0.z, -s0.w), make_float2(-s1.x, -s1.y),
+                               make_float2(-s1.z, -s1.w)};
+        rotate8(u0l, u0h, cj, sj, nsj);
+      }
+      const uint4 rowk = *reinterpret_cast<const uint4*>(stage + r * kPart + po * kPageBytes + 16 * s);
+      float2 ul[4], uh2[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        ul[k] = u0l[k];
+        uh2[k] = u0h[k];
+      }
+      float part[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t wd = (j < 2) ? rowk.x : (j < 4) ? rowk.y : (j < 6) ? rowk.z : rowk.w;
+        uint32_t al0, al1, ah0, ah1;
+        if (j & 1) {
+          al0 = row_off<2>(wd, kb0); al1 = row_off<2>(wd, kb1);
+          ah0 = row_off<3>(wd, kb0); ah1 = row_off<3>(wd, kb1);
+        } else {
+          al0 = row_off<0>(wd, kb0); al1 = row_off<0>(wd, kb1);
+          ah0 = row_off<1>(wd, kb0); ah1 = row_off<1>(wd, kb1);
+        }
+        const float4 la = *reinterpret_cast<const float4*>(ksb + al0);
+        const float4 lb = *reinterpret_cast<const float4*>(ksb + al1);
+        const float4 ha = *reinterpret_cast<const float4*>(ksb + kKSliceBytes / 2 + ah0);
+        const float4 hb = *reinterpret_cast<const float4*>(ksb + kKSliceBytes / 2 + ah1);
+        float2 acc0 = __fmul2_rn(ul[0], make_float2(la.x, la.y));
+        float2 acc1 = __fmul2_rn(uh2[0], make_float2(ha.x, ha.y));
+        acc0 = __ffma2_rn(ul[1], make_float2(la.z, la.w), acc0);
+        acc1 = __ffma2_rn(uh2[1], make_float2(ha.z, ha.w), acc1);
+        acc0 = __ffma2_rn(ul[2], make_float2(lb.x, lb.y), acc0);
+        acc1 = __ffma2_rn(uh2[2], make_float2(hb.x, hb.y), acc1);
+        acc0 = __ffma2_rn(ul[3], make_float2(lb.z, lb.w), acc0);
+        acc1 = __ffma2_rn(uh2[3], make_float2(hb.z, hb.w), acc1);
+        const float2 acc = __fadd2_rn(acc0, acc1);
+        part[j] = acc.x + acc.y;
+        if (j < 7) rotate8(ul, uh2, cth, sth, nsth);  // next token: one position later
+      }
+      transpose_reduce8(part, s, gmask);
+      const float p = online_weights(A, part[0] * scale_log2, gmask);
+      const uint4 rowv = *reinterpret_cast<const uint4*>(stage + (2 + r) * kPart + po * kPageBytes + 16 * s);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float pj = __shfl_sync(gmask, p, (lane & 24) + j);
+        const uint32_t wd = (j < 2) ? rowv.x : (j < 4) ? rowv.y : (j < 6) ? rowv.z : rowv.w;
+        const uint32_t avl = (j & 1) ? row_off<2>(wd, vb0) : row_off<0>(wd, vb0);
+        const uint32_t avh = (j & 1) ? row_off<3>(wd, vb1) : row_off<1>(wd, vb1);
+        float2 vl[4], vh[4];
+        lds8_fp16(vsb + avl, vl);
+        lds8_fp16(vsb + avh, vh);
+        const float2 p2 = make_float2(pj, pj);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          A.ol[k] = __ffma2_rn(p2, vl[k], A.ol[k]);
+          A.oh[k] = __ffma2_rn(p2, vh[k], A.oh[k]);
+        }
+      }
+    }
+
+    if (uflags & 2) {
+      // ---- end of a piece: lanes of a group (l), lane-groups (shuffles), warps (smem) ----
+      A.l += __shfl_xor_sync(0xFFFFFFFFu, A.l, 1);
+      A.l += __shfl_xor_sync(0xFFFFFFFFu, A.l, 2);
+      A.l += __shfl_xor_sync(0xFFFFFFFFu, A.l, 4);
+      merge_lane_groups(A);
+      block_sync(bsync, sphase, failed, a.err);  // every warp is done with this stage's pages
+      float* wpart = reinterpret_cast<float*>(stage);  // [warp][130] = o[128], M, l
+      if (lane < 8) {
+        float* wp = wpart + warp * (kD + 2);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          reinterpret_cast<float2*>(wp + 8 * s)[k] = A.ol[k];
+          reinterpret_cast<float2*>(wp + 64 + 8 * s)[k] = A.oh[k];
+        }
+        if (lane == 0) {
+          wp[kD] = A.M;
+          wp[kD + 1] = A.l;
+        }
+        fence_proxy_async_smem();  // before the stage is refilled by TMA
+      }
+      block_sync(bsync, sphase, failed, a.err);
+      if (tid < 2 * kD) {  // thread (request rr, channel ch) merges the 8 warps of its request
+        const int rr = tid >> 7, ch = tid & 127;
+        float Mr = -INFINITY, Lr = 0.f, o = 0.f;
+        for (int w = rr * 8; w < rr * 8 + 8; ++w) Mr = fmaxf(Mr, wpart[w * (kD + 2) + kD]);
+        if (Mr != -INFINITY) {
+          for (int w = rr * 8; w < rr * 8 + 8; ++w) {
+            const float mw = wpart[w * (kD + 2) + kD];
+            if (mw == -INFINITY) continue;
+            const float f = exp2f(mw - Mr);
+            Lr = fmaf(f, wpart[w * (kD + 2) + kD + 1], Lr);
+            o = fmaf(f, wpart[w * (kD + 2) + ch], o);
+          }
+        }
+        if (2 * upair + rr < a.B) {
+          const int dest = uflags >> 2;
+          float* pp = (dest == 0) ? a.part_whole + ((size_t)uh * n_pairs + upair) * kVqPartFloats
+                                  : a.part_slot + ((size_t)blk * 2 + (dest - 1)) * kVqPartFloats;
+          pp += rr * (kD + 2);
+          pp[2 + ch] = o;
+          if (ch == 0) {
+            pp[0] = Mr;
+            pp[1] = Lr;
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+    if (tid == 0 && ps->i < hi) {  // producer: refill this stage with the unit kStages ahead
+      if (wait_stage(&empty[st], (i / kStages) & 1, failed, a.err)) prod_next(a, *ps, ring, full, lo, hi, n_pairs);
+    }
+  }
+
+  // after a timeout, let the block's own copies in flight land before it exits
+  if (tid == 0 && *failed) {
+    const int issued = ps->issued;
+    for (int j = max(0, issued - kStages); j < issued; ++j) mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1);
+    if (ps->k_loads > 0) mbar_wait_bounded(kbar, (ps->k_loads - 1) & 1);
+  }
+}
+
+// ------------------------------------------------------------------ window + merge kernel
+constexpr int kWThreads = 128;
+
+__global__ void __launch_bounds__(kWThreads) vq_window_kernel(const VqAttnArgs a, const float scale_log2) {
+  __shared__ __align__(16) float qs[kD];
+  __shared__ __align__(16) float wpart[kWThreads / 32][kD + 2];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x / a.H, h = blockIdx.x - b * a.H;
+  int L, NP;
+  if (!req_len(a, b, L, NP) && h == 0 && tid == 0) set_error(a.err, KVQ_ERR_CAPACITY);
+  qs[tid] = bf16_to_f32(a.q[((size_t)b * a.H + h) * kD + tid]);
+  __syncthreads();
+
+  // ---- bf16 window: lane-group g takes tokens g, g + 16, ... ----------------------------
+  const int nsink = min(a.sink, L);
+  const int nwin = (L > 0) ? nsink + max(0, L - a.sink - kPage * NP) : 0;
+  const int s = lane & 7, g = tid >> 3;
+  const unsigned gmask = 0xFFu << (lane & 24);
+  const uint16_t* wk = a.win_k + ((size_t)b * a.H + h) * a.win_slots * kD;
+  const uint16_t* wv = a.win_v + ((size_t)b * a.H + h) * a.win_slots * kD;
+  Acc A;  // here l is the same in every lane of a lane-group
+  acc_reset(A);
+  for (int w = g; w < nwin; w += kWThreads / 8) {
+    const int p = (w < nsink) ? w : a.sink + kPage * NP + (w - nsink);
+    const int slot = (p < a.sink) ? p : a.sink + (p - a.sink) % (a.recent + kPage);
+    float kl[8], kh[8], vl[8], vh[8];
+    ldg8_bf16_perm(wk + (size_t)slot * kD + 8 * s, 0, kl);
+    ldg8_bf16_perm(wk + (size_t)slot * kD + 64 + 8 * s, 0, kh);
+    ldg8_bf16_perm(wv + (size_t)slot * kD + 8 * s, 0, vl);
+    ldg8_bf16_perm(wv + (size_t)slot * kD + 64 + 8 * s, 0, vh);
+    float2 ul[4], uh[4];
+    rotated_query(a.rope_cos, a.rope_sin, L - 1 - p, s, 0, qs, ul, uh);
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc = __ffma2_rn(ul[k], make_float2(kl[2 * k], kl[2 * k + 1]), acc);
+      acc = __ffma2_rn(uh[k], make_float2(kh[2 * k], kh[2 * k + 1]), acc);
+    }
+    float sc = acc.x + acc.y;
+    sc += __shfl_xor_sync(gmask, sc, 4);
+    sc += __shfl_xor_sync(gmask, sc, 2);
+    sc += __shfl_xor_sync(gmask, sc, 1);
+    sc *= scale_log2;
+    if (sc > A.M) {
+      const float f = (A.M == -INFINITY) ? 0.f : exp2f(A.M - sc);
+      const float2 f2 = make_float2(f, f);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        A.ol[k] = __fmul2_rn(A.ol[k], f2);
+        A.oh[k] = __fmul2_rn(A.oh[k], f2);
+      }
+      A.l *= f;
+      A.M = sc;
+    }
+    const float pw = exp2f(sc - A.M);
+    A.l += pw;
+    const float2 p2 = make_float2(pw, pw);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      A.ol[k] = __ffma2_rn(p2, make_float2(vl[2 * k], vl[2 * k + 1]), A.ol[k]);
+      A.oh[k] = __ffma2_rn(p2, make_float2(vh[2 * k], vh[2 * k + 1]), A.oh[k]);
+    }
+  }
+  merge_lane_groups(A);
   if (lane < 8) {
-    float* wp = wpart + warp * (kD + 2);
+    float* wp = wpart[warp];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       reinterpret_cast<float2*>(wp + 8 * s)[k] = A.ol[k];
@@ -524,87 +758,74 @@ __global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a
     }
   }
   __syncthreads();
-  if (*failed) return;  // uniform: every thread read the flag after the barrier
 
-  // threads (request rr, channel ch) merge the 8 warps of their request
-  const int rr = tid >> 7, ch = tid & 127;
-  float Mr = -INFINITY, Lr = 0.f, o = 0.f;
-  if (tid < 2 * kD) {
-    for (int w = rr * 8; w < rr * 8 + 8; ++w) Mr = fmaxf(Mr, wpart[w * (kD + 2) + kD]);
-    if (Mr != -INFINITY) {
-      for (int w = rr * 8; w < rr * 8 + 8; ++w) {
-        const float mw = wpart[w * (kD + 2) + kD];
-        if (mw == -INFINITY) continue;
-        const float f = exp2f(mw - Mr);
-        Lr = fmaf(f, wpart[w * (kD + 2) + kD + 1], Lr);
-        o = fmaf(f, wpart[w * (kD + 2) + ch], o);
+  // ---- merge: window warps, then every page piece of the (pair, head) segment ----------
+  const int ch = tid;
+  float Mx = -INFINITY, Lt = 0.f, o = 0.f;
+  auto fold = [&](float Mp, float lp, float op) {
+    if (Mp == -INFINITY) return;
+    const float Mn = fmaxf(Mx, Mp);
+    const float f = (Mx == -INFINITY) ? 0.f : exp2f(Mx - Mn);
+    const float fp = exp2f(Mp - Mn);
+    Lt = Lt * f + lp * fp;
+    o = o * f + op * fp;
+    Mx = Mn;
+  };
+#pragma unroll
+  for (int w = 0; w < kWThreads / 32; ++w) fold(wpart[w][kD], wpart[w][kD + 1], wpart[w][ch]);
+
+  const int n_pairs = (a.B + 1) / 2, pair = b >> 1, rr = b & 1;
+  const int p0 = a.pref[pair], nu = a.pref[pair + 1] - p0;
+  if (nu > 0) {
+    const int Up = a.pref[n_pairs];
+    const long long U = (long long)a.H * Up;
+    const long long s0 = (long long)h * Up + p0, s1 = s0 + nu;
+    const int k0 = share_of(s0, U, a.G), k1 = share_of(s1 - 1, U, a.G);
+    if (k0 == k1) {
+      const float* pp = a.part_whole + ((size_t)h * n_pairs + pair) * kVqPartFloats + rr * (kD + 2);
+      fold(pp[0], pp[1], pp[2 + ch]);
+    } else {
+      for (int kk = k0; kk <= k1; ++kk) {
+        const long long lk = share_lo(U, kk, a.G);
+        if (lk == share_lo(U, kk + 1, a.G)) continue;  // an empty share
+        const float* pp = a.part_slot + ((size_t)kk * 2 + (lk >= s0 ? 0 : 1)) * kVqPartFloats + rr * (kD + 2);
+        fold(pp[0], pp[1], pp[2 + ch]);
       }
     }
   }
-
-  if (a.n_split == 1) {
-    if (tid < 2 * kD && rr < nreq) {
-      const float val = (Lr > 0.f) ? o / Lr : 0.f;
-      const size_t oi = ((size_t)(b0 + rr) * H + h) * kD + ch;
-      if (a.out_fp32) reinterpret_cast<float*>(a.out)[oi] = val;
-      else reinterpret_cast<uint16_t*>(a.out)[oi] = f32_to_bf16(val);
-    }
-    return;
-  }
-
-  // ---- split partial, then the last block of this (pair, head) merges -------------------
-  if (tid < 2 * kD && rr < nreq) {
-    float* pp = a.part + (((size_t)(b0 + rr) * H + h) * a.n_split + split) * (kD + 2);
-    pp[2 + ch] = o;
-    if (ch == 0) {
-      pp[0] = Mr;
-      pp[1] = Lr;
-    }
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int prev = atomicAdd(&a.counters[pair * H + h], 1);
-    sflag[0] = (prev == a.n_split - 1);
-  }
-  __syncthreads();
-  if (!sflag[0]) return;
-  __threadfence();
-  if (tid < 2 * kD && rr < nreq) {
-    const int b = b0 + rr;
-    const float* pp = a.part + ((size_t)b * H + h) * a.n_split * (kD + 2);
-    float Mx = -INFINITY;
-    for (int sp = 0; sp < a.n_split; ++sp) Mx = fmaxf(Mx, __ldcg(pp + sp * (kD + 2)));
-    float Lt = 0.f, acc = 0.f;
-    if (Mx != -INFINITY) {
-      for (int sp = 0; sp < a.n_split; ++sp) {
-        const float ms = __ldcg(pp + sp * (kD + 2));
-        if (ms == -INFINITY) continue;
-        const float wgt = exp2f(ms - Mx);
-        Lt = fmaf(wgt, __ldcg(pp + sp * (kD + 2) + 1), Lt);
-        acc = fmaf(wgt, __ldcg(pp + sp * (kD + 2) + 2 + ch), acc);
-      }
-    }
-    const float val = (Lt > 0.f) ? acc / Lt : 0.f;
-    const size_t oi = ((size_t)b * H + h) * kD + ch;
-    if (a.out_fp32) reinterpret_cast<float*>(a.out)[oi] = val;
-    else reinterpret_cast<uint16_t*>(a.out)[oi] = f32_to_bf16(val);
-  }
-  if (tid == 0) a.counters[pair * H + h] = 0;
+  const float val = (Lt > 0.f) ? o / Lt : 0.f;
+  const size_t oi = ((size_t)b * a.H + h) * kD + ch;
+  if (a.out_fp32) reinterpret_cast<float*>(a.out)[oi] = val;
+  else reinterpret_cast<uint16_t*>(a.out)[oi] = f32_to_bf16(val);
 }
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
-int vq_attn_max_pages_per_split(int) { return 1 << 20; }  // one pass: no per-split storage
+size_t vq_attn_ws_bytes(int B, int H, int G) {
+  const size_t n_pairs = (size_t)(B + 1) / 2;
+  return align256((n_pairs + 1) * sizeof(int32_t)) + align256((size_t)H * n_pairs * kVqPartFloats * sizeof(float)) +
+         align256((size_t)G * 2 * kVqPartFloats * sizeof(float));
+}
 
-size_t vq_attn_smem_bytes(int, int) { return kSmemBytes; }
+int vq_attn_max_pairs() { return kMaxPairs; }
 
-cudaError_t launch_vq_attn(const VqAttnArgs& a, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(vq_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+cudaError_t launch_vq_attn(const VqAttnArgs& args, void* ws, cudaStream_t st) {
+  VqAttnArgs a = args;
+  const size_t n_pairs = (size_t)(a.B + 1) / 2;
+  char* w = static_cast<char*>(ws);
+  a.pref = reinterpret_cast<int32_t*>(w);
+  w += align256((n_pairs + 1) * sizeof(int32_t));
+  a.part_whole = reinterpret_cast<float*>(w);
+  w += align256((size_t)a.H * n_pairs * kVqPartFloats * sizeof(float));
+  a.part_slot = reinterpret_cast<float*>(w);
+  cudaError_t e = cudaFuncSetAttribute(vq_pages_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)kD);
-  dim3 grid(a.n_split, (a.B + 1) / 2, a.H);
-  vq_attn_kernel<<<grid, kThreads, kSmemBytes, st>>>(a, scale_log2);
+  vq_pages_kernel<<<a.G, kThreads, kSmemBytes, st>>>(a, scale_log2);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  vq_window_kernel<<<(unsigned)(a.B * a.H), kWThreads, 0, st>>>(a, scale_log2);
   return cudaGetLastError();
 }
 

@@ -89,16 +89,21 @@ def test_decode_attn_argument_checks(L):
 
 def test_workspace_size_and_split_plan(L):
     c = cfg2()
-    assert kvq.kvq_decode_workspace_size(c, 64, 1) == 0
-    n = kvq.kvq_decode_workspace_size(c, 64, 4)
-    assert n >= 64 * 16 * 4 * 130 * 4 + 32 * 16 * 4
+
+    def a256(x):
+        return (x + 255) // 256 * 256
+
+    # LoopVQ: unit prefix over the 32 request pairs, one partial per (pair, head) segment and
+    # two per page-kernel block, each partial 2 x (M, l, o[128]) floats
+    for blocks in (1, 4, 152):
+        want = a256(33 * 4) + a256(16 * 32 * 260 * 4) + a256(blocks * 2 * 260 * 4)
+        assert kvq.kvq_decode_workspace_size(c, 64, blocks) == want
     auto = kvq.kvq_decode_auto_splits(c, 64)
-    assert 1 <= auto <= 64
-    assert kvq.kvq_decode_workspace_size(c, 64, auto) == (0 if auto == 1 else
-                                                          kvq.kvq_decode_workspace_size(c, 64, auto))
-    # a long context at batch 1 is split so that every SM gets a share of its pages
+    assert auto >= 1
+    assert kvq.kvq_decode_workspace_size(c, 64, 0) == kvq.kvq_decode_workspace_size(c, 64, auto)
+    # the page kernel runs one block per SM by default, whatever the batch
     big = cfg2(max_pages=40000, max_ctx=400000)
-    assert kvq.kvq_decode_auto_splits(big, 1) >= 8
+    assert kvq.kvq_decode_auto_splits(big, 1) == auto
 
 
 def test_encode_and_prefill_argument_checks(L):

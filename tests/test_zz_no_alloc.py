@@ -1,6 +1,7 @@
 """kvq_decode_attn_noalloc: decode attention for callers that cannot allocate device memory
 (an engine whose memory pool owns the whole GPU, or code inside another framework's
-callback). It takes its split-K scratch from an array the library reserves per device.
+callback). It takes its workspace (unit prefix and partial softmaxes) from an array the
+library reserves per device.
 Checked through the C ABI against kvq_decode_attn with a caller workspace, on two calls in
 a row (the second call reuses the array the first one left behind). Collected last on
 purpose, and self-contained so that it also passes alone in a fresh process."""
@@ -45,13 +46,13 @@ def test_noalloc_matches_workspace_call_twice(n_splits):
 
 
 def test_noalloc_rejects_calls_beyond_the_reserved_scratch():
-    # 64 splits of a batch of 64 with 16 heads need ~4.3 MB per 8 requests: far over the
-    # reserved array at this batch size, so the call is refused before anything launches
+    # 4096 page-kernel blocks keep two partial slots each (2 x 1040 B): 8.5 MB, over the
+    # reserved array, so the call is refused before anything launches
     cfg = kvq.VqConfig(n_heads=16, max_pages=4063, max_batch=64, max_ctx=32768, recent=256, Tc=4, G=32)
-    need = kvq.kvq_decode_workspace_size(cfg, 64, 64)
+    need = kvq.kvq_decode_workspace_size(cfg, 64, 4096)
     assert need > (8 << 20)
     c = cfg.to_c()
     kc = kvq.VqCacheC(*([0x10000] * 12))
     st = kvq.lib().kvq_decode_attn_noalloc(kvq.FMT_LOOPVQ, ctypes.byref(c), ctypes.byref(kc), 0, 1, 0x10000, 64,
-                                           0x10000, kvq.OUT_FP32, 64, None)
+                                           0x10000, kvq.OUT_FP32, 4096, None)
     assert st == 5 and b"reserves" in kvq.lib().kvq_last_error()

@@ -20,13 +20,15 @@ constexpr int kPageBytes = kPage * kNG;
 // ---------------------------------------------------------------- LoopVQ decode attention
 // Two launches per call. The page kernel runs G persistent blocks over the work units
 // (head, request pair, chunk of 32 index pages), head-major; block k takes the contiguous
-// units [k U / G, (k + 1) U / G). It writes one partial softmax (M, l, o[128]) per request
-// for every piece of a (pair, head) segment it covers: to part_whole[seg] when the whole
-// segment lies in its share, else to part_slot[k][0] (the piece holding the block's first
-// unit) or part_slot[k][1] (the piece holding its last). The window kernel attends the bf16
-// sink/recent tokens of every (request, head) and merges them with the pieces.
+// units [k U / G, (k + 1) U / G). For every piece of a (pair, head) segment it covers, each
+// of its warps writes one partial softmax (M, l, o[128]) of its request: to part_whole[seg]
+// when the whole segment lies in the block's share, else to part_slot[k][0] (the piece
+// holding the block's first unit) or part_slot[k][1] (the piece holding its last). The
+// window kernel attends the bf16 sink/recent tokens of every (request, head) and merges
+// them with the pieces.
 constexpr int kVqChunk = 32;   // index pages of each request per work unit
-constexpr int kVqPartFloats = 2 * (kD + 2);  // one piece: [request][M, l, o[128]]
+constexpr int kVqWarpsPerReq = 8;                          // page-kernel warps per request
+constexpr int kVqPartFloats = 2 * kVqWarpsPerReq * (kD + 2);  // one piece: [request][warp][M, l, o[128]]
 
 struct VqAttnArgs {
   const uint8_t* idx_k;      // [max_batch][H][max_pages][128] of (layer, block)

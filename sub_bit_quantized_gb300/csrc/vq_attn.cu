@@ -20,10 +20,11 @@
 //    64..127 as two [256][64] tables), values in fp16 ([256][128], converted while
 //    staging; value rounding error ~1e-4 of the output). A codeword's shared-memory address
 //    is one byte permute: (index << 8) | lane offset, and every lookup is a 128-bit load.
-//  * Thread 0 streams the units through a 2-stage ring with TMA bulk copies: 32 key and 32
-//    value pages of each request, the two bf16 queries and a header naming the unit. Full
-//    and empty mbarriers; every wait is bounded and reports a timeout through the device
-//    error word instead of hanging.
+//  * The units stream through a 2-stage ring with TMA bulk copies: 32 key and 32 value
+//    pages of each request, the two bf16 queries and a header naming the unit. A full
+//    mbarrier per stage; the last warp to finish with a stage (a shared-memory arrival
+//    counter) issues its refill. Every wait is bounded and reports a timeout through the
+//    device error word instead of hanging.
 //  * 8 lanes per page, lane s owns the RoPE partner groups s and s+8 (channels 8s..8s+7 and
 //    64+8s..64+8s+7). The rotated query u = R(p_q - p) q satisfies <R(p_q) q, R(p) k> =
 //    <u, k>, so keys are never rotated: u is built from the cos/sin table at a lane-group's
@@ -52,7 +53,7 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = kVqChunk;                          // pages of each request per unit
 constexpr int kStages = 2;
-constexpr int kResync = 16;                               // units between cos/sin table reloads
+constexpr int kResync = 64;                               // units between cos/sin table reloads
 constexpr int kJump = kChunk * kPage;                     // positions between a lane-group's pages
 constexpr uint32_t kKSliceBytes = kCB * kD * 4;           // fp32 key codebook slice
 constexpr uint32_t kVSliceBytes = kCB * kD * 2;           // fp16 value codebook slice
@@ -65,7 +66,7 @@ constexpr uint32_t kStageBytes = kOffQs + 2 * kD * 2 + 64;  // [K r0|K r1|V r0|V
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kKSliceBytes;
 constexpr int kOffRing = kOffV + kVSliceBytes;
-constexpr int kOffJ = kOffRing + kStages * kStageBytes;   // float [8 slots][16]: cos, sin(256 theta)
+constexpr int kOffJ = kOffRing + kStages * kStageBytes;   // float4 [4][8 slots]: cos, sin(256 theta)
 constexpr int kOffProd = kOffJ + 8 * 16 * 4;              // producer state (thread 0)
 constexpr int kOffBar = kOffProd + 64;                    // mbarriers + flags
 constexpr int kSmemBytes = kOffBar + 128;
@@ -165,23 +166,6 @@ __device__ __forceinline__ void lds8_bf16_perm(const uint16_t* p, int o0, float 
   const uint2 b = *reinterpret_cast<const uint2*>(p + (4 - o0));
   v[0] = bf16_lo(a.x); v[1] = bf16_hi(a.x); v[2] = bf16_lo(a.y); v[3] = bf16_hi(a.y);
   v[4] = bf16_lo(b.x); v[5] = bf16_hi(b.x); v[6] = bf16_lo(b.y); v[7] = bf16_hi(b.y);
-}
-
-// rotated query u = R(d) q from a bf16 query in shared memory (lane half order)
-__device__ __forceinline__ void rotated_query_bf16(const float* rc, const float* rs, int d, int s, int o0,
-                                                   const uint16_t* q, float2 (&ul)[4], float2 (&uh)[4]) {
-  float c8[8], s8[8], ql[8], qh[8];
-  ldg8_perm(rc + (size_t)d * (kD / 2) + 8 * s, o0, c8);
-  ldg8_perm(rs + (size_t)d * (kD / 2) + 8 * s, o0, s8);
-  lds8_bf16_perm(q + 8 * s, o0, ql);
-  lds8_bf16_perm(q + 64 + 8 * s, o0, qh);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    ul[k] = make_float2(ql[2 * k] * c8[2 * k] - qh[2 * k] * s8[2 * k],
-                        ql[2 * k + 1] * c8[2 * k + 1] - qh[2 * k + 1] * s8[2 * k + 1]);
-    uh[k] = make_float2(qh[2 * k] * c8[2 * k] + ql[2 * k] * s8[2 * k],
-                        qh[2 * k + 1] * c8[2 * k + 1] + ql[2 * k + 1] * s8[2 * k + 1]);
-  }
 }
 
 // A timed-out wait marks the block as failed; every later wait then returns at once, so a
@@ -296,26 +280,48 @@ struct UnitHdr {
   int L0, NP0, L1, NP1;    // dest: 0 whole segment, 1 block's first piece, 2 block's last piece
 };
 
-// producer (thread 0) state, in shared memory so it costs the consumers no registers
-struct ProdState {
-  long long i;  // next unit to issue
+// a position in a block's share of units
+struct Walker {
+  long long i;  // unit index
   int h, pair, c, nu;
   int L0, NP0, L1, NP1;
+};
+
+// producer state (used by whichever warp refills a stage), in shared memory so it costs the
+// consumers no registers
+struct ProdState {
+  Walker cur;   // next unit to issue
   int issued;   // units issued by this block
   int k_loads;  // key-slice copies issued
 };
 
-__device__ __forceinline__ void prod_load_pair(const VqAttnArgs& a, ProdState& P) {
+__device__ __forceinline__ void walker_load_pair(const VqAttnArgs& a, Walker& P) {
   req_len(a, 2 * P.pair, P.L0, P.NP0);
   req_len(a, 2 * P.pair + 1, P.L1, P.NP1);
   P.nu = pair_units(P.NP0, P.NP1);
 }
 
-// Issue unit P.i into its ring stage (header, index pages, queries), then step to the next
-// unit of the share (skipping request pairs without pages).
-__device__ void prod_next(const VqAttnArgs& a, ProdState& P, unsigned char* ring, uint64_t* full, long long lo,
+// step to the next unit (the caller checks that one is left in the share), skipping request
+// pairs without pages
+__device__ __forceinline__ void walker_next(const VqAttnArgs& a, Walker& P, int n_pairs) {
+  ++P.i;
+  if (++P.c < P.nu) return;
+  P.c = 0;
+  do {
+    if (++P.pair == n_pairs) {
+      P.pair = 0;
+      ++P.h;
+    }
+    walker_load_pair(a, P);
+  } while (P.nu == 0 && P.h < a.H);
+}
+
+// Issue the next unit into its ring stage (header, index pages, queries) and step to the one
+// after it.
+__device__ void prod_next(const VqAttnArgs& a, ProdState& S, unsigned char* ring, uint64_t* full, long long lo,
                           long long hi, int n_pairs) {
-  const int st = P.issued % kStages;
+  Walker& P = S.cur;
+  const int st = S.issued % kStages;
   unsigned char* dst = ring + st * kStageBytes;
   UnitHdr* hd = reinterpret_cast<UnitHdr*>(dst + kOffHdr);
   const long long seg0 = P.i - P.c, seg1 = seg0 + P.nu;
@@ -351,21 +357,9 @@ __device__ void prod_next(const VqAttnArgs& a, ProdState& P, unsigned char* ring
   }
   bulk_g2s(dst + kOffQs, a.q + ((size_t)b0 * a.H + P.h) * kD, kD * 2, &full[st]);
   if (two) bulk_g2s(dst + kOffQs + kD * 2, a.q + ((size_t)(b0 + 1) * a.H + P.h) * kD, kD * 2, &full[st]);
-  ++P.issued;
-  if (P.i + 1 >= hi) {
-    ++P.i;
-    return;
-  }
-  ++P.i;
-  if (++P.c < P.nu) return;
-  P.c = 0;
-  do {
-    if (++P.pair == n_pairs) {
-      P.pair = 0;
-      ++P.h;
-    }
-    prod_load_pair(a, P);
-  } while (P.nu == 0 && P.h < a.H);
+  ++S.issued;
+  if (P.i + 1 < hi) walker_next(a, P, n_pairs);
+  else ++P.i;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs a, const float scale_log2) {
@@ -376,12 +370,16 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
   ProdState* ps = reinterpret_cast<ProdState*>(smem + kOffProd);
   uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* full = kbar + 1;
-  uint64_t* empty = full + kStages;
-  uint64_t* bsync = empty + kStages;
-  volatile int* failed = reinterpret_cast<volatile int*>(bsync + 1);
+  uint64_t* bsync = full + kStages;
+  int* iflags = reinterpret_cast<int*>(bsync + 1);
+  volatile int* failed = iflags;
+  int* released = iflags + 1;  // [kStages]: warps done with the stage's current unit
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, blk = blockIdx.x;
+  // let the window kernel launch now: its blocks take SMs as page blocks finish, attend
+  // their window tokens and wait for this grid before they read the partials
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int n_pairs = (a.B + 1) / 2;
 
   // ---- units per request pair and their exclusive prefix (every block; block 0 publishes
@@ -430,16 +428,16 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kWarps);
+      released[s] = 0;
     }
     mbar_init(bsync, kThreads);
     *failed = 0;
     fence_mbar_init();
     // first unit of the share: head, then the last pair whose prefix is <= the remainder
-    ProdState& P = *ps;
+    Walker& P = ps->cur;
+    ps->issued = 0;
+    ps->k_loads = 0;
     P.i = lo;
-    P.issued = 0;
-    P.k_loads = 0;
     P.h = (int)(lo / Up);
     const int rem = (int)(lo - (long long)P.h * Up);
     int pl = 0, ph = n_pairs - 1;
@@ -450,23 +448,31 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
     }
     P.pair = pl;
     P.c = rem - scan[pl];
-    prod_load_pair(a, P);
+    walker_load_pair(a, P);
+    // codebook slices of the (at most 4 first) heads of the share: HBM -> L2 now
+    const int h_last = min((int)((hi - 1) / Up), P.h + 3);
+    for (int hh = P.h; hh <= h_last; ++hh)
+      for (int k = 0; k < 4; ++k) {
+        bulk_prefetch_l2(a.bt_k + (size_t)hh * kCB * kD + k * (kCB * kD / 4), kKSliceBytes / 4);
+        bulk_prefetch_l2(a.bt_v + (size_t)hh * kCB * kD + k * (kCB * kD / 4), kKSliceBytes / 4);
+      }
   }
-  if (tid < 8 && a.max_ctx > kJump) {  // cos/sin(kJump theta_i) for slot tid, in that slot's half order
-    float* jt = reinterpret_cast<float*>(smem + kOffJ) + tid * 16;
+  if (tid < 8 && a.max_ctx > kJump) {
+    // cos/sin(kJump theta_i) for slot tid in that slot's half order, stored [chunk][slot] so
+    // that the 8 slots of a lane-group read 8 consecutive float4s (no bank conflicts)
+    float4* jt = reinterpret_cast<float4*>(smem + kOffJ);
     const int jo0 = (tid & 4) ? 4 : 0;
     float c8[8], s8[8];
     ldg8_perm(a.rope_cos + (size_t)kJump * (kD / 2) + 8 * tid, jo0, c8);
     ldg8_perm(a.rope_sin + (size_t)kJump * (kD / 2) + 8 * tid, jo0, s8);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      jt[k] = c8[k];
-      jt[8 + k] = s8[k];
-    }
+    jt[0 * 8 + tid] = make_float4(c8[0], c8[1], c8[2], c8[3]);
+    jt[1 * 8 + tid] = make_float4(c8[4], c8[5], c8[6], c8[7]);
+    jt[2 * 8 + tid] = make_float4(s8[0], s8[1], s8[2], s8[3]);
+    jt[3 * 8 + tid] = make_float4(s8[4], s8[5], s8[6], s8[7]);
   }
   __syncthreads();  // barriers initialised, scan read by thread 0: the value area is free
   if (tid == 0)
-    for (int s = 0; s < kStages && ps->i < hi; ++s) prod_next(a, *ps, ring, full, lo, hi, n_pairs);
+    for (int s = 0; s < kStages && ps->cur.i < hi; ++s) prod_next(a, *ps, ring, full, lo, hi, n_pairs);
 
   const int s = tid & 7;                 // slot: groups s and s + 8
   const int o0 = (s & 4) ? 4 : 0;        // key half order (bank-quad spreading)
@@ -501,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
   const uint32_t vb0 = 16 * s, vb1 = 128 + 16 * s;
   const unsigned char* ksb = reinterpret_cast<const unsigned char*>(ks);
   const unsigned char* vsb = reinterpret_cast<const unsigned char*>(vs);
-  const float* jt = reinterpret_cast<const float*>(smem + kOffJ) + s * 16;
+  const float4* jt = reinterpret_cast<const float4*>(smem + kOffJ) + s;
 
   const int n_units = (int)(hi - lo);
   int cur_head = -1;
@@ -509,10 +515,39 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
   for (int i = 0; i < n_units; ++i) {
     const int st = i % kStages;
     wait_stage(&full[st], (i / kStages) & 1, failed, a.err);
-    unsigned char* stage = ring + st * kStageBytes;
+    // ---- everything this thread needs from the stage goes to registers, then the stage is
+    //      released: its refill overlaps this unit's work
+    const unsigned char* stage = ring + st * kStageBytes;
     const int4 hv0 = *reinterpret_cast<const int4*>(stage + kOffHdr);
     const int4 hv1 = *reinterpret_cast<const int4*>(stage + kOffHdr + 16);
     const int uh = hv0.x, upair = hv0.y, uc = hv0.z, uflags = hv0.w;
+    const int L = r ? hv1.z : hv1.x, NP = r ? hv1.w : hv1.y;
+    const int pg = uc * kChunk + po;
+    const bool active = !*failed && pg < NP;
+    const bool resync = (uflags & 1) || uc % kResync == 0;
+    uint4 rowk = make_uint4(0, 0, 0, 0), rowv = rowk;
+    float ql[8], qh[8];
+    if (active) {
+      rowk = *reinterpret_cast<const uint4*>(stage + r * kPart + po * kPageBytes + 16 * s);
+      rowv = *reinterpret_cast<const uint4*>(stage + (2 + r) * kPart + po * kPageBytes + 16 * s);
+      if (resync) {
+        const uint16_t* qr = reinterpret_cast<const uint16_t*>(stage + kOffQs) + r * kD;
+        lds8_bf16_perm(qr + 8 * s, o0, ql);
+        lds8_bf16_perm(qr + 64 + 8 * s, o0, qh);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      // the last warp done with this stage refills it with the unit kStages ahead: no warp
+      // waits to produce, and the copy starts as soon as the stage is free
+      if (atom_add_acq_rel_shared(&released[st], 1) == kWarps - 1) {
+        released[st] = 0;
+        if (!*failed && ps->cur.i < hi) {
+          fence_proxy_async_smem();
+          prod_next(a, *ps, ring, full, lo, hi, n_pairs);
+        }
+      }
+    }
 
     if (uh != cur_head) {  // uniform: every thread read the same header
       // ---- stage the codebook slices of head uh ----
@@ -525,17 +560,26 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
           bulk_g2s(ks + k * (kKSliceBytes / 16), btk + k * (kKSliceBytes / 16), kKSliceBytes / 4, kbar);
         ++ps->k_loads;
       }
-      {  // value slice: fp32 [2][256][64] in L2 -> fp16 [256][128] in shared memory
+      {  // value slice: fp32 [2][256][64] in L2 -> fp16 [256][128] in shared memory, 4 loads
+         // in flight per thread
         const float4* src = reinterpret_cast<const float4*>(a.bt_v + (size_t)uh * kCB * kD);
-        for (int j = tid; j < kCB * kD / 4; j += kThreads) {
-          const float4 v = __ldg(src + j);
-          const int half = j / (kCB * kD / 8), rem = j % (kCB * kD / 8);
-          const int row = rem / (kD / 8), c4 = rem % (kD / 8);
-          __half2 lo2 = __floats2half2_rn(v.x, v.y), hi2 = __floats2half2_rn(v.z, v.w);
-          uint2 w;
-          w.x = *reinterpret_cast<uint32_t*>(&lo2);
-          w.y = *reinterpret_cast<uint32_t*>(&hi2);
-          reinterpret_cast<uint2*>(vs + row * kD + half * (kD / 2))[c4] = w;
+        constexpr int kDeep = 4;
+        static_assert((kCB * kD / 4) % (kDeep * kThreads) == 0, "value staging batches");
+        for (int j0 = tid; j0 < kCB * kD / 4; j0 += kDeep * kThreads) {
+          float4 v[kDeep];
+#pragma unroll
+          for (int u = 0; u < kDeep; ++u) v[u] = __ldg(src + j0 + u * kThreads);
+#pragma unroll
+          for (int u = 0; u < kDeep; ++u) {
+            const int j = j0 + u * kThreads;
+            const int half = j / (kCB * kD / 8), rem = j % (kCB * kD / 8);
+            const int row = rem / (kD / 8), c4 = rem % (kD / 8);
+            __half2 lo2 = __floats2half2_rn(v[u].x, v[u].y), hi2 = __floats2half2_rn(v[u].z, v[u].w);
+            uint2 w;
+            w.x = *reinterpret_cast<uint32_t*>(&lo2);
+            w.y = *reinterpret_cast<uint32_t*>(&hi2);
+            reinterpret_cast<uint2*>(vs + row * kD + half * (kD / 2))[c4] = w;
+          }
         }
       }
       block_sync(bsync, sphase, failed, a.err);  // value slice complete
@@ -545,15 +589,21 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
     }
     if (uflags & 1) acc_reset(A);  // a new piece
 
-    const int L = r ? hv1.z : hv1.x, NP = r ? hv1.w : hv1.y;
-    const int pg = uc * kChunk + po;
-    if (!*failed && pg < NP) {
-      if ((uflags & 1) || uc % kResync == 0) {
-        const uint16_t* qr = reinterpret_cast<const uint16_t*>(stage + kOffQs) + r * kD;
-        rotated_query_bf16(a.rope_cos, a.rope_sin, L - 1 - (a.sink + kPage * pg), s, o0, qr, u0l, u0h);
+    if (active) {
+      if (resync) {  // u = R(p_q - p) q from the cos/sin table
+        const int d = L - 1 - (a.sink + kPage * pg);
+        float c8[8], s8[8];
+        ldg8_perm(a.rope_cos + (size_t)d * (kD / 2) + 8 * s, o0, c8);
+        ldg8_perm(a.rope_sin + (size_t)d * (kD / 2) + 8 * s, o0, s8);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          u0l[k] = make_float2(ql[2 * k] * c8[2 * k] - qh[2 * k] * s8[2 * k],
+                               ql[2 * k + 1] * c8[2 * k + 1] - qh[2 * k + 1] * s8[2 * k + 1]);
+          u0h[k] = make_float2(qh[2 * k] * c8[2 * k] + ql[2 * k] * s8[2 * k],
+                               qh[2 * k + 1] * c8[2 * k + 1] + ql[2 * k + 1] * s8[2 * k + 1]);
+        }
       } else {  // kJump positions later
-        const float4 c0 = *reinterpret_cast<const float4*>(jt), c1 = *reinterpret_cast<const float4*>(jt + 4);
-        const float4 s0 = *reinterpret_cast<const float4*>(jt + 8), s1 = *reinterpret_cast<const float4*>(jt + 12);
+        const float4 c0 = jt[0], c1 = jt[8], s0 = jt[16], s1 = jt[24];
         const float2 cj[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w), make_float2(c1.x, c1.y),
                               make_float2(c1.z, c1.w)};
         const float2 sj[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
@@ -562,7 +612,6 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
                                make_float2(-s1.z, -s1.w)};
         rotate8(u0l, u0h, cj, sj, nsj);
       }
-      const uint4 rowk = *reinterpret_cast<const uint4*>(stage + r * kPart + po * kPageBytes + 16 * s);
       float2 ul[4], uh2[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -599,7 +648,6 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
       }
       transpose_reduce8(part, s, gmask);
       const float p = online_weights(A, part[0] * scale_log2, gmask);
-      const uint4 rowv = *reinterpret_cast<const uint4*>(stage + (2 + r) * kPart + po * kPageBytes + 16 * s);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float pj = __shfl_sync(gmask, p, (lane & 24) + j);
@@ -619,60 +667,31 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
     }
 
     if (uflags & 2) {
-      // ---- end of a piece: lanes of a group (l), lane-groups (shuffles), warps (smem) ----
+      // ---- end of a piece: lanes of a group (l), lane-groups (shuffles); each warp writes
+      //      its partial (M, l, o[128]) for the window kernel to merge
       A.l += __shfl_xor_sync(0xFFFFFFFFu, A.l, 1);
       A.l += __shfl_xor_sync(0xFFFFFFFFu, A.l, 2);
       A.l += __shfl_xor_sync(0xFFFFFFFFu, A.l, 4);
       merge_lane_groups(A);
-      block_sync(bsync, sphase, failed, a.err);  // every warp is done with this stage's pages
-      float* wpart = reinterpret_cast<float*>(stage);  // [warp][130] = o[128], M, l
-      if (lane < 8) {
-        float* wp = wpart + warp * (kD + 2);
+      if (lane < 8 && 2 * upair + r < a.B) {
+        const int dest = uflags >> 2;
+        float* pp = (dest == 0) ? a.part_whole + ((size_t)uh * n_pairs + upair) * kVqPartFloats
+                                : a.part_slot + ((size_t)blk * 2 + (dest - 1)) * kVqPartFloats;
+        pp += (r * kVqWarpsPerReq + (warp & (kVqWarpsPerReq - 1))) * (kD + 2);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          reinterpret_cast<float2*>(wp + 8 * s)[k] = A.ol[k];
-          reinterpret_cast<float2*>(wp + 64 + 8 * s)[k] = A.oh[k];
+          reinterpret_cast<float2*>(pp + 2 + 8 * s)[k] = A.ol[k];
+          reinterpret_cast<float2*>(pp + 2 + 64 + 8 * s)[k] = A.oh[k];
         }
         if (lane == 0) {
-          wp[kD] = A.M;
-          wp[kD + 1] = A.l;
-        }
-        fence_proxy_async_smem();  // before the stage is refilled by TMA
-      }
-      block_sync(bsync, sphase, failed, a.err);
-      if (tid < 2 * kD) {  // thread (request rr, channel ch) merges the 8 warps of its request
-        const int rr = tid >> 7, ch = tid & 127;
-        float Mr = -INFINITY, Lr = 0.f, o = 0.f;
-        for (int w = rr * 8; w < rr * 8 + 8; ++w) Mr = fmaxf(Mr, wpart[w * (kD + 2) + kD]);
-        if (Mr != -INFINITY) {
-          for (int w = rr * 8; w < rr * 8 + 8; ++w) {
-            const float mw = wpart[w * (kD + 2) + kD];
-            if (mw == -INFINITY) continue;
-            const float f = exp2f(mw - Mr);
-            Lr = fmaf(f, wpart[w * (kD + 2) + kD + 1], Lr);
-            o = fmaf(f, wpart[w * (kD + 2) + ch], o);
-          }
-        }
-        if (2 * upair + rr < a.B) {
-          const int dest = uflags >> 2;
-          float* pp = (dest == 0) ? a.part_whole + ((size_t)uh * n_pairs + upair) * kVqPartFloats
-                                  : a.part_slot + ((size_t)blk * 2 + (dest - 1)) * kVqPartFloats;
-          pp += rr * (kD + 2);
-          pp[2 + ch] = o;
-          if (ch == 0) {
-            pp[0] = Mr;
-            pp[1] = Lr;
-          }
+          pp[0] = A.M;
+          pp[1] = A.l;
         }
       }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
-    if (tid == 0 && ps->i < hi) {  // producer: refill this stage with the unit kStages ahead
-      if (wait_stage(&empty[st], (i / kStages) & 1, failed, a.err)) prod_next(a, *ps, ring, full, lo, hi, n_pairs);
     }
   }
 
+  __syncthreads();  // every producer step is done
   // after a timeout, let the block's own copies in flight land before it exits
   if (tid == 0 && *failed) {
     const int issued = ps->issued;
@@ -774,6 +793,9 @@ __global__ void __launch_bounds__(kWThreads) vq_window_kernel(const VqAttnArgs a
 #pragma unroll
   for (int w = 0; w < kWThreads / 32; ++w) fold(wpart[w][kD], wpart[w][kD + 1], wpart[w][ch]);
 
+  // the page kernel's prefix and partials: wait for that grid (a no-op without a
+  // programmatic dependency)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int n_pairs = (a.B + 1) / 2, pair = b >> 1, rr = b & 1;
   const int p0 = a.pref[pair], nu = a.pref[pair + 1] - p0;
   if (nu > 0) {
@@ -781,15 +803,18 @@ __global__ void __launch_bounds__(kWThreads) vq_window_kernel(const VqAttnArgs a
     const long long U = (long long)a.H * Up;
     const long long s0 = (long long)h * Up + p0, s1 = s0 + nu;
     const int k0 = share_of(s0, U, a.G), k1 = share_of(s1 - 1, U, a.G);
+    auto fold_piece = [&](const float* pp) {  // the 8 warp partials of this request
+      pp += rr * kVqWarpsPerReq * (kD + 2);
+#pragma unroll
+      for (int w = 0; w < kVqWarpsPerReq; ++w) fold(pp[w * (kD + 2)], pp[w * (kD + 2) + 1], pp[w * (kD + 2) + 2 + ch]);
+    };
     if (k0 == k1) {
-      const float* pp = a.part_whole + ((size_t)h * n_pairs + pair) * kVqPartFloats + rr * (kD + 2);
-      fold(pp[0], pp[1], pp[2 + ch]);
+      fold_piece(a.part_whole + ((size_t)h * n_pairs + pair) * kVqPartFloats);
     } else {
       for (int kk = k0; kk <= k1; ++kk) {
         const long long lk = share_lo(U, kk, a.G);
         if (lk == share_lo(U, kk + 1, a.G)) continue;  // an empty share
-        const float* pp = a.part_slot + ((size_t)kk * 2 + (lk >= s0 ? 0 : 1)) * kVqPartFloats + rr * (kD + 2);
-        fold(pp[0], pp[1], pp[2 + ch]);
+        fold_piece(a.part_slot + ((size_t)kk * 2 + (lk >= s0 ? 0 : 1)) * kVqPartFloats);
       }
     }
   }
@@ -825,8 +850,18 @@ cudaError_t launch_vq_attn(const VqAttnArgs& args, void* ws, cudaStream_t st) {
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)kD);
   vq_pages_kernel<<<a.G, kThreads, kSmemBytes, st>>>(a, scale_log2);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  vq_window_kernel<<<(unsigned)(a.B * a.H), kWThreads, 0, st>>>(a, scale_log2);
-  return cudaGetLastError();
+  // programmatic dependent launch: the window kernel may start before the page kernel ends
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)(a.B * a.H));
+  lc.blockDim = dim3(kWThreads);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, vq_window_kernel, a, scale_log2);
 }
 
 }  // namespace kvq

@@ -46,7 +46,7 @@ def test_noalloc_matches_workspace_call_twice(n_splits):
 
 
 def test_noalloc_rejects_calls_beyond_the_reserved_scratch():
-    # 4096 page-kernel blocks keep two partial slots each (2 x 1040 B): 8.5 MB, over the
+    # 4096 page-kernel blocks keep two piece slots each (2 x 8320 B): 68 MB, over the
     # reserved array, so the call is refused before anything launches
     cfg = kvq.VqConfig(n_heads=16, max_pages=4063, max_batch=64, max_ctx=32768, recent=256, Tc=4, G=32)
     need = kvq.kvq_decode_workspace_size(cfg, 64, 4096)

@@ -194,11 +194,12 @@ def cpu_oracle(wl, bytes_per_unit, unit_pairs_total, n_pairs, pool=None):
 
 def vq_call_bytes(B, H, n_pages, n_win, NB_unused=None):
     """Algorithmic bytes of one LoopVQ decode-attention call (one layer, one loop step):
-    K and V index pages, bf16 window K and V, both fp32 codebook slices, the cos/sin rows the
-    call needs (one per page start and per window token), query and bf16 output."""
+    K and V index pages, bf16 window K and V, the fp32 key and fp16 value codebook slices,
+    the cos/sin rows the call needs (one per page start and per window token), query and
+    bf16 output."""
     idx = B * H * n_pages * 128 * 2
     win = B * H * n_win * D * 2 * 2
-    bt = H * 256 * D * 4 * 2
+    bt = H * 256 * D * (4 + 2)
     rope = (n_pages + n_win) * (D // 2) * 4 * 2
     qo = B * H * D * 2 * 2
     return idx + win + bt + rope + qo

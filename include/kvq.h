@@ -91,11 +91,14 @@ typedef struct {
  * win_k, win_v  bf16   [n_layers][T][max_batch][n_heads][sink + recent + 8][D]
  *     Pre-RoPE keys / values of the bf16 tokens at each loop step. Position p < sink sits
  *     in slot p; a recent position p in slot sink + (p - sink) mod (recent + 8).
- * bt_k, bt_v    fp32   [n_layers][T][n_heads][2][K][D/2]
- *     Per-loop-step codebook slices B_t, cut once by kvq_slice_codebooks. Channel
+ * bt_k          fp32   [n_layers][T][n_heads][2][K][D/2]
+ *     Per-loop-step key codebook slices B_t, cut once by kvq_slice_codebooks. Channel
  *     ch = g*c + i of codeword r sits in half ch / (D/2) at column ch % (D/2):
  *     bt[l][t][h][ch/(D/2)][r][ch%(D/2)] = cb[l][beta][h][g][r][i*Tc + m],
  *     beta = (t-1)/Tc, m = (t-1)%Tc. (The halves hold the RoPE partner channels.)
+ * bt_v          fp16   [n_layers][T][n_heads][K][D]
+ *     Per-loop-step value codebook slices, cut once by kvq_slice_codebooks_fp16 and
+ *     rounded to fp16 (nearest even): bt_v[l][t][h][r][ch] = fp16(cb[l][beta][h][g][r][i*Tc + m]).
  * cb_k, cb_v    fp32   [n_layers][NB][n_heads][NG][K][G]   full codebooks (encode, roll)
  * rope_cos, rope_sin fp32 [max_ctx][D/2]: cos / sin(p * base^(-2i/D)) (kvq_rope_table)
  * seq_len       int32  [max_batch]: tokens cached per request, including the newest one
@@ -108,7 +111,7 @@ typedef struct {
   uint16_t* win_k;
   uint16_t* win_v;
   float* bt_k;
-  float* bt_v;
+  uint16_t* bt_v;
   const float* cb_k;
   const float* cb_v;
   const float* rope_cos;
@@ -118,10 +121,10 @@ typedef struct {
 } kvq_vq_cache;
 
 /* Byte sizes of each buffer of kvq_vq_cache for `cfg` (host-only, no device work).
- * Order: idx (each of k, v), win (each), bt (each), cb (each), rope (each of cos, sin),
- * per-request int32 arrays (each). Returns KVQ_ERR_INVALID_ARG for an invalid cfg. */
+ * Order: idx (each of k, v), win (each), bt (bt_k), bt_v, cb (each), rope (each of cos,
+ * sin), per-request int32 arrays (each). Returns KVQ_ERR_INVALID_ARG for an invalid cfg. */
 typedef struct {
-  size_t idx, win, bt, cb, rope, per_request;
+  size_t idx, win, bt, bt_v, cb, rope, per_request;
 } kvq_vq_sizes;
 kvq_status kvq_vq_cache_sizes(const kvq_vq_cfg* cfg, kvq_vq_sizes* out /* host */);
 
@@ -136,6 +139,13 @@ kvq_status kvq_rope_table(const kvq_vq_cfg* cfg, float* rope_cos, float* rope_si
  * slice). cb: [n_layers][NB][n_heads][NG][K][G]; bt: [n_layers][T][n_heads][2][K][D/2]
  * (layout in kvq_vq_cache). */
 kvq_status kvq_slice_codebooks(const kvq_vq_cfg* cfg, const float* cb, float* bt, kvq_stream stream);
+
+/* The same cut for the value codebooks, rounded to fp16 (round to nearest even) in codeword
+ * rows of natural channel order: bt16 is [n_layers][T][n_heads][K][D] (layout of bt_v in
+ * kvq_vq_cache). Decode attention accumulates values from these fp16 rows; the rounding
+ * (relative 2^-11 per entry) is far inside the attention output tolerance. */
+kvq_status kvq_slice_codebooks_fp16(const kvq_vq_cfg* cfg, const float* cb, uint16_t* bt16,
+                                    kvq_stream stream);
 
 /* Nearest-codeword encode of coupled vectors (LoopVQ background: a(z) = argmin_r
  * ||z - e_r||^2; method step 1 for the coupling, method step 4 for prefill encoding).

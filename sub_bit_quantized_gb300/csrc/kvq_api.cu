@@ -185,6 +185,7 @@ KVQ_API kvq_status kvq_vq_cache_sizes(const kvq_vq_cfg* c, kvq_vq_sizes* out) {
   out->idx = (size_t)c->n_layers * NB * c->max_batch * c->n_heads * c->max_pages * (8 * NG);
   out->win = (size_t)c->n_layers * c->T * c->max_batch * c->n_heads * win_slots(c) * c->D * 2;
   out->bt = (size_t)c->n_layers * c->T * c->n_heads * c->K * c->D * 4;
+  out->bt_v = (size_t)c->n_layers * c->T * c->n_heads * c->K * c->D * 2;
   out->cb = (size_t)c->n_layers * NB * c->n_heads * NG * c->K * c->G * 4;
   out->rope = (size_t)c->max_ctx * (c->D / 2) * 4;
   out->per_request = (size_t)c->max_batch * 4;
@@ -208,6 +209,17 @@ KVQ_API kvq_status kvq_slice_codebooks(const kvq_vq_cfg* c, const float* cb, flo
   return cuda_status(
       kvq::launch_slice_codebooks(cb, bt, c->n_layers, c->T, c->Tc, c->G, c->n_heads, (cudaStream_t)stream),
       __func__);
+}
+
+KVQ_API kvq_status kvq_slice_codebooks_fp16(const kvq_vq_cfg* c, const float* cb, uint16_t* bt16,
+                                            kvq_stream stream) {
+  kvq_status st = check_vq_cfg(c, __func__);
+  if (st != KVQ_OK) return st;
+  CHECK_PTR(cb);
+  CHECK_PTR(bt16);
+  return cuda_status(kvq::launch_slice_codebooks_fp16(cb, bt16, c->n_layers, c->T, c->Tc, c->G, c->n_heads,
+                                                      (cudaStream_t)stream),
+                     __func__);
 }
 
 static kvq_status check_x_strides(const char* fn, int64_t st, int64_t sb, int64_t sh) {

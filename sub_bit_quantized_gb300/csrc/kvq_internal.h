@@ -36,7 +36,7 @@ struct VqAttnArgs {
   const uint16_t* win_k;     // [max_batch][H][win_slots][D] of (layer, step)
   const uint16_t* win_v;
   const float* bt_k;         // [H][2][256][D/2] of (layer, step)
-  const float* bt_v;
+  const uint16_t* bt_v;      // fp16 [H][256][D] of (layer, step)
   const float* rope_cos;     // [max_ctx][D/2]
   const float* rope_sin;
   const int32_t* seq_len;    // [max_batch]
@@ -71,6 +71,8 @@ cudaError_t launch_vq_encode(const VqEncodeArgs& a, cudaStream_t s);
 cudaError_t launch_rope_table(float* cos_t, float* sin_t, int max_ctx, int D, float base, cudaStream_t s);
 cudaError_t launch_slice_codebooks(const float* cb, float* bt, int L, int T, int Tc, int G, int H,
                                    cudaStream_t s);
+cudaError_t launch_slice_codebooks_fp16(const float* cb, uint16_t* bt16, int L, int T, int Tc, int G, int H,
+                                        cudaStream_t s);
 
 struct VqWindowArgs {              // copy prefill tokens into the bf16 windows
   const uint16_t* xk; const uint16_t* xv;

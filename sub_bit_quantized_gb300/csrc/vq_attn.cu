@@ -16,9 +16,9 @@
 // per block, so every SM gets the same number of pages whatever the batch mix, and a block
 // restages the codebook slices only when its share crosses into the next head (at most
 // twice for the usual shapes).
-//  * Both slices stay resident: keys in fp32 (128 KB, TMA bulk copy; channels 0..63 and
-//    64..127 as two [256][64] tables), values in fp16 ([256][128], converted while
-//    staging; value rounding error ~1e-4 of the output). A codeword's shared-memory address
+//  * Both slices stay resident, staged by TMA bulk copies: keys in fp32 (128 KB; channels
+//    0..63 and 64..127 as two [256][64] tables), values in fp16 as the cache stores them
+//    ([256][128]; value rounding error ~1e-4 of the output). A codeword's shared-memory address
 //    is one byte permute: (index << 8) | lane offset, and every lookup is a 128-bit load.
 //  * The units stream through a 2-stage ring with TMA bulk copies: 32 key and 32 value
 //    pages of each request, the two bf16 queries and a header naming the unit. A full
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
     for (int hh = P.h; hh <= h_last; ++hh)
       for (int k = 0; k < 4; ++k) {
         bulk_prefetch_l2(a.bt_k + (size_t)hh * kCB * kD + k * (kCB * kD / 4), kKSliceBytes / 4);
-        bulk_prefetch_l2(a.bt_v + (size_t)hh * kCB * kD + k * (kCB * kD / 4), kKSliceBytes / 4);
+        bulk_prefetch_l2(a.bt_v + (size_t)hh * kCB * kD + k * (kCB * kD / 4), kVSliceBytes / 4);
       }
   }
   if (tid < 8 && a.max_ctx > kJump) {
@@ -552,37 +552,17 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
     if (uh != cur_head) {  // uniform: every thread read the same header
       // ---- stage the codebook slices of head uh ----
       block_sync(bsync, sphase, failed, a.err);  // every warp is done with the old slices
-      if (tid == 0 && !*failed) {
+      if (tid == 0 && !*failed) {  // both slices by TMA: fp32 keys 128 KB, fp16 values 64 KB
         const float* btk = a.bt_k + (size_t)uh * kCB * kD;
-        mbar_arrive_expect_tx(kbar, kKSliceBytes);
+        const uint16_t* btv = a.bt_v + (size_t)uh * kCB * kD;
+        mbar_arrive_expect_tx(kbar, kKSliceBytes + kVSliceBytes);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < 4; ++k) {
           bulk_g2s(ks + k * (kKSliceBytes / 16), btk + k * (kKSliceBytes / 16), kKSliceBytes / 4, kbar);
+          bulk_g2s(vs + k * (kVSliceBytes / 8), btv + k * (kVSliceBytes / 8), kVSliceBytes / 4, kbar);
+        }
         ++ps->k_loads;
       }
-      {  // value slice: fp32 [2][256][64] in L2 -> fp16 [256][128] in shared memory, 4 loads
-         // in flight per thread
-        const float4* src = reinterpret_cast<const float4*>(a.bt_v + (size_t)uh * kCB * kD);
-        constexpr int kDeep = 4;
-        static_assert((kCB * kD / 4) % (kDeep * kThreads) == 0, "value staging batches");
-        for (int j0 = tid; j0 < kCB * kD / 4; j0 += kDeep * kThreads) {
-          float4 v[kDeep];
-#pragma unroll
-          for (int u = 0; u < kDeep; ++u) v[u] = __ldg(src + j0 + u * kThreads);
-#pragma unroll
-          for (int u = 0; u < kDeep; ++u) {
-            const int j = j0 + u * kThreads;
-            const int half = j / (kCB * kD / 8), rem = j % (kCB * kD / 8);
-            const int row = rem / (kD / 8), c4 = rem % (kD / 8);
-            __half2 lo2 = __floats2half2_rn(v[u].x, v[u].y), hi2 = __floats2half2_rn(v[u].z, v[u].w);
-            uint2 w;
-            w.x = *reinterpret_cast<uint32_t*>(&lo2);
-            w.y = *reinterpret_cast<uint32_t*>(&hi2);
-            reinterpret_cast<uint2*>(vs + row * kD + half * (kD / 2))[c4] = w;
-          }
-        }
-      }
-      block_sync(bsync, sphase, failed, a.err);  // value slice complete
       wait_stage(kbar, kphase, failed, a.err);
       kphase ^= 1u;
       cur_head = uh;

@@ -14,6 +14,8 @@
 // 4e-6 (relative) of the fp32 minimum is re-evaluated in fp64, where bf16 inputs and fp32
 // entries subtract and square exactly. The result is the exact-arithmetic argmin with the
 // lowest index on ties; a second-best fp64 distance within 1e-6 of the best counts as a tie.
+#include <cuda_fp16.h>
+
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
 #include "../../include/kvq.h"
@@ -52,6 +54,23 @@ __global__ void slice_kernel(const float* __restrict__ cb, float* __restrict__ b
     const int ch = half * (kD / 2) + col;
     const int beta = t0 / Tc, m = t0 % Tc, g = ch / c, i = ch % c;
     bt[k] = cb[((((size_t)l * NB + beta) * H + h) * NG + g) * (size_t)kCB * G + (size_t)r * G + i * Tc + m];
+  }
+}
+
+// value slices in fp16 codeword rows: bt16[l][t][h][r][ch]
+__global__ void slice_fp16_kernel(const float* __restrict__ cb, __half* __restrict__ bt16, int L, int T, int Tc,
+                                  int G, int H) {
+  const int c = G / Tc, NG = kD / c, NB = T / Tc;
+  const long long n = (long long)L * T * H * kCB * kD;
+  for (long long k = blockIdx.x * (long long)blockDim.x + threadIdx.x; k < n; k += (long long)gridDim.x * blockDim.x) {
+    long long q = k;
+    const int ch = (int)(q % kD); q /= kD;
+    const int r = (int)(q % kCB); q /= kCB;
+    const int h = (int)(q % H); q /= H;
+    const int t0 = (int)(q % T); q /= T;  // 0-based step
+    const int l = (int)q;
+    const int beta = t0 / Tc, m = t0 % Tc, g = ch / c, i = ch % c;
+    bt16[k] = __float2half_rn(cb[((((size_t)l * NB + beta) * H + h) * NG + g) * (size_t)kCB * G + (size_t)r * G + i * Tc + m]);
   }
 }
 
@@ -287,6 +306,13 @@ cudaError_t launch_rope_table(float* cos_t, float* sin_t, int max_ctx, int D, fl
 cudaError_t launch_slice_codebooks(const float* cb, float* bt, int L, int T, int Tc, int G, int H,
                                    cudaStream_t s) {
   slice_kernel<<<grid_for((long long)L * T * H * kCB * kD, 256), 256, 0, s>>>(cb, bt, L, T, Tc, G, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_slice_codebooks_fp16(const float* cb, uint16_t* bt16, int L, int T, int Tc, int G, int H,
+                                        cudaStream_t s) {
+  slice_fp16_kernel<<<grid_for((long long)L * T * H * kCB * kD, 256), 256, 0, s>>>(
+      cb, reinterpret_cast<__half*>(bt16), L, T, Tc, G, H);
   return cudaGetLastError();
 }
 

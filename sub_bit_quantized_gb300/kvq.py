@@ -46,7 +46,7 @@ class VqCacheC(ctypes.Structure):
 
 
 class VqSizes(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_size_t) for n in ("idx", "win", "bt", "cb", "rope", "per_request")]
+    _fields_ = [(n, ctypes.c_size_t) for n in ("idx", "win", "bt", "bt_v", "cb", "rope", "per_request")]
 
 
 class KiviCfg(ctypes.Structure):
@@ -73,6 +73,7 @@ _SIGS = {
     "kvq_vq_cache_sizes": (_I, [_P, _P]),
     "kvq_rope_table": (_I, [_P, _P, _P, _P]),
     "kvq_slice_codebooks": (_I, [_P, _P, _P, _P]),
+    "kvq_slice_codebooks_fp16": (_I, [_P, _P, _P, _P]),
     "kvq_encode_vq": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P]),
     "kvq_prefill_vq": (_I, [_P, _P, _I, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _P]),
     "kvq_append_page": (_I, [_P, _P, _I, _I, _P, _P, _I, _P]),
@@ -206,7 +207,7 @@ class VqCache:
         self.win_k = torch.zeros((L, c.T, B, H, c.win_slots, c.D), dtype=torch.bfloat16, device=dev)
         self.win_v = torch.zeros_like(self.win_k)
         self.bt_k = torch.zeros((L, c.T, H, 2, c.K, c.D // 2), dtype=torch.float32, device=dev)
-        self.bt_v = torch.zeros_like(self.bt_k)
+        self.bt_v = torch.zeros((L, c.T, H, c.K, c.D), dtype=torch.float16, device=dev)
         self.cb_k = torch.zeros((L, NB, H, c.NG, c.K, c.G), dtype=torch.float32, device=dev)
         self.cb_v = torch.zeros_like(self.cb_k)
         self.rope_cos = torch.empty((c.max_ctx, c.D // 2), dtype=torch.float32, device=dev)
@@ -216,7 +217,8 @@ class VqCache:
         self._cfg_c = cfg.to_c()
         sizes = vq_cache_sizes(cfg)
         assert sizes.idx == self.idx_k.numel() and sizes.win == self.win_k.numel() * 2
-        assert sizes.bt == self.bt_k.numel() * 4 and sizes.cb == self.cb_k.numel() * 4
+        assert sizes.bt == self.bt_k.numel() * 4 and sizes.bt_v == self.bt_v.numel() * 2
+        assert sizes.cb == self.cb_k.numel() * 4
         kvq_rope_table(cfg, self.rope_cos, self.rope_sin)
 
     def c_struct(self) -> VqCacheC:
@@ -228,7 +230,7 @@ class VqCache:
         self.cb_k.copy_(cb_k)
         self.cb_v.copy_(cb_v)
         kvq_slice_codebooks(self.cfg, self.cb_k, self.bt_k, stream)
-        kvq_slice_codebooks(self.cfg, self.cb_v, self.bt_v, stream)
+        kvq_slice_codebooks_fp16(self.cfg, self.cb_v, self.bt_v, stream)
 
 
 def vq_cache_sizes(cfg: VqConfig) -> VqSizes:
@@ -248,6 +250,12 @@ def kvq_slice_codebooks(cfg: VqConfig, cb, bt, stream=None):
     c = cfg.to_c()
     _check(lib().kvq_slice_codebooks(ctypes.byref(c), _ptr(cb), _ptr(bt), _stream(stream)),
            "kvq_slice_codebooks")
+
+
+def kvq_slice_codebooks_fp16(cfg: VqConfig, cb, bt16, stream=None):
+    c = cfg.to_c()
+    _check(lib().kvq_slice_codebooks_fp16(ctypes.byref(c), _ptr(cb), _ptr(bt16), _stream(stream)),
+           "kvq_slice_codebooks_fp16")
 
 
 def kvq_encode_vq(cfg: VqConfig, x, x_strides, seq_begin, n_seq, n_tok, cb, idx, page_begin=0,

@@ -46,6 +46,7 @@ def test_cache_sizes_formula(L):
     assert s.idx == 24 * 2 * 64 * 16 * 759 * 128
     assert s.win == 24 * 4 * 64 * 16 * 80 * 128 * 2
     assert s.bt == 24 * 4 * 16 * 256 * 128 * 4
+    assert s.bt_v == 24 * 4 * 16 * 256 * 128 * 2
     assert s.cb == 24 * 2 * 16 * 16 * 256 * 16 * 4
     assert s.rope == 6144 * 64 * 4 and s.per_request == 64 * 4
     # one call reads one (layer, block) of each index array: 199.0 MB at B=64, 6K

@@ -26,8 +26,9 @@ constexpr int kPageBytes = kPage * kNG;
 // holding the block's first unit) or part_slot[k][1] (the piece holding its last). The
 // window kernel attends the bf16 sink/recent tokens of every (request, head) and merges
 // them with the pieces.
-constexpr int kVqChunk = 32;   // index pages of each request per work unit
-constexpr int kVqWarpsPerReq = 8;                          // page-kernel warps per request
+constexpr int kVqThreads = 512;                 // page-kernel block: 8 lanes per index page
+constexpr int kVqChunk = kVqThreads / 16;       // index pages of each request per work unit
+constexpr int kVqWarpsPerReq = kVqThreads / 64; // page-kernel warps per request
 constexpr int kVqPartFloats = 2 * kVqWarpsPerReq * (kD + 2);  // one piece: [request][warp][M, l, o[128]]
 
 struct VqAttnArgs {

@@ -12,8 +12,9 @@
 // every key 6 FMAs per channel pair, so the work is bound on chip, not by HBM. Two kernels:
 //
 // vq_pages_kernel: persistent, one 512-thread block per SM. The work units (head, request
-// pair, chunk of 32 index pages), head-major, are cut into G equal contiguous shares, one
-// per block, so every SM gets the same number of pages whatever the batch mix, and a block
+// pair, chunk of kVqChunk = 32 index pages), head-major, are cut into G equal contiguous
+// shares, one per block, so every SM gets the same number of pages whatever the batch mix,
+// and a block
 // restages the codebook slices only when its share crosses into the next head (at most
 // twice for the usual shapes).
 //  * Both slices stay resident, staged by TMA bulk copies: keys in fp32 (128 KB; channels
@@ -49,7 +50,7 @@
 namespace kvq {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = kVqThreads;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = kVqChunk;                          // pages of each request per unit
 constexpr int kStages = 2;
@@ -72,7 +73,6 @@ constexpr int kOffBar = kOffProd + 64;                    // mbarriers + flags
 constexpr int kSmemBytes = kOffBar + 128;
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kOffBar % 8 == 0 && kOffRing % 128 == 0 && kStageBytes % 128 == 0, "alignment");
-static_assert(kWarps * (kD + 2) * 4 <= (int)kOffHdr, "piece merge scratch fits in a stage");
 constexpr int kMaxPairs = (int)(kVSliceBytes / 4) - 1;    // unit scan runs in the value-slice area
 
 __device__ __forceinline__ void ldg8_perm(const float* p, int o0, float (&v)[8]) {
@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
   const int o0 = (s & 4) ? 4 : 0;        // key half order (bank-quad spreading)
   const unsigned gmask = 0xFFu << (lane & 24);
   const int lg = tid >> 3;
-  const int r = lg >> 5, po = lg & 31;   // this lane-group's request and page slot
+  const int r = lg / kChunk, po = lg % kChunk;  // this lane-group's request and page slot
 
   float2 cth[4], sth[4], nsth[4];
   {
@@ -657,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
         const int dest = uflags >> 2;
         float* pp = (dest == 0) ? a.part_whole + ((size_t)uh * n_pairs + upair) * kVqPartFloats
                                 : a.part_slot + ((size_t)blk * 2 + (dest - 1)) * kVqPartFloats;
-        pp += (r * kVqWarpsPerReq + (warp & (kVqWarpsPerReq - 1))) * (kD + 2);
+        pp += (r * kVqWarpsPerReq + (warp - r * kVqWarpsPerReq)) * (kD + 2);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           reinterpret_cast<float2*>(pp + 2 + 8 * s)[k] = A.ol[k];

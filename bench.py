@@ -283,7 +283,9 @@ def kivi_call_bytes(B, H, NQ, NR):
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch from an ncu capture,
 # valid only for the kernel source it was taken on (profiles/ holds the capture summary)
 PROFILED_TRAFFIC = {
-    "vq_pages_kernel+vq_window_kernel": ("sub_bit_quantized_gb300/csrc/vq_attn.cu", None, None),
+    "vq_pages_kernel+vq_window_kernel": ("sub_bit_quantized_gb300/csrc/vq_attn.cu",
+                                         "2957b85af7697c08d1211f09aae0e4e37f0d28646c882d637e7a7e317753516e",
+                                         210055424 + 43537664),
 }
 
 

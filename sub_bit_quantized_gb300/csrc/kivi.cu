@@ -49,76 +49,102 @@ __device__ __forceinline__ uint32_t quant_code(float x, const GroupQ& g) {
 
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 
-// keys: one thread per (b, h, token group, channel); 32 channels per warp
-__global__ void kivi_quant_channel_kernel(const KiviQuantArgs a) {
-  const int D = kD;
-  const int n_groups = a.n_tok / a.group;
-  const long long total = (long long)a.B * a.H * n_groups * D;
-  for (long long k = blockIdx.x * (long long)blockDim.x + threadIdx.x; k < total;
-       k += (long long)gridDim.x * blockDim.x) {
-    const int ch = (int)(k % D);
-    long long q = k / D;
-    const int gi = (int)(q % n_groups);
-    q /= n_groups;
+// keys: one warp per (b, h, 32-token group); lane l owns channels 4l..4l+3, so each of the 32
+// token rows is one coalesced 256-byte read (8 bytes per lane), all 32 in flight at once
+__global__ void __launch_bounds__(256) kivi_quant_channel_kernel(const KiviQuantArgs a) {
+  constexpr int kG = 32;  // tokens per key group (checked by the caller)
+  const int lane = threadIdx.x & 31;
+  const int n_groups = a.n_tok / kG;
+  const long long total = (long long)a.B * a.H * n_groups;
+  for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; w < total;
+       w += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const int gi = (int)(w % n_groups);
+    const long long q = w / n_groups;
     const int h = (int)(q % a.H);
     const int b = (int)(q / a.H);
-    const uint16_t* xp = a.x + (size_t)b * a.sb + (size_t)h * a.sh + (size_t)gi * a.group * D + ch;
-    float v[32];
-    float mn = INFINITY, mx = -INFINITY;
+    const uint16_t* xp = a.x + (size_t)b * a.sb + (size_t)h * a.sh + (size_t)gi * kG * kD + 4 * lane;
+    uint2 raw[kG];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      v[j] = h2f(__ldg(xp + (size_t)j * D));
-      mn = fminf(mn, v[j]);
-      mx = fmaxf(mx, v[j]);
+    for (int j = 0; j < kG; ++j) raw[j] = __ldg(reinterpret_cast<const uint2*>(xp + (size_t)j * kD));
+    float mn[4], mx[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      mn[i] = INFINITY;
+      mx[i] = -INFINITY;
     }
-    const GroupQ g = group_params(mn, mx);
-    const int tg = a.tok_begin / a.group + gi;  // global token group
-    const size_t sz = (((size_t)b * a.H + h) * (a.max_tokens / a.group) + tg) * D + ch;
-    a.scale[sz] = g.s_bits;
-    a.zero[sz] = g.z_bits;
-    uint8_t* cp = a.codes + (((size_t)b * a.H + h) * a.max_tokens + a.tok_begin + (size_t)gi * a.group) * (D / 4);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      uint32_t c = quant_code(v[j], g) << (2 * (ch & 3));
-      c |= __shfl_xor_sync(0xFFFFFFFFu, c, 1);
-      c |= __shfl_xor_sync(0xFFFFFFFFu, c, 2);
-      if ((ch & 3) == 0) cp[(size_t)j * (D / 4) + (ch >> 2)] = (uint8_t)c;
+    for (int j = 0; j < kG; ++j) {
+      const float v[4] = {h2f(raw[j].x & 0xFFFFu), h2f(raw[j].x >> 16), h2f(raw[j].y & 0xFFFFu), h2f(raw[j].y >> 16)};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        mn[i] = fminf(mn[i], v[i]);
+        mx[i] = fmaxf(mx[i], v[i]);
+      }
+    }
+    GroupQ g[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) g[i] = group_params(mn[i], mx[i]);
+    const int tg = a.tok_begin / kG + gi;  // global token group
+    const size_t sz = (((size_t)b * a.H + h) * (a.max_tokens / kG) + tg) * kD + 4 * lane;
+    *reinterpret_cast<uint2*>(a.scale + sz) =
+        make_uint2(g[0].s_bits | ((uint32_t)g[1].s_bits << 16), g[2].s_bits | ((uint32_t)g[3].s_bits << 16));
+    *reinterpret_cast<uint2*>(a.zero + sz) =
+        make_uint2(g[0].z_bits | ((uint32_t)g[1].z_bits << 16), g[2].z_bits | ((uint32_t)g[3].z_bits << 16));
+    uint8_t* cp = a.codes + (((size_t)b * a.H + h) * a.max_tokens + a.tok_begin + (size_t)gi * kG) * (kD / 4) + lane;
+#pragma unroll
+    for (int j = 0; j < kG; ++j) {
+      const float v[4] = {h2f(raw[j].x & 0xFFFFu), h2f(raw[j].x >> 16), h2f(raw[j].y & 0xFFFFu), h2f(raw[j].y >> 16)};
+      uint32_t byte = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) byte |= quant_code(v[i], g[i]) << (2 * i);
+      cp[(size_t)j * (kD / 4)] = (uint8_t)byte;
     }
   }
 }
 
-// values: one warp per (b, h, token, channel group); lane = channel in the group
-__global__ void kivi_quant_token_kernel(const KiviQuantArgs a) {
-  const int D = kD;
-  const int ng = D / a.group;
+// values: a group is 32 channels of one token; 8 lanes per group (lane l owns channels
+// 4l..4l+3), so a warp covers one 256-byte token row per step; 4 rows are loaded per step
+__global__ void __launch_bounds__(256) kivi_quant_token_kernel(const KiviQuantArgs a) {
+  constexpr int kRows = 4;
   const int lane = threadIdx.x & 31;
-  const long long total = (long long)a.B * a.H * a.n_tok * ng;
-  for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; w < total;
+  const int gi = lane >> 3;  // channel group of this lane (32 channels = 8 lanes)
+  const long long rows = (long long)a.B * a.H * a.n_tok;
+  const long long n_steps = (rows + kRows - 1) / kRows;
+  for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; w < n_steps;
        w += ((long long)gridDim.x * blockDim.x) >> 5) {
-    const int gi = (int)(w % ng);
-    long long q = w / ng;
-    const int j = (int)(q % a.n_tok);
-    q /= a.n_tok;
-    const int h = (int)(q % a.H);
-    const int b = (int)(q / a.H);
-    const int ch = gi * a.group + lane;
-    const float x = h2f(__ldg(a.x + (size_t)b * a.sb + (size_t)h * a.sh + (size_t)j * D + ch));
-    float mn = x, mx = x;
+    uint2 raw[kRows];
+    size_t tok[kRows];
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, off));
-      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+    for (int u = 0; u < kRows; ++u) {
+      const long long r = min(w * kRows + u, rows - 1);
+      const int j = (int)(r % a.n_tok);
+      const long long q = r / a.n_tok;
+      const int h = (int)(q % a.H);
+      const int b = (int)(q / a.H);
+      raw[u] = __ldg(reinterpret_cast<const uint2*>(a.x + (size_t)b * a.sb + (size_t)h * a.sh + (size_t)j * kD + 4 * lane));
+      tok[u] = ((size_t)b * a.H + h) * a.max_tokens + a.tok_begin + j;
     }
-    const GroupQ g = group_params(mn, mx);
-    const size_t tok = ((size_t)b * a.H + h) * a.max_tokens + a.tok_begin + j;
-    if (lane == 0) {
-      a.scale[tok * ng + gi] = g.s_bits;
-      a.zero[tok * ng + gi] = g.z_bits;
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) {
+      if (w * kRows + u >= rows) break;  // uniform across the warp
+      const float v[4] = {h2f(raw[u].x & 0xFFFFu), h2f(raw[u].x >> 16), h2f(raw[u].y & 0xFFFFu), h2f(raw[u].y >> 16)};
+      float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
+      float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+#pragma unroll
+      for (int off = 4; off >= 1; off >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, off));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+      }
+      const GroupQ g = group_params(mn, mx);
+      if ((lane & 7) == 0) {
+        a.scale[tok[u] * (kD / 32) + gi] = g.s_bits;
+        a.zero[tok[u] * (kD / 32) + gi] = g.z_bits;
+      }
+      uint32_t byte = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) byte |= quant_code(v[i], g) << (2 * i);
+      a.codes[tok[u] * (kD / 4) + lane] = (uint8_t)byte;
     }
-    uint32_t c = quant_code(x, g) << (2 * (lane & 3));
-    c |= __shfl_xor_sync(0xFFFFFFFFu, c, 1);
-    c |= __shfl_xor_sync(0xFFFFFFFFu, c, 2);
-    if ((lane & 3) == 0) a.codes[tok * (D / 4) + (ch >> 2)] = (uint8_t)c;
   }
 }
 
@@ -321,17 +347,16 @@ size_t kivi_attn_smem_bytes(int tok_per_split, int residual) {
 }
 
 cudaError_t launch_kivi_quantize(const KiviQuantArgs& a, cudaStream_t s) {
-  if (a.axis == KVQ_PER_CHANNEL) {
-    const long long threads = (long long)a.B * a.H * (a.n_tok / a.group) * kD;
-    long long blocks = (threads + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    kivi_quant_channel_kernel<<<(int)blocks, 256, 0, s>>>(a);
-  } else {
-    const long long warps = (long long)a.B * a.H * a.n_tok * (kD / a.group);
-    long long blocks = (warps * 32 + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    kivi_quant_token_kernel<<<(int)blocks, 256, 0, s>>>(a);
-  }
+  // grid-stride warps; 8 blocks of 256 threads per SM keep enough rows in flight
+  const long long warps = (a.axis == KVQ_PER_CHANNEL) ? (long long)a.B * a.H * (a.n_tok / a.group)
+                                                      : ((long long)a.B * a.H * a.n_tok + 3) / 4;
+  if (warps <= 0) return cudaSuccess;
+  long long blocks = (warps + 7) / 8;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+  if (a.axis == KVQ_PER_CHANNEL) kivi_quant_channel_kernel<<<(int)blocks, 256, 0, s>>>(a);
+  else kivi_quant_token_kernel<<<(int)blocks, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

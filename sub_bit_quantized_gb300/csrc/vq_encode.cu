@@ -1,5 +1,5 @@
-// LoopVQ cache maintenance: RoPE table, codebook slicing, nearest-codeword encode of coupled
-// vectors (prefill), prefill window copy, decode-time append and page roll.
+// LoopVQ cache maintenance: RoPE table, codebook slicing, prefill window copy, decode-time
+// append and page roll (the prefill encode itself runs on the tensor cores, vq_encode_tc.cu).
 //
 // "LoopVQ: Sub 1-bit KV Cache Quantization for Looped Transformers":
 //  * background "vector quantization and codebooks": a(z) = argmin_r ||z - e_r||^2;
@@ -9,11 +9,12 @@
 //    8-token index pages; during decode the oldest recent page is encoded every 8 tokens;
 //  * method step 5: the per-loop-step codebook slice B_t is cut once at load time.
 //
-// Encode arithmetic: fp32 distances sum_k (z_k - e_k)^2 screen the 256 codewords (relative
-// error below 1.1e-6 for nonnegative sums of 16..32 fp32 terms); every candidate within
-// 4e-6 (relative) of the fp32 minimum is re-evaluated in fp64, where bf16 inputs and fp32
-// entries subtract and square exactly. The result is the exact-arithmetic argmin with the
-// lowest index on ties; a second-best fp64 distance within 1e-6 of the best counts as a tie.
+// Roll encode arithmetic (one page of 8 tokens per (layer, block, head), on CUDA cores):
+// fp32 distances sum_k (z_k - e_k)^2 screen the 256 codewords (relative error below 1.1e-6
+// for nonnegative sums of 16..32 fp32 terms); every candidate within 4e-6 (relative) of the
+// fp32 minimum is re-evaluated in fp64, where bf16 inputs and fp32 entries subtract and
+// square exactly. The result is the exact-arithmetic argmin with the lowest index on ties; a
+// second-best fp64 distance within 1e-6 of the best counts as a tie.
 #include <cuda_fp16.h>
 
 #include "kvq_common.cuh"
@@ -132,46 +133,6 @@ __device__ __forceinline__ int nearest_exact(const float (&z)[G], const float* _
 
 __device__ __forceinline__ size_t page_byte(int g, int j) {  // in-page byte of (group, token)
   return (size_t)(((g & 7) * kPage + (j & 7)) * 2 + (g >> 3));
-}
-
-// Prefill encode: one block per (sequence, head, block beta, group) x token chunk. The
-// block stages its codebook (256 x G fp32) in shared memory; a thread encodes tokens.
-template <int TC>
-__global__ void __launch_bounds__(256) encode_kernel(const VqEncodeArgs a) {
-  constexpr int G = TC * kC;
-  __shared__ __align__(16) float cbs[kCB * G];
-  const int gq = blockIdx.y;              // (b, h, beta, gi) flattened
-  const int gi = gq % a.g_count;
-  const int beta = (gq / a.g_count) % a.NB;
-  const int h = (gq / (a.g_count * a.NB)) % a.H;
-  const int b = gq / (a.g_count * a.NB * a.H);
-  const int g = a.g_begin + gi;
-  const float* cb = a.cb + (((size_t)beta * a.H + h) * kNG + g) * (size_t)kCB * G;
-  for (int k = threadIdx.x; k < kCB * G / 4; k += blockDim.x)
-    reinterpret_cast<float4*>(cbs)[k] = __ldg(reinterpret_cast<const float4*>(cb) + k);
-  __syncthreads();
-  uint8_t* out = a.idx + (((size_t)beta * a.max_batch + (a.seq_begin + b)) * a.H + h) * (size_t)a.max_pages * kPageBytes;
-  int ties = 0;
-  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < a.n_tok; j += gridDim.x * blockDim.x) {
-    float z[G];
-#pragma unroll
-    for (int m = 0; m < TC; ++m) {
-      const uint16_t* xp = a.x + (size_t)(beta * TC + m) * a.st + (size_t)b * a.sb + (size_t)h * a.sh +
-                           (size_t)j * kD + g * kC;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(xp));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int i = 0; i < kC; ++i) {
-        const uint32_t bits = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu);
-        z[i * TC + m] = bf16_to_f32(bits);
-      }
-    }
-    bool tie;
-    const int r = nearest_exact<G>(z, cbs, &tie);
-    ties += tie;
-    out[(size_t)(a.page_begin + j / kPage) * kPageBytes + page_byte(g, j)] = (uint8_t)r;
-  }
-  if (a.n_ties && ties) atomicAdd(a.n_ties, ties);
 }
 
 // ---------------------------------------------------------------- prefill window copy
@@ -313,20 +274,6 @@ cudaError_t launch_slice_codebooks_fp16(const float* cb, uint16_t* bt16, int L, 
                                         cudaStream_t s) {
   slice_fp16_kernel<<<grid_for((long long)L * T * H * kCB * kD, 256), 256, 0, s>>>(
       cb, reinterpret_cast<__half*>(bt16), L, T, Tc, G, H);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_vq_encode(const VqEncodeArgs& a, cudaStream_t s) {
-  if (a.n_tok <= 0 || a.n_seq <= 0 || a.g_count <= 0) return cudaSuccess;
-  const long long planes = (long long)a.n_seq * a.H * a.NB * a.g_count;
-  const int chunks = (a.n_tok + 1023) / 1024;
-  dim3 grid(chunks, (unsigned)planes);
-  switch (a.Tc) {
-    case 1: encode_kernel<1><<<grid, 256, 0, s>>>(a); break;
-    case 2: encode_kernel<2><<<grid, 256, 0, s>>>(a); break;
-    case 4: encode_kernel<4><<<grid, 256, 0, s>>>(a); break;
-    default: return cudaErrorInvalidValue;
-  }
   return cudaGetLastError();
 }
 

@@ -13,17 +13,23 @@
 // -||e||^2 / 2 column is split the same way and multiplies an augmented A column of ones.
 // The tensor cores screen; every row whose runner-up lies within a conservative error band
 // of the best (far above the accumulation error, and above the 1e-6 tie threshold) is
-// decided again in fp64 over the candidates in the band: the result is the exact argmin
-// with the lowest index on exact ties, and a tie is reported when the runner-up's fp64
-// distance is within 1e-6 (relative) of the best.
+// decided again over the candidates in the band on distances summed with error-free fp32
+// steps (relative error ~1e-7): the result is the argmin with the lowest index on exact ties,
+// and candidates closer than 1e-6 (relative) are reported as a tie, where either index is a
+// valid answer.
 //
-// GB300 mapping. One 128-thread block per (sequence, head, block beta, group) x 32 tiles of 128
-// vectors. The block stages the three codebook parts in shared memory once (K-major, no
-// swizzle: 8-row x 16-byte core matrices), holds a 128 x 256 fp32 accumulator in TMEM
-// (256 columns), and per tile: threads load their vector rows, one thread issues the
-// tcgen05.mma chain (3 parts x K steps of 16) and commits to an mbarrier, then each thread
-// reads its accumulator row with tcgen05.ld and keeps the best two. Every wait is bounded.
+// GB300 mapping. Persistent 512-thread blocks, two per SM (each holds a 128 x 256 fp32
+// accumulator in 256 TMEM columns), over equal contiguous shares of the (plane, 128-vector
+// tile) units, a plane being one (sequence, head, block beta, group) with its codebook. A
+// block stages the three codebook parts in shared memory (K-major, no swizzle: 8-row x
+// 16-byte core matrices) when its share enters a plane. Per tile: the block loads the vector
+// rows into one of two A buffers, one thread issues the tcgen05.mma chain (3 parts x K steps
+// of 16) and commits to an mbarrier; the four warpgroups each read 64 accumulator columns of
+// every row (tcgen05.ld) and keep the best two; warpgroup 0 merges the four and writes the
+// index while the others load the next tile. Every wait is bounded.
 #include <cuda_fp16.h>
+
+#include <algorithm>
 
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
@@ -32,13 +38,13 @@
 namespace kvq {
 namespace {
 
-constexpr int kTcThreads = 128;      // one vector row per thread = one TMEM lane
+constexpr int kTcThreads = 512;      // 4 warpgroups; a thread reads one TMEM lane
 constexpr int kTcM = 128;            // vectors per tile (MMA M)
 constexpr int kTcN = 256;            // codewords (MMA N)
-constexpr int kTilesPerBlock = 32;
+constexpr int kQCols = kTcN / 4;     // accumulator columns each warpgroup reads
 constexpr uint32_t kTmemCols = 256;  // fp32 accumulator columns
 constexpr int kParts = 3;            // hi, mid, lo bf16 parts of the fp32 codebook
-constexpr int kTcMinSmem = 80 * 1024;  // keeps at most two blocks (2 x 256 TMEM columns) per SM
+constexpr int kTcBlocksPerSm = 2;    // 2 x 256 TMEM columns
 
 // 16-byte K chunks per row: TC chunks of data (8 coordinates of one loop step each), one
 // augmented chunk (A: 1, 0..; B: -||e||^2 / 2, 0..), padded to whole MMA K steps of 32 bytes
@@ -51,13 +57,11 @@ struct TcLayout {
   static constexpr int kRowBytes = KC * 16;
   static constexpr int kABytes = kTcM * kRowBytes;          // one tile of vectors
   static constexpr int kBPartBytes = kTcN * kRowBytes;      // one codebook part
-  static constexpr int kOffA = 0;
-  static constexpr int kOffB = kOffA + kABytes;
-  static constexpr int kOffCb = kOffB + kParts * kBPartBytes;  // fp32 codebook [256][G], chunk order
-  static constexpr int kOffRed = kOffCb + kTcN * G * 4;         // float [4] block reduction
-  static constexpr int kOffBar = kOffRed + 32;                  // mbarrier + TMEM address
-  static constexpr int kBytes = kOffBar + 32;
-  static constexpr int kSmem = kBytes > kTcMinSmem ? kBytes : kTcMinSmem;
+  static constexpr int kOffA = 0;                           // two tile buffers
+  static constexpr int kOffB = kOffA + 2 * kABytes;
+  static constexpr int kOffPart = kOffB + kParts * kBPartBytes;  // [row][warpgroup] best two
+  static constexpr int kOffBar = kOffPart + kTcM * 4 * 16;       // mbarrier + TMEM address
+  static constexpr int kSmem = kOffBar + 32;
 };
 
 // byte offset of (row, chunk) in a K-major, no-swizzle operand: core matrices of 8 rows x 16
@@ -120,25 +124,62 @@ __device__ __forceinline__ size_t page_byte_tc(int g, int j) {  // in-page byte 
   return (size_t)(((g & 7) * kPage + (j & 7)) * 2 + (g >> 3));
 }
 
+// hi + lo += (z - e)^2 with error-free steps: z - e = s + t exactly (two-sum), s^2 = p + q
+// exactly (fma), hi + p = h + err exactly (two-sum); the low parts gather in lo. The sum of
+// 8..32 such terms keeps a relative error near one fp32 rounding (~1e-7), far below the 1e-6
+// tie threshold, without fp64 arithmetic (slow on this GPU).
+__device__ __forceinline__ void add_sq_diff(float z, float e, float& hi, float& lo) {
+  const float s = __fsub_rn(z, e);
+  const float bb = __fsub_rn(s, z);
+  const float t = __fadd_rn(__fsub_rn(z, __fsub_rn(s, bb)), __fsub_rn(-e, bb));
+  const float p = __fmul_rn(s, s);
+  const float q = __fmaf_rn(s, s, -p);
+  const float r = __fmaf_rn(__fmul_rn(2.f, s), t, q);
+  const float h = __fadd_rn(hi, p);
+  const float b2 = __fsub_rn(h, hi);
+  const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(h, b2)), __fsub_rn(p, b2));
+  hi = h;
+  lo = __fadd_rn(lo, __fadd_rn(err, r));
+}
+
+// one warpgroup's share of a row: its maximum, the band it used, how many of its columns lie
+// within that band of its maximum, and the first of them
+struct Quarter {
+  float best, band;
+  int count, first;
+};
+
+// Error band in acc units for a row with |z|^2 = z2 whose best acc is `best`. A codeword that
+// can compete with the best lies within |z| + sqrt(d_best) of the origin, and its
+// acc = z.e - |e|^2/2 is accumulated over 3 x KC/2 MMAs of exact bf16 products: its error is
+// below about 3 (KC/2) 17 2^-24 (|z||e| + |e|^2/2) plus the 2^-24 |z||e| of the split. The
+// band takes 8 times that for two candidates, plus the 1e-6 tie threshold of the best
+// distance. A larger `best` (a better candidate) never widens it.
+template <int KC>
+__device__ __forceinline__ float acc_band(float z2, float best) {
+  const float znorm = sqrtf(z2);
+  const float dbest = fmaxf(0.f, z2 - 2.f * best);
+  const float enear = znorm + 1.01f * sqrtf(dbest) + 1e-3f * znorm + 1e-6f;
+  return 8.f * 3.f * (KC / 2) * 18.f * 5.97e-8f * (znorm * enear + 0.5f * enear * enear) + 1e-6f * dbest + 1e-30f;
+}
+
 template <int TC>
-__global__ void __launch_bounds__(kTcThreads) encode_tc_kernel(const VqEncodeArgs a) {
+__global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(const VqEncodeArgs a, const int U,
+                                                                                const int tiles_per_plane) {
   using Lay = TcLayout<TC>;
   constexpr int G = Lay::G, KC = Lay::KC;
   extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char* sa = smem + Lay::kOffA;
   unsigned char* sb = smem + Lay::kOffB;
-  float* cbp = reinterpret_cast<float*>(smem + Lay::kOffCb);
+  Quarter* part = reinterpret_cast<Quarter*>(smem + Lay::kOffPart);
   uint64_t* mma_bar = reinterpret_cast<uint64_t*>(smem + Lay::kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffBar + 8);
   volatile int* failed = reinterpret_cast<volatile int*>(smem + Lay::kOffBar + 12);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int gq = blockIdx.y;  // (b, h, beta, gi) flattened
-  const int gi = gq % a.g_count;
-  const int beta = (gq / a.g_count) % a.NB;
-  const int h = (gq / (a.g_count * a.NB)) % a.H;
-  const int b = gq / (a.g_count * a.NB * a.H);
-  const int g = a.g_begin + gi;
+  const int wg = warp >> 2;                    // warpgroup: accumulator columns 64 wg ..
+  const int row = 32 * (warp & 3) + lane;      // TMEM lane = vector row of the tile
+  const int lo = (int)((long long)U * blockIdx.x / gridDim.x), hi = (int)((long long)U * (blockIdx.x + 1) / gridDim.x);
+  if (lo >= hi) return;
 
   // ---- TMEM accumulator (warp 0), barrier ----------------------------------------------
   if (warp == 0) {
@@ -152,114 +193,116 @@ __global__ void __launch_bounds__(kTcThreads) encode_tc_kernel(const VqEncodeArg
     *failed = 0;
     fence_mbar_init();
   }
-
-  // ---- codebook: three bf16 parts (with the -||e||^2/2 column) and an fp32 copy ----------
-  // coordinate k' = c*8 + i of a row (chunk c < TC, i < 8) is coupled coordinate i*TC + c
-  const float* cb = a.cb + (((size_t)beta * a.H + h) * kNG + g) * (size_t)kCB * G;
-  for (int r = tid; r < kTcN; r += kTcThreads) {
-    float e[G];
-    double n2 = 0.0;
-#pragma unroll
-    for (int c = 0; c < TC; ++c)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        e[c * 8 + i] = __ldg(cb + (size_t)r * G + i * TC + c);
-        n2 = fma((double)e[c * 8 + i], (double)e[c * 8 + i], n2);
-      }
-#pragma unroll
-    for (int k = 0; k < G; ++k) cbp[r * G + k] = e[k];
-    const float nh = (float)(-0.5 * n2);
-    // parts: hi = bf16(v), mid = bf16(v - hi), lo = bf16(v - hi - mid)
-    for (int c = 0; c < KC; ++c) {
-      uint32_t w[kParts][4];
-#pragma unroll
-      for (int i2 = 0; i2 < 4; ++i2) {
-        uint16_t pb[kParts][2];
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = 2 * i2 + e2;
-          float v = 0.f;
-          if (c < TC) v = e[c * 8 + i];
-          else if (c == TC && i == 0) v = nh;
-#pragma unroll
-          for (int p = 0; p < kParts; ++p) {
-            const uint16_t bits = bf16_rn_bits(v);
-            pb[p][e2] = bits;
-            v = v - bf16_to_f32(bits);  // exact: v and its bf16 rounding are within 2^-8 |v|
-          }
-        }
-#pragma unroll
-        for (int p = 0; p < kParts; ++p) w[p][i2] = pb[p][0] | ((uint32_t)pb[p][1] << 16);
-      }
-#pragma unroll
-      for (int p = 0; p < kParts; ++p)
-        *reinterpret_cast<uint4*>(sb + p * Lay::kBPartBytes + op_off(r, c, KC)) =
-            make_uint4(w[p][0], w[p][1], w[p][2], w[p][3]);
-    }
+  // constant chunks of both A buffers: the ones column, zero padding
+  for (int i = tid; i < 2 * kTcM * (KC - TC); i += kTcThreads) {
+    const int buf = i / (kTcM * (KC - TC)), rem = i % (kTcM * (KC - TC));
+    const int r = rem / (KC - TC), c = TC + rem % (KC - TC);
+    *reinterpret_cast<uint4*>(smem + Lay::kOffA + buf * Lay::kABytes + op_off(r, c, KC)) =
+        make_uint4(c == TC ? 0x3F80u : 0u, 0u, 0u, 0u);
   }
-  fence_proxy_async_smem();  // codebook parts are read by the tensor cores
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t my_lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+  const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kQCols * wg;
 
-  uint8_t* out = a.idx + (((size_t)beta * a.max_batch + (a.seq_begin + b)) * a.H + h) * (size_t)a.max_pages * kPageBytes;
-  const int n_tiles = (a.n_tok + kTcM - 1) / kTcM;
-  const int t_begin = blockIdx.x * kTilesPerBlock;
-  const int t_end = min(n_tiles, t_begin + kTilesPerBlock);
   int ties = 0;
   uint32_t phase = 0;
   int pending = -1;  // thread 0: phase of an MMA chain whose completion it gave up waiting for
-  // this thread's vector row of tile t (zeros past the end)
-  auto load_row = [&](int t, uint4 (&zr)[TC]) {
-    const int j = t * kTcM + tid;
-#pragma unroll
-    for (int m = 0; m < TC; ++m) {
-      zr[m] = make_uint4(0, 0, 0, 0);
-      if (t < t_end && j < a.n_tok) {
-        const uint16_t* xp = a.x + (size_t)(beta * TC + m) * a.st + (size_t)b * a.sb + (size_t)h * a.sh +
-                             (size_t)j * kD + g * kC;
-        zr[m] = __ldg(reinterpret_cast<const uint4*>(xp));
-      }
+  int cur_plane = -1, buf = 0;
+  const float* cb = nullptr;
+  uint8_t* out = nullptr;
+  int g = 0;
+  // chunk i (< kTcM * TC) of unit u: 16 bytes of one vector row (zeros past the tokens)
+  auto load_chunk = [&](int u) {
+    uint4 v = make_uint4(0, 0, 0, 0);
+    const int i = tid;
+    if (u < hi && i < kTcM * TC) {
+      const int pl = u / tiles_per_plane, tt = u - pl * tiles_per_plane;
+      const int gi2 = pl % a.g_count, be = (pl / a.g_count) % a.NB, hh = (pl / (a.g_count * a.NB)) % a.H;
+      const int bb = pl / (a.g_count * a.NB * a.H);
+      const int r = i / TC, m = i % TC;
+      const int j = tt * kTcM + r;
+      if (j < a.n_tok)
+        v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)(be * TC + m) * a.st + (size_t)bb * a.sb +
+                                                 (size_t)hh * a.sh + (size_t)j * kD + (a.g_begin + gi2) * kC));
     }
+    return v;
   };
-  uint4 znext[TC];
-  load_row(t_begin, znext);
-  for (int t = t_begin; t < t_end; ++t) {
-    // ---- this thread's vector row -> A tile (chunks: TC data, ones column, zero pad) ----
-    const int j = t * kTcM + tid;
-    const bool valid = j < a.n_tok;
-    uint4 zr[TC];
-    float z2 = 0.f;
+  uint4 pre = load_chunk(lo);
+  // descriptors of the operands: A buffer 0, codebook part 0 (the others are fixed offsets)
+  const uint64_t a_desc0 = umma_desc(smem_u32(smem + Lay::kOffA), 128, KC * 128);
+  const uint64_t b_desc0 = umma_desc(smem_u32(sb), 128, KC * 128);
+  for (int u = lo; u < hi; ++u, buf ^= 1) {
+    const int plane = u / tiles_per_plane, t = u - plane * tiles_per_plane;
+    const int gi = plane % a.g_count;
+    const int beta = (plane / a.g_count) % a.NB;
+    const int h = (plane / (a.g_count * a.NB)) % a.H;
+    const int b = plane / (a.g_count * a.NB * a.H);
+    if (plane != cur_plane) {  // uniform
+      // ---- codebook of this plane: three bf16 parts with the -||e||^2/2 column ------------
+      // coordinate k' = c*8 + i of a row (chunk c < TC, i < 8) is coupled coordinate i*TC + c
+      g = a.g_begin + gi;
+      cb = a.cb + (((size_t)beta * a.H + h) * kNG + g) * (size_t)kCB * G;
+      out = a.idx + (((size_t)beta * a.max_batch + (a.seq_begin + b)) * a.H + h) * (size_t)a.max_pages * kPageBytes;
+      __syncthreads();  // the previous plane's MMAs have all been waited for
+      for (int r = tid; r < kTcN; r += kTcThreads) {
+        float nh_hi = 0.f, nh_lo = 0.f;  // |e|^2, compensated
+#pragma unroll 4
+        for (int k = 0; k < G; ++k) add_sq_diff(__ldg(cb + (size_t)r * G + k), 0.f, nh_hi, nh_lo);
+        const float nh = -0.5f * __fadd_rn(nh_hi, nh_lo);
+        // one 16-byte chunk at a time; parts: hi = bf16(v), mid = bf16(v - hi), lo = bf16(v - hi - mid)
+#pragma unroll 1
+        for (int c = 0; c < KC; ++c) {
+          uint32_t w[kParts][4];
 #pragma unroll
-    for (int m = 0; m < TC; ++m) {
-      zr[m] = znext[m];
-      const uint32_t w4[4] = {zr[m].x, zr[m].y, zr[m].z, zr[m].w};
+          for (int i2 = 0; i2 < 4; ++i2) {
+            uint16_t pb[kParts][2];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float lo = bf16_lo(w4[q]), hi = bf16_hi(w4[q]);
-        z2 = fmaf(lo, lo, fmaf(hi, hi, z2));
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const int i = 2 * i2 + e2;
+              float v = 0.f;
+              if (c < TC) v = __ldg(cb + (size_t)r * G + i * TC + c);
+              else if (c == TC && i == 0) v = nh;
+#pragma unroll
+              for (int p = 0; p < kParts; ++p) {
+                const uint16_t bits = bf16_rn_bits(v);
+                pb[p][e2] = bits;
+                v = v - bf16_to_f32(bits);  // exact: v and its bf16 rounding are within 2^-8 |v|
+              }
+            }
+#pragma unroll
+            for (int p = 0; p < kParts; ++p) w[p][i2] = pb[p][0] | ((uint32_t)pb[p][1] << 16);
+          }
+#pragma unroll
+          for (int p = 0; p < kParts; ++p)
+            *reinterpret_cast<uint4*>(sb + p * Lay::kBPartBytes + op_off(r, c, KC)) =
+                make_uint4(w[p][0], w[p][1], w[p][2], w[p][3]);
+        }
       }
-      *reinterpret_cast<uint4*>(sa + op_off(tid, m, KC)) = zr[m];
+      cur_plane = plane;
     }
-#pragma unroll
-    for (int c = TC; c < KC; ++c)
-      *reinterpret_cast<uint4*>(sa + op_off(tid, c, KC)) = make_uint4(c == TC ? 0x3F80u : 0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();  // A tile written; the previous tile's accumulator reads are done
 
-    // ---- one thread: 3 parts x K steps into the accumulator, commit -----------------------
+    // ---- vector rows of tile t -> A buffer (TC 16-byte chunks per row); the next tile's
+    //      rows are loaded now and land during this tile's work --------------------------------
+    unsigned char* sa = smem + Lay::kOffA + buf * Lay::kABytes;
+    static_assert(kTcM * TC <= kTcThreads, "one chunk per thread");
+    if (tid < kTcM * TC) *reinterpret_cast<uint4*>(sa + op_off(tid / TC, tid % TC, KC)) = pre;
+    pre = load_chunk(u + 1);
+    fence_proxy_async_smem();  // A (and a new codebook) are read by the tensor cores
+    tc_fence_before();
+    __syncthreads();  // operands written; the previous tile's accumulator reads are done
+
+    // ---- one thread: 3 parts x K steps into the accumulator, commit, wait ------------------
     if (tid == 0 && !*failed) {
       tc_fence_after();
+      // start addresses advance in 16-byte units in the low descriptor bits (no carry: every
+      // operand lies below 256 KB of shared memory)
 #pragma unroll
       for (int p = 0; p < kParts; ++p)
 #pragma unroll
-        for (int s = 0; s < KC / 2; ++s) {
-          const uint64_t ad = umma_desc(smem_u32(sa) + s * 256, 128, KC * 128);
-          const uint64_t bd = umma_desc(smem_u32(sb + p * Lay::kBPartBytes) + s * 256, 128, KC * 128);
-          umma_bf16(tmem, ad, bd, (p | s) != 0);
-        }
+        for (int s = 0; s < KC / 2; ++s)
+          umma_bf16(tmem, a_desc0 + (uint64_t)((buf * Lay::kABytes + s * 256) >> 4),
+                    b_desc0 + (uint64_t)((p * Lay::kBPartBytes + s * 256) >> 4), (p | s) != 0);
       umma_commit(mma_bar);
       if (!mbar_wait_bounded(mma_bar, phase)) {
         *failed = 1;
@@ -268,84 +311,131 @@ __global__ void __launch_bounds__(kTcThreads) encode_tc_kernel(const VqEncodeArg
       }
     }
     phase ^= 1u;
-    load_row(t + 1, znext);  // in flight during this tile's epilogue
     __syncthreads();  // thread 0 saw the accumulator complete (or gave up)
     tc_fence_after();
 
-    // ---- epilogue: best and runner-up of acc_r = z.e_r - ||e_r||^2/2 over 256 columns ----
-    float best = -INFINITY, second = -INFINITY;
-    int bi = 0;
-#pragma unroll 1
-    for (int c0 = 0; c0 < kTcN; c0 += 32) {
-      float v[32];
-      tmem_ld32(my_lane_addr + c0, v);
+    // ---- each warpgroup, its 64 columns of the row: maximum of acc = z.e - |e|^2/2, then the
+    //      columns within the error band of it (a bit mask per 32 columns) --------------------
+    float z2 = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const bool gt = v[i] > best;
-        second = fmaxf(second, fminf(v[i], best));
-        bi = gt ? c0 + i : bi;
-        best = fmaxf(best, v[i]);
+    for (int c = 0; c < TC; ++c) {
+      const uint4 w = *reinterpret_cast<const uint4*>(sa + op_off(row, c, KC));
+      const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float l = bf16_lo(w4[q]), hh = bf16_hi(w4[q]);
+        z2 = fmaf(l, l, fmaf(hh, hh, z2));
       }
     }
-    // Error band in acc units. A codeword that can compete with the best lies within
-    // |z| + sqrt(d_best) of the origin, and its acc = z.e - |e|^2/2 is accumulated over 3 x K/16
-    // MMAs of exact bf16 products: its error is below about 3 (K/16) 17 2^-24 (|z||e| + |e|^2/2)
-    // plus the 2^-24 |z||e| of the split. The band takes 8 times that for two candidates, plus
-    // the 1e-6 tie threshold of the best distance.
-    const float znorm = sqrtf(z2);
-    const float dbest = fmaxf(0.f, z2 - 2.f * best);
-    const float enear = znorm + 1.01f * sqrtf(dbest) + 1e-3f * znorm + 1e-6f;
-    const float band = 8.f * 3.f * (KC / 2) * 18.f * 5.97e-8f * (znorm * enear + 0.5f * enear * enear) +
-                       1e-6f * dbest + 1e-30f;
-    const bool need = valid && !*failed && (second >= best - band);
-    int result = bi;
-    if (__any_sync(0xFFFFFFFFu, need)) {
-      // exact decision over every candidate in the band, in fp64 (lowest index wins ties)
-      float zf[G];
+    {
+      float run = -INFINITY, cmax[kQCols / 32];
+      uint32_t mask[kQCols / 32];
 #pragma unroll
-      for (int m = 0; m < TC; ++m) {
-        const uint32_t w4[4] = {zr[m].x, zr[m].y, zr[m].z, zr[m].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          zf[m * 8 + 2 * q] = bf16_lo(w4[q]);
-          zf[m * 8 + 2 * q + 1] = bf16_hi(w4[q]);
-        }
-      }
-      double b64 = INFINITY, s64 = INFINITY;
-      int b64i = bi;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kTcN; c0 += 32) {
+      for (int k = 0; k < kQCols / 32; ++k) {
         float v[32];
-        tmem_ld32(my_lane_addr + c0, v);  // every lane of the warp reads (the load is warp-wide)
-        if (need) {
+        tmem_ld32(lane_addr + 32 * k, v);
+        float cm = v[0];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (v[i] < best - band) continue;
-            const int r = c0 + i;
-            const float* er = cbp + r * G;
-            double dd = 0.0;
+        for (int i = 1; i < 32; ++i) cm = fmaxf(cm, v[i]);
+        run = fmaxf(run, cm);
+        const float thr = run - acc_band<KC>(z2, run);
+        uint32_t mk = 0;
 #pragma unroll
-            for (int k = 0; k < G; ++k) {
-              const double df = (double)zf[k] - (double)er[k];
-              dd = fma(df, df, dd);
+        for (int i = 0; i < 32; ++i) mk |= (v[i] >= thr) ? (1u << i) : 0u;
+        cmax[k] = cm;
+        mask[k] = mk;
+      }
+      Quarter qr;
+      qr.best = run;
+      qr.band = acc_band<KC>(z2, run);
+      qr.count = 0;
+      qr.first = kTcN;
+#pragma unroll
+      for (int k = kQCols / 32 - 1; k >= 0; --k) {  // a chunk far below the maximum has no candidate
+        if (cmax[k] < run - qr.band) continue;
+        qr.count += __popc(mask[k]);
+        if (mask[k]) qr.first = kQCols * wg + 32 * k + __ffs(mask[k]) - 1;
+      }
+      part[row * 4 + wg] = qr;
+    }
+    tc_fence_before();
+    __syncthreads();  // the four quarters of every row are in shared memory
+
+    // ---- warpgroup 0: merge the quarters; one candidate is the answer, several are decided
+    //      on compensated distances --------------------------------------------------------------
+    if (wg == 0) {
+      float best = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) best = fmaxf(best, part[row * 4 + q].best);
+      const float band = acc_band<KC>(z2, best);
+      int count = 0, first = kTcN;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // each quarter's band is at least this one: its mask covers
+        const Quarter o = part[row * 4 + q];
+        if (o.best < best - band) continue;
+        count += o.count;
+        first = min(first, o.first);
+      }
+      const int j = t * kTcM + row;
+      const bool valid = j < a.n_tok;
+      const bool need = valid && !*failed && count > 1;
+      struct { float best; int col; } m = {best, first};
+      int result = m.col;
+      if (__any_sync(0xFFFFFFFFu, need)) {
+        // every candidate in the band, decided on compensated fp32 distances (lowest index wins
+        // exact ties); a runner-up within 1e-6 of the best is reported as a tie
+        float bd = INFINITY, sd = INFINITY;
+        int bdi = m.col;
+        const uint32_t row_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+#pragma unroll 1
+        for (int c0 = 0; c0 < kTcN; c0 += 32) {
+          uint32_t cand = 0;  // columns of this chunk inside the band
+          {
+            float v[32];
+            tmem_ld32(row_addr + c0, v);  // warp-wide load: every lane takes part
+#pragma unroll
+            for (int i = 0; i < 32; ++i) cand |= (v[i] >= m.best - band) ? (1u << i) : 0u;
+          }
+          if (!need) cand = 0;
+          while (cand) {
+            const int r = c0 + __ffs(cand) - 1;
+            cand &= cand - 1;
+            // e = hi + mid + lo exactly (each residual is a multiple of e's ulp that fits the
+            // next part), so the staged parts give the fp32 entries back
+            float dh = 0.f, dl = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < TC; ++c) {
+              const uint4 w = *reinterpret_cast<const uint4*>(sa + op_off(row, c, KC));
+              const uint4 e0 = *reinterpret_cast<const uint4*>(sb + op_off(r, c, KC));
+              const uint4 e1 = *reinterpret_cast<const uint4*>(sb + Lay::kBPartBytes + op_off(r, c, KC));
+              const uint4 e2 = *reinterpret_cast<const uint4*>(sb + 2 * Lay::kBPartBytes + op_off(r, c, KC));
+              const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+              const uint32_t h4[4] = {e0.x, e0.y, e0.z, e0.w}, m4[4] = {e1.x, e1.y, e1.z, e1.w},
+                             l4[4] = {e2.x, e2.y, e2.z, e2.w};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                add_sq_diff(bf16_lo(w4[q]), __fadd_rn(__fadd_rn(bf16_lo(h4[q]), bf16_lo(m4[q])), bf16_lo(l4[q])), dh, dl);
+                add_sq_diff(bf16_hi(w4[q]), __fadd_rn(__fadd_rn(bf16_hi(h4[q]), bf16_hi(m4[q])), bf16_hi(l4[q])), dh, dl);
+              }
             }
-            if (dd < b64) {
-              s64 = b64;
-              b64 = dd;
-              b64i = r;
-            } else if (dd < s64) {
-              s64 = dd;
+            const float dd = __fadd_rn(dh, dl);
+            if (dd < bd) {  // columns are visited in increasing order: the lowest wins exact ties
+              sd = bd;
+              bd = dd;
+              bdi = r;
+            } else if (dd < sd) {
+              sd = dd;
             }
           }
         }
+        if (need) {
+          result = bdi;
+          ties += (sd <= bd * (1.f + 1e-6f)) ? 1 : 0;
+        }
       }
-      if (need) {
-        result = b64i;
-        ties += (s64 <= b64 * (1.0 + 1e-6)) ? 1 : 0;
-      }
+      if (valid && !*failed)
+        out[(size_t)(a.page_begin + j / kPage) * kPageBytes + page_byte_tc(g, j)] = (uint8_t)result;
     }
-    if (valid && !*failed) out[(size_t)(a.page_begin + j / kPage) * kPageBytes + page_byte_tc(g, j)] = (uint8_t)result;
-    tc_fence_before();
   }
 
   // ---- tie count, then free TMEM (after the last MMA has landed) --------------------------
@@ -353,6 +443,7 @@ __global__ void __launch_bounds__(kTcThreads) encode_tc_kernel(const VqEncodeArg
   for (int off = 16; off >= 1; off >>= 1) ties += __shfl_xor_sync(0xFFFFFFFFu, ties, off);
   if (lane == 0 && ties && a.n_ties) atomicAdd(a.n_ties, ties);
   if (tid == 0 && pending >= 0) mbar_wait_bounded(mma_bar, (uint32_t)pending);  // an MMA still in flight
+  tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
@@ -367,8 +458,12 @@ cudaError_t launch_tc(const VqEncodeArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const long long planes = (long long)a.n_seq * a.H * a.NB * a.g_count;
   const int tiles = (a.n_tok + kTcM - 1) / kTcM;
-  dim3 grid((tiles + kTilesPerBlock - 1) / kTilesPerBlock, (unsigned)planes);
-  encode_tc_kernel<TC><<<grid, kTcThreads, Lay::kSmem, s>>>(a);
+  const long long U = planes * tiles;
+  if (U >= (1ll << 31)) return cudaErrorInvalidValue;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long blocks = std::min<long long>(U, (long long)kTcBlocksPerSm * sms);
+  encode_tc_kernel<TC><<<(unsigned)blocks, kTcThreads, Lay::kSmem, s>>>(a, (int)U, tiles);
   return cudaGetLastError();
 }
 

@@ -149,153 +149,285 @@ __global__ void __launch_bounds__(256) kivi_quant_token_kernel(const KiviQuantAr
 }
 
 // ---------------------------------------------------------------- attention
+// One block per (split, request, head); splits 0 .. n_split-1 take equal token ranges of the
+// quantized segment, the last block the fp16 residual segment. A quantized split streams its
+// tokens through a 4-stage shared-memory ring of 128-token chunks (TMA bulk copies of the
+// chunk's key codes, key scales and zeros, value codes, value scales and zeros: 12 KB), with a
+// block-wide online softmax across chunks. Partials of all splits merge exactly in the last
+// block of a (request, head) to finish (arrival counter, no spin-wait).
 constexpr int kAThreads = 256;
 constexpr int kAWarps = kAThreads / 32;
-constexpr int kKiviSmemLimit = 100 * 1024;
-// shared layout (floats): q[128] | qf[kAWarps][128] | ored[kAWarps][128] | red[64] | flag | scores
-constexpr int kOffQf = kD;
-constexpr int kOffOred = kOffQf + kAWarps * kD;
-constexpr int kOffRed = kOffOred + kAWarps * kD;
-constexpr int kOffFlag = kOffRed + 64;
-constexpr int kOffSc = kOffFlag + 4;
+constexpr int kAChunk = 128;                      // tokens per ring stage (4 key groups of 32)
+constexpr int kAStages = 4;
+constexpr int kCKc = 0;                           // stage layout (bytes)
+constexpr int kCKs = kCKc + kAChunk * 32;         // key scales [4 groups][128] fp16
+constexpr int kCKz = kCKs + 4 * kD * 2;
+constexpr int kCVc = kCKz + 4 * kD * 2;
+constexpr int kCVs = kCVc + kAChunk * 32;         // value scales [128 tokens][4 groups] fp16
+constexpr int kCVz = kCVs + kAChunk * 4 * 2;
+constexpr int kAStageBytes = kCVz + kAChunk * 4 * 2;  // 12 KB
+// shared layout (bytes)
+constexpr int kAOffRing = 0;
+constexpr int kAOffQ = kAOffRing + kAStages * kAStageBytes;  // float q[128]
+constexpr int kAOffQf = kAOffQ + kD * 4;                      // float q' [4 groups][128]
+constexpr int kAOffBias = kAOffQf + 4 * kD * 4;               // float [4 groups][2 halves]
+constexpr int kAOffRed = kAOffBias + 32;                      // float [8 warps] + flag
+constexpr int kAOffBar = kAOffRed + 64;                       // mbarriers [4] + failed
+constexpr int kAOffSc = kAOffBar + 64;                        // float scores [max(128, residual)]
+static_assert(kAStageBytes % 128 == 0 && kAOffBar % 8 == 0, "alignment");
 
-__global__ void __launch_bounds__(kAThreads, 2) kivi_attn_kernel(const KiviAttnArgs a, const float scale_log2) {
-  extern __shared__ __align__(16) float sm[];
-  float* qs = sm;
-  float* qf = sm + kOffQf;
-  float* ored = sm + kOffOred;
-  float* red = sm + kOffRed;
-  int* flag = reinterpret_cast<int*>(sm + kOffFlag);
-  float* sc = sm + kOffSc;
+// Codes j and j + 8 (j < 8) of a 16-code word, each as (code * 4^j) in fp32: the code is
+// masked in place (bits 2j, 2j+1 of each half word), placed in the mantissa of 2^23 and 2^23
+// is subtracted, all exact. One integer op per code and one packed add per pair instead of
+// shift + int-to-float conversion; the 4^-j scale is folded into the other operand.
+__device__ __forceinline__ float2 code_pair(uint32_t w, uint32_t w_hi, int j) {
+  const uint32_t m = 3u << (2 * j);
+  const float2 f = make_float2(__uint_as_float((w & m) | 0x4B000000u), __uint_as_float((w_hi & m) | 0x4B000000u));
+  return __fadd2_rn(f, make_float2(-8388608.f, -8388608.f));
+}
+__device__ __forceinline__ float pow4_neg(int j) { return __uint_as_float((uint32_t)(127 - 2 * j) << 23); }
+
+__device__ __forceinline__ bool kivi_wait(uint64_t* bar, uint32_t parity, volatile int* failed, int* err) {
+  if (*failed) return false;
+  if (mbar_wait_bounded(bar, parity)) return true;
+  *failed = 1;
+  set_error(err, KVQ_ERR_TIMEOUT);
+  return false;
+}
+
+__global__ void __launch_bounds__(kAThreads) kivi_attn_kernel(const KiviAttnArgs a, const float scale_log2) {
+  extern __shared__ __align__(128) unsigned char sma[];
+  float* qs = reinterpret_cast<float*>(sma + kAOffQ);
+  float* qf = reinterpret_cast<float*>(sma + kAOffQf);
+  float* bias = reinterpret_cast<float*>(sma + kAOffBias);
+  float* red = reinterpret_cast<float*>(sma + kAOffRed);
+  int* flag = reinterpret_cast<int*>(sma + kAOffRed + 8 * 4);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sma + kAOffBar);
+  volatile int* failed = reinterpret_cast<volatile int*>(sma + kAOffBar + kAStages * 8);
+  float* sc = reinterpret_cast<float*>(sma + kAOffSc);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int split = blockIdx.x, b = blockIdx.y, h = blockIdx.z, H = a.H;
-  const int NQ = a.n_quant[b];
-  const int NR = (split == 0) ? a.n_resid[b] : 0;
-  const int t0 = split * a.tok_per_split;
-  const int t1 = min(NQ, t0 + a.tok_per_split);
-  const int nq = max(0, t1 - t0);
+  const int n_total = gridDim.x;                 // quantized splits + the residual block
+  const bool resid_block = (a.residual > 0) && (split == n_total - 1);
   const size_t bh = (size_t)b * H + h;
+  const int NQ = min(a.n_quant[b], a.max_tokens) / a.group * a.group;
   if (tid < kD) qs[tid] = bf16_to_f32(a.q[bh * kD + tid]);
+  if (tid == 0) {
+    for (int s = 0; s < kAStages; ++s) mbar_init(&full[s], 1);
+    *failed = 0;
+    fence_mbar_init();
+  }
   __syncthreads();
 
-  float mloc = -INFINITY;
-  // ---- quantized keys: a warp per 32-token group, lane = token ------------------------
-  const int G = a.group;
-  for (int gl = warp; gl < nq / G; gl += kAWarps) {
-    const int tg = t0 / G + gl;  // token group index
-    const uint16_t* ks = a.k_scale + (bh * (a.max_tokens / G) + tg) * kD;
-    const uint16_t* kz = a.k_zero + (bh * (a.max_tokens / G) + tg) * kD;
-    float bias = 0.f;
+  // running softmax state; the max is block-wide
+  // quantized blocks: lane holds channels 16 (lane % 8) .. + 15 of its token slot (lane / 8);
+  // the residual block: channels 4 lane .. 4 lane + 3 in o[0..3]
+  float M = -INFINITY, l = 0.f, oz = 0.f;
+  float o[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int ch = lane * 4 + i;
-      const float qv = qs[ch] * h2f(__ldg(ks + ch));
-      qf[warp * kD + ch] = qv;
-      bias = fmaf(-qv, h2f(__ldg(kz + ch)), bias);
-    }
+  for (int i = 0; i < 16; ++i) o[i] = 0.f;
+  auto rescale_to = [&](float Mn) {
+    const float f = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) bias += __shfl_xor_sync(0xFFFFFFFFu, bias, off);
-    __syncwarp();
-    const int j = tg * G + lane;
-    const uint4* cr = reinterpret_cast<const uint4*>(a.k_codes + (bh * a.max_tokens + j) * (kD / 4));
-    const uint4 c0 = ld_stream_u4(cr), c1 = ld_stream_u4(cr + 1);
-    const uint32_t wds[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    const float4* qf4 = reinterpret_cast<const float4*>(qf + warp * kD);
-    float acc = 0.f;
+    for (int i = 0; i < 16; ++i) o[i] *= f;
+    oz *= f;
+    l *= f;
+    M = Mn;
+  };
+  // block max of sc[0, n) (every warp computes it)
+  auto scores_max = [&](int n) {
+    float m = -INFINITY;
+    for (int i = lane; i < n; i += 32) m = fmaxf(m, sc[i]);
 #pragma unroll
-    for (int wi = 0; wi < 8; ++wi) {
+    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+    return m;
+  };
+
+  if (!resid_block) {
+    // ================================ quantized tokens ======================================
+    const int t0 = split * a.tok_per_split;
+    const int t1 = min(NQ, t0 + a.tok_per_split);
+    const int n_tok = max(0, t1 - t0);
+    const int n_chunks = (n_tok + kAChunk - 1) / kAChunk;
+    const size_t tok0 = bh * a.max_tokens;         // token row base of (b, h)
+    const size_t grp0 = bh * (a.max_tokens / 32);  // key group row base of (b, h)
+    auto produce = [&](int c) {                    // thread 0
+      const int st = c % kAStages;
+      unsigned char* dst = sma + kAOffRing + st * kAStageBytes;
+      const int t = t0 + c * kAChunk;
+      const int n = min(kAChunk, t1 - t), ng = n / 32;
+      mbar_arrive_expect_tx(&full[st], (uint32_t)(n * 32 * 2 + ng * kD * 2 * 2 + n * 8 * 2));
+      bulk_g2s(dst + kCKc, a.k_codes + (tok0 + t) * 32, n * 32, &full[st]);
+      bulk_g2s(dst + kCVc, a.v_codes + (tok0 + t) * 32, n * 32, &full[st]);
+      bulk_g2s(dst + kCKs, a.k_scale + (grp0 + t / 32) * kD, ng * kD * 2, &full[st]);
+      bulk_g2s(dst + kCKz, a.k_zero + (grp0 + t / 32) * kD, ng * kD * 2, &full[st]);
+      bulk_g2s(dst + kCVs, a.v_scale + (tok0 + t) * 4, n * 8, &full[st]);
+      bulk_g2s(dst + kCVz, a.v_zero + (tok0 + t) * 4, n * 8, &full[st]);
+    };
+    int issued = 0;  // thread 0
+    if (tid == 0)
+      for (int c = 0; c < min(kAStages, n_chunks); ++c) {
+        produce(c);
+        ++issued;
+      }
+
+    for (int c = 0; c < n_chunks; ++c) {
+      const int st = c % kAStages;
+      kivi_wait(&full[st], (c / kAStages) & 1, failed, a.err);
+      const unsigned char* stage = sma + kAOffRing + st * kAStageBytes;
+      const int n = min(kAChunk, t1 - (t0 + c * kAChunk)), ng = n / 32;
+      // ---- q' = q s per key group (the scale folds into the query) and bias = -sum q' z ----
+      {
+        const int g = warp >> 1, hf = warp & 1;
+        if (g < ng) {
+          const int ch = 64 * hf + 2 * lane;
+          const uint32_t s2 = *reinterpret_cast<const uint32_t*>(stage + kCKs + (g * kD + ch) * 2);
+          const uint32_t z2 = *reinterpret_cast<const uint32_t*>(stage + kCKz + (g * kD + ch) * 2);
+          const float qa = qs[ch] * h2f(s2 & 0xFFFFu), qb = qs[ch + 1] * h2f(s2 >> 16);
+          // pair layout: [group][half][word m][j] = (channel 16m + j, channel 16m + 8 + j) of the
+          // half, scaled by 4^-j to match code_pair
 #pragma unroll
-      for (int bi = 0; bi < 4; ++bi) {
-        const uint32_t byte = (wds[wi] >> (8 * bi)) & 0xFFu;
-        const float4 qq = qf4[wi * 4 + bi];
-        acc = fmaf(qq.x, (float)(byte & 3u), acc);
-        acc = fmaf(qq.y, (float)((byte >> 2) & 3u), acc);
-        acc = fmaf(qq.z, (float)((byte >> 4) & 3u), acc);
-        acc = fmaf(qq.w, (float)(byte >> 6), acc);
+          for (int e = 0; e < 2; ++e) {
+            const int c = ch + e, k = c & 15, j = k & 7;
+            qf[g * kD + 64 * hf + 2 * (8 * ((c & 63) >> 4) + j) + (k >> 3)] = (e ? qb : qa) * pow4_neg(j);
+          }
+          float pb = -(qa * h2f(z2 & 0xFFFFu) + qb * h2f(z2 >> 16));
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) pb += __shfl_xor_sync(0xFFFFFFFFu, pb, off);
+          if (lane == 0) bias[g * 2 + hf] = pb;
+        }
+      }
+      __syncthreads();
+      // ---- scores: warp (group, 16 tokens), lanes 0-15 channels 0-63, lanes 16-31 64-127 ----
+      {
+        const int g = warp >> 1;
+        if (g < ng) {
+          const int tk = 32 * g + 16 * (warp & 1) + (lane & 15), chh = lane >> 4;
+          const uint4 cw = *reinterpret_cast<const uint4*>(stage + kCKc + tk * 32 + 16 * chh);
+          const uint32_t wds[4] = {cw.x, cw.y, cw.z, cw.w};
+          const float2* q2 = reinterpret_cast<const float2*>(qf + g * kD + 64 * chh);
+          float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t w_hi = wds[k] >> 16;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc2 = __ffma2_rn(q2[8 * k + j], code_pair(wds[k], w_hi, j), acc2);
+          }
+          float acc = acc2.x + acc2.y;
+          acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 16);
+          if (chh == 0) sc[tk] = (acc + bias[g * 2] + bias[g * 2 + 1]) * scale_log2;
+        }
+      }
+      __syncthreads();
+      // ---- online softmax, then values: warp w takes tokens 16w .. 16w + 15, four at a time;
+      //      lane: token 4 step + lane / 8, code word lane % 8 (channels 16 (lane % 8) .. + 15,
+      //      value group (lane % 8) / 2) ----
+      const float Mn = fmaxf(M, scores_max(n));
+      if (Mn > M) rescale_to(Mn);
+      {
+        const int tb = 16 * warp;
+        const float pk = (tb + (lane & 15) < n) ? exp2f(sc[tb + (lane & 15)] - M) : 0.f;
+        float ls = (lane < 16) ? pk : 0.f;
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, off);
+        l += __shfl_sync(0xFFFFFFFFu, ls, 0);
+        const int lw = lane & 7, ts = lane >> 3, gv = lw >> 1;
+#pragma unroll
+        for (int step = 0; step < 4; ++step) {
+          const float p = __shfl_sync(0xFFFFFFFFu, pk, 4 * step + ts);
+          const int tk = tb + 4 * step + ts;
+          if (tk < n) {
+            const uint32_t wv = *reinterpret_cast<const uint32_t*>(stage + kCVc + tk * 32 + 4 * lw);
+            const float wgt = p * h2f(*reinterpret_cast<const uint16_t*>(stage + kCVs + (tk * 4 + gv) * 2));
+            oz = fmaf(wgt, h2f(*reinterpret_cast<const uint16_t*>(stage + kCVz + (tk * 4 + gv) * 2)), oz);
+            const uint32_t wv_hi = wv >> 16;
+            const float2 w2 = make_float2(wgt, wgt);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {  // o2[j] = (channel j, channel 8 + j) of the word, x 4^j
+              const float2 acc = __ffma2_rn(w2, code_pair(wv, wv_hi, j), make_float2(o[2 * j], o[2 * j + 1]));
+              o[2 * j] = acc.x;
+              o[2 * j + 1] = acc.y;
+            }
+          }
+        }
+      }
+      __syncthreads();  // every thread is done with this stage
+      if (tid == 0 && c + kAStages < n_chunks && !*failed) {
+        produce(c + kAStages);
+        ++issued;
       }
     }
-    const float v = (acc + bias) * scale_log2;
-    sc[gl * G + lane] = v;
-    mloc = fmaxf(mloc, v);
-    __syncwarp();
-  }
-  // ---- residual keys (fp16): lane = token ---------------------------------------------
-  for (int r = tid; r < NR; r += kAThreads) {
-    const uint4* kr = reinterpret_cast<const uint4*>(a.k_resid + (bh * a.residual + r) * kD);
-    float acc = 0.f;
+    // after a timed-out wait, let this block's copies still in flight land first
+    if (tid == 0 && *failed)
+      for (int c = max(0, issued - kAStages); c < issued; ++c) mbar_wait_bounded(&full[c % kAStages], (c / kAStages) & 1);
+  } else {
+    // ================================ fp16 residual tokens ==================================
+    const int NR = min(a.n_resid[b], a.residual);
+    for (int r = tid; r < NR; r += kAThreads) {  // keys: a thread per token
+      const uint4* kr = reinterpret_cast<const uint4*>(a.k_resid + (bh * a.residual + r) * kD);
+      float acc = 0.f;
 #pragma unroll 4
-    for (int k8 = 0; k8 < kD / 8; ++k8) {
-      const uint4 v = __ldg(kr + k8);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      for (int k8 = 0; k8 < kD / 8; ++k8) {
+        const uint4 v = __ldg(kr + k8);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-        acc = fmaf(qs[k8 * 8 + 2 * i], f.x, acc);
-        acc = fmaf(qs[k8 * 8 + 2 * i + 1], f.y, acc);
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+          acc = fmaf(qs[k8 * 8 + 2 * i], f.x, acc);
+          acc = fmaf(qs[k8 * 8 + 2 * i + 1], f.y, acc);
+        }
+      }
+      sc[r] = acc * scale_log2;
+    }
+    __syncthreads();
+    rescale_to(scores_max(NR));
+    for (int r = warp; r < NR; r += kAWarps) {  // values: a warp per token, lane 4 channels
+      const float p = exp2f(sc[r] - M);
+      l += p;
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(a.v_resid + (bh * a.residual + r) * kD + lane * 4));
+      const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+      const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+      o[0] = fmaf(p, f0.x, o[0]);
+      o[1] = fmaf(p, f0.y, o[1]);
+      o[2] = fmaf(p, f1.x, o[2]);
+      o[3] = fmaf(p, f1.y, o[3]);
+    }
+  }
+
+  // ---- warps -> block: sum o - oz and l over the warps (one max for the block) -----------
+  __syncthreads();  // the ring is idle
+  float* ored = reinterpret_cast<float*>(sma + kAOffRing);  // [warp][128]
+  if (!resid_block) {  // the four token slots of a code word meet, then 8 lanes hold 128 channels
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      o[i] += __shfl_xor_sync(0xFFFFFFFFu, o[i], 8);
+      o[i] += __shfl_xor_sync(0xFFFFFFFFu, o[i], 16);
+    }
+    oz += __shfl_xor_sync(0xFFFFFFFFu, oz, 8);
+    oz += __shfl_xor_sync(0xFFFFFFFFu, oz, 16);
+    if (lane < 8) {  // o[2j] is channel j of the word, o[2j + 1] channel 8 + j, both x 4^j
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        ored[warp * kD + 16 * lane + j] = o[2 * j] * pow4_neg(j) - oz;
+        ored[warp * kD + 16 * lane + 8 + j] = o[2 * j + 1] * pow4_neg(j) - oz;
       }
     }
-    const float v = acc * scale_log2;
-    sc[nq + r] = v;
-    mloc = fmaxf(mloc, v);
-  }
-  // ---- softmax statistics ---------------------------------------------------------------
+  } else {
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xFFFFFFFFu, mloc, off));
-  if (lane == 0) red[warp] = mloc;
+    for (int i = 0; i < 4; ++i) ored[warp * kD + lane * 4 + i] = o[i];
+  }
+  if (lane == 0) red[warp] = l;
   __syncthreads();
-  float M = -INFINITY;
-  for (int w = 0; w < kAWarps; ++w) M = fmaxf(M, red[w]);
-  __syncthreads();
-  float ls = 0.f;
-  if (M != -INFINITY) {
-    for (int i = tid; i < nq + NR; i += kAThreads) {
-      const float e = exp2f(sc[i] - M);
-      sc[i] = e;
-      ls += e;
+  if (*failed) return;  // uniform after the barrier
+  float ov = 0.f, Ls = 0.f;
+  if (tid < kD) {
+    for (int w = 0; w < kAWarps; ++w) {
+      ov += ored[w * kD + tid];
+      Ls += red[w];
     }
   }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, off);
-  if (lane == 0) red[warp] = ls;
-  __syncthreads();
-  float Ls = 0.f;
-  for (int w = 0; w < kAWarps; ++w) Ls += red[w];
 
-  // ---- values: warp per token (strided), lane = channels 4 lane .. 4 lane + 3 -----------
-  float o[4] = {0.f, 0.f, 0.f, 0.f};
-  float oz = 0.f;
-  const int gch = (lane * 4) / G;  // value channel group of this lane
-  const int ngv = kD / G;
-  for (int jl = warp; jl < nq; jl += kAWarps) {
-    const size_t j = bh * a.max_tokens + t0 + jl;
-    const float p = sc[jl];
-    const float wgt = p * h2f(__ldg(a.v_scale + j * ngv + gch));
-    const uint32_t byte = __ldg(a.v_codes + j * (kD / 4) + lane);
-    o[0] = fmaf(wgt, (float)(byte & 3u), o[0]);
-    o[1] = fmaf(wgt, (float)((byte >> 2) & 3u), o[1]);
-    o[2] = fmaf(wgt, (float)((byte >> 4) & 3u), o[2]);
-    o[3] = fmaf(wgt, (float)(byte >> 6), o[3]);
-    oz = fmaf(wgt, h2f(__ldg(a.v_zero + j * ngv + gch)), oz);
-  }
-  for (int r = warp; r < NR; r += kAWarps) {
-    const float p = sc[nq + r];
-    const uint2 v = __ldg(reinterpret_cast<const uint2*>(a.v_resid + (bh * a.residual + r) * kD + lane * 4));
-    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
-    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
-    o[0] = fmaf(p, f0.x, o[0]);
-    o[1] = fmaf(p, f0.y, o[1]);
-    o[2] = fmaf(p, f1.x, o[2]);
-    o[3] = fmaf(p, f1.y, o[3]);
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) ored[warp * kD + lane * 4 + i] = o[i] - oz;
-  __syncthreads();
-  float ov = 0.f;
-  if (tid < kD) {
-    for (int w = 0; w < kAWarps; ++w) ov += ored[w * kD + tid];
-  }
-
-  if (a.n_split == 1) {
+  if (n_total == 1) {
     if (tid < kD) {
       const float val = (Ls > 0.f) ? ov / Ls : 0.f;
       if (a.out_fp32) reinterpret_cast<float*>(a.out)[bh * kD + tid] = val;
@@ -303,7 +435,7 @@ __global__ void __launch_bounds__(kAThreads, 2) kivi_attn_kernel(const KiviAttnA
     }
     return;
   }
-  float* pp = a.part + (bh * a.n_split + split) * (kD + 2);
+  float* pp = a.part + (bh * n_total + split) * (kD + 2);
   if (tid < kD) pp[2 + tid] = ov;
   if (tid == 0) {
     pp[0] = M;
@@ -311,17 +443,17 @@ __global__ void __launch_bounds__(kAThreads, 2) kivi_attn_kernel(const KiviAttnA
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) *flag = (atomicAdd(&a.counters[bh], 1) == a.n_split - 1);
+  if (tid == 0) *flag = (atomicAdd(&a.counters[bh], 1) == n_total - 1);
   __syncthreads();
   if (!*flag) return;
   __threadfence();
   if (tid < kD) {
-    const float* base = a.part + bh * a.n_split * (kD + 2);
+    const float* base = a.part + bh * n_total * (kD + 2);
     float Mx = -INFINITY;
-    for (int s = 0; s < a.n_split; ++s) Mx = fmaxf(Mx, __ldcg(base + s * (kD + 2)));
+    for (int s = 0; s < n_total; ++s) Mx = fmaxf(Mx, __ldcg(base + s * (kD + 2)));
     float Lt = 0.f, acc = 0.f;
     if (Mx != -INFINITY) {
-      for (int s = 0; s < a.n_split; ++s) {
+      for (int s = 0; s < n_total; ++s) {
         const float ms = __ldcg(base + s * (kD + 2));
         if (ms == -INFINITY) continue;
         const float w = exp2f(ms - Mx);
@@ -338,13 +470,9 @@ __global__ void __launch_bounds__(kAThreads, 2) kivi_attn_kernel(const KiviAttnA
 
 }  // namespace
 
-int kivi_attn_max_tok_per_split(int residual) {
-  return (kKiviSmemLimit / 4 - kOffSc) - residual;
-}
+int kivi_attn_max_tok_per_split(int) { return 1 << 30; }  // tokens stream through the ring
 
-size_t kivi_attn_smem_bytes(int tok_per_split, int residual) {
-  return (size_t)(kOffSc + tok_per_split + residual) * 4;
-}
+size_t kivi_attn_smem_bytes(int, int residual) { return (size_t)kAOffSc + 4 * (size_t)max(kAChunk, residual); }
 
 cudaError_t launch_kivi_quantize(const KiviQuantArgs& a, cudaStream_t s) {
   // grid-stride warps; 8 blocks of 256 threads per SM keep enough rows in flight
@@ -365,7 +493,8 @@ cudaError_t launch_kivi_attn(const KiviAttnArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kivi_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)kD);
-  dim3 grid(a.n_split, a.B, a.H);
+  // quantized splits, plus one block for the fp16 residual segment
+  dim3 grid(a.n_split + (a.residual > 0 ? 1 : 0), a.B, a.H);
   kivi_attn_kernel<<<grid, kAThreads, smem, st>>>(a, scale_log2);
   return cudaGetLastError();
 }

@@ -111,23 +111,26 @@ struct KiviPlan {
   int n_split, tps;
 };
 
+// Quantized-token splits of the KIVI kernel (one more block per (request, head) takes the fp16
+// residual). Fill whole waves of blocks (about four resident per SM) and balance a split's
+// quantized tokens (96 B each) against the residual block's (512 B each).
 KiviPlan plan_kivi(const kvq_kivi_cfg* c, int B, int n_splits) {
-  const int tmax = kvq::kivi_attn_max_tok_per_split(c->residual) / c->group * c->group;
-  KiviPlan p{1, c->max_tokens};
   auto tps_for = [&](int n) {
     int t = (c->max_tokens + n - 1) / n;
     return (t + c->group - 1) / c->group * c->group;
   };
   if (n_splits > 0) return KiviPlan{n_splits, tps_for(n_splits)};
   if (c->max_tokens == 0) return KiviPlan{1, 0};
-  const int sms = sm_count();
+  const int slots = 4 * sm_count();
+  const int extra = c->residual > 0 ? 1 : 0;
+  const double resid_cost = c->residual * (512.0 / 96.0);
+  KiviPlan p{1, tps_for(1)};
   double best = 1e300;
   for (int n = 1; n <= std::min(64, c->max_tokens / c->group); ++n) {
     const int tps = tps_for(n);
-    if (tps > tmax) continue;
-    const long long blocks = (long long)B * c->n_heads * n;
-    const long long waves = (blocks + 2 * sms - 1) / (2 * sms);  // two blocks per SM
-    const double cost = (double)waves * (tps + 256.0 + (n > 1 ? 32.0 : 0.0));
+    const long long blocks = (long long)B * c->n_heads * (n + extra);
+    const long long waves = (blocks + slots - 1) / slots;
+    const double cost = (double)waves * (std::max((double)tps, resid_cost) + 64.0);
     if (cost < best * 0.999) {
       best = cost;
       p = KiviPlan{n, tps};
@@ -137,8 +140,9 @@ KiviPlan plan_kivi(const kvq_kivi_cfg* c, int B, int n_splits) {
 }
 
 size_t kivi_ws_bytes(const kvq_kivi_cfg* c, int B, const KiviPlan& p) {
-  if (p.n_split <= 1) return 0;
-  return align256((size_t)B * c->n_heads * p.n_split * (kvq::kD + 2) * sizeof(float)) +
+  const int total = p.n_split + (c->residual > 0 ? 1 : 0);
+  if (total <= 1) return 0;
+  return align256((size_t)B * c->n_heads * total * (kvq::kD + 2) * sizeof(float)) +
          align256((size_t)B * c->n_heads * sizeof(int));
 }
 
@@ -471,10 +475,11 @@ KVQ_API kvq_status kvq_decode_attn(int format, const void* cfg, const void* cach
     a.v_codes = k->v_codes; a.v_scale = k->v_scale; a.v_zero = k->v_zero;
     a.k_resid = k->k_resid; a.v_resid = k->v_resid; a.n_quant = k->n_quant; a.n_resid = k->n_resid;
     a.q = q; a.out = out; a.out_fp32 = (out_dtype == KVQ_OUT_FP32);
-    if (p.n_split > 1) {
+    const int total = p.n_split + (c->residual > 0 ? 1 : 0);  // blocks per (request, head)
+    if (total > 1) {
       a.part = static_cast<float*>(ws);
       a.counters = reinterpret_cast<int*>(static_cast<char*>(ws) +
-                                          align256((size_t)B * c->n_heads * p.n_split * (kvq::kD + 2) * sizeof(float)));
+                                          align256((size_t)B * c->n_heads * total * (kvq::kD + 2) * sizeof(float)));
     }
     a.err = device_error_ptr();
     a.B = B; a.H = c->n_heads; a.max_tokens = c->max_tokens; a.residual = c->residual; a.group = c->group;

@@ -5,7 +5,7 @@ One step = one generated token through the whole looped stack: 4 loop steps x 24
 recent per request), each layer with its own cache. Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload loopvq_b64_6k|loopvq_b8_32k|kivi_b16_4k|encode_32k|kivi_quant_32k]
+                    [--workload loopvq_b64_6k|loopvq_b8_32k|kivi_b16_4k|stream_b64_6k|encode_32k|kivi_quant_32k]
 
 Under torchrun each rank runs its own replica on its own GPU (requests shard across GPUs
 with no collective on the data path); rank 0 prints the max-over-ranks timing.
@@ -43,6 +43,11 @@ WORKLOADS = {
     "kivi_b16_4k": dict(kind="kivi", B=16, H=32, n_quant=3968, n_resid=128, layers=32,
                         name="KIVI 2-bit decode attention, Llama-2-7B-shaped: 32 layers, 32 heads, batch 16, "
                              "context 4096 = 3968 quantized + 128 fp16"),
+    "stream_b64_6k": dict(kind="stream", B=64, H=16, L=6144, layers=24, T=4, Tc=2, G=16, recent=64,
+                          rho=(0.69, 0.94),
+                          name="LoopVQ 0.5-bit streaming decode, Ouro-1.4B-shaped: per generated token 24 layers x "
+                               "4 loop steps of bf16 append + decode attention, page roll every 8 tokens, "
+                               "batch 64 from context 6144"),
     "encode_32k": dict(kind="encode", H=16, L=32768, T=4, Tc=2, G=16, groups=8,
                        name="LoopVQ prefill encode: 16 heads x 8 groups x 2 loop blocks x 32768 tokens"),
     "kivi_quant_32k": dict(kind="kivi_quant", H=16, L=32768,
@@ -214,14 +219,16 @@ def vq_call_bytes(B, H, n_pages, n_win, NB_unused=None):
     return idx + win + bt + rope + qo
 
 
-def setup_loopvq(wl, dev, seed):
+def setup_loopvq(wl, dev, seed, extra_tokens=0):
+    """LoopVQ cache of the workload, prefilled to L tokens per request (room for
+    ``extra_tokens`` more, for streaming)."""
     import torch
     import synth
     from sub_bit_quantized_gb300 import kvq
     B, H, L, NL, T, Tc, G, W = wl["B"], wl["H"], wl["L"], wl["layers"], wl["T"], wl["Tc"], wl["G"], wl["recent"]
     n_pages = max(0, (L - 8 - W) // 8)
-    cfg = kvq.VqConfig(T=T, Tc=Tc, G=G, n_layers=NL, n_heads=H, recent=W, max_pages=n_pages, max_batch=B,
-                       max_ctx=L)
+    cfg = kvq.VqConfig(T=T, Tc=Tc, G=G, n_layers=NL, n_heads=H, recent=W,
+                       max_pages=n_pages + (extra_tokens + 7) // 8, max_batch=B, max_ctx=L + extra_tokens)
     cache = kvq.VqCache(cfg, dev)
     gen = torch.Generator(device=dev).manual_seed(seed)
     rhos = synth.rho_schedule(T, *wl["rho"])
@@ -431,6 +438,66 @@ def run_ours(args, wl, rank, world, dist, pool):
             result["cpu_baseline"] = {"value": round(cgbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                       "sample": f"{n_pairs} (request, head) units (8 calls' worth), fp64 NumPy "
                                                 f"oracle, {wall:.1f} s wall on {cores} processes"}
+        return result
+
+    if wl["kind"] == "stream":
+        # a step = one generated token: for every (layer, loop step) the new token's K/V is
+        # appended in bf16 and the step's decode attention runs; every 8 tokens the append of
+        # the token's last (layer, step) also encodes the oldest recent page into index pages
+        B, H, NL, T = wl["B"], wl["H"], wl["layers"], wl["T"]
+        n_tok = args.warmup + 2 * args.steps + 16
+        cfg, cache, _, _ = setup_loopvq(wl, dev, 1234 + rank, extra_tokens=n_tok)
+        gen = torch.Generator(device=dev).manual_seed(77 + rank)
+        kn = torch.randn((B, H, D), generator=gen, device=dev).to(torch.bfloat16)
+        vn = torch.randn((B, H, D), generator=gen, device=dev).to(torch.bfloat16)
+        q = torch.randn((B, H, D), generator=gen, device=dev).to(torch.bfloat16)
+        out = torch.empty((B, H, D), dtype=torch.bfloat16, device=dev)
+        ws = kvq.make_workspace(cfg, B, 0, dev)
+        calls = {(l, t): kvq.DecodeCall(cfg, cache, l, t, q, out, 0, ws, stream)
+                 for l in range(NL) for t in range(1, T + 1)}
+
+        def token(attend=True):
+            for l in range(NL):
+                for t in range(1, T + 1):
+                    kvq.kvq_append_page(cfg, cache, l, t, kn, vn, stream)
+                    if attend:
+                        calls[(l, t)]()
+
+        for _ in range(args.warmup):
+            token()
+        torch.cuda.synchronize()
+        with ClockSampler(gpu_index) as cs:
+            ms = time_region(token, args.steps, stream, dist, nvtx_name="timed") / args.steps
+        # the same 96 attention calls without appends (the cache stops growing), then per-token
+        # events over 16 more tokens: tokens whose first append rolls a page vs the others
+        ms_attn = time_region(lambda: [c() for c in calls.values()], args.steps, stream, dist) / args.steps
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(17)]
+        rolled = []
+        for i in range(16):
+            Lb = int(cache.seq_len[0].item())  # length before this token
+            np_b = int(cache.n_pages[0].item())
+            rolled.append(Lb + 1 - 8 - 8 * np_b == wl["recent"] + 8)  # the first append advances, then rolls
+            ev[i].record(stream)
+            token()
+        ev[16].record(stream)
+        torch.cuda.synchronize()
+        assert kvq.device_error() == 0
+        tms = [ev[i].elapsed_time(ev[i + 1]) for i in range(16)]
+        plain = statistics.median([t for t, r in zip(tms, rolled) if not r])
+        roll_extra = statistics.mean([t - plain for t, r in zip(tms, rolled) if r]) if any(rolled) else 0.0
+        L_end = int(cache.seq_len[0].item())
+        result.update(dict(value=round(B * world / (ms * 1e-3), 1), unit="tokens/s", ms_per_step=round(ms, 4),
+                           attention_only_ms_per_token=round(ms_attn, 4),
+                           append_roll_overhead_fraction=round((ms - ms_attn) / ms, 4),
+                           roll_ms_per_roll=round(roll_extra, 4),
+                           roll_fraction_amortized=round(roll_extra / 8 / ms, 5),
+                           # per token: NL*T appends, the roll's 2 launches (at the first append;
+                           # they leave at once unless a page is due), 2 launches per attention call
+                           higher_is_better=True, gpu_launches=args.steps * (NL * T * 3 + 2),
+                           context_end=L_end, clocks=cs.summary(),
+                           roofline={"bound": "hbm", "achieved": None, "peak": hbm_peak, "unit": "GB/s",
+                                     "frac": None, "traffic": None,
+                                     "note": "per-call rooflines: workloads loopvq_b64_6k (attention), encode_32k"}))
         return result
 
     if wl["kind"] == "encode":

@@ -99,6 +99,25 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// ---- exact-enough distances without fp64 -----------------------------------------------
+// hi + lo += (z - e)^2 with error-free steps: z - e = s + t exactly (two-sum), s^2 = p + q
+// exactly (fma), hi + p = h + err exactly (two-sum); the low parts gather in lo. The sum of
+// 8..32 such terms keeps a relative error near one fp32 rounding (~1e-7), far below the 1e-6
+// tie threshold, without fp64 arithmetic (slow on this GPU).
+__device__ __forceinline__ void add_sq_diff(float z, float e, float& hi, float& lo) {
+  const float s = __fsub_rn(z, e);
+  const float bb = __fsub_rn(s, z);
+  const float t = __fadd_rn(__fsub_rn(z, __fsub_rn(s, bb)), __fsub_rn(-e, bb));
+  const float p = __fmul_rn(s, s);
+  const float q = __fmaf_rn(s, s, -p);
+  const float r = __fmaf_rn(__fmul_rn(2.f, s), t, q);
+  const float h = __fadd_rn(hi, p);
+  const float b2 = __fsub_rn(h, hi);
+  const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(h, b2)), __fsub_rn(p, b2));
+  hi = h;
+  lo = __fadd_rn(lo, __fadd_rn(err, r));
+}
+
 // ---- streaming loads (read-once data: do not keep in L1) -------------------------------
 __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));

@@ -9,12 +9,10 @@
 //    8-token index pages; during decode the oldest recent page is encoded every 8 tokens;
 //  * method step 5: the per-loop-step codebook slice B_t is cut once at load time.
 //
-// Roll encode arithmetic (one page of 8 tokens per (layer, block, head), on CUDA cores):
-// fp32 distances sum_k (z_k - e_k)^2 screen the 256 codewords (relative error below 1.1e-6
-// for nonnegative sums of 16..32 fp32 terms); every candidate within 4e-6 (relative) of the
-// fp32 minimum is re-evaluated in fp64, where bf16 inputs and fp32 entries subtract and
-// square exactly. The result is the exact-arithmetic argmin with the lowest index on ties; a
-// second-best fp64 distance within 1e-6 of the best counts as a tie.
+// Roll encode arithmetic (one page of 8 tokens per (layer, block, head), on CUDA cores): the
+// same decision rule as the prefill encode: fp32 screening of z.e - |e|^2 / 2, and every vector
+// whose runner-up is inside the error band is decided on distances summed with error-free
+// fp32 steps; the lowest index wins exact ties.
 #include <cuda_fp16.h>
 
 #include "kvq_common.cuh"
@@ -73,62 +71,6 @@ __global__ void slice_fp16_kernel(const float* __restrict__ cb, __half* __restri
     const int beta = t0 / Tc, m = t0 % Tc, g = ch / c, i = ch % c;
     bt16[k] = __float2half_rn(cb[((((size_t)l * NB + beta) * H + h) * NG + g) * (size_t)kCB * G + (size_t)r * G + i * Tc + m]);
   }
-}
-
-// ---------------------------------------------------------------- exact nearest codeword
-// z: G floats (bf16 values, exact in fp32); e: codebook [256][G] (global or shared).
-// Returns the index; *tie set when the runner-up is within 1e-6 (relative) in fp64.
-template <int G>
-__device__ __forceinline__ int nearest_exact(const float (&z)[G], const float* __restrict__ e, bool* tie) {
-  float best = INFINITY, second = INFINITY;
-  int bi = 0;
-  for (int r = 0; r < kCB; ++r) {
-    const float* er = e + r * G;
-    float d = 0.f;
-#pragma unroll
-    for (int k = 0; k < G; ++k) {
-      const float df = z[k] - er[k];
-      d = fmaf(df, df, d);
-    }
-    if (d < best) {
-      second = best;
-      best = d;
-      bi = r;
-    } else if (d < second) {
-      second = d;
-    }
-  }
-  *tie = false;
-  const float band = best * 4e-6f + 1e-30f;
-  if (second > best + band) return bi;  // unique winner, no candidate near it
-  // refine every candidate inside the band in fp64
-  double b64 = INFINITY, s64 = INFINITY;
-  int b64i = kCB;
-  for (int r = 0; r < kCB; ++r) {
-    const float* er = e + r * G;
-    float d = 0.f;
-#pragma unroll
-    for (int k = 0; k < G; ++k) {
-      const float df = z[k] - er[k];
-      d = fmaf(df, df, d);
-    }
-    if (d > best + band) continue;
-    double dd = 0.0;
-#pragma unroll
-    for (int k = 0; k < G; ++k) {
-      const double df = (double)z[k] - (double)er[k];
-      dd = fma(df, df, dd);
-    }
-    if (dd < b64) {  // strict: the lowest index wins exact ties
-      s64 = b64;
-      b64 = dd;
-      b64i = r;
-    } else if (dd < s64) {
-      s64 = dd;
-    }
-  }
-  *tie = (s64 <= b64 * (1.0 + 1e-6));
-  return b64i;
 }
 
 __device__ __forceinline__ size_t page_byte(int g, int j) {  // in-page byte of (group, token)
@@ -206,42 +148,134 @@ __device__ __forceinline__ bool roll_due(const int32_t* seq_len, const int32_t* 
   return (L - sink - kPage * np == recent + kPage) && (np < max_pages);
 }
 
-// Roll: one block per (layer, block beta, head, K/V, sequence); 8 tokens x 16 groups.
+// Roll: one block per (layer, block beta, head, K/V, group). The block stages that group's
+// codebook (and each codeword's |e|^2 / 2) in shared memory once and encodes the oldest recent
+// page (8 tokens) of every due sequence against it, two vectors per thread: every codeword
+// row read (a broadcast: all threads of a warp read the same row) serves both. Screening uses
+// acc_r = z.e_r - |e_r|^2 / 2 (one FMA per coordinate; larger is nearer); a vector whose
+// runner-up lies within the error band of its best (8x the fp32 accumulation bound of the
+// codewords that can compete, plus the 1e-6 tie threshold) is decided on distances summed
+// with error-free fp32 steps, the lowest index winning exact ties.
 template <int TC>
-__global__ void __launch_bounds__(128) roll_kernel(const VqRollArgs a) {
+__global__ void __launch_bounds__(256) roll_kernel(const VqRollArgs a) {
   constexpr int G = TC * kC;
-  const int b = blockIdx.y;
-  if (!roll_due(a.seq_len, a.n_pages, b, a.sink, a.recent, a.max_pages)) return;
+  __shared__ __align__(16) float cbs[kCB * G];
+  __shared__ float nh[kCB];
   int q = blockIdx.x;
+  const int g = q % kNG; q /= kNG;
   const int kv = q % 2; q /= 2;
   const int h = q % a.H; q /= a.H;
   const int beta = q % a.NB; q /= a.NB;
   const int l = q;
-  const int np = a.n_pages[b];
-  const int j = threadIdx.x / kNG, g = threadIdx.x % kNG;  // token in page, group
-  const int p = a.sink + kPage * np + j;                   // position of the token
-  const int slot = a.sink + (p - a.sink) % (a.recent + kPage);
+  // between rolls no sequence is due: leave before staging anything
+  int any = 0;
+  for (int b = threadIdx.x; b < a.n_seq; b += blockDim.x)
+    any |= roll_due(a.seq_len, a.n_pages, b, a.sink, a.recent, a.max_pages) ? 1 : 0;
+  if (!__syncthreads_or(any)) return;
+  const float* cb = (kv ? a.cb_v : a.cb_k) + ((((size_t)l * a.NB + beta) * a.H + h) * kNG + g) * (size_t)kCB * G;
+  for (int k = threadIdx.x; k < kCB * G / 4; k += blockDim.x)
+    reinterpret_cast<float4*>(cbs)[k] = __ldg(reinterpret_cast<const float4*>(cb) + k);
+  for (int r = threadIdx.x; r < kCB; r += blockDim.x) {
+    float n_hi = 0.f, n_lo = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < G; ++k) add_sq_diff(__ldg(cb + (size_t)r * G + k), 0.f, n_hi, n_lo);
+    nh[r] = 0.5f * __fadd_rn(n_hi, n_lo);
+  }
+  __syncthreads();
   const uint16_t* win = kv ? a.win_v : a.win_k;
-  float z[G];
+  uint8_t* idx_base = (kv ? a.idx_v : a.idx_k) + (((size_t)l * a.NB + beta) * a.max_batch) * a.H * (size_t)a.max_pages * kPageBytes;
+  const int n_vec = a.n_seq * kPage;
+  for (int v0 = threadIdx.x; v0 < n_vec; v0 += 2 * blockDim.x) {
+    // ---- the two vectors (sequence, token in page) of this thread ------------------------
+    float z[2][G];
+    bool live[2];
+    int b_of[2], np_of[2], j_of[2];
 #pragma unroll
-  for (int m = 0; m < TC; ++m) {
-    const int t0 = beta * TC + m;
-    const uint16_t* xp =
-        win + (((((size_t)l * a.T + t0) * a.max_batch + b) * a.H + h) * a.win_slots + slot) * kD + g * kC;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(xp));
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int u = 0; u < 2; ++u) {
+      const int v = v0 + u * blockDim.x;
+      const int b = min(v, n_vec - 1) / kPage, j = v % kPage;
+      live[u] = v < n_vec && roll_due(a.seq_len, a.n_pages, b, a.sink, a.recent, a.max_pages);
+      const int np = a.n_pages[b];
+      b_of[u] = b;
+      np_of[u] = np;
+      j_of[u] = j;
+      const int p = a.sink + kPage * np + j;  // position of the token
+      const int slot = a.sink + (p - a.sink) % (a.recent + kPage);
 #pragma unroll
-    for (int i = 0; i < kC; ++i) {
-      const uint32_t bits = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu);
-      z[i * TC + m] = bf16_to_f32(bits);
+      for (int m = 0; m < TC; ++m) {
+        uint4 w4 = make_uint4(0, 0, 0, 0);
+        if (live[u]) {
+          const int t0 = beta * TC + m;
+          const uint16_t* xp =
+              win + (((((size_t)l * a.T + t0) * a.max_batch + b) * a.H + h) * a.win_slots + slot) * kD + g * kC;
+          w4 = __ldg(reinterpret_cast<const uint4*>(xp));
+        }
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int i = 0; i < kC; ++i) z[u][i * TC + m] = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
+      }
+    }
+    // ---- screening: best two of acc_r = z.e_r - |e_r|^2/2 for both vectors ---------------
+    float best[2] = {-INFINITY, -INFINITY}, second[2] = {-INFINITY, -INFINITY};
+    int bi[2] = {0, 0};
+#pragma unroll 2
+    for (int r = 0; r < kCB; ++r) {
+      const float4* er = reinterpret_cast<const float4*>(cbs + r * G);
+      float acc0 = -nh[r], acc1 = acc0;
+#pragma unroll
+      for (int k4 = 0; k4 < G / 4; ++k4) {
+        const float4 e = er[k4];
+        acc0 = fmaf(z[0][4 * k4], e.x, acc0);
+        acc1 = fmaf(z[1][4 * k4], e.x, acc1);
+        acc0 = fmaf(z[0][4 * k4 + 1], e.y, acc0);
+        acc1 = fmaf(z[1][4 * k4 + 1], e.y, acc1);
+        acc0 = fmaf(z[0][4 * k4 + 2], e.z, acc0);
+        acc1 = fmaf(z[1][4 * k4 + 2], e.z, acc1);
+        acc0 = fmaf(z[0][4 * k4 + 3], e.w, acc0);
+        acc1 = fmaf(z[1][4 * k4 + 3], e.w, acc1);
+      }
+      const float accs[2] = {acc0, acc1};
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        second[u] = fmaxf(second[u], fminf(accs[u], best[u]));
+        bi[u] = (accs[u] > best[u]) ? r : bi[u];
+        best[u] = fmaxf(best[u], accs[u]);
+      }
+    }
+    // ---- band check; exact decision of near-ties; index out ----------------------------------
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (!live[u]) continue;
+      float z2 = 0.f;
+#pragma unroll
+      for (int k = 0; k < G; ++k) z2 = fmaf(z[u][k], z[u][k], z2);
+      const float znorm = sqrtf(z2);
+      const float dbest = fmaxf(0.f, z2 - 2.f * best[u]);
+      const float enear = znorm + 1.01f * sqrtf(dbest) + 1e-3f * znorm + 1e-6f;
+      const float band = 8.f * (G + 2) * 5.97e-8f * (znorm * enear + 0.5f * enear * enear) + 1e-6f * dbest + 1e-30f;
+      int result = bi[u];
+      if (second[u] >= best[u] - band) {
+        float bd = INFINITY;
+        for (int r = 0; r < kCB; ++r) {
+          const float* er = cbs + r * G;
+          float acc = -nh[r];  // the screening value again, computed the same way
+#pragma unroll
+          for (int k = 0; k < G; ++k) acc = fmaf(z[u][k], er[k], acc);
+          if (acc < best[u] - band) continue;
+          float dh = 0.f, dl = 0.f;
+#pragma unroll
+          for (int k = 0; k < G; ++k) add_sq_diff(z[u][k], er[k], dh, dl);
+          const float dd = __fadd_rn(dh, dl);
+          if (dd < bd) {  // increasing r: the lowest index wins exact ties
+            bd = dd;
+            result = r;
+          }
+        }
+      }
+      idx_base[((size_t)b_of[u] * a.H + h) * (size_t)a.max_pages * kPageBytes + (size_t)np_of[u] * kPageBytes +
+               page_byte(g, j_of[u])] = (uint8_t)result;
     }
   }
-  const float* cb = (kv ? a.cb_v : a.cb_k) + ((((size_t)l * a.NB + beta) * a.H + h) * kNG + g) * (size_t)kCB * G;
-  bool tie;
-  const int r = nearest_exact<G>(z, cb, &tie);
-  uint8_t* idx = (kv ? a.idx_v : a.idx_k) +
-                 ((((size_t)l * a.NB + beta) * a.max_batch + b) * a.H + h) * (size_t)a.max_pages * kPageBytes;
-  idx[(size_t)np * kPageBytes + page_byte(g, j)] = (uint8_t)r;
 }
 
 __global__ void roll_commit_kernel(const VqRollArgs a) {
@@ -288,11 +322,11 @@ cudaError_t launch_vq_append(const VqAppendArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_vq_roll(const VqRollArgs& a, cudaStream_t s) {
-  dim3 grid(a.L * a.NB * a.H * 2, a.n_seq);
+  dim3 grid(a.L * a.NB * a.H * 2 * kNG);
   switch (a.Tc) {
-    case 1: roll_kernel<1><<<grid, 128, 0, s>>>(a); break;
-    case 2: roll_kernel<2><<<grid, 128, 0, s>>>(a); break;
-    case 4: roll_kernel<4><<<grid, 128, 0, s>>>(a); break;
+    case 1: roll_kernel<1><<<grid, 256, 0, s>>>(a); break;
+    case 2: roll_kernel<2><<<grid, 256, 0, s>>>(a); break;
+    case 4: roll_kernel<4><<<grid, 256, 0, s>>>(a); break;
     default: return cudaErrorInvalidValue;
   }
   cudaError_t e = cudaGetLastError();

@@ -344,11 +344,18 @@ def time_region(fn, steps, stream, dist, nvtx_name=None):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     if dist:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, "cuda")
         torch.distributed.barrier()
     return ms
+
+
+def max_over_ranks(value: float, device="cpu") -> float:
+    """The largest ``value`` over all ranks of the default process group (every rank gets it):
+    the whole job takes as long as its slowest replica."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
 
 
 def run_ours(args, wl, rank, world, dist, pool):

@@ -1,10 +1,11 @@
-"""KIVI: asymmetric 2-bit group quantization (keys per channel, values per token), its
-dequantization and decode attention over the quantized + fp16 residual cache
-(oracle; test infrastructure only).
+"""KIVI: asymmetric 2- or 4-bit group quantization (keys per channel, values per token), its
+dequantization, decode attention over the quantized + fp16 residual cache, grouped-query
+head mapping and the streaming cache of Algorithm 1 (oracle; test infrastructure only).
 
 Source: "KIVI 完全拆解：非对称 2-bit KV Cache 量化" (walkthrough of the KIVI paper):
 the quantize / dequantize formula (section on per-token and per-channel quantization),
-the grouped + residual cache and eq. (3) (core design section), the memory accounting.
+the grouped + residual cache, eq. (3) and Algorithm 1 (core design section), the memory
+accounting, the configurable bit widths and GQA (implementation section).
 
 Readings where the page is silent (each listed in the design doc):
 * The scale splits [min, max] evenly: s = (max - min) / (2^b - 1); the zero-point is
@@ -135,3 +136,112 @@ def decode_attention(q, k_codes, k_scale, k_zero, v_codes, v_scale, v_zero,
     K = np.concatenate([Kg, np.asarray(k_resid, np.float64).reshape(-1, D)], axis=0)
     V = np.concatenate([Vg, np.asarray(v_resid, np.float64).reshape(-1, D)], axis=0)
     return softmax_attention(q, K, V, 1.0 / np.sqrt(D))
+
+
+# ------------------------------------------------------------------ grouped-query attention
+
+def kv_head(h_q: int, n_q_heads: int, n_kv_heads: int) -> int:
+    """KV head read by query head ``h_q`` under grouped-query attention.
+
+    KIVI page, implementation section: the code base gained GQA support (the Llama-3
+    family). Reading: the usual GQA layout, where each run of n_q_heads / n_kv_heads
+    consecutive query heads shares one KV head, so query head h reads KV head
+    h // (n_q_heads / n_kv_heads). With n_q_heads == n_kv_heads this is multi-head attention.
+    """
+    assert n_q_heads % n_kv_heads == 0 and 0 <= h_q < n_q_heads
+    return h_q // (n_q_heads // n_kv_heads)
+
+
+# ------------------------------------------------------------------ streaming (Algorithm 1)
+
+class KiviStream:
+    """The cache of one (request, KV head) as the page's Algorithm 1 builds it.
+
+    KIVI page, core design section and Algorithm 1: the prefill quantizes all but the
+    last R tokens (keys per channel in groups of G tokens, values per token) and keeps the
+    last R in fp16; each decode token enters the fp16 residuals; a full key residual is
+    quantized whole and appended to the grouped keys; the value window keeps the newest R
+    tokens and quantizes the token that falls out of it.
+
+    Readings where the pseudo-code leaves a step open:
+    * Key flush timing. The prefill leaves R keys in the residual, and the pseudo-code's
+      test "len == R" after appending would then never fire. Taken here: a key residual
+      that already holds R tokens when a new token arrives is quantized and appended to the
+      grouped keys, and the new token starts a fresh residual. The key residual therefore
+      holds 1 to R tokens during decoding, always flushed in whole groups of G.
+    * Prefill length. X_Kg = X_K[: l - R] needs l - R to be a multiple of G for the key
+      groups. For other lengths the quantized prefix is l - R rounded up to a multiple of G
+      (so the residuals never exceed R); for l <= R nothing is quantized. The values use
+      the same prefix at prefill, then evict one token per decode step once the window
+      exceeds R (pseudo-code: X_Vr[:-R] is quantized).
+    Codes, scales and zero-points are those of quantize_keys / quantize_values; the bit
+    widths of keys and values are set separately (implementation section: K and V bits
+    are independently configurable, 2 or 4).
+    """
+
+    def __init__(self, D: int = 128, group: int = 32, residual: int = 128, k_bits: int = 2, v_bits: int = 2):
+        assert residual % group == 0 and D % group == 0
+        self.D, self.G, self.R = D, group, residual
+        self.k_bits, self.v_bits = k_bits, v_bits
+        z_i = np.zeros((0, D), np.int64)
+        self.k_codes, self.k_scale, self.k_zero = z_i, np.zeros((0, D), np.float16), np.zeros((0, D), np.float16)
+        self.v_codes = z_i
+        self.v_scale = np.zeros((0, D // group), np.float16)
+        self.v_zero = np.zeros((0, D // group), np.float16)
+        self.k_resid = np.zeros((0, D), np.float16)
+        self.v_resid = np.zeros((0, D), np.float16)
+
+    @property
+    def n_quant_k(self) -> int:
+        return len(self.k_codes)
+
+    @property
+    def n_quant_v(self) -> int:
+        return len(self.v_codes)
+
+    @property
+    def n_tok(self) -> int:
+        return self.n_quant_k + len(self.k_resid)
+
+    def _push_keys(self, K):
+        c, s, z = quantize_keys(K, self.G, self.k_bits)
+        self.k_codes = np.concatenate([self.k_codes, c])
+        self.k_scale = np.concatenate([self.k_scale, s])
+        self.k_zero = np.concatenate([self.k_zero, z])
+
+    def _push_values(self, V):
+        c, s, z = quantize_values(V, self.G, self.v_bits)
+        self.v_codes = np.concatenate([self.v_codes, c])
+        self.v_scale = np.concatenate([self.v_scale, s])
+        self.v_zero = np.concatenate([self.v_zero, z])
+
+    def prefill(self, K, V) -> None:
+        """Cache the l prompt tokens K, V ([l][D] fp16) of an empty stream."""
+        assert self.n_tok == 0
+        K = np.asarray(K, np.float16)
+        V = np.asarray(V, np.float16)
+        l = K.shape[0]
+        nq = 0 if l <= self.R else -(-(l - self.R) // self.G) * self.G
+        if nq:
+            self._push_keys(K[:nq])
+            self._push_values(V[:nq])
+        self.k_resid = K[nq:].copy()
+        self.v_resid = V[nq:].copy()
+
+    def append(self, k, v) -> None:
+        """One decode token: k, v [D] fp16."""
+        k = np.asarray(k, np.float16).reshape(1, self.D)
+        v = np.asarray(v, np.float16).reshape(1, self.D)
+        if len(self.k_resid) == self.R:            # full key residual: quantize it whole
+            self._push_keys(self.k_resid)
+            self.k_resid = self.k_resid[:0]
+        self.k_resid = np.concatenate([self.k_resid, k])
+        self.v_resid = np.concatenate([self.v_resid, v])
+        if len(self.v_resid) > self.R:              # value window overflow: oldest token out
+            self._push_values(self.v_resid[:-self.R])
+            self.v_resid = self.v_resid[-self.R:]
+
+    def attention(self, q) -> np.ndarray:
+        """Decode attention of query q [D] over this stream (eq. (3), one softmax)."""
+        return decode_attention(q, self.k_codes, self.k_scale, self.k_zero, self.v_codes, self.v_scale,
+                                self.v_zero, self.k_resid, self.v_resid, self.G)

@@ -5,7 +5,8 @@ One step = one generated token through the whole looped stack: 4 loop steps x 24
 recent per request), each layer with its own cache. Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload loopvq_b64_6k|loopvq_b8_32k|kivi_b16_4k|stream_b64_6k|encode_32k|kivi_quant_32k]
+                    [--workload loopvq_b64_6k|loopvq_b8_32k|kivi_b16_4k|kivi4_gqa_b16_4k|stream_b64_6k|
+                                kivi_stream_b16_4k|encode_32k|kivi_quant_32k]
 
 Under torchrun each rank runs its own replica on its own GPU (requests shard across GPUs
 with no collective on the data path); rank 0 prints the max-over-ranks timing.
@@ -13,6 +14,7 @@ with no collective on the data path); rank 0 prints the max-over-ranks timing.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import multiprocessing as mp
@@ -43,6 +45,14 @@ WORKLOADS = {
     "kivi_b16_4k": dict(kind="kivi", B=16, H=32, n_quant=3968, n_resid=128, layers=32,
                         name="KIVI 2-bit decode attention, Llama-2-7B-shaped: 32 layers, 32 heads, batch 16, "
                              "context 4096 = 3968 quantized + 128 fp16"),
+    "kivi4_gqa_b16_4k": dict(kind="kivi", B=16, H=8, Hq=32, k_bits=4, v_bits=4, n_quant=3968, n_resid=128,
+                             layers=32,
+                             name="KIVI-4 decode attention with GQA, Llama-3-8B-shaped: 32 layers, 32 query heads "
+                                  "over 8 KV heads, 4-bit K and V, batch 16, context 4096 = 3968 quantized + 128 fp16"),
+    "kivi_stream_b16_4k": dict(kind="kivi_stream", B=16, H=32, n_quant=3968, n_resid=128, layers=32,
+                               name="KIVI 2-bit streaming decode, Llama-2-7B-shaped: per generated token 32 layers "
+                                    "of fp16 append (a whole key residual quantized every 128 tokens, one value "
+                                    "quantized per token) + decode attention, batch 16 from context 4096"),
     "stream_b64_6k": dict(kind="stream", B=64, H=16, L=6144, layers=24, T=4, Tc=2, G=16, recent=64,
                           rho=(0.69, 0.94),
                           name="LoopVQ 0.5-bit streaming decode, Ouro-1.4B-shaped: per generated token 24 layers x "
@@ -156,16 +166,16 @@ def _oracle_vq_job(args):
 
 
 def _oracle_kivi_job(args):
-    seed, n_pairs, nq, nr = args
+    seed, n_pairs, nq, nr, kb, vb = args
     import numpy as np
     import synth
     from oracle import kivi as okivi
     g = synth.rng(seed)
     inputs = []
     for _ in range(n_pairs):
-        inputs.append((g.standard_normal(D), g.integers(0, 4, (nq, D)),
+        inputs.append((g.standard_normal(D), g.integers(0, 2 ** kb, (nq, D)),
                        (np.abs(g.standard_normal((nq // 32, D))) + 0.05).astype(np.float16),
-                       g.standard_normal((nq // 32, D)).astype(np.float16), g.integers(0, 4, (nq, D)),
+                       g.standard_normal((nq // 32, D)).astype(np.float16), g.integers(0, 2 ** vb, (nq, D)),
                        (np.abs(g.standard_normal((nq, D // 32))) + 0.05).astype(np.float16),
                        g.standard_normal((nq, D // 32)).astype(np.float16),
                        g.standard_normal((nr, D)).astype(np.float16), g.standard_normal((nr, D)).astype(np.float16)))
@@ -188,7 +198,7 @@ def cpu_oracle(wl, bytes_per_unit, unit_pairs_total, n_pairs, pool=None):
         if wl["kind"] == "loopvq":
             jobs.append((1000 + k, n, wl["L"], wl["T"], wl["Tc"], wl["G"], wl["recent"]))
         else:
-            jobs.append((1000 + k, n, wl["n_quant"], wl["n_resid"]))
+            jobs.append((1000 + k, n, wl["n_quant"], wl["n_resid"], wl.get("k_bits", 2), wl.get("v_bits", 2)))
         done += n
         k += 1
     fn = _oracle_vq_job if wl["kind"] == "loopvq" else _oracle_kivi_job
@@ -262,11 +272,20 @@ def setup_loopvq(wl, dev, seed, extra_tokens=0):
     return cfg, cache, n_pages, (L - 8 * n_pages)
 
 
-def setup_kivi(wl, dev, seed):
+def kivi_cfg(wl, extra_tokens=0):
+    from sub_bit_quantized_gb300 import kvq
+    return kvq.KiviConfig(n_heads=wl["H"], n_q_heads=wl.get("Hq", wl["H"]), k_bits=wl.get("k_bits", 2),
+                          v_bits=wl.get("v_bits", 2), residual=wl["n_resid"], max_batch=wl["B"],
+                          max_tokens=wl["n_quant"] + extra_tokens)
+
+
+def setup_kivi(wl, dev, seed, extra_tokens=0):
+    """One KIVI cache per layer, filled by the library's prefill from random fp16 K/V
+    (keys with 6 outlier channels scaled 20x): n_quant quantized + n_resid fp16 tokens."""
     import torch
     from sub_bit_quantized_gb300 import kvq
     B, H, NQ, NR, NL = wl["B"], wl["H"], wl["n_quant"], wl["n_resid"], wl["layers"]
-    cfg = kvq.KiviConfig(n_heads=H, residual=NR, max_batch=B, max_tokens=NQ)
+    cfg = kivi_cfg(wl, extra_tokens)
     gen = torch.Generator(device=dev).manual_seed(seed)
     caches = []
     for layer in range(NL):
@@ -276,24 +295,29 @@ def setup_kivi(wl, dev, seed):
         K[..., outl] *= 20.0
         K = K.half()
         V = torch.randn((B, H, NQ + NR, D), generator=gen, device=dev).half()
-        kvq.kvq_quantize_kivi(cfg, kvq.PER_CHANNEL, K[:, :, :NQ].contiguous(), c.k_codes, c.k_scale, c.k_zero)
-        kvq.kvq_quantize_kivi(cfg, kvq.PER_TOKEN, V[:, :, :NQ].contiguous(), c.v_codes, c.v_scale, c.v_zero)
-        c.k_resid.copy_(K[:, :, NQ:])
-        c.v_resid.copy_(V[:, :, NQ:])
-        c.n_quant.fill_(NQ)
-        c.n_resid.fill_(NR)
+        kvq.kvq_kivi_prefill(cfg, c, K, V)
         caches.append(c)
     torch.cuda.synchronize(dev)
+    assert kvq.device_error() == 0
+    assert int(caches[0].n_quant_k[0]) == NQ
     return cfg, caches
 
 
-def kivi_call_bytes(B, H, NQ, NR):
-    codes = B * H * NQ * D // 4 * 2
+def kivi_call_bytes(B, H, NQ, NR, Hq=None, k_bits=2, v_bits=2):
+    """Algorithmic bytes of one KIVI attention call: codes, key and value scales and zeros,
+    the fp16 residual K and V, the bf16 queries read and outputs written."""
+    Hq = Hq or H
+    codes = B * H * NQ * D * (k_bits + v_bits) // 8
     ksz = B * H * (NQ // 32) * D * 2 * 2
     vsz = B * H * NQ * (D // 32) * 2 * 2
     res = B * H * NR * D * 2 * 2
-    qo = B * H * D * 2 * 2
+    qo = B * Hq * D * 2 * 2
     return codes + ksz + vsz + res + qo
+
+
+def kivi_wl_bytes(wl):
+    return kivi_call_bytes(wl["B"], wl["H"], wl["n_quant"], wl["n_resid"], wl.get("Hq"), wl.get("k_bits", 2),
+                           wl.get("v_bits", 2))
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch from an ncu capture,
@@ -377,9 +401,9 @@ def run_ours(args, wl, rank, world, dist, pool):
             caches = None
         else:
             cfg, caches = setup_kivi(wl, dev, 1234 + rank)
-            B, H, NL = wl["B"], wl["H"], wl["layers"]
+            B, H, NL = wl["B"], wl.get("Hq", wl["H"]), wl["layers"]   # H: query heads from here on
             calls = [(l, 1) for l in range(NL)]
-            call_bytes = kivi_call_bytes(B, H, wl["n_quant"], wl["n_resid"])
+            call_bytes = kivi_wl_bytes(wl)
         n_calls = len(calls)
         # a LoopVQ call is two launches (page kernel, then window + merge kernel); the roofline
         # covers both, timed together per call
@@ -507,6 +531,66 @@ def run_ours(args, wl, rank, world, dist, pool):
                                      "note": "per-call rooflines: workloads loopvq_b64_6k (attention), encode_32k"}))
         return result
 
+    if wl["kind"] == "kivi_stream":
+        # a step = one generated token: for every layer the token's K/V enters the cache
+        # (kvq_kivi_append: a whole key residual is quantized every 128 tokens, the value
+        # window quantizes its oldest token every token) and the layer's decode attention runs
+        B, H, NL, R = wl["B"], wl["H"], wl["layers"], wl["n_resid"]
+        n_tok = args.warmup + 2 * args.steps + 2 * R + 16
+        cfg, caches = setup_kivi(wl, dev, 1234 + rank, extra_tokens=(n_tok + R - 1) // R * R)
+        gen = torch.Generator(device=dev).manual_seed(77 + rank)
+        kn = torch.randn((B, H, D), generator=gen, device=dev).half()
+        vn = torch.randn((B, H, D), generator=gen, device=dev).half()
+        q = torch.randn((B, H, D), generator=gen, device=dev).to(torch.bfloat16)
+        out = torch.empty((B, H, D), dtype=torch.bfloat16, device=dev)
+        ws = kvq.make_workspace(cfg, B, 0, dev)
+        calls = [kvq.DecodeCall(cfg, caches[l], l, 1, q, out, 0, ws, stream) for l in range(NL)]
+        appends = [(kvq.lib().kvq_kivi_append, (ctypes.byref(cfg.to_c()), ctypes.byref(caches[l].c_struct()),
+                                                 kn.data_ptr(), vn.data_ptr(), B, stream.cuda_stream))
+                   for l in range(NL)]
+        keep = [a[1] for a in appends]   # the ctypes structs must outlive the calls
+
+        def token():
+            for l in range(NL):
+                f, a = appends[l]
+                if f(*a) != 0:
+                    raise RuntimeError("kvq_kivi_append failed")
+                calls[l]()
+
+        for _ in range(args.warmup):
+            token()
+        torch.cuda.synchronize()
+        assert kvq.device_error() == 0
+        with ClockSampler(gpu_index) as cs:
+            ms = time_region(token, args.steps, stream, dist, nvtx_name="timed") / args.steps
+        ms_attn = time_region(lambda: [c() for c in calls], args.steps, stream, dist) / args.steps
+        # per-token events over the next R + 8 tokens: the token whose append flushes a key
+        # residual against the others
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(R + 9)]
+        flushed = []
+        for i in range(R + 8):
+            flushed.append(int(caches[0].n_tok[0]) - int(caches[0].n_quant_k[0]) == R)
+            ev[i].record(stream)
+            token()
+        ev[R + 8].record(stream)
+        torch.cuda.synchronize()
+        assert kvq.device_error() == 0
+        tms = [ev[i].elapsed_time(ev[i + 1]) for i in range(R + 8)]
+        plain = statistics.median([t for t, f in zip(tms, flushed) if not f])
+        flush_extra = statistics.mean([t - plain for t, f in zip(tms, flushed) if f]) if any(flushed) else 0.0
+        del keep
+        result.update(dict(value=round(B * world / (ms * 1e-3), 1), unit="tokens/s", ms_per_step=round(ms, 4),
+                           attention_only_ms_per_token=round(ms_attn, 4),
+                           append_overhead_fraction=round((ms - ms_attn) / ms, 4),
+                           key_flush_ms_per_flush=round(flush_extra, 4),
+                           key_flush_fraction_amortized=round(flush_extra / R / ms, 5),
+                           higher_is_better=True, gpu_launches=args.steps * NL * 2,
+                           context_end=int(caches[0].n_tok[0]), clocks=cs.summary(),
+                           roofline={"bound": "hbm", "achieved": None, "peak": hbm_peak, "unit": "GB/s",
+                                     "frac": None, "traffic": None,
+                                     "note": "per-call roofline: workload kivi_b16_4k (attention)"}))
+        return result
+
     if wl["kind"] == "encode":
         import synth
         tc_peak, tc_src = bf16_peak()
@@ -574,8 +658,8 @@ def run_reference(args, wl, pool):
         call_bytes = vq_call_bytes(wl["B"], wl["H"], n_pages, wl["L"] - 8 * n_pages)
         units = wl["B"] * wl["H"]
     elif wl["kind"] == "kivi":
-        call_bytes = kivi_call_bytes(wl["B"], wl["H"], wl["n_quant"], wl["n_resid"])
-        units = wl["B"] * wl["H"]
+        call_bytes = kivi_wl_bytes(wl)
+        units = wl["B"] * wl.get("Hq", wl["H"])   # (request, query head) units
     else:
         raise SystemExit(json.dumps({"impl": "reference", "unavailable": "the CPU oracle arm covers the decode "
                                      "attention workloads only"}))
@@ -640,7 +724,7 @@ def main():
         cfgd = {"workload": wl["name"], "parallelism": f"replicas x{world} (requests shard, no collective)",
                 "l2": "inputs larger than L2: each call reads its own layer's cache (~240 MB)"
                 if wl["kind"] == "loopvq" else "inputs larger than L2"}
-        for k in ("B", "H", "L", "layers", "T", "Tc", "G", "recent", "n_quant", "n_resid"):
+        for k in ("B", "H", "Hq", "k_bits", "v_bits", "L", "layers", "T", "Tc", "G", "recent", "n_quant", "n_resid"):
             if k in wl:
                 cfgd[k] = wl[k]
         if "n_splits" in res:

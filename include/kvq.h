@@ -10,11 +10,12 @@
  *           step 4, Figure 5); decode attention looks codewords up through the per-step
  *           slice B_t, applies RoPE and merges the bf16 and quantized partials exactly
  *           (method step 5, Algorithm 1).
- *   KIVI    "KIVI 完全拆解：非对称 2-bit KV Cache 量化": asymmetric 2-bit quantization
+ *   KIVI    "KIVI 完全拆解：非对称 2-bit KV Cache 量化": asymmetric 2- or 4-bit quantization
  *           q = clamp(round(X/s + z), 0, 2^b - 1) with fp16 scale and zero-point per group
  *           (section on per-token / per-channel quantization); keys per channel over 32
- *           tokens, values per token over 32 channels, an fp16 residual window, and one
- *           softmax over both segments (core design, eq. (3)).
+ *           tokens, values per token over 32 channels, fp16 residual windows filled and
+ *           drained as Algorithm 1 streams tokens in, and one softmax over both segments
+ *           (core design, eq. (3)); grouped-query heads (implementation section).
  *
  * Conventions for every call:
  *   - Pointers are CUDA device pointers unless stated otherwise, owned by the caller; the
@@ -198,23 +199,39 @@ kvq_status kvq_append_page(const kvq_vq_cfg* cfg, const kvq_vq_cache* cache, int
 /* ---------------------------------------------------------------------------------- */
 
 typedef struct {
-  int D;            /* head dimension (128)                                     */
-  int n_heads;      /* KV heads (= query heads)                                 */
-  int bits;         /* 2                                                        */
-  int group;        /* 32: tokens per key group, channels per value group       */
-  int residual;     /* R: fp16 residual window capacity (128)                   */
+  int D;            /* head dimension (128)                                              */
+  int n_heads;      /* KV heads                                                          */
+  int n_q_heads;    /* query heads, a multiple of n_heads: query head h reads KV head     */
+                    /* h / (n_q_heads / n_heads) (grouped-query attention, KIVI page,     */
+                    /* implementation section); n_q_heads == n_heads is multi-head        */
+  int k_bits;       /* 2 or 4: key code width   (implementation section: K and V bits     */
+  int v_bits;       /* 2 or 4: value code width  are configured independently)            */
+  int group;        /* 32: tokens per key group, channels per value group                */
+  int residual;     /* R: fp16 residual capacity, a multiple of group (128 on the page);  */
+                    /* 0 is allowed for attention-only caches with no residual           */
   int max_batch;
-  int max_tokens;   /* quantized-token capacity per (request, head), multiple of group */
+  int max_tokens;   /* quantized-token capacity per (request, KV head), multiple of group */
 } kvq_kivi_cfg;
 
-/* Device buffers of a KIVI cache (caller-owned).
- * k_codes, v_codes uint8 [max_batch][n_heads][max_tokens][D/4]: 4 codes per byte along
- *     channels, channel 4k + i in bits [2i, 2i + 2).
+/* Device buffers of a KIVI cache (caller-owned, zero-filled before first use).
+ * k_codes uint8 [max_batch][n_heads][max_tokens][D*k_bits/8], v_codes likewise with
+ *     v_bits: 8/b codes per byte along channels, channel (8/b)k + i of a token in bits
+ *     [b*i, b*i + b) of byte k.
  * k_scale, k_zero  fp16 [max_batch][n_heads][max_tokens/group][D]   (per channel)
  * v_scale, v_zero  fp16 [max_batch][n_heads][max_tokens][D/group]   (per token)
- * k_resid, v_resid fp16 [max_batch][n_heads][residual][D]            (newest tokens)
- * n_quant  int32 [max_batch]: quantized tokens per request (a multiple of group)
- * n_resid  int32 [max_batch]: residual tokens per request (<= residual)
+ * k_resid fp16 [max_batch][n_heads][residual][D]: key of token t at row t - n_quant_k[b]
+ * v_resid fp16 [max_batch][n_heads][residual][D]: value of token t at row t % residual
+ *     (a ring: the window drops one token at a time)
+ * n_tok     int32 [max_batch]: tokens cached per request
+ * n_quant_k int32 [max_batch]: keys of tokens [0, n_quant_k) are quantized (a multiple
+ *     of group), the rest are in k_resid
+ * n_quant_v int32 [max_batch]: values of tokens [0, n_quant_v) are quantized, the rest
+ *     are in v_resid
+ * sync      int32 [max_batch]: scratch of kvq_kivi_append (its blocks count their arrivals
+ *     per request there); zero before the first call, every call leaves it zero
+ * A valid state has n_quant_v <= n_quant_k <= n_tok, n_tok - n_quant_v <= residual and
+ * n_quant_k <= max_tokens; kvq_kivi_prefill and kvq_kivi_append keep it valid. Attention
+ * over an invalid state stays inside the buffers but its result is undefined.
  */
 typedef struct {
   uint8_t* k_codes;
@@ -225,8 +242,10 @@ typedef struct {
   uint16_t* v_zero;
   uint16_t* k_resid;
   uint16_t* v_resid;
-  int32_t* n_quant;
-  int32_t* n_resid;
+  int32_t* n_tok;
+  int32_t* n_quant_k;
+  int32_t* n_quant_v;
+  int32_t* sync;
 } kvq_kivi_cache;
 
 /* Group quantization (KIVI page, quantization-direction section and the group-quant
@@ -234,9 +253,9 @@ typedef struct {
  * s16 = fp16(s) (1 if that is 0), z16 = fp16(-min/s16),
  * q = clamp(rint(x/s16 + z16), 0, 2^b - 1) with IEEE division and no fused multiply-add,
  * so codes, scales and zero-points are reproducible bit for bit.
- * axis = KVQ_PER_CHANNEL: keys, groups of `group` tokens per channel; n_tok and
- *        tok_begin multiples of group; writes k-style codes/scale/zero.
- * axis = KVQ_PER_TOKEN:   values, groups of `group` channels per token.
+ * axis = KVQ_PER_CHANNEL: keys (b = k_bits), groups of `group` tokens per channel; n_tok
+ *        and tok_begin multiples of group; writes k-style codes/scale/zero.
+ * axis = KVQ_PER_TOKEN:   values (b = v_bits), groups of `group` channels per token.
  * x: fp16, element (b, h, j, ch) at x[b*x_stride_b + h*x_stride_h + j*D + ch], b < B.
  * codes / scale / zero: cache arrays (layouts in kvq_kivi_cache); token j of request b is
  *    written at token tok_begin + j.
@@ -246,12 +265,44 @@ kvq_status kvq_quantize_kivi(const kvq_kivi_cfg* cfg, int axis, const uint16_t* 
                              uint8_t* codes, uint16_t* scale, uint16_t* zero, int tok_begin,
                              kvq_stream stream);
 
+/* Prefill (KIVI page, core design section, Algorithm 1, prefill): requests b0 .. b0+B-1
+ * of the cache receive the n_tok prompt tokens in k and v (fp16, element (b, h, j, ch) at
+ * x[b*x_stride_b + h*x_stride_h + j*D + ch]). The first nq tokens are quantized (keys per
+ * channel, values per token) and the rest are copied to the residuals, where
+ * nq = 0 if n_tok <= residual, else n_tok - residual rounded up to a multiple of group (the
+ * page's split l - R when that is a multiple of group). Sets n_tok, n_quant_k = n_quant_v
+ * = nq on the device. Any earlier content of those requests is replaced.
+ * Errors: KVQ_ERR_INVALID_ARG (residual not a positive multiple of group), KVQ_ERR_CAPACITY
+ * (b0 + B > max_batch or nq > max_tokens). */
+kvq_status kvq_kivi_prefill(const kvq_kivi_cfg* cfg, const kvq_kivi_cache* cache,
+                            const uint16_t* k, const uint16_t* v, int64_t x_stride_b,
+                            int64_t x_stride_h, int b0, int B, int n_tok, kvq_stream stream);
+
+/* Decode append (KIVI page, Algorithm 1, decoding): one new token per request b < n_seq,
+ * k_new and v_new fp16 [n_seq][n_heads][D].
+ *  - keys: if the key residual already holds `residual` tokens, they are quantized per
+ *    channel and appended to the quantized keys (n_quant_k += residual) and the new key
+ *    starts a fresh residual; otherwise it is appended to the residual;
+ *  - values: the new value enters the window; if the window then holds more than
+ *    `residual` tokens, its oldest token is quantized per token (n_quant_v += 1);
+ *  - n_tok += 1.
+ * One kernel launch (a block per (request, KV head); the last block of a request to finish
+ * advances its lengths); the lengths live on the device, so a whole decode loop can run in a
+ * CUDA graph. Two appends to one cache must not run at the same time. A request whose state is invalid or whose key flush would exceed max_tokens
+ * is left unchanged and KVQ_ERR_CAPACITY is raised through kvq_device_error().
+ * Errors: KVQ_ERR_INVALID_ARG (residual not a positive multiple of group, n_seq < 0),
+ * KVQ_ERR_CAPACITY (n_seq > max_batch). */
+kvq_status kvq_kivi_append(const kvq_kivi_cfg* cfg, const kvq_kivi_cache* cache,
+                           const uint16_t* k_new, const uint16_t* v_new, int n_seq,
+                           kvq_stream stream);
+
 /* ---------------------------------------------------------------------------------- */
 /* Decode attention (both formats)                                                     */
 /* ---------------------------------------------------------------------------------- */
 
 /* One decode attention call: every request b < B attends with its query (bf16
- * [B][n_heads][D], pre-RoPE for LoopVQ) to its whole cache, split-K over the quantized
+ * [B][Hq][D], Hq = n_heads for LoopVQ and n_q_heads for KIVI; pre-RoPE for LoopVQ) to its
+ * whole cache, split-K over the quantized
  * pages with partial softmax per split and an exact logsumexp merge (LoopVQ page:
  * Flash-Decoding background and method step 5; KIVI page: eq. (3), one softmax over the
  * quantized and residual segments). Scale 1/sqrt(D).
@@ -260,14 +311,18 @@ kvq_status kvq_quantize_kivi(const kvq_kivi_cfg* cfg, int axis, const uint16_t* 
  *   select the cache slice. The query sits at position seq_len[b] - 1; every key and the
  *   query are rotated by RoPE at their positions.
  * format KVQ_FMT_KIVI: cfg is kvq_kivi_cfg*, cache kvq_kivi_cache*; layer and loop_step
- *   are ignored; no RoPE (KIVI caches post-RoPE keys).
- * out: [B][n_heads][D], bf16 (KVQ_OUT_BF16) or fp32 (KVQ_OUT_FP32).
+ *   are ignored; no RoPE (KIVI caches post-RoPE keys). Token t of request b uses the
+ *   quantized key if t < n_quant_k[b] (else k_resid) and the quantized value if
+ *   t < n_quant_v[b] (else v_resid), for t < n_tok[b].
+ * out: [B][Hq][D], bf16 (KVQ_OUT_BF16) or fp32 (KVQ_OUT_FP32).
  * n_splits: how the quantized pages are split, 0 picks for the GPU.
  *   LoopVQ: thread blocks of the page kernel. The units (head, request pair, 32 index
  *   pages), head-major, are cut into n_splits equal contiguous shares, one per block; each
  *   block writes a partial softmax for every piece of a (request, head) it covers and a
  *   second kernel merges them with the bf16 window tokens. 0 = one block per SM.
- *   KIVI: token splits per (request, head), merged by the last block of each.
+ *   KIVI: splits of the quantized keys per (request, KV head), plus one block for the
+ *   fp16 key residual, merged by the last block of each; a block serves up to 4 query
+ *   heads of its KV head, so their codes are read once.
  * ws: device workspace of at least kvq_decode_workspace_size() bytes (may be NULL when
  *   that size is 0; LoopVQ always needs one). A KIVI workspace must be zero-filled before
  *   its first use; every call leaves it reusable. Two calls that run at the same time need

@@ -1,11 +1,14 @@
-// KIVI 2-bit KV cache: group quantization and decode attention.
+// KIVI KV cache: group quantization with 2- or 4-bit codes, the streaming cache of
+// Algorithm 1 (prefill and decode append) and decode attention with grouped-query heads.
 //
 // "KIVI 完全拆解：非对称 2-bit KV Cache 量化":
 //  * quantization-direction section: q = clamp(round(X/s + z), 0, 2^b - 1), X_hat = s(q - z),
 //    [min, max] split evenly by s; keys per channel, values per token (core design);
 //  * core design, eq. (3) and Algorithm 1: grouped (quantized) + fp16 residual segments,
-//    logits of both concatenated before one softmax;
-//  * implementation section: the Q_MatMul kernel fuses dequantization into the product.
+//    logits of both concatenated before one softmax; during decoding a full key residual is
+//    quantized whole and the value window drops its oldest token into the quantized part;
+//  * implementation section: the Q_MatMul kernel fuses dequantization into the product;
+//    key and value bit widths are configured independently (2 or 4); GQA.
 //
 // Quantize: one fp32 sequence (IEEE division, separate rounding of every step, round half
 // to even) so codes, scales and zero-points match a reference that follows the same steps
@@ -13,6 +16,8 @@
 // sum_ch q_ch s_ch (code - z_ch) = sum_ch (q_ch s_ch) code + bias - so each 32-token group
 // folds its per-channel scale into the query once; values accumulate
 // sum_j p_j s_jg code_j,ch and subtract sum_j p_j s_jg z_jg per channel group at the end.
+// Under GQA one block serves up to four query heads of a KV head: the codes are read from
+// HBM and unpacked once for all of them.
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
 #include "../../include/kvq.h"
@@ -22,13 +27,16 @@
 namespace kvq {
 namespace {
 
+constexpr int kGroup = 32;  // tokens per key group, channels per value group (checked by the host)
+
 struct GroupQ {
   float s16f, z16f;
   uint16_t s_bits, z_bits;
 };
 
+template <int BITS>
 __device__ __forceinline__ GroupQ group_params(float mn, float mx) {
-  const float s = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+  const float s = __fdiv_rn(__fsub_rn(mx, mn), (float)((1 << BITS) - 1));
   __half s16 = __float2half_rn(s);
   if (__half2float(s16) == 0.0f) s16 = __float2half_rn(1.0f);
   const float s16f = __half2float(s16);
@@ -41,20 +49,110 @@ __device__ __forceinline__ GroupQ group_params(float mn, float mx) {
   return g;
 }
 
+template <int BITS>
 __device__ __forceinline__ uint32_t quant_code(float x, const GroupQ& g) {
   const float t = __fadd_rn(__fdiv_rn(x, g.s16f), g.z16f);
-  const float r = fminf(fmaxf(rintf(t), 0.0f), 3.0f);
-  return (uint32_t)r;
+  return (uint32_t)fminf(fmaxf(rintf(t), 0.0f), (float)((1 << BITS) - 1));
 }
 
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 
-// keys: one warp per (b, h, 32-token group); lane l owns channels 4l..4l+3, so each of the 32
-// token rows is one coalesced 256-byte read (8 bytes per lane), all 32 in flight at once
+__device__ __forceinline__ void unpack4(const uint2 r, float v[4]) {
+  v[0] = h2f(r.x & 0xFFFFu);
+  v[1] = h2f(r.x >> 16);
+  v[2] = h2f(r.y & 0xFFFFu);
+  v[3] = h2f(r.y >> 16);
+}
+
+// The codes of a lane's four channels 4 lane .. 4 lane + 3 as stored: channel (8/b)k + i of a
+// token sits in bits [b i, b i + b) of byte k, so 2-bit codes fill byte `lane` and 4-bit
+// codes bytes 2 lane and 2 lane + 1.
+template <int BITS>
+__device__ __forceinline__ void store_codes4(uint8_t* row, int lane, const uint32_t c[4]) {
+  if constexpr (BITS == 2) row[lane] = (uint8_t)(c[0] | (c[1] << 2) | (c[2] << 4) | (c[3] << 6));
+  else *reinterpret_cast<uint16_t*>(row + 2 * lane) = (uint16_t)(c[0] | (c[1] << 4) | (c[2] << 8) | (c[3] << 12));
+}
+
+// One warp quantizes one 32-token key group over all 128 channels; lane l owns channels
+// 4l .. 4l + 3, so each token row is one coalesced 256-byte read, all 32 rows in flight.
+// src: row j at src + j * src_row elements; codes: row j at codes + j * (D b / 8) bytes;
+// scale / zero: the group's [D] row.
+template <int BITS, bool kReadOnly>
+__device__ __forceinline__ void quant_key_group(const uint16_t* src, size_t src_row, uint8_t* codes,
+                                                uint16_t* scale, uint16_t* zero, int lane) {
+  constexpr int kRow = kD * BITS / 8;
+  uint2 raw[kGroup];
+#pragma unroll
+  for (int j = 0; j < kGroup; ++j) {
+    const uint2* p = reinterpret_cast<const uint2*>(src + (size_t)j * src_row + 4 * lane);
+    raw[j] = kReadOnly ? __ldg(p) : *p;
+  }
+  float mn[4], mx[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    mn[i] = INFINITY;
+    mx[i] = -INFINITY;
+  }
+#pragma unroll
+  for (int j = 0; j < kGroup; ++j) {
+    float v[4];
+    unpack4(raw[j], v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      mn[i] = fminf(mn[i], v[i]);
+      mx[i] = fmaxf(mx[i], v[i]);
+    }
+  }
+  GroupQ g[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) g[i] = group_params<BITS>(mn[i], mx[i]);
+  *reinterpret_cast<uint2*>(scale + 4 * lane) =
+      make_uint2(g[0].s_bits | ((uint32_t)g[1].s_bits << 16), g[2].s_bits | ((uint32_t)g[3].s_bits << 16));
+  *reinterpret_cast<uint2*>(zero + 4 * lane) =
+      make_uint2(g[0].z_bits | ((uint32_t)g[1].z_bits << 16), g[2].z_bits | ((uint32_t)g[3].z_bits << 16));
+#pragma unroll
+  for (int j = 0; j < kGroup; ++j) {
+    float v[4];
+    unpack4(raw[j], v);
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = quant_code<BITS>(v[i], g[i]);
+    store_codes4<BITS>(codes + (size_t)j * kRow, lane, c);
+  }
+}
+
+// One warp quantizes one token's 128 values (four 32-channel groups): lane l owns channels
+// 4l .. 4l + 3 (raw), the 8 lanes of a group reduce min and max by shuffles. All 32 lanes
+// must call it. scale / zero: the token's [D/32] row.
+template <int BITS>
+__device__ __forceinline__ void quant_value_row(const uint2 raw, uint8_t* codes, uint16_t* scale, uint16_t* zero,
+                                                int lane) {
+  float v[4];
+  unpack4(raw, v);
+  float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
+  float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+#pragma unroll
+  for (int off = 4; off >= 1; off >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, off));
+    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+  }
+  const GroupQ g = group_params<BITS>(mn, mx);
+  if ((lane & 7) == 0) {
+    scale[lane >> 3] = g.s_bits;
+    zero[lane >> 3] = g.z_bits;
+  }
+  uint32_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = quant_code<BITS>(v[i], g);
+  store_codes4<BITS>(codes, lane, c);
+}
+
+// keys: one warp per (b, h, 32-token group), grid-stride
+template <int BITS>
 __global__ void __launch_bounds__(256) kivi_quant_channel_kernel(const KiviQuantArgs a) {
-  constexpr int kG = 32;  // tokens per key group (checked by the caller)
+  constexpr int kRow = kD * BITS / 8;
   const int lane = threadIdx.x & 31;
-  const int n_groups = a.n_tok / kG;
+  const int n_groups = a.n_tok / kGroup;
   const long long total = (long long)a.B * a.H * n_groups;
   for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; w < total;
        w += ((long long)gridDim.x * blockDim.x) >> 5) {
@@ -62,52 +160,20 @@ __global__ void __launch_bounds__(256) kivi_quant_channel_kernel(const KiviQuant
     const long long q = w / n_groups;
     const int h = (int)(q % a.H);
     const int b = (int)(q / a.H);
-    const uint16_t* xp = a.x + (size_t)b * a.sb + (size_t)h * a.sh + (size_t)gi * kG * kD + 4 * lane;
-    uint2 raw[kG];
-#pragma unroll
-    for (int j = 0; j < kG; ++j) raw[j] = __ldg(reinterpret_cast<const uint2*>(xp + (size_t)j * kD));
-    float mn[4], mx[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      mn[i] = INFINITY;
-      mx[i] = -INFINITY;
-    }
-#pragma unroll
-    for (int j = 0; j < kG; ++j) {
-      const float v[4] = {h2f(raw[j].x & 0xFFFFu), h2f(raw[j].x >> 16), h2f(raw[j].y & 0xFFFFu), h2f(raw[j].y >> 16)};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        mn[i] = fminf(mn[i], v[i]);
-        mx[i] = fmaxf(mx[i], v[i]);
-      }
-    }
-    GroupQ g[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) g[i] = group_params(mn[i], mx[i]);
-    const int tg = a.tok_begin / kG + gi;  // global token group
-    const size_t sz = (((size_t)b * a.H + h) * (a.max_tokens / kG) + tg) * kD + 4 * lane;
-    *reinterpret_cast<uint2*>(a.scale + sz) =
-        make_uint2(g[0].s_bits | ((uint32_t)g[1].s_bits << 16), g[2].s_bits | ((uint32_t)g[3].s_bits << 16));
-    *reinterpret_cast<uint2*>(a.zero + sz) =
-        make_uint2(g[0].z_bits | ((uint32_t)g[1].z_bits << 16), g[2].z_bits | ((uint32_t)g[3].z_bits << 16));
-    uint8_t* cp = a.codes + (((size_t)b * a.H + h) * a.max_tokens + a.tok_begin + (size_t)gi * kG) * (kD / 4) + lane;
-#pragma unroll
-    for (int j = 0; j < kG; ++j) {
-      const float v[4] = {h2f(raw[j].x & 0xFFFFu), h2f(raw[j].x >> 16), h2f(raw[j].y & 0xFFFFu), h2f(raw[j].y >> 16)};
-      uint32_t byte = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) byte |= quant_code(v[i], g[i]) << (2 * i);
-      cp[(size_t)j * (kD / 4)] = (uint8_t)byte;
-    }
+    const size_t bh = (size_t)b * a.H + h;
+    const size_t sz = (bh * (a.max_tokens / kGroup) + a.tok_begin / kGroup + gi) * kD;
+    quant_key_group<BITS, true>(a.x + (size_t)b * a.sb + (size_t)h * a.sh + (size_t)gi * kGroup * kD, kD,
+                                a.codes + (bh * a.max_tokens + a.tok_begin + (size_t)gi * kGroup) * kRow,
+                                a.scale + sz, a.zero + sz, lane);
   }
 }
 
-// values: a group is 32 channels of one token; 8 lanes per group (lane l owns channels
-// 4l..4l+3), so a warp covers one 256-byte token row per step; 4 rows are loaded per step
+// values: a warp covers one 256-byte token row per step, 4 rows loaded per step
+template <int BITS>
 __global__ void __launch_bounds__(256) kivi_quant_token_kernel(const KiviQuantArgs a) {
   constexpr int kRows = 4;
+  constexpr int kRow = kD * BITS / 8;
   const int lane = threadIdx.x & 31;
-  const int gi = lane >> 3;  // channel group of this lane (32 channels = 8 lanes)
   const long long rows = (long long)a.B * a.H * a.n_tok;
   const long long n_steps = (rows + kRows - 1) / kRows;
   for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; w < n_steps;
@@ -127,65 +193,157 @@ __global__ void __launch_bounds__(256) kivi_quant_token_kernel(const KiviQuantAr
 #pragma unroll
     for (int u = 0; u < kRows; ++u) {
       if (w * kRows + u >= rows) break;  // uniform across the warp
-      const float v[4] = {h2f(raw[u].x & 0xFFFFu), h2f(raw[u].x >> 16), h2f(raw[u].y & 0xFFFFu), h2f(raw[u].y >> 16)};
-      float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
-      float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-#pragma unroll
-      for (int off = 4; off >= 1; off >>= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, off));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-      }
-      const GroupQ g = group_params(mn, mx);
-      if ((lane & 7) == 0) {
-        a.scale[tok[u] * (kD / 32) + gi] = g.s_bits;
-        a.zero[tok[u] * (kD / 32) + gi] = g.z_bits;
-      }
-      uint32_t byte = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) byte |= quant_code(v[i], g) << (2 * i);
-      a.codes[tok[u] * (kD / 4) + lane] = (uint8_t)byte;
+      quant_value_row<BITS>(raw[u], a.codes + tok[u] * kRow, a.scale + tok[u] * (kD / kGroup),
+                            a.zero + tok[u] * (kD / kGroup), lane);
     }
   }
 }
 
+// ---------------------------------------------------------------- streaming cache
+// Prefill tail: block (b, h) copies tokens [nq, n) to the residuals (keys from row 0, values
+// at row t % R) and block (b, 0) sets the request's lengths.
+__global__ void __launch_bounds__(128) kivi_prefill_tail_kernel(const KiviTailArgs a) {
+  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int n_tail = a.n_tok_new - a.nq;
+  const size_t row0 = ((size_t)(a.b0 + b) * a.H + h) * a.residual;
+  const uint16_t* ks = a.k + (size_t)b * a.sb + (size_t)h * a.sh + (size_t)a.nq * kD;
+  const uint16_t* vs = a.v + (size_t)b * a.sb + (size_t)h * a.sh + (size_t)a.nq * kD;
+  for (int i = tid; i < n_tail * (kD / 8); i += blockDim.x) {  // one 16-byte piece per thread
+    const int r = i / (kD / 8), c8 = (i % (kD / 8)) * 8;
+    const int slot = (a.nq + r) % a.residual;
+    *reinterpret_cast<uint4*>(a.k_resid + (row0 + r) * kD + c8) = __ldg(reinterpret_cast<const uint4*>(ks + (size_t)r * kD + c8));
+    *reinterpret_cast<uint4*>(a.v_resid + (row0 + slot) * kD + c8) = __ldg(reinterpret_cast<const uint4*>(vs + (size_t)r * kD + c8));
+  }
+  if (h == 0 && tid == 0) {
+    a.n_tok[a.b0 + b] = a.n_tok_new;
+    a.n_quant_k[a.b0 + b] = a.nq;
+    a.n_quant_v[a.b0 + b] = a.nq;
+  }
+}
+
+// Decode append: one 128-thread block per (request, KV head). Every block of a request reads
+// the request's lengths and takes the same decisions; the last block of the request to finish
+// (an arrival counter in the cache's sync array) advances the lengths, so no block reads them
+// after they changed. Quantization (a key flush: warp w takes 32-token groups w, w + 4, ...;
+// a value eviction: warp 0) reads the residual rows before the barrier; the new token is
+// written after it, because the evicted value and the new value share a ring row and the
+// flushed key residual restarts at row 0.
+template <int KB, int VB>
+__global__ void __launch_bounds__(128) kivi_append_kernel(const KiviAppendArgs a) {
+  constexpr int kKRow = kD * KB / 8, kVRow = kD * VB / 8;
+  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_warps = blockDim.x >> 5;
+  const int R = a.residual, H = a.H;
+  const int n = a.n_tok[b], nqk = a.n_quant_k[b], nqv = a.n_quant_v[b];
+  const bool valid = nqk >= 0 && nqk % kGroup == 0 && nqv >= 0 && nqv <= nqk && nqk <= n && n - nqv <= R &&
+                     nqk <= a.max_tokens;
+  const bool flush = valid && (n - nqk == R);
+  if (!valid || (flush && nqk + R > a.max_tokens)) {  // every block of the request leaves it as it is
+    if (h == 0 && tid == 0) set_error(a.err, KVQ_ERR_CAPACITY);
+    return;
+  }
+  const bool evict = (n + 1 - nqv > R);
+  const size_t bh = (size_t)b * H + h;
+  if (flush) {
+    for (int gi = warp; gi < R / kGroup; gi += n_warps) {
+      const size_t sz = (bh * (a.max_tokens / kGroup) + nqk / kGroup + gi) * kD;
+      quant_key_group<KB, false>(a.k_resid + (bh * R + (size_t)gi * kGroup) * kD, kD,
+                                 a.k_codes + (bh * a.max_tokens + nqk + (size_t)gi * kGroup) * kKRow, a.k_scale + sz,
+                                 a.k_zero + sz, lane);
+    }
+  }
+  if (evict && warp == 0) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(a.v_resid + (bh * R + nqv % R) * kD + 4 * lane);
+    const size_t tok = bh * a.max_tokens + nqv;
+    quant_value_row<VB>(raw, a.v_codes + tok * kVRow, a.v_scale + tok * (kD / kGroup), a.v_zero + tok * (kD / kGroup),
+                        lane);
+  }
+  __syncthreads();
+  const int kslot = flush ? 0 : n - nqk, vslot = n % R;
+  if (tid < 2 * (kD / 8)) {  // 16 threads per fp16 row: the key, then the value
+    const int c8 = (tid % (kD / 8)) * 8;
+    const bool is_v = tid >= kD / 8;
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>((is_v ? a.v_new : a.k_new) + bh * kD + c8));
+    uint16_t* dst = is_v ? a.v_resid + (bh * R + vslot) * kD : a.k_resid + (bh * R + kslot) * kD;
+    *reinterpret_cast<uint4*>(dst + c8) = x;
+  }
+  __syncthreads();
+  if (tid == 0 && atomicAdd(&a.sync[b], 1) == H - 1) {  // every block of the request has read the lengths
+    a.n_tok[b] = n + 1;
+    if (flush) a.n_quant_k[b] = nqk + R;
+    if (evict) a.n_quant_v[b] = nqv + 1;
+    a.sync[b] = 0;
+  }
+}
+
 // ---------------------------------------------------------------- attention
-// One block per (split, request, head); splits 0 .. n_split-1 take equal token ranges of the
-// quantized segment, the last block the fp16 residual segment. A quantized split streams its
-// tokens through a 4-stage shared-memory ring of 128-token chunks (TMA bulk copies of the
-// chunk's key codes, key scales and zeros, value codes, value scales and zeros: 12 KB), with a
-// block-wide online softmax across chunks. Partials of all splits merge exactly in the last
-// block of a (request, head) to finish (arrival counter, no spin-wait).
+// Blocks (split, head subgroup) x request x KV head; splits 0 .. n_split-1 take equal token
+// ranges of the quantized keys, the last split the fp16 key residual. A subgroup is RH query
+// heads of the KV head (RH = 4 when the GQA ratio allows), and the blocks of one split's
+// subgroups are adjacent in launch order so their code reads meet in L2. A quantized split
+// streams its tokens through a 4-stage shared-memory ring of 128-token chunks (TMA bulk
+// copies of the chunk's key codes, key scales and zeros, value codes, value scales and
+// zeros), with a block-wide online softmax per query head across chunks. Tokens whose key is
+// quantized but whose value is still in the fp16 window (the streaming cache's tail) take
+// the value from the window. Partials of all splits merge exactly in the last block of a
+// (request, subgroup) to finish (arrival counter, no spin-wait).
 constexpr int kAThreads = 256;
 constexpr int kAWarps = kAThreads / 32;
-constexpr int kAChunk = 128;                      // tokens per ring stage (4 key groups of 32)
+constexpr int kAChunk = 128;  // tokens per ring stage (4 key groups of 32)
 constexpr int kAStages = 4;
-constexpr int kCKc = 0;                           // stage layout (bytes)
-constexpr int kCKs = kCKc + kAChunk * 32;         // key scales [4 groups][128] fp16
-constexpr int kCKz = kCKs + 4 * kD * 2;
-constexpr int kCVc = kCKz + 4 * kD * 2;
-constexpr int kCVs = kCVc + kAChunk * 32;         // value scales [128 tokens][4 groups] fp16
-constexpr int kCVz = kCVs + kAChunk * 4 * 2;
-constexpr int kAStageBytes = kCVz + kAChunk * 4 * 2;  // 12 KB
-// shared layout (bytes)
-constexpr int kAOffRing = 0;
-constexpr int kAOffQ = kAOffRing + kAStages * kAStageBytes;  // float q[128]
-constexpr int kAOffQf = kAOffQ + kD * 4;                      // float q' [4 groups][128]
-constexpr int kAOffBias = kAOffQf + 4 * kD * 4;               // float [4 groups][2 halves]
-constexpr int kAOffRed = kAOffBias + 32;                      // float [8 warps] + flag
-constexpr int kAOffBar = kAOffRed + 64;                       // mbarriers [4] + failed
-constexpr int kAOffSc = kAOffBar + 64;                        // float scores [max(128, residual)]
-static_assert(kAStageBytes % 128 == 0 && kAOffBar % 8 == 0, "alignment");
 
-// Codes j and j + 8 (j < 8) of a 16-code word, each as (code * 4^j) in fp32: the code is
-// masked in place (bits 2j, 2j+1 of each half word), placed in the mantissa of 2^23 and 2^23
-// is subtracted, all exact. One integer op per code and one packed add per pair instead of
-// shift + int-to-float conversion; the 4^-j scale is folded into the other operand.
+template <int KB, int VB, int RH>
+struct AttnLayout {
+  static constexpr int kKRow = kD * KB / 8;               // key code bytes per token
+  static constexpr int kVRow = kD * VB / 8;               // value code bytes per token
+  static constexpr int kCKc = 0;                          // stage layout (bytes)
+  static constexpr int kCKs = kCKc + kAChunk * kKRow;     // key scales [4 groups][128] fp16
+  static constexpr int kCKz = kCKs + 4 * kD * 2;
+  static constexpr int kCVc = kCKz + 4 * kD * 2;
+  static constexpr int kCVs = kCVc + kAChunk * kVRow;     // value scales [128 tokens][4 groups] fp16
+  static constexpr int kCVz = kCVs + kAChunk * 4 * 2;
+  static constexpr int kStage = kCVz + kAChunk * 4 * 2;
+  static constexpr int kOffQ = kAStages * kStage;         // float q [RH][128]
+  static constexpr int kOffQf = kOffQ + RH * kD * 4;      // float q' [RH][4 groups][128]
+  static constexpr int kOffBias = kOffQf + RH * 4 * kD * 4;  // float [RH][4 groups][2 halves]
+  static constexpr int kOffRed = kOffBias + RH * 8 * 4;      // float [8 warps][RH] + flag
+  static constexpr int kOffBar = kOffRed + ((kAWarps * RH + 4) * 4 + 15) / 16 * 16;  // mbarriers + failed
+  static constexpr int kOffSc = kOffBar + 64;             // float scores [RH][max(128, residual)]
+  // value phase: a warp-step covers TS tokens, a lane one code word of VPW channels
+  static constexpr int kVW = kVRow / 4;                   // code words per token
+  static constexpr int kTS = 32 / kVW;                    // tokens per warp-step
+  static constexpr int kCPWv = 32 / VB;                   // value channels per word
+  static constexpr int kPV = kCPWv / 2;                   // channel pairs per word
+  static constexpr int kWPG = kGroup / kCPWv;             // words per value group
+  // score phase: a lane covers 64 channels of one token
+  static constexpr int kKW = kKRow / 8;                   // key code words per half token
+  static constexpr int kPK = 16 / KB;                     // channel pairs per key word
+  static_assert(kStage % 128 == 0 && kOffBar % 8 == 0, "alignment");
+  static_assert(kAWarps * RH * kD * 4 <= kAStages * kStage, "block reduction fits in the ring");
+};
+
+// Codes j and j + 16/b (j < 16/b) of a 32-bit word of b-bit codes, each as (code * 2^(b j))
+// in fp32: the code is masked in place, placed in the mantissa of 2^23 and 2^23 is
+// subtracted, all exact. One integer op per code and one packed add per pair instead of
+// shift + int-to-float conversion; the 2^(-b j) scale is folded into the other operand.
+template <int BITS>
 __device__ __forceinline__ float2 code_pair(uint32_t w, uint32_t w_hi, int j) {
-  const uint32_t m = 3u << (2 * j);
+  const uint32_t m = ((1u << BITS) - 1u) << (BITS * j);
   const float2 f = make_float2(__uint_as_float((w & m) | 0x4B000000u), __uint_as_float((w_hi & m) | 0x4B000000u));
   return __fadd2_rn(f, make_float2(-8388608.f, -8388608.f));
 }
-__device__ __forceinline__ float pow4_neg(int j) { return __uint_as_float((uint32_t)(127 - 2 * j) << 23); }
+__device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
+__device__ __forceinline__ float pow2_pos(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
+// position of channel c (< 64) of a key half in the query pair layout: word k = c / (32/b),
+// within it pair j and member (low or high half word)
+template <int BITS>
+__device__ __forceinline__ int qpair_index(int c, int& j) {
+  constexpr int kCPW = 32 / BITS, kP = kCPW / 2;
+  const int k = c / kCPW, p = c % kCPW;
+  j = p % kP;
+  return 2 * (k * kP + j) + p / kP;
+}
 
 __device__ __forceinline__ bool kivi_wait(uint64_t* bar, uint32_t parity, volatile int* failed, int* err) {
   if (*failed) return false;
@@ -195,23 +353,30 @@ __device__ __forceinline__ bool kivi_wait(uint64_t* bar, uint32_t parity, volati
   return false;
 }
 
-__global__ void __launch_bounds__(kAThreads) kivi_attn_kernel(const KiviAttnArgs a, const float scale_log2) {
+template <int KB, int VB, int RH>
+__global__ void __launch_bounds__(kAThreads) kivi_attn_kernel(const KiviAttnArgs a, const float scale_log2,
+                                                              const int sc_stride) {
+  using L = AttnLayout<KB, VB, RH>;
   extern __shared__ __align__(128) unsigned char sma[];
-  float* qs = reinterpret_cast<float*>(sma + kAOffQ);
-  float* qf = reinterpret_cast<float*>(sma + kAOffQf);
-  float* bias = reinterpret_cast<float*>(sma + kAOffBias);
-  float* red = reinterpret_cast<float*>(sma + kAOffRed);
-  int* flag = reinterpret_cast<int*>(sma + kAOffRed + 8 * 4);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sma + kAOffBar);
-  volatile int* failed = reinterpret_cast<volatile int*>(sma + kAOffBar + kAStages * 8);
-  float* sc = reinterpret_cast<float*>(sma + kAOffSc);
+  float* qs = reinterpret_cast<float*>(sma + L::kOffQ);
+  float* qf = reinterpret_cast<float*>(sma + L::kOffQf);
+  float* bias = reinterpret_cast<float*>(sma + L::kOffBias);
+  float* red = reinterpret_cast<float*>(sma + L::kOffRed);
+  int* flag = reinterpret_cast<int*>(red + kAWarps * RH);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sma + L::kOffBar);
+  volatile int* failed = reinterpret_cast<volatile int*>(sma + L::kOffBar + kAStages * 8);
+  float* sc = reinterpret_cast<float*>(sma + L::kOffSc);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int split = blockIdx.x, b = blockIdx.y, h = blockIdx.z, H = a.H;
-  const int n_total = gridDim.x;                 // quantized splits + the residual block
-  const bool resid_block = (a.residual > 0) && (split == n_total - 1);
-  const size_t bh = (size_t)b * H + h;
-  const int NQ = min(a.n_quant[b], a.max_tokens) / a.group * a.group;
-  if (tid < kD) qs[tid] = bf16_to_f32(a.q[bh * kD + tid]);
+  const int rep = a.Hq / a.H, n_sub = rep / RH;
+  const int split = blockIdx.x / n_sub, sub = blockIdx.x % n_sub, b = blockIdx.y, hk = blockIdx.z;
+  const int n_total = gridDim.x / n_sub;  // quantized splits + the residual block
+  const int R = a.residual;
+  const bool resid_block = (R > 0) && (split == n_total - 1);
+  const size_t bh = (size_t)b * a.H + hk;                       // KV row of (b, hk)
+  const size_t bq0 = (size_t)b * a.Hq + (size_t)hk * rep + sub * RH;  // first query row
+  const int NQK = min(max(a.n_quant_k[b], 0), a.max_tokens) / kGroup * kGroup;
+  const int NQV = (R > 0) ? min(max(a.n_quant_v[b], 0), NQK) : NQK;
+  for (int i = tid; i < RH * kD; i += kAThreads) qs[i] = bf16_to_f32(a.q[bq0 * kD + i]);
   if (tid == 0) {
     for (int s = 0; s < kAStages; ++s) mbar_init(&full[s], 1);
     *failed = 0;
@@ -219,50 +384,57 @@ __global__ void __launch_bounds__(kAThreads) kivi_attn_kernel(const KiviAttnArgs
   }
   __syncthreads();
 
-  // running softmax state; the max is block-wide
-  // quantized blocks: lane holds channels 16 (lane % 8) .. + 15 of its token slot (lane / 8);
-  // the residual block: channels 4 lane .. 4 lane + 3 in o[0..3]
-  float M = -INFINITY, l = 0.f, oz = 0.f;
-  float o[16];
+  // running softmax state per query head; the max is block-wide
+  // quantized blocks: lane holds the kCPWv channels of code word lane % kVW of its token slot;
+  // the residual block: channels 4 lane .. 4 lane + 3 in o[r][0..3]
+  float M[RH], l[RH], oz[RH];
+  float o[RH][L::kCPWv];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) o[i] = 0.f;
-  auto rescale_to = [&](float Mn) {
-    const float f = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
+  for (int r = 0; r < RH; ++r) {
+    M[r] = -INFINITY;
+    l[r] = 0.f;
+    oz[r] = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) o[i] *= f;
-    oz *= f;
-    l *= f;
-    M = Mn;
+    for (int i = 0; i < L::kCPWv; ++i) o[r][i] = 0.f;
+  }
+  // raise head r's running max to Mn
+  auto rescale_to = [&](int r, float Mn) {
+    const float f = (M[r] == -INFINITY) ? 0.f : exp2f(M[r] - Mn);
+#pragma unroll
+    for (int i = 0; i < L::kCPWv; ++i) o[r][i] *= f;
+    oz[r] *= f;
+    l[r] *= f;
+    M[r] = Mn;
   };
-  // block max of sc[0, n) (every warp computes it)
-  auto scores_max = [&](int n) {
+  // max of s[0, n) (every warp computes it)
+  auto scores_max = [&](const float* s, int n) {
     float m = -INFINITY;
-    for (int i = lane; i < n; i += 32) m = fmaxf(m, sc[i]);
+    for (int i = lane; i < n; i += 32) m = fmaxf(m, s[i]);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
     return m;
   };
 
   if (!resid_block) {
-    // ================================ quantized tokens ======================================
+    // ================================ quantized keys ========================================
     const int t0 = split * a.tok_per_split;
-    const int t1 = min(NQ, t0 + a.tok_per_split);
+    const int t1 = min(NQK, t0 + a.tok_per_split);
     const int n_tok = max(0, t1 - t0);
     const int n_chunks = (n_tok + kAChunk - 1) / kAChunk;
-    const size_t tok0 = bh * a.max_tokens;         // token row base of (b, h)
-    const size_t grp0 = bh * (a.max_tokens / 32);  // key group row base of (b, h)
-    auto produce = [&](int c) {                    // thread 0
+    const size_t tok0 = bh * a.max_tokens;              // token row base of (b, hk)
+    const size_t grp0 = bh * (a.max_tokens / kGroup);   // key group row base of (b, hk)
+    auto produce = [&](int c) {                         // thread 0
       const int st = c % kAStages;
-      unsigned char* dst = sma + kAOffRing + st * kAStageBytes;
+      unsigned char* dst = sma + st * L::kStage;
       const int t = t0 + c * kAChunk;
-      const int n = min(kAChunk, t1 - t), ng = n / 32;
-      mbar_arrive_expect_tx(&full[st], (uint32_t)(n * 32 * 2 + ng * kD * 2 * 2 + n * 8 * 2));
-      bulk_g2s(dst + kCKc, a.k_codes + (tok0 + t) * 32, n * 32, &full[st]);
-      bulk_g2s(dst + kCVc, a.v_codes + (tok0 + t) * 32, n * 32, &full[st]);
-      bulk_g2s(dst + kCKs, a.k_scale + (grp0 + t / 32) * kD, ng * kD * 2, &full[st]);
-      bulk_g2s(dst + kCKz, a.k_zero + (grp0 + t / 32) * kD, ng * kD * 2, &full[st]);
-      bulk_g2s(dst + kCVs, a.v_scale + (tok0 + t) * 4, n * 8, &full[st]);
-      bulk_g2s(dst + kCVz, a.v_zero + (tok0 + t) * 4, n * 8, &full[st]);
+      const int n = min(kAChunk, t1 - t), ng = n / kGroup;
+      mbar_arrive_expect_tx(&full[st], (uint32_t)(n * (L::kKRow + L::kVRow) + ng * kD * 2 * 2 + n * 8 * 2));
+      bulk_g2s(dst + L::kCKc, a.k_codes + (tok0 + t) * L::kKRow, n * L::kKRow, &full[st]);
+      bulk_g2s(dst + L::kCVc, a.v_codes + (tok0 + t) * L::kVRow, n * L::kVRow, &full[st]);
+      bulk_g2s(dst + L::kCKs, a.k_scale + (grp0 + t / kGroup) * kD, ng * kD * 2, &full[st]);
+      bulk_g2s(dst + L::kCKz, a.k_zero + (grp0 + t / kGroup) * kD, ng * kD * 2, &full[st]);
+      bulk_g2s(dst + L::kCVs, a.v_scale + (tok0 + t) * 4, n * 8, &full[st]);
+      bulk_g2s(dst + L::kCVz, a.v_zero + (tok0 + t) * 4, n * 8, &full[st]);
     };
     int issued = 0;  // thread 0
     if (tid == 0)
@@ -274,27 +446,30 @@ __global__ void __launch_bounds__(kAThreads) kivi_attn_kernel(const KiviAttnArgs
     for (int c = 0; c < n_chunks; ++c) {
       const int st = c % kAStages;
       kivi_wait(&full[st], (c / kAStages) & 1, failed, a.err);
-      const unsigned char* stage = sma + kAOffRing + st * kAStageBytes;
-      const int n = min(kAChunk, t1 - (t0 + c * kAChunk)), ng = n / 32;
+      const unsigned char* stage = sma + st * L::kStage;
+      const int tc0 = t0 + c * kAChunk;  // token of chunk row 0
+      const int n = min(kAChunk, t1 - tc0), ng = n / kGroup;
       // ---- q' = q s per key group (the scale folds into the query) and bias = -sum q' z ----
       {
         const int g = warp >> 1, hf = warp & 1;
         if (g < ng) {
           const int ch = 64 * hf + 2 * lane;
-          const uint32_t s2 = *reinterpret_cast<const uint32_t*>(stage + kCKs + (g * kD + ch) * 2);
-          const uint32_t z2 = *reinterpret_cast<const uint32_t*>(stage + kCKz + (g * kD + ch) * 2);
-          const float qa = qs[ch] * h2f(s2 & 0xFFFFu), qb = qs[ch + 1] * h2f(s2 >> 16);
-          // pair layout: [group][half][word m][j] = (channel 16m + j, channel 16m + 8 + j) of the
-          // half, scaled by 4^-j to match code_pair
+          const uint32_t s2 = *reinterpret_cast<const uint32_t*>(stage + L::kCKs + (g * kD + ch) * 2);
+          const uint32_t z2 = *reinterpret_cast<const uint32_t*>(stage + L::kCKz + (g * kD + ch) * 2);
+          const float sa = h2f(s2 & 0xFFFFu), sb = h2f(s2 >> 16), za = h2f(z2 & 0xFFFFu), zb = h2f(z2 >> 16);
+          int ja, jb;
+          const int ia = qpair_index<KB>(ch & 63, ja), ib = qpair_index<KB>((ch + 1) & 63, jb);
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = ch + e, k = c & 15, j = k & 7;
-            qf[g * kD + 64 * hf + 2 * (8 * ((c & 63) >> 4) + j) + (k >> 3)] = (e ? qb : qa) * pow4_neg(j);
+          for (int r = 0; r < RH; ++r) {
+            const float qa = qs[r * kD + ch] * sa, qb = qs[r * kD + ch + 1] * sb;
+            float* qr = qf + (r * 4 + g) * kD + 64 * hf;
+            qr[ia] = qa * pow2_neg(KB * ja);
+            qr[ib] = qb * pow2_neg(KB * jb);
+            float pb = -(qa * za + qb * zb);
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) pb += __shfl_xor_sync(0xFFFFFFFFu, pb, off);
+            if (lane == 0) bias[(r * 4 + g) * 2 + hf] = pb;
           }
-          float pb = -(qa * h2f(z2 & 0xFFFFu) + qb * h2f(z2 >> 16));
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) pb += __shfl_xor_sync(0xFFFFFFFFu, pb, off);
-          if (lane == 0) bias[g * 2 + hf] = pb;
         }
       }
       __syncthreads();
@@ -303,50 +478,111 @@ __global__ void __launch_bounds__(kAThreads) kivi_attn_kernel(const KiviAttnArgs
         const int g = warp >> 1;
         if (g < ng) {
           const int tk = 32 * g + 16 * (warp & 1) + (lane & 15), chh = lane >> 4;
-          const uint4 cw = *reinterpret_cast<const uint4*>(stage + kCKc + tk * 32 + 16 * chh);
-          const uint32_t wds[4] = {cw.x, cw.y, cw.z, cw.w};
-          const float2* q2 = reinterpret_cast<const float2*>(qf + g * kD + 64 * chh);
-          float2 acc2 = make_float2(0.f, 0.f);
+          uint32_t wds[L::kKW];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
+          for (int k4 = 0; k4 < L::kKW / 4; ++k4) {
+            const uint4 cw = *reinterpret_cast<const uint4*>(stage + L::kCKc + tk * L::kKRow + chh * (L::kKRow / 2) + 16 * k4);
+            wds[4 * k4] = cw.x;
+            wds[4 * k4 + 1] = cw.y;
+            wds[4 * k4 + 2] = cw.z;
+            wds[4 * k4 + 3] = cw.w;
+          }
+          float2 acc2[RH];
+#pragma unroll
+          for (int r = 0; r < RH; ++r) acc2[r] = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int k = 0; k < L::kKW; ++k) {
             const uint32_t w_hi = wds[k] >> 16;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc2 = __ffma2_rn(q2[8 * k + j], code_pair(wds[k], w_hi, j), acc2);
+            for (int j = 0; j < L::kPK; ++j) {
+              const float2 cp = code_pair<KB>(wds[k], w_hi, j);
+#pragma unroll
+              for (int r = 0; r < RH; ++r) {
+                const float2* q2 = reinterpret_cast<const float2*>(qf + (r * 4 + g) * kD + 64 * chh);
+                acc2[r] = __ffma2_rn(q2[k * L::kPK + j], cp, acc2[r]);
+              }
+            }
           }
-          float acc = acc2.x + acc2.y;
-          acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 16);
-          if (chh == 0) sc[tk] = (acc + bias[g * 2] + bias[g * 2 + 1]) * scale_log2;
+#pragma unroll
+          for (int r = 0; r < RH; ++r) {
+            float acc = acc2[r].x + acc2[r].y;
+            acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 16);
+            if (chh == 0) sc[r * sc_stride + tk] = (acc + bias[(r * 4 + g) * 2] + bias[(r * 4 + g) * 2 + 1]) * scale_log2;
+          }
         }
       }
       __syncthreads();
-      // ---- online softmax, then values: warp w takes tokens 16w .. 16w + 15, four at a time;
-      //      lane: token 4 step + lane / 8, code word lane % 8 (channels 16 (lane % 8) .. + 15,
-      //      value group (lane % 8) / 2) ----
-      const float Mn = fmaxf(M, scores_max(n));
-      if (Mn > M) rescale_to(Mn);
+      // ---- online softmax, then values: warp w takes tokens 16w .. 16w + 15, kTS at a time;
+      //      lane: token slot lane / kVW, code word lane % kVW (value group word / kWPG) ----
+#pragma unroll
+      for (int r = 0; r < RH; ++r) {
+        const float Mn = fmaxf(M[r], scores_max(sc + r * sc_stride, n));
+        if (Mn > M[r]) rescale_to(r, Mn);
+      }
       {
         const int tb = 16 * warp;
-        const float pk = (tb + (lane & 15) < n) ? exp2f(sc[tb + (lane & 15)] - M) : 0.f;
-        float ls = (lane < 16) ? pk : 0.f;
+        float pk[RH];
 #pragma unroll
-        for (int off = 8; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, off);
-        l += __shfl_sync(0xFFFFFFFFu, ls, 0);
-        const int lw = lane & 7, ts = lane >> 3, gv = lw >> 1;
+        for (int r = 0; r < RH; ++r) {
+          pk[r] = (tb + (lane & 15) < n) ? exp2f(sc[r * sc_stride + tb + (lane & 15)] - M[r]) : 0.f;
+          float ls = (lane < 16) ? pk[r] : 0.f;
 #pragma unroll
-        for (int step = 0; step < 4; ++step) {
-          const float p = __shfl_sync(0xFFFFFFFFu, pk, 4 * step + ts);
-          const int tk = tb + 4 * step + ts;
-          if (tk < n) {
-            const uint32_t wv = *reinterpret_cast<const uint32_t*>(stage + kCVc + tk * 32 + 4 * lw);
-            const float wgt = p * h2f(*reinterpret_cast<const uint16_t*>(stage + kCVs + (tk * 4 + gv) * 2));
-            oz = fmaf(wgt, h2f(*reinterpret_cast<const uint16_t*>(stage + kCVz + (tk * 4 + gv) * 2)), oz);
+          for (int off = 8; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, off);
+          l[r] += __shfl_sync(0xFFFFFFFFu, ls, 0);
+        }
+        const int lw = lane % L::kVW, ts = lane / L::kVW, gv = lw / L::kWPG;
+#pragma unroll
+        for (int step = 0; step < 16 / L::kTS; ++step) {
+          float p[RH];
+#pragma unroll
+          for (int r = 0; r < RH; ++r) p[r] = __shfl_sync(0xFFFFFFFFu, pk[r], L::kTS * step + ts);
+          const int tk = tb + L::kTS * step + ts;
+          if (tk >= n) continue;
+          if (tc0 + tk < NQV) {
+            const uint32_t wv = *reinterpret_cast<const uint32_t*>(stage + L::kCVc + tk * L::kVRow + 4 * lw);
+            const float sv = h2f(*reinterpret_cast<const uint16_t*>(stage + L::kCVs + (tk * 4 + gv) * 2));
+            const float zv = h2f(*reinterpret_cast<const uint16_t*>(stage + L::kCVz + (tk * 4 + gv) * 2));
+            float2 w2[RH];
+#pragma unroll
+            for (int r = 0; r < RH; ++r) {
+              const float wgt = p[r] * sv;
+              oz[r] = fmaf(wgt, zv, oz[r]);
+              w2[r] = make_float2(wgt, wgt);
+            }
             const uint32_t wv_hi = wv >> 16;
-            const float2 w2 = make_float2(wgt, wgt);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {  // o2[j] = (channel j, channel 8 + j) of the word, x 4^j
-              const float2 acc = __ffma2_rn(w2, code_pair(wv, wv_hi, j), make_float2(o[2 * j], o[2 * j + 1]));
-              o[2 * j] = acc.x;
-              o[2 * j + 1] = acc.y;
+            for (int j = 0; j < L::kPV; ++j) {  // (channel j, channel kPV + j) of the word, x 2^(b j)
+              const float2 cp = code_pair<VB>(wv, wv_hi, j);
+#pragma unroll
+              for (int r = 0; r < RH; ++r) {
+                const float2 acc = __ffma2_rn(w2[r], cp, make_float2(o[r][2 * j], o[r][2 * j + 1]));
+                o[r][2 * j] = acc.x;
+                o[r][2 * j + 1] = acc.y;
+              }
+            }
+          } else {  // key quantized, value still in the fp16 window
+            const int t = tc0 + tk;
+            const uint4* vr = reinterpret_cast<const uint4*>(a.v_resid + (bh * R + t % R) * kD + lw * L::kCPWv);
+            uint32_t hv[L::kCPWv / 2];
+#pragma unroll
+            for (int k4 = 0; k4 < L::kCPWv / 8; ++k4) {
+              const uint4 u = __ldg(vr + k4);
+              hv[4 * k4] = u.x;
+              hv[4 * k4 + 1] = u.y;
+              hv[4 * k4 + 2] = u.z;
+              hv[4 * k4 + 3] = u.w;
+            }
+#pragma unroll
+            for (int j = 0; j < L::kPV; ++j) {
+              const int e0 = j, e1 = L::kPV + j;
+              const float v0 = h2f((e0 & 1) ? (hv[e0 >> 1] >> 16) : (hv[e0 >> 1] & 0xFFFFu));
+              const float v1 = h2f((e1 & 1) ? (hv[e1 >> 1] >> 16) : (hv[e1 >> 1] & 0xFFFFu));
+              const float sj = pow2_pos(VB * j);
+#pragma unroll
+              for (int r = 0; r < RH; ++r) {
+                o[r][2 * j] = fmaf(p[r] * sj, v0, o[r][2 * j]);
+                o[r][2 * j + 1] = fmaf(p[r] * sj, v1, o[r][2 * j + 1]);
+              }
             }
           }
         }
@@ -361,11 +597,13 @@ __global__ void __launch_bounds__(kAThreads) kivi_attn_kernel(const KiviAttnArgs
     if (tid == 0 && *failed)
       for (int c = max(0, issued - kAStages); c < issued; ++c) mbar_wait_bounded(&full[c % kAStages], (c / kAStages) & 1);
   } else {
-    // ================================ fp16 residual tokens ==================================
-    const int NR = min(a.n_resid[b], a.residual);
-    for (int r = tid; r < NR; r += kAThreads) {  // keys: a thread per token
-      const uint4* kr = reinterpret_cast<const uint4*>(a.k_resid + (bh * a.residual + r) * kD);
-      float acc = 0.f;
+    // ================================ fp16 key residual =====================================
+    const int NR = max(0, min(a.n_tok[b] - NQK, R));
+    for (int rr = tid; rr < NR; rr += kAThreads) {  // keys: a thread per token
+      const uint4* kr = reinterpret_cast<const uint4*>(a.k_resid + (bh * R + rr) * kD);
+      float acc[RH];
+#pragma unroll
+      for (int r = 0; r < RH; ++r) acc[r] = 0.f;
 #pragma unroll 4
       for (int k8 = 0; k8 < kD / 8; ++k8) {
         const uint4 v = __ldg(kr + k8);
@@ -373,82 +611,126 @@ __global__ void __launch_bounds__(kAThreads) kivi_attn_kernel(const KiviAttnArgs
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-          acc = fmaf(qs[k8 * 8 + 2 * i], f.x, acc);
-          acc = fmaf(qs[k8 * 8 + 2 * i + 1], f.y, acc);
+#pragma unroll
+          for (int r = 0; r < RH; ++r) {
+            acc[r] = fmaf(qs[r * kD + k8 * 8 + 2 * i], f.x, acc[r]);
+            acc[r] = fmaf(qs[r * kD + k8 * 8 + 2 * i + 1], f.y, acc[r]);
+          }
         }
       }
-      sc[r] = acc * scale_log2;
+#pragma unroll
+      for (int r = 0; r < RH; ++r) sc[r * sc_stride + rr] = acc[r] * scale_log2;
     }
     __syncthreads();
-    rescale_to(scores_max(NR));
-    for (int r = warp; r < NR; r += kAWarps) {  // values: a warp per token, lane 4 channels
-      const float p = exp2f(sc[r] - M);
-      l += p;
-      const uint2 v = __ldg(reinterpret_cast<const uint2*>(a.v_resid + (bh * a.residual + r) * kD + lane * 4));
+#pragma unroll
+    for (int r = 0; r < RH; ++r) rescale_to(r, scores_max(sc + r * sc_stride, NR));
+    for (int rr = warp; rr < NR; rr += kAWarps) {  // values: a warp per token, lane 4 channels
+      const int t = NQK + rr;
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(a.v_resid + (bh * R + t % R) * kD + lane * 4));
       const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
       const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
-      o[0] = fmaf(p, f0.x, o[0]);
-      o[1] = fmaf(p, f0.y, o[1]);
-      o[2] = fmaf(p, f1.x, o[2]);
-      o[3] = fmaf(p, f1.y, o[3]);
+#pragma unroll
+      for (int r = 0; r < RH; ++r) {
+        const float p = exp2f(sc[r * sc_stride + rr] - M[r]);
+        l[r] += p;
+        o[r][0] = fmaf(p, f0.x, o[r][0]);
+        o[r][1] = fmaf(p, f0.y, o[r][1]);
+        o[r][2] = fmaf(p, f1.x, o[r][2]);
+        o[r][3] = fmaf(p, f1.y, o[r][3]);
+      }
     }
   }
 
-  // ---- warps -> block: sum o - oz and l over the warps (one max for the block) -----------
+  // ---- warps -> block: sum o - oz and l over the warps (one max per head for the block) ----
   __syncthreads();  // the ring is idle
-  float* ored = reinterpret_cast<float*>(sma + kAOffRing);  // [warp][128]
-  if (!resid_block) {  // the four token slots of a code word meet, then 8 lanes hold 128 channels
+  float* ored = reinterpret_cast<float*>(sma);  // [warp][RH][128]
+  if (!resid_block) {  // the token slots of a code word meet, then kVW lanes hold 128 channels
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      o[i] += __shfl_xor_sync(0xFFFFFFFFu, o[i], 8);
-      o[i] += __shfl_xor_sync(0xFFFFFFFFu, o[i], 16);
+    for (int r = 0; r < RH; ++r) {
+#pragma unroll
+      for (int off = L::kVW; off < 32; off <<= 1) {
+#pragma unroll
+        for (int i = 0; i < L::kCPWv; ++i) o[r][i] += __shfl_xor_sync(0xFFFFFFFFu, o[r][i], off);
+        oz[r] += __shfl_xor_sync(0xFFFFFFFFu, oz[r], off);
+      }
     }
-    oz += __shfl_xor_sync(0xFFFFFFFFu, oz, 8);
-    oz += __shfl_xor_sync(0xFFFFFFFFu, oz, 16);
-    if (lane < 8) {  // o[2j] is channel j of the word, o[2j + 1] channel 8 + j, both x 4^j
+    if (lane < L::kVW) {  // o[r][2j] is channel j of the word, o[r][2j + 1] channel kPV + j, x 2^(b j)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        ored[warp * kD + 16 * lane + j] = o[2 * j] * pow4_neg(j) - oz;
-        ored[warp * kD + 16 * lane + 8 + j] = o[2 * j + 1] * pow4_neg(j) - oz;
+      for (int r = 0; r < RH; ++r) {
+        float* dst = ored + (warp * RH + r) * kD + lane * L::kCPWv;
+#pragma unroll
+        for (int j = 0; j < L::kPV; ++j) {
+          dst[j] = o[r][2 * j] * pow2_neg(VB * j) - oz[r];
+          dst[L::kPV + j] = o[r][2 * j + 1] * pow2_neg(VB * j) - oz[r];
+        }
       }
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) ored[warp * kD + lane * 4 + i] = o[i];
+    for (int r = 0; r < RH; ++r)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ored[(warp * RH + r) * kD + lane * 4 + i] = o[r][i];
   }
-  if (lane == 0) red[warp] = l;
+  if (lane == 0)
+#pragma unroll
+    for (int r = 0; r < RH; ++r) red[warp * RH + r] = l[r];
   __syncthreads();
   if (*failed) return;  // uniform after the barrier
-  float ov = 0.f, Ls = 0.f;
-  if (tid < kD) {
-    for (int w = 0; w < kAWarps; ++w) {
-      ov += ored[w * kD + tid];
-      Ls += red[w];
+
+  constexpr int kIt = (RH * kD + kAThreads - 1) / kAThreads;  // outputs per thread
+  float ov[kIt], Ls[kIt], Mv[kIt];
+#pragma unroll
+  for (int it = 0; it < kIt; ++it) {
+    const int i = it * kAThreads + tid, r = i / kD, ch = i % kD;
+    ov[it] = 0.f;
+    Ls[it] = 0.f;
+    Mv[it] = M[0];
+#pragma unroll
+    for (int rr = 1; rr < RH; ++rr)
+      if (r == rr) Mv[it] = M[rr];
+    if (i < RH * kD) {
+      for (int w = 0; w < kAWarps; ++w) {
+        ov[it] += ored[(w * RH + r) * kD + ch];
+        Ls[it] += red[w * RH + r];
+      }
     }
   }
+  auto write_out = [&](int i, float val) {
+    if (a.out_fp32) reinterpret_cast<float*>(a.out)[bq0 * kD + i] = val;
+    else reinterpret_cast<uint16_t*>(a.out)[bq0 * kD + i] = f32_to_bf16(val);
+  };
 
   if (n_total == 1) {
-    if (tid < kD) {
-      const float val = (Ls > 0.f) ? ov / Ls : 0.f;
-      if (a.out_fp32) reinterpret_cast<float*>(a.out)[bh * kD + tid] = val;
-      else reinterpret_cast<uint16_t*>(a.out)[bh * kD + tid] = f32_to_bf16(val);
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) {
+      const int i = it * kAThreads + tid;
+      if (i < RH * kD) write_out(i, (Ls[it] > 0.f) ? ov[it] / Ls[it] : 0.f);
     }
     return;
   }
-  float* pp = a.part + (bh * n_total + split) * (kD + 2);
-  if (tid < kD) pp[2 + tid] = ov;
-  if (tid == 0) {
-    pp[0] = M;
-    pp[1] = Ls;
+#pragma unroll
+  for (int it = 0; it < kIt; ++it) {
+    const int i = it * kAThreads + tid, r = i / kD, ch = i % kD;
+    if (i < RH * kD) {
+      float* pp = a.part + ((bq0 + r) * n_total + split) * (kD + 2);
+      pp[2 + ch] = ov[it];
+      if (ch == 0) {
+        pp[0] = Mv[it];
+        pp[1] = Ls[it];
+      }
+    }
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) *flag = (atomicAdd(&a.counters[bh], 1) == n_total - 1);
+  if (tid == 0) *flag = (atomicAdd(&a.counters[bq0], 1) == n_total - 1);
   __syncthreads();
   if (!*flag) return;
   __threadfence();
-  if (tid < kD) {
-    const float* base = a.part + bh * n_total * (kD + 2);
+#pragma unroll
+  for (int it = 0; it < kIt; ++it) {
+    const int i = it * kAThreads + tid, r = i / kD, ch = i % kD;
+    if (i >= RH * kD) continue;
+    const float* base = a.part + (bq0 + r) * n_total * (kD + 2);
     float Mx = -INFINITY;
     for (int s = 0; s < n_total; ++s) Mx = fmaxf(Mx, __ldcg(base + s * (kD + 2)));
     float Lt = 0.f, acc = 0.f;
@@ -458,21 +740,64 @@ __global__ void __launch_bounds__(kAThreads) kivi_attn_kernel(const KiviAttnArgs
         if (ms == -INFINITY) continue;
         const float w = exp2f(ms - Mx);
         Lt = fmaf(w, __ldcg(base + s * (kD + 2) + 1), Lt);
-        acc = fmaf(w, __ldcg(base + s * (kD + 2) + 2 + tid), acc);
+        acc = fmaf(w, __ldcg(base + s * (kD + 2) + 2 + ch), acc);
       }
     }
-    const float val = (Lt > 0.f) ? acc / Lt : 0.f;
-    if (a.out_fp32) reinterpret_cast<float*>(a.out)[bh * kD + tid] = val;
-    else reinterpret_cast<uint16_t*>(a.out)[bh * kD + tid] = f32_to_bf16(val);
+    write_out(i, (Lt > 0.f) ? acc / Lt : 0.f);
   }
-  if (tid == 0) a.counters[bh] = 0;
+  if (tid == 0) a.counters[bq0] = 0;
+}
+
+template <int KB, int VB, int RH>
+size_t attn_smem(int residual) {
+  return (size_t)AttnLayout<KB, VB, RH>::kOffSc + 4 * (size_t)RH * max(kAChunk, residual);
+}
+
+template <int KB, int VB, int RH>
+cudaError_t launch_attn(const KiviAttnArgs& a, cudaStream_t st) {
+  const size_t smem = attn_smem<KB, VB, RH>(a.residual);
+  cudaError_t e = cudaFuncSetAttribute(kivi_attn_kernel<KB, VB, RH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)kD);
+  const int n_sub = (a.Hq / a.H) / RH;
+  // quantized splits, plus one block for the fp16 residual segment, per head subgroup
+  dim3 grid((a.n_split + (a.residual > 0 ? 1 : 0)) * n_sub, a.B, a.H);
+  kivi_attn_kernel<KB, VB, RH><<<grid, kAThreads, smem, st>>>(a, scale_log2, max(kAChunk, a.residual));
+  return cudaGetLastError();
+}
+
+template <int KB, int VB>
+cudaError_t launch_attn_rh(const KiviAttnArgs& a, int rh, cudaStream_t st) {
+  if (rh == 4) return launch_attn<KB, VB, 4>(a, st);
+  if (rh == 2) return launch_attn<KB, VB, 2>(a, st);
+  return launch_attn<KB, VB, 1>(a, st);
+}
+
+template <int KB, int VB>
+size_t smem_rh(int rh, int residual) {
+  if (rh == 4) return attn_smem<KB, VB, 4>(residual);
+  if (rh == 2) return attn_smem<KB, VB, 2>(residual);
+  return attn_smem<KB, VB, 1>(residual);
+}
+
+int sm_count_cached() {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
 }
 
 }  // namespace
 
+int kivi_heads_per_block(int rep) { return (rep % 4 == 0) ? 4 : (rep % 2 == 0) ? 2 : 1; }
+
 int kivi_attn_max_tok_per_split(int) { return 1 << 30; }  // tokens stream through the ring
 
-size_t kivi_attn_smem_bytes(int, int residual) { return (size_t)kAOffSc + 4 * (size_t)max(kAChunk, residual); }
+size_t kivi_attn_smem_bytes(int k_bits, int v_bits, int rh, int residual) {
+  if (k_bits == 2 && v_bits == 2) return smem_rh<2, 2>(rh, residual);
+  if (k_bits == 2 && v_bits == 4) return smem_rh<2, 4>(rh, residual);
+  if (k_bits == 4 && v_bits == 2) return smem_rh<4, 2>(rh, residual);
+  return smem_rh<4, 4>(rh, residual);
+}
 
 cudaError_t launch_kivi_quantize(const KiviQuantArgs& a, cudaStream_t s) {
   // grid-stride warps; 8 blocks of 256 threads per SM keep enough rows in flight
@@ -480,23 +805,40 @@ cudaError_t launch_kivi_quantize(const KiviQuantArgs& a, cudaStream_t s) {
                                                       : ((long long)a.B * a.H * a.n_tok + 3) / 4;
   if (warps <= 0) return cudaSuccess;
   long long blocks = (warps + 7) / 8;
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = sm_count_cached();
   if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
-  if (a.axis == KVQ_PER_CHANNEL) kivi_quant_channel_kernel<<<(int)blocks, 256, 0, s>>>(a);
-  else kivi_quant_token_kernel<<<(int)blocks, 256, 0, s>>>(a);
+  if (a.axis == KVQ_PER_CHANNEL) {
+    if (a.bits == 4) kivi_quant_channel_kernel<4><<<(int)blocks, 256, 0, s>>>(a);
+    else kivi_quant_channel_kernel<2><<<(int)blocks, 256, 0, s>>>(a);
+  } else {
+    if (a.bits == 4) kivi_quant_token_kernel<4><<<(int)blocks, 256, 0, s>>>(a);
+    else kivi_quant_token_kernel<2><<<(int)blocks, 256, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kivi_prefill_tail(const KiviTailArgs& a, cudaStream_t s) {
+  if (a.B <= 0) return cudaSuccess;
+  kivi_prefill_tail_kernel<<<dim3(a.B, a.H), 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kivi_append(const KiviAppendArgs& a, cudaStream_t s) {
+  if (a.n_seq <= 0) return cudaSuccess;
+  const dim3 grid(a.n_seq, a.H);
+  if (a.k_bits == 2 && a.v_bits == 2) kivi_append_kernel<2, 2><<<grid, 128, 0, s>>>(a);
+  else if (a.k_bits == 2) kivi_append_kernel<2, 4><<<grid, 128, 0, s>>>(a);
+  else if (a.v_bits == 2) kivi_append_kernel<4, 2><<<grid, 128, 0, s>>>(a);
+  else kivi_append_kernel<4, 4><<<grid, 128, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_kivi_attn(const KiviAttnArgs& a, cudaStream_t st) {
-  const size_t smem = kivi_attn_smem_bytes(a.tok_per_split, a.residual);
-  cudaError_t e = cudaFuncSetAttribute(kivi_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  const float scale_log2 = 1.4426950408889634f / sqrtf((float)kD);
-  // quantized splits, plus one block for the fp16 residual segment
-  dim3 grid(a.n_split + (a.residual > 0 ? 1 : 0), a.B, a.H);
-  kivi_attn_kernel<<<grid, kAThreads, smem, st>>>(a, scale_log2);
-  return cudaGetLastError();
+  const int rh = kivi_heads_per_block(a.Hq / a.H);
+  if (a.k_bits == 2 && a.v_bits == 2) return launch_attn_rh<2, 2>(a, rh, st);
+  if (a.k_bits == 2 && a.v_bits == 4) return launch_attn_rh<2, 4>(a, rh, st);
+  if (a.k_bits == 4 && a.v_bits == 2) return launch_attn_rh<4, 2>(a, rh, st);
+  return launch_attn_rh<4, 4>(a, rh, st);
 }
 
 }  // namespace kvq

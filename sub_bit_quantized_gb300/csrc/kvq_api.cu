@@ -95,15 +95,31 @@ size_t vq_ws_bytes(const kvq_vq_cfg* c, int B, int blocks) { return kvq::vq_attn
 // ---- KIVI config -----------------------------------------------------------------------
 kvq_status check_kivi_cfg(const kvq_kivi_cfg* c, const char* fn) {
   if (!c) return fail(KVQ_ERR_INVALID_ARG, "%s: cfg is null", fn);
-  if (c->D <= 0 || c->n_heads <= 0 || c->bits <= 0 || c->group <= 0 || c->residual < 0 || c->max_batch <= 0 ||
-      c->max_tokens < 0)
+  if (c->D <= 0 || c->n_heads <= 0 || c->n_q_heads <= 0 || c->k_bits <= 0 || c->v_bits <= 0 || c->group <= 0 ||
+      c->residual < 0 || c->max_batch <= 0 || c->max_tokens < 0)
     return fail(KVQ_ERR_INVALID_ARG, "%s: cfg has a non-positive field", fn);
-  if (c->max_tokens % c->group != 0 || c->D % c->group != 0)
-    return fail(KVQ_ERR_INVALID_ARG, "%s: group=%d must divide D=%d and max_tokens=%d", fn, c->group, c->D,
-                c->max_tokens);
+  if (c->max_tokens % c->group != 0 || c->D % c->group != 0 || c->residual % c->group != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "%s: group=%d must divide D=%d, max_tokens=%d and residual=%d", fn, c->group,
+                c->D, c->max_tokens, c->residual);
+  if (c->n_q_heads % c->n_heads != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "%s: n_q_heads=%d is not a multiple of n_heads=%d", fn, c->n_q_heads,
+                c->n_heads);
   if (c->D != kvq::kD) return fail(KVQ_ERR_UNSUPPORTED, "%s: D=%d (this build supports 128)", fn, c->D);
-  if (c->bits != 2) return fail(KVQ_ERR_UNSUPPORTED, "%s: bits=%d (this build supports 2)", fn, c->bits);
+  if ((c->k_bits != 2 && c->k_bits != 4) || (c->v_bits != 2 && c->v_bits != 4))
+    return fail(KVQ_ERR_UNSUPPORTED, "%s: k_bits=%d v_bits=%d (this build supports 2 and 4)", fn, c->k_bits,
+                c->v_bits);
   if (c->group != 32) return fail(KVQ_ERR_UNSUPPORTED, "%s: group=%d (this build supports 32)", fn, c->group);
+  if (c->n_heads > 65535 || c->max_batch > 65535)
+    return fail(KVQ_ERR_UNSUPPORTED, "%s: n_heads and max_batch must be at most 65535", fn);
+  return KVQ_OK;
+}
+
+kvq_status check_kivi_cache(const kvq_kivi_cache* k, const char* fn) {
+  if (!k) return fail(KVQ_ERR_INVALID_ARG, "%s: cache is null", fn);
+  const void* ptrs[] = {k->k_codes, k->k_scale, k->k_zero, k->v_codes, k->v_scale, k->v_zero,
+                        k->k_resid, k->v_resid, k->n_tok,  k->n_quant_k, k->n_quant_v, k->sync};
+  for (const void* pp : ptrs)
+    if (!aligned16(pp)) return fail(KVQ_ERR_INVALID_ARG, "%s: a cache pointer is null or misaligned", fn);
   return KVQ_OK;
 }
 
@@ -111,9 +127,10 @@ struct KiviPlan {
   int n_split, tps;
 };
 
-// Quantized-token splits of the KIVI kernel (one more block per (request, head) takes the fp16
-// residual). Fill whole waves of blocks (about four resident per SM) and balance a split's
-// quantized tokens (96 B each) against the residual block's (512 B each).
+// Quantized-token splits of the KIVI kernel (one more block per (request, KV head, head
+// subgroup) takes the fp16 key residual). Fill whole waves of blocks (about four resident per
+// SM) and balance a split's quantized tokens against the residual block's fp16 tokens (512 B
+// each) by the bytes each streams.
 KiviPlan plan_kivi(const kvq_kivi_cfg* c, int B, int n_splits) {
   auto tps_for = [&](int n) {
     int t = (c->max_tokens + n - 1) / n;
@@ -123,12 +140,14 @@ KiviPlan plan_kivi(const kvq_kivi_cfg* c, int B, int n_splits) {
   if (c->max_tokens == 0) return KiviPlan{1, 0};
   const int slots = 4 * sm_count();
   const int extra = c->residual > 0 ? 1 : 0;
-  const double resid_cost = c->residual * (512.0 / 96.0);
+  const int rh = kvq::kivi_heads_per_block(c->n_q_heads / c->n_heads);
+  const double q_bytes = (c->k_bits + c->v_bits) * 16.0 + 24.0;  // codes + per-token share of scales
+  const double resid_cost = c->residual * (512.0 / q_bytes);
   KiviPlan p{1, tps_for(1)};
   double best = 1e300;
   for (int n = 1; n <= std::min(64, c->max_tokens / c->group); ++n) {
     const int tps = tps_for(n);
-    const long long blocks = (long long)B * c->n_heads * (n + extra);
+    const long long blocks = (long long)B * (c->n_q_heads / rh) * (n + extra);
     const long long waves = (blocks + slots - 1) / slots;
     const double cost = (double)waves * (std::max((double)tps, resid_cost) + 64.0);
     if (cost < best * 0.999) {
@@ -142,8 +161,8 @@ KiviPlan plan_kivi(const kvq_kivi_cfg* c, int B, int n_splits) {
 size_t kivi_ws_bytes(const kvq_kivi_cfg* c, int B, const KiviPlan& p) {
   const int total = p.n_split + (c->residual > 0 ? 1 : 0);
   if (total <= 1) return 0;
-  return align256((size_t)B * c->n_heads * total * (kvq::kD + 2) * sizeof(float)) +
-         align256((size_t)B * c->n_heads * sizeof(int));
+  return align256((size_t)B * c->n_q_heads * total * (kvq::kD + 2) * sizeof(float)) +
+         align256((size_t)B * c->n_q_heads * sizeof(int));
 }
 
 }  // namespace
@@ -369,9 +388,73 @@ KVQ_API kvq_status kvq_quantize_kivi(const kvq_kivi_cfg* c, int axis, const uint
   if (B == 0 || n_tok == 0) return KVQ_OK;
   kvq::KiviQuantArgs a{};
   a.x = x; a.sb = st_b; a.sh = st_h; a.codes = codes; a.scale = scale; a.zero = zero;
-  a.axis = axis; a.B = B; a.H = c->n_heads; a.n_tok = n_tok; a.tok_begin = tok_begin;
+  a.axis = axis; a.bits = (axis == KVQ_PER_CHANNEL) ? c->k_bits : c->v_bits;
+  a.B = B; a.H = c->n_heads; a.n_tok = n_tok; a.tok_begin = tok_begin;
   a.max_tokens = c->max_tokens; a.group = c->group;
   return cuda_status(kvq::launch_kivi_quantize(a, (cudaStream_t)stream), __func__);
+}
+
+KVQ_API kvq_status kvq_kivi_prefill(const kvq_kivi_cfg* c, const kvq_kivi_cache* k, const uint16_t* xk,
+                                    const uint16_t* xv, int64_t st_b, int64_t st_h, int b0, int B, int n_tok,
+                                    kvq_stream stream) {
+  kvq_status st = check_kivi_cfg(c, __func__);
+  if (st != KVQ_OK) return st;
+  if ((st = check_kivi_cache(k, __func__)) != KVQ_OK) return st;
+  if ((st = check_x_strides(__func__, 0, st_b, st_h)) != KVQ_OK) return st;
+  CHECK_PTR(xk);
+  CHECK_PTR(xv);
+  if (c->residual <= 0) return fail(KVQ_ERR_INVALID_ARG, "%s: the streaming cache needs residual > 0", __func__);
+  if (b0 < 0 || B < 0 || n_tok < 0) return fail(KVQ_ERR_INVALID_ARG, "%s: negative size", __func__);
+  const int R = c->residual, G = c->group;
+  const int nq = n_tok <= R ? 0 : (n_tok - R + G - 1) / G * G;
+  if (b0 + B > c->max_batch || nq > c->max_tokens)
+    return fail(KVQ_ERR_CAPACITY, "%s: requests or quantized tokens exceed the cache capacity", __func__);
+  if (B == 0) return KVQ_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t H = c->n_heads, N = c->max_tokens, D = c->D;
+  if (nq > 0) {
+    kvq::KiviQuantArgs a{};
+    a.sb = st_b; a.sh = st_h; a.B = B; a.H = c->n_heads; a.n_tok = nq; a.tok_begin = 0;
+    a.max_tokens = c->max_tokens; a.group = G;
+    a.x = xk; a.axis = KVQ_PER_CHANNEL; a.bits = c->k_bits;
+    a.codes = k->k_codes + (size_t)b0 * H * N * (D * c->k_bits / 8);
+    a.scale = k->k_scale + (size_t)b0 * H * (N / G) * D;
+    a.zero = k->k_zero + (size_t)b0 * H * (N / G) * D;
+    if ((st = cuda_status(kvq::launch_kivi_quantize(a, s), __func__)) != KVQ_OK) return st;
+    a.x = xv; a.axis = KVQ_PER_TOKEN; a.bits = c->v_bits;
+    a.codes = k->v_codes + (size_t)b0 * H * N * (D * c->v_bits / 8);
+    a.scale = k->v_scale + (size_t)b0 * H * N * (D / G);
+    a.zero = k->v_zero + (size_t)b0 * H * N * (D / G);
+    if ((st = cuda_status(kvq::launch_kivi_quantize(a, s), __func__)) != KVQ_OK) return st;
+  }
+  kvq::KiviTailArgs t{};
+  t.k = xk; t.v = xv; t.sb = st_b; t.sh = st_h; t.k_resid = k->k_resid; t.v_resid = k->v_resid;
+  t.n_tok = k->n_tok; t.n_quant_k = k->n_quant_k; t.n_quant_v = k->n_quant_v;
+  t.b0 = b0; t.B = B; t.H = c->n_heads; t.n_tok_new = n_tok; t.nq = nq; t.residual = R;
+  return cuda_status(kvq::launch_kivi_prefill_tail(t, s), __func__);
+}
+
+KVQ_API kvq_status kvq_kivi_append(const kvq_kivi_cfg* c, const kvq_kivi_cache* k, const uint16_t* k_new,
+                                   const uint16_t* v_new, int n_seq, kvq_stream stream) {
+  kvq_status st = check_kivi_cfg(c, __func__);
+  if (st != KVQ_OK) return st;
+  if ((st = check_kivi_cache(k, __func__)) != KVQ_OK) return st;
+  CHECK_PTR(k_new);
+  CHECK_PTR(v_new);
+  if (c->residual <= 0) return fail(KVQ_ERR_INVALID_ARG, "%s: the streaming cache needs residual > 0", __func__);
+  if (n_seq < 0) return fail(KVQ_ERR_INVALID_ARG, "%s: n_seq < 0", __func__);
+  if (n_seq > c->max_batch) return fail(KVQ_ERR_CAPACITY, "%s: n_seq > max_batch", __func__);
+  if (n_seq == 0) return KVQ_OK;
+  kvq::KiviAppendArgs a{};
+  a.k_new = k_new; a.v_new = v_new;
+  a.k_codes = k->k_codes; a.k_scale = k->k_scale; a.k_zero = k->k_zero;
+  a.v_codes = k->v_codes; a.v_scale = k->v_scale; a.v_zero = k->v_zero;
+  a.k_resid = k->k_resid; a.v_resid = k->v_resid;
+  a.n_tok = k->n_tok; a.n_quant_k = k->n_quant_k; a.n_quant_v = k->n_quant_v; a.sync = k->sync;
+  a.err = device_error_ptr();
+  a.n_seq = n_seq; a.H = c->n_heads; a.k_bits = c->k_bits; a.v_bits = c->v_bits; a.residual = c->residual;
+  a.max_tokens = c->max_tokens;
+  return cuda_status(kvq::launch_kivi_append(a, (cudaStream_t)stream), __func__);
 }
 
 KVQ_API size_t kvq_decode_workspace_size(int format, const void* cfg, int B, int n_splits) {
@@ -456,33 +539,37 @@ KVQ_API kvq_status kvq_decode_attn(int format, const void* cfg, const void* cach
     kvq_status st = check_kivi_cfg(c, __func__);
     if (st != KVQ_OK) return st;
     const kvq_kivi_cache* k = static_cast<const kvq_kivi_cache*>(cache);
-    if (!k) return fail(KVQ_ERR_INVALID_ARG, "%s: cache is null", __func__);
-    const void* ptrs[] = {k->k_codes, k->k_scale, k->k_zero, k->v_codes, k->v_scale,
-                          k->v_zero,  k->k_resid, k->v_resid, k->n_quant, k->n_resid};
-    for (const void* pp : ptrs)
-      if (!aligned16(pp)) return fail(KVQ_ERR_INVALID_ARG, "%s: a cache pointer is null or misaligned", __func__);
+    if ((st = check_kivi_cache(k, __func__)) != KVQ_OK) return st;
     if (B < 1) return fail(KVQ_ERR_INVALID_ARG, "%s: B < 1", __func__);
     if (B > c->max_batch) return fail(KVQ_ERR_CAPACITY, "%s: B > max_batch", __func__);
+    const int rh = kvq::kivi_heads_per_block(c->n_q_heads / c->n_heads);
+    if (kvq::kivi_attn_smem_bytes(c->k_bits, c->v_bits, rh, c->residual) > 232448)
+      return fail(KVQ_ERR_UNSUPPORTED, "%s: residual=%d needs more shared memory than a block has", __func__,
+                  c->residual);
     const KiviPlan p = plan_kivi(c, B, n_splits);
     if (p.tps > kvq::kivi_attn_max_tok_per_split(c->residual))
       return fail(KVQ_ERR_UNSUPPORTED, "%s: tokens per split exceed the shared-memory limit; use more splits",
                   __func__);
+    const int total = p.n_split + (c->residual > 0 ? 1 : 0);  // blocks per (request, head subgroup)
+    if ((long long)total * (c->n_q_heads / c->n_heads / rh) >= (1ll << 31))
+      return fail(KVQ_ERR_UNSUPPORTED, "%s: too many splits", __func__);
     const size_t need = kivi_ws_bytes(c, B, p);
     if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws)))
       return fail(KVQ_ERR_WORKSPACE, "%s: workspace needs %zu bytes (got %zu)", __func__, need, ws_bytes);
     kvq::KiviAttnArgs a{};
     a.k_codes = k->k_codes; a.k_scale = k->k_scale; a.k_zero = k->k_zero;
     a.v_codes = k->v_codes; a.v_scale = k->v_scale; a.v_zero = k->v_zero;
-    a.k_resid = k->k_resid; a.v_resid = k->v_resid; a.n_quant = k->n_quant; a.n_resid = k->n_resid;
+    a.k_resid = k->k_resid; a.v_resid = k->v_resid;
+    a.n_tok = k->n_tok; a.n_quant_k = k->n_quant_k; a.n_quant_v = k->n_quant_v;
     a.q = q; a.out = out; a.out_fp32 = (out_dtype == KVQ_OUT_FP32);
-    const int total = p.n_split + (c->residual > 0 ? 1 : 0);  // blocks per (request, head)
     if (total > 1) {
       a.part = static_cast<float*>(ws);
       a.counters = reinterpret_cast<int*>(static_cast<char*>(ws) +
-                                          align256((size_t)B * c->n_heads * total * (kvq::kD + 2) * sizeof(float)));
+                                          align256((size_t)B * c->n_q_heads * total * (kvq::kD + 2) * sizeof(float)));
     }
     a.err = device_error_ptr();
-    a.B = B; a.H = c->n_heads; a.max_tokens = c->max_tokens; a.residual = c->residual; a.group = c->group;
+    a.B = B; a.H = c->n_heads; a.Hq = c->n_q_heads; a.k_bits = c->k_bits; a.v_bits = c->v_bits;
+    a.max_tokens = c->max_tokens; a.residual = c->residual; a.group = c->group;
     a.n_split = p.n_split; a.tok_per_split = p.tps;
     return cuda_status(kvq::launch_kivi_attn(a, s), __func__);
   }

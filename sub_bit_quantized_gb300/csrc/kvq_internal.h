@@ -110,22 +110,45 @@ struct KiviQuantArgs {
   const uint16_t* x;               // fp16 (b, h, j, ch)
   int64_t sb, sh;
   uint8_t* codes; uint16_t* scale; uint16_t* zero;
-  int axis, B, H, n_tok, tok_begin, max_tokens, group;
+  int axis, bits, B, H, n_tok, tok_begin, max_tokens, group;
 };
 cudaError_t launch_kivi_quantize(const KiviQuantArgs& a, cudaStream_t s);
+
+// prefill tail: copy tokens [nq, n_tok) to the residuals and set the lengths
+struct KiviTailArgs {
+  const uint16_t* k; const uint16_t* v;  // fp16 (b, h, j, ch), b relative to b0
+  int64_t sb, sh;
+  uint16_t* k_resid; uint16_t* v_resid;
+  int32_t* n_tok; int32_t* n_quant_k; int32_t* n_quant_v;
+  int b0, B, H, n_tok_new, nq, residual;
+};
+cudaError_t launch_kivi_prefill_tail(const KiviTailArgs& a, cudaStream_t s);
+
+struct KiviAppendArgs {
+  const uint16_t* k_new; const uint16_t* v_new;  // fp16 [n_seq][H][D]
+  uint8_t* k_codes; uint16_t* k_scale; uint16_t* k_zero;
+  uint8_t* v_codes; uint16_t* v_scale; uint16_t* v_zero;
+  uint16_t* k_resid; uint16_t* v_resid;
+  int32_t* n_tok; int32_t* n_quant_k; int32_t* n_quant_v; int32_t* sync;
+  int* err;
+  int n_seq, H, k_bits, v_bits, residual, max_tokens;
+};
+cudaError_t launch_kivi_append(const KiviAppendArgs& a, cudaStream_t s);
 
 struct KiviAttnArgs {
   const uint8_t* k_codes; const uint16_t* k_scale; const uint16_t* k_zero;
   const uint8_t* v_codes; const uint16_t* v_scale; const uint16_t* v_zero;
   const uint16_t* k_resid; const uint16_t* v_resid;
-  const int32_t* n_quant; const int32_t* n_resid;
-  const uint16_t* q;
+  const int32_t* n_tok; const int32_t* n_quant_k; const int32_t* n_quant_v;
+  const uint16_t* q;               // bf16 [B][Hq][D]
   void* out; int out_fp32;
   float* part; int* counters; int* err;
-  int B, H, max_tokens, residual, group;
+  int B, H, Hq, k_bits, v_bits, max_tokens, residual, group;
   int n_split, tok_per_split;
 };
-size_t kivi_attn_smem_bytes(int tok_per_split, int residual);
+// query heads one attention block serves (a divisor of Hq / H, at most 4)
+int kivi_heads_per_block(int rep);
+size_t kivi_attn_smem_bytes(int k_bits, int v_bits, int heads_per_block, int residual);
 int kivi_attn_max_tok_per_split(int residual);
 cudaError_t launch_kivi_attn(const KiviAttnArgs& a, cudaStream_t s);
 

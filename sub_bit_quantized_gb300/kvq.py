@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(HERE, "libkvq.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "kvq.h")
 
 KVQ_OK = 0
+ERR_INVALID_ARG, ERR_CAPACITY, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT = 1, 2, 3, 4, 5, 6
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_CAPACITY", 3: "KVQ_ERR_UNSUPPORTED",
           4: "KVQ_ERR_CUDA", 5: "KVQ_ERR_WORKSPACE", 6: "KVQ_ERR_TIMEOUT"}
 FMT_LOOPVQ, FMT_KIVI = 0, 1
@@ -50,15 +51,17 @@ class VqSizes(ctypes.Structure):
 
 
 class KiviCfg(ctypes.Structure):
-    _fields_ = [("D", ctypes.c_int), ("n_heads", ctypes.c_int), ("bits", ctypes.c_int),
-                ("group", ctypes.c_int), ("residual", ctypes.c_int), ("max_batch", ctypes.c_int),
-                ("max_tokens", ctypes.c_int)]
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("D", "n_heads", "n_q_heads", "k_bits", "v_bits", "group", "residual", "max_batch",
+                 "max_tokens")]
+
+
+KIVI_CACHE_FIELDS = ("k_codes", "k_scale", "k_zero", "v_codes", "v_scale", "v_zero",
+                     "k_resid", "v_resid", "n_tok", "n_quant_k", "n_quant_v", "sync")
 
 
 class KiviCacheC(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in
-                ("k_codes", "k_scale", "k_zero", "v_codes", "v_scale", "v_zero",
-                 "k_resid", "v_resid", "n_quant", "n_resid")]
+    _fields_ = [(n, ctypes.c_void_p) for n in KIVI_CACHE_FIELDS]
 
 
 _P = ctypes.c_void_p
@@ -78,6 +81,8 @@ _SIGS = {
     "kvq_prefill_vq": (_I, [_P, _P, _I, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _P]),
     "kvq_append_page": (_I, [_P, _P, _I, _I, _P, _P, _I, _P]),
     "kvq_quantize_kivi": (_I, [_P, _I, _P, _I64, _I64, _I, _I, _P, _P, _P, _I, _P]),
+    "kvq_kivi_prefill": (_I, [_P, _P, _P, _P, _I64, _I64, _I, _I, _I, _P]),
+    "kvq_kivi_append": (_I, [_P, _P, _P, _P, _I, _P]),
     "kvq_decode_attn": (_I, [_I, _P, _P, _I, _I, _P, _I, _P, _I, _I, _P, _SZ, _P]),
     "kvq_decode_attn_noalloc": (_I, [_I, _P, _P, _I, _I, _P, _I, _P, _I, _I, _P]),
     "kvq_decode_workspace_size": (_SZ, [_I, _P, _I, _I]),
@@ -300,40 +305,49 @@ def kvq_append_page(cfg: VqConfig, cache: VqCache, layer: int, loop_step: int, k
 
 @dataclass
 class KiviConfig:
+    """kvq_kivi_cfg. n_q_heads defaults to n_heads (multi-head attention)."""
     D: int = 128
     n_heads: int = 1
-    bits: int = 2
+    n_q_heads: int | None = None
+    k_bits: int = 2
+    v_bits: int = 2
     group: int = 32
     residual: int = 128
     max_batch: int = 1
     max_tokens: int = 0
 
+    @property
+    def q_heads(self) -> int:
+        return self.n_heads if self.n_q_heads is None else self.n_q_heads
+
     def to_c(self) -> KiviCfg:
-        return KiviCfg(self.D, self.n_heads, self.bits, self.group, self.residual, self.max_batch,
-                       self.max_tokens)
+        return KiviCfg(self.D, self.n_heads, self.q_heads, self.k_bits, self.v_bits, self.group,
+                       self.residual, self.max_batch, self.max_tokens)
 
 
 class KiviCache:
+    """Device buffers of a KIVI cache (layouts of kvq_kivi_cache), zero-filled."""
+
     def __init__(self, cfg: KiviConfig, device="cuda"):
         self.cfg = cfg
         c = cfg
         dev = torch.device(device)
         B, H, N, D, Gq = c.max_batch, c.n_heads, c.max_tokens, c.D, c.group
-        self.k_codes = torch.zeros((B, H, N, D // 4), dtype=torch.uint8, device=dev)
-        self.v_codes = torch.zeros_like(self.k_codes)
+        self.k_codes = torch.zeros((B, H, N, D * c.k_bits // 8), dtype=torch.uint8, device=dev)
+        self.v_codes = torch.zeros((B, H, N, D * c.v_bits // 8), dtype=torch.uint8, device=dev)
         self.k_scale = torch.zeros((B, H, N // Gq, D), dtype=torch.float16, device=dev)
         self.k_zero = torch.zeros_like(self.k_scale)
         self.v_scale = torch.zeros((B, H, N, D // Gq), dtype=torch.float16, device=dev)
         self.v_zero = torch.zeros_like(self.v_scale)
         self.k_resid = torch.zeros((B, H, max(c.residual, 1), D), dtype=torch.float16, device=dev)
         self.v_resid = torch.zeros_like(self.k_resid)
-        self.n_quant = torch.zeros(B, dtype=torch.int32, device=dev)
-        self.n_resid = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.n_tok = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.n_quant_k = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.n_quant_v = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.sync = torch.zeros(B, dtype=torch.int32, device=dev)
 
     def c_struct(self) -> KiviCacheC:
-        return KiviCacheC(*[_ptr(getattr(self, n)) for n in
-                            ("k_codes", "k_scale", "k_zero", "v_codes", "v_scale", "v_zero",
-                             "k_resid", "v_resid", "n_quant", "n_resid")])
+        return KiviCacheC(*[_ptr(getattr(self, n)) for n in KIVI_CACHE_FIELDS])
 
 
 def kvq_quantize_kivi(cfg: KiviConfig, axis: int, x, codes, scale, zero, tok_begin=0, stream=None):
@@ -344,6 +358,29 @@ def kvq_quantize_kivi(cfg: KiviConfig, axis: int, x, codes, scale, zero, tok_beg
     _check(lib().kvq_quantize_kivi(ctypes.byref(c), axis, _ptr(x), H * n * D, n * D, B, n, _ptr(codes),
                                    _ptr(scale), _ptr(zero), tok_begin, _stream(stream)),
            "kvq_quantize_kivi")
+
+
+def kvq_kivi_prefill(cfg: KiviConfig, cache: KiviCache, k, v, b0: int = 0, stream=None):
+    """k, v: fp16 [B][H][n_tok][D] (same strides) for requests b0 .. b0+B-1."""
+    _bits(k, (torch.float16,))
+    _bits(v, (torch.float16,))
+    if k.shape != v.shape or k.stride() != v.stride() or k.stride(3) != 1 or k.stride(2) != k.shape[3]:
+        raise ValueError("k and v need one shape and rows of D contiguous channels")
+    B, H, n, D = k.shape
+    c = cfg.to_c()
+    kc = cache.c_struct()
+    _check(lib().kvq_kivi_prefill(ctypes.byref(c), ctypes.byref(kc), _ptr(k), _ptr(v), k.stride(0), k.stride(1),
+                                  b0, B, n, _stream(stream)), "kvq_kivi_prefill")
+
+
+def kvq_kivi_append(cfg: KiviConfig, cache: KiviCache, k_new, v_new, stream=None):
+    """k_new, v_new: fp16 [n_seq][H][D], contiguous."""
+    _bits(k_new, (torch.float16,))
+    _bits(v_new, (torch.float16,))
+    c = cfg.to_c()
+    kc = cache.c_struct()
+    _check(lib().kvq_kivi_append(ctypes.byref(c), ctypes.byref(kc), _ptr(k_new), _ptr(v_new), k_new.shape[0],
+                                 _stream(stream)), "kvq_kivi_append")
 
 
 # ------------------------------------------------------------------------------------------

@@ -127,53 +127,75 @@ def check_close(got: np.ndarray, ref: np.ndarray, max_abs=2e-3, rel_l2=1e-3):
 @dataclass
 class KiviCase:
     cfg: kvq.KiviConfig
-    n_quant: list
-    n_resid: list
+    n_tok: list
+    n_quant_k: list
+    n_quant_v: list
     k_codes: np.ndarray   # [B][H][N][D] int
     k_scale: np.ndarray   # [B][H][N/32][D] fp16
     k_zero: np.ndarray
     v_codes: np.ndarray
     v_scale: np.ndarray   # [B][H][N][D/32]
     v_zero: np.ndarray
-    k_resid: np.ndarray   # [B][H][R][D] fp16
-    v_resid: np.ndarray
-    q: np.ndarray         # [B][H][D] bf16 values
+    k_res: np.ndarray     # [B][H][R][D] fp16: row i is token n_quant_k + i
+    v_res: np.ndarray     # [B][H][R][D] fp16: row i is token n_quant_v + i
+    q: np.ndarray         # [B][Hq][D] bf16 values
 
 
-def make_kivi_case(seed, B, H, n_quant, n_resid, max_tokens=None, residual=128) -> KiviCase:
-    """Random codes and fp16 scales / zero-points of the shapes KIVI stores (attention-only)."""
+def make_kivi_case(seed, B, H, n_quant, n_resid, max_tokens=None, residual=128, Hq=None, k_bits=2, v_bits=2,
+                   n_quant_v=None) -> KiviCase:
+    """Random codes and fp16 scales / zero-points of the shapes KIVI stores (attention-only).
+
+    Request b holds n_quant[b] quantized keys and n_resid[b] fp16 keys; its values are
+    quantized for tokens below n_quant_v[b] (default n_quant[b]) and fp16 above."""
     g = synth.rng(seed)
     N = max_tokens or max(max(n_quant), 32)
-    cfg = kvq.KiviConfig(n_heads=H, residual=residual, max_batch=B, max_tokens=N)
-    kc = g.integers(0, 4, size=(B, H, N, D), dtype=np.uint8)
-    vc = g.integers(0, 4, size=(B, H, N, D), dtype=np.uint8)
-    ks = np.abs(synth.gaussian(g, (B, H, N // 32, D), 0.7)).astype(np.float16) + np.float16(0.05)
+    Hq = Hq or H
+    cfg = kvq.KiviConfig(n_heads=H, n_q_heads=Hq, k_bits=k_bits, v_bits=v_bits, residual=residual,
+                         max_batch=B, max_tokens=N)
+    kc = g.integers(0, 2 ** k_bits, size=(B, H, N, D), dtype=np.uint8)
+    vc = g.integers(0, 2 ** v_bits, size=(B, H, N, D), dtype=np.uint8)
+    # scales shrink with more levels so dequantized values keep the same range
+    ks = (np.abs(synth.gaussian(g, (B, H, N // 32, D), 0.7)) * 3 / (2 ** k_bits - 1)).astype(np.float16)
+    ks += np.float16(0.05)
     outl = synth.outlier_channels(g, D, 6)
     ks[..., outl] *= np.float16(20)
-    kz = np.asarray(synth.gaussian(g, (B, H, N // 32, D), 1.5), np.float16)
-    vs = (np.abs(synth.gaussian(g, (B, H, N, D // 32), 0.7)) + 0.05).astype(np.float16)
-    vz = np.asarray(synth.gaussian(g, (B, H, N, D // 32), 1.5), np.float16)
-    kr, vr = synth.kivi_kv(g, B * H * residual, D, outl)
-    kr = kr.reshape(B, H, residual, D).astype(np.float16)
-    vr = vr.reshape(B, H, residual, D).astype(np.float16)
-    q = synth.bf16_round(synth.gaussian(g, (B, H, D)))
-    return KiviCase(cfg, list(n_quant), list(n_resid), kc, ks, kz, vc, vs, vz, kr, vr, q)
+    kz = np.asarray(synth.gaussian(g, (B, H, N // 32, D), 1.5) * (2 ** k_bits - 1) / 3, np.float16)
+    vs = ((np.abs(synth.gaussian(g, (B, H, N, D // 32), 0.7)) + 0.05) * 3 / (2 ** v_bits - 1)).astype(np.float16)
+    vz = np.asarray(synth.gaussian(g, (B, H, N, D // 32), 1.5) * (2 ** v_bits - 1) / 3, np.float16)
+    R = max(residual, 1)
+    kr, vr = synth.kivi_kv(g, B * H * R, D, outl)
+    kr = kr.reshape(B, H, R, D).astype(np.float16)
+    vr = vr.reshape(B, H, R, D).astype(np.float16)
+    q = synth.bf16_round(synth.gaussian(g, (B, Hq, D)))
+    nqv = list(n_quant) if n_quant_v is None else list(n_quant_v)
+    n_tok = [a + r for a, r in zip(n_quant, n_resid)]
+    return KiviCase(cfg, n_tok, list(n_quant), nqv, kc, ks, kz, vc, vs, vz, kr, vr, q)
 
 
 def fill_kivi_cache(case: KiviCase) -> kvq.KiviCache:
-    cache = kvq.KiviCache(case.cfg)
-    cache.k_codes.copy_(torch.from_numpy(_layout.pack_codes(case.k_codes)))
-    cache.v_codes.copy_(torch.from_numpy(_layout.pack_codes(case.v_codes)))
-    for name in ("k_scale", "k_zero", "v_scale", "v_zero", "k_resid", "v_resid"):
+    cfg = case.cfg
+    cache = kvq.KiviCache(cfg)
+    cache.k_codes.copy_(torch.from_numpy(_layout.pack_codes(case.k_codes, cfg.k_bits)))
+    cache.v_codes.copy_(torch.from_numpy(_layout.pack_codes(case.v_codes, cfg.v_bits)))
+    for name in ("k_scale", "k_zero", "v_scale", "v_zero"):
         getattr(cache, name).copy_(fp16_tensor(getattr(case, name)))
-    cache.n_quant.copy_(torch.tensor(case.n_quant, dtype=torch.int32))
-    cache.n_resid.copy_(torch.tensor(case.n_resid, dtype=torch.int32))
+    cache.k_resid.copy_(fp16_tensor(case.k_res))
+    if cfg.residual > 0:   # value of token t at ring row t % R
+        vr = np.zeros_like(case.v_res)
+        for b, (n, nqv) in enumerate(zip(case.n_tok, case.n_quant_v)):
+            for i in range(n - nqv):
+                vr[b, :, (nqv + i) % cfg.residual] = case.v_res[b, :, i]
+        cache.v_resid.copy_(fp16_tensor(vr))
+    cache.n_tok.copy_(torch.tensor(case.n_tok, dtype=torch.int32))
+    cache.n_quant_k.copy_(torch.tensor(case.n_quant_k, dtype=torch.int32))
+    cache.n_quant_v.copy_(torch.tensor(case.n_quant_v, dtype=torch.int32))
     return cache
 
 
-def oracle_kivi(case: KiviCase, b: int, h: int) -> np.ndarray:
-    nq, nr = case.n_quant[b], case.n_resid[b]
-    return okivi.decode_attention(case.q[b, h], case.k_codes[b, h, :nq], case.k_scale[b, h, :nq // 32],
-                                  case.k_zero[b, h, :nq // 32], case.v_codes[b, h, :nq],
-                                  case.v_scale[b, h, :nq], case.v_zero[b, h, :nq],
-                                  case.k_resid[b, h, :nr], case.v_resid[b, h, :nr])
+def oracle_kivi(case: KiviCase, b: int, hq: int) -> np.ndarray:
+    hk = okivi.kv_head(hq, case.cfg.q_heads, case.cfg.n_heads)
+    n, nqk, nqv = case.n_tok[b], case.n_quant_k[b], case.n_quant_v[b]
+    return okivi.decode_attention(case.q[b, hq], case.k_codes[b, hk, :nqk], case.k_scale[b, hk, :nqk // 32],
+                                  case.k_zero[b, hk, :nqk // 32], case.v_codes[b, hk, :nqv],
+                                  case.v_scale[b, hk, :nqv], case.v_zero[b, hk, :nqv],
+                                  case.k_res[b, hk, :n - nqk], case.v_res[b, hk, :n - nqv])

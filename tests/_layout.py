@@ -47,15 +47,20 @@ def window_slot(p: int, sink: int = 8, recent: int = 64) -> int:
     return p if p < sink else sink + (p - sink) % (recent + PAGE)
 
 
-def pack_codes(codes: np.ndarray) -> np.ndarray:
-    """2-bit codes [..., D] -> bytes [..., D/4], channel 4k+i in bits [2i, 2i+2)."""
+def pack_codes(codes: np.ndarray, bits: int = 2) -> np.ndarray:
+    """b-bit codes [..., D] -> bytes [..., D*b/8]: channel (8/b)k + i in bits [b i, b i + b) of byte k."""
     c = np.asarray(codes, dtype=np.uint8)
     *lead, D = c.shape
-    c = c.reshape(*lead, D // 4, 4)
-    return (c[..., 0] | (c[..., 1] << 2) | (c[..., 2] << 4) | (c[..., 3] << 6)).astype(np.uint8)
+    per = 8 // bits
+    c = c.reshape(*lead, D // per, per)
+    out = np.zeros((*lead, D // per), dtype=np.uint8)
+    for i in range(per):
+        out |= (c[..., i] << (bits * i)).astype(np.uint8)
+    return out
 
 
-def unpack_codes(b: np.ndarray) -> np.ndarray:
+def unpack_codes(b: np.ndarray, bits: int = 2) -> np.ndarray:
     b = np.asarray(b, dtype=np.uint8)
-    out = np.stack([(b >> (2 * i)) & 3 for i in range(4)], axis=-1)
-    return out.reshape(*b.shape[:-1], b.shape[-1] * 4)
+    per = 8 // bits
+    out = np.stack([(b >> (bits * i)) & ((1 << bits) - 1) for i in range(per)], axis=-1)
+    return out.reshape(*b.shape[:-1], b.shape[-1] * per)

@@ -138,8 +138,24 @@ def test_kivi_argument_checks(L):
     assert f(B(k), 0, FAKE, 0, 0, 16, 31, FAKE, FAKE, FAKE, 0, None) == 1   # keys need 32-token groups
     assert f(B(k), 0, FAKE, 0, 0, 16, 64, FAKE, FAKE, FAKE, 3936, None) == 2  # past capacity
     assert f(B(k), 2, FAKE, 0, 0, 16, 64, FAKE, FAKE, FAKE, 0, None) == 1   # axis
-    k4 = kvq.KiviConfig(bits=4, max_tokens=64).to_c()
-    assert f(B(k4), 1, FAKE, 0, 0, 1, 1, FAKE, FAKE, FAKE, 0, None) == 3    # 4-bit not built
+    k3 = kvq.KiviConfig(k_bits=3, max_tokens=64).to_c()
+    assert f(B(k3), 1, FAKE, 0, 0, 1, 1, FAKE, FAKE, FAKE, 0, None) == 3    # 3-bit not built
+    kq = kvq.KiviConfig(n_heads=8, n_q_heads=12, max_tokens=64).to_c()
+    assert f(B(kq), 1, FAKE, 0, 0, 1, 1, FAKE, FAKE, FAKE, 0, None) == 1    # GQA ratio not whole
+    kr = kvq.KiviConfig(residual=100, max_tokens=64).to_c()
+    assert f(B(kr), 1, FAKE, 0, 0, 1, 1, FAKE, FAKE, FAKE, 0, None) == 1    # R not a multiple of 32
+    kc = kvq.KiviCacheC(*([FAKE] * len(kvq.KIVI_CACHE_FIELDS)))
+    p = L.kvq_kivi_prefill
+    assert p(B(k), B(kc), FAKE, FAKE, 0, 0, 15, 2, 64, None) == 2            # b0 + B > max_batch
+    assert p(B(k), B(kc), FAKE, FAKE, 0, 0, 0, 1, 3968 + 129, None) == 2     # quantized part too long
+    assert p(B(k), B(kc), FAKE, FAKE, 0, 0, 0, 1, -1, None) == 1
+    bad = kvq.KiviCacheC(*([FAKE] * (len(kvq.KIVI_CACHE_FIELDS) - 1) + [None]))
+    assert p(B(k), B(bad), FAKE, FAKE, 0, 0, 0, 1, 64, None) == 1            # null length array
+    k0 = kvq.KiviConfig(residual=0, max_tokens=64).to_c()
+    a = L.kvq_kivi_append
+    assert a(B(k0), B(kc), FAKE, FAKE, 1, None) == 1                         # streaming needs R > 0
+    assert a(B(k), B(kc), FAKE, FAKE, 17, None) == 2                         # n_seq > max_batch
+    assert a(B(k), B(kc), FAKE, FAKE, 0, None) == 0                          # nothing to do
 
 
 def test_library_missing_fails_loudly(monkeypatch):
@@ -165,3 +181,7 @@ def test_code_packing_round_trip():
     b = _layout.pack_codes(codes)
     assert b.shape == (7, 32) and np.array_equal(_layout.unpack_codes(b), codes)
     assert b[0, 0] == codes[0, 0] | (codes[0, 1] << 2) | (codes[0, 2] << 4) | (codes[0, 3] << 6)
+    c4 = g.integers(0, 16, size=(7, 128))
+    b4 = _layout.pack_codes(c4, 4)
+    assert b4.shape == (7, 64) and np.array_equal(_layout.unpack_codes(b4, 4), c4)
+    assert b4[2, 5] == c4[2, 10] | (c4[2, 11] << 4)

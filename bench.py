@@ -38,6 +38,15 @@ WORKLOADS = {
                           rho=(0.69, 0.94), n_splits=0,
                           name="LoopVQ 0.5-bit serving decode, Ouro-1.4B-shaped: 24 layers x 4 loop steps, "
                                "16 heads, D=128, Tc=2, G=16, batch 64, context 6144"),
+    "loopvq_b64_6k_tc1": dict(kind="loopvq", B=64, H=16, L=6144, layers=24, T=4, Tc=1, G=16, recent=64,
+                              rho=(0.69, 0.94), n_splits=0,
+                              name="LoopVQ 0.5-bit serving decode without loop coupling (Tc=1, c=16: per-step "
+                                   "codewords), Ouro-1.4B-shaped: 24 layers x 4 loop steps, 16 heads, batch 64, "
+                                   "context 6144"),
+    "loopvq_b64_6k_tc4": dict(kind="loopvq", B=64, H=16, L=6144, layers=24, T=4, Tc=4, G=16, recent=64,
+                              rho=(0.69, 0.94), n_splits=0,
+                              name="LoopVQ 0.5-bit serving decode, one index for all 4 loop steps (Tc=4, c=4), "
+                                   "Ouro-1.4B-shaped: 24 layers x 4 loop steps, 16 heads, batch 64, context 6144"),
     "loopvq_b8_32k": dict(kind="loopvq", B=8, H=16, L=32768, layers=1, T=4, Tc=4, G=32, recent=256,
                           rho=(0.85, 0.85), n_splits=0,
                           name="LoopVQ 0.25-bit long-context decode: 16 heads, D=128, Tc=4, G=32, batch 8, "
@@ -216,12 +225,17 @@ def cpu_oracle(wl, bytes_per_unit, unit_pairs_total, n_pairs, pool=None):
 
 # ------------------------------------------------------------------------------ GPU legs
 
-def vq_call_bytes(B, H, n_pages, n_win, NB_unused=None):
+def vq_ng(wl):
+    """Index groups per token: D / c with c = G / Tc channels per codeword."""
+    return D // (wl["G"] // wl["Tc"])
+
+
+def vq_call_bytes(B, H, n_pages, n_win, NG=16):
     """Algorithmic bytes of one LoopVQ decode-attention call (one layer, one loop step):
-    K and V index pages, bf16 window K and V, the fp32 key and fp16 value codebook slices,
-    the cos/sin rows the call needs (one per page start and per window token), query and
-    bf16 output."""
-    idx = B * H * n_pages * 128 * 2
+    K and V index pages (8 NG bytes each), bf16 window K and V, the fp32 key and fp16 value
+    codebook slices, the cos/sin rows the call needs (one per page start and per window
+    token), query and bf16 output."""
+    idx = B * H * n_pages * 8 * NG * 2
     win = B * H * n_win * D * 2 * 2
     bt = H * 256 * D * (4 + 2)
     rope = (n_pages + n_win) * (D // 2) * 4 * 2
@@ -323,16 +337,17 @@ def kivi_wl_bytes(wl):
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch from an ncu capture,
 # valid only for the kernel source it was taken on (profiles/ holds the capture summary)
 PROFILED_TRAFFIC = {
-    "vq_pages_kernel+vq_window_kernel": ("sub_bit_quantized_gb300/csrc/vq_attn.cu",
+    "loopvq_b64_6k:vq_pages_kernel+vq_window_kernel": ("sub_bit_quantized_gb300/csrc/vq_attn.cu",
                                          "2957b85af7697c08d1211f09aae0e4e37f0d28646c882d637e7a7e317753516e",
                                          210055424 + 43537664),
 }
 
 
-def profiled_traffic(kernel):
-    """Per-launch DRAM bytes of ``kernel`` if its source is unchanged since the capture, else None."""
+def profiled_traffic(workload, kernel):
+    """Per-launch DRAM bytes of ``kernel`` on ``workload`` if its source is unchanged since the
+    capture, else None."""
     import hashlib
-    entry = PROFILED_TRAFFIC.get(kernel)
+    entry = PROFILED_TRAFFIC.get(f"{workload}:{kernel}")
     if entry is None:
         return None
     path, digest, nbytes = entry
@@ -397,7 +412,7 @@ def run_ours(args, wl, rank, world, dist, pool):
             cfg, cache, n_pages, n_win = setup_loopvq(wl, dev, 1234 + rank)
             B, H, NL, T = wl["B"], wl["H"], wl["layers"], wl["T"]
             calls = [(l, t) for t in range(1, T + 1) for l in range(NL)]
-            call_bytes = vq_call_bytes(B, H, n_pages, n_win)
+            call_bytes = vq_call_bytes(B, H, n_pages, n_win, vq_ng(wl))
             caches = None
         else:
             cfg, caches = setup_kivi(wl, dev, 1234 + rank)
@@ -456,7 +471,7 @@ def run_ours(args, wl, rank, world, dist, pool):
                            tokens_per_s=round(B * world / (ms_step * 1e-3), 1), e2e=e2e, clocks=clocks,
                            roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                                     "traffic": profiled_traffic(kernel_name),
+                                     "traffic": profiled_traffic(args.workload, kernel_name),
                                      "peak_source": peak_src,
                                      "kernel": kernel_name,
                                      "bytes_per_launch": call_bytes},
@@ -655,7 +670,7 @@ def run_reference(args, wl, pool):
     """The CPU oracle as the reference arm: each step is a bounded sample of the workload."""
     if wl["kind"] == "loopvq":
         n_pages = max(0, (wl["L"] - 8 - wl["recent"]) // 8)
-        call_bytes = vq_call_bytes(wl["B"], wl["H"], n_pages, wl["L"] - 8 * n_pages)
+        call_bytes = vq_call_bytes(wl["B"], wl["H"], n_pages, wl["L"] - 8 * n_pages, vq_ng(wl))
         units = wl["B"] * wl["H"]
     elif wl["kind"] == "kivi":
         call_bytes = kivi_wl_bytes(wl)

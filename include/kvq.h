@@ -29,8 +29,10 @@
  *   - Device-side waits (the TMA completion barrier) are bounded; a timed-out wait sets a
  *     device error word that kvq_device_error() reads after the stream has drained.
  *   - Loop steps are 1-based (t = 1..T) as on the LoopVQ page; layers and heads 0-based.
- *   - Head dimension D = 128 and page size 8; c = G/Tc must be 8 (so that D/c = 16
- *     index groups per token) in this version; other shapes return KVQ_ERR_UNSUPPORTED.
+ *   - Head dimension D = 128 and page size 8. LoopVQ shapes built: c = G/Tc = 8 with
+ *     Tc = 1, 2, 4 (G = 8, 16, 32: 1, 0.5, 0.25 bit), and at G = 16 (0.5 bit) also Tc = 1
+ *     (c = 16, codewords of one loop step) and Tc = 4 (c = 4, one index for four steps);
+ *     other shapes return KVQ_ERR_UNSUPPORTED.
  */
 #ifndef KVQ_H
 #define KVQ_H

@@ -75,9 +75,13 @@ kvq_status check_vq_cfg(const kvq_vq_cfg* c, const char* fn) {
   const int cc = c->G / c->Tc;
   if (c->D % cc != 0) return fail(KVQ_ERR_INVALID_ARG, "%s: c=G/Tc=%d must divide D=%d", fn, cc, c->D);
   if (c->D != kvq::kD) return fail(KVQ_ERR_UNSUPPORTED, "%s: D=%d (this build supports 128)", fn, c->D);
-  if (cc != kvq::kC) return fail(KVQ_ERR_UNSUPPORTED, "%s: c=G/Tc=%d (this build supports 8)", fn, cc);
-  if (c->Tc != 1 && c->Tc != 2 && c->Tc != 4)
-    return fail(KVQ_ERR_UNSUPPORTED, "%s: Tc=%d (this build supports 1, 2, 4)", fn, c->Tc);
+  // (Tc, c): c = 8 at Tc = 1, 2, 4 (G = 8, 16, 32); at G = 16 also Tc = 1 (c = 16, the
+  // per-step special case) and Tc = 4 (c = 4)
+  const bool built = (cc == 8 && (c->Tc == 1 || c->Tc == 2 || c->Tc == 4)) || (cc == 16 && c->Tc == 1) ||
+                     (cc == 4 && c->Tc == 4);
+  if (!built)
+    return fail(KVQ_ERR_UNSUPPORTED, "%s: Tc=%d with c=G/Tc=%d (this build: c=8 with Tc=1,2,4; c=16 with Tc=1; "
+                "c=4 with Tc=4)", fn, c->Tc, cc);
   if (c->K != kvq::kCB) return fail(KVQ_ERR_UNSUPPORTED, "%s: K=%d (8-bit indices need 256)", fn, c->K);
   return KVQ_OK;
 }
@@ -531,7 +535,7 @@ KVQ_API kvq_status kvq_decode_attn(int format, const void* cfg, const void* cach
     a.q = q; a.out = out; a.out_fp32 = (out_dtype == KVQ_OUT_FP32);
     a.err = device_error_ptr();
     a.B = B; a.H = c->n_heads; a.max_pages = c->max_pages; a.max_ctx = c->max_ctx; a.sink = c->sink;
-    a.recent = c->recent; a.win_slots = win_slots(c); a.G = blocks;
+    a.recent = c->recent; a.win_slots = win_slots(c); a.G = blocks; a.NG = NG;
     return cuda_status(kvq::launch_vq_attn(a, ws, s), __func__);
   }
   if (format == KVQ_FMT_KIVI) {

@@ -12,10 +12,16 @@ void set_last_error(const char* msg);
 
 constexpr int kD = 128;        // head dimension
 constexpr int kPage = 8;       // tokens per index page
-constexpr int kNG = 16;        // index groups per token (c = 8)
-constexpr int kC = 8;          // channels per group
 constexpr int kCB = 256;       // codebook entries
-constexpr int kPageBytes = kPage * kNG;
+
+// In-page byte of (group g, token j) for NG index groups per token (pages of 8 NG bytes):
+// byte (p * 8 + j) * 2 + h holds group p + h NG/2, so the two groups whose channels are RoPE
+// partners (channel ch and ch + 64) sit side by side and a lane reads its 8 tokens' pairs as
+// one 16-byte row.
+__host__ __device__ inline size_t page_byte(int g, int j, int NG) {
+  const int half = NG / 2;
+  return (size_t)(((g % half) * kPage + j) * 2 + g / half);
+}
 
 // ---------------------------------------------------------------- LoopVQ decode attention
 // Two launches per call. The page kernel runs G persistent blocks over the work units
@@ -32,7 +38,7 @@ constexpr int kVqWarpsPerReq = kVqThreads / 64; // page-kernel warps per request
 constexpr int kVqPartFloats = 2 * kVqWarpsPerReq * (kD + 2);  // one piece: [request][warp][M, l, o[128]]
 
 struct VqAttnArgs {
-  const uint8_t* idx_k;      // [max_batch][H][max_pages][128] of (layer, block)
+  const uint8_t* idx_k;      // [max_batch][H][max_pages][8 NG] of (layer, block)
   const uint8_t* idx_v;
   const uint16_t* win_k;     // [max_batch][H][win_slots][D] of (layer, step)
   const uint16_t* win_v;
@@ -51,6 +57,7 @@ struct VqAttnArgs {
   int* err;
   int B, H, max_pages, max_ctx, sink, recent, win_slots;
   int G;                     // page-kernel blocks
+  int NG;                    // index groups per token (8, 16 or 32): pages of 8 NG bytes
 };
 size_t vq_attn_ws_bytes(int B, int H, int G);
 int vq_attn_max_pairs();

@@ -53,26 +53,33 @@ namespace {
 constexpr int kThreads = kVqThreads;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = kVqChunk;                          // pages of each request per unit
-constexpr int kStages = 2;
 constexpr int kResync = 64;                               // units between cos/sin table reloads
 constexpr int kJump = kChunk * kPage;                     // positions between a lane-group's pages
 constexpr uint32_t kKSliceBytes = kCB * kD * 4;           // fp32 key codebook slice
 constexpr uint32_t kVSliceBytes = kCB * kD * 2;           // fp16 value codebook slice
-constexpr uint32_t kPart = kChunk * kPageBytes;           // 4 KB: one request's pages of one kind
-constexpr uint32_t kOffHdr = 4 * kPart;                   // unit header within a stage
-constexpr uint32_t kOffQs = kOffHdr + 64;                 // bf16 queries [2][128] within a stage
-constexpr uint32_t kStageBytes = kOffQs + 2 * kD * 2 + 64;  // [K r0|K r1|V r0|V r1|hdr|q r0|q r1]
-
-// shared-memory layout (bytes)
-constexpr int kOffK = 0;
+constexpr int kOffK = 0;                                  // shared-memory layout (bytes)
 constexpr int kOffV = kOffK + kKSliceBytes;
-constexpr int kOffRing = kOffV + kVSliceBytes;
-constexpr int kOffJ = kOffRing + kStages * kStageBytes;   // float4 [4][8 slots]: cos, sin(256 theta)
-constexpr int kOffProd = kOffJ + 8 * 16 * 4;              // producer state (thread 0)
-constexpr int kOffBar = kOffProd + 64;                    // mbarriers + flags
-constexpr int kSmemBytes = kOffBar + 128;
-static_assert(kSmemBytes <= 232448, "shared memory");
-static_assert(kOffBar % 8 == 0 && kOffRing % 128 == 0 && kStageBytes % 128 == 0, "alignment");
+
+// Ring and shared-memory layout for NG index groups per token (c = 128 / NG channels per
+// codeword): a page is 8 NG bytes. NG = 32 (c = 4) keeps a single ring stage so that its
+// 256-byte pages fit beside the two codebook slices; its refill still overlaps the unit's work
+// because every thread copies what it needs from the stage to registers first.
+template <int NG>
+struct PageLay {
+  static constexpr int kPageB = kPage * NG;
+  static constexpr int kStg = (NG == 32) ? 1 : 2;
+  static constexpr uint32_t kPart = kChunk * kPageB;           // one request's pages of one kind
+  static constexpr uint32_t kOffHdr = 4 * kPart;               // unit header within a stage
+  static constexpr uint32_t kOffQs = kOffHdr + 64;             // bf16 queries [2][128] within a stage
+  static constexpr uint32_t kStageBytes = kOffQs + 2 * kD * 2 + 64;  // [K r0|K r1|V r0|V r1|hdr|q r0|q r1]
+  static constexpr int kOffRing = kOffV + kVSliceBytes;
+  static constexpr int kOffJ = kOffRing + kStg * kStageBytes;  // float4 [4][8 slots]: cos, sin(256 theta)
+  static constexpr int kOffProd = kOffJ + 8 * 16 * 4;          // producer state (thread 0)
+  static constexpr int kOffBar = kOffProd + 64;                // mbarriers + flags
+  static constexpr int kSmemBytes = kOffBar + 128;
+  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(kOffBar % 8 == 0 && kOffRing % 128 == 0 && kStageBytes % 128 == 0, "alignment");
+};
 constexpr int kMaxPairs = (int)(kVSliceBytes / 4) - 1;    // unit scan runs in the value-slice area
 
 __device__ __forceinline__ void ldg8_perm(const float* p, int o0, float (&v)[8]) {
@@ -101,6 +108,12 @@ __device__ __forceinline__ void lds8_fp16(const unsigned char* p, float2 (&v)[4]
   v[1] = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
   v[2] = __half22float2(*reinterpret_cast<const __half2*>(&w.z));
   v[3] = __half22float2(*reinterpret_cast<const __half2*>(&w.w));
+}
+// 4 consecutive fp16 values (one 64-bit shared load), natural order
+__device__ __forceinline__ void lds4_fp16(const unsigned char* p, float2& v0, float2& v1) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  v0 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+  v1 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
 }
 // byte offset (index << 8) | lane_byte, the index being byte k of w (lane_byte < 256)
 template <int K>
@@ -318,12 +331,14 @@ __device__ __forceinline__ void walker_next(const VqAttnArgs& a, Walker& P, int 
 
 // Issue the next unit into its ring stage (header, index pages, queries) and step to the one
 // after it.
+template <int NG>
 __device__ void prod_next(const VqAttnArgs& a, ProdState& S, unsigned char* ring, uint64_t* full, long long lo,
                           long long hi, int n_pairs) {
+  using Ly = PageLay<NG>;
   Walker& P = S.cur;
-  const int st = S.issued % kStages;
-  unsigned char* dst = ring + st * kStageBytes;
-  UnitHdr* hd = reinterpret_cast<UnitHdr*>(dst + kOffHdr);
+  const int st = S.issued % Ly::kStg;
+  unsigned char* dst = ring + st * Ly::kStageBytes;
+  UnitHdr* hd = reinterpret_cast<UnitHdr*>(dst + Ly::kOffHdr);
   const long long seg0 = P.i - P.c, seg1 = seg0 + P.nu;
   int flags = 0;
   if (P.i == lo || P.c == 0) flags |= 1;
@@ -343,37 +358,39 @@ __device__ void prod_next(const VqAttnArgs& a, ProdState& S, unsigned char* ring
   const int b0 = 2 * P.pair;
   const bool two = b0 + 1 < a.B;
   // the header stores above are released to the consumers by this arrive
-  mbar_arrive_expect_tx(&full[st], (uint32_t)(n0 + n1) * 2 * kPageBytes + (two ? 2u : 1u) * kD * 2);
-  const size_t off = (size_t)p_first * kPageBytes;
-  const size_t bh0 = ((size_t)b0 * a.H + P.h) * (size_t)a.max_pages * kPageBytes;
+  mbar_arrive_expect_tx(&full[st], (uint32_t)(n0 + n1) * 2 * Ly::kPageB + (two ? 2u : 1u) * kD * 2);
+  const size_t off = (size_t)p_first * Ly::kPageB;
+  const size_t bh0 = ((size_t)b0 * a.H + P.h) * (size_t)a.max_pages * Ly::kPageB;
   if (n0 > 0) {
-    bulk_g2s(dst, a.idx_k + bh0 + off, n0 * kPageBytes, &full[st]);
-    bulk_g2s(dst + 2 * kPart, a.idx_v + bh0 + off, n0 * kPageBytes, &full[st]);
+    bulk_g2s(dst, a.idx_k + bh0 + off, n0 * Ly::kPageB, &full[st]);
+    bulk_g2s(dst + 2 * Ly::kPart, a.idx_v + bh0 + off, n0 * Ly::kPageB, &full[st]);
   }
   if (n1 > 0) {
-    const size_t bh1 = ((size_t)(b0 + 1) * a.H + P.h) * (size_t)a.max_pages * kPageBytes;
-    bulk_g2s(dst + kPart, a.idx_k + bh1 + off, n1 * kPageBytes, &full[st]);
-    bulk_g2s(dst + 3 * kPart, a.idx_v + bh1 + off, n1 * kPageBytes, &full[st]);
+    const size_t bh1 = ((size_t)(b0 + 1) * a.H + P.h) * (size_t)a.max_pages * Ly::kPageB;
+    bulk_g2s(dst + Ly::kPart, a.idx_k + bh1 + off, n1 * Ly::kPageB, &full[st]);
+    bulk_g2s(dst + 3 * Ly::kPart, a.idx_v + bh1 + off, n1 * Ly::kPageB, &full[st]);
   }
-  bulk_g2s(dst + kOffQs, a.q + ((size_t)b0 * a.H + P.h) * kD, kD * 2, &full[st]);
-  if (two) bulk_g2s(dst + kOffQs + kD * 2, a.q + ((size_t)(b0 + 1) * a.H + P.h) * kD, kD * 2, &full[st]);
+  bulk_g2s(dst + Ly::kOffQs, a.q + ((size_t)b0 * a.H + P.h) * kD, kD * 2, &full[st]);
+  if (two) bulk_g2s(dst + Ly::kOffQs + kD * 2, a.q + ((size_t)(b0 + 1) * a.H + P.h) * kD, kD * 2, &full[st]);
   ++S.issued;
   if (P.i + 1 < hi) walker_next(a, P, n_pairs);
   else ++P.i;
 }
 
+template <int NG>
 __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs a, const float scale_log2) {
+  using Ly = PageLay<NG>;
   extern __shared__ __align__(128) unsigned char smem[];
   float* ks = reinterpret_cast<float*>(smem + kOffK);
   __half* vs = reinterpret_cast<__half*>(smem + kOffV);
-  unsigned char* ring = smem + kOffRing;
-  ProdState* ps = reinterpret_cast<ProdState*>(smem + kOffProd);
-  uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  unsigned char* ring = smem + Ly::kOffRing;
+  ProdState* ps = reinterpret_cast<ProdState*>(smem + Ly::kOffProd);
+  uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + Ly::kOffBar);
   uint64_t* full = kbar + 1;
-  uint64_t* bsync = full + kStages;
+  uint64_t* bsync = full + Ly::kStg;
   int* iflags = reinterpret_cast<int*>(bsync + 1);
   volatile int* failed = iflags;
-  int* released = iflags + 1;  // [kStages]: warps done with the stage's current unit
+  int* released = iflags + 1;  // [Ly::kStg]: warps done with the stage's current unit
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, blk = blockIdx.x;
@@ -426,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
   if (tid == 0) {
     mbar_init(kbar, 1);
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < Ly::kStg; ++s) {
       mbar_init(&full[s], 1);
       released[s] = 0;
     }
@@ -460,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
   if (tid < 8 && a.max_ctx > kJump) {
     // cos/sin(kJump theta_i) for slot tid in that slot's half order, stored [chunk][slot] so
     // that the 8 slots of a lane-group read 8 consecutive float4s (no bank conflicts)
-    float4* jt = reinterpret_cast<float4*>(smem + kOffJ);
+    float4* jt = reinterpret_cast<float4*>(smem + Ly::kOffJ);
     const int jo0 = (tid & 4) ? 4 : 0;
     float c8[8], s8[8];
     ldg8_perm(a.rope_cos + (size_t)kJump * (kD / 2) + 8 * tid, jo0, c8);
@@ -472,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
   }
   __syncthreads();  // barriers initialised, scan read by thread 0: the value area is free
   if (tid == 0)
-    for (int s = 0; s < kStages && ps->cur.i < hi; ++s) prod_next(a, *ps, ring, full, lo, hi, n_pairs);
+    for (int s = 0; s < Ly::kStg && ps->cur.i < hi; ++s) prod_next<NG>(a, *ps, ring, full, lo, hi, n_pairs);
 
   const int s = tid & 7;                 // slot: groups s and s + 8
   const int o0 = (s & 4) ? 4 : 0;        // key half order (bank-quad spreading)
@@ -507,44 +524,56 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
   const uint32_t vb0 = 16 * s, vb1 = 128 + 16 * s;
   const unsigned char* ksb = reinterpret_cast<const unsigned char*>(ks);
   const unsigned char* vsb = reinterpret_cast<const unsigned char*>(vs);
-  const float4* jt = reinterpret_cast<const float4*>(smem + kOffJ) + s;
+  const float4* jt = reinterpret_cast<const float4*>(smem + Ly::kOffJ) + s;
 
   const int n_units = (int)(hi - lo);
   int cur_head = -1;
   uint32_t kphase = 0, sphase = 0;
   for (int i = 0; i < n_units; ++i) {
-    const int st = i % kStages;
-    wait_stage(&full[st], (i / kStages) & 1, failed, a.err);
+    const int st = i % Ly::kStg;
+    wait_stage(&full[st], (i / Ly::kStg) & 1, failed, a.err);
     // ---- everything this thread needs from the stage goes to registers, then the stage is
     //      released: its refill overlaps this unit's work
-    const unsigned char* stage = ring + st * kStageBytes;
-    const int4 hv0 = *reinterpret_cast<const int4*>(stage + kOffHdr);
-    const int4 hv1 = *reinterpret_cast<const int4*>(stage + kOffHdr + 16);
+    const unsigned char* stage = ring + st * Ly::kStageBytes;
+    const int4 hv0 = *reinterpret_cast<const int4*>(stage + Ly::kOffHdr);
+    const int4 hv1 = *reinterpret_cast<const int4*>(stage + Ly::kOffHdr + 16);
     const int uh = hv0.x, upair = hv0.y, uc = hv0.z, uflags = hv0.w;
     const int L = r ? hv1.z : hv1.x, NP = r ? hv1.w : hv1.y;
     const int pg = uc * kChunk + po;
     const bool active = !*failed && pg < NP;
     const bool resync = (uflags & 1) || uc % kResync == 0;
-    uint4 rowk = make_uint4(0, 0, 0, 0), rowv = rowk;
+    // the lane's index words: 16 bytes (tokens 0..7 x lo/hi group) of its slot's row; with
+    // c = 4 two slots (groups 2s and 2s + 1 of each half), the key row serving la first
+    uint4 rowk = make_uint4(0, 0, 0, 0), rowv = rowk, rowk2 = rowk, rowv2 = rowk;
     float ql[8], qh[8];
     if (active) {
-      rowk = *reinterpret_cast<const uint4*>(stage + r * kPart + po * kPageBytes + 16 * s);
-      rowv = *reinterpret_cast<const uint4*>(stage + (2 + r) * kPart + po * kPageBytes + 16 * s);
+      const unsigned char* pk = stage + r * Ly::kPart + po * Ly::kPageB;
+      const unsigned char* pv = stage + (2 + r) * Ly::kPart + po * Ly::kPageB;
+      if constexpr (NG == 32) {
+        rowk = *reinterpret_cast<const uint4*>(pk + 32 * s + 4 * o0);
+        rowk2 = *reinterpret_cast<const uint4*>(pk + 32 * s + 16 - 4 * o0);
+        rowv = *reinterpret_cast<const uint4*>(pv + 32 * s);
+        rowv2 = *reinterpret_cast<const uint4*>(pv + 32 * s + 16);
+      } else {
+        constexpr int kSlotShift = (NG == 8) ? 1 : 0;  // c = 16: lanes 2p and 2p + 1 share slot p
+        rowk = *reinterpret_cast<const uint4*>(pk + 16 * (s >> kSlotShift));
+        rowv = *reinterpret_cast<const uint4*>(pv + 16 * (s >> kSlotShift));
+      }
       if (resync) {
-        const uint16_t* qr = reinterpret_cast<const uint16_t*>(stage + kOffQs) + r * kD;
+        const uint16_t* qr = reinterpret_cast<const uint16_t*>(stage + Ly::kOffQs) + r * kD;
         lds8_bf16_perm(qr + 8 * s, o0, ql);
         lds8_bf16_perm(qr + 64 + 8 * s, o0, qh);
       }
     }
     __syncwarp();
     if (lane == 0) {
-      // the last warp done with this stage refills it with the unit kStages ahead: no warp
+      // the last warp done with this stage refills it with the unit Ly::kStg ahead: no warp
       // waits to produce, and the copy starts as soon as the stage is free
       if (atom_add_acq_rel_shared(&released[st], 1) == kWarps - 1) {
         released[st] = 0;
         if (!*failed && ps->cur.i < hi) {
           fence_proxy_async_smem();
-          prod_next(a, *ps, ring, full, lo, hi, n_pairs);
+          prod_next<NG>(a, *ps, ring, full, lo, hi, n_pairs);
         }
       }
     }
@@ -602,13 +631,15 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const uint32_t wd = (j < 2) ? rowk.x : (j < 4) ? rowk.y : (j < 6) ? rowk.z : rowk.w;
+        uint32_t wd2 = wd;  // c = 4: the index of the other 4 channels of each half
+        if constexpr (NG == 32) wd2 = (j < 2) ? rowk2.x : (j < 4) ? rowk2.y : (j < 6) ? rowk2.z : rowk2.w;
         uint32_t al0, al1, ah0, ah1;
         if (j & 1) {
-          al0 = row_off<2>(wd, kb0); al1 = row_off<2>(wd, kb1);
-          ah0 = row_off<3>(wd, kb0); ah1 = row_off<3>(wd, kb1);
+          al0 = row_off<2>(wd, kb0); al1 = row_off<2>(wd2, kb1);
+          ah0 = row_off<3>(wd, kb0); ah1 = row_off<3>(wd2, kb1);
         } else {
-          al0 = row_off<0>(wd, kb0); al1 = row_off<0>(wd, kb1);
-          ah0 = row_off<1>(wd, kb0); ah1 = row_off<1>(wd, kb1);
+          al0 = row_off<0>(wd, kb0); al1 = row_off<0>(wd2, kb1);
+          ah0 = row_off<1>(wd, kb0); ah1 = row_off<1>(wd2, kb1);
         }
         const float4 la = *reinterpret_cast<const float4*>(ksb + al0);
         const float4 lb = *reinterpret_cast<const float4*>(ksb + al1);
@@ -635,8 +666,18 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
         const uint32_t avl = (j & 1) ? row_off<2>(wd, vb0) : row_off<0>(wd, vb0);
         const uint32_t avh = (j & 1) ? row_off<3>(wd, vb1) : row_off<1>(wd, vb1);
         float2 vl[4], vh[4];
-        lds8_fp16(vsb + avl, vl);
-        lds8_fp16(vsb + avh, vh);
+        if constexpr (NG == 32) {  // channels 8s .. 8s + 3 and 8s + 4 .. 8s + 7 from two codewords
+          const uint32_t wd2 = (j < 2) ? rowv2.x : (j < 4) ? rowv2.y : (j < 6) ? rowv2.z : rowv2.w;
+          const uint32_t avl2 = (j & 1) ? row_off<2>(wd2, vb0 + 8) : row_off<0>(wd2, vb0 + 8);
+          const uint32_t avh2 = (j & 1) ? row_off<3>(wd2, vb1 + 8) : row_off<1>(wd2, vb1 + 8);
+          lds4_fp16(vsb + avl, vl[0], vl[1]);
+          lds4_fp16(vsb + avl2, vl[2], vl[3]);
+          lds4_fp16(vsb + avh, vh[0], vh[1]);
+          lds4_fp16(vsb + avh2, vh[2], vh[3]);
+        } else {
+          lds8_fp16(vsb + avl, vl);
+          lds8_fp16(vsb + avh, vh);
+        }
         const float2 p2 = make_float2(pj, pj);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -675,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
   // after a timeout, let the block's own copies in flight land before it exits
   if (tid == 0 && *failed) {
     const int issued = ps->issued;
-    for (int j = max(0, issued - kStages); j < issued; ++j) mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1);
+    for (int j = max(0, issued - Ly::kStg); j < issued; ++j) mbar_wait_bounded(&full[j % Ly::kStg], (j / Ly::kStg) & 1);
     if (ps->k_loads > 0) mbar_wait_bounded(kbar, (ps->k_loads - 1) & 1);
   }
 }
@@ -806,6 +847,15 @@ __global__ void __launch_bounds__(kWThreads) vq_window_kernel(const VqAttnArgs a
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+template <int NG>
+cudaError_t launch_pages(const VqAttnArgs& a, float scale_log2, cudaStream_t st) {
+  using Ly = PageLay<NG>;
+  cudaError_t e = cudaFuncSetAttribute(vq_pages_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  vq_pages_kernel<NG><<<a.G, kThreads, Ly::kSmemBytes, st>>>(a, scale_log2);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t vq_attn_ws_bytes(int B, int H, int G) {
@@ -825,11 +875,15 @@ cudaError_t launch_vq_attn(const VqAttnArgs& args, void* ws, cudaStream_t st) {
   a.part_whole = reinterpret_cast<float*>(w);
   w += align256((size_t)a.H * n_pairs * kVqPartFloats * sizeof(float));
   a.part_slot = reinterpret_cast<float*>(w);
-  cudaError_t e = cudaFuncSetAttribute(vq_pages_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)kD);
-  vq_pages_kernel<<<a.G, kThreads, kSmemBytes, st>>>(a, scale_log2);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  switch (a.NG) {
+    case 16: e = launch_pages<16>(a, scale_log2, st); break;
+    case 8: e = launch_pages<8>(a, scale_log2, st); break;
+    case 32: e = launch_pages<32>(a, scale_log2, st); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
   // programmatic dependent launch: the window kernel may start before the page kernel ends
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)(a.B * a.H));

@@ -73,9 +73,6 @@ __global__ void slice_fp16_kernel(const float* __restrict__ cb, __half* __restri
   }
 }
 
-__device__ __forceinline__ size_t page_byte(int g, int j) {  // in-page byte of (group, token)
-  return (size_t)(((g & 7) * kPage + (j & 7)) * 2 + (g >> 3));
-}
 
 // ---------------------------------------------------------------- prefill window copy
 // One block per (step, sequence, head); copies sink + recent tokens to their slots.
@@ -156,9 +153,9 @@ __device__ __forceinline__ bool roll_due(const int32_t* seq_len, const int32_t* 
 // runner-up lies within the error band of its best (8x the fp32 accumulation bound of the
 // codewords that can compete, plus the 1e-6 tie threshold) is decided on distances summed
 // with error-free fp32 steps, the lowest index winning exact ties.
-template <int TC>
+template <int TC, int C>
 __global__ void __launch_bounds__(256) roll_kernel(const VqRollArgs a) {
-  constexpr int G = TC * kC;
+  constexpr int G = TC * C, kNG = kD / C, kPageBytes = kPage * kNG;
   __shared__ __align__(16) float cbs[kCB * G];
   __shared__ float nh[kCB];
   int q = blockIdx.x;
@@ -202,17 +199,31 @@ __global__ void __launch_bounds__(256) roll_kernel(const VqRollArgs a) {
       const int p = a.sink + kPage * np + j;  // position of the token
       const int slot = a.sink + (p - a.sink) % (a.recent + kPage);
 #pragma unroll
-      for (int m = 0; m < TC; ++m) {
-        uint4 w4 = make_uint4(0, 0, 0, 0);
+      for (int m = 0; m < TC; ++m) {  // channels g C .. g C + C - 1 of loop step beta TC + m
+        uint32_t w[C / 2];
+#pragma unroll
+        for (int k = 0; k < C / 2; ++k) w[k] = 0;
         if (live[u]) {
           const int t0 = beta * TC + m;
           const uint16_t* xp =
-              win + (((((size_t)l * a.T + t0) * a.max_batch + b) * a.H + h) * a.win_slots + slot) * kD + g * kC;
-          w4 = __ldg(reinterpret_cast<const uint4*>(xp));
-        }
-        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+              win + (((((size_t)l * a.T + t0) * a.max_batch + b) * a.H + h) * a.win_slots + slot) * kD + g * C;
+          if constexpr (C == 4) {
+            const uint2 w2 = __ldg(reinterpret_cast<const uint2*>(xp));
+            w[0] = w2.x;
+            w[1] = w2.y;
+          } else {
 #pragma unroll
-        for (int i = 0; i < kC; ++i) z[u][i * TC + m] = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
+            for (int k4 = 0; k4 < C / 8; ++k4) {
+              const uint4 w4 = __ldg(reinterpret_cast<const uint4*>(xp) + k4);
+              w[4 * k4] = w4.x;
+              w[4 * k4 + 1] = w4.y;
+              w[4 * k4 + 2] = w4.z;
+              w[4 * k4 + 3] = w4.w;
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < C; ++i) z[u][i * TC + m] = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
       }
     }
     // ---- screening: best two of acc_r = z.e_r - |e_r|^2/2 for both vectors ---------------
@@ -273,7 +284,7 @@ __global__ void __launch_bounds__(256) roll_kernel(const VqRollArgs a) {
         }
       }
       idx_base[((size_t)b_of[u] * a.H + h) * (size_t)a.max_pages * kPageBytes + (size_t)np_of[u] * kPageBytes +
-               page_byte(g, j_of[u])] = (uint8_t)result;
+               page_byte(g, j_of[u], kNG)] = (uint8_t)result;
     }
   }
 }
@@ -322,13 +333,14 @@ cudaError_t launch_vq_append(const VqAppendArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_vq_roll(const VqRollArgs& a, cudaStream_t s) {
-  dim3 grid(a.L * a.NB * a.H * 2 * kNG);
-  switch (a.Tc) {
-    case 1: roll_kernel<1><<<grid, 256, 0, s>>>(a); break;
-    case 2: roll_kernel<2><<<grid, 256, 0, s>>>(a); break;
-    case 4: roll_kernel<4><<<grid, 256, 0, s>>>(a); break;
-    default: return cudaErrorInvalidValue;
-  }
+  const int C = a.G / a.Tc;
+  dim3 grid(a.L * a.NB * a.H * 2 * (kD / C));
+  if (a.Tc == 1 && C == 8) roll_kernel<1, 8><<<grid, 256, 0, s>>>(a);
+  else if (a.Tc == 2 && C == 8) roll_kernel<2, 8><<<grid, 256, 0, s>>>(a);
+  else if (a.Tc == 4 && C == 8) roll_kernel<4, 8><<<grid, 256, 0, s>>>(a);
+  else if (a.Tc == 1 && C == 16) roll_kernel<1, 16><<<grid, 256, 0, s>>>(a);
+  else if (a.Tc == 4 && C == 4) roll_kernel<4, 4><<<grid, 256, 0, s>>>(a);
+  else return cudaErrorInvalidValue;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   roll_commit_kernel<<<1, 256, 0, s>>>(a);

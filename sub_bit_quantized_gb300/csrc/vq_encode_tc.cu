@@ -46,14 +46,18 @@ constexpr uint32_t kTmemCols = 256;  // fp32 accumulator columns
 constexpr int kParts = 3;            // hi, mid, lo bf16 parts of the fp32 codebook
 constexpr int kTcBlocksPerSm = 2;    // 2 x 256 TMEM columns
 
-// 16-byte K chunks per row: TC chunks of data (8 coordinates of one loop step each), one
-// augmented chunk (A: 1, 0..; B: -||e||^2 / 2, 0..), padded to whole MMA K steps of 32 bytes
-__host__ __device__ constexpr int tc_chunks(int TC) { return 2 * ((TC + 2) / 2); }
+// 16-byte K chunks per row: G/8 chunks of data (row coordinate k' = m c + i holds channel
+// g c + i of loop step m, i.e. coupled coordinate i Tc + m), one augmented chunk (A: 1, 0..;
+// B: -||e||^2 / 2, 0..), padded to whole MMA K steps of 32 bytes
+__host__ __device__ constexpr int tc_chunks(int DC) { return 2 * ((DC + 2) / 2); }
 
-template <int TC>
+template <int TC, int C>
 struct TcLayout {
-  static constexpr int G = TC * kC;
-  static constexpr int KC = tc_chunks(TC);
+  static constexpr int G = TC * C;
+  static constexpr int DC = G / 8;                          // data chunks per row
+  static constexpr int NG = kD / C;                         // groups per token
+  static constexpr int kPageBytes = kPage * NG;
+  static constexpr int KC = tc_chunks(DC);
   static constexpr int kRowBytes = KC * 16;
   static constexpr int kABytes = kTcM * kRowBytes;          // one tile of vectors
   static constexpr int kBPartBytes = kTcN * kRowBytes;      // one codebook part
@@ -120,10 +124,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 
 __device__ __forceinline__ uint16_t bf16_rn_bits(float f) { return f32_to_bf16(f); }
 
-__device__ __forceinline__ size_t page_byte_tc(int g, int j) {  // in-page byte of (group, token)
-  return (size_t)(((g & 7) * kPage + (j & 7)) * 2 + (g >> 3));
-}
-
 // one warpgroup's share of a row: its maximum, the band it used, how many of its columns lie
 // within that band of its maximum, and the first of them
 struct Quarter {
@@ -145,11 +145,11 @@ __device__ __forceinline__ float acc_band(float z2, float best) {
   return 8.f * 3.f * (KC / 2) * 18.f * 5.97e-8f * (znorm * enear + 0.5f * enear * enear) + 1e-6f * dbest + 1e-30f;
 }
 
-template <int TC>
+template <int TC, int C>
 __global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(const VqEncodeArgs a, const int U,
                                                                                 const int tiles_per_plane) {
-  using Lay = TcLayout<TC>;
-  constexpr int G = Lay::G, KC = Lay::KC;
+  using Lay = TcLayout<TC, C>;
+  constexpr int G = Lay::G, KC = Lay::KC, DC = Lay::DC;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* sb = smem + Lay::kOffB;
   Quarter* part = reinterpret_cast<Quarter*>(smem + Lay::kOffPart);
@@ -176,11 +176,11 @@ __global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(c
     fence_mbar_init();
   }
   // constant chunks of both A buffers: the ones column, zero padding
-  for (int i = tid; i < 2 * kTcM * (KC - TC); i += kTcThreads) {
-    const int buf = i / (kTcM * (KC - TC)), rem = i % (kTcM * (KC - TC));
-    const int r = rem / (KC - TC), c = TC + rem % (KC - TC);
+  for (int i = tid; i < 2 * kTcM * (KC - DC); i += kTcThreads) {
+    const int buf = i / (kTcM * (KC - DC)), rem = i % (kTcM * (KC - DC));
+    const int r = rem / (KC - DC), c = DC + rem % (KC - DC);
     *reinterpret_cast<uint4*>(smem + Lay::kOffA + buf * Lay::kABytes + op_off(r, c, KC)) =
-        make_uint4(c == TC ? 0x3F80u : 0u, 0u, 0u, 0u);
+        make_uint4(c == DC ? 0x3F80u : 0u, 0u, 0u, 0u);
   }
   __syncthreads();
   tc_fence_after();
@@ -194,19 +194,28 @@ __global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(c
   const float* cb = nullptr;
   uint8_t* out = nullptr;
   int g = 0;
-  // chunk i (< kTcM * TC) of unit u: 16 bytes of one vector row (zeros past the tokens)
+  // chunk i (< kTcM * DC) of unit u: 16 bytes of one vector row (zeros past the tokens):
+  // row coordinates 8d .. 8d + 7 of chunk d are channels of one loop step (c >= 8) or of
+  // two (c = 4)
   auto load_chunk = [&](int u) {
     uint4 v = make_uint4(0, 0, 0, 0);
     const int i = tid;
-    if (u < hi && i < kTcM * TC) {
+    if (u < hi && i < kTcM * DC) {
       const int pl = u / tiles_per_plane, tt = u - pl * tiles_per_plane;
       const int gi2 = pl % a.g_count, be = (pl / a.g_count) % a.NB, hh = (pl / (a.g_count * a.NB)) % a.H;
       const int bb = pl / (a.g_count * a.NB * a.H);
-      const int r = i / TC, m = i % TC;
+      const int r = i / DC, d = i % DC;
       const int j = tt * kTcM + r;
-      if (j < a.n_tok)
-        v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)(be * TC + m) * a.st + (size_t)bb * a.sb +
-                                                 (size_t)hh * a.sh + (size_t)j * kD + (a.g_begin + gi2) * kC));
+      if (j < a.n_tok) {
+        const uint16_t* xr = a.x + (size_t)bb * a.sb + (size_t)hh * a.sh + (size_t)j * kD + (a.g_begin + gi2) * C;
+        if constexpr (C >= 8) {
+          v = __ldg(reinterpret_cast<const uint4*>(xr + (size_t)(be * TC + (8 * d) / C) * a.st + (8 * d) % C));
+        } else {
+          const uint2 w0 = __ldg(reinterpret_cast<const uint2*>(xr + (size_t)(be * TC + 2 * d) * a.st));
+          const uint2 w1 = __ldg(reinterpret_cast<const uint2*>(xr + (size_t)(be * TC + 2 * d + 1) * a.st));
+          v = make_uint4(w0.x, w0.y, w1.x, w1.y);
+        }
+      }
     }
     return v;
   };
@@ -222,10 +231,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(c
     const int b = plane / (a.g_count * a.NB * a.H);
     if (plane != cur_plane) {  // uniform
       // ---- codebook of this plane: three bf16 parts with the -||e||^2/2 column ------------
-      // coordinate k' = c*8 + i of a row (chunk c < TC, i < 8) is coupled coordinate i*TC + c
+      // row coordinate k' = 8 c + i (chunk c < DC, i < 8) = m C + i2 is coupled coordinate i2 TC + m
       g = a.g_begin + gi;
-      cb = a.cb + (((size_t)beta * a.H + h) * kNG + g) * (size_t)kCB * G;
-      out = a.idx + (((size_t)beta * a.max_batch + (a.seq_begin + b)) * a.H + h) * (size_t)a.max_pages * kPageBytes;
+      cb = a.cb + (((size_t)beta * a.H + h) * Lay::NG + g) * (size_t)kCB * G;
+      out = a.idx + (((size_t)beta * a.max_batch + (a.seq_begin + b)) * a.H + h) * (size_t)a.max_pages * Lay::kPageBytes;
       __syncthreads();  // the previous plane's MMAs have all been waited for
       for (int r = tid; r < kTcN; r += kTcThreads) {
         float nh_hi = 0.f, nh_lo = 0.f;  // |e|^2, compensated
@@ -243,8 +252,12 @@ __global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(c
             for (int e2 = 0; e2 < 2; ++e2) {
               const int i = 2 * i2 + e2;
               float v = 0.f;
-              if (c < TC) v = __ldg(cb + (size_t)r * G + i * TC + c);
-              else if (c == TC && i == 0) v = nh;
+              if (c < DC) {
+                const int kk = 8 * c + i;
+                v = __ldg(cb + (size_t)r * G + (kk % C) * TC + kk / C);
+              } else if (c == DC && i == 0) {
+                v = nh;
+              }
 #pragma unroll
               for (int p = 0; p < kParts; ++p) {
                 const uint16_t bits = bf16_rn_bits(v);
@@ -264,11 +277,11 @@ __global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(c
       cur_plane = plane;
     }
 
-    // ---- vector rows of tile t -> A buffer (TC 16-byte chunks per row); the next tile's
+    // ---- vector rows of tile t -> A buffer (DC 16-byte chunks per row); the next tile's
     //      rows are loaded now and land during this tile's work --------------------------------
     unsigned char* sa = smem + Lay::kOffA + buf * Lay::kABytes;
-    static_assert(kTcM * TC <= kTcThreads, "one chunk per thread");
-    if (tid < kTcM * TC) *reinterpret_cast<uint4*>(sa + op_off(tid / TC, tid % TC, KC)) = pre;
+    static_assert(kTcM * DC <= kTcThreads, "one chunk per thread");
+    if (tid < kTcM * DC) *reinterpret_cast<uint4*>(sa + op_off(tid / DC, tid % DC, KC)) = pre;
     pre = load_chunk(u + 1);
     fence_proxy_async_smem();  // A (and a new codebook) are read by the tensor cores
     tc_fence_before();
@@ -300,7 +313,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(c
     //      columns within the error band of it (a bit mask per 32 columns) --------------------
     float z2 = 0.f;
 #pragma unroll
-    for (int c = 0; c < TC; ++c) {
+    for (int c = 0; c < DC; ++c) {
       const uint4 w = *reinterpret_cast<const uint4*>(sa + op_off(row, c, KC));
       const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -386,7 +399,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(c
             // next part), so the staged parts give the fp32 entries back
             float dh = 0.f, dl = 0.f;
 #pragma unroll 1
-            for (int c = 0; c < TC; ++c) {
+            for (int c = 0; c < DC; ++c) {
               const uint4 w = *reinterpret_cast<const uint4*>(sa + op_off(row, c, KC));
               const uint4 e0 = *reinterpret_cast<const uint4*>(sb + op_off(r, c, KC));
               const uint4 e1 = *reinterpret_cast<const uint4*>(sb + Lay::kBPartBytes + op_off(r, c, KC));
@@ -416,7 +429,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(c
         }
       }
       if (valid && !*failed)
-        out[(size_t)(a.page_begin + j / kPage) * kPageBytes + page_byte_tc(g, j)] = (uint8_t)result;
+        out[(size_t)(a.page_begin + j / kPage) * Lay::kPageBytes + page_byte(g, j % kPage, Lay::NG)] = (uint8_t)result;
     }
   }
 
@@ -433,10 +446,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(c
   }
 }
 
-template <int TC>
+template <int TC, int C>
 cudaError_t launch_tc(const VqEncodeArgs& a, cudaStream_t s) {
-  using Lay = TcLayout<TC>;
-  cudaError_t e = cudaFuncSetAttribute(encode_tc_kernel<TC>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
+  using Lay = TcLayout<TC, C>;
+  cudaError_t e = cudaFuncSetAttribute(encode_tc_kernel<TC, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
   if (e != cudaSuccess) return e;
   const long long planes = (long long)a.n_seq * a.H * a.NB * a.g_count;
   const int tiles = (a.n_tok + kTcM - 1) / kTcM;
@@ -445,7 +458,7 @@ cudaError_t launch_tc(const VqEncodeArgs& a, cudaStream_t s) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long blocks = std::min<long long>(U, (long long)kTcBlocksPerSm * sms);
-  encode_tc_kernel<TC><<<(unsigned)blocks, kTcThreads, Lay::kSmem, s>>>(a, (int)U, tiles);
+  encode_tc_kernel<TC, C><<<(unsigned)blocks, kTcThreads, Lay::kSmem, s>>>(a, (int)U, tiles);
   return cudaGetLastError();
 }
 
@@ -453,12 +466,13 @@ cudaError_t launch_tc(const VqEncodeArgs& a, cudaStream_t s) {
 
 cudaError_t launch_vq_encode(const VqEncodeArgs& a, cudaStream_t s) {
   if (a.n_tok <= 0 || a.n_seq <= 0 || a.g_count <= 0) return cudaSuccess;
-  switch (a.Tc) {
-    case 1: return launch_tc<1>(a, s);
-    case 2: return launch_tc<2>(a, s);
-    case 4: return launch_tc<4>(a, s);
-    default: return cudaErrorInvalidValue;
-  }
+  const int C = a.G / a.Tc;
+  if (a.Tc == 1 && C == 8) return launch_tc<1, 8>(a, s);
+  if (a.Tc == 2 && C == 8) return launch_tc<2, 8>(a, s);
+  if (a.Tc == 4 && C == 8) return launch_tc<4, 8>(a, s);
+  if (a.Tc == 1 && C == 16) return launch_tc<1, 16>(a, s);
+  if (a.Tc == 4 && C == 4) return launch_tc<4, 4>(a, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace kvq

@@ -53,9 +53,20 @@ def test_cache_sizes_formula(L):
     assert s.idx / 24 / 2 * 2 == pytest.approx(199.0e6, rel=1e-3)
 
 
+@pytest.mark.parametrize("Tc,NG", [(1, 8), (2, 16), (4, 32)])
+def test_half_bit_loop_grouping_sizes(L, Tc, NG):
+    # 0.5 bit (G = 16) at Tc = 1, 2, 4: c = 16, 8, 4 channels per codeword, NG = 8, 16, 32 index
+    # bytes per (token, head, block), T / Tc blocks: the index arrays hold the same bytes
+    s = kvq.vq_cache_sizes(cfg2(Tc=Tc, G=16))
+    assert s.idx == 24 * (4 // Tc) * 64 * 16 * 759 * 8 * NG
+    assert s.idx == kvq.vq_cache_sizes(cfg2()).idx
+    assert s.cb == 24 * (4 // Tc) * 16 * NG * 256 * 16 * 4
+
+
 @pytest.mark.parametrize("kw,code", [(dict(Tc=3), 1), (dict(G=12), 1), (dict(G=32), 3),
                                      (dict(D=64), 3), (dict(K=16), 3), (dict(max_ctx=1), 1),
-                                     (dict(T=8, Tc=8, G=64), 3), (dict(max_batch=0), 1)])
+                                     (dict(T=8, Tc=8, G=64), 3), (dict(max_batch=0), 1),
+                                     (dict(Tc=2, G=8), 3), (dict(Tc=4, G=64), 3)])
 def test_bad_configs_rejected(L, kw, code):
     with pytest.raises(kvq.KvqError) as e:
         kvq.vq_cache_sizes(cfg2(**kw))

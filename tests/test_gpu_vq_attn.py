@@ -79,6 +79,17 @@ def test_quarter_bit_long_context_layout():
     check_all(case, cache, steps=(3,), n_splits=0)
 
 
+@pytest.mark.parametrize("Tc", [1, 4])
+def test_half_bit_loop_grouping_variants(Tc):
+    # 0.5 bit (G = 16) with Tc = 1 (c = 16: per-step codewords, 8 index groups per token,
+    # 64-byte pages) and Tc = 4 (c = 4: one index serves all four steps, 32 groups, 256-byte
+    # pages); ragged batch, every loop step, several split counts
+    case = C.make_vq_case(108 + Tc, B=3, H=2, lens=[73, 8 + 64 + 8 * 70 + 3, 513], Tc=Tc, G=16)
+    cache = C.fill_vq_cache(case)
+    check_all(case, cache, steps=(1, 2, 3, 4))
+    check_all(case, cache, steps=(2, 4), n_splits=7)
+
+
 def test_repeated_calls_reuse_workspace():
     case = C.make_vq_case(105, B=4, H=3, lens=[600, 1000, 999, 1500])
     cache = C.fill_vq_cache(case)
@@ -90,12 +101,14 @@ def test_repeated_calls_reuse_workspace():
     check_all(case, cache, steps=(1,), n_splits=5)
 
 
-@pytest.mark.parametrize("cfgname", ["b64_ctx6144_half_bit", "b8_ctx32768_quarter_bit"])
+@pytest.mark.parametrize("cfgname", ["b64_ctx6144_half_bit", "b8_ctx32768_quarter_bit", "b64_ctx6144_half_bit_tc1",
+                                     "b64_ctx6144_half_bit_tc4"])
 def test_full_size_sampled(cfgname):
     # full workload sizes in the launch configuration the bench uses (automatic split);
     # the oracle evaluates a sample of (request, head) pairs one by one
-    if cfgname == "b64_ctx6144_half_bit":
-        case = C.make_vq_case(106, B=64, H=16, lens=[6144] * 64)
+    if cfgname.startswith("b64_ctx6144_half_bit"):
+        Tc = {"b64_ctx6144_half_bit": 2, "b64_ctx6144_half_bit_tc1": 1, "b64_ctx6144_half_bit_tc4": 4}[cfgname]
+        case = C.make_vq_case(106, B=64, H=16, lens=[6144] * 64, Tc=Tc, G=16)
         steps = (1, 2, 3, 4)
     else:
         case = C.make_vq_case(107, B=8, H=16, lens=[32768] * 8, Tc=4, G=32, recent=256, rho=(0.85, 0.85))

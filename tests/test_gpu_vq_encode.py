@@ -48,7 +48,7 @@ def check_indices(got, want, ties):
     return int(diff.sum())
 
 
-@pytest.mark.parametrize("Tc,G", [(2, 16), (4, 32), (1, 8)])
+@pytest.mark.parametrize("Tc,G", [(2, 16), (4, 32), (1, 8), (1, 16), (4, 16)])
 def test_encode_matches_oracle(Tc, G):
     T, B, H, L = 4, 2, 2, 96
     g, xk, _ = gen_kv(200 + Tc, B, H, L, T)
@@ -134,10 +134,12 @@ def test_encode_full_size_sampled():
     assert n_tie <= int(ties.item())
 
 
-def test_prefill_then_attention_integration():
+@pytest.mark.parametrize("Tc", [2, 1, 4])
+def test_prefill_then_attention_integration(Tc):
     # each side runs its own pipeline from the same synthetic K/V: GPU prefill (encode +
-    # windows) then GPU attention, against oracle encode then oracle attention
-    T, Tc, G, B, H = 4, 2, 16, 3, 2
+    # windows) then GPU attention, against oracle encode then oracle attention; at 0.5 bit
+    # with Tc = 2 (c = 8), Tc = 1 (c = 16) and Tc = 4 (c = 4)
+    T, G, B, H = 4, 16, 3, 2
     lens = [200, 77, 8 + 64 + 8 * 20 + 3]
     Lmax = max(lens)
     g, xk, xv = gen_kv(220, B, H, Lmax, T)
@@ -154,8 +156,8 @@ def test_prefill_then_attention_integration():
     assert cache.seq_len.tolist() == lens and cache.n_pages.tolist() == n_pages
     q = synth.bf16_round(synth.gaussian(g, (B, H, D)))
     out = torch.empty((B, H, D), dtype=torch.float32, device="cuda")
-    pk = _layout.unpack_pages(cache.idx_k[0].cpu().numpy(), 16)
-    pv = _layout.unpack_pages(cache.idx_v[0].cpu().numpy(), 16)
+    pk = _layout.unpack_pages(cache.idx_k[0].cpu().numpy(), cfg.NG)
+    pv = _layout.unpack_pages(cache.idx_v[0].cpu().numpy(), cfg.NG)
     for t in (1, 2, 3, 4):
         kvq.kvq_decode_attn(cfg, cache, 0, t, C.bf16_tensor(q), out)
         got = out.cpu().numpy()
@@ -173,11 +175,12 @@ def test_prefill_then_attention_integration():
                 C.check_close(got[b, h], ref)
 
 
-def test_append_and_roll_equal_prefill_encoding():
+@pytest.mark.parametrize("Tc", [2, 1, 4])
+def test_append_and_roll_equal_prefill_encoding(Tc):
     # stream 40 tokens through kvq_append_page (2 layers x 4 loop steps each): the rolled
     # pages must equal the oracle's encoding of the same tokens, lengths must follow the
     # sink / page / recent rule, and attention must match the oracle at the end
-    T, Tc, G, B, H, NL = 4, 2, 16, 2, 2, 2
+    T, G, B, H, NL = 4, 16, 2, 2, 2
     L0 = [101, 90]
     n_new = 40
     Lmax = max(L0) + n_new
@@ -209,7 +212,7 @@ def test_append_and_roll_equal_prefill_encoding():
     assert kvq.device_error() == 0
     for l in range(NL):
         for name, x2, cb in (("idx_k", xk2, cbk), ("idx_v", xv2, cbv)):
-            pages = _layout.unpack_pages(getattr(cache, name)[l].cpu().numpy(), 16)
+            pages = _layout.unpack_pages(getattr(cache, name)[l].cpu().numpy(), cfg.NG)
             for b in range(B):
                 npg = olv.prefill_split(lens[b])[1]
                 qpos = np.arange(8, 8 + 8 * npg)

@@ -32,7 +32,7 @@ def test_index_map_hand_table():
             assert z[g].tolist() == gd["z"][f"beta{beta}_g{g}"]
 
 
-@pytest.mark.parametrize("T,Tc,G,D", [(4, 2, 16, 128), (4, 4, 32, 128), (4, 1, 16, 128), (32, 4, 16, 64)])
+@pytest.mark.parametrize("T,Tc,G,D", [(4, 2, 16, 128), (4, 4, 32, 128), (4, 1, 16, 128), (4, 4, 16, 128), (32, 4, 16, 64)])
 def test_index_map_codeword_spans_c_channels_by_Tc_steps(T, Tc, G, D):
     # one codeword spans c = G/Tc consecutive channels of group g across the Tc steps of
     # block beta, each (step, channel) pair exactly once, and no group overlaps another
@@ -49,7 +49,7 @@ def test_index_map_codeword_spans_c_channels_by_Tc_steps(T, Tc, G, D):
     assert len(seen) == T * D
 
 
-@pytest.mark.parametrize("T,Tc,G", [(4, 2, 16), (4, 4, 32), (4, 1, 16)])
+@pytest.mark.parametrize("T,Tc,G", [(4, 2, 16), (4, 4, 32), (4, 1, 16), (4, 4, 16)])
 def test_one_index_serves_every_step_of_its_block(T, Tc, G):
     # codebook = the tokens' own coupled vectors -> indices are the token ids, and
     # dequantizing at each in-block step m returns that step's values exactly
@@ -118,7 +118,7 @@ def torch_rope(x, pos, base=1e4):
     return torch.cat([zc.real, zc.imag], -1)
 
 
-@pytest.mark.parametrize("T,Tc,G,t", [(4, 2, 16, 1), (4, 2, 16, 4), (4, 4, 32, 3), (4, 1, 16, 2)])
+@pytest.mark.parametrize("T,Tc,G,t", [(4, 2, 16, 1), (4, 2, 16, 4), (4, 4, 32, 3), (4, 1, 16, 2), (4, 4, 16, 3)])
 def test_attention_equals_plain_attention_when_tokens_are_codewords(T, Tc, G, t):
     # when every quantized token equals a codeword exactly, LoopVQ attention must equal
     # textbook RoPE attention on the unquantized cache (library SDPA, complex-form RoPE)

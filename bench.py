@@ -337,9 +337,18 @@ def kivi_wl_bytes(wl):
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch from an ncu capture,
 # valid only for the kernel source it was taken on (profiles/ holds the capture summary)
 PROFILED_TRAFFIC = {
-    "loopvq_b64_6k:vq_pages_kernel+vq_window_kernel": ("sub_bit_quantized_gb300/csrc/vq_attn.cu",
-                                         "2957b85af7697c08d1211f09aae0e4e37f0d28646c882d637e7a7e317753516e",
-                                         210055424 + 43537664),
+    "loopvq_b64_6k:vq_pages_kernel+vq_window_kernel": (
+        "sub_bit_quantized_gb300/csrc/vq_attn.cu",
+        "ceb0c59fa786a314ca24fe1c7e1e2f02093c5a355da5176c46778d049518c92c",
+        204150016 + 5767424 + 43536640 + 3072),
+    "kivi_b16_4k:kivi_attn_kernel": (
+        "sub_bit_quantized_gb300/csrc/kivi.cu",
+        "0474bba73e3cf49c0a5e6860728af987755220c7d31cf08b8ff9430cae00d5f5",
+        228799488 + 4636928),
+    "kivi4_gqa_b16_4k:kivi_attn_kernel": (
+        "sub_bit_quantized_gb300/csrc/kivi.cu",
+        None,  # captured on an earlier revision of kivi.cu (profiles/): not current
+        89868544 + 2781952),
 }
 
 

@@ -347,7 +347,7 @@ PROFILED_TRAFFIC = {
         228799488 + 4636928),
     "kivi4_gqa_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        None,  # captured on an earlier revision of kivi.cu (profiles/): not current
+        "0474bba73e3cf49c0a5e6860728af987755220c7d31cf08b8ff9430cae00d5f5",
         89868544 + 2781952),
 }
 

@@ -18,15 +18,23 @@
 // and candidates closer than 1e-6 (relative) are reported as a tie, where either index is a
 // valid answer.
 //
-// GB300 mapping. Persistent 512-thread blocks, two per SM (each holds a 128 x 256 fp32
-// accumulator in 256 TMEM columns), over equal contiguous shares of the (plane, 128-vector
-// tile) units, a plane being one (sequence, head, block beta, group) with its codebook. A
-// block stages the three codebook parts in shared memory (K-major, no swizzle: 8-row x
-// 16-byte core matrices) when its share enters a plane. Per tile: the block loads the vector
-// rows into one of two A buffers, one thread issues the tcgen05.mma chain (3 parts x K steps
-// of 16) and commits to an mbarrier; the four warpgroups each read 64 accumulator columns of
-// every row (tcgen05.ld) and keep the best two; warpgroup 0 merges the four and writes the
-// index while the others load the next tile. Every wait is bounded.
+// GB300 mapping. One persistent block per SM over an equal contiguous share of the (plane,
+// 128-vector tile) units, a plane being one (sequence, head, block beta, group) with its
+// codebook, whose three bf16 parts sit in shared memory (K-major, no swizzle: 8-row x 16-byte
+// core matrices). The block is a warp-specialised pipeline synchronised only by mbarriers:
+//  * a loader warp copies each tile's vector rows into a 4-stage ring with cp.async (zero
+//    fill past the last token), two tiles in flight;
+//  * an MMA warp issues, from one thread, the tcgen05.mma chain of a tile (3 parts x K steps
+//    of 16) into one of two 128 x 256 fp32 TMEM accumulators and commits to that
+//    accumulator's barrier; at a plane change it restages the codebook once the earlier
+//    tiles are done with it;
+//  * two epilogue warpgroups take alternate tiles, one accumulator each: a thread owns a row
+//    and reads its 256 columns twice (tcgen05.ld): the best acc (3-input max), then how many
+//    columns lie in the error band below it and, when one does, which (a weighted sum on the
+//    FMA pipe, so the half-rate ALU pipe is not the limit); it releases the accumulator, decides
+//    near-ties as above from shared memory, writes the index and releases the ring stage.
+// So the MMAs of one tile run while the other accumulator's epilogue works. Every wait is
+// bounded; a timeout sets the device error word and every warp leaves its loop.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -38,13 +46,18 @@
 namespace kvq {
 namespace {
 
-constexpr int kTcThreads = 512;      // 4 warpgroups; a thread reads one TMEM lane
 constexpr int kTcM = 128;            // vectors per tile (MMA M)
 constexpr int kTcN = 256;            // codewords (MMA N)
-constexpr int kQCols = kTcN / 4;     // accumulator columns each warpgroup reads
-constexpr uint32_t kTmemCols = 256;  // fp32 accumulator columns
 constexpr int kParts = 3;            // hi, mid, lo bf16 parts of the fp32 codebook
-constexpr int kTcBlocksPerSm = 2;    // 2 x 256 TMEM columns
+constexpr int kEpiWarps = 8;         // two epilogue warpgroups, one accumulator each
+constexpr int kLoadWarp = 8;         // cp.async loader
+constexpr int kMmaWarp = 9;          // MMA issue (lane 0) and codebook restaging
+constexpr int kEncThreads = 320;
+constexpr int kAStages = 4;          // vector-row ring
+constexpr int kLoadDepth = 2;        // tiles whose row copies the loader keeps in flight
+constexpr uint32_t kTmemCols = 512;  // two 128 x 256 fp32 accumulators
+static_assert(kEpiWarps == 8 && kLoadWarp == kEpiWarps && kMmaWarp == kLoadWarp + 1 &&
+              kEncThreads == 32 * (kMmaWarp + 1), "warp roles");
 
 // 16-byte K chunks per row: G/8 chunks of data (row coordinate k' = m c + i holds channel
 // g c + i of loop step m, i.e. coupled coordinate i Tc + m), one augmented chunk (A: 1, 0..;
@@ -61,11 +74,13 @@ struct TcLayout {
   static constexpr int kRowBytes = KC * 16;
   static constexpr int kABytes = kTcM * kRowBytes;          // one tile of vectors
   static constexpr int kBPartBytes = kTcN * kRowBytes;      // one codebook part
-  static constexpr int kOffA = 0;                           // two tile buffers
-  static constexpr int kOffB = kOffA + 2 * kABytes;
-  static constexpr int kOffPart = kOffB + kParts * kBPartBytes;  // [row][warpgroup] best two
-  static constexpr int kOffBar = kOffPart + kTcM * 4 * 16;       // mbarrier + TMEM address
-  static constexpr int kSmem = kOffBar + 32;
+  static constexpr int kOffA = 0;                           // kAStages tile buffers
+  static constexpr int kOffB = kOffA + kAStages * kABytes;  // the three codebook parts
+  static constexpr int kOffBar = kOffB + kParts * kBPartBytes;  // mbarriers, TMEM address, flag
+  static constexpr int kSmem = kOffBar + 160;
+  // requested per block so that a second block cannot share the SM (and its 512 TMEM columns)
+  static constexpr int kSmemLaunch = kSmem > 120 * 1024 ? kSmem : 120 * 1024;
+  static_assert(kSmemLaunch <= 232448, "shared memory");
 };
 
 // byte offset of (row, chunk) in a K-major, no-swizzle operand: core matrices of 8 rows x 16
@@ -122,48 +137,179 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ uint16_t bf16_rn_bits(float f) { return f32_to_bf16(f); }
+// 64 consecutive fp32 columns of this thread's TMEM lane: two loads, one wait
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[32 * h + 0]), "=r"(r[32 * h + 1]), "=r"(r[32 * h + 2]), "=r"(r[32 * h + 3]), "=r"(r[32 * h + 4]),
+          "=r"(r[32 * h + 5]), "=r"(r[32 * h + 6]), "=r"(r[32 * h + 7]), "=r"(r[32 * h + 8]), "=r"(r[32 * h + 9]),
+          "=r"(r[32 * h + 10]), "=r"(r[32 * h + 11]), "=r"(r[32 * h + 12]), "=r"(r[32 * h + 13]),
+          "=r"(r[32 * h + 14]), "=r"(r[32 * h + 15]), "=r"(r[32 * h + 16]), "=r"(r[32 * h + 17]),
+          "=r"(r[32 * h + 18]), "=r"(r[32 * h + 19]), "=r"(r[32 * h + 20]), "=r"(r[32 * h + 21]),
+          "=r"(r[32 * h + 22]), "=r"(r[32 * h + 23]), "=r"(r[32 * h + 24]), "=r"(r[32 * h + 25]),
+          "=r"(r[32 * h + 26]), "=r"(r[32 * h + 27]), "=r"(r[32 * h + 28]), "=r"(r[32 * h + 29]),
+          "=r"(r[32 * h + 30]), "=r"(r[32 * h + 31])
+        : "r"(taddr + 32 * h)
+        : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
 
-// one warpgroup's share of a row: its maximum, the band it used, how many of its columns lie
-// within that band of its maximum, and the first of them
-struct Quarter {
-  float best, band;
-  int count, first;
-};
+// cp.async of 16 (or 8) bytes, zero-filled when `fill` is false (src is then not read)
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool fill) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(fill ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src, bool fill) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(fill ? 8 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ uint16_t bf16_rn_bits(float f) { return f32_to_bf16(f); }
 
 // Error band in acc units for a row with |z|^2 = z2 whose best acc is `best`. A codeword that
 // can compete with the best lies within |z| + sqrt(d_best) of the origin, and its
 // acc = z.e - |e|^2/2 is accumulated over 3 x KC/2 MMAs of exact bf16 products: its error is
 // below about 3 (KC/2) 17 2^-24 (|z||e| + |e|^2/2) plus the 2^-24 |z||e| of the split. The
-// band takes 8 times that for two candidates, plus the 1e-6 tie threshold of the best
-// distance. A larger `best` (a better candidate) never widens it.
+// band takes 4 times that (the difference of two candidates, each accumulated with rounding
+// that may go toward zero), plus the 1e-6 tie threshold of the best distance. A larger `best`
+// (a better candidate) never widens it.
 template <int KC>
 __device__ __forceinline__ float acc_band(float z2, float best) {
   const float znorm = sqrtf(z2);
   const float dbest = fmaxf(0.f, z2 - 2.f * best);
   const float enear = znorm + 1.01f * sqrtf(dbest) + 1e-3f * znorm + 1e-6f;
-  return 8.f * 3.f * (KC / 2) * 18.f * 5.97e-8f * (znorm * enear + 0.5f * enear * enear) + 1e-6f * dbest + 1e-30f;
+  return 4.f * 3.f * (KC / 2) * 18.f * 5.97e-8f * (znorm * enear + 0.5f * enear * enear) + 1e-6f * dbest + 1e-30f;
+}
+
+// plane p of the encode: (sequence b, head h, block beta, group index gi)
+struct Plane {
+  int b, h, beta, gi;
+};
+__device__ __forceinline__ Plane plane_of(const VqEncodeArgs& a, int p) {
+  Plane q;
+  q.gi = p % a.g_count;
+  q.beta = (p / a.g_count) % a.NB;
+  q.h = (p / (a.g_count * a.NB)) % a.H;
+  q.b = p / (a.g_count * a.NB * a.H);
+  return q;
+}
+
+// three bf16 parts of the plane's codebook (and its -||e||^2/2 column), rows r0, r0 + nt, ..
+template <int TC, int C>
+__device__ void stage_codebook(const VqEncodeArgs& a, int plane, unsigned char* sb, int r0, int nt) {
+  using Lay = TcLayout<TC, C>;
+  constexpr int G = Lay::G, KC = Lay::KC, DC = Lay::DC;
+  const Plane P = plane_of(a, plane);
+  const float* cb = a.cb + (((size_t)P.beta * a.H + P.h) * Lay::NG + a.g_begin + P.gi) * (size_t)kCB * G;
+#pragma unroll 1
+  for (int r = r0; r < kTcN; r += nt) {
+    float ev[G];  // the row's coordinates, all loads in flight together
+#pragma unroll
+    for (int k = 0; k < G; k += 4) {
+      const float4 q4 = __ldg(reinterpret_cast<const float4*>(cb + (size_t)r * G + k));
+      ev[k] = q4.x;
+      ev[k + 1] = q4.y;
+      ev[k + 2] = q4.z;
+      ev[k + 3] = q4.w;
+    }
+    float nh_hi = 0.f, nh_lo = 0.f;  // |e|^2, compensated
+#pragma unroll
+    for (int k = 0; k < G; ++k) add_sq_diff(ev[k], 0.f, nh_hi, nh_lo);
+    const float nh = -0.5f * __fadd_rn(nh_hi, nh_lo);
+    // row coordinate k' = 8 c + i (chunk c < DC, i < 8) = m C + i2 is coupled coordinate i2 TC + m;
+    // one 16-byte chunk at a time; parts: hi = bf16(v), mid = bf16(v - hi), lo = bf16(v - hi - mid)
+#pragma unroll
+    for (int c = 0; c < KC; ++c) {
+      uint32_t w[kParts][4];
+#pragma unroll
+      for (int i2 = 0; i2 < 4; ++i2) {
+        uint16_t pb[kParts][2];
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int i = 2 * i2 + e2, kk = 8 * c + i;
+          float v = 0.f;
+          if (c < DC) v = ev[(kk % C) * TC + kk / C];
+          else if (c == DC && i == 0) v = nh;
+#pragma unroll
+          for (int p = 0; p < kParts; ++p) {
+            const uint16_t bits = bf16_rn_bits(v);
+            pb[p][e2] = bits;
+            v = v - bf16_to_f32(bits);  // exact: v and its bf16 rounding are within 2^-8 |v|
+          }
+        }
+#pragma unroll
+        for (int p = 0; p < kParts; ++p) w[p][i2] = pb[p][0] | ((uint32_t)pb[p][1] << 16);
+      }
+#pragma unroll
+      for (int p = 0; p < kParts; ++p)
+        *reinterpret_cast<uint4*>(sb + p * Lay::kBPartBytes + op_off(r, c, KC)) =
+            make_uint4(w[p][0], w[p][1], w[p][2], w[p][3]);
+    }
+  }
+}
+
+__device__ __forceinline__ bool enc_wait(uint64_t* bar, uint32_t parity, volatile int* failed, int* err) {
+  if (*failed) return false;
+  if (mbar_wait_bounded(bar, parity)) return true;
+  *failed = 1;
+  set_error(err, KVQ_ERR_TIMEOUT);
+  return false;
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// 1 when v >= thr, else 0, on the FMA pipe: sat(v 2^90 + (1 - thr 2^90)). v 2^90 rounds to
+// ~2^-24 of itself, so values within a few ulps of thr may land either way; the error band
+// around the best is far wider than that.
+__device__ __forceinline__ float at_least(float v, float cth) {
+  float d;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(v), "f"(1.2379400392853803e27f), "f"(cth));
+  return d;
 }
 
 template <int TC, int C>
-__global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(const VqEncodeArgs a, const int U,
-                                                                                const int tiles_per_plane) {
+__global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncodeArgs a, const int U,
+                                                                  const int tiles_per_plane) {
   using Lay = TcLayout<TC, C>;
-  constexpr int G = Lay::G, KC = Lay::KC, DC = Lay::DC;
+  constexpr int KC = Lay::KC, DC = Lay::DC;
   extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char* sa0 = smem + Lay::kOffA;
   unsigned char* sb = smem + Lay::kOffB;
-  Quarter* part = reinterpret_cast<Quarter*>(smem + Lay::kOffPart);
-  uint64_t* mma_bar = reinterpret_cast<uint64_t*>(smem + Lay::kOffBar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffBar + 8);
-  volatile int* failed = reinterpret_cast<volatile int*>(smem + Lay::kOffBar + 12);
+  uint64_t* afull = reinterpret_cast<uint64_t*>(smem + Lay::kOffBar);  // rows landed (32 loader lanes)
+  uint64_t* aempty = afull + kAStages;                                  // rows released (4 epilogue warps)
+  uint64_t* accfull = aempty + kAStages;                                // MMAs done (commit)
+  uint64_t* accempty = accfull + 2;                                     // accumulator read (4 warps)
+  uint64_t* bdone = accempty + 2;                                       // tile done with the codebook (4 warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bdone + 2);
+  volatile int* failed = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int wg = warp >> 2;                    // warpgroup: accumulator columns 64 wg ..
-  const int row = 32 * (warp & 3) + lane;      // TMEM lane = vector row of the tile
-  const int lo = (int)((long long)U * blockIdx.x / gridDim.x), hi = (int)((long long)U * (blockIdx.x + 1) / gridDim.x);
-  if (lo >= hi) return;
+  // Block k encodes group gi = k mod g_count over slots [m S / sets, (m + 1) S / sets) of the
+  // (sequence, head, block beta, tile) slots, m = k / g_count: the g_count blocks of a set walk
+  // the same token rows at the same time, so each row's 16-byte group slices come from DRAM
+  // once and from L2 for the other groups.
+  const int gsel = blockIdx.x % a.g_count, set = blockIdx.x / a.g_count, n_sets = gridDim.x / a.g_count;
+  const int lo = (int)((long long)U * set / n_sets), hi = (int)((long long)U * (set + 1) / n_sets);
+  if (lo >= hi) return;  // uniform
+  const int n = hi - lo;  // tiles of this block
+  // tile i of the block: slot lo + i -> plane ((sequence, head, beta) of the slot, group gsel), tile
+  auto plane_at = [&](int i) { return ((lo + i) / tiles_per_plane) * a.g_count + gsel; };
+  auto tile_at = [&](int i) { return (lo + i) % tiles_per_plane; };
 
-  // ---- TMEM accumulator (warp 0), barrier ----------------------------------------------
+  // ---- TMEM (warp 0), barriers, constant A chunks, the first plane's codebook (all threads) ----
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols)
@@ -171,230 +317,214 @@ __global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(c
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    mbar_init(mma_bar, 1);
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(&afull[s], 32);
+      mbar_init(&aempty[s], 4);
+    }
+    for (int e = 0; e < 2; ++e) {
+      mbar_init(&accfull[e], 1);
+      mbar_init(&accempty[e], 4);
+      mbar_init(&bdone[e], 4);
+    }
     *failed = 0;
     fence_mbar_init();
+    // the codebooks of the block's later planes: HBM -> L2 while the pipeline starts
+    for (int pl = plane_at(0) + a.g_count; pl <= plane_at(n - 1); pl += a.g_count) {
+      const Plane P = plane_of(a, pl);
+      bulk_prefetch_l2(a.cb + (((size_t)P.beta * a.H + P.h) * Lay::NG + a.g_begin + P.gi) * (size_t)kCB * Lay::G,
+                       kCB * Lay::G * 4);
+    }
   }
-  // constant chunks of both A buffers: the ones column, zero padding
-  for (int i = tid; i < 2 * kTcM * (KC - DC); i += kTcThreads) {
-    const int buf = i / (kTcM * (KC - DC)), rem = i % (kTcM * (KC - DC));
+  for (int i = tid; i < kAStages * kTcM * (KC - DC); i += kEncThreads) {  // the ones column, zero padding
+    const int st = i / (kTcM * (KC - DC)), rem = i % (kTcM * (KC - DC));
     const int r = rem / (KC - DC), c = DC + rem % (KC - DC);
-    *reinterpret_cast<uint4*>(smem + Lay::kOffA + buf * Lay::kABytes + op_off(r, c, KC)) =
-        make_uint4(c == DC ? 0x3F80u : 0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(sa0 + st * Lay::kABytes + op_off(r, c, KC)) = make_uint4(c == DC ? 0x3F80u : 0u, 0u, 0u, 0u);
   }
+  stage_codebook<TC, C>(a, plane_at(0), sb, tid, kEncThreads);
+  fence_proxy_async_smem();  // generic writes -> the tensor cores' view
+  tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kQCols * wg;
 
-  int ties = 0;
-  uint32_t phase = 0;
-  int pending = -1;  // thread 0: phase of an MMA chain whose completion it gave up waiting for
-  int cur_plane = -1, buf = 0;
-  const float* cb = nullptr;
-  uint8_t* out = nullptr;
-  int g = 0;
-  // chunk i (< kTcM * DC) of unit u: 16 bytes of one vector row (zeros past the tokens):
-  // row coordinates 8d .. 8d + 7 of chunk d are channels of one loop step (c >= 8) or of
-  // two (c = 4)
-  auto load_chunk = [&](int u) {
-    uint4 v = make_uint4(0, 0, 0, 0);
-    const int i = tid;
-    if (u < hi && i < kTcM * DC) {
-      const int pl = u / tiles_per_plane, tt = u - pl * tiles_per_plane;
-      const int gi2 = pl % a.g_count, be = (pl / a.g_count) % a.NB, hh = (pl / (a.g_count * a.NB)) % a.H;
-      const int bb = pl / (a.g_count * a.NB * a.H);
-      const int r = i / DC, d = i % DC;
-      const int j = tt * kTcM + r;
-      if (j < a.n_tok) {
-        const uint16_t* xr = a.x + (size_t)bb * a.sb + (size_t)hh * a.sh + (size_t)j * kD + (a.g_begin + gi2) * C;
+  if (warp == kLoadWarp) {
+    // ================= loader: vector rows of tile i -> ring stage i % kAStages ================
+    auto land = [&](int i) {  // tile i's copies by this lane are complete: publish them
+      fence_proxy_async_smem();
+      mbar_arrive(&afull[i % kAStages]);
+    };
+    int i = 0;
+    for (; i < n; ++i) {
+      const int st = i % kAStages;
+      if (i >= kAStages && !__all_sync(0xFFFFFFFFu, enc_wait(&aempty[st], ((i / kAStages) - 1) & 1, failed, a.err)))
+        break;  // warp-uniform
+      const int plane = plane_at(i), t = tile_at(i);
+      const Plane P = plane_of(a, plane);
+      const uint16_t* xb = a.x + (size_t)P.b * a.sb + (size_t)P.h * a.sh + (size_t)(a.g_begin + P.gi) * C;
+      unsigned char* sa = sa0 + st * Lay::kABytes;
+      for (int q = lane; q < kTcM * DC; q += 32) {  // chunk d of row r: coordinates 8d .. 8d + 7
+        const int r = q / DC, d = q % DC, j = t * kTcM + r;
+        const bool in = j < a.n_tok;
+        const uint16_t* xr = xb + (size_t)(in ? j : 0) * kD;
+        unsigned char* dst = sa + op_off(r, d, KC);
         if constexpr (C >= 8) {
-          v = __ldg(reinterpret_cast<const uint4*>(xr + (size_t)(be * TC + (8 * d) / C) * a.st + (8 * d) % C));
-        } else {
-          const uint2 w0 = __ldg(reinterpret_cast<const uint2*>(xr + (size_t)(be * TC + 2 * d) * a.st));
-          const uint2 w1 = __ldg(reinterpret_cast<const uint2*>(xr + (size_t)(be * TC + 2 * d + 1) * a.st));
-          v = make_uint4(w0.x, w0.y, w1.x, w1.y);
+          cp_async16(dst, xr + (size_t)(P.beta * TC + (8 * d) / C) * a.st + (8 * d) % C, in);
+        } else {  // two loop steps of 4 channels
+          cp_async8(dst, xr + (size_t)(P.beta * TC + 2 * d) * a.st, in);
+          cp_async8(dst + 8, xr + (size_t)(P.beta * TC + 2 * d + 1) * a.st, in);
         }
       }
+      cp_async_commit();
+      if (i >= kLoadDepth - 1) {
+        cp_async_wait<kLoadDepth - 1>();
+        land(i - (kLoadDepth - 1));
+      }
     }
-    return v;
-  };
-  uint4 pre = load_chunk(lo);
-  // descriptors of the operands: A buffer 0, codebook part 0 (the others are fixed offsets)
-  const uint64_t a_desc0 = umma_desc(smem_u32(smem + Lay::kOffA), 128, KC * 128);
-  const uint64_t b_desc0 = umma_desc(smem_u32(sb), 128, KC * 128);
-  for (int u = lo; u < hi; ++u, buf ^= 1) {
-    const int plane = u / tiles_per_plane, t = u - plane * tiles_per_plane;
-    const int gi = plane % a.g_count;
-    const int beta = (plane / a.g_count) % a.NB;
-    const int h = (plane / (a.g_count * a.NB)) % a.H;
-    const int b = plane / (a.g_count * a.NB * a.H);
-    if (plane != cur_plane) {  // uniform
-      // ---- codebook of this plane: three bf16 parts with the -||e||^2/2 column ------------
-      // row coordinate k' = 8 c + i (chunk c < DC, i < 8) = m C + i2 is coupled coordinate i2 TC + m
-      g = a.g_begin + gi;
-      cb = a.cb + (((size_t)beta * a.H + h) * Lay::NG + g) * (size_t)kCB * G;
-      out = a.idx + (((size_t)beta * a.max_batch + (a.seq_begin + b)) * a.H + h) * (size_t)a.max_pages * Lay::kPageBytes;
-      __syncthreads();  // the previous plane's MMAs have all been waited for
-      for (int r = tid; r < kTcN; r += kTcThreads) {
-        float nh_hi = 0.f, nh_lo = 0.f;  // |e|^2, compensated
-#pragma unroll 4
-        for (int k = 0; k < G; ++k) add_sq_diff(__ldg(cb + (size_t)r * G + k), 0.f, nh_hi, nh_lo);
-        const float nh = -0.5f * __fadd_rn(nh_hi, nh_lo);
-        // one 16-byte chunk at a time; parts: hi = bf16(v), mid = bf16(v - hi), lo = bf16(v - hi - mid)
-#pragma unroll 1
-        for (int c = 0; c < KC; ++c) {
-          uint32_t w[kParts][4];
-#pragma unroll
-          for (int i2 = 0; i2 < 4; ++i2) {
-            uint16_t pb[kParts][2];
-#pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
-              const int i = 2 * i2 + e2;
-              float v = 0.f;
-              if (c < DC) {
-                const int kk = 8 * c + i;
-                v = __ldg(cb + (size_t)r * G + (kk % C) * TC + kk / C);
-              } else if (c == DC && i == 0) {
-                v = nh;
-              }
-#pragma unroll
-              for (int p = 0; p < kParts; ++p) {
-                const uint16_t bits = bf16_rn_bits(v);
-                pb[p][e2] = bits;
-                v = v - bf16_to_f32(bits);  // exact: v and its bf16 rounding are within 2^-8 |v|
-              }
-            }
-#pragma unroll
-            for (int p = 0; p < kParts; ++p) w[p][i2] = pb[p][0] | ((uint32_t)pb[p][1] << 16);
-          }
+    cp_async_wait<0>();  // nothing of this block's may land after it exits
+    for (int k = max(0, i - (kLoadDepth - 1)); k < i; ++k) land(k);
+  } else if (warp == kMmaWarp) {
+    // ================= MMA issue; codebook restaging at plane changes ==========================
+    const uint64_t a_desc0 = umma_desc(smem_u32(sa0), 128, KC * 128);
+    const uint64_t b_desc0 = umma_desc(smem_u32(sb), 128, KC * 128);
+    int cur_plane = plane_at(0);
+    int last = -1;  // last tile whose MMAs were committed
+    for (int i = 0; i < n; ++i) {
+      const int st = i % kAStages, e = i & 1;
+      const int plane = plane_at(i);
+      if (plane != cur_plane) {
+        // every earlier tile is done with the codebook: its MMAs and its epilogue (near-ties
+        // read the parts)
+        bool ok = true;
+        if (lane == 0) {
+          ok = enc_wait(&bdone[(i - 1) & 1], ((i - 1) >> 1) & 1, failed, a.err);
+          if (ok && i >= 2) ok = enc_wait(&bdone[i & 1], ((i - 2) >> 1) & 1, failed, a.err);
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) break;
+        stage_codebook<TC, C>(a, plane, sb, lane, 32);
+        fence_proxy_async_smem();
+        __syncwarp();
+        cur_plane = plane;
+      }
+      int ok = 1;
+      if (lane == 0) {
+        ok = enc_wait(&afull[st], (i / kAStages) & 1, failed, a.err);
+        if (ok && i >= 2) ok = enc_wait(&accempty[e], ((i >> 1) - 1) & 1, failed, a.err);
+        if (ok) {
+          tc_fence_after();
+          // start addresses advance in 16-byte units in the low descriptor bits (no carry: every
+          // operand lies below 256 KB of shared memory)
 #pragma unroll
           for (int p = 0; p < kParts; ++p)
-            *reinterpret_cast<uint4*>(sb + p * Lay::kBPartBytes + op_off(r, c, KC)) =
-                make_uint4(w[p][0], w[p][1], w[p][2], w[p][3]);
+#pragma unroll
+            for (int s = 0; s < KC / 2; ++s)
+              umma_bf16(tmem + kTcN * e, a_desc0 + (uint64_t)((st * Lay::kABytes + s * 256) >> 4),
+                        b_desc0 + (uint64_t)((p * Lay::kBPartBytes + s * 256) >> 4), (p | s) != 0);
+          umma_commit(&accfull[e]);
+          last = i;
         }
       }
-      cur_plane = plane;
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
     }
-
-    // ---- vector rows of tile t -> A buffer (DC 16-byte chunks per row); the next tile's
-    //      rows are loaded now and land during this tile's work --------------------------------
-    unsigned char* sa = smem + Lay::kOffA + buf * Lay::kABytes;
-    static_assert(kTcM * DC <= kTcThreads, "one chunk per thread");
-    if (tid < kTcM * DC) *reinterpret_cast<uint4*>(sa + op_off(tid / DC, tid % DC, KC)) = pre;
-    pre = load_chunk(u + 1);
-    fence_proxy_async_smem();  // A (and a new codebook) are read by the tensor cores
-    tc_fence_before();
-    __syncthreads();  // operands written; the previous tile's accumulator reads are done
-
-    // ---- one thread: 3 parts x K steps into the accumulator, commit, wait ------------------
-    if (tid == 0 && !*failed) {
+    // the block may only free TMEM once its last MMAs have landed
+    if (lane == 0 && last >= 0) mbar_wait_bounded(&accfull[last & 1], (last >> 1) & 1);
+  } else {
+    // ================= epilogue: warpgroup e takes tiles e, e + 2, ...; a thread owns a row =====
+    // Pass 1: the best acc of the row (3-input max). Pass 2: with thr = best - band, the number
+    // of columns at or above thr and, when that is one, its column, as sum [v >= thr] (1 + col/512)
+    // on the FMA pipe. More than one column in the band: the row is decided on exact distances.
+    const int e = warp >> 2, row = 32 * (warp & 3) + lane;
+    const uint32_t row_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kTcN * e);
+    int ties = 0;
+    for (int i = e; i < n; i += 2) {
+      const int st = i % kAStages;
+      // warp-uniform: the accumulator reads below are warp-collective
+      if (!__all_sync(0xFFFFFFFFu, enc_wait(&accfull[e], (i >> 1) & 1, failed, a.err))) break;
       tc_fence_after();
-      // start addresses advance in 16-byte units in the low descriptor bits (no carry: every
-      // operand lies below 256 KB of shared memory)
+      float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll 1
+      for (int k = 0; k < kTcN / 64; ++k) {
+        float v[64];
+        tmem_ld64(row_addr + 64 * k, v);
 #pragma unroll
-      for (int p = 0; p < kParts; ++p)
-#pragma unroll
-        for (int s = 0; s < KC / 2; ++s)
-          umma_bf16(tmem, a_desc0 + (uint64_t)((buf * Lay::kABytes + s * 256) >> 4),
-                    b_desc0 + (uint64_t)((p * Lay::kBPartBytes + s * 256) >> 4), (p | s) != 0);
-      umma_commit(mma_bar);
-      if (!mbar_wait_bounded(mma_bar, phase)) {
-        *failed = 1;
-        pending = (int)phase;
-        set_error(a.err, KVQ_ERR_TIMEOUT);
+        for (int c = 0; c < 64; c += 8) {
+          m0 = max3f(m0, v[c], v[c + 1]);
+          m1 = max3f(m1, v[c + 2], v[c + 3]);
+          m2 = max3f(m2, v[c + 4], v[c + 5]);
+          m3 = max3f(m3, v[c + 6], v[c + 7]);
+        }
       }
-    }
-    phase ^= 1u;
-    __syncthreads();  // thread 0 saw the accumulator complete (or gave up)
-    tc_fence_after();
-
-    // ---- each warpgroup, its 64 columns of the row: maximum of acc = z.e - |e|^2/2, then the
-    //      columns within the error band of it (a bit mask per 32 columns) --------------------
-    float z2 = 0.f;
+      const float best = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+      const int plane = plane_at(i), t = tile_at(i);
+      const unsigned char* sa = sa0 + st * Lay::kABytes;
+      float z2 = 0.f;
 #pragma unroll
-    for (int c = 0; c < DC; ++c) {
-      const uint4 w = *reinterpret_cast<const uint4*>(sa + op_off(row, c, KC));
-      const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+      for (int c = 0; c < DC; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4*>(sa + op_off(row, c, KC));
+        const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float l = bf16_lo(w4[q]), hh = bf16_hi(w4[q]);
-        z2 = fmaf(l, l, fmaf(hh, hh, z2));
+        for (int q = 0; q < 4; ++q) {
+          const float l = bf16_lo(w4[q]), hh = bf16_hi(w4[q]);
+          z2 = fmaf(l, l, fmaf(hh, hh, z2));
+        }
       }
-    }
-    {
-      float run = -INFINITY, cmax[kQCols / 32];
-      uint32_t mask[kQCols / 32];
-#pragma unroll
-      for (int k = 0; k < kQCols / 32; ++k) {
-        float v[32];
-        tmem_ld32(lane_addr + 32 * k, v);
-        float cm = v[0];
-#pragma unroll
-        for (int i = 1; i < 32; ++i) cm = fmaxf(cm, v[i]);
-        run = fmaxf(run, cm);
-        const float thr = run - acc_band<KC>(z2, run);
-        uint32_t mk = 0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) mk |= (v[i] >= thr) ? (1u << i) : 0u;
-        cmax[k] = cm;
-        mask[k] = mk;
-      }
-      Quarter qr;
-      qr.best = run;
-      qr.band = acc_band<KC>(z2, run);
-      qr.count = 0;
-      qr.first = kTcN;
-#pragma unroll
-      for (int k = kQCols / 32 - 1; k >= 0; --k) {  // a chunk far below the maximum has no candidate
-        if (cmax[k] < run - qr.band) continue;
-        qr.count += __popc(mask[k]);
-        if (mask[k]) qr.first = kQCols * wg + 32 * k + __ffs(mask[k]) - 1;
-      }
-      part[row * 4 + wg] = qr;
-    }
-    tc_fence_before();
-    __syncthreads();  // the four quarters of every row are in shared memory
-
-    // ---- warpgroup 0: merge the quarters; one candidate is the answer, several are decided
-    //      on compensated distances --------------------------------------------------------------
-    if (wg == 0) {
-      float best = -INFINITY;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) best = fmaxf(best, part[row * 4 + q].best);
       const float band = acc_band<KC>(z2, best);
-      int count = 0, first = kTcN;
+      const float thr = best - band;
+      const float cth = fmaf(-thr, 1.2379400392853803e27f, 1.0f);
+      // per 64-column chunk k: sum [v >= thr] (1 + c/512), c the column within the chunk; the
+      // whole row's tally is below 1.5 exactly when one column is in the band, and then the
+      // chunk holding it has a sum of 1 + c/512
+      float tally = 0.f, ksum = 0.f;
+      int ksel = 0;
+#pragma unroll 1
+      for (int k = 0; k < kTcN / 64; ++k) {
+        float v[64];
+        tmem_ld64(row_addr + 64 * k, v);
+        float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {  // each quarter's band is at least this one: its mask covers
-        const Quarter o = part[row * 4 + q];
-        if (o.best < best - band) continue;
-        count += o.count;
-        first = min(first, o.first);
+        for (int c = 0; c < 64; c += 4) {
+          const float2 f01 = make_float2(at_least(v[c], cth), at_least(v[c + 1], cth));
+          const float2 f23 = make_float2(at_least(v[c + 2], cth), at_least(v[c + 3], cth));
+          s01 = __ffma2_rn(f01, make_float2(1.f + c / 512.f, 1.f + (c + 1) / 512.f), s01);
+          s23 = __ffma2_rn(f23, make_float2(1.f + (c + 2) / 512.f, 1.f + (c + 3) / 512.f), s23);
+        }
+        const float sk = (s01.x + s01.y) + (s23.x + s23.y);
+        if (sk > 0.5f) {
+          ksel = k;
+          ksum = sk;
+        }
+        tally += sk;
       }
       const int j = t * kTcM + row;
       const bool valid = j < a.n_tok;
-      const bool need = valid && !*failed && count > 1;
-      struct { float best; int col; } m = {best, first};
-      int result = m.col;
-      if (__any_sync(0xFFFFFFFFu, need)) {
+      const bool need = valid && !*failed && !(tally < 1.5f);
+      int result = 64 * ksel + __float2int_rn((ksum - 1.f) * 512.f);
+      uint32_t cand[kTcN / 32];  // candidate masks of this row (need only)
+#pragma unroll
+      for (int q = 0; q < kTcN / 32; ++q) cand[q] = 0;
+      const bool any_need = __any_sync(0xFFFFFFFFu, need);
+      if (any_need) {
+#pragma unroll
+        for (int q = 0; q < kTcN / 32; ++q) {
+          float v[32];
+          tmem_ld32(row_addr + 32 * q, v);  // warp-wide load: every lane takes part
+#pragma unroll
+          for (int b = 0; b < 32; ++b) cand[q] |= (v[b] >= thr) ? (1u << b) : 0u;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&accempty[e]);  // the accumulator is read: the next MMAs may go
+      if (any_need) {
         // every candidate in the band, decided on compensated fp32 distances (lowest index wins
         // exact ties); a runner-up within 1e-6 of the best is reported as a tie
         float bd = INFINITY, sd = INFINITY;
-        int bdi = m.col;
-        const uint32_t row_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-#pragma unroll 1
-        for (int c0 = 0; c0 < kTcN; c0 += 32) {
-          uint32_t cand = 0;  // columns of this chunk inside the band
-          {
-            float v[32];
-            tmem_ld32(row_addr + c0, v);  // warp-wide load: every lane takes part
+        int bdi = result;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) cand |= (v[i] >= m.best - band) ? (1u << i) : 0u;
-          }
-          if (!need) cand = 0;
-          while (cand) {
-            const int r = c0 + __ffs(cand) - 1;
-            cand &= cand - 1;
+        for (int q = 0; q < kTcN / 32; ++q) {
+          uint32_t cm = need ? cand[q] : 0u;
+          while (cm) {
+            const int r = 32 * q + __ffs(cm) - 1;
+            cm &= cm - 1;
             // e = hi + mid + lo exactly (each residual is a multiple of e's ulp that fits the
             // next part), so the staged parts give the fp32 entries back
             float dh = 0.f, dl = 0.f;
@@ -408,9 +538,9 @@ __global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(c
               const uint32_t h4[4] = {e0.x, e0.y, e0.z, e0.w}, m4[4] = {e1.x, e1.y, e1.z, e1.w},
                              l4[4] = {e2.x, e2.y, e2.z, e2.w};
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                add_sq_diff(bf16_lo(w4[q]), __fadd_rn(__fadd_rn(bf16_lo(h4[q]), bf16_lo(m4[q])), bf16_lo(l4[q])), dh, dl);
-                add_sq_diff(bf16_hi(w4[q]), __fadd_rn(__fadd_rn(bf16_hi(h4[q]), bf16_hi(m4[q])), bf16_hi(l4[q])), dh, dl);
+              for (int q2 = 0; q2 < 4; ++q2) {
+                add_sq_diff(bf16_lo(w4[q2]), __fadd_rn(__fadd_rn(bf16_lo(h4[q2]), bf16_lo(m4[q2])), bf16_lo(l4[q2])), dh, dl);
+                add_sq_diff(bf16_hi(w4[q2]), __fadd_rn(__fadd_rn(bf16_hi(h4[q2]), bf16_hi(m4[q2])), bf16_hi(l4[q2])), dh, dl);
               }
             }
             const float dd = __fadd_rn(dh, dl);
@@ -428,16 +558,25 @@ __global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(c
           ties += (sd <= bd * (1.f + 1e-6f)) ? 1 : 0;
         }
       }
-      if (valid && !*failed)
-        out[(size_t)(a.page_begin + j / kPage) * Lay::kPageBytes + page_byte(g, j % kPage, Lay::NG)] = (uint8_t)result;
+      if (valid && !*failed) {
+        const Plane P = plane_of(a, plane);
+        uint8_t* out = a.idx + (((size_t)P.beta * a.max_batch + (a.seq_begin + P.b)) * a.H + P.h) *
+                                   (size_t)a.max_pages * Lay::kPageBytes;
+        out[(size_t)(a.page_begin + j / kPage) * Lay::kPageBytes + page_byte(a.g_begin + P.gi, j % kPage, Lay::NG)] =
+            (uint8_t)result;
+      }
+      __syncwarp();
+      if (lane == 0) {  // this warp is done with the vector rows and the codebook
+        mbar_arrive(&aempty[st]);
+        mbar_arrive(&bdone[e]);
+      }
     }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) ties += __shfl_xor_sync(0xFFFFFFFFu, ties, off);
+    if (lane == 0 && ties && a.n_ties) atomicAdd(a.n_ties, ties);
   }
 
-  // ---- tie count, then free TMEM (after the last MMA has landed) --------------------------
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) ties += __shfl_xor_sync(0xFFFFFFFFu, ties, off);
-  if (lane == 0 && ties && a.n_ties) atomicAdd(a.n_ties, ties);
-  if (tid == 0 && pending >= 0) mbar_wait_bounded(mma_bar, (uint32_t)pending);  // an MMA still in flight
+  // ---- free TMEM once every warp is out of its loop (the MMA warp saw its last MMAs land) ----
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -449,16 +588,18 @@ __global__ void __launch_bounds__(kTcThreads, kTcBlocksPerSm) encode_tc_kernel(c
 template <int TC, int C>
 cudaError_t launch_tc(const VqEncodeArgs& a, cudaStream_t s) {
   using Lay = TcLayout<TC, C>;
-  cudaError_t e = cudaFuncSetAttribute(encode_tc_kernel<TC, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
+  cudaError_t e =
+      cudaFuncSetAttribute(encode_tc_kernel<TC, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemLaunch);
   if (e != cudaSuccess) return e;
-  const long long planes = (long long)a.n_seq * a.H * a.NB * a.g_count;
   const int tiles = (a.n_tok + kTcM - 1) / kTcM;
-  const long long U = planes * tiles;
-  if (U >= (1ll << 31)) return cudaErrorInvalidValue;
+  const long long U = (long long)a.n_seq * a.H * a.NB * tiles;  // (sequence, head, beta, tile) slots
+  if (U * a.g_count >= (1ll << 31)) return cudaErrorInvalidValue;
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long blocks = std::min<long long>(U, (long long)kTcBlocksPerSm * sms);
-  encode_tc_kernel<TC, C><<<(unsigned)blocks, kTcThreads, Lay::kSmem, s>>>(a, (int)U, tiles);
+  // sets of g_count blocks (one per group), as many as fit one block per SM and have slots
+  const long long sets = std::max(1ll, std::min<long long>(U, sms / std::max(1, a.g_count)));
+  const long long blocks = sets * a.g_count;
+  encode_tc_kernel<TC, C><<<(unsigned)blocks, kEncThreads, Lay::kSmemLaunch, s>>>(a, (int)U, tiles);
   return cudaGetLastError();
 }
 

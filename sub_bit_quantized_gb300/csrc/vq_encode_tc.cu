@@ -119,24 +119,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // 64 consecutive fp32 columns of this thread's TMEM lane: two loads, one wait
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   uint32_t r[64];
@@ -475,6 +457,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
       // chunk holding it has a sum of 1 + c/512
       float tally = 0.f, ksum = 0.f;
       int ksel = 0;
+      uint32_t kmask = 0;  // chunks holding a column in the band
 #pragma unroll 1
       for (int k = 0; k < kTcN / 64; ++k) {
         float v[64];
@@ -491,6 +474,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
         if (sk > 0.5f) {
           ksel = k;
           ksum = sk;
+          kmask |= 1u << k;
         }
         tally += sk;
       }
@@ -502,13 +486,20 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
 #pragma unroll
       for (int q = 0; q < kTcN / 32; ++q) cand[q] = 0;
       const bool any_need = __any_sync(0xFFFFFFFFu, need);
-      if (any_need) {
+      if (any_need) {  // candidate masks, reading only the chunks some row of the warp needs
 #pragma unroll
-        for (int q = 0; q < kTcN / 32; ++q) {
-          float v[32];
-          tmem_ld32(row_addr + 32 * q, v);  // warp-wide load: every lane takes part
+        for (int k = 0; k < kTcN / 64; ++k) {
+          const bool mine = need && ((kmask >> k) & 1u);
+          if (!__any_sync(0xFFFFFFFFu, mine)) continue;  // warp-uniform
+          float v[64];
+          tmem_ld64(row_addr + 64 * k, v);  // warp-wide load: every lane takes part
+          if (mine) {
 #pragma unroll
-          for (int b = 0; b < 32; ++b) cand[q] |= (v[b] >= thr) ? (1u << b) : 0u;
+            for (int b = 0; b < 32; ++b) {
+              cand[2 * k] |= (v[b] >= thr) ? (1u << b) : 0u;
+              cand[2 * k + 1] |= (v[32 + b] >= thr) ? (1u << b) : 0u;
+            }
+          }
         }
       }
       tc_fence_before();

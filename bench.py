@@ -345,6 +345,10 @@ PROFILED_TRAFFIC = {
         "sub_bit_quantized_gb300/csrc/kivi.cu",
         "0474bba73e3cf49c0a5e6860728af987755220c7d31cf08b8ff9430cae00d5f5",
         228799488 + 4636928),
+    "encode_32k:encode_tc_kernel": (
+        "sub_bit_quantized_gb300/csrc/vq_encode_tc.cu",
+        "ef1de63a1e981fbaffcca621d390e0766bde42fc23fb6dc9dd5c7249efe9c38c",
+        287318784 + 14957568),
     "kivi4_gqa_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
         "0474bba73e3cf49c0a5e6860728af987755220c7d31cf08b8ff9430cae00d5f5",
@@ -645,7 +649,8 @@ def run_ours(args, wl, rank, world, dist, pool):
                            roofline={"bound": "tensor", "achieved": round(flops / (ms * 1e-3) / 1e12, 2),
                                      "peak": tc_peak, "unit": "TFLOP/s",
                                      "frac": round(flops / (ms * 1e-3) / 1e12 / tc_peak, 4),
-                                     "traffic": None, "peak_source": tc_src, "kernel": "encode_tc_kernel"}))
+                                     "traffic": profiled_traffic(args.workload, "encode_tc_kernel"),
+                                     "peak_source": tc_src, "kernel": "encode_tc_kernel"}))
         return result
 
     if wl["kind"] == "kivi_quant":

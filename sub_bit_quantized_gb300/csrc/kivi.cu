@@ -290,10 +290,15 @@ __global__ void __launch_bounds__(128) kivi_append_kernel(const KiviAppendArgs a
 constexpr int kAThreads = 256;
 constexpr int kAWarps = kAThreads / 32;
 constexpr int kAChunk = 128;  // tokens per ring stage (4 key groups of 32)
-constexpr int kAStages = 4;
 
 template <int KB, int VB, int RH>
 struct AttnLayout {
+  // ring depth: 4 stages of 12 KB at 2 bits; 3 of up to 20 KB at 4 bits, so that three blocks
+  // of the multi-head-group variants fit an SM
+  static constexpr int kAStages = (KB + VB >= 6) ? 3 : 4;
+  // resident blocks per SM the register budget targets with several query heads (2-bit
+  // values with four heads hold 64 accumulators a thread and keep two); one head: no bound
+  static constexpr int kMinBlocks = (RH == 1) ? 0 : (VB == 2 && RH == 4) ? 2 : 3;
   static constexpr int kKRow = kD * KB / 8;               // key code bytes per token
   static constexpr int kVRow = kD * VB / 8;               // value code bytes per token
   static constexpr int kCKc = 0;                          // stage layout (bytes)
@@ -354,7 +359,7 @@ __device__ __forceinline__ bool kivi_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 template <int KB, int VB, int RH>
-__global__ void __launch_bounds__(kAThreads) kivi_attn_kernel(const KiviAttnArgs a, const float scale_log2,
+__global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks) kivi_attn_kernel(const KiviAttnArgs a, const float scale_log2,
                                                               const int sc_stride) {
   using L = AttnLayout<KB, VB, RH>;
   extern __shared__ __align__(128) unsigned char sma[];
@@ -364,7 +369,7 @@ __global__ void __launch_bounds__(kAThreads) kivi_attn_kernel(const KiviAttnArgs
   float* red = reinterpret_cast<float*>(sma + L::kOffRed);
   int* flag = reinterpret_cast<int*>(red + kAWarps * RH);
   uint64_t* full = reinterpret_cast<uint64_t*>(sma + L::kOffBar);
-  volatile int* failed = reinterpret_cast<volatile int*>(sma + L::kOffBar + kAStages * 8);
+  volatile int* failed = reinterpret_cast<volatile int*>(sma + L::kOffBar + L::kAStages * 8);
   float* sc = reinterpret_cast<float*>(sma + L::kOffSc);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rep = a.Hq / a.H, n_sub = rep / RH;
@@ -378,7 +383,7 @@ __global__ void __launch_bounds__(kAThreads) kivi_attn_kernel(const KiviAttnArgs
   const int NQV = (R > 0) ? min(max(a.n_quant_v[b], 0), NQK) : NQK;
   for (int i = tid; i < RH * kD; i += kAThreads) qs[i] = bf16_to_f32(a.q[bq0 * kD + i]);
   if (tid == 0) {
-    for (int s = 0; s < kAStages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < L::kAStages; ++s) mbar_init(&full[s], 1);
     *failed = 0;
     fence_mbar_init();
   }
@@ -424,7 +429,7 @@ __global__ void __launch_bounds__(kAThreads) kivi_attn_kernel(const KiviAttnArgs
     const size_t tok0 = bh * a.max_tokens;              // token row base of (b, hk)
     const size_t grp0 = bh * (a.max_tokens / kGroup);   // key group row base of (b, hk)
     auto produce = [&](int c) {                         // thread 0
-      const int st = c % kAStages;
+      const int st = c % L::kAStages;
       unsigned char* dst = sma + st * L::kStage;
       const int t = t0 + c * kAChunk;
       const int n = min(kAChunk, t1 - t), ng = n / kGroup;
@@ -438,14 +443,14 @@ __global__ void __launch_bounds__(kAThreads) kivi_attn_kernel(const KiviAttnArgs
     };
     int issued = 0;  // thread 0
     if (tid == 0)
-      for (int c = 0; c < min(kAStages, n_chunks); ++c) {
+      for (int c = 0; c < min(L::kAStages, n_chunks); ++c) {
         produce(c);
         ++issued;
       }
 
     for (int c = 0; c < n_chunks; ++c) {
-      const int st = c % kAStages;
-      kivi_wait(&full[st], (c / kAStages) & 1, failed, a.err);
+      const int st = c % L::kAStages;
+      kivi_wait(&full[st], (c / L::kAStages) & 1, failed, a.err);
       const unsigned char* stage = sma + st * L::kStage;
       const int tc0 = t0 + c * kAChunk;  // token of chunk row 0
       const int n = min(kAChunk, t1 - tc0), ng = n / kGroup;
@@ -588,14 +593,14 @@ __global__ void __launch_bounds__(kAThreads) kivi_attn_kernel(const KiviAttnArgs
         }
       }
       __syncthreads();  // every thread is done with this stage
-      if (tid == 0 && c + kAStages < n_chunks && !*failed) {
-        produce(c + kAStages);
+      if (tid == 0 && c + L::kAStages < n_chunks && !*failed) {
+        produce(c + L::kAStages);
         ++issued;
       }
     }
     // after a timed-out wait, let this block's copies still in flight land first
     if (tid == 0 && *failed)
-      for (int c = max(0, issued - kAStages); c < issued; ++c) mbar_wait_bounded(&full[c % kAStages], (c / kAStages) & 1);
+      for (int c = max(0, issued - L::kAStages); c < issued; ++c) mbar_wait_bounded(&full[c % L::kAStages], (c / L::kAStages) & 1);
   } else {
     // ================================ fp16 key residual =====================================
     const int NR = max(0, min(a.n_tok[b] - NQK, R));

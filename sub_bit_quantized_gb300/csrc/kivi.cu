@@ -296,9 +296,10 @@ struct AttnLayout {
   // ring depth: 4 stages of 12 KB at 2 bits; 3 of up to 20 KB at 4 bits, so that three blocks
   // of the multi-head-group variants fit an SM
   static constexpr int kAStages = (KB + VB >= 6) ? 3 : 4;
-  // resident blocks per SM the register budget targets with several query heads (2-bit
-  // values with four heads hold 64 accumulators a thread and keep two); one head: no bound
-  static constexpr int kMinBlocks = (RH == 1) ? 0 : (VB == 2 && RH == 4) ? 2 : 3;
+  // resident blocks per SM the register budget targets: four with one query head and 2-bit
+  // codes (64 registers), three otherwise, two for 2-bit values with four heads (64
+  // accumulators a thread)
+  static constexpr int kMinBlocks = (RH == 1) ? ((KB + VB == 4) ? 4 : 3) : (VB == 2 && RH == 4) ? 2 : 3;
   static constexpr int kKRow = kD * KB / 8;               // key code bytes per token
   static constexpr int kVRow = kD * VB / 8;               // value code bytes per token
   static constexpr int kCKc = 0;                          // stage layout (bytes)
@@ -311,15 +312,21 @@ struct AttnLayout {
   static constexpr int kOffQ = kAStages * kStage;         // float q [RH][128]
   static constexpr int kOffQf = kOffQ + RH * kD * 4;      // float q' [RH][4 groups][128]
   static constexpr int kOffBias = kOffQf + RH * 4 * kD * 4;  // float [RH][4 groups][2 halves]
-  static constexpr int kOffRed = kOffBias + RH * 8 * 4;      // float [8 warps][RH] + flag
-  static constexpr int kOffBar = kOffRed + ((kAWarps * RH + 4) * 4 + 15) / 16 * 16;  // mbarriers + failed
+  // float l [8 warps][RH], float M [8 warps][RH], int flag, int released [stages], int issued
+  static constexpr int kOffRed = kOffBias + RH * 8 * 4;
+  static constexpr int kOffBar = kOffRed + ((2 * kAWarps * RH + 2 + kAStages) * 4 + 15) / 16 * 16;  // mbarriers + failed
   static constexpr int kOffSc = kOffBar + 64;             // float scores [RH][max(128, residual)]
-  // value phase: a warp-step covers TS tokens, a lane one code word of VPW channels
+  // value phase: a lane takes kLW code words of one token, all in one value group (with one
+  // query head the whole group, so its scale and zero-point are read once); a warp-step
+  // covers kTS tokens
   static constexpr int kVW = kVRow / 4;                   // code words per token
-  static constexpr int kTS = 32 / kVW;                    // tokens per warp-step
   static constexpr int kCPWv = 32 / VB;                   // value channels per word
   static constexpr int kPV = kCPWv / 2;                   // channel pairs per word
   static constexpr int kWPG = kGroup / kCPWv;             // words per value group
+  static constexpr int kLW = (RH == 1 && VB == 4) ? kWPG : 1;  // words per lane
+  static constexpr int kLPT = kVW / kLW;                  // lanes per token
+  static constexpr int kTS = 32 / kLPT;                   // tokens per warp-step
+  static constexpr int kOV = kLW * kCPWv;                 // value accumulators per lane and head
   // score phase: a lane covers 64 channels of one token
   static constexpr int kKW = kKRow / 8;                   // key code words per half token
   static constexpr int kPK = 16 / KB;                     // channel pairs per key word
@@ -328,14 +335,49 @@ struct AttnLayout {
 };
 
 // Codes j and j + 16/b (j < 16/b) of a 32-bit word of b-bit codes, each as (code * 2^(b j))
-// in fp32: the code is masked in place, placed in the mantissa of 2^23 and 2^23 is
-// subtracted, all exact. One integer op per code and one packed add per pair instead of
-// shift + int-to-float conversion; the 2^(-b j) scale is folded into the other operand.
+// in fp32: the code is masked in place inside the mantissa of 2^23 and 2^23 is subtracted,
+// all exact. A byte permute puts each 16-bit half of the word under the exponent of 2^23
+// once per word (magic_lo / magic_hi); then every code costs one AND with an immediate and
+// every pair one packed add, instead of shift + int-to-float conversion. The 2^(-b j) scale
+// is folded into the other operand.
+constexpr uint32_t kMagic = 0x4B000000u;  // 2^23
+__device__ __forceinline__ uint32_t magic_lo(uint32_t w) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, 0x7410;" : "=r"(r) : "r"(w), "r"(kMagic));
+  return r;
+}
+__device__ __forceinline__ uint32_t magic_hi(uint32_t w) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, 0x7432;" : "=r"(r) : "r"(w), "r"(kMagic));
+  return r;
+}
 template <int BITS>
-__device__ __forceinline__ float2 code_pair(uint32_t w, uint32_t w_hi, int j) {
-  const uint32_t m = ((1u << BITS) - 1u) << (BITS * j);
-  const float2 f = make_float2(__uint_as_float((w & m) | 0x4B000000u), __uint_as_float((w_hi & m) | 0x4B000000u));
+__device__ __forceinline__ float2 code_pair(uint32_t ml, uint32_t mh, int j) {
+  const uint32_t m = (((1u << BITS) - 1u) << (BITS * j)) | kMagic;
+  const float2 f = make_float2(__uint_as_float(ml & m), __uint_as_float(mh & m));
   return __fadd2_rn(f, make_float2(-8388608.f, -8388608.f));
+}
+template <bool B>
+struct BoolTag {
+  static constexpr bool value = B;
+};
+// barrier of the two warps 2g and 2g + 1 (named barrier 1 + g, 64 threads)
+__device__ __forceinline__ void pair_sync(int g) {
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + g) : "memory");
+}
+// K consecutive 32-bit words from shared memory (p aligned to 4 K bytes)
+template <int K>
+__device__ __forceinline__ void load_words(const unsigned char* p, uint32_t (&w)[K]) {
+  if constexpr (K == 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else if constexpr (K == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    w[0] = v.x; w[1] = v.y;
+  } else {
+    static_assert(K == 1, "1, 2 or 4 words");
+    w[0] = *reinterpret_cast<const uint32_t*>(p);
+  }
 }
 __device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
 __device__ __forceinline__ float pow2_pos(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
@@ -366,8 +408,11 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
   float* qs = reinterpret_cast<float*>(sma + L::kOffQ);
   float* qf = reinterpret_cast<float*>(sma + L::kOffQf);
   float* bias = reinterpret_cast<float*>(sma + L::kOffBias);
-  float* red = reinterpret_cast<float*>(sma + L::kOffRed);
-  int* flag = reinterpret_cast<int*>(red + kAWarps * RH);
+  float* red = reinterpret_cast<float*>(sma + L::kOffRed);  // l per warp and head
+  float* redm = red + kAWarps * RH;                          // running max per warp and head
+  int* flag = reinterpret_cast<int*>(redm + kAWarps * RH);
+  int* released = flag + 1;                                  // warps done with a stage's chunk
+  int* issued = released + L::kAStages;                      // chunks whose copies were issued
   uint64_t* full = reinterpret_cast<uint64_t*>(sma + L::kOffBar);
   volatile int* failed = reinterpret_cast<volatile int*>(sma + L::kOffBar + L::kAStages * 8);
   float* sc = reinterpret_cast<float*>(sma + L::kOffSc);
@@ -383,30 +428,34 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
   const int NQV = (R > 0) ? min(max(a.n_quant_v[b], 0), NQK) : NQK;
   for (int i = tid; i < RH * kD; i += kAThreads) qs[i] = bf16_to_f32(a.q[bq0 * kD + i]);
   if (tid == 0) {
-    for (int s = 0; s < L::kAStages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < L::kAStages; ++s) {
+      mbar_init(&full[s], 1);
+      released[s] = 0;
+    }
+    *issued = 0;
     *failed = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
   // running softmax state per query head; the max is block-wide
-  // quantized blocks: lane holds the kCPWv channels of code word lane % kVW of its token slot;
-  // the residual block: channels 4 lane .. 4 lane + 3 in o[r][0..3]
+  // quantized blocks: lane holds the kOV channels of code words kLW (lane % kLPT) .. + kLW - 1
+  // of its token slot; the residual block: channels 4 lane .. 4 lane + 3 in o[r][0..3]
   float M[RH], l[RH], oz[RH];
-  float o[RH][L::kCPWv];
+  float o[RH][L::kOV];
 #pragma unroll
   for (int r = 0; r < RH; ++r) {
     M[r] = -INFINITY;
     l[r] = 0.f;
     oz[r] = 0.f;
 #pragma unroll
-    for (int i = 0; i < L::kCPWv; ++i) o[r][i] = 0.f;
+    for (int i = 0; i < L::kOV; ++i) o[r][i] = 0.f;
   }
   // raise head r's running max to Mn
   auto rescale_to = [&](int r, float Mn) {
     const float f = (M[r] == -INFINITY) ? 0.f : exp2f(M[r] - Mn);
 #pragma unroll
-    for (int i = 0; i < L::kCPWv; ++i) o[r][i] *= f;
+    for (int i = 0; i < L::kOV; ++i) o[r][i] *= f;
     oz[r] *= f;
     l[r] *= f;
     M[r] = Mn;
@@ -441,23 +490,28 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
       bulk_g2s(dst + L::kCVs, a.v_scale + (tok0 + t) * 4, n * 8, &full[st]);
       bulk_g2s(dst + L::kCVz, a.v_zero + (tok0 + t) * 4, n * 8, &full[st]);
     };
-    int issued = 0;  // thread 0
-    if (tid == 0)
-      for (int c = 0; c < min(L::kAStages, n_chunks); ++c) {
-        produce(c);
-        ++issued;
-      }
+    if (tid == 0) {
+      for (int c = 0; c < min(L::kAStages, n_chunks); ++c) produce(c);
+      *issued = min(L::kAStages, n_chunks);
+    }
 
+    // Every warp works on its 16 tokens of each chunk (half of one key group) with a
+    // warp-local online softmax; the two warps of a group share its q' and bias (each builds
+    // one channel half; a 64-thread named barrier per pair before and after), warps meet only
+    // at the end, and the last warp done with a stage refills it.
+    const int tb = 16 * warp, g = warp >> 1, hf = warp & 1;
+    const int tk = tb + (lane & 15), chh = lane >> 4;  // score phase: token, channel half
     for (int c = 0; c < n_chunks; ++c) {
       const int st = c % L::kAStages;
-      kivi_wait(&full[st], (c / L::kAStages) & 1, failed, a.err);
+      kivi_wait(&full[st], (c / L::kAStages) & 1, failed, a.err);  // a timeout leaves stale data: harmless, reported
       const unsigned char* stage = sma + st * L::kStage;
       const int tc0 = t0 + c * kAChunk;  // token of chunk row 0
-      const int n = min(kAChunk, t1 - tc0), ng = n / kGroup;
-      // ---- q' = q s per key group (the scale folds into the query) and bias = -sum q' z ----
-      {
-        const int g = warp >> 1, hf = warp & 1;
-        if (g < ng) {
+      const int n = min(kAChunk, t1 - tc0);  // a multiple of 32: both warps of a group have all 16 tokens or none
+      if (tb < n) {
+        // ---- q' = q s per key group (the scale folds into the query) and bias = -sum q' z:
+        //      warp hf builds channels 64 hf .. 64 hf + 63 ----
+        pair_sync(g);  // the partner is done reading the previous chunk's q'
+        {
           const int ch = 64 * hf + 2 * lane;
           const uint32_t s2 = *reinterpret_cast<const uint32_t*>(stage + L::kCKs + (g * kD + ch) * 2);
           const uint32_t z2 = *reinterpret_cast<const uint32_t*>(stage + L::kCKz + (g * kD + ch) * 2);
@@ -476,13 +530,10 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
             if (lane == 0) bias[(r * 4 + g) * 2 + hf] = pb;
           }
         }
-      }
-      __syncthreads();
-      // ---- scores: warp (group, 16 tokens), lanes 0-15 channels 0-63, lanes 16-31 64-127 ----
-      {
-        const int g = warp >> 1;
-        if (g < ng) {
-          const int tk = 32 * g + 16 * (warp & 1) + (lane & 15), chh = lane >> 4;
+        pair_sync(g);  // both halves written
+        // ---- scores: lanes 0-15 channels 0-63 of token tb + lane, lanes 16-31 channels 64-127 ----
+        float pk[RH];
+        {
           uint32_t wds[L::kKW];
 #pragma unroll
           for (int k4 = 0; k4 < L::kKW / 4; ++k4) {
@@ -497,10 +548,10 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
           for (int r = 0; r < RH; ++r) acc2[r] = make_float2(0.f, 0.f);
 #pragma unroll
           for (int k = 0; k < L::kKW; ++k) {
-            const uint32_t w_hi = wds[k] >> 16;
+            const uint32_t ml = magic_lo(wds[k]), mh = magic_hi(wds[k]);
 #pragma unroll
             for (int j = 0; j < L::kPK; ++j) {
-              const float2 cp = code_pair<KB>(wds[k], w_hi, j);
+              const float2 cp = code_pair<KB>(ml, mh, j);
 #pragma unroll
               for (int r = 0; r < RH; ++r) {
                 const float2* q2 = reinterpret_cast<const float2*>(qf + (r * 4 + g) * kD + 64 * chh);
@@ -508,99 +559,113 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
               }
             }
           }
+          // ---- warp-local online softmax over the 16 tokens (lanes l and l + 16 share one) ----
 #pragma unroll
           for (int r = 0; r < RH; ++r) {
-            float acc = acc2[r].x + acc2[r].y;
-            acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 16);
-            if (chh == 0) sc[r * sc_stride + tk] = (acc + bias[(r * 4 + g) * 2] + bias[(r * 4 + g) * 2 + 1]) * scale_log2;
+            float sc_r = acc2[r].x + acc2[r].y;
+            sc_r += __shfl_xor_sync(0xFFFFFFFFu, sc_r, 16);
+            sc_r = (sc_r + bias[(r * 4 + g) * 2] + bias[(r * 4 + g) * 2 + 1]) * scale_log2;
+            float mx = sc_r;
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+            if (mx > M[r]) rescale_to(r, mx);  // warp-uniform
+            pk[r] = exp2f(sc_r - M[r]);
+            float ls = pk[r];
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, off);
+            l[r] += ls;
           }
         }
-      }
-      __syncthreads();
-      // ---- online softmax, then values: warp w takes tokens 16w .. 16w + 15, kTS at a time;
-      //      lane: token slot lane / kVW, code word lane % kVW (value group word / kWPG) ----
+        // ---- values: kTS tokens of the warp per step ----
+        const int lt = lane % L::kLPT, ts = lane / L::kLPT;
+        const int w0 = lt * L::kLW, gv = w0 / L::kWPG;  // the lane's first code word, its value group
+        // kFull: every token of the warp has a quantized value, so the steps need no per-token
+        // test (warp-uniform; only the streaming cache's tail takes the checked path)
+        auto value_steps = [&](auto full_tag) {
+          constexpr bool kFull = decltype(full_tag)::value;
 #pragma unroll
-      for (int r = 0; r < RH; ++r) {
-        const float Mn = fmaxf(M[r], scores_max(sc + r * sc_stride, n));
-        if (Mn > M[r]) rescale_to(r, Mn);
-      }
-      {
-        const int tb = 16 * warp;
-        float pk[RH];
+          for (int step = 0; step < 16 / L::kTS; ++step) {
+            float p[RH];
 #pragma unroll
-        for (int r = 0; r < RH; ++r) {
-          pk[r] = (tb + (lane & 15) < n) ? exp2f(sc[r * sc_stride + tb + (lane & 15)] - M[r]) : 0.f;
-          float ls = (lane < 16) ? pk[r] : 0.f;
-#pragma unroll
-          for (int off = 8; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, off);
-          l[r] += __shfl_sync(0xFFFFFFFFu, ls, 0);
-        }
-        const int lw = lane % L::kVW, ts = lane / L::kVW, gv = lw / L::kWPG;
-#pragma unroll
-        for (int step = 0; step < 16 / L::kTS; ++step) {
-          float p[RH];
-#pragma unroll
-          for (int r = 0; r < RH; ++r) p[r] = __shfl_sync(0xFFFFFFFFu, pk[r], L::kTS * step + ts);
-          const int tk = tb + L::kTS * step + ts;
-          if (tk >= n) continue;
-          if (tc0 + tk < NQV) {
-            const uint32_t wv = *reinterpret_cast<const uint32_t*>(stage + L::kCVc + tk * L::kVRow + 4 * lw);
-            const float sv = h2f(*reinterpret_cast<const uint16_t*>(stage + L::kCVs + (tk * 4 + gv) * 2));
-            const float zv = h2f(*reinterpret_cast<const uint16_t*>(stage + L::kCVz + (tk * 4 + gv) * 2));
-            float2 w2[RH];
-#pragma unroll
-            for (int r = 0; r < RH; ++r) {
-              const float wgt = p[r] * sv;
-              oz[r] = fmaf(wgt, zv, oz[r]);
-              w2[r] = make_float2(wgt, wgt);
-            }
-            const uint32_t wv_hi = wv >> 16;
-#pragma unroll
-            for (int j = 0; j < L::kPV; ++j) {  // (channel j, channel kPV + j) of the word, x 2^(b j)
-              const float2 cp = code_pair<VB>(wv, wv_hi, j);
+            for (int r = 0; r < RH; ++r) p[r] = __shfl_sync(0xFFFFFFFFu, pk[r], L::kTS * step + ts);
+            const int tv = tb + L::kTS * step + ts;
+            if (kFull || tc0 + tv < NQV) {
+              uint32_t wv[L::kLW];
+              load_words<L::kLW>(stage + L::kCVc + tv * L::kVRow + 4 * w0, wv);
+              const float sv = h2f(*reinterpret_cast<const uint16_t*>(stage + L::kCVs + (tv * 4 + gv) * 2));
+              const float zv = h2f(*reinterpret_cast<const uint16_t*>(stage + L::kCVz + (tv * 4 + gv) * 2));
+              float2 w2[RH];
 #pragma unroll
               for (int r = 0; r < RH; ++r) {
-                const float2 acc = __ffma2_rn(w2[r], cp, make_float2(o[r][2 * j], o[r][2 * j + 1]));
-                o[r][2 * j] = acc.x;
-                o[r][2 * j + 1] = acc.y;
+                const float wgt = p[r] * sv;
+                oz[r] = fmaf(wgt, zv, oz[r]);
+                w2[r] = make_float2(wgt, wgt);
               }
-            }
-          } else {  // key quantized, value still in the fp16 window
-            const int t = tc0 + tk;
-            const uint4* vr = reinterpret_cast<const uint4*>(a.v_resid + (bh * R + t % R) * kD + lw * L::kCPWv);
-            uint32_t hv[L::kCPWv / 2];
 #pragma unroll
-            for (int k4 = 0; k4 < L::kCPWv / 8; ++k4) {
-              const uint4 u = __ldg(vr + k4);
-              hv[4 * k4] = u.x;
-              hv[4 * k4 + 1] = u.y;
-              hv[4 * k4 + 2] = u.z;
-              hv[4 * k4 + 3] = u.w;
-            }
+              for (int w = 0; w < L::kLW; ++w) {
+                const uint32_t ml = magic_lo(wv[w]), mh = magic_hi(wv[w]);
 #pragma unroll
-            for (int j = 0; j < L::kPV; ++j) {
-              const int e0 = j, e1 = L::kPV + j;
-              const float v0 = h2f((e0 & 1) ? (hv[e0 >> 1] >> 16) : (hv[e0 >> 1] & 0xFFFFu));
-              const float v1 = h2f((e1 & 1) ? (hv[e1 >> 1] >> 16) : (hv[e1 >> 1] & 0xFFFFu));
-              const float sj = pow2_pos(VB * j);
+                for (int j = 0; j < L::kPV; ++j) {  // (channel j, channel kPV + j) of the word, x 2^(b j)
+                  const float2 cp = code_pair<VB>(ml, mh, j);
+                  const int i = w * L::kCPWv + 2 * j;
 #pragma unroll
-              for (int r = 0; r < RH; ++r) {
-                o[r][2 * j] = fmaf(p[r] * sj, v0, o[r][2 * j]);
-                o[r][2 * j + 1] = fmaf(p[r] * sj, v1, o[r][2 * j + 1]);
+                  for (int r = 0; r < RH; ++r) {
+                    const float2 acc = __ffma2_rn(w2[r], cp, make_float2(o[r][i], o[r][i + 1]));
+                    o[r][i] = acc.x;
+                    o[r][i + 1] = acc.y;
+                  }
+                }
+              }
+            } else {  // key quantized, value still in the fp16 window
+              const int t = tc0 + tv;
+#pragma unroll
+              for (int w = 0; w < L::kLW; ++w) {
+                const uint4* vr =
+                    reinterpret_cast<const uint4*>(a.v_resid + (bh * R + t % R) * kD + (w0 + w) * L::kCPWv);
+                uint32_t hv[L::kCPWv / 2];
+#pragma unroll
+                for (int k4 = 0; k4 < L::kCPWv / 8; ++k4) {
+                  const uint4 u = __ldg(vr + k4);
+                  hv[4 * k4] = u.x;
+                  hv[4 * k4 + 1] = u.y;
+                  hv[4 * k4 + 2] = u.z;
+                  hv[4 * k4 + 3] = u.w;
+                }
+#pragma unroll
+                for (int j = 0; j < L::kPV; ++j) {
+                  const int e0 = j, e1 = L::kPV + j, i = w * L::kCPWv + 2 * j;
+                  const float v0 = h2f((e0 & 1) ? (hv[e0 >> 1] >> 16) : (hv[e0 >> 1] & 0xFFFFu));
+                  const float v1 = h2f((e1 & 1) ? (hv[e1 >> 1] >> 16) : (hv[e1 >> 1] & 0xFFFFu));
+                  const float sj = pow2_pos(VB * j);
+#pragma unroll
+                  for (int r = 0; r < RH; ++r) {
+                    o[r][i] = fmaf(p[r] * sj, v0, o[r][i]);
+                    o[r][i + 1] = fmaf(p[r] * sj, v1, o[r][i + 1]);
+                  }
+                }
               }
             }
           }
-        }
+        };
+        if (tc0 + tb + 16 <= NQV) value_steps(BoolTag<true>{});
+        else value_steps(BoolTag<false>{});
       }
-      __syncthreads();  // every thread is done with this stage
-      if (tid == 0 && c + L::kAStages < n_chunks && !*failed) {
-        produce(c + L::kAStages);
-        ++issued;
+      // ---- this warp is done with the stage; the last one refills it ----
+      __syncwarp();
+      if (lane == 0 && atom_add_acq_rel_shared(&released[st], 1) == kAWarps - 1) {
+        released[st] = 0;
+        if (c + L::kAStages < n_chunks && !*failed) {
+          fence_proxy_async_smem();
+          produce(c + L::kAStages);
+          atomicAdd(issued, 1);
+        }
       }
     }
+    __syncthreads();  // every warp is out of the loop
     // after a timed-out wait, let this block's copies still in flight land first
     if (tid == 0 && *failed)
-      for (int c = max(0, issued - L::kAStages); c < issued; ++c) mbar_wait_bounded(&full[c % L::kAStages], (c / L::kAStages) & 1);
+      for (int c = max(0, *issued - L::kAStages); c < *issued; ++c)
+        mbar_wait_bounded(&full[c % L::kAStages], (c / L::kAStages) & 1);
   } else {
     // ================================ fp16 key residual =====================================
     const int NR = max(0, min(a.n_tok[b] - NQK, R));
@@ -649,24 +714,27 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
   // ---- warps -> block: sum o - oz and l over the warps (one max per head for the block) ----
   __syncthreads();  // the ring is idle
   float* ored = reinterpret_cast<float*>(sma);  // [warp][RH][128]
-  if (!resid_block) {  // the token slots of a code word meet, then kVW lanes hold 128 channels
+  if (!resid_block) {  // the token slots of a lane position meet, then kLPT lanes hold 128 channels
 #pragma unroll
     for (int r = 0; r < RH; ++r) {
 #pragma unroll
-      for (int off = L::kVW; off < 32; off <<= 1) {
+      for (int off = L::kLPT; off < 32; off <<= 1) {
 #pragma unroll
-        for (int i = 0; i < L::kCPWv; ++i) o[r][i] += __shfl_xor_sync(0xFFFFFFFFu, o[r][i], off);
+        for (int i = 0; i < L::kOV; ++i) o[r][i] += __shfl_xor_sync(0xFFFFFFFFu, o[r][i], off);
         oz[r] += __shfl_xor_sync(0xFFFFFFFFu, oz[r], off);
       }
     }
-    if (lane < L::kVW) {  // o[r][2j] is channel j of the word, o[r][2j + 1] channel kPV + j, x 2^(b j)
+    if (lane < L::kLPT) {  // o[r][w kCPWv + 2j] is channel j of word w, + 1 channel kPV + j, x 2^(b j)
 #pragma unroll
       for (int r = 0; r < RH; ++r) {
-        float* dst = ored + (warp * RH + r) * kD + lane * L::kCPWv;
 #pragma unroll
-        for (int j = 0; j < L::kPV; ++j) {
-          dst[j] = o[r][2 * j] * pow2_neg(VB * j) - oz[r];
-          dst[L::kPV + j] = o[r][2 * j + 1] * pow2_neg(VB * j) - oz[r];
+        for (int w = 0; w < L::kLW; ++w) {
+          float* dst = ored + (warp * RH + r) * kD + (lane * L::kLW + w) * L::kCPWv;
+#pragma unroll
+          for (int j = 0; j < L::kPV; ++j) {
+            dst[j] = o[r][w * L::kCPWv + 2 * j] * pow2_neg(VB * j) - oz[r];
+            dst[L::kPV + j] = o[r][w * L::kCPWv + 2 * j + 1] * pow2_neg(VB * j) - oz[r];
+          }
         }
       }
     }
@@ -678,7 +746,10 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
   }
   if (lane == 0)
 #pragma unroll
-    for (int r = 0; r < RH; ++r) red[warp * RH + r] = l[r];
+    for (int r = 0; r < RH; ++r) {
+      red[warp * RH + r] = l[r];
+      redm[warp * RH + r] = M[r];
+    }
   __syncthreads();
   if (*failed) return;  // uniform after the barrier
 
@@ -689,15 +760,17 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
     const int i = it * kAThreads + tid, r = i / kD, ch = i % kD;
     ov[it] = 0.f;
     Ls[it] = 0.f;
-    Mv[it] = M[0];
-#pragma unroll
-    for (int rr = 1; rr < RH; ++rr)
-      if (r == rr) Mv[it] = M[rr];
-    if (i < RH * kD) {
-      for (int w = 0; w < kAWarps; ++w) {
-        ov[it] += ored[(w * RH + r) * kD + ch];
-        Ls[it] += red[w * RH + r];
-      }
+    Mv[it] = -INFINITY;
+    if (i < RH * kD) {  // each warp's running max differs: rescale to the block's
+      for (int w = 0; w < kAWarps; ++w) Mv[it] = fmaxf(Mv[it], redm[w * RH + r]);
+      if (Mv[it] != -INFINITY)
+        for (int w = 0; w < kAWarps; ++w) {
+          const float mw = redm[w * RH + r];
+          if (mw == -INFINITY) continue;
+          const float f = exp2f(mw - Mv[it]);
+          ov[it] = fmaf(f, ored[(w * RH + r) * kD + ch], ov[it]);
+          Ls[it] = fmaf(f, red[w * RH + r], Ls[it]);
+        }
     }
   }
   auto write_out = [&](int i, float val) {

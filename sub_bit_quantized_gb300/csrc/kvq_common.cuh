@@ -99,6 +99,30 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// As mbar_wait_bounded, but each retry lets the hardware suspend the warp for up to
+// `hint_ns` until the phase completes, instead of spinning: a warp that waits long (a
+// producer or consumer of a pipeline) then takes few issue slots from the warps that work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint64_t* bar, uint32_t parity,
+                                                        uint64_t limit_ns = 1000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
 // ---- exact-enough distances without fp64 -----------------------------------------------
 // hi + lo += (z - e)^2 with error-free steps: z - e = s + t exactly (two-sum), s^2 = p + q
 // exactly (fma), hi + p = h + err exactly (two-sum); the low parts gather in lo. The sum of

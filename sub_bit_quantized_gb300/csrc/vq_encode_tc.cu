@@ -119,11 +119,13 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 64 consecutive fp32 columns of this thread's TMEM lane: two loads, one wait
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
-  uint32_t r[64];
+// N (a multiple of 32) consecutive fp32 columns of this thread's TMEM lane: N / 32 loads,
+// one wait
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]) {
+  uint32_t r[N];
 #pragma unroll
-  for (int h = 0; h < 2; ++h)
+  for (int h = 0; h < N / 32; ++h)
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -140,7 +142,7 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
         : "memory");
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // cp.async of 16 (or 8) bytes, zero-filled when `fill` is false (src is then not read)
@@ -242,7 +244,7 @@ __device__ void stage_codebook(const VqEncodeArgs& a, int plane, unsigned char* 
 
 __device__ __forceinline__ bool enc_wait(uint64_t* bar, uint32_t parity, volatile int* failed, int* err) {
   if (*failed) return false;
-  if (mbar_wait_bounded(bar, parity)) return true;
+  if (mbar_wait_bounded_sleep(bar, parity)) return true;
   *failed = 1;
   set_error(err, KVQ_ERR_TIMEOUT);
   return false;
@@ -424,11 +426,11 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
       tc_fence_after();
       float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll 1
-      for (int k = 0; k < kTcN / 64; ++k) {
-        float v[64];
-        tmem_ld64(row_addr + 64 * k, v);
+      for (int k = 0; k < kTcN / 128; ++k) {
+        float v[128];
+        tmem_ld<128>(row_addr + 128 * k, v);
 #pragma unroll
-        for (int c = 0; c < 64; c += 8) {
+        for (int c = 0; c < 128; c += 8) {
           m0 = max3f(m0, v[c], v[c + 1]);
           m1 = max3f(m1, v[c + 2], v[c + 3]);
           m2 = max3f(m2, v[c + 4], v[c + 5]);
@@ -459,24 +461,29 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
       int ksel = 0;
       uint32_t kmask = 0;  // chunks holding a column in the band
 #pragma unroll 1
-      for (int k = 0; k < kTcN / 64; ++k) {
-        float v[64];
-        tmem_ld64(row_addr + 64 * k, v);
-        float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
+      for (int k2 = 0; k2 < kTcN / 128; ++k2) {
+        float v[128];
+        tmem_ld<128>(row_addr + 128 * k2, v);
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          const float2 f01 = make_float2(at_least(v[c], cth), at_least(v[c + 1], cth));
-          const float2 f23 = make_float2(at_least(v[c + 2], cth), at_least(v[c + 3], cth));
-          s01 = __ffma2_rn(f01, make_float2(1.f + c / 512.f, 1.f + (c + 1) / 512.f), s01);
-          s23 = __ffma2_rn(f23, make_float2(1.f + (c + 2) / 512.f, 1.f + (c + 3) / 512.f), s23);
+        for (int hh = 0; hh < 2; ++hh) {
+          const int k = 2 * k2 + hh;
+          const float* vk = v + 64 * hh;
+          float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            const float2 f01 = make_float2(at_least(vk[c], cth), at_least(vk[c + 1], cth));
+            const float2 f23 = make_float2(at_least(vk[c + 2], cth), at_least(vk[c + 3], cth));
+            s01 = __ffma2_rn(f01, make_float2(1.f + c / 512.f, 1.f + (c + 1) / 512.f), s01);
+            s23 = __ffma2_rn(f23, make_float2(1.f + (c + 2) / 512.f, 1.f + (c + 3) / 512.f), s23);
+          }
+          const float sk = (s01.x + s01.y) + (s23.x + s23.y);
+          if (sk > 0.5f) {
+            ksel = k;
+            ksum = sk;
+            kmask |= 1u << k;
+          }
+          tally += sk;
         }
-        const float sk = (s01.x + s01.y) + (s23.x + s23.y);
-        if (sk > 0.5f) {
-          ksel = k;
-          ksum = sk;
-          kmask |= 1u << k;
-        }
-        tally += sk;
       }
       const int j = t * kTcM + row;
       const bool valid = j < a.n_tok;
@@ -492,7 +499,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
           const bool mine = need && ((kmask >> k) & 1u);
           if (!__any_sync(0xFFFFFFFFu, mine)) continue;  // warp-uniform
           float v[64];
-          tmem_ld64(row_addr + 64 * k, v);  // warp-wide load: every lane takes part
+          tmem_ld<64>(row_addr + 64 * k, v);  // warp-wide load: every lane takes part
           if (mine) {
 #pragma unroll
             for (int b = 0; b < 32; ++b) {

@@ -56,6 +56,7 @@ constexpr int kEncThreads = 320;
 constexpr int kAStages = 4;          // vector-row ring
 constexpr int kLoadDepth = 2;        // tiles whose row copies the loader keeps in flight
 constexpr uint32_t kTmemCols = 512;  // two 128 x 256 fp32 accumulators
+constexpr int kNearCap = 64;         // near-tie (row, candidate) pairs an epilogue warp decides together
 static_assert(kEpiWarps == 8 && kLoadWarp == kEpiWarps && kMmaWarp == kLoadWarp + 1 &&
               kEncThreads == 32 * (kMmaWarp + 1), "warp roles");
 
@@ -77,7 +78,8 @@ struct TcLayout {
   static constexpr int kOffA = 0;                           // kAStages tile buffers
   static constexpr int kOffB = kOffA + kAStages * kABytes;  // the three codebook parts
   static constexpr int kOffBar = kOffB + kParts * kBPartBytes;  // mbarriers, TMEM address, flag
-  static constexpr int kSmem = kOffBar + 160;
+  static constexpr int kOffNear = kOffBar + 160;            // per epilogue warp: near-tie pairs, distances
+  static constexpr int kSmem = kOffNear + kEpiWarps * kNearCap * 8;
   // requested per block so that a second block cannot share the SM (and its 512 TMEM columns)
   static constexpr int kSmemLaunch = kSmem > 120 * 1024 ? kSmem : 120 * 1024;
   static_assert(kSmemLaunch <= 232448, "shared memory");
@@ -417,6 +419,8 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
     // of columns at or above thr and, when that is one, its column, as sum [v >= thr] (1 + col/512)
     // on the FMA pipe. More than one column in the band: the row is decided on exact distances.
     const int e = warp >> 2, row = 32 * (warp & 3) + lane;
+    uint32_t* near_list = reinterpret_cast<uint32_t*>(smem + Lay::kOffNear) + warp * kNearCap;
+    float* near_d = reinterpret_cast<float*>(smem + Lay::kOffNear) + kEpiWarps * kNearCap + warp * kNearCap;
     const uint32_t row_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kTcN * e);
     int ties = 0;
     for (int i = e; i < n; i += 2) {
@@ -514,40 +518,78 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
       if (lane == 0) mbar_arrive(&accempty[e]);  // the accumulator is read: the next MMAs may go
       if (any_need) {
         // every candidate in the band, decided on compensated fp32 distances (lowest index wins
-        // exact ties); a runner-up within 1e-6 of the best is reported as a tie
+        // exact ties); a runner-up within 1e-6 of the best is reported as a tie. The warp's
+        // (row, candidate) pairs go to a list that all 32 lanes work through together (a row
+        // rarely has more than a few candidates, and only some rows of a warp have any); a
+        // longer list than kNearCap is done row by row.
         float bd = INFINITY, sd = INFINITY;
         int bdi = result;
-#pragma unroll
-        for (int q = 0; q < kTcN / 32; ++q) {
-          uint32_t cm = need ? cand[q] : 0u;
-          while (cm) {
-            const int r = 32 * q + __ffs(cm) - 1;
-            cm &= cm - 1;
-            // e = hi + mid + lo exactly (each residual is a multiple of e's ulp that fits the
-            // next part), so the staged parts give the fp32 entries back
-            float dh = 0.f, dl = 0.f;
+        auto consider = [&](int r, float dd) {  // in increasing column order: the lowest wins exact ties
+          if (dd < bd) {
+            sd = bd;
+            bd = dd;
+            bdi = r;
+          } else if (dd < sd) {
+            sd = dd;
+          }
+        };
+        // e = hi + mid + lo exactly (each residual is a multiple of e's ulp that fits the next
+        // part), so the staged parts give the fp32 entries back
+        auto exact_d = [&](int rr, int r) {
+          float dh = 0.f, dl = 0.f;
 #pragma unroll 1
-            for (int c = 0; c < DC; ++c) {
-              const uint4 w = *reinterpret_cast<const uint4*>(sa + op_off(row, c, KC));
-              const uint4 e0 = *reinterpret_cast<const uint4*>(sb + op_off(r, c, KC));
-              const uint4 e1 = *reinterpret_cast<const uint4*>(sb + Lay::kBPartBytes + op_off(r, c, KC));
-              const uint4 e2 = *reinterpret_cast<const uint4*>(sb + 2 * Lay::kBPartBytes + op_off(r, c, KC));
-              const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
-              const uint32_t h4[4] = {e0.x, e0.y, e0.z, e0.w}, m4[4] = {e1.x, e1.y, e1.z, e1.w},
-                             l4[4] = {e2.x, e2.y, e2.z, e2.w};
+          for (int c = 0; c < DC; ++c) {
+            const uint4 w = *reinterpret_cast<const uint4*>(sa + op_off(rr, c, KC));
+            const uint4 e0 = *reinterpret_cast<const uint4*>(sb + op_off(r, c, KC));
+            const uint4 e1 = *reinterpret_cast<const uint4*>(sb + Lay::kBPartBytes + op_off(r, c, KC));
+            const uint4 e2 = *reinterpret_cast<const uint4*>(sb + 2 * Lay::kBPartBytes + op_off(r, c, KC));
+            const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+            const uint32_t h4[4] = {e0.x, e0.y, e0.z, e0.w}, m4[4] = {e1.x, e1.y, e1.z, e1.w},
+                           l4[4] = {e2.x, e2.y, e2.z, e2.w};
 #pragma unroll
-              for (int q2 = 0; q2 < 4; ++q2) {
-                add_sq_diff(bf16_lo(w4[q2]), __fadd_rn(__fadd_rn(bf16_lo(h4[q2]), bf16_lo(m4[q2])), bf16_lo(l4[q2])), dh, dl);
-                add_sq_diff(bf16_hi(w4[q2]), __fadd_rn(__fadd_rn(bf16_hi(h4[q2]), bf16_hi(m4[q2])), bf16_hi(l4[q2])), dh, dl);
-              }
+            for (int q2 = 0; q2 < 4; ++q2) {
+              add_sq_diff(bf16_lo(w4[q2]), __fadd_rn(__fadd_rn(bf16_lo(h4[q2]), bf16_lo(m4[q2])), bf16_lo(l4[q2])), dh, dl);
+              add_sq_diff(bf16_hi(w4[q2]), __fadd_rn(__fadd_rn(bf16_hi(h4[q2]), bf16_hi(m4[q2])), bf16_hi(l4[q2])), dh, dl);
             }
-            const float dd = __fadd_rn(dh, dl);
-            if (dd < bd) {  // columns are visited in increasing order: the lowest wins exact ties
-              sd = bd;
-              bd = dd;
-              bdi = r;
-            } else if (dd < sd) {
-              sd = dd;
+          }
+          return __fadd_rn(dh, dl);
+        };
+        int cnt = 0;
+#pragma unroll
+        for (int q = 0; q < kTcN / 32; ++q) cnt += __popc(need ? cand[q] : 0u);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        if (total <= kNearCap) {  // warp-uniform
+          int en = incl - cnt;
+#pragma unroll
+          for (int q = 0; q < kTcN / 32; ++q) {
+            uint32_t cm = need ? cand[q] : 0u;
+            while (cm) {
+              near_list[en++] = ((uint32_t)row << 8) | (uint32_t)(32 * q + __ffs(cm) - 1);
+              cm &= cm - 1;
+            }
+          }
+          __syncwarp();
+          for (int e2 = lane; e2 < total; e2 += 32) {
+            const uint32_t v = near_list[e2];
+            near_d[e2] = exact_d((int)(v >> 8), (int)(v & 255u));
+          }
+          __syncwarp();
+          for (int e2 = incl - cnt; e2 < incl; ++e2) consider((int)(near_list[e2] & 255u), near_d[e2]);
+          __syncwarp();  // the list is free for the next tile
+        } else {
+#pragma unroll
+          for (int q = 0; q < kTcN / 32; ++q) {
+            uint32_t cm = need ? cand[q] : 0u;
+            while (cm) {
+              const int r = 32 * q + __ffs(cm) - 1;
+              cm &= cm - 1;
+              consider(r, exact_d(row, r));
             }
           }
         }

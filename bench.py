@@ -243,6 +243,18 @@ def vq_call_bytes(B, H, n_pages, n_win, NG=16):
     return idx + win + bt + rope + qo
 
 
+# Shared-memory bytes the page kernel must read per quantized token and head: every index
+# selects one codeword row per channel group, fp32 keys (4 B per channel) and fp16 values (2 B
+# per channel), plus the token's key and value index bytes from the ring. On this GPU that
+# on-chip traffic, not HBM, is the binding resource of the LoopVQ decode (121 B per SM cycle
+# measured for conflict-free 128-bit shared loads; 128 nominal).
+SMEM_BYTES_PER_CLK_SM = 121.0
+
+
+def vq_smem_bytes(B, H, n_pages, NG=16):
+    return B * H * n_pages * 8 * (D * 4 + D * 2 + 2 * NG)
+
+
 def setup_loopvq(wl, dev, seed, extra_tokens=0):
     """LoopVQ cache of the workload, prefilled to L tokens per request (room for
     ``extra_tokens`` more, for streaming)."""
@@ -343,16 +355,16 @@ PROFILED_TRAFFIC = {
         204150016 + 5767424 + 43536640 + 3072),
     "kivi_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "0474bba73e3cf49c0a5e6860728af987755220c7d31cf08b8ff9430cae00d5f5",
-        228799488 + 4636928),
+        "d4479ca4c4e11b240e5aebde4fd19716e3e29d0b504f3f93f6483e8d8bbd3045",
+        228796416 + 4545536),
     "encode_32k:encode_tc_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_encode_tc.cu",
-        "ef1de63a1e981fbaffcca621d390e0766bde42fc23fb6dc9dd5c7249efe9c38c",
-        287318784 + 14957568),
+        "42e194feda74fa6a5e78177d6a39c04b4785de3db0db60096413109cc4b1cd1a",
+        287192064 + 14977024),
     "kivi4_gqa_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "0474bba73e3cf49c0a5e6860728af987755220c7d31cf08b8ff9430cae00d5f5",
-        89868544 + 2781952),
+        "d4479ca4c4e11b240e5aebde4fd19716e3e29d0b504f3f93f6483e8d8bbd3045",
+        89874944 + 2716416),
 }
 
 
@@ -489,6 +501,16 @@ def run_ours(args, wl, rank, world, dist, pool):
                                      "kernel": kernel_name,
                                      "bytes_per_launch": call_bytes},
                            n_splits=n_splits))
+        # LoopVQ's on-chip bound: codeword-row bytes read from shared memory per call over the
+        # same call time, against the shared-memory rate of all SMs at the sampled clock
+        if wl["kind"] == "loopvq":
+            sm_mhz = clocks.get("sm_mhz") or 2070.0  # the sampled median under load, else the maximum
+            smem_peak = torch.cuda.get_device_properties(dev).multi_processor_count * SMEM_BYTES_PER_CLK_SM * sm_mhz * 1e6 / 1e9
+            smem_b = vq_smem_bytes(B, H, n_pages, vq_ng(wl))
+            smem_ach = smem_b / (per_launch_us * 1e-6) / 1e9
+            result["roofline"]["on_chip"] = {"bound": "smem", "achieved": round(smem_ach, 1), "peak": round(smem_peak, 1),
+                                             "unit": "GB/s", "frac": round(smem_ach / smem_peak, 4),
+                                             "bytes_per_launch": smem_b}
         if rank == 0 and not args.no_cpu_baseline:
             # eight calls' worth of (request, head) units: about 10 s on 16 host cores
             n_pairs = 8 * B * H

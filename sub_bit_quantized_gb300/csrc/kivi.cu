@@ -568,7 +568,10 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
             float mx = sc_r;
 #pragma unroll
             for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-            if (mx > M[r]) rescale_to(r, mx);  // warp-uniform
+            // the running maximum is raised only when a score passes it by more than 2^8 (or on
+            // the first chunk): weights stay below 256, the sums exact relative to M, and most
+            // chunks skip the rescale (warp-uniform)
+            if (mx > M[r] + 8.f) rescale_to(r, mx);
             pk[r] = exp2f(sc_r - M[r]);
             float ls = pk[r];
 #pragma unroll

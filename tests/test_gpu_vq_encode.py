@@ -100,6 +100,34 @@ def test_encode_group_subset_and_exact_ties():
         check_indices(got[beta, 0, 0, :, 3:12], want[:, 3:12], tie[:, 3:12])
 
 
+@pytest.mark.parametrize("copies", [2, 3])
+def test_encode_duplicated_codebook_ties(copies):
+    """Every codeword repeated `copies` times (entry r + k * 256 // copies copies entry r), so
+    every vector has `copies` exact-tie candidates: the lowest copy must win each one. Two
+    copies fill a warp's near-tie list exactly (32 rows x 2 pairs); three overflow it and take
+    the row-by-row path."""
+    T, Tc, G, B, H, L = 4, 2, 16, 1, 1, 160
+    g, xk, _ = gen_kv(220 + copies, B, H, L, T)
+    cb = codebooks(g, xk, Tc, G)
+    span = 256 // copies
+    for k in range(1, copies):
+        cb[:, :, :, k * span:(k + 1) * span] = cb[:, :, :, :span]
+    cb[:, :, :, copies * span:] = cb[:, :, :, :256 - copies * span]  # the remainder copies too
+    cfg = kvq.VqConfig(T=T, Tc=Tc, G=G, n_heads=H, max_pages=L // 8, max_batch=B, max_ctx=L + 80)
+    idx = torch.zeros((cfg.NB, B, H, L // 8, 128), dtype=torch.uint8, device="cuda")
+    ties = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq.kvq_encode_vq(cfg, C.bf16_tensor(xk), (B * H * L * D, H * L * D, L * D), 0, B, L,
+                      torch.from_numpy(cb).cuda(), idx, n_ties=ties)
+    torch.cuda.synchronize()
+    got = _layout.unpack_pages(idx.cpu().numpy(), 16)
+    for beta in range(T // Tc):
+        want, tie = olv.encode_block(xk[:, 0, 0], cb[beta, 0], beta, Tc)
+        check_indices(got[beta, 0, 0], want, tie)
+        assert (want < span).all()
+        assert (got[beta, 0, 0] < span).all(), "an exact tie went to a higher copy"
+    assert int(ties.item()) >= (T // Tc) * L * 16  # every vector has a tie
+
+
 def test_encode_full_size_sampled():
     # prefill encode workload: 16 heads x 8 channel groups x 2 loop blocks x 32768 tokens
     T, Tc, G, H, L = 4, 2, 16, 16, 32768

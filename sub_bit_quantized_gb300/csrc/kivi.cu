@@ -73,30 +73,34 @@ __device__ __forceinline__ void store_codes4(uint8_t* row, int lane, const uint3
   else *reinterpret_cast<uint16_t*>(row + 2 * lane) = (uint16_t)(c[0] | (c[1] << 4) | (c[2] << 8) | (c[3] << 12));
 }
 
+// 8 bytes of a row (4 fp16 values), through the read-only cache when the data is not written
+// by the same kernel
+template <bool kReadOnly>
+__device__ __forceinline__ uint2 load_row(const uint16_t* p) {
+  return kReadOnly ? __ldg(reinterpret_cast<const uint2*>(p)) : *reinterpret_cast<const uint2*>(p);
+}
+
 // One warp quantizes one 32-token key group over all 128 channels; lane l owns channels
-// 4l .. 4l + 3, so each token row is one coalesced 256-byte read, all 32 rows in flight.
+// 4l .. 4l + 3, so each token row is one coalesced 256-byte read, all 32 rows in flight. The
+// first pass finds each channel's minimum and maximum, the second reads the rows again (from
+// L1: the warp read them just before) and writes the codes, so the rows need no registers.
 // src: row j at src + j * src_row elements; codes: row j at codes + j * (D b / 8) bytes;
 // scale / zero: the group's [D] row.
 template <int BITS, bool kReadOnly>
 __device__ __forceinline__ void quant_key_group(const uint16_t* src, size_t src_row, uint8_t* codes,
                                                 uint16_t* scale, uint16_t* zero, int lane) {
   constexpr int kRow = kD * BITS / 8;
-  uint2 raw[kGroup];
-#pragma unroll
-  for (int j = 0; j < kGroup; ++j) {
-    const uint2* p = reinterpret_cast<const uint2*>(src + (size_t)j * src_row + 4 * lane);
-    raw[j] = kReadOnly ? __ldg(p) : *p;
-  }
+  const uint16_t* base = src + 4 * lane;
   float mn[4], mx[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     mn[i] = INFINITY;
     mx[i] = -INFINITY;
   }
-#pragma unroll
+#pragma unroll 8
   for (int j = 0; j < kGroup; ++j) {
     float v[4];
-    unpack4(raw[j], v);
+    unpack4(load_row<kReadOnly>(base + (size_t)j * src_row), v);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       mn[i] = fminf(mn[i], v[i]);
@@ -110,10 +114,10 @@ __device__ __forceinline__ void quant_key_group(const uint16_t* src, size_t src_
       make_uint2(g[0].s_bits | ((uint32_t)g[1].s_bits << 16), g[2].s_bits | ((uint32_t)g[3].s_bits << 16));
   *reinterpret_cast<uint2*>(zero + 4 * lane) =
       make_uint2(g[0].z_bits | ((uint32_t)g[1].z_bits << 16), g[2].z_bits | ((uint32_t)g[3].z_bits << 16));
-#pragma unroll
+#pragma unroll 8
   for (int j = 0; j < kGroup; ++j) {
     float v[4];
-    unpack4(raw[j], v);
+    unpack4(load_row<kReadOnly>(base + (size_t)j * src_row), v);
     uint32_t c[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) c[i] = quant_code<BITS>(v[i], g[i]);
@@ -168,33 +172,31 @@ __global__ void __launch_bounds__(256) kivi_quant_channel_kernel(const KiviQuant
   }
 }
 
-// values: a warp covers one 256-byte token row per step, 4 rows loaded per step
+// values: a warp covers one 256-byte token row per step, 8 consecutive rows of one
+// (b, h) loaded per step (one index division per 8 rows)
 template <int BITS>
 __global__ void __launch_bounds__(256) kivi_quant_token_kernel(const KiviQuantArgs a) {
-  constexpr int kRows = 4;
+  constexpr int kRows = 8;
   constexpr int kRow = kD * BITS / 8;
   const int lane = threadIdx.x & 31;
-  const long long rows = (long long)a.B * a.H * a.n_tok;
-  const long long n_steps = (rows + kRows - 1) / kRows;
+  const int per_bh = (a.n_tok + kRows - 1) / kRows;  // row blocks of one (b, h)
+  const long long n_steps = (long long)a.B * a.H * per_bh;
   for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; w < n_steps;
        w += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const long long bh = w / per_bh;  // b * H + h
+    const int j0 = (int)(w - bh * per_bh) * kRows;
+    const int h = (int)(bh % a.H), b = (int)(bh / a.H);
+    const int nr = min(kRows, a.n_tok - j0);
+    const uint16_t* src = a.x + (size_t)b * a.sb + (size_t)h * a.sh + (size_t)j0 * kD + 4 * lane;
+    const size_t tok0 = (size_t)bh * a.max_tokens + a.tok_begin + j0;
     uint2 raw[kRows];
-    size_t tok[kRows];
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) raw[u] = __ldg(reinterpret_cast<const uint2*>(src + (size_t)min(u, nr - 1) * kD));
 #pragma unroll
     for (int u = 0; u < kRows; ++u) {
-      const long long r = min(w * kRows + u, rows - 1);
-      const int j = (int)(r % a.n_tok);
-      const long long q = r / a.n_tok;
-      const int h = (int)(q % a.H);
-      const int b = (int)(q / a.H);
-      raw[u] = __ldg(reinterpret_cast<const uint2*>(a.x + (size_t)b * a.sb + (size_t)h * a.sh + (size_t)j * kD + 4 * lane));
-      tok[u] = ((size_t)b * a.H + h) * a.max_tokens + a.tok_begin + j;
-    }
-#pragma unroll
-    for (int u = 0; u < kRows; ++u) {
-      if (w * kRows + u >= rows) break;  // uniform across the warp
-      quant_value_row<BITS>(raw[u], a.codes + tok[u] * kRow, a.scale + tok[u] * (kD / kGroup),
-                            a.zero + tok[u] * (kD / kGroup), lane);
+      if (u >= nr) break;  // uniform across the warp
+      quant_value_row<BITS>(raw[u], a.codes + (tok0 + u) * kRow, a.scale + (tok0 + u) * (kD / kGroup),
+                            a.zero + (tok0 + u) * (kD / kGroup), lane);
     }
   }
 }
@@ -883,7 +885,7 @@ size_t kivi_attn_smem_bytes(int k_bits, int v_bits, int rh, int residual) {
 cudaError_t launch_kivi_quantize(const KiviQuantArgs& a, cudaStream_t s) {
   // grid-stride warps; 8 blocks of 256 threads per SM keep enough rows in flight
   const long long warps = (a.axis == KVQ_PER_CHANNEL) ? (long long)a.B * a.H * (a.n_tok / a.group)
-                                                      : ((long long)a.B * a.H * a.n_tok + 3) / 4;
+                                                      : (long long)a.B * a.H * ((a.n_tok + 7) / 8);
   if (warps <= 0) return cudaSuccess;
   long long blocks = (warps + 7) / 8;
   const int sms = sm_count_cached();

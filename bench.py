@@ -361,6 +361,11 @@ PROFILED_TRAFFIC = {
         "sub_bit_quantized_gb300/csrc/vq_encode_tc.cu",
         "42e194feda74fa6a5e78177d6a39c04b4785de3db0db60096413109cc4b1cd1a",
         287192064 + 14977024),
+    # both quantize kernels (keys per channel, values per token) of one step
+    "kivi_quant_32k:kivi_quant_*_kernel": (
+        "sub_bit_quantized_gb300/csrc/kivi.cu",
+        "ac0f6a6b2606006f6b041ca0b393793f59f998c175c40932fff00244e0367dbf",
+        135003648 + 14183168 + 134271744 + 12630784),
     "kivi4_gqa_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
         "d4479ca4c4e11b240e5aebde4fd19716e3e29d0b504f3f93f6483e8d8bbd3045",
@@ -696,7 +701,8 @@ def run_ours(args, wl, rank, world, dist, pool):
         result.update(dict(value=round(gbs * world, 1), unit="GB/s", ms_per_step=round(ms, 4),
                            gpu_launches=2 * args.steps, clocks=cs.summary(),
                            roofline={"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                                     "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                                     "frac": round(gbs / hbm_peak, 4),
+                                     "traffic": profiled_traffic(args.workload, "kivi_quant_*_kernel"),
                                      "kernel": "kivi_quant_*_kernel"}))
         return result
     raise ValueError(wl["kind"])

@@ -30,7 +30,7 @@ namespace {
 constexpr int kGroup = 32;  // tokens per key group, channels per value group (checked by the host)
 
 struct GroupQ {
-  float s16f, z16f;
+  float s16f, z16f, rs;  // rs = 1 / s16f, correctly rounded
   uint16_t s_bits, z_bits;
 };
 
@@ -43,16 +43,36 @@ __device__ __forceinline__ GroupQ group_params(float mn, float mx) {
   const __half z16 = __float2half_rn(__fdiv_rn(-mn, s16f));
   GroupQ g;
   g.s16f = s16f;
+  g.rs = __frcp_rn(s16f);
   g.z16f = __half2float(z16);
   g.s_bits = __half_as_ushort(s16);
   g.z_bits = __half_as_ushort(z16);
   return g;
 }
 
+// The codes of four values x_i (group parameters g_i): clamp(rint(t_i), 0, 2^b - 1) with
+// t = (x / s) + z, an IEEE division and a separate rounded add. t' = fma(x, 1/s, z) differs
+// from t by at most about 2^-23 (|x / s| + |t'|) (one rounding each in 1/s, the fma, x / s
+// and the add), so when every t'_i lies farther than four times that from the rounding
+// boundary k + 1/2 nearest to it, rint(t) = rint(t') and the codes are the same; otherwise
+// (about 1e-6 of the values, |t'| >= 2^23 and any NaN) the exact sequence decides all four.
 template <int BITS>
-__device__ __forceinline__ uint32_t quant_code(float x, const GroupQ& g) {
-  const float t = __fadd_rn(__fdiv_rn(x, g.s16f), g.z16f);
-  return (uint32_t)fminf(fmaxf(rintf(t), 0.0f), (float)((1 << BITS) - 1));
+__device__ __forceinline__ void quant_codes4(const float (&x)[4], const GroupQ* const (&g)[4], uint32_t (&c)[4]) {
+  float k[4];
+  bool fast = true;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float tf = __fmaf_rn(x[i], g[i]->rs, g[i]->z16f);
+    k[i] = rintf(tf);
+    const float bound = __fmul_rn(__fmaf_rn(fabsf(x[i]), g[i]->rs, fabsf(tf)), 4.8e-7f);  // 4 x 2^-23 (...)
+    fast = fast && (fabsf(tf - k[i]) < 0.5f - bound);
+  }
+  if (!fast) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) k[i] = rintf(__fadd_rn(__fdiv_rn(x[i], g[i]->s16f), g[i]->z16f));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = (uint32_t)fminf(fmaxf(k[i], 0.0f), (float)((1 << BITS) - 1));
 }
 
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
@@ -119,8 +139,8 @@ __device__ __forceinline__ void quant_key_group(const uint16_t* src, size_t src_
     float v[4];
     unpack4(load_row<kReadOnly>(base + (size_t)j * src_row), v);
     uint32_t c[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) c[i] = quant_code<BITS>(v[i], g[i]);
+    const GroupQ* const gp[4] = {&g[0], &g[1], &g[2], &g[3]};
+    quant_codes4<BITS>(v, gp, c);
     store_codes4<BITS>(codes + (size_t)j * kRow, lane, c);
   }
 }
@@ -146,8 +166,8 @@ __device__ __forceinline__ void quant_value_row(const uint2 raw, uint8_t* codes,
     zero[lane >> 3] = g.z_bits;
   }
   uint32_t c[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) c[i] = quant_code<BITS>(v[i], g);
+  const GroupQ* const gp[4] = {&g, &g, &g, &g};
+  quant_codes4<BITS>(v, gp, c);
   store_codes4<BITS>(codes, lane, c);
 }
 

@@ -37,6 +37,13 @@ def kv_data(seed, B, H, n):
 def test_quantize_bit_exact(bits):
     B, H, n = 2, 3, 96
     g, K, V = kv_data(300, B, H, n)
+    # groups whose scaled values x / s + z fall exactly on k + 1/2 (s a power of two, z = 0):
+    # the rounding ties that the exact division decides (half to even)
+    s0, top = 0.25, (1 << bits) - 1
+    ties = (np.arange(32) % top + 0.5) * s0
+    ties[0], ties[1] = 0.0, top * s0  # the group's minimum and maximum
+    K[1, 2, 64:96, 17] = ties.astype(np.float16)  # a key group: channel 17, tokens 64..95
+    V[1, 1, 7, 32:64] = ties.astype(np.float16)   # a value group: token 7, channels 32..63
     cfg = kvq.KiviConfig(n_heads=H, k_bits=bits, v_bits=bits, max_batch=B, max_tokens=160)
     cache = kvq.KiviCache(cfg)
     kvq.kvq_quantize_kivi(cfg, kvq.PER_CHANNEL, torch.from_numpy(K).cuda(), cache.k_codes, cache.k_scale,

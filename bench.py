@@ -355,8 +355,8 @@ PROFILED_TRAFFIC = {
         204150016 + 5767424 + 43536640 + 3072),
     "kivi_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "d4479ca4c4e11b240e5aebde4fd19716e3e29d0b504f3f93f6483e8d8bbd3045",
-        228796416 + 4545536),
+        "ac0f6a6b2606006f6b041ca0b393793f59f998c175c40932fff00244e0367dbf",
+        228796416 + 4419584),
     "encode_32k:encode_tc_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_encode_tc.cu",
         "42e194feda74fa6a5e78177d6a39c04b4785de3db0db60096413109cc4b1cd1a",
@@ -368,8 +368,8 @@ PROFILED_TRAFFIC = {
         135003648 + 14183168 + 134271744 + 12630784),
     "kivi4_gqa_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "d4479ca4c4e11b240e5aebde4fd19716e3e29d0b504f3f93f6483e8d8bbd3045",
-        89874944 + 2716416),
+        "ac0f6a6b2606006f6b041ca0b393793f59f998c175c40932fff00244e0367dbf",
+        89876480 + 2961408),
 }
 
 

@@ -38,9 +38,10 @@
 //    then warps through the stage's shared memory) and the block writes the piece's partial
 //    (M, l, o) per request to the workspace.
 //
-// vq_window_kernel: one 128-thread block per (request, head) attends the bf16 sink and
-// recent tokens (one token per lane-group step, online softmax) and merges the result with
-// every page piece of its segment, found from the same share arithmetic.
+// vq_window_kernel: one block (128 threads, or 512 for few long windows) per (request, head)
+// attends the bf16 sink and recent tokens (one token per lane-group step, online softmax) and
+// merges the result with every page piece of its segment, found from the same share
+// arithmetic.
 #include <cuda_fp16.h>
 
 #include "kvq_common.cuh"
@@ -722,16 +723,18 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
 }
 
 // ------------------------------------------------------------------ window + merge kernel
-constexpr int kWThreads = 128;
-
-__global__ void __launch_bounds__(kWThreads) vq_window_kernel(const VqAttnArgs a, const float scale_log2) {
+// WT threads per block: 128 when the (request, head) blocks fill the GPU (7 resident per SM),
+// 512 when there are no more blocks than SMs (long windows of few requests: 4 times the
+// lane-groups per window, so a window's tokens take a quarter of the serial steps)
+template <int WT>
+__global__ void __launch_bounds__(WT, (WT == 128) ? 7 : 1) vq_window_kernel(const VqAttnArgs a, const float scale_log2) {
   __shared__ __align__(16) float qs[kD];
-  __shared__ __align__(16) float wpart[kWThreads / 32][kD + 2];
+  __shared__ __align__(16) float wpart[WT / 32][kD + 2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x / a.H, h = blockIdx.x - b * a.H;
   int L, NP;
   if (!req_len(a, b, L, NP) && h == 0 && tid == 0) set_error(a.err, KVQ_ERR_CAPACITY);
-  qs[tid] = bf16_to_f32(a.q[((size_t)b * a.H + h) * kD + tid]);
+  if (tid < kD) qs[tid] = bf16_to_f32(a.q[((size_t)b * a.H + h) * kD + tid]);
   __syncthreads();
 
   // ---- bf16 window: lane-group g takes tokens g, g + 16, ... ----------------------------
@@ -743,7 +746,7 @@ __global__ void __launch_bounds__(kWThreads) vq_window_kernel(const VqAttnArgs a
   const uint16_t* wv = a.win_v + ((size_t)b * a.H + h) * a.win_slots * kD;
   Acc A;  // here l is the same in every lane of a lane-group
   acc_reset(A);
-  for (int w = g; w < nwin; w += kWThreads / 8) {
+  for (int w = g; w < nwin; w += WT / 8) {
     const int p = (w < nsink) ? w : a.sink + kPage * NP + (w - nsink);
     const int slot = (p < a.sink) ? p : a.sink + (p - a.sink) % (a.recent + kPage);
     float kl[8], kh[8], vl[8], vh[8];
@@ -799,7 +802,12 @@ __global__ void __launch_bounds__(kWThreads) vq_window_kernel(const VqAttnArgs a
   }
   __syncthreads();
 
-  // ---- merge: window warps, then every page piece of the (pair, head) segment ----------
+  // ---- merge: window warps, then every page piece of the (pair, head) segment; a thread per
+  //      channel ----------
+  // the page kernel's prefix and partials: wait for that grid (a no-op without a
+  // programmatic dependency)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid >= kD) return;
   const int ch = tid;
   float Mx = -INFINITY, Lt = 0.f, o = 0.f;
   auto fold = [&](float Mp, float lp, float op) {
@@ -812,11 +820,7 @@ __global__ void __launch_bounds__(kWThreads) vq_window_kernel(const VqAttnArgs a
     Mx = Mn;
   };
 #pragma unroll
-  for (int w = 0; w < kWThreads / 32; ++w) fold(wpart[w][kD], wpart[w][kD + 1], wpart[w][ch]);
-
-  // the page kernel's prefix and partials: wait for that grid (a no-op without a
-  // programmatic dependency)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int w = 0; w < WT / 32; ++w) fold(wpart[w][kD], wpart[w][kD + 1], wpart[w][ch]);
   const int n_pairs = (a.B + 1) / 2, pair = b >> 1, rr = b & 1;
   const int p0 = a.pref[pair], nu = a.pref[pair + 1] - p0;
   if (nu > 0) {
@@ -846,6 +850,12 @@ __global__ void __launch_bounds__(kWThreads) vq_window_kernel(const VqAttnArgs a
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int device_sms() {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
 
 template <int NG>
 cudaError_t launch_pages(const VqAttnArgs& a, float scale_log2, cudaStream_t st) {
@@ -887,7 +897,8 @@ cudaError_t launch_vq_attn(const VqAttnArgs& args, void* ws, cudaStream_t st) {
   // programmatic dependent launch: the window kernel may start before the page kernel ends
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)(a.B * a.H));
-  lc.blockDim = dim3(kWThreads);
+  const bool wide = a.B * a.H <= device_sms();
+  lc.blockDim = dim3(wide ? 512 : 128);
   lc.dynamicSmemBytes = 0;
   lc.stream = st;
   cudaLaunchAttribute attr[1];
@@ -895,7 +906,8 @@ cudaError_t launch_vq_attn(const VqAttnArgs& args, void* ws, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, vq_window_kernel, a, scale_log2);
+  return wide ? cudaLaunchKernelEx(&lc, vq_window_kernel<512>, a, scale_log2)
+              : cudaLaunchKernelEx(&lc, vq_window_kernel<128>, a, scale_log2);
 }
 
 }  // namespace kvq

@@ -351,8 +351,8 @@ def kivi_wl_bytes(wl):
 PROFILED_TRAFFIC = {
     "loopvq_b64_6k:vq_pages_kernel+vq_window_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_attn.cu",
-        "ceb0c59fa786a314ca24fe1c7e1e2f02093c5a355da5176c46778d049518c92c",
-        204150016 + 5767424 + 43536640 + 3072),
+        "bbf0c666ed1ae2a3cd96c4a3936d024aaa8a3abeb9e9d96cda2064ad1b816d04",
+        204120320 + 5800192 + 43537408 + 2560),
     "kivi_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
         "ac0f6a6b2606006f6b041ca0b393793f59f998c175c40932fff00244e0367dbf",

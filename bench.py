@@ -351,11 +351,11 @@ def kivi_wl_bytes(wl):
 PROFILED_TRAFFIC = {
     "loopvq_b64_6k:vq_pages_kernel+vq_window_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_attn.cu",
-        "bbf0c666ed1ae2a3cd96c4a3936d024aaa8a3abeb9e9d96cda2064ad1b816d04",
+        "f36914c7e7d958aded7ab901557ca6802d3c27788dfe045653a4b549596a9621",
         204120320 + 5800192 + 43537408 + 2560),
     "kivi_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "ac0f6a6b2606006f6b041ca0b393793f59f998c175c40932fff00244e0367dbf",
+        "4c1a1ac95af0697a2cd61bf09141b1d98e96401994696b6197e1a149fc8a795b",
         228796416 + 4419584),
     "encode_32k:encode_tc_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_encode_tc.cu",
@@ -364,11 +364,11 @@ PROFILED_TRAFFIC = {
     # both quantize kernels (keys per channel, values per token) of one step
     "kivi_quant_32k:kivi_quant_*_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "ac0f6a6b2606006f6b041ca0b393793f59f998c175c40932fff00244e0367dbf",
+        "4c1a1ac95af0697a2cd61bf09141b1d98e96401994696b6197e1a149fc8a795b",
         135003648 + 14183168 + 134271744 + 12630784),
     "kivi4_gqa_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "ac0f6a6b2606006f6b041ca0b393793f59f998c175c40932fff00244e0367dbf",
+        "4c1a1ac95af0697a2cd61bf09141b1d98e96401994696b6197e1a149fc8a795b",
         89876480 + 2961408),
 }
 

@@ -303,12 +303,13 @@ __global__ void __launch_bounds__(128) kivi_append_kernel(const KiviAppendArgs a
 // ranges of the quantized keys, the last split the fp16 key residual. A subgroup is RH query
 // heads of the KV head (RH = 4 when the GQA ratio allows), and the blocks of one split's
 // subgroups are adjacent in launch order so their code reads meet in L2. A quantized split
-// streams its tokens through a 4-stage shared-memory ring of 128-token chunks (TMA bulk
+// streams its tokens through a 3- or 4-stage shared-memory ring of 128-token chunks (TMA bulk
 // copies of the chunk's key codes, key scales and zeros, value codes, value scales and
-// zeros), with a block-wide online softmax per query head across chunks. Tokens whose key is
-// quantized but whose value is still in the fp16 window (the streaming cache's tail) take
-// the value from the window. Partials of all splits merge exactly in the last block of a
-// (request, subgroup) to finish (arrival counter, no spin-wait).
+// zeros); each warp keeps its own online softmax per query head over its 16 tokens of every
+// chunk, and the block merges the warps at the end. Tokens whose key is quantized but whose
+// value is still in the fp16 window (the streaming cache's tail) take the value from the
+// window. Partials of all splits merge exactly in the last block of a (request, subgroup) to
+// finish (arrival counter, no spin-wait).
 constexpr int kAThreads = 256;
 constexpr int kAWarps = kAThreads / 32;
 constexpr int kAChunk = 128;  // tokens per ring stage (4 key groups of 32)
@@ -460,7 +461,8 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
   }
   __syncthreads();
 
-  // running softmax state per query head; the max is block-wide
+  // running softmax state per query head: per warp in the quantized splits, block-wide in the
+  // residual block
   // quantized blocks: lane holds the kOV channels of code words kLW (lane % kLPT) .. + kLW - 1
   // of its token slot; the residual block: channels 4 lane .. 4 lane + 3 in o[r][0..3]
   float M[RH], l[RH], oz[RH];

@@ -3,7 +3,7 @@
 //
 // Follows "LoopVQ: Sub 1-bit KV Cache Quantization for Looped Transformers", method
 // step 5, Algorithm 1 and Figure 5: the step's codebook slice B_t is staged in shared
-// memory, keys and values are rebuilt from D/c = 16 indices per token, keys are rotated by
+// memory, keys and values are rebuilt from D/c indices per token, keys are rotated by
 // RoPE and dotted with the query, the bf16 sink/recent tokens are attended directly, and
 // the partial results are merged exactly (the Flash-Decoding merge the page builds on).
 //
@@ -14,9 +14,8 @@
 // vq_pages_kernel: persistent, one 512-thread block per SM. The work units (head, request
 // pair, chunk of kVqChunk = 32 index pages), head-major, are cut into G equal contiguous
 // shares, one per block, so every SM gets the same number of pages whatever the batch mix,
-// and a block
-// restages the codebook slices only when its share crosses into the next head (at most
-// twice for the usual shapes).
+// and a block restages the codebook slices only when its share crosses into the next head
+// (at most twice for the usual shapes).
 //  * Both slices stay resident, staged by TMA bulk copies: keys in fp32 (128 KB; channels
 //    0..63 and 64..127 as two [256][64] tables), values in fp16 as the cache stores them
 //    ([256][128]; value rounding error ~1e-4 of the output). A codeword's shared-memory address
@@ -30,18 +29,18 @@
 //    64+8s..64+8s+7). The rotated query u = R(p_q - p) q satisfies <R(p_q) q, R(p) k> =
 //    <u, k>, so keys are never rotated: u is built from the cos/sin table at a lane-group's
 //    first page of a piece, advanced one position per token by R(-theta) and one unit (256
-//    positions) by R(-256 theta), and re-read from the table every 16 units. A transposing
+//    positions) by R(-256 theta), and re-read from the table every 64 units. A transposing
 //    shuffle reduction leaves lane s with the score of token s.
 //  * One pass with an online softmax per lane-group; the 8 weights of a page are broadcast
 //    by shuffles and each lane accumulates its 16 value channels from the fp16 table.
-//  * At the end of each piece of a (pair, head) segment the lane-groups merge (shuffles,
-//    then warps through the stage's shared memory) and the block writes the piece's partial
-//    (M, l, o) per request to the workspace.
+//  * At the end of each piece of a (pair, head) segment the lane-groups of a warp merge by
+//    shuffles and every warp writes its partial (M, l, o) to the workspace (eight per
+//    request), with no block-wide barrier.
 //
 // vq_window_kernel: one block (128 threads, or 512 for few long windows) per (request, head)
 // attends the bf16 sink and recent tokens (one token per lane-group step, online softmax) and
-// merges the result with every page piece of its segment, found from the same share
-// arithmetic.
+// merges the result with the warp partials of every page piece of its segment, found from
+// the same share arithmetic.
 #include <cuda_fp16.h>
 
 #include "kvq_common.cuh"

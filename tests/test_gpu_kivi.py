@@ -144,6 +144,26 @@ def test_attention_mixed_value_segment(k_bits, v_bits, rep):
         check_all(case, run(case, C.fill_kivi_cache(case), n_splits).cpu().numpy())
 
 
+def test_attention_repeated_calls_identical():
+    # splits merge in split order and warps in warp order: repeated calls agree bit for bit,
+    # with the same workspace (its arrival counters reset by the last block) or a fresh one
+    case = C.make_kivi_case(316, B=3, H=2, Hq=8, k_bits=4, v_bits=2, n_quant=[992, 640, 1504], n_resid=[77, 128, 5])
+    cache = C.fill_kivi_cache(case)
+    B, Hq = len(case.n_tok), case.cfg.q_heads
+    ws = kvq.make_workspace(case.cfg, B, 5)
+    outs = []
+    for _ in range(3):
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
+        kvq.kvq_decode_attn(case.cfg, cache, 0, 1, C.bf16_tensor(case.q), out, 5, ws)
+        torch.cuda.synchronize()
+        assert kvq.device_error() == 0
+        outs.append(out)
+    outs.append(run(case, cache, 5))
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    check_all(case, outs[0].cpu().numpy())
+
+
 def test_attention_empty_cache_gives_zero():
     case = C.make_kivi_case(311, B=1, H=1, n_quant=[0], n_resid=[0])
     cache = C.fill_kivi_cache(case)

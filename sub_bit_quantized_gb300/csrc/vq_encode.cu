@@ -146,9 +146,10 @@ __device__ __forceinline__ bool roll_due(const int32_t* seq_len, const int32_t* 
 }
 
 // Roll: one block per (layer, block beta, head, K/V, group). The block stages that group's
-// codebook (and each codeword's |e|^2 / 2) in shared memory once and encodes the oldest recent
-// page (8 tokens) of every due sequence against it, two vectors per thread: every codeword
-// row read (a broadcast: all threads of a warp read the same row) serves both. Screening uses
+// codebook (and each codeword's |e|^2 / 2) in shared memory once, codewords 2i and 2i + 1
+// side by side per coordinate, and encodes the oldest recent page (8 tokens) of every due
+// sequence against it, two vectors per thread: every codeword read (a broadcast: all threads
+// of a warp read the same pair) serves both, and one packed FMA advances two codewords. Screening uses
 // acc_r = z.e_r - |e_r|^2 / 2 (one FMA per coordinate; larger is nearer); a vector whose
 // runner-up lies within the error band of its best (8x the fp32 accumulation bound of the
 // codewords that can compete, plus the 1e-6 tie threshold) is decided on distances summed
@@ -156,8 +157,8 @@ __device__ __forceinline__ bool roll_due(const int32_t* seq_len, const int32_t* 
 template <int TC, int C>
 __global__ void __launch_bounds__(256) roll_kernel(const VqRollArgs a) {
   constexpr int G = TC * C, kNG = kD / C, kPageBytes = kPage * kNG;
-  __shared__ __align__(16) float cbs[kCB * G];
-  __shared__ float nh[kCB];
+  __shared__ __align__(16) float2 cbp[kCB / 2 * G];  // codewords 2i and 2i + 1 side by side per coordinate
+  __shared__ __align__(8) float2 nhp[kCB / 2];
   int q = blockIdx.x;
   const int g = q % kNG; q /= kNG;
   const int kv = q % 2; q /= 2;
@@ -170,15 +171,18 @@ __global__ void __launch_bounds__(256) roll_kernel(const VqRollArgs a) {
     any |= roll_due(a.seq_len, a.n_pages, b, a.sink, a.recent, a.max_pages) ? 1 : 0;
   if (!__syncthreads_or(any)) return;
   const float* cb = (kv ? a.cb_v : a.cb_k) + ((((size_t)l * a.NB + beta) * a.H + h) * kNG + g) * (size_t)kCB * G;
-  for (int k = threadIdx.x; k < kCB * G / 4; k += blockDim.x)
-    reinterpret_cast<float4*>(cbs)[k] = __ldg(reinterpret_cast<const float4*>(cb) + k);
   for (int r = threadIdx.x; r < kCB; r += blockDim.x) {
     float n_hi = 0.f, n_lo = 0.f;
 #pragma unroll 4
-    for (int k = 0; k < G; ++k) add_sq_diff(__ldg(cb + (size_t)r * G + k), 0.f, n_hi, n_lo);
-    nh[r] = 0.5f * __fadd_rn(n_hi, n_lo);
+    for (int k = 0; k < G; ++k) {
+      const float e = __ldg(cb + (size_t)r * G + k);
+      add_sq_diff(e, 0.f, n_hi, n_lo);
+      reinterpret_cast<float*>(cbp)[((r >> 1) * G + k) * 2 + (r & 1)] = e;
+    }
+    reinterpret_cast<float*>(nhp)[r] = 0.5f * __fadd_rn(n_hi, n_lo);
   }
   __syncthreads();
+  const float* nh = reinterpret_cast<const float*>(nhp);
   const uint16_t* win = kv ? a.win_v : a.win_k;
   uint8_t* idx_base = (kv ? a.idx_v : a.idx_k) + (((size_t)l * a.NB + beta) * a.max_batch) * a.H * (size_t)a.max_pages * kPageBytes;
   const int n_vec = a.n_seq * kPage;
@@ -226,31 +230,38 @@ __global__ void __launch_bounds__(256) roll_kernel(const VqRollArgs a) {
         for (int i = 0; i < C; ++i) z[u][i * TC + m] = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
       }
     }
-    // ---- screening: best two of acc_r = z.e_r - |e_r|^2/2 for both vectors ---------------
+    // ---- screening: best two of acc_r = z.e_r - |e_r|^2/2 for both vectors, codewords two
+    //      at a time with packed FMAs (each lane the same fma sequence as a scalar loop) ----
     float best[2] = {-INFINITY, -INFINITY}, second[2] = {-INFINITY, -INFINITY};
     int bi[2] = {0, 0};
-#pragma unroll 2
-    for (int r = 0; r < kCB; ++r) {
-      const float4* er = reinterpret_cast<const float4*>(cbs + r * G);
-      float acc0 = -nh[r], acc1 = acc0;
+    float2 zz[2][G];
 #pragma unroll
-      for (int k4 = 0; k4 < G / 4; ++k4) {
-        const float4 e = er[k4];
-        acc0 = fmaf(z[0][4 * k4], e.x, acc0);
-        acc1 = fmaf(z[1][4 * k4], e.x, acc1);
-        acc0 = fmaf(z[0][4 * k4 + 1], e.y, acc0);
-        acc1 = fmaf(z[1][4 * k4 + 1], e.y, acc1);
-        acc0 = fmaf(z[0][4 * k4 + 2], e.z, acc0);
-        acc1 = fmaf(z[1][4 * k4 + 2], e.z, acc1);
-        acc0 = fmaf(z[0][4 * k4 + 3], e.w, acc0);
-        acc1 = fmaf(z[1][4 * k4 + 3], e.w, acc1);
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int k = 0; k < G; ++k) zz[u][k] = make_float2(z[u][k], z[u][k]);
+#pragma unroll 2
+    for (int rp = 0; rp < kCB / 2; ++rp) {
+      const float4* er = reinterpret_cast<const float4*>(cbp + rp * G);
+      const float2 n2 = nhp[rp];
+      float2 acc[2] = {make_float2(-n2.x, -n2.y), make_float2(-n2.x, -n2.y)};
+#pragma unroll
+      for (int k2 = 0; k2 < G / 2; ++k2) {
+        const float4 e = er[k2];  // (e_r, e_r+1) at coordinates 2 k2 and 2 k2 + 1
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          acc[u] = __ffma2_rn(zz[u][2 * k2], make_float2(e.x, e.y), acc[u]);
+          acc[u] = __ffma2_rn(zz[u][2 * k2 + 1], make_float2(e.z, e.w), acc[u]);
+        }
       }
-      const float accs[2] = {acc0, acc1};
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        second[u] = fmaxf(second[u], fminf(accs[u], best[u]));
-        bi[u] = (accs[u] > best[u]) ? r : bi[u];
-        best[u] = fmaxf(best[u], accs[u]);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {  // codeword 2 rp, then 2 rp + 1
+          const float av = h2 ? acc[u].y : acc[u].x;
+          second[u] = fmaxf(second[u], fminf(av, best[u]));
+          bi[u] = (av > best[u]) ? 2 * rp + h2 : bi[u];
+          best[u] = fmaxf(best[u], av);
+        }
       }
     }
     // ---- band check; exact decision of near-ties; index out ----------------------------------
@@ -268,14 +279,14 @@ __global__ void __launch_bounds__(256) roll_kernel(const VqRollArgs a) {
       if (second[u] >= best[u] - band) {
         float bd = INFINITY;
         for (int r = 0; r < kCB; ++r) {
-          const float* er = cbs + r * G;
+          const float* er = reinterpret_cast<const float*>(cbp + (r >> 1) * G) + (r & 1);  // stride 2
           float acc = -nh[r];  // the screening value again, computed the same way
 #pragma unroll
-          for (int k = 0; k < G; ++k) acc = fmaf(z[u][k], er[k], acc);
+          for (int k = 0; k < G; ++k) acc = fmaf(z[u][k], er[2 * k], acc);
           if (acc < best[u] - band) continue;
           float dh = 0.f, dl = 0.f;
 #pragma unroll
-          for (int k = 0; k < G; ++k) add_sq_diff(z[u][k], er[k], dh, dl);
+          for (int k = 0; k < G; ++k) add_sq_diff(z[u][k], er[2 * k], dh, dl);
           const float dd = __fadd_rn(dh, dl);
           if (dd < bd) {  // increasing r: the lowest index wins exact ties
             bd = dd;

@@ -322,9 +322,10 @@ kvq_status kvq_kivi_append(const kvq_kivi_cfg* cfg, const kvq_kivi_cache* cache,
  *   pages), head-major, are cut into n_splits equal contiguous shares, one per block; each
  *   block writes a partial softmax for every piece of a (request, head) it covers and a
  *   second kernel merges them with the bf16 window tokens. 0 = one block per SM.
- *   KIVI: splits of the quantized keys per (request, KV head), plus one block for the
- *   fp16 key residual, merged by the last block of each; a block serves up to 4 query
- *   heads of its KV head, so their codes are read once.
+ *   KIVI: token splits per (request, KV head): split k takes an equal range of the
+ *   quantized keys and the last split also the fp16 residual (its bytes counted in the
+ *   ranges), merged by the last block of each (request, KV head) to finish; a block serves
+ *   up to 4 query heads of its KV head, so their codes are read once.
  * ws: device workspace of at least kvq_decode_workspace_size() bytes (may be NULL when
  *   that size is 0; LoopVQ always needs one). A KIVI workspace must be zero-filled before
  *   its first use; every call leaves it reusable. Two calls that run at the same time need

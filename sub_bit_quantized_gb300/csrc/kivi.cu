@@ -338,7 +338,7 @@ struct AttnLayout {
   // float l [8 warps][RH], float M [8 warps][RH], int flag, int released [stages], int issued
   static constexpr int kOffRed = kOffBias + RH * 8 * 4;
   static constexpr int kOffBar = kOffRed + ((2 * kAWarps * RH + 2 + kAStages) * 4 + 15) / 16 * 16;  // mbarriers + failed
-  static constexpr int kOffSc = kOffBar + 64;             // float scores [RH][max(128, residual)]
+  static constexpr int kSmem = kOffBar + 64;
   // value phase: a lane takes kLW code words of one token, all in one value group (with one
   // query head the whole group, so its scale and zero-point are read once); a warp-step
   // covers kTS tokens
@@ -424,8 +424,8 @@ __device__ __forceinline__ bool kivi_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 template <int KB, int VB, int RH>
-__global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks) kivi_attn_kernel(const KiviAttnArgs a, const float scale_log2,
-                                                              const int sc_stride) {
+__global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
+    kivi_attn_kernel(const KiviAttnArgs a, const float scale_log2) {
   using L = AttnLayout<KB, VB, RH>;
   extern __shared__ __align__(128) unsigned char sma[];
   float* qs = reinterpret_cast<float*>(sma + L::kOffQ);
@@ -438,13 +438,12 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
   int* issued = released + L::kAStages;                      // chunks whose copies were issued
   uint64_t* full = reinterpret_cast<uint64_t*>(sma + L::kOffBar);
   volatile int* failed = reinterpret_cast<volatile int*>(sma + L::kOffBar + L::kAStages * 8);
-  float* sc = reinterpret_cast<float*>(sma + L::kOffSc);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rep = a.Hq / a.H, n_sub = rep / RH;
   const int split = blockIdx.x / n_sub, sub = blockIdx.x % n_sub, b = blockIdx.y, hk = blockIdx.z;
-  const int n_total = gridDim.x / n_sub;  // quantized splits + the residual block
+  const int n_total = gridDim.x / n_sub;  // token splits; the last one also takes the fp16 residual
   const int R = a.residual;
-  const bool resid_block = (R > 0) && (split == n_total - 1);
+  const bool has_resid = (R > 0) && (split == n_total - 1);
   const size_t bh = (size_t)b * a.H + hk;                       // KV row of (b, hk)
   const size_t bq0 = (size_t)b * a.Hq + (size_t)hk * rep + sub * RH;  // first query row
   const int NQK = min(max(a.n_quant_k[b], 0), a.max_tokens) / kGroup * kGroup;
@@ -461,12 +460,12 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
   }
   __syncthreads();
 
-  // running softmax state per query head: per warp in the quantized splits, block-wide in the
-  // residual block
-  // quantized blocks: lane holds the kOV channels of code words kLW (lane % kLPT) .. + kLW - 1
-  // of its token slot; the residual block: channels 4 lane .. 4 lane + 3 in o[r][0..3]
+  // running softmax state per query head, per warp; a lane holds the kOV channels of code
+  // words kLW (lane % kLPT) .. + kLW - 1 of its token slot (kTS token slots per warp step)
   float M[RH], l[RH], oz[RH];
   float o[RH][L::kOV];
+  const int lt = lane % L::kLPT, ts = lane / L::kLPT;
+  const int w0 = lt * L::kLW, gv = w0 / L::kWPG;  // the lane's first code word, its value group
 #pragma unroll
   for (int r = 0; r < RH; ++r) {
     M[r] = -INFINITY;
@@ -484,16 +483,36 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
     l[r] *= f;
     M[r] = Mn;
   };
-  // max of s[0, n) (every warp computes it)
-  auto scores_max = [&](const float* s, int n) {
-    float m = -INFINITY;
-    for (int i = lane; i < n; i += 32) m = fmaxf(m, s[i]);
+  // the lane's value channels of fp16 value-ring row t % R, weighted by p[r]
+  auto value_fp16 = [&](int t, const float (&p)[RH]) {
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-    return m;
+    for (int w = 0; w < L::kLW; ++w) {
+      const uint4* vr = reinterpret_cast<const uint4*>(a.v_resid + (bh * R + t % R) * kD + (w0 + w) * L::kCPWv);
+      uint32_t hv[L::kCPWv / 2];
+#pragma unroll
+      for (int k4 = 0; k4 < L::kCPWv / 8; ++k4) {
+        const uint4 u = __ldg(vr + k4);
+        hv[4 * k4] = u.x;
+        hv[4 * k4 + 1] = u.y;
+        hv[4 * k4 + 2] = u.z;
+        hv[4 * k4 + 3] = u.w;
+      }
+#pragma unroll
+      for (int j = 0; j < L::kPV; ++j) {
+        const int e0 = j, e1 = L::kPV + j, i = w * L::kCPWv + 2 * j;
+        const float v0 = h2f((e0 & 1) ? (hv[e0 >> 1] >> 16) : (hv[e0 >> 1] & 0xFFFFu));
+        const float v1 = h2f((e1 & 1) ? (hv[e1 >> 1] >> 16) : (hv[e1 >> 1] & 0xFFFFu));
+        const float sj = pow2_pos(VB * j);
+#pragma unroll
+        for (int r = 0; r < RH; ++r) {
+          o[r][i] = fmaf(p[r] * sj, v0, o[r][i]);
+          o[r][i + 1] = fmaf(p[r] * sj, v1, o[r][i + 1]);
+        }
+      }
+    }
   };
 
-  if (!resid_block) {
+  {
     // ================================ quantized keys ========================================
     const int t0 = split * a.tok_per_split;
     const int t1 = min(NQK, t0 + a.tok_per_split);
@@ -604,8 +623,6 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
           }
         }
         // ---- values: kTS tokens of the warp per step ----
-        const int lt = lane % L::kLPT, ts = lane / L::kLPT;
-        const int w0 = lt * L::kLW, gv = w0 / L::kWPG;  // the lane's first code word, its value group
         // kFull: every token of the warp has a quantized value, so the steps need no per-token
         // test (warp-uniform; only the streaming cache's tail takes the checked path)
         auto value_steps = [&](auto full_tag) {
@@ -644,33 +661,7 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
                 }
               }
             } else {  // key quantized, value still in the fp16 window
-              const int t = tc0 + tv;
-#pragma unroll
-              for (int w = 0; w < L::kLW; ++w) {
-                const uint4* vr =
-                    reinterpret_cast<const uint4*>(a.v_resid + (bh * R + t % R) * kD + (w0 + w) * L::kCPWv);
-                uint32_t hv[L::kCPWv / 2];
-#pragma unroll
-                for (int k4 = 0; k4 < L::kCPWv / 8; ++k4) {
-                  const uint4 u = __ldg(vr + k4);
-                  hv[4 * k4] = u.x;
-                  hv[4 * k4 + 1] = u.y;
-                  hv[4 * k4 + 2] = u.z;
-                  hv[4 * k4 + 3] = u.w;
-                }
-#pragma unroll
-                for (int j = 0; j < L::kPV; ++j) {
-                  const int e0 = j, e1 = L::kPV + j, i = w * L::kCPWv + 2 * j;
-                  const float v0 = h2f((e0 & 1) ? (hv[e0 >> 1] >> 16) : (hv[e0 >> 1] & 0xFFFFu));
-                  const float v1 = h2f((e1 & 1) ? (hv[e1 >> 1] >> 16) : (hv[e1 >> 1] & 0xFFFFu));
-                  const float sj = pow2_pos(VB * j);
-#pragma unroll
-                  for (int r = 0; r < RH; ++r) {
-                    o[r][i] = fmaf(p[r] * sj, v0, o[r][i]);
-                    o[r][i + 1] = fmaf(p[r] * sj, v1, o[r][i + 1]);
-                  }
-                }
-              }
+              value_fp16(tc0 + tv, p);
             }
           }
         };
@@ -693,47 +684,58 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
     if (tid == 0 && *failed)
       for (int c = max(0, *issued - L::kAStages); c < *issued; ++c)
         mbar_wait_bounded(&full[c % L::kAStages], (c / L::kAStages) & 1);
-  } else {
-    // ================================ fp16 key residual =====================================
+  }
+  if (has_resid) {
+    // ============ fp16 residual (keys and values), after the last split's quantized keys ============
+    // warp w takes residual tokens 16 w .. 16 w + 15 of every 128: scores with lanes 0-15 on
+    // channels 0-63 and lanes 16-31 on 64-127, the same warp-local softmax, then the values
+    // from the fp16 ring
     const int NR = max(0, min(a.n_tok[b] - NQK, R));
-    for (int rr = tid; rr < NR; rr += kAThreads) {  // keys: a thread per token
-      const uint4* kr = reinterpret_cast<const uint4*>(a.k_resid + (bh * R + rr) * kD);
+    for (int rb = 0; rb < NR; rb += 16 * kAWarps) {
+      const int tw = rb + 16 * warp;
+      if (tw >= NR) continue;  // warp-uniform
+      const int rr = tw + (lane & 15), chh = lane >> 4;
+      const bool valid = rr < NR;
       float acc[RH];
 #pragma unroll
       for (int r = 0; r < RH; ++r) acc[r] = 0.f;
-#pragma unroll 4
-      for (int k8 = 0; k8 < kD / 8; ++k8) {
+      const uint4* kr = reinterpret_cast<const uint4*>(a.k_resid + (bh * R + min(rr, NR - 1)) * kD + 64 * chh);
+#pragma unroll 1
+      for (int k8 = 0; k8 < 8; ++k8) {
         const uint4 v = __ldg(kr + k8);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t hw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[i]));
 #pragma unroll
           for (int r = 0; r < RH; ++r) {
-            acc[r] = fmaf(qs[r * kD + k8 * 8 + 2 * i], f.x, acc[r]);
-            acc[r] = fmaf(qs[r * kD + k8 * 8 + 2 * i + 1], f.y, acc[r]);
+            const float2 q2 = *reinterpret_cast<const float2*>(qs + r * kD + 64 * chh + 8 * k8 + 2 * i);
+            acc[r] = fmaf(q2.x, f.x, fmaf(q2.y, f.y, acc[r]));
           }
         }
       }
-#pragma unroll
-      for (int r = 0; r < RH; ++r) sc[r * sc_stride + rr] = acc[r] * scale_log2;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < RH; ++r) rescale_to(r, scores_max(sc + r * sc_stride, NR));
-    for (int rr = warp; rr < NR; rr += kAWarps) {  // values: a warp per token, lane 4 channels
-      const int t = NQK + rr;
-      const uint2 v = __ldg(reinterpret_cast<const uint2*>(a.v_resid + (bh * R + t % R) * kD + lane * 4));
-      const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
-      const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+      float pk[RH];
 #pragma unroll
       for (int r = 0; r < RH; ++r) {
-        const float p = exp2f(sc[r * sc_stride + rr] - M[r]);
-        l[r] += p;
-        o[r][0] = fmaf(p, f0.x, o[r][0]);
-        o[r][1] = fmaf(p, f0.y, o[r][1]);
-        o[r][2] = fmaf(p, f1.x, o[r][2]);
-        o[r][3] = fmaf(p, f1.y, o[r][3]);
+        float sc_r = acc[r] + __shfl_xor_sync(0xFFFFFFFFu, acc[r], 16);
+        sc_r = valid ? sc_r * scale_log2 : -INFINITY;
+        float mx = sc_r;
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+        if (mx > M[r] + 8.f) rescale_to(r, mx);  // warp-uniform; token tw is valid
+        pk[r] = valid ? exp2f(sc_r - M[r]) : 0.f;
+        float ls = pk[r];
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, off);
+        l[r] += ls;
+      }
+#pragma unroll
+      for (int step = 0; step < 16 / L::kTS; ++step) {
+        float p[RH];
+#pragma unroll
+        for (int r = 0; r < RH; ++r) p[r] = __shfl_sync(0xFFFFFFFFu, pk[r], L::kTS * step + ts);
+        const int tv = tw + L::kTS * step + ts;
+        if (tv < NR) value_fp16(NQK + tv, p);
       }
     }
   }
@@ -741,7 +743,7 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
   // ---- warps -> block: sum o - oz and l over the warps (one max per head for the block) ----
   __syncthreads();  // the ring is idle
   float* ored = reinterpret_cast<float*>(sma);  // [warp][RH][128]
-  if (!resid_block) {  // the token slots of a lane position meet, then kLPT lanes hold 128 channels
+  {  // the token slots of a lane position meet, then kLPT lanes hold 128 channels
 #pragma unroll
     for (int r = 0; r < RH; ++r) {
 #pragma unroll
@@ -765,11 +767,6 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
         }
       }
     }
-  } else {
-#pragma unroll
-    for (int r = 0; r < RH; ++r)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) ored[(warp * RH + r) * kD + lane * 4 + i] = o[r][i];
   }
   if (lane == 0)
 #pragma unroll
@@ -854,8 +851,8 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
 }
 
 template <int KB, int VB, int RH>
-size_t attn_smem(int residual) {
-  return (size_t)AttnLayout<KB, VB, RH>::kOffSc + 4 * (size_t)RH * max(kAChunk, residual);
+size_t attn_smem(int) {
+  return (size_t)AttnLayout<KB, VB, RH>::kSmem;
 }
 
 template <int KB, int VB, int RH>
@@ -865,9 +862,9 @@ cudaError_t launch_attn(const KiviAttnArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)kD);
   const int n_sub = (a.Hq / a.H) / RH;
-  // quantized splits, plus one block for the fp16 residual segment, per head subgroup
-  dim3 grid((a.n_split + (a.residual > 0 ? 1 : 0)) * n_sub, a.B, a.H);
-  kivi_attn_kernel<KB, VB, RH><<<grid, kAThreads, smem, st>>>(a, scale_log2, max(kAChunk, a.residual));
+  // token splits per head subgroup; the last split also attends the fp16 residual
+  dim3 grid(a.n_split * n_sub, a.B, a.H);
+  kivi_attn_kernel<KB, VB, RH><<<grid, kAThreads, smem, st>>>(a, scale_log2);
   return cudaGetLastError();
 }
 
@@ -902,6 +899,36 @@ size_t kivi_attn_smem_bytes(int k_bits, int v_bits, int rh, int residual) {
   if (k_bits == 2 && v_bits == 4) return smem_rh<2, 4>(rh, residual);
   if (k_bits == 4 && v_bits == 2) return smem_rh<4, 2>(rh, residual);
   return smem_rh<4, 4>(rh, residual);
+}
+
+template <int KB, int VB, int RH>
+int blocks_per_sm_of() {
+  int n = 0;
+  const size_t smem = attn_smem<KB, VB, RH>(0);
+  if (cudaFuncSetAttribute(kivi_attn_kernel<KB, VB, RH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kivi_attn_kernel<KB, VB, RH>, kAThreads, smem) != cudaSuccess)
+    return 4;
+  return n > 0 ? n : 1;
+}
+template <int KB, int VB>
+int blocks_per_sm_rh(int rh) {
+  if (rh == 4) return blocks_per_sm_of<KB, VB, 4>();
+  if (rh == 2) return blocks_per_sm_of<KB, VB, 2>();
+  return blocks_per_sm_of<KB, VB, 1>();
+}
+
+int kivi_attn_blocks_per_sm(int k_bits, int v_bits, int rh) {
+  // one query per kernel instance and process (a property of the build and the GPU model)
+  static int cached[2][2][3] = {};
+  int& c = cached[k_bits == 4][v_bits == 4][rh == 4 ? 2 : rh == 2 ? 1 : 0];
+  if (c == 0) {
+    if (k_bits == 2 && v_bits == 2) c = blocks_per_sm_rh<2, 2>(rh);
+    else if (k_bits == 2 && v_bits == 4) c = blocks_per_sm_rh<2, 4>(rh);
+    else if (k_bits == 4 && v_bits == 2) c = blocks_per_sm_rh<4, 2>(rh);
+    else c = blocks_per_sm_rh<4, 4>(rh);
+  }
+  return c;
 }
 
 cudaError_t launch_kivi_quantize(const KiviQuantArgs& a, cudaStream_t s) {

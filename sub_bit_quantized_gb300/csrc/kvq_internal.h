@@ -156,6 +156,7 @@ struct KiviAttnArgs {
 // query heads one attention block serves (a divisor of Hq / H, at most 4)
 int kivi_heads_per_block(int rep);
 size_t kivi_attn_smem_bytes(int k_bits, int v_bits, int heads_per_block, int residual);
+int kivi_attn_blocks_per_sm(int k_bits, int v_bits, int heads_per_block);  // resident attention blocks per SM
 int kivi_attn_max_tok_per_split(int residual);
 cudaError_t launch_kivi_attn(const KiviAttnArgs& a, cudaStream_t s);
 

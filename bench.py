@@ -355,8 +355,8 @@ PROFILED_TRAFFIC = {
         204120320 + 5800192 + 43537408 + 2560),
     "kivi_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "4c1a1ac95af0697a2cd61bf09141b1d98e96401994696b6197e1a149fc8a795b",
-        228796416 + 4419584),
+        "a11cf430e855f4e50ddc6957cd14a05f864bdd835c5be9db09fde2acfc0161bc",
+        228804096 + 3292416),
     "encode_32k:encode_tc_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_encode_tc.cu",
         "42e194feda74fa6a5e78177d6a39c04b4785de3db0db60096413109cc4b1cd1a",
@@ -364,12 +364,12 @@ PROFILED_TRAFFIC = {
     # both quantize kernels (keys per channel, values per token) of one step
     "kivi_quant_32k:kivi_quant_*_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "4c1a1ac95af0697a2cd61bf09141b1d98e96401994696b6197e1a149fc8a795b",
-        135003648 + 14183168 + 134271744 + 12630784),
+        "a11cf430e855f4e50ddc6957cd14a05f864bdd835c5be9db09fde2acfc0161bc",
+        135021568 + 14449920 + 134288640 + 12688384),
     "kivi4_gqa_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "4c1a1ac95af0697a2cd61bf09141b1d98e96401994696b6197e1a149fc8a795b",
-        89876480 + 2961408),
+        "a11cf430e855f4e50ddc6957cd14a05f864bdd835c5be9db09fde2acfc0161bc",
+        89877248 + 2775040),
 }
 
 

@@ -32,7 +32,8 @@
 //    positions) by R(-256 theta), and re-read from the table every 64 units. A transposing
 //    shuffle reduction leaves lane s with the score of token s.
 //  * One pass with an online softmax per lane-group; the 8 weights of a page are broadcast
-//    by shuffles and each lane accumulates its 16 value channels from the fp16 table.
+//    by shuffles (as fp16) and each lane accumulates its 16 value channels from the fp16
+//    table with the mixed-precision FMA (fp16 operands, fp32 sums: no conversions).
 //  * At the end of each piece of a (pair, head) segment the lane-groups of a warp merge by
 //    shuffles and every warp writes its partial (M, l, o) to the workspace (eight per
 //    request), with no block-wide barrier.
@@ -101,19 +102,31 @@ __device__ __forceinline__ void ldg8_bf16_perm(const uint16_t* p, int o0, float 
   v[0] = bf16_lo(a.x); v[1] = bf16_hi(a.x); v[2] = bf16_lo(a.y); v[3] = bf16_hi(a.y);
   v[4] = bf16_lo(b.x); v[5] = bf16_hi(b.x); v[6] = bf16_lo(b.y); v[7] = bf16_hi(b.y);
 }
-// 8 consecutive fp16 values (one 128-bit shared load), natural order
-__device__ __forceinline__ void lds8_fp16(const unsigned char* p, float2 (&v)[4]) {
-  const uint4 w = *reinterpret_cast<const uint4*>(p);
-  v[0] = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
-  v[1] = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
-  v[2] = __half22float2(*reinterpret_cast<const __half2*>(&w.z));
-  v[3] = __half22float2(*reinterpret_cast<const __half2*>(&w.w));
+// acc += p * v for the two fp16 values of w (low half -> acc.x), p an fp16 in the low 16 bits
+// of ph: the mixed-precision FMA takes fp16 operands and accumulates in fp32 (the product of
+// two fp16 is exact in fp32), so a value row needs no separate conversion to fp32
+__device__ __forceinline__ void fma_f16x2(float2& acc, uint32_t w, uint32_t ph) {
+  asm("{\n\t.reg .b16 l, h, p;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.u16.u32 p, %3;\n\t"
+      "fma.rn.f32.f16 %0, l, p, %0;\n\t"
+      "fma.rn.f32.f16 %1, h, p, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "r"(w), "r"(ph));
 }
-// 4 consecutive fp16 values (one 64-bit shared load), natural order
-__device__ __forceinline__ void lds4_fp16(const unsigned char* p, float2& v0, float2& v1) {
+// 8 consecutive fp16 values (one 128-bit shared load) into acc[0..3]
+__device__ __forceinline__ void lds8_fp16_fma(const unsigned char* p, uint32_t ph, float2 (&acc)[4]) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  fma_f16x2(acc[0], w.x, ph);
+  fma_f16x2(acc[1], w.y, ph);
+  fma_f16x2(acc[2], w.z, ph);
+  fma_f16x2(acc[3], w.w, ph);
+}
+// 4 consecutive fp16 values (one 64-bit shared load) into a0, a1
+__device__ __forceinline__ void lds4_fp16_fma(const unsigned char* p, uint32_t ph, float2& a0, float2& a1) {
   const uint2 w = *reinterpret_cast<const uint2*>(p);
-  v0 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
-  v1 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+  fma_f16x2(a0, w.x, ph);
+  fma_f16x2(a1, w.y, ph);
 }
 // byte offset (index << 8) | lane_byte, the index being byte k of w (lane_byte < 256)
 template <int K>
@@ -659,30 +672,26 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
       }
       transpose_reduce8(part, s, gmask);
       const float p = online_weights(A, part[0] * scale_log2, gmask);
+      // the weights enter the value sums rounded to fp16 (relative error 2^-12; the
+      // normaliser l keeps the fp32 weights)
+      const uint32_t ph = __half_as_ushort(__float2half_rn(p));
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float pj = __shfl_sync(gmask, p, (lane & 24) + j);
+        const uint32_t pj = __shfl_sync(gmask, ph, (lane & 24) + j);
         const uint32_t wd = (j < 2) ? rowv.x : (j < 4) ? rowv.y : (j < 6) ? rowv.z : rowv.w;
         const uint32_t avl = (j & 1) ? row_off<2>(wd, vb0) : row_off<0>(wd, vb0);
         const uint32_t avh = (j & 1) ? row_off<3>(wd, vb1) : row_off<1>(wd, vb1);
-        float2 vl[4], vh[4];
         if constexpr (NG == 32) {  // channels 8s .. 8s + 3 and 8s + 4 .. 8s + 7 from two codewords
           const uint32_t wd2 = (j < 2) ? rowv2.x : (j < 4) ? rowv2.y : (j < 6) ? rowv2.z : rowv2.w;
           const uint32_t avl2 = (j & 1) ? row_off<2>(wd2, vb0 + 8) : row_off<0>(wd2, vb0 + 8);
           const uint32_t avh2 = (j & 1) ? row_off<3>(wd2, vb1 + 8) : row_off<1>(wd2, vb1 + 8);
-          lds4_fp16(vsb + avl, vl[0], vl[1]);
-          lds4_fp16(vsb + avl2, vl[2], vl[3]);
-          lds4_fp16(vsb + avh, vh[0], vh[1]);
-          lds4_fp16(vsb + avh2, vh[2], vh[3]);
+          lds4_fp16_fma(vsb + avl, pj, A.ol[0], A.ol[1]);
+          lds4_fp16_fma(vsb + avl2, pj, A.ol[2], A.ol[3]);
+          lds4_fp16_fma(vsb + avh, pj, A.oh[0], A.oh[1]);
+          lds4_fp16_fma(vsb + avh2, pj, A.oh[2], A.oh[3]);
         } else {
-          lds8_fp16(vsb + avl, vl);
-          lds8_fp16(vsb + avh, vh);
-        }
-        const float2 p2 = make_float2(pj, pj);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          A.ol[k] = __ffma2_rn(p2, vl[k], A.ol[k]);
-          A.oh[k] = __ffma2_rn(p2, vh[k], A.oh[k]);
+          lds8_fp16_fma(vsb + avl, pj, A.ol);
+          lds8_fp16_fma(vsb + avh, pj, A.oh);
         }
       }
     }

@@ -28,9 +28,11 @@
 //  * 8 lanes per page, lane s owns the RoPE partner groups s and s+8 (channels 8s..8s+7 and
 //    64+8s..64+8s+7). The rotated query u = R(p_q - p) q satisfies <R(p_q) q, R(p) k> =
 //    <u, k>, so keys are never rotated: u is built from the cos/sin table at a lane-group's
-//    first page of a piece, advanced one position per token by R(-theta) and one unit (256
-//    positions) by R(-256 theta), and re-read from the table every 64 units. A transposing
-//    shuffle reduction leaves lane s with the score of token s.
+//    first page of a piece, advanced one position per token by R(-theta) and, from the last
+//    token of a page to the first of the lane-group's next page (one unit, 256 positions,
+//    later), by R(-249 theta), so a lane keeps a single copy of u; it is re-read from the
+//    table every 64 units. Every score is one chain of packed FMAs. A transposing shuffle
+//    reduction leaves lane s with the score of token s.
 //  * One pass with an online softmax per lane-group; the 8 weights of a page are broadcast
 //    by shuffles (as fp16) and each lane accumulates its 16 value channels from the fp16
 //    table with the mixed-precision FMA (fp16 operands, fp32 sums: no conversions).
@@ -160,12 +162,12 @@ __device__ __forceinline__ void transpose_reduce8(float (&p)[8], int s, unsigned
 // u <- R(-a) u for 8 channel pairs held as 4 float2 (pairs k, k+1) per half:
 //   lo' = lo cos(a) + hi sin(a),  hi' = hi cos(a) - lo sin(a)
 __device__ __forceinline__ void rotate8(float2 (&ul)[4], float2 (&uh)[4], const float2 (&c)[4],
-                                        const float2 (&sn)[4], const float2 (&nsn)[4]) {
+                                        const float2 (&sn)[4]) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const float2 l = ul[k], hh = uh[k];
     ul[k] = __ffma2_rn(l, c[k], __fmul2_rn(hh, sn[k]));
-    uh[k] = __ffma2_rn(l, nsn[k], __fmul2_rn(hh, c[k]));
+    uh[k] = __ffma2_rn(make_float2(-l.x, -l.y), sn[k], __fmul2_rn(hh, c[k]));
   }
 }
 
@@ -488,13 +490,14 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
       }
   }
   if (tid < 8 && a.max_ctx > kJump) {
-    // cos/sin(kJump theta_i) for slot tid in that slot's half order, stored [chunk][slot] so
-    // that the 8 slots of a lane-group read 8 consecutive float4s (no bank conflicts)
+    // cos/sin((kJump - 7) theta_i) for slot tid in that slot's half order, stored [chunk][slot]
+    // so that the 8 slots of a lane-group read 8 consecutive float4s (no bank conflicts): the
+    // step from the last token of one of a lane-group's pages to the first of its next
     float4* jt = reinterpret_cast<float4*>(smem + Ly::kOffJ);
     const int jo0 = (tid & 4) ? 4 : 0;
     float c8[8], s8[8];
-    ldg8_perm(a.rope_cos + (size_t)kJump * (kD / 2) + 8 * tid, jo0, c8);
-    ldg8_perm(a.rope_sin + (size_t)kJump * (kD / 2) + 8 * tid, jo0, s8);
+    ldg8_perm(a.rope_cos + (size_t)(kJump - 7) * (kD / 2) + 8 * tid, jo0, c8);
+    ldg8_perm(a.rope_sin + (size_t)(kJump - 7) * (kD / 2) + 8 * tid, jo0, s8);
     jt[0 * 8 + tid] = make_float4(c8[0], c8[1], c8[2], c8[3]);
     jt[1 * 8 + tid] = make_float4(c8[4], c8[5], c8[6], c8[7]);
     jt[2 * 8 + tid] = make_float4(s8[0], s8[1], s8[2], s8[3]);
@@ -510,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
   const int lg = tid >> 3;
   const int r = lg / kChunk, po = lg % kChunk;  // this lane-group's request and page slot
 
-  float2 cth[4], sth[4], nsth[4];
+  float2 cth[4], sth[4];
   {
     float c8[8], s8[8];
     const int row = (a.max_ctx > 1) ? 1 : 0;
@@ -520,14 +523,14 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
     for (int k = 0; k < 4; ++k) {
       cth[k] = make_float2(c8[2 * k], c8[2 * k + 1]);
       sth[k] = make_float2(s8[2 * k], s8[2 * k + 1]);
-      nsth[k] = make_float2(-s8[2 * k], -s8[2 * k + 1]);
     }
   }
-  float2 u0l[4], u0h[4];
+  // the lane-group's rotated query, advanced token by token through its pages
+  float2 ulo[4], uhi[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    u0l[k] = make_float2(0.f, 0.f);
-    u0h[k] = make_float2(0.f, 0.f);
+    ulo[k] = make_float2(0.f, 0.f);
+    uhi[k] = make_float2(0.f, 0.f);
   }
   Acc A;
   acc_reset(A);
@@ -619,26 +622,18 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
         ldg8_perm(a.rope_sin + (size_t)d * (kD / 2) + 8 * s, o0, s8);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          u0l[k] = make_float2(ql[2 * k] * c8[2 * k] - qh[2 * k] * s8[2 * k],
-                               ql[2 * k + 1] * c8[2 * k + 1] - qh[2 * k + 1] * s8[2 * k + 1]);
-          u0h[k] = make_float2(qh[2 * k] * c8[2 * k] + ql[2 * k] * s8[2 * k],
-                               qh[2 * k + 1] * c8[2 * k + 1] + ql[2 * k + 1] * s8[2 * k + 1]);
+          ulo[k] = make_float2(ql[2 * k] * c8[2 * k] - qh[2 * k] * s8[2 * k],
+                                ql[2 * k + 1] * c8[2 * k + 1] - qh[2 * k + 1] * s8[2 * k + 1]);
+          uhi[k] = make_float2(qh[2 * k] * c8[2 * k] + ql[2 * k] * s8[2 * k],
+                                qh[2 * k + 1] * c8[2 * k + 1] + ql[2 * k + 1] * s8[2 * k + 1]);
         }
-      } else {  // kJump positions later
+      } else {  // the next page: kJump - 7 positions after this lane-group's last token
         const float4 c0 = jt[0], c1 = jt[8], s0 = jt[16], s1 = jt[24];
         const float2 cj[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w), make_float2(c1.x, c1.y),
                               make_float2(c1.z, c1.w)};
         const float2 sj[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
                               make_float2(s1.z, s1.w)};
-        const float2 nsj[4] = {make_float2(-s0.x, -s0.y), make_float2(-s0.z, -s0.w), make_float2(-s1.x, -s1.y),
-                               make_float2(-s1.z, -s1.w)};
-        rotate8(u0l, u0h, cj, sj, nsj);
-      }
-      float2 ul[4], uh2[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        ul[k] = u0l[k];
-        uh2[k] = u0h[k];
+        rotate8(ulo, uhi, cj, sj);
       }
       float part[8];
 #pragma unroll
@@ -658,17 +653,16 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
         const float4 lb = *reinterpret_cast<const float4*>(ksb + al1);
         const float4 ha = *reinterpret_cast<const float4*>(ksb + kKSliceBytes / 2 + ah0);
         const float4 hb = *reinterpret_cast<const float4*>(ksb + kKSliceBytes / 2 + ah1);
-        float2 acc0 = __fmul2_rn(ul[0], make_float2(la.x, la.y));
-        float2 acc1 = __fmul2_rn(uh2[0], make_float2(ha.x, ha.y));
-        acc0 = __ffma2_rn(ul[1], make_float2(la.z, la.w), acc0);
-        acc1 = __ffma2_rn(uh2[1], make_float2(ha.z, ha.w), acc1);
-        acc0 = __ffma2_rn(ul[2], make_float2(lb.x, lb.y), acc0);
-        acc1 = __ffma2_rn(uh2[2], make_float2(hb.x, hb.y), acc1);
-        acc0 = __ffma2_rn(ul[3], make_float2(lb.z, lb.w), acc0);
-        acc1 = __ffma2_rn(uh2[3], make_float2(hb.z, hb.w), acc1);
-        const float2 acc = __fadd2_rn(acc0, acc1);
+        float2 acc = __fmul2_rn(ulo[0], make_float2(la.x, la.y));  // one chain: fewer live registers
+        acc = __ffma2_rn(uhi[0], make_float2(ha.x, ha.y), acc);
+        acc = __ffma2_rn(ulo[1], make_float2(la.z, la.w), acc);
+        acc = __ffma2_rn(uhi[1], make_float2(ha.z, ha.w), acc);
+        acc = __ffma2_rn(ulo[2], make_float2(lb.x, lb.y), acc);
+        acc = __ffma2_rn(uhi[2], make_float2(hb.x, hb.y), acc);
+        acc = __ffma2_rn(ulo[3], make_float2(lb.z, lb.w), acc);
+        acc = __ffma2_rn(uhi[3], make_float2(hb.z, hb.w), acc);
         part[j] = acc.x + acc.y;
-        if (j < 7) rotate8(ul, uh2, cth, sth, nsth);  // next token: one position later
+        if (j < 7) rotate8(ulo, uhi, cth, sth);  // next token: one position later
       }
       transpose_reduce8(part, s, gmask);
       const float p = online_weights(A, part[0] * scale_log2, gmask);

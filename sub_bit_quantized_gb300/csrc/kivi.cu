@@ -17,7 +17,10 @@
 // folds its per-channel scale into the query once; values accumulate
 // sum_j p_j s_jg code_j,ch and subtract sum_j p_j s_jg z_jg per channel group at the end.
 // Under GQA one block serves up to four query heads of a KV head: the codes are read from
-// HBM and unpacked once for all of them.
+// HBM and unpacked once for all of them. With one query head per block the value codes feed
+// the mixed-precision FMA directly (fp16 operands, fp32 sums) with the token weight p_j s_jg
+// rounded to fp16 once (relative error 2^-12 per token, in the code and zero-point terms
+// alike).
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
 #include "../../include/kvq.h"
@@ -380,6 +383,29 @@ __device__ __forceinline__ float2 code_pair(uint32_t ml, uint32_t mh, int j) {
   const float2 f = make_float2(__uint_as_float(ml & m), __uint_as_float(mh & m));
   return __fadd2_rn(f, make_float2(-8388608.f, -8388608.f));
 }
+// One query head per block (no grouped heads): the value codes go straight into the
+// mixed-precision FMA (fp16 operands, fp32 sums), one FMA per code and no conversion. A masked
+// code word is read as two fp16 bit patterns; an integer pattern n below 2^11 is exactly the
+// fp16 n * 2^-24 (subnormal below 2^10, the first binade above), so code c at bit position k
+// of a half reads as c * 2^(k - 24). Codes j < kSplit of each half are masked in place; the
+// rest come from the word shifted right by b * kSplit. Accumulator pair (2j, 2j + 1) therefore
+// holds 2^(b jj - 24) * sum(w c) with jj = j or j - kSplit (value_scale_exp gives b jj - 24),
+// w being the token's weight p * s_v rounded to fp16 once.
+template <int BITS>
+struct HalfCodes {
+  static constexpr int kSplit = (BITS == 2) ? 5 : 2;  // codes per half below bit 11
+  static __device__ __forceinline__ int value_scale_exp(int j) { return BITS * (j < kSplit ? j : j - kSplit) - 24; }
+};
+// a0 += lo16(m) * wh, a1 += hi16(m) * wh, lo16 / hi16 and wh (low 16 bits) as fp16
+__device__ __forceinline__ void fma_f16x2(float& a0, float& a1, uint32_t m, uint32_t wh) {
+  asm("{\n\t.reg .b16 l, h, p;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.u16.u32 p, %3;\n\t"
+      "fma.rn.f32.f16 %0, l, p, %0;\n\t"
+      "fma.rn.f32.f16 %1, h, p, %1;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(m), "r"(wh));
+}
 template <bool B>
 struct BoolTag {
   static constexpr bool value = B;
@@ -502,7 +528,8 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
         const int e0 = j, e1 = L::kPV + j, i = w * L::kCPWv + 2 * j;
         const float v0 = h2f((e0 & 1) ? (hv[e0 >> 1] >> 16) : (hv[e0 >> 1] & 0xFFFFu));
         const float v1 = h2f((e1 & 1) ? (hv[e1 >> 1] >> 16) : (hv[e1 >> 1] & 0xFFFFu));
-        const float sj = pow2_pos(VB * j);
+        // the scale of accumulator pair j: 2^(b j) for grouped heads, 2^(b jj - 24) for one head
+        const float sj = (RH == 1) ? pow2_pos(HalfCodes<VB>::value_scale_exp(j)) : pow2_pos(VB * j);
 #pragma unroll
         for (int r = 0; r < RH; ++r) {
           o[r][i] = fmaf(p[r] * sj, v0, o[r][i]);
@@ -638,25 +665,44 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
               load_words<L::kLW>(stage + L::kCVc + tv * L::kVRow + 4 * w0, wv);
               const float sv = h2f(*reinterpret_cast<const uint16_t*>(stage + L::kCVs + (tv * 4 + gv) * 2));
               const float zv = h2f(*reinterpret_cast<const uint16_t*>(stage + L::kCVz + (tv * 4 + gv) * 2));
-              float2 w2[RH];
+              if constexpr (RH == 1) {
+                // the zero-point term takes the same fp16-rounded weight as the codes
+                const __half wgt = __float2half_rn(p[0] * sv);
+                oz[0] = fmaf(__half2float(wgt), zv, oz[0]);
+                const uint32_t wh = __half_as_ushort(wgt);
+                constexpr int kSp = HalfCodes<VB>::kSplit;
 #pragma unroll
-              for (int r = 0; r < RH; ++r) {
-                const float wgt = p[r] * sv;
-                oz[r] = fmaf(wgt, zv, oz[r]);
-                w2[r] = make_float2(wgt, wgt);
-              }
+                for (int w = 0; w < L::kLW; ++w) {
+                  const uint32_t hi_codes = wv[w] >> (VB * kSp);
 #pragma unroll
-              for (int w = 0; w < L::kLW; ++w) {
-                const uint32_t ml = magic_lo(wv[w]), mh = magic_hi(wv[w]);
+                  for (int j = 0; j < L::kPV; ++j) {  // (channel j, channel kPV + j) of the word
+                    const int jj = (j < kSp) ? j : j - kSp;
+                    const uint32_t m = ((j < kSp) ? wv[w] : hi_codes) & ((((1u << VB) - 1u) << (VB * jj)) * 0x10001u);
+                    const int i = w * L::kCPWv + 2 * j;
+                    fma_f16x2(o[0][i], o[0][i + 1], m, wh);
+                  }
+                }
+              } else {
+                float2 w2[RH];
 #pragma unroll
-                for (int j = 0; j < L::kPV; ++j) {  // (channel j, channel kPV + j) of the word, x 2^(b j)
-                  const float2 cp = code_pair<VB>(ml, mh, j);
-                  const int i = w * L::kCPWv + 2 * j;
+                for (int r = 0; r < RH; ++r) {
+                  const float wgt = p[r] * sv;
+                  oz[r] = fmaf(wgt, zv, oz[r]);
+                  w2[r] = make_float2(wgt, wgt);
+                }
 #pragma unroll
-                  for (int r = 0; r < RH; ++r) {
-                    const float2 acc = __ffma2_rn(w2[r], cp, make_float2(o[r][i], o[r][i + 1]));
-                    o[r][i] = acc.x;
-                    o[r][i + 1] = acc.y;
+                for (int w = 0; w < L::kLW; ++w) {
+                  const uint32_t ml = magic_lo(wv[w]), mh = magic_hi(wv[w]);
+#pragma unroll
+                  for (int j = 0; j < L::kPV; ++j) {  // (channel j, channel kPV + j) of the word, x 2^(b j)
+                    const float2 cp = code_pair<VB>(ml, mh, j);
+                    const int i = w * L::kCPWv + 2 * j;
+#pragma unroll
+                    for (int r = 0; r < RH; ++r) {
+                      const float2 acc = __ffma2_rn(w2[r], cp, make_float2(o[r][i], o[r][i + 1]));
+                      o[r][i] = acc.x;
+                      o[r][i + 1] = acc.y;
+                    }
                   }
                 }
               }
@@ -761,8 +807,9 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
           float* dst = ored + (warp * RH + r) * kD + (lane * L::kLW + w) * L::kCPWv;
 #pragma unroll
           for (int j = 0; j < L::kPV; ++j) {
-            dst[j] = o[r][w * L::kCPWv + 2 * j] * pow2_neg(VB * j) - oz[r];
-            dst[L::kPV + j] = o[r][w * L::kCPWv + 2 * j + 1] * pow2_neg(VB * j) - oz[r];
+            const float sc = (RH == 1) ? pow2_pos(-HalfCodes<VB>::value_scale_exp(j)) : pow2_neg(VB * j);
+            dst[j] = o[r][w * L::kCPWv + 2 * j] * sc - oz[r];
+            dst[L::kPV + j] = o[r][w * L::kCPWv + 2 * j + 1] * sc - oz[r];
           }
         }
       }

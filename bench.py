@@ -351,12 +351,12 @@ def kivi_wl_bytes(wl):
 PROFILED_TRAFFIC = {
     "loopvq_b64_6k:vq_pages_kernel+vq_window_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_attn.cu",
-        "f36914c7e7d958aded7ab901557ca6802d3c27788dfe045653a4b549596a9621",
-        204120320 + 5800192 + 43537408 + 2560),
+        "26eb4365a9ad8b1833a87b6dceb2dae29737fcc360f7e98df8c7b6039542fbbd",
+        204137984 + 5525248 + 43538176 + 3072),
     "kivi_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "a11cf430e855f4e50ddc6957cd14a05f864bdd835c5be9db09fde2acfc0161bc",
-        228804096 + 3292416),
+        "f9a971efd8ea1d5d4c32f9fcda3c4b12e017e1e4b6780049d481c08c1c92b352",
+        228799232 + 3666176),
     "encode_32k:encode_tc_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_encode_tc.cu",
         "42e194feda74fa6a5e78177d6a39c04b4785de3db0db60096413109cc4b1cd1a",
@@ -364,12 +364,12 @@ PROFILED_TRAFFIC = {
     # both quantize kernels (keys per channel, values per token) of one step
     "kivi_quant_32k:kivi_quant_*_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "a11cf430e855f4e50ddc6957cd14a05f864bdd835c5be9db09fde2acfc0161bc",
-        135021568 + 14449920 + 134288640 + 12688384),
+        "f9a971efd8ea1d5d4c32f9fcda3c4b12e017e1e4b6780049d481c08c1c92b352",
+        135000064 + 14761728 + 134275328 + 12550912),
     "kivi4_gqa_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "a11cf430e855f4e50ddc6957cd14a05f864bdd835c5be9db09fde2acfc0161bc",
-        89877248 + 2775040),
+        "f9a971efd8ea1d5d4c32f9fcda3c4b12e017e1e4b6780049d481c08c1c92b352",
+        89879040 + 2842624),
 }
 
 

@@ -351,8 +351,8 @@ def kivi_wl_bytes(wl):
 PROFILED_TRAFFIC = {
     "loopvq_b64_6k:vq_pages_kernel+vq_window_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_attn.cu",
-        "26eb4365a9ad8b1833a87b6dceb2dae29737fcc360f7e98df8c7b6039542fbbd",
-        204137984 + 5525248 + 43538176 + 3072),
+        "9dd7204b769f22979bfb5ec26a759d5e48fb4dc48537f979e0fe357e7f10bb1c",
+        203993344 + 5491200 + 43538688 + 0),
     "kivi_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
         "f9a971efd8ea1d5d4c32f9fcda3c4b12e017e1e4b6780049d481c08c1c92b352",

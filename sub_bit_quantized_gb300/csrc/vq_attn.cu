@@ -321,7 +321,10 @@ struct ProdState {
   Walker cur;   // next unit to issue
   int issued;   // units issued by this block
   int k_loads;  // key-slice copies issued
+  long long lo, hi;  // the block's share: read here by the refilling warp, so the consumers
+                     // keep no registers for it
 };
+static_assert(sizeof(ProdState) <= 64, "producer state fits its shared-memory slot");
 
 __device__ __forceinline__ void walker_load_pair(const VqAttnArgs& a, Walker& P) {
   req_len(a, 2 * P.pair, P.L0, P.NP0);
@@ -469,6 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
     Walker& P = ps->cur;
     ps->issued = 0;
     ps->k_loads = 0;
+    ps->lo = lo;
+    ps->hi = hi;
     P.i = lo;
     P.h = (int)(lo / Up);
     const int rem = (int)(lo - (long long)P.h * Up);
@@ -587,9 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
       // waits to produce, and the copy starts as soon as the stage is free
       if (atom_add_acq_rel_shared(&released[st], 1) == kWarps - 1) {
         released[st] = 0;
-        if (!*failed && ps->cur.i < hi) {
+        if (!*failed && ps->cur.i < ps->hi) {
           fence_proxy_async_smem();
-          prod_next<NG>(a, *ps, ring, full, lo, hi, n_pairs);
+          prod_next<NG>(a, *ps, ring, full, ps->lo, ps->hi, n_pairs);
         }
       }
     }

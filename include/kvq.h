@@ -309,8 +309,9 @@ kvq_status kvq_kivi_append(const kvq_kivi_cfg* cfg, const kvq_kivi_cache* cache,
  * Flash-Decoding background and method step 5; KIVI page: eq. (3), one softmax over the
  * quantized and residual segments). Scale 1/sqrt(D).
  * Arithmetic: scores, softmax and sums in fp32; in the value sums a token's weight enters an
- * fp16 x fp16 + fp32 FMA rounded to fp16 once (LoopVQ always; KIVI when no query heads share
- * a KV head), a relative error of 2^-12 per token, far inside the output tolerance.
+ * fp16 x fp16 + fp32 FMA rounded to fp16 once (LoopVQ always; KIVI when a block serves one
+ * query head, i.e. n_q_heads / n_heads odd), a relative error of 2^-12 per token, far inside
+ * the output tolerance.
  *
  * format KVQ_FMT_LOOPVQ: cfg is kvq_vq_cfg*, cache kvq_vq_cache*; layer and loop_step
  *   select the cache slice. The query sits at position seq_len[b] - 1; every key and the

@@ -243,16 +243,16 @@ def vq_call_bytes(B, H, n_pages, n_win, NG=16):
     return idx + win + bt + rope + qo
 
 
-# Shared-memory bytes the page kernel must read per quantized token and head: every index
-# selects one codeword row per channel group, fp32 keys (4 B per channel) and fp16 values (2 B
-# per channel), plus the token's key and value index bytes from the ring. On this GPU that
-# on-chip traffic, not HBM, is the binding resource of the LoopVQ decode (121 B per SM cycle
-# measured for conflict-free 128-bit shared loads; 128 nominal).
+# Shared-memory bytes the decode kernel must move per quantized token and head: every key index
+# selects one fp32 codeword row of its channel group (4 B per channel), every value index adds
+# the token's 4-byte integer weight into its (group, codeword) bin, and both index bytes are read
+# from the ring. On this GPU that on-chip traffic, not HBM, is the binding resource of the
+# LoopVQ decode (121 B per SM cycle measured for conflict-free 128-bit shared loads; 128 nominal).
 SMEM_BYTES_PER_CLK_SM = 121.0
 
 
 def vq_smem_bytes(B, H, n_pages, NG=16):
-    return B * H * n_pages * 8 * (D * 4 + D * 2 + 2 * NG)
+    return B * H * n_pages * 8 * (D * 4 + NG * 4 + 2 * NG)
 
 
 def setup_loopvq(wl, dev, seed, extra_tokens=0):
@@ -346,13 +346,23 @@ def kivi_wl_bytes(wl):
                            wl.get("v_bits", 2))
 
 
+# arithmetic of each path (the JSON line's dtype)
+DTYPE_LABEL = {
+    "loopvq": "f32 (fp32 key codebook; values: fp16 codebook, weights in 2^-20 fixed point)",
+    "stream": "f32 (fp32 key codebook; values: fp16 codebook, weights in 2^-20 fixed point)",
+    "kivi": "f32 (2/4-bit codes, fp16 scales; fp16-rounded weights when one query head per block)",
+    "kivi_stream": "f32 (2-bit codes, fp16 scales; fp16-rounded weights when one query head per block)",
+    "encode": "bf16 x 3-part bf16 codebook -> f32 (compensated f32 near-tie decisions)",
+    "kivi_quant": "f32->u8",
+}
+
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch from an ncu capture,
 # valid only for the kernel source it was taken on (profiles/ holds the capture summary)
 PROFILED_TRAFFIC = {
-    "loopvq_b64_6k:vq_pages_kernel+vq_window_kernel": (
+    "loopvq_b64_6k:vq_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_attn.cu",
-        "9dd7204b769f22979bfb5ec26a759d5e48fb4dc48537f979e0fe357e7f10bb1c",
-        203993344 + 5491200 + 43538688 + 0),
+        "52d88be2aa96800b115504f8559cdc96f2322d2daa509bad5ac2f78499fc650d",
+        241494272 + 3686144),
     "kivi_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
         "f9a971efd8ea1d5d4c32f9fcda3c4b12e017e1e4b6780049d481c08c1c92b352",
@@ -450,10 +460,9 @@ def run_ours(args, wl, rank, world, dist, pool):
             calls = [(l, 1) for l in range(NL)]
             call_bytes = kivi_wl_bytes(wl)
         n_calls = len(calls)
-        # a LoopVQ call is two launches (page kernel, then window + merge kernel); the roofline
-        # covers both, timed together per call
-        launches_per_call = 2 if wl["kind"] == "loopvq" else 1
-        kernel_name = "vq_pages_kernel+vq_window_kernel" if wl["kind"] == "loopvq" else "kivi_attn_kernel"
+        # one launch per call for either format: the roofline is that kernel's
+        launches_per_call = 1
+        kernel_name = "vq_attn_kernel" if wl["kind"] == "loopvq" else "kivi_attn_kernel"
         gen = torch.Generator(device=dev).manual_seed(99 + rank)
         q = torch.randn((n_calls, B, H, D), generator=gen, device=dev).to(torch.bfloat16)
         out = torch.empty((n_calls, B, H, D), dtype=torch.bfloat16, device=dev)
@@ -578,8 +587,8 @@ def run_ours(args, wl, rank, world, dist, pool):
                            roll_ms_per_roll=round(roll_extra, 4),
                            roll_fraction_amortized=round(roll_extra / 8 / ms, 5),
                            # per token: NL*T appends, the roll's 2 launches (at the first append;
-                           # they leave at once unless a page is due), 2 launches per attention call
-                           higher_is_better=True, gpu_launches=args.steps * (NL * T * 3 + 2),
+                           # they leave at once unless a page is due), 1 launch per attention call
+                           higher_is_better=True, gpu_launches=args.steps * (NL * T * 2 + 2),
                            context_end=L_end, clocks=cs.summary(),
                            roofline={"bound": "hbm", "achieved": None, "peak": hbm_peak, "unit": "GB/s",
                                      "frac": None, "traffic": None,
@@ -786,7 +795,7 @@ def main():
                 cfgd[k] = wl[k]
         if "n_splits" in res:
             cfgd["n_splits"] = res.pop("n_splits")
-        line = dict(base, dtype="f32" if wl["kind"] != "kivi_quant" else "f32->u8", config=cfgd, **res)
+        line = dict(base, dtype=DTYPE_LABEL.get(wl["kind"], "f32"), config=cfgd, **res)
         print(json.dumps(line))
     if pool is not None:
         pool.close()

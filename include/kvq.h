@@ -308,10 +308,13 @@ kvq_status kvq_kivi_append(const kvq_kivi_cfg* cfg, const kvq_kivi_cache* cache,
  * pages with partial softmax per split and an exact logsumexp merge (LoopVQ page:
  * Flash-Decoding background and method step 5; KIVI page: eq. (3), one softmax over the
  * quantized and residual segments). Scale 1/sqrt(D).
- * Arithmetic: scores, softmax and sums in fp32; in the value sums a token's weight enters an
- * fp16 x fp16 + fp32 FMA rounded to fp16 once (LoopVQ always; KIVI when a block serves one
- * query head, i.e. n_q_heads / n_heads odd), a relative error of 2^-12 per token, far inside
- * the output tolerance.
+ * Arithmetic: scores and softmax in fp32. LoopVQ sums the values by codeword: per
+ * (group, codeword) the weights p = exp2(s - M) <= 1 of the tokens using it (M the maximum
+ * over a sub-piece of at most 3584 tokens) are added as integers in units of 2^-20 (each
+ * weight rounded to the nearest unit once, an absolute error of at most 2^-21), then
+ * multiplied by the fp16 value codebook in fp32. KIVI, when a block serves one query head
+ * (n_q_heads / n_heads odd), rounds each token's weight to fp16 once in an fp16 x fp16 + fp32
+ * FMA (relative error 2^-12); otherwise fp32 throughout.
  *
  * format KVQ_FMT_LOOPVQ: cfg is kvq_vq_cfg*, cache kvq_vq_cache*; layer and loop_step
  *   select the cache slice. The query sits at position seq_len[b] - 1; every key and the
@@ -322,19 +325,22 @@ kvq_status kvq_kivi_append(const kvq_kivi_cfg* cfg, const kvq_kivi_cache* cache,
  *   t < n_quant_v[b] (else v_resid), for t < n_tok[b].
  * out: [B][Hq][D], bf16 (KVQ_OUT_BF16) or fp32 (KVQ_OUT_FP32).
  * n_splits: how the quantized pages are split, 0 picks for the GPU.
- *   LoopVQ: thread blocks of the page kernel. The units (head, request pair, 32 index
- *   pages), head-major, are cut into n_splits equal contiguous shares, one per block; each
- *   block writes a partial softmax for every piece of a (request, head) it covers and a
- *   second kernel merges them with the bf16 window tokens. 0 = one block per SM.
+ *   LoopVQ: thread blocks of the one persistent kernel. All index pages, in (head, request)
+ *   segments, head-major, are cut into n_splits equal contiguous shares, one per block; the
+ *   block holding a segment's first page also attends its bf16 window tokens (a block takes
+ *   the windows of requests without index pages in turn). A segment split between blocks is
+ *   merged exactly by the last of them to finish. 0 = one block per SM.
  *   KIVI: token splits per (request, KV head): split k takes an equal range of the
  *   quantized keys and the last split also the fp16 residual (its bytes counted in the
  *   ranges), merged by the last block of each (request, KV head) to finish; a block serves
  *   up to 4 query heads of its KV head, so their codes are read once.
  * ws: device workspace of at least kvq_decode_workspace_size() bytes (may be NULL when
- *   that size is 0; LoopVQ always needs one). A KIVI workspace must be zero-filled before
- *   its first use; every call leaves it reusable. Two calls that run at the same time need
- *   two workspaces.
- * Errors: KVQ_ERR_WORKSPACE, KVQ_ERR_CAPACITY (B > max_batch). */
+ *   that size is 0; LoopVQ always needs one): merge counters (zero between calls) and
+ *   partial softmaxes. A workspace must be zero-filled before its first use; every call
+ *   that completes leaves it reusable (its counters back at zero). Two calls that run at the
+ *   same time need two workspaces.
+ * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_WORKSPACE, KVQ_ERR_CAPACITY (B > max_batch),
+ *   KVQ_ERR_UNSUPPORTED (LoopVQ: B > 8191). */
 kvq_status kvq_decode_attn(int format, const void* cfg, const void* cache, int layer,
                            int loop_step, const uint16_t* q, int B, void* out, int out_dtype,
                            int n_splits, void* ws, size_t ws_bytes, kvq_stream stream);
@@ -343,11 +349,16 @@ kvq_status kvq_decode_attn(int format, const void* cfg, const void* cache, int l
  * gives all device memory to its own pool at start-up and forbids later allocations, or code
  * running inside another framework's callback that only sees the tensors it is handed.
  * The pages have no counterpart of this call; it is kvq_decode_attn with the workspace taken
- * from an array the library reserves on every device it is loaded on
- * (KVQ_NOALLOC_SCRATCH_BYTES, held until the process exits) instead of from the caller.
- * - Arguments and results are those of kvq_decode_attn without ws / ws_bytes.
- * - The first call on a device looks the array's device address up (cudaGetSymbolAddress);
- *   make that first call before any stream capture on that device.
+ * from a fixed array inside the library (KVQ_NOALLOC_SCRATCH_BYTES per device) instead of
+ * from the caller.
+ * - Arguments and results are those of kvq_decode_attn without ws / ws_bytes; a call that
+ *   kvq_decode_attn would refuse is refused with the same status before anything runs.
+ * - CUDA loads the library's device code on a device lazily (first launch or symbol lookup
+ *   there) and sets the array aside at that moment; it is then held until the process exits.
+ *   The first call on a device looks the array's address up (cudaGetSymbolAddress), so make
+ *   that first call before a memory pool takes the device's memory, and before any stream
+ *   capture on that device.
+ * - The address is kept per device: do not use the library across a cudaDeviceReset.
  * - Each call clears the part of the array it uses (cudaMemsetAsync on `stream`) and then
  *   launches; it never calls cudaMalloc or cudaFree.
  * - All calls on a device share the one array: calls that can run at the same time on the
@@ -373,7 +384,8 @@ const char* kvq_status_string(kvq_status s);
 /* Detail of the last error on the calling host thread ("" if none). */
 const char* kvq_last_error(void);
 /* Reads and clears the device error word of the current device (synchronizes the device).
- * 0 = no device-side error; otherwise a KVQ_ERR_* code. */
+ * 0 = no device-side error; otherwise a KVQ_ERR_* code. The word's device address is looked
+ * up once per device and kept, so the library must not be used across a cudaDeviceReset. */
 int kvq_device_error(void);
 /* Library version, major*10000 + minor*100 + patch. */
 int kvq_version(void);

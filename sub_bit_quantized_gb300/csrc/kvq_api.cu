@@ -495,28 +495,53 @@ KVQ_API int kvq_decode_auto_splits(int format, const void* cfg, int B) {
   return 0;
 }
 
+namespace kvq {
+// Every host-side check of kvq_decode_attn except the workspace (shared with the no-allocation
+// entry point, so that both refuse the same calls with the same status before touching memory).
+kvq_status check_decode_args(int format, const void* cfg, const void* cache, int layer, int loop_step,
+                             const uint16_t* q, int B, const void* out, int out_dtype, int n_splits, const char* fn) {
+  if (out_dtype != KVQ_OUT_BF16 && out_dtype != KVQ_OUT_FP32)
+    return fail(KVQ_ERR_INVALID_ARG, "%s: out_dtype must be KVQ_OUT_BF16 or KVQ_OUT_FP32", fn);
+  if (n_splits < 0 || n_splits > 4096) return fail(KVQ_ERR_INVALID_ARG, "%s: n_splits out of range", fn);
+  if (!aligned16(q) || !aligned16(out))
+    return fail(KVQ_ERR_INVALID_ARG, "%s: q or out is null or not 16-byte aligned", fn);
+  if (format == KVQ_FMT_LOOPVQ) {
+    const kvq_vq_cfg* c = static_cast<const kvq_vq_cfg*>(cfg);
+    kvq_status st = check_vq_cfg(c, fn);
+    if (st != KVQ_OK) return st;
+    if ((st = check_vq_cache(static_cast<const kvq_vq_cache*>(cache), fn)) != KVQ_OK) return st;
+    if (layer < 0 || layer >= c->n_layers || loop_step < 1 || loop_step > c->T || B < 1)
+      return fail(KVQ_ERR_INVALID_ARG, "%s: layer/loop_step/B out of range", fn);
+    if (B > c->max_batch) return fail(KVQ_ERR_CAPACITY, "%s: B=%d > max_batch=%d", fn, B, c->max_batch);
+    if (B > kvq::kVqMaxBatch)
+      return fail(KVQ_ERR_UNSUPPORTED, "%s: B=%d exceeds %d requests", fn, B, kvq::kVqMaxBatch);
+    if ((long long)B * c->max_pages >= (1ll << 31))
+      return fail(KVQ_ERR_UNSUPPORTED, "%s: too many index pages for one call", fn);
+    return KVQ_OK;
+  }
+  if (format == KVQ_FMT_KIVI) {
+    const kvq_kivi_cfg* c = static_cast<const kvq_kivi_cfg*>(cfg);
+    kvq_status st = check_kivi_cfg(c, fn);
+    if (st != KVQ_OK) return st;
+    if ((st = check_kivi_cache(static_cast<const kvq_kivi_cache*>(cache), fn)) != KVQ_OK) return st;
+    if (B < 1) return fail(KVQ_ERR_INVALID_ARG, "%s: B < 1", fn);
+    if (B > c->max_batch) return fail(KVQ_ERR_CAPACITY, "%s: B > max_batch", fn);
+    return KVQ_OK;
+  }
+  return fail(KVQ_ERR_INVALID_ARG, "%s: unknown format %d", fn, format);
+}
+}  // namespace kvq
+
 KVQ_API kvq_status kvq_decode_attn(int format, const void* cfg, const void* cache, int layer, int loop_step,
                                    const uint16_t* q, int B, void* out, int out_dtype, int n_splits, void* ws,
                                    size_t ws_bytes, kvq_stream stream) {
-  if (out_dtype != KVQ_OUT_BF16 && out_dtype != KVQ_OUT_FP32)
-    return fail(KVQ_ERR_INVALID_ARG, "%s: out_dtype must be KVQ_OUT_BF16 or KVQ_OUT_FP32", __func__);
-  if (n_splits < 0 || n_splits > 4096) return fail(KVQ_ERR_INVALID_ARG, "%s: n_splits out of range", __func__);
-  CHECK_PTR(q);
-  CHECK_PTR(out);
+  kvq_status st0 = kvq::check_decode_args(format, cfg, cache, layer, loop_step, q, B, out, out_dtype, n_splits,
+                                          __func__);
+  if (st0 != KVQ_OK) return st0;
   cudaStream_t s = (cudaStream_t)stream;
   if (format == KVQ_FMT_LOOPVQ) {
     const kvq_vq_cfg* c = static_cast<const kvq_vq_cfg*>(cfg);
-    kvq_status st = check_vq_cfg(c, __func__);
-    if (st != KVQ_OK) return st;
     const kvq_vq_cache* k = static_cast<const kvq_vq_cache*>(cache);
-    if ((st = check_vq_cache(k, __func__)) != KVQ_OK) return st;
-    if (layer < 0 || layer >= c->n_layers || loop_step < 1 || loop_step > c->T || B < 1)
-      return fail(KVQ_ERR_INVALID_ARG, "%s: layer/loop_step/B out of range", __func__);
-    if (B > c->max_batch) return fail(KVQ_ERR_CAPACITY, "%s: B=%d > max_batch=%d", __func__, B, c->max_batch);
-    if ((B + 1) / 2 > kvq::vq_attn_max_pairs())
-      return fail(KVQ_ERR_UNSUPPORTED, "%s: B=%d exceeds %d requests", __func__, B, 2 * kvq::vq_attn_max_pairs());
-    const long long units = (long long)c->n_heads * ((B + 1) / 2) * ((c->max_pages + kvq::kVqChunk - 1) / kvq::kVqChunk);
-    if (units >= (1ll << 31)) return fail(KVQ_ERR_UNSUPPORTED, "%s: too many page units for one call", __func__);
     const int blocks = plan_vq_blocks(n_splits);
     const size_t need = vq_ws_bytes(c, B, blocks);
     if (!ws || ws_bytes < need || !aligned16(ws))
@@ -544,12 +569,7 @@ KVQ_API kvq_status kvq_decode_attn(int format, const void* cfg, const void* cach
   }
   if (format == KVQ_FMT_KIVI) {
     const kvq_kivi_cfg* c = static_cast<const kvq_kivi_cfg*>(cfg);
-    kvq_status st = check_kivi_cfg(c, __func__);
-    if (st != KVQ_OK) return st;
     const kvq_kivi_cache* k = static_cast<const kvq_kivi_cache*>(cache);
-    if ((st = check_kivi_cache(k, __func__)) != KVQ_OK) return st;
-    if (B < 1) return fail(KVQ_ERR_INVALID_ARG, "%s: B < 1", __func__);
-    if (B > c->max_batch) return fail(KVQ_ERR_CAPACITY, "%s: B > max_batch", __func__);
     const int rh = kvq::kivi_heads_per_block(c->n_q_heads / c->n_heads);
     if (kvq::kivi_attn_smem_bytes(c->k_bits, c->v_bits, rh, c->residual) > 232448)
       return fail(KVQ_ERR_UNSUPPORTED, "%s: residual=%d needs more shared memory than a block has", __func__,

@@ -5,10 +5,17 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/kvq.h"
+
 namespace kvq {
 
 // stores the detail message kvq_last_error() returns on this host thread
 void set_last_error(const char* msg);
+
+// every host-side check of kvq_decode_attn except the workspace (fn names the caller in the
+// message kvq_last_error() returns)
+kvq_status check_decode_args(int format, const void* cfg, const void* cache, int layer, int loop_step,
+                             const uint16_t* q, int B, const void* out, int out_dtype, int n_splits, const char* fn);
 
 constexpr int kD = 128;        // head dimension
 constexpr int kPage = 8;       // tokens per index page
@@ -24,18 +31,19 @@ __host__ __device__ inline size_t page_byte(int g, int j, int NG) {
 }
 
 // ---------------------------------------------------------------- LoopVQ decode attention
-// Two launches per call. The page kernel runs G persistent blocks over the work units
-// (head, request pair, chunk of 32 index pages), head-major; block k takes the contiguous
-// units [k U / G, (k + 1) U / G). For every piece of a (pair, head) segment it covers, each
-// of its warps writes one partial softmax (M, l, o[128]) of its request: to part_whole[seg]
-// when the whole segment lies in the block's share, else to part_slot[k][0] (the piece
-// holding the block's first unit) or part_slot[k][1] (the piece holding its last). The
-// window kernel attends the bf16 sink/recent tokens of every (request, head) and merges
-// them with the pieces.
-constexpr int kVqThreads = 512;                 // page-kernel block: 8 lanes per index page
-constexpr int kVqChunk = kVqThreads / 16;       // index pages of each request per work unit
-constexpr int kVqWarpsPerReq = kVqThreads / 64; // page-kernel warps per request
-constexpr int kVqPartFloats = 2 * kVqWarpsPerReq * (kD + 2);  // one piece: [request][warp][M, l, o[128]]
+// One persistent launch per call. The quantized pages of every (head, request) segment,
+// head-major, form one list of page positions; block k of G takes positions
+// [k P / G, (k + 1) P / G). Inside a block, 16 compute warps score the keys of up to
+// kVqSubPages pages (pass 1), then add the fixed-point softmax weights of the same pages into
+// a per-(group, codeword) histogram (pass 2); aux warps turn each histogram into value sums,
+// attend the bf16 window of every segment whose first page the block holds, and merge. A
+// segment split over several blocks is merged by the last block to finish its part: each
+// writes a partial (M, l, o[128]) to a per-block slot and counts itself in cnt[segment]; the
+// last one merges the slots, writes the output and resets the counter to 0.
+constexpr int kVqComputeWarps = 16;              // compute warps per block
+constexpr int kVqSubPages = 384;                 // index pages per sub-piece (fixed-point capacity)
+constexpr int kVqSlotFloats = 132;               // one partial: M, l, 2 pad, o[128]
+constexpr int kVqMaxBatch = 8191;                // requests per call (prefix scan in shared memory)
 
 struct VqAttnArgs {
   const uint8_t* idx_k;      // [max_batch][H][max_pages][8 NG] of (layer, block)
@@ -51,16 +59,14 @@ struct VqAttnArgs {
   const uint16_t* q;         // [B][H][D] bf16
   void* out;                 // [B][H][D]
   int out_fp32;
-  int32_t* pref;             // [n_pairs + 1] unit prefix over pairs (written by page block 0)
-  float* part_whole;         // [H * n_pairs][kVqPartFloats]
-  float* part_slot;          // [G][2][kVqPartFloats]
+  int32_t* cnt;              // [B * H] merge counters (zero between calls)
+  float* slots;              // [G][2][kVqSlotFloats] partials of segments shared between blocks
   int* err;
   int B, H, max_pages, max_ctx, sink, recent, win_slots;
-  int G;                     // page-kernel blocks
+  int G;                     // blocks
   int NG;                    // index groups per token (8, 16 or 32): pages of 8 NG bytes
 };
 size_t vq_attn_ws_bytes(int B, int H, int G);
-int vq_attn_max_pairs();
 cudaError_t launch_vq_attn(const VqAttnArgs& a, void* ws, cudaStream_t s);
 
 // ---------------------------------------------------------------- LoopVQ encode and friends

@@ -4,9 +4,15 @@
 // own pool at start-up and refuses any further cudaMalloc, or code running inside a host
 // framework's callback that is handed only the tensors it works on. They cannot provide the
 // split-K workspace that kvq_decode_attn asks for. This entry point keeps that workspace in
-// a fixed array inside the library instead (KVQ_NOALLOC_SCRATCH_BYTES per device, reserved
-// when the library is loaded and held until the process exits) and otherwise runs exactly
-// kvq_decode_attn.
+// a fixed array inside the library instead (KVQ_NOALLOC_SCRATCH_BYTES per device) and
+// otherwise runs exactly kvq_decode_attn.
+//
+// When the array takes device memory: CUDA loads the library's device code on a device
+// lazily, at the first kernel launch or symbol lookup there, and sets the array aside then;
+// from that point it is held until the process exits. A caller whose pool takes all device
+// memory must therefore make its first call on each device (which looks the address up)
+// before the pool is created. The address is looked up once per device and kept: after a
+// cudaDeviceReset the array may move, so the library must not be used across a reset.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -49,6 +55,11 @@ cudaError_t scratch_address(void** out) {
 KVQ_API kvq_status kvq_decode_attn_noalloc(int format, const void* cfg, const void* cache, int layer,
                                            int loop_step, const uint16_t* q, int B, void* out, int out_dtype,
                                            int n_splits, kvq_stream stream) {
+  // the same argument checks as kvq_decode_attn first, so a call it would refuse is refused
+  // here with the same status, before the scratch array is touched
+  const kvq_status st = kvq::check_decode_args(format, cfg, cache, layer, loop_step, q, B, out, out_dtype, n_splits,
+                                               __func__);
+  if (st != KVQ_OK) return st;
   const size_t need = kvq_decode_workspace_size(format, cfg, B, n_splits);
   if (need > KVQ_NOALLOC_SCRATCH_BYTES) {
     char msg[256];

@@ -1,49 +1,46 @@
-// LoopVQ decode attention over the bf16 window and the 8-token index pages of one
-// (layer, loop step), with an exact logsumexp merge of partial softmaxes.
+// LoopVQ decode attention over the index pages and the bf16 window of one (layer, loop step),
+// with an exact logsumexp merge of partial softmaxes.
 //
-// Follows "LoopVQ: Sub 1-bit KV Cache Quantization for Looped Transformers", method
-// step 5, Algorithm 1 and Figure 5: the step's codebook slice B_t is staged in shared
-// memory, keys and values are rebuilt from D/c indices per token, keys are rotated by
-// RoPE and dotted with the query, the bf16 sink/recent tokens are attended directly, and
-// the partial results are merged exactly (the Flash-Decoding merge the page builds on).
+// Follows "LoopVQ: Sub 1-bit KV Cache Quantization for Looped Transformers", method step 5,
+// Algorithm 1 and Figure 5: keys and values are rebuilt from D/c indices per token through the
+// step's codebook slice B_t, keys are rotated by RoPE and dotted with the query, the bf16
+// sink/recent tokens are attended directly, and the partial results are merged exactly (the
+// Flash-Decoding merge the page builds on).
 //
-// GB300 design (differs from the page's Triton kernel, which gives every (request, head,
-// split) its own program). On this GPU a codeword lookup costs shared-memory bandwidth and
-// every key 6 FMAs per channel pair, so the work is bound on chip, not by HBM. Two kernels:
+// GB300 design (the page's kernel gives every (request, head, split) its own program and
+// rebuilds value rows token by token). Here a codeword lookup costs shared-memory bandwidth
+// and every key 6 FMAs per channel pair, so the work is bound on chip, not by HBM. One
+// persistent launch, one block per SM; block k takes the k-th of G equal contiguous shares
+// of all index pages (head-major segments of (head, request)). Warp roles:
 //
-// vq_pages_kernel: persistent, one 512-thread block per SM. The work units (head, request
-// pair, chunk of kVqChunk = 32 index pages), head-major, are cut into G equal contiguous
-// shares, one per block, so every SM gets the same number of pages whatever the batch mix,
-// and a block restages the codebook slices only when its share crosses into the next head
-// (at most twice for the usual shapes).
-//  * Both slices stay resident, staged by TMA bulk copies: keys in fp32 (128 KB; channels
-//    0..63 and 64..127 as two [256][64] tables), values in fp16 as the cache stores them
-//    ([256][128]; value rounding error ~1e-4 of the output). A codeword's shared-memory address
-//    is one byte permute: (index << 8) | lane offset, and every lookup is a 128-bit load.
-//  * The units stream through a 2-stage ring with TMA bulk copies: 32 key and 32 value
-//    pages of each request, the two bf16 queries and a header naming the unit. A full
-//    mbarrier per stage; the last warp to finish with a stage (a shared-memory arrival
-//    counter) issues its refill. Every wait is bounded and reports a timeout through the
-//    device error word instead of hanging.
-//  * 8 lanes per page, lane s owns the RoPE partner groups s and s+8 (channels 8s..8s+7 and
-//    64+8s..64+8s+7). The rotated query u = R(p_q - p) q satisfies <R(p_q) q, R(p) k> =
-//    <u, k>, so keys are never rotated: u is built from the cos/sin table at a lane-group's
-//    first page of a piece, advanced one position per token by R(-theta) and, from the last
-//    token of a page to the first of the lane-group's next page (one unit, 256 positions,
-//    later), by R(-249 theta), so a lane keeps a single copy of u; it is re-read from the
-//    table every 64 units. Every score is one chain of packed FMAs. A transposing shuffle
-//    reduction leaves lane s with the score of token s.
-//  * One pass with an online softmax per lane-group; the 8 weights of a page are broadcast
-//    by shuffles (as fp16) and each lane accumulates its 16 value channels from the fp16
-//    table with the mixed-precision FMA (fp16 operands, fp32 sums: no conversions).
-//  * At the end of each piece of a (pair, head) segment the lane-groups of a warp merge by
-//    shuffles and every warp writes its partial (M, l, o) to the workspace (eight per
-//    request), with no block-wide barrier.
+//  * 16 compute warps, 16 lanes per index page (lane = RoPE slot s, channel quarter m:
+//    channels 8s+4m..8s+4m+3 and their partners 64+8s+4m..), PPL consecutive pages per
+//    16-lane group per work unit (4 with c = 8 or 16, 2 with c = 4). Pages are taken in
+//    sub-pieces of at most 384 pages of one segment, in two passes:
+//      pass 1 (keys): the key slice B_t stays resident in shared memory (fp32, two [256][64]
+//      tables for the two RoPE halves); each lookup is one 128-bit load at (index << 8) | lane
+//      offset. The rotated query u = R(p_q - p) q satisfies <R(p_q) q, R(p) k> = <u, k>, so
+//      keys are never rotated: u is built from the cos/sin table at a sub-piece's first page,
+//      advanced token by token with the three-term recurrence u' = 2 cos(theta) u - u_prev
+//      (one FMA per component) and moved between units by one exact rotation. Scores go to a
+//      shared buffer; the warps then agree on the sub-piece maximum M.
+//      pass 2 (values): the re-association o_g = sum_j p_j B_V[g][idx_jg] = sum_r w[g][r]
+//      B_V[g][r] with w[g][r] = sum of p_j over the tokens whose group-g index is r. Each
+//      weight p_j = exp2(s_j - M) <= 1 is added as a fixed-point integer (2^-20 units) into a
+//      per-(group, codeword) histogram with shared-memory integer atomics (native on this
+//      GPU; float atomics are not), laid out [256][32 columns] so that the 32 lanes of every
+//      atomic hit 32 different banks. No value row is read per token.
+//  * 4 aux warps: for each sub-piece, w . B_V (the fp16 value slice, read from L2) gives the
+//    sub-piece's partial (M, l, o); they attend the bf16 window of every segment whose first
+//    page this block holds (rotated query from the table, online softmax), merge, and write
+//    the output. A segment shared with other blocks is merged by the last block to finish
+//    its part (a per-segment counter in the workspace).
+//  * 1 producer warp (one lane): TMA bulk copies of each unit's index pages (and the query)
+//    into a ring of stages, and of the key slice whenever the share enters a new head.
 //
-// vq_window_kernel: one block (128 threads, or 512 for few long windows) per (request, head)
-// attends the bf16 sink and recent tokens (one token per lane-group step, online softmax) and
-// merges the result with the warp partials of every page piece of its segment, found from
-// the same share arithmetic.
+// Every wait is an mbarrier wait with a time limit (the waiting warp suspends between polls);
+// a timeout sets the device error word and a block-wide flag, after which every role leaves
+// its loop.
 #include <cuda_fp16.h>
 
 #include "kvq_common.cuh"
@@ -53,234 +50,113 @@
 namespace kvq {
 namespace {
 
-constexpr int kThreads = kVqThreads;
-constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = kVqChunk;                          // pages of each request per unit
-constexpr int kResync = 64;                               // units between cos/sin table reloads
-constexpr int kJump = kChunk * kPage;                     // positions between a lane-group's pages
-constexpr uint32_t kKSliceBytes = kCB * kD * 4;           // fp32 key codebook slice
-constexpr uint32_t kVSliceBytes = kCB * kD * 2;           // fp16 value codebook slice
-constexpr int kOffK = 0;                                  // shared-memory layout (bytes)
-constexpr int kOffV = kOffK + kKSliceBytes;
+constexpr int kCW = kVqComputeWarps;                 // compute warps
+constexpr int kAW = 4;                               // aux warps
+constexpr int kThreads = (kCW + kAW + 1) * 32;       // + one producer warp
+constexpr int kAuxT0 = kCW * 32;                     // first aux thread
+constexpr int kAuxN = kAW * 32;
+constexpr int kProdWarp = kCW + kAW;
+constexpr int kSubP = kVqSubPages;                   // pages per sub-piece
+constexpr int kFixBits = 20;                         // fixed-point weight resolution 2^-20
+// capacity: a bin sums at most kSubP * 8 weights of at most 2^20 each
+static_assert((long long)kSubP * kPage * (1ll << kFixBits) < (1ll << 32), "fixed-point histogram fits 32 bits");
+constexpr uint32_t kKSliceBytes = kCB * kD * 4;      // fp32 key slice (two [256][64] tables)
+constexpr int kBinCols = 32;                         // histogram columns: copies x groups
+constexpr int kBinBytes = kCB * kBinCols * 4;        // 32 KB
+constexpr int kSbufBytes = kSubP * kPage * 4;        // scores of one sub-piece
+static_assert(kVqMaxBatch + 1 <= kBinBytes / 4, "request prefix scan fits the histogram area");
 
-// Ring and shared-memory layout for NG index groups per token (c = 128 / NG channels per
-// codeword): a page is 8 NG bytes. NG = 32 (c = 4) keeps a single ring stage so that its
-// 256-byte pages fit beside the two codebook slices; its refill still overlaps the unit's work
-// because every thread copies what it needs from the stage to registers first.
+// unit header flags
+constexpr int kFV = 1;       // a value unit (pass 2), else a key unit (pass 1)
+constexpr int kFFirst = 2;   // first unit of its sub-piece (of its kind)
+constexpr int kFLast = 4;    // last unit of its sub-piece (of its kind)
+constexpr int kFHeadEnd = 8; // last key unit of its head in this block's share
+constexpr int kFPar = 16;    // sub-piece parity
+constexpr int kFEnd = 32;    // no more units
+
 template <int NG>
-struct PageLay {
+struct Lay {
   static constexpr int kPageB = kPage * NG;
-  static constexpr int kStg = (NG == 32) ? 1 : 2;
-  static constexpr uint32_t kPart = kChunk * kPageB;           // one request's pages of one kind
-  static constexpr uint32_t kOffHdr = 4 * kPart;               // unit header within a stage
-  static constexpr uint32_t kOffQs = kOffHdr + 64;             // bf16 queries [2][128] within a stage
-  static constexpr uint32_t kStageBytes = kOffQs + 2 * kD * 2 + 64;  // [K r0|K r1|V r0|V r1|hdr|q r0|q r1]
-  static constexpr int kOffRing = kOffV + kVSliceBytes;
-  static constexpr int kOffJ = kOffRing + kStg * kStageBytes;  // float4 [4][8 slots]: cos, sin(256 theta)
-  static constexpr int kOffProd = kOffJ + 8 * 16 * 4;          // producer state (thread 0)
-  static constexpr int kOffBar = kOffProd + 64;                // mbarriers + flags
-  static constexpr int kSmemBytes = kOffBar + 128;
+  static constexpr int kPPL = (NG == 32) ? 2 : 4;              // consecutive pages per 16-lane group per unit
+  static constexpr int kUP = 2 * kCW * kPPL;                   // pages per unit
+  static constexpr int kJump = (kUP - kPPL) * kPage;           // a group's last token + 1 -> its first of the next unit
+  static constexpr int kStg = (NG == 8) ? 4 : 2;
+  static_assert(kSubP % kUP == 0, "a sub-piece is a whole number of units");
+  static constexpr int kOffHdr = kUP * kPageB;                 // unit header within a stage
+  static constexpr int kOffQ = kOffHdr + 64;                   // bf16 query within a stage
+  static constexpr int kStageB = ((kOffQ + kD * 2) + 127) / 128 * 128;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffBins = kOffK + (int)kKSliceBytes;
+  static constexpr int kOffSbuf = kOffBins + kBinBytes;
+  static constexpr int kOffRing = kOffSbuf + kSbufBytes;
+  static constexpr int kOffJ = kOffRing + kStg * kStageB;       // cos, sin(kJump theta), cos, sin(theta) [4][64]
+  static constexpr int kOffWm = kOffJ + 4 * 64 * 4;            // sub-piece maxima [2 parities][kCW]
+  static constexpr int kOffWp = kOffWm + 2 * kCW * 4;          // aux window partials [kAW][132]
+  static constexpr int kOffRed = kOffWp + kAW * 132 * 4;       // aux reduction [4][128] + [4] + flag
+  static constexpr int kOffWalk = kOffRed + (4 * 128 + 8) * 4; // the share's first piece
+  static constexpr int kOffBar = kOffWalk + 64;
+  // full[kStg], empty[kStg], kbar, ktfree, maxbar, hfull, hfree, then flags
+  static constexpr int kSmemBytes = kOffBar + (2 * kStg + 5) * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory");
-  static_assert(kOffBar % 8 == 0 && kOffRing % 128 == 0 && kStageBytes % 128 == 0, "alignment");
+  static_assert(kOffRing % 128 == 0 && kStageB % 128 == 0 && kOffBar % 8 == 0 && kOffWalk % 16 == 0, "alignment");
 };
-constexpr int kMaxPairs = (int)(kVSliceBytes / 4) - 1;    // unit scan runs in the value-slice area
 
-__device__ __forceinline__ void ldg8_perm(const float* p, int o0, float (&v)[8]) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(p + o0));
-  const float4 b = __ldg(reinterpret_cast<const float4*>(p + (4 - o0)));
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+// ------------------------------------------------------------------ small helpers
+__device__ __forceinline__ void red_add_u32(uint32_t saddr, uint32_t v) {
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
 }
-__device__ __forceinline__ void load8_perm(const float* p, int o0, float (&v)[8]) {
-  const float4 a = *reinterpret_cast<const float4*>(p + o0);
-  const float4 b = *reinterpret_cast<const float4*>(p + (4 - o0));
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-// 8 consecutive bf16 values in the lane's half order
-__device__ __forceinline__ void ldg8_bf16_perm(const uint16_t* p, int o0, float (&v)[8]) {
-  const uint2 a = __ldg(reinterpret_cast<const uint2*>(p + o0));
-  const uint2 b = __ldg(reinterpret_cast<const uint2*>(p + (4 - o0)));
-  v[0] = bf16_lo(a.x); v[1] = bf16_hi(a.x); v[2] = bf16_lo(a.y); v[3] = bf16_hi(a.y);
-  v[4] = bf16_lo(b.x); v[5] = bf16_hi(b.x); v[6] = bf16_lo(b.y); v[7] = bf16_hi(b.y);
-}
-// acc += p * v for the two fp16 values of w (low half -> acc.x), p an fp16 in the low 16 bits
-// of ph: the mixed-precision FMA takes fp16 operands and accumulates in fp32 (the product of
-// two fp16 is exact in fp32), so a value row needs no separate conversion to fp32
-__device__ __forceinline__ void fma_f16x2(float2& acc, uint32_t w, uint32_t ph) {
-  asm("{\n\t.reg .b16 l, h, p;\n\t"
-      "mov.b32 {l, h}, %2;\n\t"
-      "cvt.u16.u32 p, %3;\n\t"
-      "fma.rn.f32.f16 %0, l, p, %0;\n\t"
-      "fma.rn.f32.f16 %1, h, p, %1;\n\t}"
-      : "+f"(acc.x), "+f"(acc.y)
-      : "r"(w), "r"(ph));
-}
-// 8 consecutive fp16 values (one 128-bit shared load) into acc[0..3]
-__device__ __forceinline__ void lds8_fp16_fma(const unsigned char* p, uint32_t ph, float2 (&acc)[4]) {
-  const uint4 w = *reinterpret_cast<const uint4*>(p);
-  fma_f16x2(acc[0], w.x, ph);
-  fma_f16x2(acc[1], w.y, ph);
-  fma_f16x2(acc[2], w.z, ph);
-  fma_f16x2(acc[3], w.w, ph);
-}
-// 4 consecutive fp16 values (one 64-bit shared load) into a0, a1
-__device__ __forceinline__ void lds4_fp16_fma(const unsigned char* p, uint32_t ph, float2& a0, float2& a1) {
-  const uint2 w = *reinterpret_cast<const uint2*>(p);
-  fma_f16x2(a0, w.x, ph);
-  fma_f16x2(a1, w.y, ph);
-}
-// byte offset (index << 8) | lane_byte, the index being byte k of w (lane_byte < 256)
+
+// byte offset (index << 8) | lane_byte, the index being byte K of w (lane_byte < 256)
 template <int K>
 __device__ __forceinline__ uint32_t row_off(uint32_t w, uint32_t lane_byte) {
   return __byte_perm(w, lane_byte, 0x5504u | (K << 4));
 }
 
-__device__ __forceinline__ void transpose_reduce8(float (&p)[8], int s, unsigned mask) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const bool up = (s & 4) != 0;
-    const float send = up ? p[k] : p[k + 4];
-    const float keep = up ? p[k + 4] : p[k];
-    p[k] = keep + __shfl_xor_sync(mask, send, 4);
-  }
+// u <- R(-a) u for 4 channel pairs held as 2 float2 per half: lo' = lo c + hi s, hi' = hi c - lo s
+__device__ __forceinline__ void rotate4(float2 (&ul)[2], float2 (&uh)[2], const float2 (&c)[2], const float2 (&sn)[2]) {
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
-    const bool up = (s & 2) != 0;
-    const float send = up ? p[k] : p[k + 2];
-    const float keep = up ? p[k + 2] : p[k];
-    p[k] = keep + __shfl_xor_sync(mask, send, 2);
-  }
-  {
-    const bool up = (s & 1) != 0;
-    const float send = up ? p[0] : p[1];
-    const float keep = up ? p[1] : p[0];
-    p[0] = keep + __shfl_xor_sync(mask, send, 1);
-  }
-}
-
-// u <- R(-a) u for 8 channel pairs held as 4 float2 (pairs k, k+1) per half:
-//   lo' = lo cos(a) + hi sin(a),  hi' = hi cos(a) - lo sin(a)
-__device__ __forceinline__ void rotate8(float2 (&ul)[4], float2 (&uh)[4], const float2 (&c)[4],
-                                        const float2 (&sn)[4]) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
     const float2 l = ul[k], hh = uh[k];
     ul[k] = __ffma2_rn(l, c[k], __fmul2_rn(hh, sn[k]));
     uh[k] = __ffma2_rn(make_float2(-l.x, -l.y), sn[k], __fmul2_rn(hh, c[k]));
   }
 }
 
-// rotated query u = R(d) q for the lane's 8 pairs (lane half order), q from shared memory
-__device__ __forceinline__ void rotated_query(const float* rc, const float* rs, int d, int s, int o0,
-                                              const float* q, float2 (&ul)[4], float2 (&uh)[4]) {
-  float c8[8], s8[8], ql[8], qh[8];
-  ldg8_perm(rc + (size_t)d * (kD / 2) + 8 * s, o0, c8);
-  ldg8_perm(rs + (size_t)d * (kD / 2) + 8 * s, o0, s8);
-  load8_perm(q + 8 * s, o0, ql);
-  load8_perm(q + 64 + 8 * s, o0, qh);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    ul[k] = make_float2(ql[2 * k] * c8[2 * k] - qh[2 * k] * s8[2 * k],
-                        ql[2 * k + 1] * c8[2 * k + 1] - qh[2 * k + 1] * s8[2 * k + 1]);
-    uh[k] = make_float2(qh[2 * k] * c8[2 * k] + ql[2 * k] * s8[2 * k],
-                        qh[2 * k + 1] * c8[2 * k + 1] + ql[2 * k + 1] * s8[2 * k + 1]);
-  }
-}
+__device__ __forceinline__ float4 ldg_f4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
 
-// 8 consecutive bf16 values from shared memory in the lane's half order
-__device__ __forceinline__ void lds8_bf16_perm(const uint16_t* p, int o0, float (&v)[8]) {
-  const uint2 a = *reinterpret_cast<const uint2*>(p + o0);
-  const uint2 b = *reinterpret_cast<const uint2*>(p + (4 - o0));
-  v[0] = bf16_lo(a.x); v[1] = bf16_hi(a.x); v[2] = bf16_lo(a.y); v[3] = bf16_hi(a.y);
-  v[4] = bf16_lo(b.x); v[5] = bf16_hi(b.x); v[6] = bf16_lo(b.y); v[7] = bf16_hi(b.y);
+// 4 bf16 (8 bytes) -> 4 floats
+__device__ __forceinline__ void bf16x4(uint2 w, float (&v)[4]) {
+  v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
 }
 
 // A timed-out wait marks the block as failed; every later wait then returns at once, so a
-// block that lost a copy finishes (with the error word set) instead of hanging.
-__device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, volatile int* failed, int* err) {
+// block that lost a copy finishes (with the error word set) instead of hanging. Between polls
+// the hardware may suspend the waiting warp.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* failed, int* err) {
   if (*failed) return false;
-  if (mbar_wait_bounded(bar, parity)) return true;
+  if (mbar_wait_bounded_sleep(bar, parity)) return true;
   *failed = 1;
   set_error(err, KVQ_ERR_TIMEOUT);
   return false;
 }
 
-// Block-wide barrier on an mbarrier that every thread arrives on, with a bounded wait. Used
-// inside the unit loop instead of __syncthreads so that a failed wait elsewhere can never
-// leave threads parked at a barrier.
-__device__ __forceinline__ void block_sync(uint64_t* bar, uint32_t& phase, volatile int* failed, int* err) {
-  mbar_arrive(bar);
-  wait_stage(bar, phase, failed, err);
-  phase ^= 1u;
-}
-
-// running softmax state of one lane (the max is shared by its lane-group)
-struct Acc {
-  float M, l;
-  float2 ol[4], oh[4];
-};
-
-__device__ __forceinline__ void acc_reset(Acc& A) {
-  A.M = -INFINITY;
-  A.l = 0.f;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    A.ol[k] = make_float2(0.f, 0.f);
-    A.oh[k] = make_float2(0.f, 0.f);
-  }
-}
-
-// Fold the 8 scores of a page (lane s holds token s; -inf for a missing token) into the
-// running state: raise the shared max if needed (rescaling the sums), return this lane's
-// token weight.
-__device__ __forceinline__ float online_weights(Acc& A, float sc, unsigned mask) {
-  float mp = sc;
-  mp = fmaxf(mp, __shfl_xor_sync(mask, mp, 4));
-  mp = fmaxf(mp, __shfl_xor_sync(mask, mp, 2));
-  mp = fmaxf(mp, __shfl_xor_sync(mask, mp, 1));
-  if (mp > A.M) {  // uniform within the lane-group
-    const float f = (A.M == -INFINITY) ? 0.f : exp2f(A.M - mp);
-    const float2 f2 = make_float2(f, f);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      A.ol[k] = __fmul2_rn(A.ol[k], f2);
-      A.oh[k] = __fmul2_rn(A.oh[k], f2);
-    }
-    A.l *= f;
-    A.M = mp;
-  }
-  const float p = (sc == -INFINITY) ? 0.f : exp2f(sc - A.M);
-  A.l += p;
-  return p;
-}
-
-// Merge the running states of the lane-groups 8 and 16 lanes apart (all lanes end with the
-// merged state of their warp half pair, i.e. of the whole warp after both steps).
-__device__ __forceinline__ void merge_lane_groups(Acc& A) {
-#pragma unroll
-  for (int off = 8; off <= 16; off <<= 1) {
-    const float Mo = __shfl_xor_sync(0xFFFFFFFFu, A.M, off);
-    const float lo = __shfl_xor_sync(0xFFFFFFFFu, A.l, off);
-    const float Mn = fmaxf(A.M, Mo);
-    const float f = (A.M == -INFINITY) ? 0.f : exp2f(A.M - Mn);
-    const float fo = (Mo == -INFINITY) ? 0.f : exp2f(Mo - Mn);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 xl = make_float2(__shfl_xor_sync(0xFFFFFFFFu, A.ol[k].x, off),
-                                    __shfl_xor_sync(0xFFFFFFFFu, A.ol[k].y, off));
-      const float2 xh = make_float2(__shfl_xor_sync(0xFFFFFFFFu, A.oh[k].x, off),
-                                    __shfl_xor_sync(0xFFFFFFFFu, A.oh[k].y, off));
-      A.ol[k] = __ffma2_rn(A.ol[k], make_float2(f, f), __fmul2_rn(xl, make_float2(fo, fo)));
-      A.oh[k] = __ffma2_rn(A.oh[k], make_float2(f, f), __fmul2_rn(xh, make_float2(fo, fo)));
-    }
-    A.l = A.l * f + lo * fo;
-    A.M = Mn;
-  }
+// true in every aux thread when it is true in any (a barrier over the aux warps): the aux warps
+// take their exit decisions together, so none is left waiting at a named barrier
+__device__ __forceinline__ bool aux_any(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, %2, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)p), "n"(kAuxN)
+      : "memory");
+  return r != 0;
 }
 
 // Lengths of request b, or zeros when b >= B or when they do not describe a valid cache
-// (returns false then; the window kernel reports it).
+// (returns false then; block 0 reports it).
 __device__ __forceinline__ bool req_len(const VqAttnArgs& a, int b, int& L, int& NP) {
   L = 0;
   NP = 0;
@@ -295,144 +171,595 @@ __device__ __forceinline__ bool req_len(const VqAttnArgs& a, int b, int& L, int&
   return ok;
 }
 
-__device__ __forceinline__ int pair_units(int NP0, int NP1) { return (max(NP0, NP1) + kChunk - 1) / kChunk; }
+// share k of P page positions among G blocks starts at floor(k P / G)
+__device__ __forceinline__ long long share_lo(long long P, int k, int G) { return P * k / G; }
+// the block whose share holds position u (0 <= u < P)
+__device__ __forceinline__ int share_of(long long u, long long P, int G) { return (int)(((u + 1) * G - 1) / P); }
 
-// share k of U units among G blocks starts at unit floor(k U / G)
-__device__ __forceinline__ long long share_lo(long long U, int k, int G) { return U * k / G; }
-// the block whose share holds unit u (0 <= u < U)
-__device__ __forceinline__ int share_of(long long u, long long U, int G) { return (int)(((u + 1) * G - 1) / U); }
-
-// header of a unit in its ring stage
-struct UnitHdr {
-  int h, pair, c, flags;   // flags: 1 first unit of a piece, 2 last unit, (dest << 2)
-  int L0, NP0, L1, NP1;    // dest: 0 whole segment, 1 block's first piece, 2 block's last piece
+// A position in a block's share, one (head, request) segment at a time.
+struct Walk {
+  long long pos;   // global page position of the piece's first page
+  int h, b;        // segment
+  int pa, pb;      // its pages [pa, pb) inside the share
+  int L, np;       // request lengths
+  int valid;
 };
+static_assert(sizeof(Walk) <= 64, "walk fits its shared-memory slot");
 
-// a position in a block's share of units
-struct Walker {
-  long long i;  // unit index
-  int h, pair, c, nu;
-  int L0, NP0, L1, NP1;
-};
-
-// producer state (used by whichever warp refills a stage), in shared memory so it costs the
-// consumers no registers
-struct ProdState {
-  Walker cur;   // next unit to issue
-  int issued;   // units issued by this block
-  int k_loads;  // key-slice copies issued
-  long long lo, hi;  // the block's share: read here by the refilling warp, so the consumers
-                     // keep no registers for it
-};
-static_assert(sizeof(ProdState) <= 64, "producer state fits its shared-memory slot");
-
-__device__ __forceinline__ void walker_load_pair(const VqAttnArgs& a, Walker& P) {
-  req_len(a, 2 * P.pair, P.L0, P.NP0);
-  req_len(a, 2 * P.pair + 1, P.L1, P.NP1);
-  P.nu = pair_units(P.NP0, P.NP1);
-}
-
-// step to the next unit (the caller checks that one is left in the share), skipping request
-// pairs without pages
-__device__ __forceinline__ void walker_next(const VqAttnArgs& a, Walker& P, int n_pairs) {
-  ++P.i;
-  if (++P.c < P.nu) return;
-  P.c = 0;
+__device__ __forceinline__ void walk_next(const VqAttnArgs& a, Walk& W, long long hi) {
+  W.pos += W.pb - W.pa;
+  if (W.pos >= hi) {
+    W.valid = 0;
+    return;
+  }
   do {
-    if (++P.pair == n_pairs) {
-      P.pair = 0;
-      ++P.h;
+    if (++W.b == a.B) {
+      W.b = 0;
+      ++W.h;
     }
-    walker_load_pair(a, P);
-  } while (P.nu == 0 && P.h < a.H);
+    req_len(a, W.b, W.L, W.np);
+  } while (W.np == 0 && W.h < a.H);
+  if (W.h >= a.H) {
+    W.valid = 0;
+    return;
+  }
+  W.pa = 0;
+  W.pb = (int)min((long long)W.np, hi - W.pos);
 }
 
-// Issue the next unit into its ring stage (header, index pages, queries) and step to the one
-// after it.
-template <int NG>
-__device__ void prod_next(const VqAttnArgs& a, ProdState& S, unsigned char* ring, uint64_t* full, long long lo,
-                          long long hi, int n_pairs) {
-  using Ly = PageLay<NG>;
-  Walker& P = S.cur;
-  const int st = S.issued % Ly::kStg;
-  unsigned char* dst = ring + st * Ly::kStageBytes;
-  UnitHdr* hd = reinterpret_cast<UnitHdr*>(dst + Ly::kOffHdr);
-  const long long seg0 = P.i - P.c, seg1 = seg0 + P.nu;
-  int flags = 0;
-  if (P.i == lo || P.c == 0) flags |= 1;
-  if (P.i == hi - 1 || P.c == P.nu - 1) flags |= 2;
-  const int dest = (seg0 >= lo && seg1 <= hi) ? 0 : (seg0 <= lo ? 1 : 2);
-  hd->h = P.h;
-  hd->pair = P.pair;
-  hd->c = P.c;
-  hd->flags = flags | (dest << 2);
-  hd->L0 = P.L0;
-  hd->NP0 = P.NP0;
-  hd->L1 = P.L1;
-  hd->NP1 = P.NP1;
-  const int p_first = P.c * kChunk;
-  const int n0 = min(kChunk, max(0, P.NP0 - p_first));
-  const int n1 = min(kChunk, max(0, P.NP1 - p_first));
-  const int b0 = 2 * P.pair;
-  const bool two = b0 + 1 < a.B;
-  // the header stores above are released to the consumers by this arrive
-  mbar_arrive_expect_tx(&full[st], (uint32_t)(n0 + n1) * 2 * Ly::kPageB + (two ? 2u : 1u) * kD * 2);
-  const size_t off = (size_t)p_first * Ly::kPageB;
-  const size_t bh0 = ((size_t)b0 * a.H + P.h) * (size_t)a.max_pages * Ly::kPageB;
-  if (n0 > 0) {
-    bulk_g2s(dst, a.idx_k + bh0 + off, n0 * Ly::kPageB, &full[st]);
-    bulk_g2s(dst + 2 * Ly::kPart, a.idx_v + bh0 + off, n0 * Ly::kPageB, &full[st]);
+// ------------------------------------------------------------------ pass 1: scores of one page
+// Lane (s, m) of a 16-lane group: row = the 16-byte index row holding the lane's two groups for
+// the page's 8 tokens (byte 2t: lo-half group, 2t + 1: hi-half group). (u, up) = the rotated
+// query at the page's first token and one position earlier; each token advances them by the
+// three-term recurrence u' = 2 cos(theta) u - up, one FMA per component (a rotation by -theta
+// is a linear map whose two eigenvalues exp(-+i theta) sum to 2 cos theta). Returns the score of
+// token s in lanes 2s and 2s + 1.
+__device__ __forceinline__ float page_scores(const unsigned char* ksb, const uint4 row, const uint32_t lb,
+                                             float2 (&ul)[2], float2 (&uh)[2], float2 (&pl)[2], float2 (&ph)[2],
+                                             const float2 (&c2)[2], const int j, const unsigned gmask) {
+  float part[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    const uint32_t wd = (t < 2) ? row.x : (t < 4) ? row.y : (t < 6) ? row.z : row.w;
+    const uint32_t al = (t & 1) ? row_off<2>(wd, lb) : row_off<0>(wd, lb);
+    const uint32_t ah = (t & 1) ? row_off<3>(wd, lb) : row_off<1>(wd, lb);
+    const float4 lo = *reinterpret_cast<const float4*>(ksb + al);
+    const float4 hi = *reinterpret_cast<const float4*>(ksb + kKSliceBytes / 2 + ah);
+    float2 acc = __fmul2_rn(ul[0], make_float2(lo.x, lo.y));
+    acc = __ffma2_rn(uh[0], make_float2(hi.x, hi.y), acc);
+    acc = __ffma2_rn(ul[1], make_float2(lo.z, lo.w), acc);
+    acc = __ffma2_rn(uh[1], make_float2(hi.z, hi.w), acc);
+    part[t] = acc.x + acc.y;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float2 nl = __ffma2_rn(c2[k], ul[k], make_float2(-pl[k].x, -pl[k].y));
+      const float2 nh = __ffma2_rn(c2[k], uh[k], make_float2(-ph[k].x, -ph[k].y));
+      pl[k] = ul[k];
+      ph[k] = uh[k];
+      ul[k] = nl;
+      uh[k] = nh;
+    }
   }
-  if (n1 > 0) {
-    const size_t bh1 = ((size_t)(b0 + 1) * a.H + P.h) * (size_t)a.max_pages * Ly::kPageB;
-    bulk_g2s(dst + Ly::kPart, a.idx_k + bh1 + off, n1 * Ly::kPageB, &full[st]);
-    bulk_g2s(dst + 3 * Ly::kPart, a.idx_v + bh1 + off, n1 * Ly::kPageB, &full[st]);
+  // transposing reduction over the 16 lanes: after the xor-8/4/2 steps lane j holds token
+  // j >> 1 summed over 8 lanes, the xor-1 step adds the other channel quarter
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const bool up = (j & 8) != 0;
+    const float send = up ? part[k] : part[k + 4];
+    const float keep = up ? part[k + 4] : part[k];
+    part[k] = keep + __shfl_xor_sync(gmask, send, 8);
   }
-  bulk_g2s(dst + Ly::kOffQs, a.q + ((size_t)b0 * a.H + P.h) * kD, kD * 2, &full[st]);
-  if (two) bulk_g2s(dst + Ly::kOffQs + kD * 2, a.q + ((size_t)(b0 + 1) * a.H + P.h) * kD, kD * 2, &full[st]);
-  ++S.issued;
-  if (P.i + 1 < hi) walker_next(a, P, n_pairs);
-  else ++P.i;
-}
-
-template <int NG>
-__global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs a, const float scale_log2) {
-  using Ly = PageLay<NG>;
-  extern __shared__ __align__(128) unsigned char smem[];
-  float* ks = reinterpret_cast<float*>(smem + kOffK);
-  __half* vs = reinterpret_cast<__half*>(smem + kOffV);
-  unsigned char* ring = smem + Ly::kOffRing;
-  ProdState* ps = reinterpret_cast<ProdState*>(smem + Ly::kOffProd);
-  uint64_t* kbar = reinterpret_cast<uint64_t*>(smem + Ly::kOffBar);
-  uint64_t* full = kbar + 1;
-  uint64_t* bsync = full + Ly::kStg;
-  int* iflags = reinterpret_cast<int*>(bsync + 1);
-  volatile int* failed = iflags;
-  int* released = iflags + 1;  // [Ly::kStg]: warps done with the stage's current unit
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = gridDim.x, blk = blockIdx.x;
-  // let the window kernel launch now: its blocks take SMs as page blocks finish, attend
-  // their window tokens and wait for this grid before they read the partials
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int n_pairs = (a.B + 1) / 2;
-
-  // ---- units per request pair and their exclusive prefix (every block; block 0 publishes
-  //      it for the window kernel). Runs in the value-slice area before the slice is staged.
-  int* scan = reinterpret_cast<int*>(smem + kOffV);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const bool up = (j & 4) != 0;
+    const float send = up ? part[k] : part[k + 2];
+    const float keep = up ? part[k + 2] : part[k];
+    part[k] = keep + __shfl_xor_sync(gmask, send, 4);
+  }
   {
-    int* wsum = reinterpret_cast<int*>(ring);
-    for (int p = tid; p < n_pairs; p += kThreads) {
-      int L0, NP0, L1, NP1;
-      req_len(a, 2 * p, L0, NP0);
-      req_len(a, 2 * p + 1, L1, NP1);
-      scan[p] = pair_units(NP0, NP1);
+    const bool up = (j & 2) != 0;
+    const float send = up ? part[0] : part[1];
+    const float keep = up ? part[1] : part[0];
+    part[0] = keep + __shfl_xor_sync(gmask, send, 2);
+  }
+  part[0] += __shfl_xor_sync(gmask, part[0], 1);
+  return part[0];
+}
+
+// (x, y) -> R(a) (x, y) for the lane's 4 pairs: lo' = lo c - hi s, hi' = hi c + lo s
+__device__ __forceinline__ void rotate_fwd(const float2 (&ul)[2], const float2 (&uh)[2], const float2 (&c)[2],
+                                           const float2 (&sn)[2], float2 (&ol)[2], float2 (&oh)[2]) {
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    ol[k] = __ffma2_rn(ul[k], c[k], make_float2(-uh[k].x * sn[k].x, -uh[k].y * sn[k].y));
+    oh[k] = __ffma2_rn(uh[k], c[k], __fmul2_rn(ul[k], sn[k]));
+  }
+}
+
+// ------------------------------------------------------------------ pass 2: histogram of one page
+// w: this lane's fixed-point weight of token s (lanes 2t hold token t). bins: shared address of
+// the [256][32] u32 histogram. The lanes' columns make every red hit 32 distinct banks.
+template <int NG>
+__device__ __forceinline__ void page_hist(const uint4 row, const uint32_t w, const uint32_t bins, const int lane,
+                                          const unsigned gmask) {
+  const int j = lane & 15, s = j >> 1, m = j & 1, half = lane >> 4, base = lane & 16;
+  if constexpr (NG == 16) {
+    // group s + 8m, column 16 half + s + 8m; token t's index: byte 2t + m of the row
+    const uint32_t b0 = bins + (uint32_t)(16 * half + s + 8 * m) * 4;
+    const uint32_t sh = 8u * m;
+    const uint32_t rw[4] = {row.x >> sh, row.y >> sh, row.z >> sh, row.w >> sh};
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const uint32_t wt = __shfl_sync(gmask, w, base + 2 * t);
+      const uint32_t r = (rw[t >> 1] >> (16 * (t & 1))) & 0xFFu;
+      red_add_u32(b0 + (r << 7), wt);
+    }
+  } else if constexpr (NG == 8) {
+    // row s >> 1 holds groups s >> 1 (byte 2t) and (s >> 1) + 4 (byte 2t + 1); the lane takes
+    // group (s >> 1) + 4m for tokens 4 (s & 1) .. 4 (s & 1) + 3; copy 2 half + (s & 1)
+    const uint32_t b0 = bins + (uint32_t)(8 * (2 * half + (s & 1)) + (s >> 1) + 4 * m) * 4;
+    const uint32_t sh = 8u * m;
+    const uint32_t w0 = ((s & 1) ? row.z : row.x) >> sh, w1 = ((s & 1) ? row.w : row.y) >> sh;
+    const int t0 = 4 * (s & 1);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t wt = __shfl_sync(gmask, w, base + 2 * (t0 + t));
+      const uint32_t r = (((t < 2) ? w0 : w1) >> (16 * (t & 1))) & 0xFFu;
+      red_add_u32(b0 + (r << 7), wt);
+    }
+  } else {
+    // NG == 32: row j holds groups j (byte 2t) and j + 16 (byte 2t + 1); page half 0 takes the
+    // lo group first, half 1 the hi group first, so the two halves never share a column
+    const uint32_t ga = (uint32_t)(j + 16 * half), gb = (uint32_t)(j + 16 * (1 - half));
+    const uint32_t sa = 8u * half, sb = 8u * (1 - half);
+    const uint32_t ra[4] = {row.x >> sa, row.y >> sa, row.z >> sa, row.w >> sa};
+    const uint32_t rb[4] = {row.x >> sb, row.y >> sb, row.z >> sb, row.w >> sb};
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const uint32_t wt = __shfl_sync(gmask, w, base + 2 * t);
+      const uint32_t r0 = (ra[t >> 1] >> (16 * (t & 1))) & 0xFFu;
+      const uint32_t r1 = (rb[t >> 1] >> (16 * (t & 1))) & 0xFFu;
+      red_add_u32(bins + ga * 4 + (r0 << 7), wt);
+      red_add_u32(bins + gb * 4 + (r1 << 7), wt);
+    }
+  }
+}
+
+struct Bars {
+  uint64_t *full, *empty, *kbar, *ktfree, *maxbar, *hfull, *hfree;
+  volatile int* failed;
+  int* flag;  // aux: last-contributor flag
+};
+
+// ------------------------------------------------------------------ compute warps
+template <int NG>
+__device__ void compute_role(const VqAttnArgs& a, unsigned char* smem, const Bars& B, const float scale_log2) {
+  using Ly = Lay<NG>;
+  constexpr int PPL = Ly::kPPL;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int half = lane >> 4, j = lane & 15, s = j >> 1, m = j & 1;
+  const int pg0 = (warp * 2 + half) * PPL;  // this 16-lane group's first page of each unit
+  const unsigned gmask = 0xFFFFu << (lane & 16);
+  const int rowsel = (NG == 8) ? (s >> 1) : (NG == 16) ? s : j;
+  const uint32_t lb = 32u * s + 16u * m;  // the lane's 4 channels in a 256-byte key-table row
+  const int k0 = 8 * s + 4 * m;           // its first RoPE pair
+  const unsigned char* ksb = smem + Ly::kOffK;
+  float* sbuf = reinterpret_cast<float*>(smem + Ly::kOffSbuf);
+  float* wm = reinterpret_cast<float*>(smem + Ly::kOffWm);
+  const float* jt = reinterpret_cast<const float*>(smem + Ly::kOffJ);
+  const unsigned char* ring = smem + Ly::kOffRing;
+  const uint32_t bins = smem_u32(smem + Ly::kOffBins);
+
+  float2 c2[2];  // 2 cos(theta) of the lane's pairs
+  {
+    const float4 c4 = *reinterpret_cast<const float4*>(jt + 128 + k0);
+    c2[0] = make_float2(2.f * c4.x, 2.f * c4.y);
+    c2[1] = make_float2(2.f * c4.z, 2.f * c4.w);
+  }
+  // rotated query at the group's current token (u) and one position earlier (p)
+  float2 ul[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}, uh[2] = {ul[0], ul[1]};
+  float2 pl[2] = {ul[0], ul[1]}, ph[2] = {ul[0], ul[1]};
+  float wmax = -INFINITY, M = 0.f;
+  int cur_h = -1;
+  uint32_t kph = 0, mph = 0, hfph = 1;
+
+  for (int i = 0;; ++i) {
+    const int st = i % Ly::kStg;
+    if (!__all_sync(0xFFFFFFFFu, wait_bar(&B.full[st], (i / Ly::kStg) & 1, B.failed, a.err))) break;
+    const unsigned char* stage = ring + st * Ly::kStageB;
+    const int4 h0 = *reinterpret_cast<const int4*>(stage + Ly::kOffHdr);
+    const int4 h1 = *reinterpret_cast<const int4*>(stage + Ly::kOffHdr + 16);
+    const int flags = h0.x;
+    if (flags & kFEnd) break;
+    const int uh_ = h0.y, p0 = h0.w, npg = h1.x, L = h1.y, usub = h1.z;
+    uint4 rows[PPL];
+#pragma unroll
+    for (int pp = 0; pp < PPL; ++pp)
+      rows[pp] = (pg0 + pp < npg) ? *reinterpret_cast<const uint4*>(stage + (pg0 + pp) * Ly::kPageB + 16 * rowsel)
+                                  : make_uint4(0, 0, 0, 0);
+    const bool kunit = !(flags & kFV);
+    const bool act = pg0 < npg;
+    float ql[4], qh[4];
+    if (kunit && (flags & kFFirst) && act) {
+      const uint16_t* qs = reinterpret_cast<const uint16_t*>(stage + Ly::kOffQ);
+      bf16x4(*reinterpret_cast<const uint2*>(qs + k0), ql);
+      bf16x4(*reinterpret_cast<const uint2*>(qs + 64 + k0), qh);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&B.empty[st]);  // the stage is no longer needed: refill it
+    const int par = (flags & kFPar) ? 1 : 0;
+    float* sp = sbuf + (usub * Ly::kUP + pg0) * kPage;
+
+    if (kunit) {
+      if (uh_ != cur_h) {  // the producer staged this head's key slice
+        if (!__all_sync(0xFFFFFFFFu, wait_bar(B.kbar, kph, B.failed, a.err))) break;
+        kph ^= 1u;
+        cur_h = uh_;
+      }
+      if (flags & kFFirst) wmax = -INFINITY;
+      if (act) {
+        if (flags & kFFirst) {  // u = R(p_q - p) q from the cos/sin table at the group's first token
+          const int d = L - 1 - (a.sink + kPage * (p0 + pg0));
+          const float4 c4 = ldg_f4(a.rope_cos + (size_t)d * (kD / 2) + k0);
+          const float4 s4 = ldg_f4(a.rope_sin + (size_t)d * (kD / 2) + k0);
+          const float c[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
+          ul[0] = make_float2(ql[0] * c[0] - qh[0] * sn[0], ql[1] * c[1] - qh[1] * sn[1]);
+          ul[1] = make_float2(ql[2] * c[2] - qh[2] * sn[2], ql[3] * c[3] - qh[3] * sn[3]);
+          uh[0] = make_float2(qh[0] * c[0] + ql[0] * sn[0], qh[1] * c[1] + ql[1] * sn[1]);
+          uh[1] = make_float2(qh[2] * c[2] + ql[2] * sn[2], qh[3] * c[3] + ql[3] * sn[3]);
+        } else {  // one exact rotation over the other groups' pages of the last unit
+          const float4 jc = *reinterpret_cast<const float4*>(jt + k0);
+          const float4 js = *reinterpret_cast<const float4*>(jt + 64 + k0);
+          const float2 cj[2] = {make_float2(jc.x, jc.y), make_float2(jc.z, jc.w)};
+          const float2 sj[2] = {make_float2(js.x, js.y), make_float2(js.z, js.w)};
+          rotate4(ul, uh, cj, sj);
+        }
+        {  // the recurrence restarts from an exact pair: p = R(theta) u
+          const float4 tc = *reinterpret_cast<const float4*>(jt + 128 + k0);
+          const float4 ts = *reinterpret_cast<const float4*>(jt + 192 + k0);
+          const float2 cth[2] = {make_float2(tc.x, tc.y), make_float2(tc.z, tc.w)};
+          const float2 sth[2] = {make_float2(ts.x, ts.y), make_float2(ts.z, ts.w)};
+          rotate_fwd(ul, uh, cth, sth, pl, ph);
+        }
+#pragma unroll
+        for (int pp = 0; pp < PPL; ++pp) {
+          if (pg0 + pp < npg) {
+            const float sc = page_scores(ksb, rows[pp], lb, ul, uh, pl, ph, c2, j, gmask) * scale_log2;
+            if (m == 0) sp[pp * kPage + s] = sc;
+            wmax = fmaxf(wmax, sc);
+          }
+        }
+      }
+      if (flags & kFLast) {  // the warp's maximum over the sub-piece
+        float x = wmax;
+        x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, 16));
+        x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, 8));
+        x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, 4));
+        x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, 2));
+        x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, 1));
+        if (lane == 0) {
+          wm[par * kCW + warp] = x;
+          mbar_arrive(B.maxbar);
+        }
+      }
+      if (flags & kFHeadEnd) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B.ktfree);  // done with this head's key slice
+      }
+    } else {
+      if (flags & kFFirst) {
+        if (!__all_sync(0xFFFFFFFFu, wait_bar(B.maxbar, mph, B.failed, a.err))) break;
+        mph ^= 1u;
+        const float4* w4 = reinterpret_cast<const float4*>(wm + par * kCW);
+        float x = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kCW / 4; ++k) {
+          const float4 v = w4[k];
+          x = fmaxf(fmaxf(x, v.x), fmaxf(v.y, fmaxf(v.z, v.w)));
+        }
+        M = x;
+        // the aux warps cleared the histogram
+        if (!__all_sync(0xFFFFFFFFu, wait_bar(B.hfree, hfph, B.failed, a.err))) break;
+        hfph ^= 1u;
+      }
+#pragma unroll
+      for (int pp = 0; pp < PPL; ++pp) {
+        if (pg0 + pp < npg) {
+          // p = exp2(s - M) <= 1 in units of 2^-20: p + 8 has an ulp of 2^-20, so its mantissa is
+          // round(p 2^20) (nearest, ties to even)
+          const float p = exp2f(sp[pp * kPage + s] - M);
+          const uint32_t w = __float_as_uint(p + 8.0f) - 0x41000000u;
+          page_hist<NG>(rows[pp], w, bins, lane, gmask);
+        }
+      }
+      if (flags & kFLast) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B.hfull);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ producer (one lane)
+template <int NG>
+__device__ void producer_role(const VqAttnArgs& a, unsigned char* smem, const Bars& B, Walk W, const long long hi,
+                              int& issued, int& k_loads) {
+  using Ly = Lay<NG>;
+  unsigned char* ring = smem + Ly::kOffRing;
+  int cur_h = -1, sub_par = 0;
+  uint32_t ktf = 0;
+  while (W.valid) {
+    Walk nx = W;
+    walk_next(a, nx, hi);
+    if (W.h != cur_h) {
+      if (cur_h >= 0) {  // every compute warp is done with the previous head's slice
+        if (!wait_bar(B.ktfree, ktf, B.failed, a.err)) return;
+        ktf ^= 1u;
+      }
+      fence_proxy_async_smem();
+      const float* btk = a.bt_k + (size_t)W.h * kCB * kD;
+      mbar_arrive_expect_tx(B.kbar, kKSliceBytes);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        bulk_g2s(smem + Ly::kOffK + k * (kKSliceBytes / 4), btk + k * (kKSliceBytes / 16), kKSliceBytes / 4, B.kbar);
+      ++k_loads;
+      cur_h = W.h;
+    }
+    const size_t seg = ((size_t)W.b * a.H + W.h) * (size_t)a.max_pages;
+    for (int sa = W.pa; sa < W.pb; sa += kSubP) {
+      const int sb = min(sa + kSubP, W.pb), nu = (sb - sa + Ly::kUP - 1) / Ly::kUP;
+      const bool head_end = (sb == W.pb) && (!nx.valid || nx.h != W.h);
+      for (int kind = 0; kind < 2; ++kind)
+        for (int u = 0; u < nu; ++u) {
+          const int st = issued % Ly::kStg;
+          if (!wait_bar(&B.empty[st], ((issued / Ly::kStg) & 1) ^ 1, B.failed, a.err)) return;
+          fence_proxy_async_smem();
+          unsigned char* dst = ring + st * Ly::kStageB;
+          const int p0 = sa + u * Ly::kUP, npg = min(Ly::kUP, sb - p0);
+          int flags = (kind ? kFV : 0) | (u == 0 ? kFFirst : 0) | (u == nu - 1 ? kFLast : 0) | (sub_par ? kFPar : 0);
+          if (!kind && u == nu - 1 && head_end) flags |= kFHeadEnd;
+          int4* hd = reinterpret_cast<int4*>(dst + Ly::kOffHdr);
+          hd[0] = make_int4(flags, W.h, W.b, p0);
+          hd[1] = make_int4(npg, W.L, u, 0);
+          const uint32_t pb = (uint32_t)npg * Ly::kPageB;
+          mbar_arrive_expect_tx(&B.full[st], pb + (kind ? 0u : (uint32_t)kD * 2));
+          bulk_g2s(dst, (kind ? a.idx_v : a.idx_k) + (seg + p0) * Ly::kPageB, pb, &B.full[st]);
+          if (!kind) bulk_g2s(dst + Ly::kOffQ, a.q + ((size_t)W.b * a.H + W.h) * kD, kD * 2, &B.full[st]);
+          ++issued;
+        }
+      sub_par ^= 1;
+    }
+    W = nx;
+  }
+  const int st = issued % Ly::kStg;  // end marker: a header only
+  if (!wait_bar(&B.empty[st], ((issued / Ly::kStg) & 1) ^ 1, B.failed, a.err)) return;
+  int4* hd = reinterpret_cast<int4*>(ring + st * Ly::kStageB + Ly::kOffHdr);
+  hd[0] = make_int4(kFEnd, 0, 0, 0);
+  mbar_arrive(&B.full[st]);
+  ++issued;
+}
+
+// ------------------------------------------------------------------ aux warps
+__device__ __forceinline__ void aux_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kAuxN) : "memory"); }
+
+// merge (Mp, lp, op) into (M, l, o) (log2 domain)
+__device__ __forceinline__ void merge_part(float& M, float& l, float& o, float Mp, float lp, float op) {
+  if (Mp == -INFINITY) return;
+  const float Mn = fmaxf(M, Mp);
+  const float f = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
+  const float fp = exp2f(Mp - Mn);
+  l = l * f + lp * fp;
+  o = o * f + op * fp;
+  M = Mn;
+}
+
+// bf16 sink and recent tokens of segment (h, b): 4 warps take every 4th token, lane l holds
+// channels 2l, 2l+1 and their RoPE partners; returns the window's partial for channel `at`.
+__device__ void aux_window(const VqAttnArgs& a, int h, int b, int L, int NP, float scale_log2, float* wp, int at,
+                           float& Mo, float& lo_, float& oo) {
+  const int aw = at >> 5, lane = at & 31;
+  const int nsink = min(a.sink, L);
+  const int nwin = (L > 0) ? nsink + max(0, L - a.sink - kPage * NP) : 0;
+  const size_t bh = (size_t)b * a.H + h;
+  const uint32_t qa = __ldg(reinterpret_cast<const uint32_t*>(a.q + bh * kD + 2 * lane));
+  const uint32_t qb = __ldg(reinterpret_cast<const uint32_t*>(a.q + bh * kD + 64 + 2 * lane));
+  const float q0 = bf16_lo(qa), q1 = bf16_hi(qa), q2 = bf16_lo(qb), q3 = bf16_hi(qb);
+  const uint16_t* wk = a.win_k + bh * a.win_slots * kD;
+  const uint16_t* wv = a.win_v + bh * a.win_slots * kD;
+  float M = -INFINITY, l = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+  for (int w = aw; w < nwin; w += kAW) {
+    const int p = (w < nsink) ? w : a.sink + kPage * NP + (w - nsink);
+    const int slot = (p < a.sink) ? p : a.sink + (p - a.sink) % (a.recent + kPage);
+    const uint32_t ka = __ldg(reinterpret_cast<const uint32_t*>(wk + (size_t)slot * kD + 2 * lane));
+    const uint32_t kb = __ldg(reinterpret_cast<const uint32_t*>(wk + (size_t)slot * kD + 64 + 2 * lane));
+    const uint32_t va = __ldg(reinterpret_cast<const uint32_t*>(wv + (size_t)slot * kD + 2 * lane));
+    const uint32_t vb = __ldg(reinterpret_cast<const uint32_t*>(wv + (size_t)slot * kD + 64 + 2 * lane));
+    const int d = L - 1 - p;
+    const float2 c = __ldg(reinterpret_cast<const float2*>(a.rope_cos + (size_t)d * (kD / 2) + 2 * lane));
+    const float2 sn = __ldg(reinterpret_cast<const float2*>(a.rope_sin + (size_t)d * (kD / 2) + 2 * lane));
+    const float u0 = q0 * c.x - q2 * sn.x, u2 = q2 * c.x + q0 * sn.x;
+    const float u1 = q1 * c.y - q3 * sn.y, u3 = q3 * c.y + q1 * sn.y;
+    float dot = u0 * bf16_lo(ka) + u1 * bf16_hi(ka) + u2 * bf16_lo(kb) + u3 * bf16_hi(kb);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
+    const float sc = dot * scale_log2;
+    if (sc > M) {
+      const float f = (M == -INFINITY) ? 0.f : exp2f(M - sc);
+      l *= f; o0 *= f; o1 *= f; o2 *= f; o3 *= f;
+      M = sc;
+    }
+    const float pw = exp2f(sc - M);
+    l += pw;
+    o0 += pw * bf16_lo(va); o1 += pw * bf16_hi(va); o2 += pw * bf16_lo(vb); o3 += pw * bf16_hi(vb);
+  }
+  float* mine = wp + aw * 132;
+  mine[4 + 2 * lane] = o0; mine[5 + 2 * lane] = o1; mine[68 + 2 * lane] = o2; mine[69 + 2 * lane] = o3;
+  if (lane == 0) { mine[0] = M; mine[1] = l; }
+  aux_sync();
+  Mo = -INFINITY; lo_ = 0.f; oo = 0.f;
+#pragma unroll
+  for (int w = 0; w < kAW; ++w) merge_part(Mo, lo_, oo, wp[w * 132], wp[w * 132 + 1], wp[w * 132 + 4 + at]);
+  aux_sync();  // before the partial area is reused
+}
+
+// histogram of a finished sub-piece -> its partial (Ms, ls, os[at]); clears the histogram
+template <int NG>
+__device__ void aux_finalize(const VqAttnArgs& a, unsigned char* smem, int h, int par, int at, float& Ms, float& ls,
+                             float& os) {
+  using Ly = Lay<NG>;
+  constexpr int kCopies = kBinCols / NG, kCh = kD / NG;  // histogram copies, channels per group
+  const uint32_t* bins = reinterpret_cast<const uint32_t*>(smem + Ly::kOffBins);
+  float* red = reinterpret_cast<float*>(smem + Ly::kOffRed);
+  uint32_t* lred = reinterpret_cast<uint32_t*>(red + 4 * 128);
+  const float* wm = reinterpret_cast<const float*>(smem + Ly::kOffWm) + par * kCW;
+  Ms = wm[0];
+#pragma unroll
+  for (int w = 1; w < kCW; ++w) Ms = fmaxf(Ms, wm[w]);
+  const int cq = at & 31, rq = at >> 5;  // channels 4 cq .. 4 cq + 3, codewords 64 rq .. 64 rq + 63
+  const int g = (4 * cq) / kCh;
+  const uint16_t* E = a.bt_v + (size_t)h * kCB * kD + 4 * cq;
+  float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+  uint32_t lsum = 0;
+#pragma unroll 16
+  for (int r = 64 * rq; r < 64 * rq + 64; ++r) {
+    uint32_t bs = 0;
+#pragma unroll
+    for (int c = 0; c < kCopies; ++c) bs += bins[r * kBinCols + c * NG + g];
+    const uint2 e = __ldg(reinterpret_cast<const uint2*>(E + (size_t)r * kD));
+    const float f = (float)bs;
+    const float2 e01 = __half22float2(*reinterpret_cast<const __half2*>(&e.x));
+    const float2 e23 = __half22float2(*reinterpret_cast<const __half2*>(&e.y));
+    acc0 = fmaf(f, e01.x, acc0); acc1 = fmaf(f, e01.y, acc1); acc2 = fmaf(f, e23.x, acc2); acc3 = fmaf(f, e23.y, acc3);
+    lsum += bs;
+  }
+  *reinterpret_cast<float4*>(red + rq * 128 + 4 * cq) = make_float4(acc0, acc1, acc2, acc3);
+  if (cq == 0) lred[rq] = lsum;  // group 0: every token once
+  aux_sync();
+  const float inv = 1.f / (float)(1u << kFixBits);
+  os = (red[at] + red[128 + at] + red[256 + at] + red[384 + at]) * inv;
+  ls = (float)(lred[0] + lred[1] + lred[2] + lred[3]) * inv;
+  uint4* bz = reinterpret_cast<uint4*>(smem + Ly::kOffBins) + at;
+#pragma unroll
+  for (int k = 0; k < kBinBytes / 16 / kAuxN; ++k) bz[k * kAuxN] = make_uint4(0, 0, 0, 0);
+}
+
+// the segment's result from this block: the output itself when no other block holds part of
+// the segment, else a slot partial (and the merge, by the last contributor)
+__device__ void aux_emit(const VqAttnArgs& a, unsigned char* flag_smem, int h, int b, long long Ps, int np,
+                         long long Ptot, int blk, int at, float M, float l, float o) {
+  int k0 = 0, k1 = 0, count = 1;
+  if (np > 0) {
+    k0 = share_of(Ps, Ptot, a.G);
+    k1 = share_of(Ps + np - 1, Ptot, a.G);
+    count = 0;
+    for (int k = k0; k <= k1; ++k) count += share_lo(Ptot, k + 1, a.G) > share_lo(Ptot, k, a.G);
+  }
+  const size_t oi = ((size_t)b * a.H + h) * kD + at;
+  if (count <= 1) {
+    const float val = (l > 0.f) ? o / l : 0.f;
+    if (a.out_fp32) reinterpret_cast<float*>(a.out)[oi] = val;
+    else reinterpret_cast<uint16_t*>(a.out)[oi] = f32_to_bf16(val);
+    return;
+  }
+  volatile int* flag = reinterpret_cast<volatile int*>(flag_smem);
+  float* sp = a.slots + ((size_t)blk * 2 + (blk == k0 ? 1 : 0)) * kVqSlotFloats;
+  sp[4 + at] = o;
+  if (at == 0) { sp[0] = M; sp[1] = l; }
+  __threadfence();
+  aux_sync();
+  if (at == 0) {
+    const int old = atomicAdd(a.cnt + (size_t)h * a.B + b, 1);
+    *flag = (old == count - 1);
+  }
+  aux_sync();
+  if (*flag) {
+    __threadfence();
+    float Mx = -INFINITY, Lt = 0.f, ox = 0.f;
+    for (int k = k0; k <= k1; ++k) {
+      if (share_lo(Ptot, k + 1, a.G) == share_lo(Ptot, k, a.G)) continue;
+      const float* pp = a.slots + ((size_t)k * 2 + (k == k0 ? 1 : 0)) * kVqSlotFloats;
+      merge_part(Mx, Lt, ox, __ldcg(pp), __ldcg(pp + 1), __ldcg(pp + 4 + at));
+    }
+    const float val = (Lt > 0.f) ? ox / Lt : 0.f;
+    if (a.out_fp32) reinterpret_cast<float*>(a.out)[oi] = val;
+    else reinterpret_cast<uint16_t*>(a.out)[oi] = f32_to_bf16(val);
+    if (at == 0) a.cnt[(size_t)h * a.B + b] = 0;  // ready for the next call
+  }
+  aux_sync();  // before the flag is reused
+}
+
+template <int NG>
+__device__ void aux_role(const VqAttnArgs& a, unsigned char* smem, const Bars& B, Walk W, const long long hi,
+                         const long long Ptot, const float scale_log2) {
+  using Ly = Lay<NG>;
+  const int at = threadIdx.x - kAuxT0;
+  float* wp = reinterpret_cast<float*>(smem + Ly::kOffWp);
+  unsigned char* flag = reinterpret_cast<unsigned char*>(B.flag);
+  const int blk = blockIdx.x, G = a.G;
+  // segments without index pages: window only, spread over the blocks
+  for (long long sg = blk; sg < (long long)a.B * a.H; sg += G) {
+    const int h = (int)(sg / a.B), b = (int)(sg - (long long)h * a.B);
+    int L, NP;
+    req_len(a, b, L, NP);
+    if (NP != 0) continue;
+    float M, l, o;
+    aux_window(a, h, b, L, NP, scale_log2, wp, at, M, l, o);
+    aux_emit(a, flag, h, b, 0, 0, Ptot, blk, at, M, l, o);
+  }
+  uint32_t hfull_ph = 0;
+  int par = 0;
+  while (W.valid) {
+    float M = -INFINITY, l = 0.f, o = 0.f;
+    if (W.pa == 0) aux_window(a, W.h, W.b, W.L, W.np, scale_log2, wp, at, M, l, o);
+    for (int sa = W.pa; sa < W.pb; sa += kSubP) {
+      if (aux_any(!wait_bar(B.hfull, hfull_ph, B.failed, a.err))) return;
+      hfull_ph ^= 1u;
+      float Ms, ls, os;
+      aux_finalize<NG>(a, smem, W.h, par, at, Ms, ls, os);
+      mbar_arrive(B.hfree);  // this thread's reads and clears are done
+      merge_part(M, l, o, Ms, ls, os);
+      par ^= 1;
+    }
+    aux_emit(a, flag, W.h, W.b, W.pos - W.pa, W.np, Ptot, blk, at, M, l, o);
+    walk_next(a, W, hi);
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int NG>
+__global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a, const float scale_log2) {
+  using Ly = Lay<NG>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = a.G, blk = blockIdx.x;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Ly::kOffBar);
+  Bars B;
+  B.full = bar;
+  B.empty = bar + Ly::kStg;
+  B.kbar = bar + 2 * Ly::kStg;
+  B.ktfree = B.kbar + 1;
+  B.maxbar = B.kbar + 2;
+  B.hfull = B.kbar + 3;
+  B.hfree = B.kbar + 4;
+  int* iflags = reinterpret_cast<int*>(B.kbar + 5);
+  B.failed = iflags;
+  B.flag = iflags + 1;
+  Walk* wstart = reinterpret_cast<Walk*>(smem + Ly::kOffWalk);
+
+  // ---- pages per request and their exclusive prefix (in the histogram area, cleared after)
+  int* pre = reinterpret_cast<int*>(smem + Ly::kOffBins);
+  {
+    int* wsum = reinterpret_cast<int*>(smem + Ly::kOffSbuf);
+    for (int b = tid; b < a.B; b += kThreads) {
+      int L, NP;
+      if (!req_len(a, b, L, NP) && blk == 0) set_error(a.err, KVQ_ERR_CAPACITY);
+      pre[b] = NP;
     }
     __syncthreads();
-    const int per = (n_pairs + kThreads - 1) / kThreads;
-    const int beg = min(n_pairs, tid * per), end = min(n_pairs, beg + per);
+    const int per = (a.B + kThreads - 1) / kThreads;
+    const int beg = min(a.B, tid * per), end = min(a.B, beg + per);
     int local = 0;
-    for (int p = beg; p < end; ++p) local += scan[p];
+    for (int b = beg; b < end; ++b) local += pre[b];
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -443,478 +770,116 @@ __global__ void __launch_bounds__(kThreads, 1) vq_pages_kernel(const VqAttnArgs 
     __syncthreads();
     int run = incl - local;
     for (int w = 0; w < warp; ++w) run += wsum[w];
-    for (int p = beg; p < end; ++p) {
-      const int u = scan[p];
-      scan[p] = run;
+    for (int b = beg; b < end; ++b) {
+      const int u = pre[b];
+      pre[b] = run;
       run += u;
     }
-    if (tid == kThreads - 1) scan[n_pairs] = run;  // the last thread ends on the total
+    if (tid == kThreads - 1) pre[a.B] = run;  // the last thread ends on the total
     __syncthreads();
   }
-  if (blk == 0)
-    for (int p = tid; p <= n_pairs; p += kThreads) a.pref[p] = scan[p];
-  const int Up = scan[n_pairs];
-  const long long U = (long long)a.H * Up;
-  const long long lo = share_lo(U, blk, G), hi = share_lo(U, blk + 1, G);
-  if (lo >= hi) return;  // uniform: an empty share
+  const long long Pb = pre[a.B];
+  const long long Ptot = (long long)a.H * Pb;
+  const long long lo = share_lo(Ptot, blk, G), hi = share_lo(Ptot, blk + 1, G);
 
   if (tid == 0) {
-    mbar_init(kbar, 1);
 #pragma unroll
     for (int s = 0; s < Ly::kStg; ++s) {
-      mbar_init(&full[s], 1);
-      released[s] = 0;
+      mbar_init(&B.full[s], 1);
+      mbar_init(&B.empty[s], kCW);
     }
-    mbar_init(bsync, kThreads);
-    *failed = 0;
+    mbar_init(B.kbar, 1);
+    mbar_init(B.ktfree, kCW);
+    mbar_init(B.maxbar, kCW);
+    mbar_init(B.hfull, kCW);
+    mbar_init(B.hfree, kAuxN);
+    *B.failed = 0;
     fence_mbar_init();
-    // first unit of the share: head, then the last pair whose prefix is <= the remainder
-    Walker& P = ps->cur;
-    ps->issued = 0;
-    ps->k_loads = 0;
-    ps->lo = lo;
-    ps->hi = hi;
-    P.i = lo;
-    P.h = (int)(lo / Up);
-    const int rem = (int)(lo - (long long)P.h * Up);
-    int pl = 0, ph = n_pairs - 1;
-    while (pl < ph) {
-      const int mid = (pl + ph + 1) >> 1;
-      if (scan[mid] <= rem) pl = mid;
-      else ph = mid - 1;
-    }
-    P.pair = pl;
-    P.c = rem - scan[pl];
-    walker_load_pair(a, P);
-    // codebook slices of the (at most 4 first) heads of the share: HBM -> L2 now
-    const int h_last = min((int)((hi - 1) / Up), P.h + 3);
-    for (int hh = P.h; hh <= h_last; ++hh)
-      for (int k = 0; k < 4; ++k) {
-        bulk_prefetch_l2(a.bt_k + (size_t)hh * kCB * kD + k * (kCB * kD / 4), kKSliceBytes / 4);
-        bulk_prefetch_l2(a.bt_v + (size_t)hh * kCB * kD + k * (kCB * kD / 4), kVSliceBytes / 4);
+    Walk W;
+    W.valid = 0;
+    if (lo < hi) {  // the first piece: head, then the last request whose prefix is <= the remainder
+      W.valid = 1;
+      W.pos = lo;
+      W.h = (int)(lo / Pb);
+      const int rem = (int)(lo - (long long)W.h * Pb);
+      int bl = 0, bh = a.B - 1;
+      while (bl < bh) {
+        const int mid = (bl + bh + 1) >> 1;
+        if (pre[mid] <= rem) bl = mid;
+        else bh = mid - 1;
       }
+      W.b = bl;
+      W.pa = rem - pre[bl];
+      req_len(a, W.b, W.L, W.np);
+      W.pb = (int)min((long long)W.np, W.pa + (hi - lo));
+      // the share's later key slices: HBM -> L2 now (a share spans few heads)
+      const int h_last = min((int)((hi - 1) / Pb), W.h + 3);
+      for (int hh = W.h + 1; hh <= h_last; ++hh) bulk_prefetch_l2(a.bt_k + (size_t)hh * kCB * kD, kKSliceBytes);
+    }
+    *wstart = W;
   }
-  if (tid < 8 && a.max_ctx > kJump) {
-    // cos/sin((kJump - 7) theta_i) for slot tid in that slot's half order, stored [chunk][slot]
-    // so that the 8 slots of a lane-group read 8 consecutive float4s (no bank conflicts): the
-    // step from the last token of one of a lane-group's pages to the first of its next
-    float4* jt = reinterpret_cast<float4*>(smem + Ly::kOffJ);
-    const int jo0 = (tid & 4) ? 4 : 0;
-    float c8[8], s8[8];
-    ldg8_perm(a.rope_cos + (size_t)(kJump - 7) * (kD / 2) + 8 * tid, jo0, c8);
-    ldg8_perm(a.rope_sin + (size_t)(kJump - 7) * (kD / 2) + 8 * tid, jo0, s8);
-    jt[0 * 8 + tid] = make_float4(c8[0], c8[1], c8[2], c8[3]);
-    jt[1 * 8 + tid] = make_float4(c8[4], c8[5], c8[6], c8[7]);
-    jt[2 * 8 + tid] = make_float4(s8[0], s8[1], s8[2], s8[3]);
-    jt[3 * 8 + tid] = make_float4(s8[4], s8[5], s8[6], s8[7]);
+  if (tid < 64) {  // cos, sin(kJump theta_i): from one past a group's last token of a unit to its next
+    float* jt = reinterpret_cast<float*>(smem + Ly::kOffJ);
+    const bool have = a.max_ctx > Ly::kJump;
+    jt[tid] = have ? __ldg(a.rope_cos + (size_t)Ly::kJump * (kD / 2) + tid) : 1.f;
+    jt[64 + tid] = have ? __ldg(a.rope_sin + (size_t)Ly::kJump * (kD / 2) + tid) : 0.f;
+    const int row = (a.max_ctx > 1) ? 1 : 0;  // one position: the per-token step
+    jt[128 + tid] = __ldg(a.rope_cos + (size_t)row * (kD / 2) + tid);
+    jt[192 + tid] = __ldg(a.rope_sin + (size_t)row * (kD / 2) + tid);
   }
-  __syncthreads();  // barriers initialised, scan read by thread 0: the value area is free
-  if (tid == 0)
-    for (int s = 0; s < Ly::kStg && ps->cur.i < hi; ++s) prod_next<NG>(a, *ps, ring, full, lo, hi, n_pairs);
-
-  const int s = tid & 7;                 // slot: groups s and s + 8
-  const int o0 = (s & 4) ? 4 : 0;        // key half order (bank-quad spreading)
-  const unsigned gmask = 0xFFu << (lane & 24);
-  const int lg = tid >> 3;
-  const int r = lg / kChunk, po = lg % kChunk;  // this lane-group's request and page slot
-
-  float2 cth[4], sth[4];
+  __syncthreads();  // barriers initialised, prefix read: the histogram area is free
   {
-    float c8[8], s8[8];
-    const int row = (a.max_ctx > 1) ? 1 : 0;
-    ldg8_perm(a.rope_cos + (size_t)row * (kD / 2) + 8 * s, o0, c8);
-    ldg8_perm(a.rope_sin + (size_t)row * (kD / 2) + 8 * s, o0, s8);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      cth[k] = make_float2(c8[2 * k], c8[2 * k + 1]);
-      sth[k] = make_float2(s8[2 * k], s8[2 * k + 1]);
-    }
+    uint4* bz = reinterpret_cast<uint4*>(smem + Ly::kOffBins);
+    for (int k = tid; k < kBinBytes / 16; k += kThreads) bz[k] = make_uint4(0, 0, 0, 0);
   }
-  // the lane-group's rotated query, advanced token by token through its pages
-  float2 ulo[4], uhi[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    ulo[k] = make_float2(0.f, 0.f);
-    uhi[k] = make_float2(0.f, 0.f);
+  __syncthreads();
+
+  int issued = 0, k_loads = 0;
+  if (warp < kCW) {
+    compute_role<NG>(a, smem, B, scale_log2);
+  } else if (warp < kCW + kAW) {
+    aux_role<NG>(a, smem, B, *wstart, hi, Ptot, scale_log2);
+  } else if (lane == 0) {
+    producer_role<NG>(a, smem, B, *wstart, hi, issued, k_loads);
   }
-  Acc A;
-  acc_reset(A);
-  // lane byte offsets inside a 256-byte table row: key halves swapped for s >= 4 so the 8
-  // lanes of a phase hit 8 bank quads; value lanes read 16 natural bytes each
-  const uint32_t kb0 = 32 * s + 4 * o0, kb1 = kb0 ^ 16u;
-  const uint32_t vb0 = 16 * s, vb1 = 128 + 16 * s;
-  const unsigned char* ksb = reinterpret_cast<const unsigned char*>(ks);
-  const unsigned char* vsb = reinterpret_cast<const unsigned char*>(vs);
-  const float4* jt = reinterpret_cast<const float4*>(smem + Ly::kOffJ) + s;
-
-  const int n_units = (int)(hi - lo);
-  int cur_head = -1;
-  uint32_t kphase = 0, sphase = 0;
-  for (int i = 0; i < n_units; ++i) {
-    const int st = i % Ly::kStg;
-    wait_stage(&full[st], (i / Ly::kStg) & 1, failed, a.err);
-    // ---- everything this thread needs from the stage goes to registers, then the stage is
-    //      released: its refill overlaps this unit's work
-    const unsigned char* stage = ring + st * Ly::kStageBytes;
-    const int4 hv0 = *reinterpret_cast<const int4*>(stage + Ly::kOffHdr);
-    const int4 hv1 = *reinterpret_cast<const int4*>(stage + Ly::kOffHdr + 16);
-    const int uh = hv0.x, upair = hv0.y, uc = hv0.z, uflags = hv0.w;
-    const int L = r ? hv1.z : hv1.x, NP = r ? hv1.w : hv1.y;
-    const int pg = uc * kChunk + po;
-    const bool active = !*failed && pg < NP;
-    const bool resync = (uflags & 1) || uc % kResync == 0;
-    // the lane's index words: 16 bytes (tokens 0..7 x lo/hi group) of its slot's row; with
-    // c = 4 two slots (groups 2s and 2s + 1 of each half), the key row serving la first
-    uint4 rowk = make_uint4(0, 0, 0, 0), rowv = rowk, rowk2 = rowk, rowv2 = rowk;
-    float ql[8], qh[8];
-    if (active) {
-      const unsigned char* pk = stage + r * Ly::kPart + po * Ly::kPageB;
-      const unsigned char* pv = stage + (2 + r) * Ly::kPart + po * Ly::kPageB;
-      if constexpr (NG == 32) {
-        rowk = *reinterpret_cast<const uint4*>(pk + 32 * s + 4 * o0);
-        rowk2 = *reinterpret_cast<const uint4*>(pk + 32 * s + 16 - 4 * o0);
-        rowv = *reinterpret_cast<const uint4*>(pv + 32 * s);
-        rowv2 = *reinterpret_cast<const uint4*>(pv + 32 * s + 16);
-      } else {
-        constexpr int kSlotShift = (NG == 8) ? 1 : 0;  // c = 16: lanes 2p and 2p + 1 share slot p
-        rowk = *reinterpret_cast<const uint4*>(pk + 16 * (s >> kSlotShift));
-        rowv = *reinterpret_cast<const uint4*>(pv + 16 * (s >> kSlotShift));
-      }
-      if (resync) {
-        const uint16_t* qr = reinterpret_cast<const uint16_t*>(stage + Ly::kOffQs) + r * kD;
-        lds8_bf16_perm(qr + 8 * s, o0, ql);
-        lds8_bf16_perm(qr + 64 + 8 * s, o0, qh);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) {
-      // the last warp done with this stage refills it with the unit Ly::kStg ahead: no warp
-      // waits to produce, and the copy starts as soon as the stage is free
-      if (atom_add_acq_rel_shared(&released[st], 1) == kWarps - 1) {
-        released[st] = 0;
-        if (!*failed && ps->cur.i < ps->hi) {
-          fence_proxy_async_smem();
-          prod_next<NG>(a, *ps, ring, full, ps->lo, ps->hi, n_pairs);
-        }
-      }
-    }
-
-    if (uh != cur_head) {  // uniform: every thread read the same header
-      // ---- stage the codebook slices of head uh ----
-      block_sync(bsync, sphase, failed, a.err);  // every warp is done with the old slices
-      if (tid == 0 && !*failed) {  // both slices by TMA: fp32 keys 128 KB, fp16 values 64 KB
-        const float* btk = a.bt_k + (size_t)uh * kCB * kD;
-        const uint16_t* btv = a.bt_v + (size_t)uh * kCB * kD;
-        mbar_arrive_expect_tx(kbar, kKSliceBytes + kVSliceBytes);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          bulk_g2s(ks + k * (kKSliceBytes / 16), btk + k * (kKSliceBytes / 16), kKSliceBytes / 4, kbar);
-          bulk_g2s(vs + k * (kVSliceBytes / 8), btv + k * (kVSliceBytes / 8), kVSliceBytes / 4, kbar);
-        }
-        ++ps->k_loads;
-      }
-      wait_stage(kbar, kphase, failed, a.err);
-      kphase ^= 1u;
-      cur_head = uh;
-    }
-    if (uflags & 1) acc_reset(A);  // a new piece
-
-    if (active) {
-      if (resync) {  // u = R(p_q - p) q from the cos/sin table
-        const int d = L - 1 - (a.sink + kPage * pg);
-        float c8[8], s8[8];
-        ldg8_perm(a.rope_cos + (size_t)d * (kD / 2) + 8 * s, o0, c8);
-        ldg8_perm(a.rope_sin + (size_t)d * (kD / 2) + 8 * s, o0, s8);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          ulo[k] = make_float2(ql[2 * k] * c8[2 * k] - qh[2 * k] * s8[2 * k],
-                                ql[2 * k + 1] * c8[2 * k + 1] - qh[2 * k + 1] * s8[2 * k + 1]);
-          uhi[k] = make_float2(qh[2 * k] * c8[2 * k] + ql[2 * k] * s8[2 * k],
-                                qh[2 * k + 1] * c8[2 * k + 1] + ql[2 * k + 1] * s8[2 * k + 1]);
-        }
-      } else {  // the next page: kJump - 7 positions after this lane-group's last token
-        const float4 c0 = jt[0], c1 = jt[8], s0 = jt[16], s1 = jt[24];
-        const float2 cj[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w), make_float2(c1.x, c1.y),
-                              make_float2(c1.z, c1.w)};
-        const float2 sj[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
-                              make_float2(s1.z, s1.w)};
-        rotate8(ulo, uhi, cj, sj);
-      }
-      float part[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t wd = (j < 2) ? rowk.x : (j < 4) ? rowk.y : (j < 6) ? rowk.z : rowk.w;
-        uint32_t wd2 = wd;  // c = 4: the index of the other 4 channels of each half
-        if constexpr (NG == 32) wd2 = (j < 2) ? rowk2.x : (j < 4) ? rowk2.y : (j < 6) ? rowk2.z : rowk2.w;
-        uint32_t al0, al1, ah0, ah1;
-        if (j & 1) {
-          al0 = row_off<2>(wd, kb0); al1 = row_off<2>(wd2, kb1);
-          ah0 = row_off<3>(wd, kb0); ah1 = row_off<3>(wd2, kb1);
-        } else {
-          al0 = row_off<0>(wd, kb0); al1 = row_off<0>(wd2, kb1);
-          ah0 = row_off<1>(wd, kb0); ah1 = row_off<1>(wd2, kb1);
-        }
-        const float4 la = *reinterpret_cast<const float4*>(ksb + al0);
-        const float4 lb = *reinterpret_cast<const float4*>(ksb + al1);
-        const float4 ha = *reinterpret_cast<const float4*>(ksb + kKSliceBytes / 2 + ah0);
-        const float4 hb = *reinterpret_cast<const float4*>(ksb + kKSliceBytes / 2 + ah1);
-        float2 acc = __fmul2_rn(ulo[0], make_float2(la.x, la.y));  // one chain: fewer live registers
-        acc = __ffma2_rn(uhi[0], make_float2(ha.x, ha.y), acc);
-        acc = __ffma2_rn(ulo[1], make_float2(la.z, la.w), acc);
-        acc = __ffma2_rn(uhi[1], make_float2(ha.z, ha.w), acc);
-        acc = __ffma2_rn(ulo[2], make_float2(lb.x, lb.y), acc);
-        acc = __ffma2_rn(uhi[2], make_float2(hb.x, hb.y), acc);
-        acc = __ffma2_rn(ulo[3], make_float2(lb.z, lb.w), acc);
-        acc = __ffma2_rn(uhi[3], make_float2(hb.z, hb.w), acc);
-        part[j] = acc.x + acc.y;
-        if (j < 7) rotate8(ulo, uhi, cth, sth);  // next token: one position later
-      }
-      transpose_reduce8(part, s, gmask);
-      const float p = online_weights(A, part[0] * scale_log2, gmask);
-      // the weights enter the value sums rounded to fp16 (relative error 2^-12; the
-      // normaliser l keeps the fp32 weights)
-      const uint32_t ph = __half_as_ushort(__float2half_rn(p));
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t pj = __shfl_sync(gmask, ph, (lane & 24) + j);
-        const uint32_t wd = (j < 2) ? rowv.x : (j < 4) ? rowv.y : (j < 6) ? rowv.z : rowv.w;
-        const uint32_t avl = (j & 1) ? row_off<2>(wd, vb0) : row_off<0>(wd, vb0);
-        const uint32_t avh = (j & 1) ? row_off<3>(wd, vb1) : row_off<1>(wd, vb1);
-        if constexpr (NG == 32) {  // channels 8s .. 8s + 3 and 8s + 4 .. 8s + 7 from two codewords
-          const uint32_t wd2 = (j < 2) ? rowv2.x : (j < 4) ? rowv2.y : (j < 6) ? rowv2.z : rowv2.w;
-          const uint32_t avl2 = (j & 1) ? row_off<2>(wd2, vb0 + 8) : row_off<0>(wd2, vb0 + 8);
-          const uint32_t avh2 = (j & 1) ? row_off<3>(wd2, vb1 + 8) : row_off<1>(wd2, vb1 + 8);
-          lds4_fp16_fma(vsb + avl, pj, A.ol[0], A.ol[1]);
-          lds4_fp16_fma(vsb + avl2, pj, A.ol[2], A.ol[3]);
-          lds4_fp16_fma(vsb + avh, pj, A.oh[0], A.oh[1]);
-          lds4_fp16_fma(vsb + avh2, pj, A.oh[2], A.oh[3]);
-        } else {
-          lds8_fp16_fma(vsb + avl, pj, A.ol);
-          lds8_fp16_fma(vsb + avh, pj, A.oh);
-        }
-      }
-    }
-
-    if (uflags & 2) {
-      // ---- end of a piece: lanes of a group (l), lane-groups (shuffles); each warp writes
-      //      its partial (M, l, o[128]) for the window kernel to merge
-      A.l += __shfl_xor_sync(0xFFFFFFFFu, A.l, 1);
-      A.l += __shfl_xor_sync(0xFFFFFFFFu, A.l, 2);
-      A.l += __shfl_xor_sync(0xFFFFFFFFu, A.l, 4);
-      merge_lane_groups(A);
-      if (lane < 8 && 2 * upair + r < a.B) {
-        const int dest = uflags >> 2;
-        float* pp = (dest == 0) ? a.part_whole + ((size_t)uh * n_pairs + upair) * kVqPartFloats
-                                : a.part_slot + ((size_t)blk * 2 + (dest - 1)) * kVqPartFloats;
-        pp += (r * kVqWarpsPerReq + (warp - r * kVqWarpsPerReq)) * (kD + 2);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          reinterpret_cast<float2*>(pp + 2 + 8 * s)[k] = A.ol[k];
-          reinterpret_cast<float2*>(pp + 2 + 64 + 8 * s)[k] = A.oh[k];
-        }
-        if (lane == 0) {
-          pp[0] = A.M;
-          pp[1] = A.l;
-        }
-      }
-    }
-  }
-
-  __syncthreads();  // every producer step is done
+  __syncthreads();
   // after a timeout, let the block's own copies in flight land before it exits
-  if (tid == 0 && *failed) {
-    const int issued = ps->issued;
-    for (int j = max(0, issued - Ly::kStg); j < issued; ++j) mbar_wait_bounded(&full[j % Ly::kStg], (j / Ly::kStg) & 1);
-    if (ps->k_loads > 0) mbar_wait_bounded(kbar, (ps->k_loads - 1) & 1);
+  if (warp == kProdWarp && lane == 0 && *B.failed) {
+    for (int k = max(0, issued - Ly::kStg); k < issued; ++k) mbar_wait_bounded(&B.full[k % Ly::kStg], (k / Ly::kStg) & 1);
+    if (k_loads > 0) mbar_wait_bounded(B.kbar, (k_loads - 1) & 1);
   }
-}
-
-// ------------------------------------------------------------------ window + merge kernel
-// WT threads per block: 128 when the (request, head) blocks fill the GPU (7 resident per SM),
-// 512 when there are no more blocks than SMs (long windows of few requests: 4 times the
-// lane-groups per window, so a window's tokens take a quarter of the serial steps)
-template <int WT>
-__global__ void __launch_bounds__(WT, (WT == 128) ? 7 : 1) vq_window_kernel(const VqAttnArgs a, const float scale_log2) {
-  __shared__ __align__(16) float qs[kD];
-  __shared__ __align__(16) float wpart[WT / 32][kD + 2];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = blockIdx.x / a.H, h = blockIdx.x - b * a.H;
-  int L, NP;
-  if (!req_len(a, b, L, NP) && h == 0 && tid == 0) set_error(a.err, KVQ_ERR_CAPACITY);
-  if (tid < kD) qs[tid] = bf16_to_f32(a.q[((size_t)b * a.H + h) * kD + tid]);
-  __syncthreads();
-
-  // ---- bf16 window: lane-group g takes tokens g, g + 16, ... ----------------------------
-  const int nsink = min(a.sink, L);
-  const int nwin = (L > 0) ? nsink + max(0, L - a.sink - kPage * NP) : 0;
-  const int s = lane & 7, g = tid >> 3;
-  const unsigned gmask = 0xFFu << (lane & 24);
-  const uint16_t* wk = a.win_k + ((size_t)b * a.H + h) * a.win_slots * kD;
-  const uint16_t* wv = a.win_v + ((size_t)b * a.H + h) * a.win_slots * kD;
-  Acc A;  // here l is the same in every lane of a lane-group
-  acc_reset(A);
-  for (int w = g; w < nwin; w += WT / 8) {
-    const int p = (w < nsink) ? w : a.sink + kPage * NP + (w - nsink);
-    const int slot = (p < a.sink) ? p : a.sink + (p - a.sink) % (a.recent + kPage);
-    float kl[8], kh[8], vl[8], vh[8];
-    ldg8_bf16_perm(wk + (size_t)slot * kD + 8 * s, 0, kl);
-    ldg8_bf16_perm(wk + (size_t)slot * kD + 64 + 8 * s, 0, kh);
-    ldg8_bf16_perm(wv + (size_t)slot * kD + 8 * s, 0, vl);
-    ldg8_bf16_perm(wv + (size_t)slot * kD + 64 + 8 * s, 0, vh);
-    float2 ul[4], uh[4];
-    rotated_query(a.rope_cos, a.rope_sin, L - 1 - p, s, 0, qs, ul, uh);
-    float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      acc = __ffma2_rn(ul[k], make_float2(kl[2 * k], kl[2 * k + 1]), acc);
-      acc = __ffma2_rn(uh[k], make_float2(kh[2 * k], kh[2 * k + 1]), acc);
-    }
-    float sc = acc.x + acc.y;
-    sc += __shfl_xor_sync(gmask, sc, 4);
-    sc += __shfl_xor_sync(gmask, sc, 2);
-    sc += __shfl_xor_sync(gmask, sc, 1);
-    sc *= scale_log2;
-    if (sc > A.M) {
-      const float f = (A.M == -INFINITY) ? 0.f : exp2f(A.M - sc);
-      const float2 f2 = make_float2(f, f);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        A.ol[k] = __fmul2_rn(A.ol[k], f2);
-        A.oh[k] = __fmul2_rn(A.oh[k], f2);
-      }
-      A.l *= f;
-      A.M = sc;
-    }
-    const float pw = exp2f(sc - A.M);
-    A.l += pw;
-    const float2 p2 = make_float2(pw, pw);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      A.ol[k] = __ffma2_rn(p2, make_float2(vl[2 * k], vl[2 * k + 1]), A.ol[k]);
-      A.oh[k] = __ffma2_rn(p2, make_float2(vh[2 * k], vh[2 * k + 1]), A.oh[k]);
-    }
-  }
-  merge_lane_groups(A);
-  if (lane < 8) {
-    float* wp = wpart[warp];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      reinterpret_cast<float2*>(wp + 8 * s)[k] = A.ol[k];
-      reinterpret_cast<float2*>(wp + 64 + 8 * s)[k] = A.oh[k];
-    }
-    if (lane == 0) {
-      wp[kD] = A.M;
-      wp[kD + 1] = A.l;
-    }
-  }
-  __syncthreads();
-
-  // ---- merge: window warps, then every page piece of the (pair, head) segment; a thread per
-  //      channel ----------
-  // the page kernel's prefix and partials: wait for that grid (a no-op without a
-  // programmatic dependency)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (tid >= kD) return;
-  const int ch = tid;
-  float Mx = -INFINITY, Lt = 0.f, o = 0.f;
-  auto fold = [&](float Mp, float lp, float op) {
-    if (Mp == -INFINITY) return;
-    const float Mn = fmaxf(Mx, Mp);
-    const float f = (Mx == -INFINITY) ? 0.f : exp2f(Mx - Mn);
-    const float fp = exp2f(Mp - Mn);
-    Lt = Lt * f + lp * fp;
-    o = o * f + op * fp;
-    Mx = Mn;
-  };
-#pragma unroll
-  for (int w = 0; w < WT / 32; ++w) fold(wpart[w][kD], wpart[w][kD + 1], wpart[w][ch]);
-  const int n_pairs = (a.B + 1) / 2, pair = b >> 1, rr = b & 1;
-  const int p0 = a.pref[pair], nu = a.pref[pair + 1] - p0;
-  if (nu > 0) {
-    const int Up = a.pref[n_pairs];
-    const long long U = (long long)a.H * Up;
-    const long long s0 = (long long)h * Up + p0, s1 = s0 + nu;
-    const int k0 = share_of(s0, U, a.G), k1 = share_of(s1 - 1, U, a.G);
-    auto fold_piece = [&](const float* pp) {  // the 8 warp partials of this request
-      pp += rr * kVqWarpsPerReq * (kD + 2);
-#pragma unroll
-      for (int w = 0; w < kVqWarpsPerReq; ++w) fold(pp[w * (kD + 2)], pp[w * (kD + 2) + 1], pp[w * (kD + 2) + 2 + ch]);
-    };
-    if (k0 == k1) {
-      fold_piece(a.part_whole + ((size_t)h * n_pairs + pair) * kVqPartFloats);
-    } else {
-      for (int kk = k0; kk <= k1; ++kk) {
-        const long long lk = share_lo(U, kk, a.G);
-        if (lk == share_lo(U, kk + 1, a.G)) continue;  // an empty share
-        fold_piece(a.part_slot + ((size_t)kk * 2 + (lk >= s0 ? 0 : 1)) * kVqPartFloats);
-      }
-    }
-  }
-  const float val = (Lt > 0.f) ? o / Lt : 0.f;
-  const size_t oi = ((size_t)b * a.H + h) * kD + ch;
-  if (a.out_fp32) reinterpret_cast<float*>(a.out)[oi] = val;
-  else reinterpret_cast<uint16_t*>(a.out)[oi] = f32_to_bf16(val);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-int device_sms() {
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  return sms;
-}
-
 template <int NG>
-cudaError_t launch_pages(const VqAttnArgs& a, float scale_log2, cudaStream_t st) {
-  using Ly = PageLay<NG>;
-  cudaError_t e = cudaFuncSetAttribute(vq_pages_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kSmemBytes);
+cudaError_t launch(const VqAttnArgs& a, float scale_log2, cudaStream_t st) {
+  using Ly = Lay<NG>;
+  cudaError_t e = cudaFuncSetAttribute(vq_attn_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kSmemBytes);
   if (e != cudaSuccess) return e;
-  vq_pages_kernel<NG><<<a.G, kThreads, Ly::kSmemBytes, st>>>(a, scale_log2);
+  vq_attn_kernel<NG><<<a.G, kThreads, Ly::kSmemBytes, st>>>(a, scale_log2);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t vq_attn_ws_bytes(int B, int H, int G) {
-  const size_t n_pairs = (size_t)(B + 1) / 2;
-  return align256((n_pairs + 1) * sizeof(int32_t)) + align256((size_t)H * n_pairs * kVqPartFloats * sizeof(float)) +
-         align256((size_t)G * 2 * kVqPartFloats * sizeof(float));
+  return align256((size_t)B * H * sizeof(int32_t)) + align256((size_t)G * 2 * kVqSlotFloats * sizeof(float));
 }
-
-int vq_attn_max_pairs() { return kMaxPairs; }
 
 cudaError_t launch_vq_attn(const VqAttnArgs& args, void* ws, cudaStream_t st) {
   VqAttnArgs a = args;
-  const size_t n_pairs = (size_t)(a.B + 1) / 2;
   char* w = static_cast<char*>(ws);
-  a.pref = reinterpret_cast<int32_t*>(w);
-  w += align256((n_pairs + 1) * sizeof(int32_t));
-  a.part_whole = reinterpret_cast<float*>(w);
-  w += align256((size_t)a.H * n_pairs * kVqPartFloats * sizeof(float));
-  a.part_slot = reinterpret_cast<float*>(w);
+  a.cnt = reinterpret_cast<int32_t*>(w);
+  w += align256((size_t)a.B * a.H * sizeof(int32_t));
+  a.slots = reinterpret_cast<float*>(w);
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)kD);
-  cudaError_t e = cudaSuccess;
   switch (a.NG) {
-    case 16: e = launch_pages<16>(a, scale_log2, st); break;
-    case 8: e = launch_pages<8>(a, scale_log2, st); break;
-    case 32: e = launch_pages<32>(a, scale_log2, st); break;
+    case 16: return launch<16>(a, scale_log2, st);
+    case 8: return launch<8>(a, scale_log2, st);
+    case 32: return launch<32>(a, scale_log2, st);
     default: return cudaErrorInvalidValue;
   }
-  if (e != cudaSuccess) return e;
-  // programmatic dependent launch: the window kernel may start before the page kernel ends
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3((unsigned)(a.B * a.H));
-  const bool wide = a.B * a.H <= device_sms();
-  lc.blockDim = dim3(wide ? 512 : 128);
-  lc.dynamicSmemBytes = 0;
-  lc.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  return wide ? cudaLaunchKernelEx(&lc, vq_window_kernel<512>, a, scale_log2)
-              : cudaLaunchKernelEx(&lc, vq_window_kernel<128>, a, scale_log2);
 }
 
 }  // namespace kvq

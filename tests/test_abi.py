@@ -105,11 +105,10 @@ def test_workspace_size_and_split_plan(L):
     def a256(x):
         return (x + 255) // 256 * 256
 
-    # LoopVQ: unit prefix over the 32 request pairs, one piece per (pair, head) segment and
-    # two per page-kernel block, each piece 2 requests x 8 warps x (M, l, o[128]) floats
-    piece = 2 * 8 * 130 * 4
+    # LoopVQ: one merge counter per (request, head) segment, and two partial slots per block
+    # (the segments a block shares with its neighbours), each (M, l, 2 pad, o[128]) floats
     for blocks in (1, 4, 152):
-        want = a256(33 * 4) + a256(16 * 32 * piece) + a256(blocks * 2 * piece)
+        want = a256(64 * 16 * 4) + a256(blocks * 2 * 132 * 4)
         assert kvq.kvq_decode_workspace_size(c, 64, blocks) == want
     auto = kvq.kvq_decode_auto_splits(c, 64)
     assert auto >= 1

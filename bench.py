@@ -194,9 +194,27 @@ def _oracle_kivi_job(args):
     return time.perf_counter() - t0
 
 
+def cpu_oracle_single(wl, bytes_per_unit, n_pairs, pool=None):
+    """Time the oracle on ``n_pairs`` (request, head) units in one single-threaded process while
+    the other cores stay idle. Returns (GB/s, wall seconds)."""
+    if wl["kind"] == "loopvq":
+        job = (999, n_pairs, wl["L"], wl["T"], wl["Tc"], wl["G"], wl["recent"])
+        fn = _oracle_vq_job
+    else:
+        job = (999, n_pairs, wl["n_quant"], wl["n_resid"], wl.get("k_bits", 2), wl.get("v_bits", 2))
+        fn = _oracle_kivi_job
+    own = pool is None
+    if own:
+        pool = mp.get_context("spawn").Pool(1)
+    secs = pool.apply(fn, (job,))
+    if own:
+        pool.close()
+    return bytes_per_unit * n_pairs / secs / 1e9, secs
+
+
 def cpu_oracle(wl, bytes_per_unit, unit_pairs_total, n_pairs, pool=None):
-    """Time the oracle on ``n_pairs`` (request, head) units on all host cores.
-    Returns (GB/s, cores, wall seconds)."""
+    """Time the oracle on ``n_pairs`` (request, head) units on all host cores, one
+    single-threaded process per core. Returns (GB/s, cores, wall seconds)."""
     cores = os.cpu_count() or 1
     per = max(1, math.ceil(n_pairs / cores))
     jobs = []
@@ -530,9 +548,15 @@ def run_ours(args, wl, rank, world, dist, pool):
             n_pairs = 8 * B * H
             unit_bytes = call_bytes / (B * H)
             cgbs, cores, wall = cpu_oracle(wl, unit_bytes, B * H, n_pairs, pool)
+            n1 = 64 if wl["kind"] == "loopvq" else 32
+            sgbs, swall = cpu_oracle_single(wl, unit_bytes, n1, pool)
             result["cpu_baseline"] = {"value": round(cgbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                      "nproc": os.cpu_count(),
                                       "sample": f"{n_pairs} (request, head) units (8 calls' worth), fp64 NumPy "
-                                                f"oracle, {wall:.1f} s wall on {cores} processes"}
+                                                f"oracle, {wall:.1f} s wall on {cores} single-threaded processes",
+                                      "single_thread": {"value": round(sgbs, 5), "unit": "GB/s", "cores": 1,
+                                                        "sample": f"{n1} (request, head) units in one process, "
+                                                                  f"{swall:.1f} s"}}
         return result
 
     if wl["kind"] == "stream":
@@ -742,7 +766,9 @@ def run_reference(args, wl, pool):
     gbs = unit_bytes * n_pairs * args.steps / wall / 1e9
     return dict(value=round(gbs, 4), unit="GB/s", ms_per_step=round(wall / args.steps * 1e3, 3),
                 cpu_baseline={"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                              "sample": f"{n_pairs} (request, head) units of one call per step"},
+                              "nproc": os.cpu_count(),
+                              "sample": f"{n_pairs} (request, head) units of one call per step, one "
+                                        f"single-threaded process per core"},
                 e2e={"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                 gpu_launches=0)
 

@@ -7,7 +7,7 @@ the quantize / dequantize formula (section on per-token and per-channel quantiza
 the grouped + residual cache, eq. (3) and Algorithm 1 (core design section), the memory
 accounting, the configurable bit widths and GQA (implementation section).
 
-Readings where the page is silent (each listed in the design doc):
+Readings where the page is silent, taken here:
 * The scale splits [min, max] evenly: s = (max - min) / (2^b - 1); the zero-point is
   z = -min / s, kept as fp16 like the scale, so that X_hat = s * (q - z) is the printed
   dequantization. A group whose fp16 scale rounds to 0 (all values equal) uses s = 1.

@@ -7,7 +7,7 @@ Figure 5. Notation follows the page: T loop steps (1-based t), blocks of Tc cons
 steps (beta = block index), G coupled dimensions, c = G / Tc channels per codeword,
 NG = D / c index groups per token, head and block, K = 256 codebook entries.
 
-Readings where the page is silent or garbled (each listed in the design doc):
+Readings where the page is silent or garbled, taken here:
 * The coupled-vector map is printed as "channel g_{c+i}"; it is read as channel g*c + i.
 * Keys and values have separate codebooks and separate indices of the same structure.
 * Ties in the argmin go to the lowest index.

@@ -1,6 +1,8 @@
 """GPU parity of LoopVQ decode attention (kvq_decode_attn, format LoopVQ) against the fp64
 oracle, on the same seeded inputs. Tolerance: max-abs 2e-3 and relative L2 1e-3 on the
 fp32-output mode; the bf16 output must be the bf16 rounding of the fp32 result."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -9,6 +11,7 @@ from sub_bit_quantized_gb300 import kvq
 from tests import _cases as C
 
 pytestmark = pytest.mark.gpu
+D = 128
 
 
 def run_attn(case, cache, t, n_splits=0, out_dtype=torch.float32, ws=None):
@@ -150,3 +153,79 @@ def test_full_size_sampled(cfgname):
     check_all(case, cache, steps=steps, pairs=pairs)
     if cfgname == "b8_ctx32768_quarter_bit":
         check_all(case, cache, steps=(2,), n_splits=64, pairs=pairs[:3])
+
+
+def _oracle_encoded_pair(args):
+    """Oracle side of one (request, head) of the prefill-encoded full-size case: encode the
+    pages of each step's block from the same synthetic K/V, then decode attention (runs in a
+    spawned worker)."""
+    from oracle import loopvq as olv
+    xk, xv, cbk, cbv, q, L, npg, Tc, steps = args
+    qpos = np.arange(8, 8 + 8 * npg)
+    refs = []
+    for t in steps:
+        beta, _ = olv.step_to_block(t, Tc)
+        ik, _ = olv.encode_block(xk[:, qpos], cbk[beta], beta, Tc)
+        iv, _ = olv.encode_block(xv[:, qpos], cbv[beta], beta, Tc)
+        refs.append(olv.decode_attention(q, t, Tc, L, npg, ik, iv, cbk[beta], cbv[beta], xk[t - 1, :L], xv[t - 1, :L]))
+    return refs
+
+
+def test_full_size_prefill_encoded():
+    # batch 64, 16 heads, context 6144, 0.5 bit (Tc = 2) in the bench's launch configuration,
+    # on a cache filled by the library's own prefill encode (the index distribution the bench
+    # times); 8 requests of seeded loop-correlated K/V are generated and request b holds the
+    # data of request b % 8. 32 (request, head) pairs, one step of each loop block, are
+    # checked against the oracle, which encodes the same K/V itself (spawned worker pool).
+    import multiprocessing as mp
+
+    import synth
+    from oracle import loopvq as olv
+
+    B, H, L, T, Tc, G, NSRC = 64, 16, 6144, 4, 2, 16, 8
+    g = synth.rng(120)
+    rhos = synth.rho_schedule(T, 0.69, 0.94)
+    outl = [synth.outlier_channels(g, D, 4) for _ in range(H)]
+    xk = np.empty((NSRC, T, H, L, D), np.float32)
+    xv = np.empty_like(xk)
+    for r in range(NSRC):
+        for h in range(H):
+            xk[r, :, h] = synth.bf16_round(synth.scale_channels(synth.loop_correlated(g, T, L, D, rhos), outl[h], 15.0))
+            xv[r, :, h] = synth.bf16_round(synth.loop_correlated(g, T, L, D, rhos))
+    cbk = np.stack([synth.sample_codebooks(g, xk[:, :, h].transpose(1, 0, 2, 3).reshape(T, NSRC * L, D)[:, ::7], Tc, G)
+                    for h in range(H)], axis=1)
+    cbv = np.stack([synth.sample_codebooks(g, xv[:, :, h].transpose(1, 0, 2, 3).reshape(T, NSRC * L, D)[:, ::7], Tc, G)
+                    for h in range(H)], axis=1)
+    npg = olv.prefill_split(L)[1]
+    cfg = kvq.VqConfig(T=T, Tc=Tc, G=G, n_heads=H, max_pages=npg, max_batch=B, max_ctx=L + 8)
+    cache = kvq.VqCache(cfg)
+    C.load_codebooks(cache, cbk, cbv)
+    src = [(C.bf16_tensor(np.ascontiguousarray(xk[r][:, None])), C.bf16_tensor(np.ascontiguousarray(xv[r][:, None])))
+           for r in range(NSRC)]
+    for b in range(B):
+        kvq.kvq_prefill_vq(cfg, cache, 0, src[b % NSRC][0], src[b % NSRC][1], b, L)
+    del src
+    torch.cuda.synchronize()
+    assert kvq.device_error() == 0
+    assert cache.n_pages.tolist() == [npg] * B
+    q = synth.bf16_round(synth.gaussian(g, (B, H, D)))
+    rng = np.random.default_rng(8)
+    pairs = sorted({(int(b), int(h)) for b, h in zip(rng.integers(0, B, 64), rng.integers(0, H, 64))})[:30]
+    pairs += [(0, 0), (B - 1, H - 1)]
+    assert len(set(pairs)) >= 32
+    steps = (2, 3)  # blocks 0 and 1
+    outs = []
+    for t in steps:
+        out = torch.empty((B, H, D), dtype=torch.float32, device="cuda")
+        kvq.kvq_decode_attn(cfg, cache, 0, t, C.bf16_tensor(q), out)
+        torch.cuda.synchronize()
+        assert kvq.device_error() == 0
+        outs.append(out.cpu().numpy().astype(np.float64))
+    jobs = [(xk[b % NSRC, :, h].astype(np.float64), xv[b % NSRC, :, h].astype(np.float64), cbk[:, h], cbv[:, h],
+             q[b, h], L, npg, Tc, steps) for b, h in pairs]
+    with mp.get_context("spawn").Pool(min(16, os.cpu_count() or 1)) as pool:
+        refs = pool.map(_oracle_encoded_pair, jobs)
+    for k, t in enumerate(steps):
+        got = np.stack([outs[k][b, h] for b, h in pairs])
+        ref = np.stack([r[k] for r in refs])
+        C.check_close(got, ref)

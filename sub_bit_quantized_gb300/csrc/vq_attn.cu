@@ -506,6 +506,11 @@ __device__ void producer_role(const VqAttnArgs& a, unsigned char* smem, const Ba
       cur_h = W.h;
     }
     const size_t seg = ((size_t)W.b * a.H + W.h) * (size_t)a.max_pages;
+    if (W.pa == 0) {  // this block attends the segment's bf16 window (aux warps): HBM -> L2 now
+      const size_t wo = ((size_t)W.b * a.H + W.h) * a.win_slots * kD;
+      bulk_prefetch_l2(a.win_k + wo, (uint32_t)a.win_slots * kD * 2);
+      bulk_prefetch_l2(a.win_v + wo, (uint32_t)a.win_slots * kD * 2);
+    }
     for (int sa = W.pa; sa < W.pb; sa += kSubP) {
       const int sb = min(sa + kSubP, W.pb), nu = (sb - sa + Ly::kUP - 1) / Ly::kUP;
       const bool head_end = (sb == W.pb) && (!nx.valid || nx.h != W.h);
@@ -567,30 +572,42 @@ __device__ void aux_window(const VqAttnArgs& a, int h, int b, int L, int NP, flo
   const uint16_t* wk = a.win_k + bh * a.win_slots * kD;
   const uint16_t* wv = a.win_v + bh * a.win_slots * kD;
   float M = -INFINITY, l = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-  for (int w = aw; w < nwin; w += kAW) {
-    const int p = (w < nsink) ? w : a.sink + kPage * NP + (w - nsink);
-    const int slot = (p < a.sink) ? p : a.sink + (p - a.sink) % (a.recent + kPage);
-    const uint32_t ka = __ldg(reinterpret_cast<const uint32_t*>(wk + (size_t)slot * kD + 2 * lane));
-    const uint32_t kb = __ldg(reinterpret_cast<const uint32_t*>(wk + (size_t)slot * kD + 64 + 2 * lane));
-    const uint32_t va = __ldg(reinterpret_cast<const uint32_t*>(wv + (size_t)slot * kD + 2 * lane));
-    const uint32_t vb = __ldg(reinterpret_cast<const uint32_t*>(wv + (size_t)slot * kD + 64 + 2 * lane));
-    const int d = L - 1 - p;
-    const float2 c = __ldg(reinterpret_cast<const float2*>(a.rope_cos + (size_t)d * (kD / 2) + 2 * lane));
-    const float2 sn = __ldg(reinterpret_cast<const float2*>(a.rope_sin + (size_t)d * (kD / 2) + 2 * lane));
-    const float u0 = q0 * c.x - q2 * sn.x, u2 = q2 * c.x + q0 * sn.x;
-    const float u1 = q1 * c.y - q3 * sn.y, u3 = q3 * c.y + q1 * sn.y;
-    float dot = u0 * bf16_lo(ka) + u1 * bf16_hi(ka) + u2 * bf16_lo(kb) + u3 * bf16_hi(kb);
+  // two tokens per step (w, w + kAW), their loads issued together
+  constexpr int kTW = 2;
+  for (int w = aw; w < nwin; w += kTW * kAW) {
+    uint32_t ka[kTW], kb[kTW], va[kTW], vb[kTW];
+    float2 c[kTW], sn[kTW];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-    const float sc = dot * scale_log2;
-    if (sc > M) {
-      const float f = (M == -INFINITY) ? 0.f : exp2f(M - sc);
-      l *= f; o0 *= f; o1 *= f; o2 *= f; o3 *= f;
-      M = sc;
+    for (int e = 0; e < kTW; ++e) {
+      const int we = min(w + e * kAW, nwin - 1);  // a missing token reloads the last one
+      const int p = (we < nsink) ? we : a.sink + kPage * NP + (we - nsink);
+      const int slot = (p < a.sink) ? p : a.sink + (p - a.sink) % (a.recent + kPage);
+      ka[e] = __ldg(reinterpret_cast<const uint32_t*>(wk + (size_t)slot * kD + 2 * lane));
+      kb[e] = __ldg(reinterpret_cast<const uint32_t*>(wk + (size_t)slot * kD + 64 + 2 * lane));
+      va[e] = __ldg(reinterpret_cast<const uint32_t*>(wv + (size_t)slot * kD + 2 * lane));
+      vb[e] = __ldg(reinterpret_cast<const uint32_t*>(wv + (size_t)slot * kD + 64 + 2 * lane));
+      const int d = L - 1 - p;
+      c[e] = __ldg(reinterpret_cast<const float2*>(a.rope_cos + (size_t)d * (kD / 2) + 2 * lane));
+      sn[e] = __ldg(reinterpret_cast<const float2*>(a.rope_sin + (size_t)d * (kD / 2) + 2 * lane));
     }
-    const float pw = exp2f(sc - M);
-    l += pw;
-    o0 += pw * bf16_lo(va); o1 += pw * bf16_hi(va); o2 += pw * bf16_lo(vb); o3 += pw * bf16_hi(vb);
+#pragma unroll
+    for (int e = 0; e < kTW; ++e) {
+      if (w + e * kAW >= nwin) break;  // uniform across the warp
+      const float u0 = q0 * c[e].x - q2 * sn[e].x, u2 = q2 * c[e].x + q0 * sn[e].x;
+      const float u1 = q1 * c[e].y - q3 * sn[e].y, u3 = q3 * c[e].y + q1 * sn[e].y;
+      float dot = u0 * bf16_lo(ka[e]) + u1 * bf16_hi(ka[e]) + u2 * bf16_lo(kb[e]) + u3 * bf16_hi(kb[e]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
+      const float sc = dot * scale_log2;
+      if (sc > M) {
+        const float f = (M == -INFINITY) ? 0.f : exp2f(M - sc);
+        l *= f; o0 *= f; o1 *= f; o2 *= f; o3 *= f;
+        M = sc;
+      }
+      const float pw = exp2f(sc - M);
+      l += pw;
+      o0 += pw * bf16_lo(va[e]); o1 += pw * bf16_hi(va[e]); o2 += pw * bf16_lo(vb[e]); o3 += pw * bf16_hi(vb[e]);
+    }
   }
   float* mine = wp + aw * 132;
   mine[4 + 2 * lane] = o0; mine[5 + 2 * lane] = o1; mine[68 + 2 * lane] = o2; mine[69 + 2 * lane] = o3;

@@ -174,52 +174,299 @@ __device__ __forceinline__ void quant_value_row(const uint2 raw, uint8_t* codes,
   store_codes4<BITS>(codes, lane, c);
 }
 
-// keys: one warp per (b, h, 32-token group), grid-stride
+// ---------------------------------------------------------------- kvq_quantize_kivi
+// Persistent warps, each with a one-tile stage of shared memory (8 KB: 32 tokens x 128
+// channels of one (b, h)) filled by one bulk copy. A warp moves the tile into registers as
+// packed halves (lane l: channels 4l .. 4l + 3 of every row, 64 registers) and at once
+// issues the copy of its next tile into the stage, so the copy runs while it quantizes.
+// A warp takes a contiguous range of the tiles.
+constexpr int kQWarps = 16;
+constexpr int kQThreads = kQWarps * 32;
+constexpr int kQTileB = kGroup * kD * 2;
+constexpr int kQParB = 8 * 4 * 16;  // per warp: (rs, z16, threshold, s16) of 8 rows x 4 groups
+constexpr int kQOffPar = kQWarps * kQTileB;
+constexpr int kQOffBar = kQOffPar + kQWarps * kQParB;
+constexpr int kQSmem = kQOffBar + kQWarps * 8;
+static_assert(kQSmem <= 232448, "shared memory");
+
+// A group's quantization constants for the fast path. The per-value bound of quant_codes4,
+// 4 x 2^-23 (|x / s| + |t'|), is at most 4.8e-7 (2 M / s + |z|) for every x of a group whose
+// largest magnitude is M (|t'| <= |x| / s + |z|), so one threshold serves the whole group:
+// rint(t') is the reading's code when |t' - rint(t')| < 0.5 - that bound. A group with
+// infinite members gets a NaN or negative threshold and always takes the exact path; a NaN
+// member fails its own comparison.
+struct GroupF {
+  float rs, z, th, s;
+};
+__device__ __forceinline__ GroupF group_fast(const GroupQ& g, float mn, float mx) {
+  GroupF f;
+  f.rs = g.rs;
+  f.z = g.z16f;
+  f.s = g.s16f;
+  f.th = 0.5f - 4.8e-7f * (2.0f * fmaxf(fabsf(mn), fabsf(mx)) * g.rs + fabsf(g.z16f));
+  return f;
+}
+
+__device__ __forceinline__ __half2 u2h2(uint32_t w) { return *reinterpret_cast<const __half2*>(&w); }
+__device__ __forceinline__ uint32_t h22u(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
+
+// The codes of four values of (up to) four groups, packed as stored: code i in bits
+// [b i, b i + b). The packing runs in float arithmetic on small integers (exact) above 2^23,
+// whose low mantissa bits are then the packed codes.
+template <int BITS, bool kClamp>
+__device__ __forceinline__ uint32_t pack_codes4(const float (&k)[4]) {
+  constexpr float kMax = (float)((1 << BITS) - 1);
+  float c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = kClamp ? fminf(fmaxf(k[i], 0.0f), kMax) : k[i];
+  float acc = c[0] + 8388608.0f;
+#pragma unroll
+  for (int i = 1; i < 4; ++i) acc = __fmaf_rn(c[i], (float)(1 << (BITS * i)), acc);
+  return __float_as_uint(acc);
+}
+
+// Packed constants of a lane's four values: (rs, z, th) of channels (0, 1) and (2, 3).
+struct Quad {
+  float2 rs01, rs23, z01, z23, th01, th23;
+};
+
+// Fast codes of one row (four fp16 values): t' = fma(x, 1/s, z) and its rounding to nearest
+// even by adding and removing 1.5 * 2^23 (exact for |t'| < 2^22), two values per packed
+// operation; `bad` is set when a value lies too close to a rounding boundary (or is NaN, or
+// |t'| is too large for the rounding: the threshold is negative then). kClamp: the group's
+// extremes may round outside [0, 2^b - 1].
+template <int BITS, bool kClamp>
+__device__ __forceinline__ uint32_t row_codes_fast(const uint2 w, const Quad& q, bool& bad) {
+  const float2 x01 = __half22float2(u2h2(w.x)), x23 = __half22float2(u2h2(w.y));
+  const float2 M2 = make_float2(12582912.0f, 12582912.0f), nM2 = make_float2(-12582912.0f, -12582912.0f);
+  const float2 m1 = make_float2(-1.0f, -1.0f);
+  const float2 t01 = __ffma2_rn(x01, q.rs01, q.z01), t23 = __ffma2_rn(x23, q.rs23, q.z23);
+  const float2 k01 = __fadd2_rn(__fadd2_rn(t01, M2), nM2), k23 = __fadd2_rn(__fadd2_rn(t23, M2), nM2);
+  const float2 d01 = __ffma2_rn(k01, m1, t01), d23 = __ffma2_rn(k23, m1, t23);
+  bad = !(fabsf(d01.x) < q.th01.x) || !(fabsf(d01.y) < q.th01.y) || !(fabsf(d23.x) < q.th23.x) ||
+        !(fabsf(d23.y) < q.th23.y);
+  const float k[4] = {k01.x, k01.y, k23.x, k23.y};
+  return pack_codes4<BITS, kClamp>(k);
+}
+
+// The reading's sequence for one row: rint(x / s + z), clamped
 template <int BITS>
-__global__ void __launch_bounds__(256) kivi_quant_channel_kernel(const KiviQuantArgs a) {
+__device__ __forceinline__ uint32_t row_codes_exact(const uint2 w, const GroupF (&g)[4]) {
+  float x[4], k[4];
+  unpack4(w, x);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) k[i] = rintf(__fadd_rn(__fdiv_rn(x[i], g[i].s), g[i].z));
+  return pack_codes4<BITS, true>(k);
+}
+
+// true when every x of the group [mn, mx] has a fast-path code inside [0, 2^b - 1]: t' and
+// its rounding are monotone in x, so the extremes decide
+template <int BITS>
+__device__ __forceinline__ bool group_in_range(const GroupF& f, float mn, float mx) {
+  const float lo = rintf(__fmaf_rn(mn, f.rs, f.z)), hi = rintf(__fmaf_rn(mx, f.rs, f.z));
+  return lo >= 0.0f && hi <= (float)((1 << BITS) - 1);
+}
+
+template <int BITS>
+__device__ __forceinline__ void store_packed4(uint8_t* row, int lane, uint32_t packed) {
+  if constexpr (BITS == 2) row[lane] = (uint8_t)packed;
+  else *reinterpret_cast<uint16_t*>(row + 2 * lane) = (uint16_t)packed;
+}
+
+
+// keys of one tile (held as t[row] = the lane's 4 fp16 channels): one 32-token group per
+// channel. Minimum and maximum on packed halves (exact: the order of fp16 values is that of
+// their fp32 conversions), then the codes.
+template <int BITS>
+__device__ __forceinline__ void quant_key_tile(const uint2 (&t)[kGroup], const uint16_t* gsrc, uint8_t* codes,
+                                               uint16_t* scale, uint16_t* zero, int lane) {
   constexpr int kRow = kD * BITS / 8;
-  const int lane = threadIdx.x & 31;
-  const int n_groups = a.n_tok / kGroup;
-  const long long total = (long long)a.B * a.H * n_groups;
-  for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; w < total;
-       w += ((long long)gridDim.x * blockDim.x) >> 5) {
-    const int gi = (int)(w % n_groups);
-    const long long q = w / n_groups;
-    const int h = (int)(q % a.H);
-    const int b = (int)(q / a.H);
-    const size_t bh = (size_t)b * a.H + h;
-    const size_t sz = (bh * (a.max_tokens / kGroup) + a.tok_begin / kGroup + gi) * kD;
-    quant_key_group<BITS, true>(a.x + (size_t)b * a.sb + (size_t)h * a.sh + (size_t)gi * kGroup * kD, kD,
-                                a.codes + (bh * a.max_tokens + a.tok_begin + (size_t)gi * kGroup) * kRow,
-                                a.scale + sz, a.zero + sz, lane);
+  __half2 mn0 = u2h2(t[0].x), mn1 = u2h2(t[0].y), mx0 = mn0, mx1 = mn1;
+#pragma unroll
+  for (int j = 1; j < kGroup; ++j) {
+    mn0 = __hmin2(mn0, u2h2(t[j].x));
+    mn1 = __hmin2(mn1, u2h2(t[j].y));
+    mx0 = __hmax2(mx0, u2h2(t[j].x));
+    mx1 = __hmax2(mx1, u2h2(t[j].y));
+  }
+  const float2 a0 = __half22float2(mn0), a1 = __half22float2(mn1), b0 = __half22float2(mx0), b1 = __half22float2(mx1);
+  const float mn[4] = {a0.x, a0.y, a1.x, a1.y}, mx[4] = {b0.x, b0.y, b1.x, b1.y};
+  GroupF f[4];
+  uint32_t sb[4], zb[4];
+  bool in_range = true;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const GroupQ g = group_params<BITS>(mn[i], mx[i]);
+    f[i] = group_fast(g, mn[i], mx[i]);
+    in_range = in_range && group_in_range<BITS>(f[i], mn[i], mx[i]);
+    sb[i] = g.s_bits;
+    zb[i] = g.z_bits;
+  }
+  *reinterpret_cast<uint2*>(scale + 4 * lane) = make_uint2(sb[0] | (sb[1] << 16), sb[2] | (sb[3] << 16));
+  *reinterpret_cast<uint2*>(zero + 4 * lane) = make_uint2(zb[0] | (zb[1] << 16), zb[2] | (zb[3] << 16));
+  const Quad q = {make_float2(f[0].rs, f[1].rs), make_float2(f[2].rs, f[3].rs), make_float2(f[0].z, f[1].z),
+                  make_float2(f[2].z, f[3].z),   make_float2(f[0].th, f[1].th), make_float2(f[2].th, f[3].th)};
+  uint32_t badrows = 0;
+  if (__all_sync(0xFFFFFFFFu, in_range)) {
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      bool bad;
+      store_packed4<BITS>(codes + (size_t)j * kRow, lane, row_codes_fast<BITS, false>(t[j], q, bad));
+      badrows |= (uint32_t)bad << j;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      bool bad;
+      store_packed4<BITS>(codes + (size_t)j * kRow, lane, row_codes_fast<BITS, true>(t[j], q, bad));
+      badrows |= (uint32_t)bad << j;
+    }
+  }
+  while (badrows) {  // rare: rows with a value near a rounding boundary, re-read from HBM
+    const int j = __ffs(badrows) - 1;
+    badrows &= badrows - 1;
+    store_packed4<BITS>(codes + (size_t)j * kRow, lane,
+                        row_codes_exact<BITS>(__ldg(reinterpret_cast<const uint2*>(gsrc + (size_t)j * kD + 4 * lane)), f));
   }
 }
 
-// values: a warp covers one 256-byte token row per step, 8 consecutive rows of one
-// (b, h) loaded per step (one index division per 8 rows)
-template <int BITS>
-__global__ void __launch_bounds__(256) kivi_quant_token_kernel(const KiviQuantArgs a) {
-  constexpr int kRows = 8;
+// fast codes of rows r0 .. r0 + 7 of a value tile (constants of row k, group grp at
+// par[4 k + grp]); returns the rows (bit k) with a value near a rounding boundary
+template <int BITS, bool kClamp>
+__device__ __forceinline__ uint32_t value_rows8(const uint2 (&t)[kGroup], const int r0, const int rows,
+                                                uint8_t* codes, const float4* par, const int grp, const int lane) {
   constexpr int kRow = kD * BITS / 8;
-  const int lane = threadIdx.x & 31;
-  const int per_bh = (a.n_tok + kRows - 1) / kRows;  // row blocks of one (b, h)
-  const long long n_steps = (long long)a.B * a.H * per_bh;
-  for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; w < n_steps;
-       w += ((long long)gridDim.x * blockDim.x) >> 5) {
-    const long long bh = w / per_bh;  // b * H + h
-    const int j0 = (int)(w - bh * per_bh) * kRows;
-    const int h = (int)(bh % a.H), b = (int)(bh / a.H);
-    const int nr = min(kRows, a.n_tok - j0);
-    const uint16_t* src = a.x + (size_t)b * a.sb + (size_t)h * a.sh + (size_t)j0 * kD + 4 * lane;
-    const size_t tok0 = (size_t)bh * a.max_tokens + a.tok_begin + j0;
-    uint2 raw[kRows];
+  uint32_t badrows = 0;
 #pragma unroll
-    for (int u = 0; u < kRows; ++u) raw[u] = __ldg(reinterpret_cast<const uint2*>(src + (size_t)min(u, nr - 1) * kD));
+  for (int k = 0; k < 8; ++k) {
+    const float4 p = par[k * 4 + grp];
+    const Quad q = {make_float2(p.x, p.x), make_float2(p.x, p.x), make_float2(p.y, p.y),
+                    make_float2(p.y, p.y), make_float2(p.z, p.z), make_float2(p.z, p.z)};
+    bool bad;
+    const uint32_t c = row_codes_fast<BITS, kClamp>(t[r0 + k], q, bad);
+    if (r0 + k < rows) {
+      store_packed4<BITS>(codes + (size_t)(r0 + k) * kRow, lane, c);
+      badrows |= (uint32_t)bad << k;
+    }
+  }
+  return badrows;
+}
+
+// values of one tile (rows < 32 valid), 8 rows at a time: lane l holds channels 4l .. 4l + 3
+// of each row, i.e. group l / 8. Each row's (min, -max) over the lane's 4 channels is one
+// packed half pair; a transposing reduction over the 8 lanes of a group leaves lane 8g + k
+// with row k's extremes of group g. That lane computes the group's constants once, writes
+// its scale and zero-point, and posts the constants for the other lanes in shared memory.
+template <int BITS>
+__device__ __forceinline__ void quant_value_tile(const uint2 (&t)[kGroup], const uint16_t* gsrc, int rows,
+                                                 uint8_t* codes, uint16_t* scale, uint16_t* zero, float4* par,
+                                                 int lane) {
+  constexpr int kRow = kD * BITS / 8;
+  const int kk = lane & 7, grp = lane >> 3;
 #pragma unroll
-    for (int u = 0; u < kRows; ++u) {
-      if (u >= nr) break;  // uniform across the warp
-      quant_value_row<BITS>(raw[u], a.codes + (tok0 + u) * kRow, a.scale + (tok0 + u) * (kD / kGroup),
-                            a.zero + (tok0 + u) * (kD / kGroup), lane);
+  for (int r0 = 0; r0 < kGroup; r0 += 8) {
+    if (r0 >= rows) break;  // uniform across the warp
+    uint32_t e[8];  // (min, -max) of row r0 + k over the lane's channels
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const __half2 m = __hmin2(u2h2(t[r0 + k].x), u2h2(t[r0 + k].y));
+      const uint32_t nM = h22u(__hmax2(u2h2(t[r0 + k].x), u2h2(t[r0 + k].y))) ^ 0x80008000u;
+      const uint32_t um = h22u(m);
+      e[k] = h22u(__hmin2(u2h2(__byte_perm(um, nM, 0x5410)), u2h2(__byte_perm(um, nM, 0x7632))));
+    }
+#pragma unroll
+    for (int w = 4; w >= 1; w >>= 1) {
+      const bool up = (lane & w) != 0;
+#pragma unroll
+      for (int k = 0; k < w; ++k) {
+        const uint32_t send = up ? e[k] : e[k + w], keep = up ? e[k + w] : e[k];
+        e[k] = h22u(__hmin2(u2h2(keep), u2h2(__shfl_xor_sync(0xFFFFFFFFu, send, w))));
+      }
+    }
+    const float2 ex = __half22float2(u2h2(e[0]));
+    const float mn = ex.x, mx = -ex.y;
+    const GroupQ g = group_params<BITS>(mn, mx);
+    const GroupF f = group_fast(g, mn, mx);
+    const bool in_range = group_in_range<BITS>(f, mn, mx) || r0 + kk >= rows;
+    if (r0 + kk < rows) {  // lane 8 grp + kk: row r0 + kk, group grp
+      scale[(size_t)(r0 + kk) * (kD / kGroup) + grp] = g.s_bits;
+      zero[(size_t)(r0 + kk) * (kD / kGroup) + grp] = g.z_bits;
+    }
+    par[kk * 4 + grp] = make_float4(f.rs, f.z, f.th, f.s);
+    __syncwarp();
+    uint32_t badrows;
+    if (__all_sync(0xFFFFFFFFu, in_range))
+      badrows = value_rows8<BITS, false>(t, r0, rows, codes, par, grp, lane);
+    else
+      badrows = value_rows8<BITS, true>(t, r0, rows, codes, par, grp, lane);
+    while (badrows) {  // rare: rows with a value near a rounding boundary, re-read from HBM
+      const int k = __ffs(badrows) - 1;
+      badrows &= badrows - 1;
+      const float4 p = par[k * 4 + grp];
+      const GroupF gk = {p.x, p.y, p.z, p.w};
+      const GroupF gg[4] = {gk, gk, gk, gk};
+      store_packed4<BITS>(codes + (size_t)(r0 + k) * kRow, lane,
+                          row_codes_exact<BITS>(__ldg(reinterpret_cast<const uint2*>(gsrc + (size_t)(r0 + k) * kD + 4 * lane)), gg));
+    }
+    __syncwarp();  // before the constants are overwritten
+  }
+}
+
+template <int BITS, bool kKeys>
+__global__ void __launch_bounds__(kQThreads, 1) kivi_quant_kernel(const KiviQuantArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int kRow = kD * BITS / 8;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned char* stage = smem + warp * kQTileB;
+  float4* par = reinterpret_cast<float4*>(smem + kQOffPar + warp * kQParB);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kQOffBar) + warp;
+  const int n_gi = (a.n_tok + kGroup - 1) / kGroup;
+  const long long T = (long long)a.B * a.H * n_gi;
+  const long long W = (long long)gridDim.x * kQWarps, gw = (long long)blockIdx.x * kQWarps + warp;
+  const long long t0 = T * gw / W, t1 = T * (gw + 1) / W;
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  auto tile_rows = [&](long long t) { return min(kGroup, a.n_tok - (int)(t % n_gi) * kGroup); };
+  auto issue = [&](long long t) {  // lane 0: tile t into the stage
+    const long long bh = t / n_gi;
+    const int gi = (int)(t - bh * n_gi), b = (int)(bh / a.H), h = (int)(bh - (long long)b * a.H);
+    const uint16_t* src = a.x + (size_t)b * a.sb + (size_t)h * a.sh + (size_t)gi * kGroup * kD;
+    const uint32_t bytes = (uint32_t)tile_rows(t) * kD * 2;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(stage, src, bytes, bar);
+  };
+  if (lane == 0 && t0 < t1) issue(t0);
+  for (long long t = t0; t < t1; ++t) {
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar, (uint32_t)((t - t0) & 1)))) {
+      // the copy did not land in time: record it, let it land (bounded) and leave
+      if (lane == 0) {
+        set_error(a.err, KVQ_ERR_TIMEOUT);
+        mbar_wait_bounded(bar, (uint32_t)((t - t0) & 1));
+      }
+      __syncwarp();
+      return;
+    }
+    uint2 tl[kGroup];
+    const uint16_t* tp = reinterpret_cast<const uint16_t*>(stage) + 4 * lane;
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) tl[j] = *reinterpret_cast<const uint2*>(tp + j * kD);
+    const int rows = tile_rows(t);
+    __syncwarp();  // every lane has its rows: the stage takes the next tile
+    if (lane == 0 && t + 1 < t1) issue(t + 1);
+    const long long bh = t / n_gi;
+    const int gi = (int)(t - bh * n_gi), b = (int)(bh / a.H), h = (int)(bh - (long long)b * a.H);
+    const uint16_t* gsrc = a.x + (size_t)b * a.sb + (size_t)h * a.sh + (size_t)gi * kGroup * kD;
+    const size_t tok = (size_t)bh * a.max_tokens + a.tok_begin + (size_t)gi * kGroup;
+    if constexpr (kKeys) {
+      const size_t sz = ((size_t)bh * (a.max_tokens / kGroup) + a.tok_begin / kGroup + gi) * kD;
+      quant_key_tile<BITS>(tl, gsrc, a.codes + tok * kRow, a.scale + sz, a.zero + sz, lane);
+    } else {
+      quant_value_tile<BITS>(tl, gsrc, rows, a.codes + tok * kRow, a.scale + tok * (kD / kGroup),
+                             a.zero + tok * (kD / kGroup), par, lane);
     }
   }
 }
@@ -978,22 +1225,22 @@ int kivi_attn_blocks_per_sm(int k_bits, int v_bits, int rh) {
   return c;
 }
 
-cudaError_t launch_kivi_quantize(const KiviQuantArgs& a, cudaStream_t s) {
-  // grid-stride warps; 8 blocks of 256 threads per SM keep enough rows in flight
-  const long long warps = (a.axis == KVQ_PER_CHANNEL) ? (long long)a.B * a.H * (a.n_tok / a.group)
-                                                      : (long long)a.B * a.H * ((a.n_tok + 7) / 8);
-  if (warps <= 0) return cudaSuccess;
-  long long blocks = (warps + 7) / 8;
-  const int sms = sm_count_cached();
-  if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
-  if (a.axis == KVQ_PER_CHANNEL) {
-    if (a.bits == 4) kivi_quant_channel_kernel<4><<<(int)blocks, 256, 0, s>>>(a);
-    else kivi_quant_channel_kernel<2><<<(int)blocks, 256, 0, s>>>(a);
-  } else {
-    if (a.bits == 4) kivi_quant_token_kernel<4><<<(int)blocks, 256, 0, s>>>(a);
-    else kivi_quant_token_kernel<2><<<(int)blocks, 256, 0, s>>>(a);
-  }
+template <int BITS, bool kKeys>
+cudaError_t launch_quant(const KiviQuantArgs& a, int blocks, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kivi_quant_kernel<BITS, kKeys>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+  if (e != cudaSuccess) return e;
+  kivi_quant_kernel<BITS, kKeys><<<blocks, kQThreads, kQSmem, s>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_kivi_quantize(const KiviQuantArgs& a, cudaStream_t s) {
+  // one block of kQWarps persistent warps per SM, fewer when there are few tiles
+  const long long tiles = (long long)a.B * a.H * ((a.n_tok + kGroup - 1) / kGroup);
+  if (tiles <= 0) return cudaSuccess;
+  const int blocks = (int)std::min<long long>(sm_count_cached(), (tiles + kQWarps - 1) / kQWarps);
+  const bool keys = (a.axis == KVQ_PER_CHANNEL);
+  if (a.bits == 4) return keys ? launch_quant<4, true>(a, blocks, s) : launch_quant<4, false>(a, blocks, s);
+  return keys ? launch_quant<2, true>(a, blocks, s) : launch_quant<2, false>(a, blocks, s);
 }
 
 cudaError_t launch_kivi_prefill_tail(const KiviTailArgs& a, cudaStream_t s) {

@@ -398,7 +398,7 @@ KVQ_API kvq_status kvq_quantize_kivi(const kvq_kivi_cfg* c, int axis, const uint
   a.x = x; a.sb = st_b; a.sh = st_h; a.codes = codes; a.scale = scale; a.zero = zero;
   a.axis = axis; a.bits = (axis == KVQ_PER_CHANNEL) ? c->k_bits : c->v_bits;
   a.B = B; a.H = c->n_heads; a.n_tok = n_tok; a.tok_begin = tok_begin;
-  a.max_tokens = c->max_tokens; a.group = c->group;
+  a.max_tokens = c->max_tokens; a.group = c->group; a.err = device_error_ptr();
   return cuda_status(kvq::launch_kivi_quantize(a, (cudaStream_t)stream), __func__);
 }
 
@@ -423,7 +423,7 @@ KVQ_API kvq_status kvq_kivi_prefill(const kvq_kivi_cfg* c, const kvq_kivi_cache*
   if (nq > 0) {
     kvq::KiviQuantArgs a{};
     a.sb = st_b; a.sh = st_h; a.B = B; a.H = c->n_heads; a.n_tok = nq; a.tok_begin = 0;
-    a.max_tokens = c->max_tokens; a.group = G;
+    a.max_tokens = c->max_tokens; a.group = G; a.err = device_error_ptr();
     a.x = xk; a.axis = KVQ_PER_CHANNEL; a.bits = c->k_bits;
     a.codes = k->k_codes + (size_t)b0 * H * N * (D * c->k_bits / 8);
     a.scale = k->k_scale + (size_t)b0 * H * (N / G) * D;

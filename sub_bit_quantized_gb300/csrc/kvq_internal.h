@@ -124,6 +124,7 @@ struct KiviQuantArgs {
   int64_t sb, sh;
   uint8_t* codes; uint16_t* scale; uint16_t* zero;
   int axis, bits, B, H, n_tok, tok_begin, max_tokens, group;
+  int* err;  // device error word (a bounded wait that timed out)
 };
 cudaError_t launch_kivi_quantize(const KiviQuantArgs& a, cudaStream_t s);
 

@@ -103,6 +103,12 @@ typedef struct {
  *     Per-loop-step value codebook slices, cut once by kvq_slice_codebooks_fp16 and
  *     rounded to fp16 (nearest even): bt_v[l][t][h][r][ch] = fp16(cb[l][beta][h][g][r][i*Tc + m]).
  * cb_k, cb_v    fp32   [n_layers][NB][n_heads][NG][K][G]   full codebooks (encode, roll)
+ * cbp_k, cbp_v  bytes  [n_layers][NB][n_heads][NG][3 parts][K rows x KC 16-byte chunks]
+ *     Optional (may be NULL): each codebook split into three bf16 parts hi + mid + lo (hi =
+ *     bf16(e), mid = bf16(e - hi), lo = bf16(e - hi - mid), round to nearest even) with the
+ *     -|e|^2/2 column appended, in the tensor cores' operand layout (kvq_split_codebooks).
+ *     With both set, the page roll of kvq_append_page runs on the tensor cores; with either
+ *     NULL it runs on CUDA cores (same decisions).
  * rope_cos, rope_sin fp32 [max_ctx][D/2]: cos / sin(p * base^(-2i/D)) (kvq_rope_table)
  * seq_len       int32  [max_batch]: tokens cached per request, including the newest one
  *                      (the query position is seq_len - 1)
@@ -121,13 +127,16 @@ typedef struct {
   const float* rope_sin;
   int32_t* seq_len;
   int32_t* n_pages;
+  uint8_t* cbp_k;
+  uint8_t* cbp_v;
 } kvq_vq_cache;
 
 /* Byte sizes of each buffer of kvq_vq_cache for `cfg` (host-only, no device work).
  * Order: idx (each of k, v), win (each), bt (bt_k), bt_v, cb (each), rope (each of cos,
- * sin), per-request int32 arrays (each). Returns KVQ_ERR_INVALID_ARG for an invalid cfg. */
+ * sin), per-request int32 arrays (each), cbp (each of cbp_k, cbp_v). Returns
+ * KVQ_ERR_INVALID_ARG for an invalid cfg. */
 typedef struct {
-  size_t idx, win, bt, bt_v, cb, rope, per_request;
+  size_t idx, win, bt, bt_v, cb, rope, per_request, cbp;
 } kvq_vq_sizes;
 kvq_status kvq_vq_cache_sizes(const kvq_vq_cfg* cfg, kvq_vq_sizes* out /* host */);
 
@@ -149,6 +158,13 @@ kvq_status kvq_slice_codebooks(const kvq_vq_cfg* cfg, const float* cb, float* bt
  * (relative 2^-11 per entry) is far inside the attention output tolerance. */
 kvq_status kvq_slice_codebooks_fp16(const kvq_vq_cfg* cfg, const float* cb, uint16_t* bt16,
                                     kvq_stream stream);
+
+/* Split every codebook of cb ([n_layers][NB][n_heads][NG][K][G] fp32) into the three bf16
+ * parts the tensor-core encode multiplies (layout of cbp_k in kvq_vq_cache), once at load
+ * time, for the page roll (LoopVQ method step 4: the oldest recent page is encoded during
+ * decode; each roll reads every codebook, so the split is not redone per roll). The parts sum
+ * back to the fp32 entries exactly. Errors: KVQ_ERR_INVALID_ARG (cfg, pointers). */
+kvq_status kvq_split_codebooks(const kvq_vq_cfg* cfg, const float* cb, uint8_t* cbp, kvq_stream stream);
 
 /* Nearest-codeword encode of coupled vectors (LoopVQ background: a(z) = argmin_r
  * ||z - e_r||^2; method step 1 for the coupling, method step 4 for prefill encoding).

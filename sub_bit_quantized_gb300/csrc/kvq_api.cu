@@ -220,6 +220,7 @@ KVQ_API kvq_status kvq_vq_cache_sizes(const kvq_vq_cfg* c, kvq_vq_sizes* out) {
   out->cb = (size_t)c->n_layers * NB * c->n_heads * NG * c->K * c->G * 4;
   out->rope = (size_t)c->max_ctx * (c->D / 2) * 4;
   out->per_request = (size_t)c->max_batch * 4;
+  out->cbp = (size_t)c->n_layers * NB * c->n_heads * NG * kvq::split_codebook_bytes(c->G);
   return KVQ_OK;
 }
 
@@ -251,6 +252,15 @@ KVQ_API kvq_status kvq_slice_codebooks_fp16(const kvq_vq_cfg* c, const float* cb
   return cuda_status(kvq::launch_slice_codebooks_fp16(cb, bt16, c->n_layers, c->T, c->Tc, c->G, c->n_heads,
                                                       (cudaStream_t)stream),
                      __func__);
+}
+
+KVQ_API kvq_status kvq_split_codebooks(const kvq_vq_cfg* c, const float* cb, uint8_t* cbp, kvq_stream stream) {
+  kvq_status st = check_vq_cfg(c, __func__);
+  if (st != KVQ_OK) return st;
+  CHECK_PTR(cb);
+  CHECK_PTR(cbp);
+  const long long n = (long long)c->n_layers * (c->T / c->Tc) * c->n_heads * (c->D / (c->G / c->Tc));
+  return cuda_status(kvq::launch_split_codebooks(cb, cbp, n, c->Tc, c->G, (cudaStream_t)stream), __func__);
 }
 
 static kvq_status check_x_strides(const char* fn, int64_t st, int64_t sb, int64_t sh) {
@@ -292,6 +302,8 @@ static kvq_status check_vq_cache(const kvq_vq_cache* k, const char* fn) {
                         k->cb_k, k->cb_v, k->rope_cos, k->rope_sin, k->seq_len, k->n_pages};
   for (const void* p : ptrs)
     if (!aligned16(p)) return fail(KVQ_ERR_INVALID_ARG, "%s: a cache pointer is null or not 16-byte aligned", fn);
+  for (const void* p : {static_cast<const void*>(k->cbp_k), static_cast<const void*>(k->cbp_v)})
+    if (p && !aligned16(p)) return fail(KVQ_ERR_INVALID_ARG, "%s: cbp_k / cbp_v not 16-byte aligned", fn);
   return KVQ_OK;
 }
 
@@ -368,6 +380,7 @@ KVQ_API kvq_status kvq_append_page(const kvq_vq_cfg* c, const kvq_vq_cache* k, i
   kvq::VqRollArgs r{};
   r.win_k = k->win_k; r.win_v = k->win_v; r.cb_k = k->cb_k; r.cb_v = k->cb_v;
   r.idx_k = k->idx_k; r.idx_v = k->idx_v; r.seq_len = k->seq_len; r.n_pages = k->n_pages;
+  r.cbp_k = k->cbp_k; r.cbp_v = k->cbp_v;
   r.err = device_error_ptr();
   r.L = c->n_layers; r.T = c->T; r.Tc = c->Tc; r.G = c->G; r.NB = c->T / c->Tc; r.H = c->n_heads;
   r.n_seq = n_seq; r.max_batch = c->max_batch; r.max_pages = c->max_pages; r.win_slots = win_slots(c);

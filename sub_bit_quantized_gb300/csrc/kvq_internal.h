@@ -79,6 +79,17 @@ struct VqEncodeArgs {
   int* err;
   int T, Tc, G, NB, H, max_batch, max_pages;
   int seq_begin, n_seq, n_tok, page_begin, g_begin, g_count;
+  // Page roll (launch_vq_roll_tc): the planes' sequence index is (layer, K/V) = 2 layer + kv,
+  // the rows of a plane are (request b, token j of b's oldest recent page) = 8 b + j, read
+  // from the bf16 windows (x: win_k of layer 0, x2: win_v; st, sb, sh: loop-step, request and
+  // head strides, rows at slot * D) and written to page n_pages[b] of the requests that are
+  // due (idx: idx_k of layer 0, idx2: idx_v); codebook parts from cbp (K) and cbp2 (V);
+  // n_tok = 8 n_req.
+  const uint16_t* x2; uint8_t* idx2;
+  const uint8_t* cbp; const uint8_t* cbp2;
+  int64_t x_layer, cbp_layer, idx_layer;  // per-layer strides: elements, bytes, bytes
+  const int32_t* seq_len; const int32_t* n_pages;
+  int sink, recent, n_req;
 };
 cudaError_t launch_vq_encode(const VqEncodeArgs& a, cudaStream_t s);
 
@@ -113,10 +124,17 @@ struct VqRollArgs {                // encode the oldest recent page where the ri
   const float* cb_k; const float* cb_v;           // [L][NB][H][NG][256][G]
   uint8_t* idx_k; uint8_t* idx_v;                 // [L][NB][max_batch][H][max_pages][128]
   int32_t* seq_len; int32_t* n_pages;
+  const uint8_t* cbp_k; const uint8_t* cbp_v;     // split codebook parts (null: CUDA-core roll)
   int* err;
   int L, T, Tc, G, NB, H, n_seq, max_batch, max_pages, win_slots, sink, recent;
 };
 cudaError_t launch_vq_roll(const VqRollArgs& a, cudaStream_t s);
+// the roll's encode on the tensor cores (needs the split codebook parts)
+cudaError_t launch_vq_roll_tc(const VqEncodeArgs& a, cudaStream_t s);
+// three bf16 parts of every [256][G] codebook of cb (n codebooks) in the tensor-core operand
+// layout; bytes per codebook from split_codebook_bytes
+cudaError_t launch_split_codebooks(const float* cb, uint8_t* cbp, long long n, int Tc, int G, cudaStream_t s);
+size_t split_codebook_bytes(int G);
 
 // ---------------------------------------------------------------- KIVI
 struct KiviQuantArgs {

@@ -9,10 +9,11 @@
 //    8-token index pages; during decode the oldest recent page is encoded every 8 tokens;
 //  * method step 5: the per-loop-step codebook slice B_t is cut once at load time.
 //
-// Roll encode arithmetic (one page of 8 tokens per (layer, block, head), on CUDA cores): the
-// same decision rule as the prefill encode: fp32 screening of z.e - |e|^2 / 2, and every vector
-// whose runner-up is inside the error band is decided on distances summed with error-free
-// fp32 steps; the lowest index wins exact ties.
+// Roll encode: with the split codebook parts in the cache it runs on the tensor cores (the
+// prefill encode kernel's roll instantiation, vq_encode_tc.cu); without them on CUDA cores
+// (roll_kernel below) with the same decision rule: fp32 screening of z.e - |e|^2 / 2, every
+// vector whose runner-up is inside the error band decided on distances summed with
+// error-free fp32 steps, the lowest index winning exact ties.
 #include <cuda_fp16.h>
 
 #include "kvq_common.cuh"
@@ -345,6 +346,30 @@ cudaError_t launch_vq_append(const VqAppendArgs& a, cudaStream_t s) {
 
 cudaError_t launch_vq_roll(const VqRollArgs& a, cudaStream_t s) {
   const int C = a.G / a.Tc;
+  if (a.cbp_k && a.cbp_v) {
+    // on the tensor cores: every (layer, K/V, beta, head, group) codebook against the oldest
+    // recent page of every due request, the (request, token) rows of one plane sharing it
+    const int NG = kD / C;
+    const int64_t st = (int64_t)a.max_batch * a.H * a.win_slots * kD;  // loop-step stride of a window
+    VqEncodeArgs e{};
+    e.x = a.win_k; e.x2 = a.win_v;
+    e.cb = a.cb_k;
+    e.cbp = a.cbp_k; e.cbp2 = a.cbp_v;
+    e.idx = a.idx_k; e.idx2 = a.idx_v;
+    e.st = st; e.sb = (int64_t)a.H * a.win_slots * kD; e.sh = (int64_t)a.win_slots * kD;
+    e.x_layer = (int64_t)a.T * st;
+    e.cbp_layer = (int64_t)a.NB * a.H * NG * (int64_t)split_codebook_bytes(a.G);
+    e.idx_layer = (int64_t)a.NB * a.max_batch * a.H * a.max_pages * kPage * NG;
+    e.seq_len = a.seq_len; e.n_pages = a.n_pages;
+    e.sink = a.sink; e.recent = a.recent; e.n_req = a.n_seq;
+    e.n_ties = nullptr; e.err = a.err;
+    e.T = a.T; e.Tc = a.Tc; e.G = a.G; e.NB = a.NB; e.H = a.H; e.max_batch = a.max_batch; e.max_pages = a.max_pages;
+    e.seq_begin = 0; e.n_seq = 2 * a.L; e.n_tok = kPage * a.n_seq; e.page_begin = 0; e.g_begin = 0; e.g_count = NG;
+    cudaError_t err = launch_vq_roll_tc(e, s);
+    if (err != cudaSuccess) return err;
+    roll_commit_kernel<<<1, 256, 0, s>>>(a);
+    return cudaGetLastError();
+  }
   dim3 grid(a.L * a.NB * a.H * 2 * (kD / C));
   if (a.Tc == 1 && C == 8) roll_kernel<1, 8><<<grid, 256, 0, s>>>(a);
   else if (a.Tc == 2 && C == 8) roll_kernel<2, 8><<<grid, 256, 0, s>>>(a);

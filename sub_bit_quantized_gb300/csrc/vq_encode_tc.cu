@@ -35,6 +35,15 @@
 //    near-ties as above from shared memory, writes the index and releases the ring stage.
 // So the MMAs of one tile run while the other accumulator's epilogue works. Every wait is
 // bounded; a timeout sets the device error word and every warp leaves its loop.
+//
+// Page-roll instantiation (kRoll; method step 4 / Figure 5: during decode the oldest recent
+// page is encoded every 8 tokens): a plane is (layer, K/V, head, beta, group) and its rows are
+// the 8 tokens of the oldest recent page of every request, read from the bf16 windows, so all
+// requests' rows share one staged codebook. A plane then has few tiles, so the three bf16
+// parts are cut once at load time (kvq_split_codebooks, the same arithmetic as the staging
+// below) and the loader copies each plane's parts with one bulk copy into one of two
+// buffers while the previous plane's tiles run. Rows of requests that are not due are
+// zero-filled and not written; a launch with no request due returns at once.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -65,7 +74,7 @@ static_assert(kEpiWarps == 8 && kLoadWarp == kEpiWarps && kMmaWarp == kLoadWarp 
 // B: -||e||^2 / 2, 0..), padded to whole MMA K steps of 32 bytes
 __host__ __device__ constexpr int tc_chunks(int DC) { return 2 * ((DC + 2) / 2); }
 
-template <int TC, int C>
+template <int TC, int C, bool kRoll = false>
 struct TcLayout {
   static constexpr int G = TC * C;
   static constexpr int DC = G / 8;                          // data chunks per row
@@ -76,8 +85,9 @@ struct TcLayout {
   static constexpr int kABytes = kTcM * kRowBytes;          // one tile of vectors
   static constexpr int kBPartBytes = kTcN * kRowBytes;      // one codebook part
   static constexpr int kOffA = 0;                           // kAStages tile buffers
-  static constexpr int kOffB = kOffA + kAStages * kABytes;  // the three codebook parts
-  static constexpr int kOffBar = kOffB + kParts * kBPartBytes;  // mbarriers, TMEM address, flag
+  static constexpr int kOffB = kOffA + kAStages * kABytes;  // the three codebook parts (two buffers: roll)
+  static constexpr int kBufBytes = kParts * kBPartBytes;
+  static constexpr int kOffBar = kOffB + (kRoll ? 2 : 1) * kBufBytes;  // mbarriers, TMEM address, flags
   static constexpr int kOffNear = kOffBar + 160;            // per epilogue warp: near-tie pairs, distances
   static constexpr int kSmem = kOffNear + kEpiWarps * kNearCap * 8;
   // requested per block so that a second block cannot share the SM (and its 512 TMEM columns)
@@ -190,13 +200,24 @@ __device__ __forceinline__ Plane plane_of(const VqEncodeArgs& a, int p) {
   return q;
 }
 
+// Roll rows: row q of a plane is token j = q mod 8 of request b = q / 8's oldest recent page;
+// true when q is a row and b is due (its recent window holds W + 8 tokens and a page is free)
+__device__ __forceinline__ bool roll_row(const VqEncodeArgs& a, int q, int& b, int& jj, int& np) {
+  b = q >> 3;
+  jj = q & 7;
+  np = 0;
+  if (q >= a.n_tok) return false;
+  const int L = a.seq_len[b];
+  np = a.n_pages[b];
+  return (L - a.sink - kPage * np == a.recent + kPage) && (np < a.max_pages);
+}
+
 // three bf16 parts of the plane's codebook (and its -||e||^2/2 column), rows r0, r0 + nt, ..
+// cb: a [256][G] fp32 codebook; sb: the three parts' destination (shared or global memory)
 template <int TC, int C>
-__device__ void stage_codebook(const VqEncodeArgs& a, int plane, unsigned char* sb, int r0, int nt) {
+__device__ void split_codebook(const float* cb, unsigned char* sb, int r0, int nt) {
   using Lay = TcLayout<TC, C>;
   constexpr int G = Lay::G, KC = Lay::KC, DC = Lay::DC;
-  const Plane P = plane_of(a, plane);
-  const float* cb = a.cb + (((size_t)P.beta * a.H + P.h) * Lay::NG + a.g_begin + P.gi) * (size_t)kCB * G;
 #pragma unroll 1
   for (int r = r0; r < kTcN; r += nt) {
     float ev[G];  // the row's coordinates, all loads in flight together
@@ -244,6 +265,22 @@ __device__ void stage_codebook(const VqEncodeArgs& a, int plane, unsigned char* 
   }
 }
 
+template <int TC, int C>
+__device__ __forceinline__ void stage_codebook(const VqEncodeArgs& a, int plane, unsigned char* sb, int r0, int nt) {
+  using Lay = TcLayout<TC, C>;
+  const Plane P = plane_of(a, plane);
+  split_codebook<TC, C>(a.cb + (((size_t)P.beta * a.H + P.h) * Lay::NG + a.g_begin + P.gi) * (size_t)kCB * Lay::G, sb,
+                        r0, nt);
+}
+
+// kvq_split_codebooks: one block per codebook, a thread per row
+template <int TC, int C>
+__global__ void __launch_bounds__(256) split_codebooks_kernel(const float* cb, uint8_t* cbp) {
+  using Lay = TcLayout<TC, C>;
+  split_codebook<TC, C>(cb + (size_t)blockIdx.x * kCB * Lay::G, cbp + (size_t)blockIdx.x * Lay::kBufBytes, threadIdx.x,
+                        blockDim.x);
+}
+
 __device__ __forceinline__ bool enc_wait(uint64_t* bar, uint32_t parity, volatile int* failed, int* err) {
   if (*failed) return false;
   if (mbar_wait_bounded_sleep(bar, parity)) return true;
@@ -266,10 +303,10 @@ __device__ __forceinline__ float at_least(float v, float cth) {
   return d;
 }
 
-template <int TC, int C>
+template <int TC, int C, bool kRoll>
 __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncodeArgs a, const int U,
                                                                   const int tiles_per_plane) {
-  using Lay = TcLayout<TC, C>;
+  using Lay = TcLayout<TC, C, kRoll>;
   constexpr int KC = Lay::KC, DC = Lay::DC;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* sa0 = smem + Lay::kOffA;
@@ -279,8 +316,10 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
   uint64_t* accfull = aempty + kAStages;                                // MMAs done (commit)
   uint64_t* accempty = accfull + 2;                                     // accumulator read (4 warps)
   uint64_t* bdone = accempty + 2;                                       // tile done with the codebook (4 warps)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bdone + 2);
+  uint64_t* bfull = bdone + 2;                                          // roll: codebook buffer landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bfull + 2);
   volatile int* failed = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* done = reinterpret_cast<int*>(tmem_slot + 2);  // roll, per epilogue warpgroup: tiles finished x 4 warps
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // Block k encodes group gi = k mod g_count over slots [m S / sets, (m + 1) S / sets) of the
@@ -290,10 +329,22 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
   const int gsel = blockIdx.x % a.g_count, set = blockIdx.x / a.g_count, n_sets = gridDim.x / a.g_count;
   const int lo = (int)((long long)U * set / n_sets), hi = (int)((long long)U * (set + 1) / n_sets);
   if (lo >= hi) return;  // uniform
+  if constexpr (kRoll) {  // between rolls no request is due: leave before anything is set up
+    int any = 0;
+    for (int b = tid; b < a.n_req; b += kEncThreads) {
+      int bb, jj, np;
+      any |= roll_row(a, kPage * b, bb, jj, np) ? 1 : 0;
+    }
+    if (!__syncthreads_or(any)) return;
+  }
   const int n = hi - lo;  // tiles of this block
   // tile i of the block: slot lo + i -> plane ((sequence, head, beta) of the slot, group gsel), tile
   auto plane_at = [&](int i) { return ((lo + i) / tiles_per_plane) * a.g_count + gsel; };
   auto tile_at = [&](int i) { return (lo + i) % tiles_per_plane; };
+  // roll: the block's planes in order (ordinal of tile i's plane, first tile of ordinal q);
+  // plane ordinal q uses codebook buffer q & 1, copied once the plane two before it is done
+  auto pk_of = [&](int i) { return (lo + i) / tiles_per_plane - lo / tiles_per_plane; };
+  auto first_of = [&](int q) { return q == 0 ? 0 : (lo / tiles_per_plane + q) * tiles_per_plane - lo; };
 
   // ---- TMEM (warp 0), barriers, constant A chunks, the first plane's codebook (all threads) ----
   if (warp == 0) {
@@ -311,11 +362,13 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
       mbar_init(&accfull[e], 1);
       mbar_init(&accempty[e], 4);
       mbar_init(&bdone[e], 4);
+      mbar_init(&bfull[e], 1);
+      done[e] = 0;
     }
     *failed = 0;
     fence_mbar_init();
     // the codebooks of the block's later planes: HBM -> L2 while the pipeline starts
-    for (int pl = plane_at(0) + a.g_count; pl <= plane_at(n - 1); pl += a.g_count) {
+    for (int pl = plane_at(0) + a.g_count; !kRoll && pl <= plane_at(n - 1); pl += a.g_count) {
       const Plane P = plane_of(a, pl);
       bulk_prefetch_l2(a.cb + (((size_t)P.beta * a.H + P.h) * Lay::NG + a.g_begin + P.gi) * (size_t)kCB * Lay::G,
                        kCB * Lay::G * 4);
@@ -326,7 +379,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
     const int r = rem / (KC - DC), c = DC + rem % (KC - DC);
     *reinterpret_cast<uint4*>(sa0 + st * Lay::kABytes + op_off(r, c, KC)) = make_uint4(c == DC ? 0x3F80u : 0u, 0u, 0u, 0u);
   }
-  stage_codebook<TC, C>(a, plane_at(0), sb, tid, kEncThreads);
+  if constexpr (!kRoll) stage_codebook<TC, C>(a, plane_at(0), sb, tid, kEncThreads);
   fence_proxy_async_smem();  // generic writes -> the tensor cores' view
   tc_fence_before();
   __syncthreads();
@@ -339,19 +392,75 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
       fence_proxy_async_smem();
       mbar_arrive(&afull[i % kAStages]);
     };
+    // roll: the codebook parts of the block's planes, one bulk copy each into buffer q & 1
+    // (completion q >> 1 of bfull[q & 1]) once plane q - 2 is done with that buffer
+    const int n_planes = kRoll ? pk_of(n - 1) + 1 : 1;
+    int copied = -1;  // planes 0 .. copied have been issued
+    volatile int* vdone = done;
+    auto done_below = [&](int X) {  // every tile < X is finished by its epilogue warpgroup
+      return vdone[0] >= 4 * ((X + 1) / 2) && vdone[1] >= 4 * (X / 2);
+    };
+    auto copy_parts = [&](int q) {  // lane 0
+      const Plane P = plane_of(a, plane_at(first_of(q)));
+      const uint8_t* src = ((P.b & 1) ? a.cbp2 : a.cbp) + (size_t)(P.b >> 1) * a.cbp_layer +
+                           (((size_t)P.beta * a.H + P.h) * Lay::NG + P.gi) * (size_t)Lay::kBufBytes;
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&bfull[q & 1], Lay::kBufBytes);
+      bulk_g2s(sb + (q & 1) * Lay::kBufBytes, src, Lay::kBufBytes, &bfull[q & 1]);
+    };
+    if constexpr (kRoll) {
+      if (lane == 0)
+        for (int q = 0; q < min(2, n_planes); ++q) copy_parts(q);
+      copied = min(2, n_planes) - 1;
+    }
     int i = 0;
     for (; i < n; ++i) {
       const int st = i % kAStages;
+      if constexpr (kRoll) {
+        // the next plane's parts, once the plane two before it is done (needed before this
+        // tile's MMAs when it starts that plane: then wait for the buffer)
+        const int q = copied + 1;
+        if (q < n_planes) {
+          const bool need = q <= pk_of(i);
+          bool free_buf = __all_sync(0xFFFFFFFFu, done_below(first_of(q - 1)));
+          if (need && !free_buf) {
+            const uint64_t t0 = global_ns();
+            while (!free_buf) {
+              if (*failed) break;
+              if (global_ns() - t0 > 1000000000ull) {
+                *failed = 1;
+                set_error(a.err, KVQ_ERR_TIMEOUT);
+                break;
+              }
+              __nanosleep(64);
+              free_buf = __all_sync(0xFFFFFFFFu, done_below(first_of(q - 1)));
+            }
+            if (!free_buf) break;  // warp-uniform
+          }
+          if (free_buf) {
+            if (lane == 0) copy_parts(q);
+            copied = q;
+          }
+        }
+      }
       if (i >= kAStages && !__all_sync(0xFFFFFFFFu, enc_wait(&aempty[st], ((i / kAStages) - 1) & 1, failed, a.err)))
         break;  // warp-uniform
       const int plane = plane_at(i), t = tile_at(i);
       const Plane P = plane_of(a, plane);
       const uint16_t* xb = a.x + (size_t)P.b * a.sb + (size_t)P.h * a.sh + (size_t)(a.g_begin + P.gi) * C;
+      if constexpr (kRoll) xb = ((P.b & 1) ? a.x2 : a.x) + (size_t)(P.b >> 1) * a.x_layer + (size_t)P.h * a.sh + (size_t)P.gi * C;
       unsigned char* sa = sa0 + st * Lay::kABytes;
       for (int q = lane; q < kTcM * DC; q += 32) {  // chunk d of row r: coordinates 8d .. 8d + 7
         const int r = q / DC, d = q % DC, j = t * kTcM + r;
-        const bool in = j < a.n_tok;
+        bool in = j < a.n_tok;
         const uint16_t* xr = xb + (size_t)(in ? j : 0) * kD;
+        if constexpr (kRoll) {  // the request's window slot of the token
+          int b, jj, np;
+          in = roll_row(a, j, b, jj, np);
+          const int pos = a.sink + kPage * np + jj;
+          const int slot = a.sink + (pos - a.sink) % (a.recent + kPage);
+          xr = xb + (in ? (size_t)b * a.sb + (size_t)slot * kD : 0);
+        }
         unsigned char* dst = sa + op_off(r, d, KC);
         if constexpr (C >= 8) {
           cp_async16(dst, xr + (size_t)(P.beta * TC + (8 * d) / C) * a.st + (8 * d) % C, in);
@@ -368,6 +477,10 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
     }
     cp_async_wait<0>();  // nothing of this block's may land after it exits
     for (int k = max(0, i - (kLoadDepth - 1)); k < i; ++k) land(k);
+    if constexpr (kRoll) {  // the last codebook copies issued: let them land (bounded)
+      if (lane == 0)
+        for (int q = max(0, copied - 1); q <= copied; ++q) mbar_wait_bounded(&bfull[q & 1], (uint32_t)((q >> 1) & 1));
+    }
   } else if (warp == kMmaWarp) {
     // ================= MMA issue; codebook restaging at plane changes ==========================
     const uint64_t a_desc0 = umma_desc(smem_u32(sa0), 128, KC * 128);
@@ -377,7 +490,8 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
     for (int i = 0; i < n; ++i) {
       const int st = i % kAStages, e = i & 1;
       const int plane = plane_at(i);
-      if (plane != cur_plane) {
+      const int bufo = kRoll ? (pk_of(i) & 1) * Lay::kBufBytes : 0;  // this plane's codebook buffer
+      if (!kRoll && plane != cur_plane) {
         // every earlier tile is done with the codebook: its MMAs and its epilogue (near-ties
         // read the parts)
         bool ok = true;
@@ -393,7 +507,11 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
       }
       int ok = 1;
       if (lane == 0) {
-        ok = enc_wait(&afull[st], (i / kAStages) & 1, failed, a.err);
+        if (kRoll && (i == 0 || pk_of(i - 1) != pk_of(i))) {  // the plane's parts have landed
+          const int pk = pk_of(i);
+          ok = enc_wait(&bfull[pk & 1], (pk >> 1) & 1, failed, a.err);
+        }
+        if (ok) ok = enc_wait(&afull[st], (i / kAStages) & 1, failed, a.err);
         if (ok && i >= 2) ok = enc_wait(&accempty[e], ((i >> 1) - 1) & 1, failed, a.err);
         if (ok) {
           tc_fence_after();
@@ -404,7 +522,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
 #pragma unroll
             for (int s = 0; s < KC / 2; ++s)
               umma_bf16(tmem + kTcN * e, a_desc0 + (uint64_t)((st * Lay::kABytes + s * 256) >> 4),
-                        b_desc0 + (uint64_t)((p * Lay::kBPartBytes + s * 256) >> 4), (p | s) != 0);
+                        b_desc0 + (uint64_t)((bufo + p * Lay::kBPartBytes + s * 256) >> 4), (p | s) != 0);
           umma_commit(&accfull[e]);
           last = i;
         }
@@ -444,6 +562,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
       const float best = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
       const int plane = plane_at(i), t = tile_at(i);
       const unsigned char* sa = sa0 + st * Lay::kABytes;
+      const unsigned char* sbt = sb + (kRoll ? (pk_of(i) & 1) * Lay::kBufBytes : 0);  // this tile's codebook
       float z2 = 0.f;
 #pragma unroll
       for (int c = 0; c < DC; ++c) {
@@ -490,7 +609,9 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
         }
       }
       const int j = t * kTcM + row;
-      const bool valid = j < a.n_tok;
+      int rb = 0, rj = 0, rnp = 0;
+      bool valid = j < a.n_tok;
+      if constexpr (kRoll) valid = roll_row(a, j, rb, rj, rnp);
       const bool need = valid && !*failed && !(tally < 1.5f);
       int result = 64 * ksel + __float2int_rn((ksum - 1.f) * 512.f);
       uint32_t cand[kTcN / 32];  // candidate masks of this row (need only)
@@ -540,9 +661,9 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
 #pragma unroll 1
           for (int c = 0; c < DC; ++c) {
             const uint4 w = *reinterpret_cast<const uint4*>(sa + op_off(rr, c, KC));
-            const uint4 e0 = *reinterpret_cast<const uint4*>(sb + op_off(r, c, KC));
-            const uint4 e1 = *reinterpret_cast<const uint4*>(sb + Lay::kBPartBytes + op_off(r, c, KC));
-            const uint4 e2 = *reinterpret_cast<const uint4*>(sb + 2 * Lay::kBPartBytes + op_off(r, c, KC));
+            const uint4 e0 = *reinterpret_cast<const uint4*>(sbt + op_off(r, c, KC));
+            const uint4 e1 = *reinterpret_cast<const uint4*>(sbt + Lay::kBPartBytes + op_off(r, c, KC));
+            const uint4 e2 = *reinterpret_cast<const uint4*>(sbt + 2 * Lay::kBPartBytes + op_off(r, c, KC));
             const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
             const uint32_t h4[4] = {e0.x, e0.y, e0.z, e0.w}, m4[4] = {e1.x, e1.y, e1.z, e1.w},
                            l4[4] = {e2.x, e2.y, e2.z, e2.w};
@@ -600,15 +721,22 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
       }
       if (valid && !*failed) {
         const Plane P = plane_of(a, plane);
-        uint8_t* out = a.idx + (((size_t)P.beta * a.max_batch + (a.seq_begin + P.b)) * a.H + P.h) *
-                                   (size_t)a.max_pages * Lay::kPageBytes;
-        out[(size_t)(a.page_begin + j / kPage) * Lay::kPageBytes + page_byte(a.g_begin + P.gi, j % kPage, Lay::NG)] =
-            (uint8_t)result;
+        if constexpr (kRoll) {
+          uint8_t* out = ((P.b & 1) ? a.idx2 : a.idx) + (size_t)(P.b >> 1) * a.idx_layer +
+                         (((size_t)P.beta * a.max_batch + rb) * a.H + P.h) * (size_t)a.max_pages * Lay::kPageBytes;
+          out[(size_t)rnp * Lay::kPageBytes + page_byte(P.gi, rj, Lay::NG)] = (uint8_t)result;
+        } else {
+          uint8_t* out = a.idx + (((size_t)P.beta * a.max_batch + (a.seq_begin + P.b)) * a.H + P.h) *
+                                     (size_t)a.max_pages * Lay::kPageBytes;
+          out[(size_t)(a.page_begin + j / kPage) * Lay::kPageBytes + page_byte(a.g_begin + P.gi, j % kPage, Lay::NG)] =
+              (uint8_t)result;
+        }
       }
       __syncwarp();
       if (lane == 0) {  // this warp is done with the vector rows and the codebook
         mbar_arrive(&aempty[st]);
-        mbar_arrive(&bdone[e]);
+        if constexpr (kRoll) atomicAdd(&done[e], 1);  // after __syncwarp: the warp's reads are done
+        else mbar_arrive(&bdone[e]);
       }
     }
 #pragma unroll
@@ -625,11 +753,11 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_tc_kernel(const VqEncod
   }
 }
 
-template <int TC, int C>
+template <int TC, int C, bool kRoll>
 cudaError_t launch_tc(const VqEncodeArgs& a, cudaStream_t s) {
-  using Lay = TcLayout<TC, C>;
+  using Lay = TcLayout<TC, C, kRoll>;
   cudaError_t e =
-      cudaFuncSetAttribute(encode_tc_kernel<TC, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemLaunch);
+      cudaFuncSetAttribute(encode_tc_kernel<TC, C, kRoll>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemLaunch);
   if (e != cudaSuccess) return e;
   const int tiles = (a.n_tok + kTcM - 1) / kTcM;
   const long long U = (long long)a.n_seq * a.H * a.NB * tiles;  // (sequence, head, beta, tile) slots
@@ -639,20 +767,45 @@ cudaError_t launch_tc(const VqEncodeArgs& a, cudaStream_t s) {
   // sets of g_count blocks (one per group), as many as fit one block per SM and have slots
   const long long sets = std::max(1ll, std::min<long long>(U, sms / std::max(1, a.g_count)));
   const long long blocks = sets * a.g_count;
-  encode_tc_kernel<TC, C><<<(unsigned)blocks, kEncThreads, Lay::kSmemLaunch, s>>>(a, (int)U, tiles);
+  encode_tc_kernel<TC, C, kRoll><<<(unsigned)blocks, kEncThreads, Lay::kSmemLaunch, s>>>(a, (int)U, tiles);
+  return cudaGetLastError();
+}
+
+
+template <bool kRoll>
+cudaError_t launch_encode_any(const VqEncodeArgs& a, cudaStream_t s) {
+  if (a.n_tok <= 0 || a.n_seq <= 0 || a.g_count <= 0) return cudaSuccess;
+  const int C = a.G / a.Tc;
+  if (a.Tc == 1 && C == 8) return launch_tc<1, 8, kRoll>(a, s);
+  if (a.Tc == 2 && C == 8) return launch_tc<2, 8, kRoll>(a, s);
+  if (a.Tc == 4 && C == 8) return launch_tc<4, 8, kRoll>(a, s);
+  if (a.Tc == 1 && C == 16) return launch_tc<1, 16, kRoll>(a, s);
+  if (a.Tc == 4 && C == 4) return launch_tc<4, 4, kRoll>(a, s);
+  return cudaErrorInvalidValue;
+}
+
+template <int TC, int C>
+cudaError_t launch_split(const float* cb, uint8_t* cbp, long long n, cudaStream_t s) {
+  split_codebooks_kernel<TC, C><<<(unsigned)n, 256, 0, s>>>(cb, cbp);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_vq_encode(const VqEncodeArgs& a, cudaStream_t s) {
-  if (a.n_tok <= 0 || a.n_seq <= 0 || a.g_count <= 0) return cudaSuccess;
-  const int C = a.G / a.Tc;
-  if (a.Tc == 1 && C == 8) return launch_tc<1, 8>(a, s);
-  if (a.Tc == 2 && C == 8) return launch_tc<2, 8>(a, s);
-  if (a.Tc == 4 && C == 8) return launch_tc<4, 8>(a, s);
-  if (a.Tc == 1 && C == 16) return launch_tc<1, 16>(a, s);
-  if (a.Tc == 4 && C == 4) return launch_tc<4, 4>(a, s);
+cudaError_t launch_vq_encode(const VqEncodeArgs& a, cudaStream_t s) { return launch_encode_any<false>(a, s); }
+cudaError_t launch_vq_roll_tc(const VqEncodeArgs& a, cudaStream_t s) { return launch_encode_any<true>(a, s); }
+
+size_t split_codebook_bytes(int G) { return (size_t)kParts * kTcN * tc_chunks(G / 8) * 16; }
+
+cudaError_t launch_split_codebooks(const float* cb, uint8_t* cbp, long long n, int Tc, int G, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  if (n >= (1ll << 31)) return cudaErrorInvalidValue;
+  const int C = G / Tc;
+  if (Tc == 1 && C == 8) return launch_split<1, 8>(cb, cbp, n, s);
+  if (Tc == 2 && C == 8) return launch_split<2, 8>(cb, cbp, n, s);
+  if (Tc == 4 && C == 8) return launch_split<4, 8>(cb, cbp, n, s);
+  if (Tc == 1 && C == 16) return launch_split<1, 16>(cb, cbp, n, s);
+  if (Tc == 4 && C == 4) return launch_split<4, 4>(cb, cbp, n, s);
   return cudaErrorInvalidValue;
 }
 

@@ -43,11 +43,11 @@ class VqCfg(ctypes.Structure):
 class VqCacheC(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("idx_k", "idx_v", "win_k", "win_v", "bt_k", "bt_v", "cb_k", "cb_v",
-                 "rope_cos", "rope_sin", "seq_len", "n_pages")]
+                 "rope_cos", "rope_sin", "seq_len", "n_pages", "cbp_k", "cbp_v")]
 
 
 class VqSizes(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_size_t) for n in ("idx", "win", "bt", "bt_v", "cb", "rope", "per_request")]
+    _fields_ = [(n, ctypes.c_size_t) for n in ("idx", "win", "bt", "bt_v", "cb", "rope", "per_request", "cbp")]
 
 
 class KiviCfg(ctypes.Structure):
@@ -77,6 +77,7 @@ _SIGS = {
     "kvq_rope_table": (_I, [_P, _P, _P, _P]),
     "kvq_slice_codebooks": (_I, [_P, _P, _P, _P]),
     "kvq_slice_codebooks_fp16": (_I, [_P, _P, _P, _P]),
+    "kvq_split_codebooks": (_I, [_P, _P, _P, _P]),
     "kvq_encode_vq": (_I, [_P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P]),
     "kvq_prefill_vq": (_I, [_P, _P, _I, _P, _P, _I64, _I64, _I64, _I, _I, _I, _P, _P]),
     "kvq_append_page": (_I, [_P, _P, _I, _I, _P, _P, _I, _P]),
@@ -215,6 +216,10 @@ class VqCache:
         self.bt_v = torch.zeros((L, c.T, H, c.K, c.D), dtype=torch.float16, device=dev)
         self.cb_k = torch.zeros((L, NB, H, c.NG, c.K, c.G), dtype=torch.float32, device=dev)
         self.cb_v = torch.zeros_like(self.cb_k)
+        sizes = vq_cache_sizes(cfg)
+        # codebook parts for the tensor-core page roll (kvq_split_codebooks)
+        self.cbp_k = torch.zeros(sizes.cbp, dtype=torch.uint8, device=dev)
+        self.cbp_v = torch.zeros_like(self.cbp_k)
         self.rope_cos = torch.empty((c.max_ctx, c.D // 2), dtype=torch.float32, device=dev)
         self.rope_sin = torch.empty_like(self.rope_cos)
         self.seq_len = torch.zeros(B, dtype=torch.int32, device=dev)
@@ -229,13 +234,15 @@ class VqCache:
     def c_struct(self) -> VqCacheC:
         return VqCacheC(*[_ptr(getattr(self, n)) for n in
                           ("idx_k", "idx_v", "win_k", "win_v", "bt_k", "bt_v", "cb_k", "cb_v",
-                           "rope_cos", "rope_sin", "seq_len", "n_pages")])
+                           "rope_cos", "rope_sin", "seq_len", "n_pages", "cbp_k", "cbp_v")])
 
     def load_codebooks(self, cb_k: torch.Tensor, cb_v: torch.Tensor, stream=None):
         self.cb_k.copy_(cb_k)
         self.cb_v.copy_(cb_v)
         kvq_slice_codebooks(self.cfg, self.cb_k, self.bt_k, stream)
         kvq_slice_codebooks_fp16(self.cfg, self.cb_v, self.bt_v, stream)
+        kvq_split_codebooks(self.cfg, self.cb_k, self.cbp_k, stream)
+        kvq_split_codebooks(self.cfg, self.cb_v, self.cbp_v, stream)
 
 
 def vq_cache_sizes(cfg: VqConfig) -> VqSizes:
@@ -261,6 +268,11 @@ def kvq_slice_codebooks_fp16(cfg: VqConfig, cb, bt16, stream=None):
     c = cfg.to_c()
     _check(lib().kvq_slice_codebooks_fp16(ctypes.byref(c), _ptr(cb), _ptr(bt16), _stream(stream)),
            "kvq_slice_codebooks_fp16")
+
+
+def kvq_split_codebooks(cfg: VqConfig, cb, cbp, stream=None):
+    c = cfg.to_c()
+    _check(lib().kvq_split_codebooks(ctypes.byref(c), _ptr(cb), _ptr(cbp), _stream(stream)), "kvq_split_codebooks")
 
 
 def kvq_encode_vq(cfg: VqConfig, x, x_strides, seq_begin, n_seq, n_tok, cb, idx, page_begin=0,

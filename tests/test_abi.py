@@ -49,6 +49,9 @@ def test_cache_sizes_formula(L):
     assert s.bt_v == 24 * 4 * 16 * 256 * 128 * 2
     assert s.cb == 24 * 2 * 16 * 16 * 256 * 16 * 4
     assert s.rope == 6144 * 64 * 4 and s.per_request == 64 * 4
+    # three bf16 parts of each codebook, 256 rows x 4 chunks of 16 bytes (16 coordinates, the
+    # -|e|^2/2 chunk, one padding chunk)
+    assert s.cbp == 24 * 2 * 16 * 16 * 3 * 256 * 4 * 16
     # one call reads one (layer, block) of each index array: 199.0 MB at B=64, 6K
     assert s.idx / 24 / 2 * 2 == pytest.approx(199.0e6, rel=1e-3)
 

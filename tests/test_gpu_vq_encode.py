@@ -203,8 +203,44 @@ def test_prefill_then_attention_integration(Tc):
                 C.check_close(got[b, h], ref)
 
 
+def test_split_codebook_parts_sum_back():
+    # kvq_split_codebooks: in the tensor-core operand layout (row groups of 8 rows x 16-byte
+    # chunks), hi + mid + lo of every coordinate is the fp32 entry exactly, and the augmented
+    # chunk's first element carries -|e|^2/2 (its parts summed); the rest is zero
+    for Tc, G in ((2, 16), (4, 32), (1, 8)):
+        C_ = G // Tc
+        cfg = kvq.VqConfig(T=4, Tc=Tc, G=G, n_layers=1, n_heads=1, max_pages=4, max_batch=1, max_ctx=64)
+        rng = np.random.default_rng(11 + G)
+        cb = (rng.standard_normal((1, cfg.NB, 1, cfg.NG, 256, G)) * rng.choice([1.0, 15.0], size=G)).astype(np.float32)
+        cbp = torch.zeros(kvq.vq_cache_sizes(cfg).cbp, dtype=torch.uint8, device="cuda")
+        kvq.kvq_split_codebooks(cfg, torch.from_numpy(cb).cuda(), cbp)
+        raw = cbp.cpu().numpy()
+        DC = G // 8
+        KC = 2 * ((DC + 2) // 2)
+        part = 256 * KC * 16
+        n_cb = cfg.NB * cfg.NG
+        words = raw.reshape(n_cb, 3, 256 // 8, KC, 8, 16).view(np.uint16)  # [cb][part][rg][chunk][row][8 bf16]
+        vals = (words.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        total = vals.sum(axis=1)  # hi + mid + lo, exact in float64
+        flat = cb.reshape(n_cb, 256, G).astype(np.float64)
+        rows = np.arange(256)
+        for c in range(DC):
+            for i in range(8):
+                kk = 8 * c + i
+                coord = (kk % C_) * Tc + kk // C_
+                got = total[:, rows // 8, c, rows % 8, i]
+                assert np.array_equal(got, flat[:, :, coord]), (G, c, i)
+        nh = total[:, rows // 8, DC, rows % 8, 0]
+        want = -0.5 * (flat ** 2).sum(axis=2)
+        assert np.allclose(nh, want, rtol=1e-6, atol=0)
+        rest = total[:, :, DC:, :, :].copy()
+        rest[:, :, 0, :, 0] = 0.0
+        assert not rest.any()
+
+
+@pytest.mark.parametrize("path", ["tensor", "cuda"])
 @pytest.mark.parametrize("Tc", [2, 1, 4])
-def test_append_and_roll_equal_prefill_encoding(Tc):
+def test_append_and_roll_equal_prefill_encoding(Tc, path):
     # stream 40 tokens through kvq_append_page (2 layers x 4 loop steps each): the rolled
     # pages must equal the oracle's encoding of the same tokens, lengths must follow the
     # sink / page / recent rule, and attention must match the oracle at the end
@@ -220,6 +256,8 @@ def test_append_and_roll_equal_prefill_encoding(Tc):
     cfg = kvq.VqConfig(T=T, Tc=Tc, G=G, n_layers=NL, n_heads=H, max_pages=16, max_batch=B, max_ctx=Lmax)
     cache = kvq.VqCache(cfg)
     cache.load_codebooks(torch.from_numpy(cbk).cuda(), torch.from_numpy(cbv).cuda())
+    if path == "cuda":  # no split codebook parts: the roll runs on CUDA cores
+        cache.cbp_k = cache.cbp_v = None
     xk_t = [C.bf16_tensor(np.ascontiguousarray(xk2[l])) for l in range(NL)]
     xv_t = [C.bf16_tensor(np.ascontiguousarray(xv2[l])) for l in range(NL)]
     for l in range(NL):

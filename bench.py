@@ -393,8 +393,8 @@ DTYPE_LABEL = {
 PROFILED_TRAFFIC = {
     "loopvq_b64_6k:vq_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_attn.cu",
-        "52d88be2aa96800b115504f8559cdc96f2322d2daa509bad5ac2f78499fc650d",
-        241494272 + 3686144),
+        "d91aa8fe3231d26338f9c3f7864f1edf7f5fc697b4e6566ea226e833304f4103",
+        245847296 + 3481088),
     "kivi_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
         "f9a971efd8ea1d5d4c32f9fcda3c4b12e017e1e4b6780049d481c08c1c92b352",

@@ -277,12 +277,11 @@ __device__ __forceinline__ void rotate_fwd(const float2 (&ul)[2], const float2 (
 }
 
 // ------------------------------------------------------------------ pass 2: histogram of one page
-// w: this lane's fixed-point weight of token s (lanes 2t hold token t). bins: shared address of
-// the [256][32] u32 histogram. The lanes' columns make every red hit 32 distinct banks.
+// wt: the fixed-point weights of the page's 8 tokens. bins: shared address of the [256][32]
+// u32 histogram. The lanes' columns make every red hit 32 distinct banks.
 template <int NG>
-__device__ __forceinline__ void page_hist(const uint4 row, const uint32_t w, const uint32_t bins, const int lane,
-                                          const unsigned gmask) {
-  const int j = lane & 15, s = j >> 1, m = j & 1, half = lane >> 4, base = lane & 16;
+__device__ __forceinline__ void page_hist(const uint4 row, const uint32_t (&wt)[8], const uint32_t bins, const int lane) {
+  const int j = lane & 15, s = j >> 1, m = j & 1, half = lane >> 4;
   if constexpr (NG == 16) {
     // group s + 8m, column 16 half + s + 8m; token t's index: byte 2t + m of the row
     const uint32_t b0 = bins + (uint32_t)(16 * half + s + 8 * m) * 4;
@@ -290,9 +289,8 @@ __device__ __forceinline__ void page_hist(const uint4 row, const uint32_t w, con
     const uint32_t rw[4] = {row.x >> sh, row.y >> sh, row.z >> sh, row.w >> sh};
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-      const uint32_t wt = __shfl_sync(gmask, w, base + 2 * t);
       const uint32_t r = (rw[t >> 1] >> (16 * (t & 1))) & 0xFFu;
-      red_add_u32(b0 + (r << 7), wt);
+      red_add_u32(b0 + (r << 7), wt[t]);
     }
   } else if constexpr (NG == 8) {
     // row s >> 1 holds groups s >> 1 (byte 2t) and (s >> 1) + 4 (byte 2t + 1); the lane takes
@@ -300,12 +298,10 @@ __device__ __forceinline__ void page_hist(const uint4 row, const uint32_t w, con
     const uint32_t b0 = bins + (uint32_t)(8 * (2 * half + (s & 1)) + (s >> 1) + 4 * m) * 4;
     const uint32_t sh = 8u * m;
     const uint32_t w0 = ((s & 1) ? row.z : row.x) >> sh, w1 = ((s & 1) ? row.w : row.y) >> sh;
-    const int t0 = 4 * (s & 1);
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const uint32_t wt = __shfl_sync(gmask, w, base + 2 * (t0 + t));
       const uint32_t r = (((t < 2) ? w0 : w1) >> (16 * (t & 1))) & 0xFFu;
-      red_add_u32(b0 + (r << 7), wt);
+      red_add_u32(b0 + (r << 7), (s & 1) ? wt[4 + t] : wt[t]);
     }
   } else {
     // NG == 32: row j holds groups j (byte 2t) and j + 16 (byte 2t + 1); page half 0 takes the
@@ -316,11 +312,10 @@ __device__ __forceinline__ void page_hist(const uint4 row, const uint32_t w, con
     const uint32_t rb[4] = {row.x >> sb, row.y >> sb, row.z >> sb, row.w >> sb};
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-      const uint32_t wt = __shfl_sync(gmask, w, base + 2 * t);
       const uint32_t r0 = (ra[t >> 1] >> (16 * (t & 1))) & 0xFFu;
       const uint32_t r1 = (rb[t >> 1] >> (16 * (t & 1))) & 0xFFu;
-      red_add_u32(bins + ga * 4 + (r0 << 7), wt);
-      red_add_u32(bins + gb * 4 + (r1 << 7), wt);
+      red_add_u32(bins + ga * 4 + (r0 << 7), wt[t]);
+      red_add_u32(bins + gb * 4 + (r1 << 7), wt[t]);
     }
   }
 }
@@ -462,14 +457,23 @@ __device__ void compute_role(const VqAttnArgs& a, unsigned char* smem, const Bar
         if (!__all_sync(0xFFFFFFFFu, wait_bar(B.hfree, hfph, B.failed, a.err))) break;
         hfph ^= 1u;
       }
+      // p = exp2(s - M) <= 1 in units of 2^-20: p + 8 has an ulp of 2^-20, so its mantissa is
+      // round(p 2^20) (nearest, ties to even); lanes 2t write token t's weight over its score
 #pragma unroll
       for (int pp = 0; pp < PPL; ++pp) {
-        if (pg0 + pp < npg) {
-          // p = exp2(s - M) <= 1 in units of 2^-20: p + 8 has an ulp of 2^-20, so its mantissa is
-          // round(p 2^20) (nearest, ties to even)
+        if (pg0 + pp < npg && m == 0) {
           const float p = exp2f(sp[pp * kPage + s] - M);
-          const uint32_t w = __float_as_uint(p + 8.0f) - 0x41000000u;
-          page_hist<NG>(rows[pp], w, bins, lane, gmask);
+          reinterpret_cast<uint32_t*>(sp)[pp * kPage + s] = __float_as_uint(p + 8.0f) - 0x41000000u;
+        }
+      }
+      __syncwarp();
+#pragma unroll
+      for (int pp = 0; pp < PPL; ++pp) {
+        if (pg0 + pp < npg) {  // the page's 8 weights: two 16-byte reads every lane of the page shares
+          const uint4 w03 = *reinterpret_cast<const uint4*>(sp + pp * kPage);
+          const uint4 w47 = *reinterpret_cast<const uint4*>(sp + pp * kPage + 4);
+          const uint32_t wt[8] = {w03.x, w03.y, w03.z, w03.w, w47.x, w47.y, w47.z, w47.w};
+          page_hist<NG>(rows[pp], wt, bins, lane);
         }
       }
       if (flags & kFLast) {

@@ -69,6 +69,30 @@ def test_quantize_bit_exact(bits):
     assert not kc[:, :, :32].any() and not vc[:, :, 128:].any()
 
 
+@pytest.mark.parametrize("n", [5, 37, 70])
+def test_quantize_values_ragged_tiles(n):
+    # per-token quantization of a token count that leaves the last 32-row tile (and its last
+    # 8-row block) partly empty: codes, scales and zero-points bit-exact, nothing written past
+    # the last token
+    B, H, bits = 2, 3, 2
+    V = np.ascontiguousarray(kv_data(301, B, H, max(n, 32))[2][:, :, :n])
+    cfg = kvq.KiviConfig(n_heads=H, k_bits=bits, v_bits=bits, max_batch=B, max_tokens=128)
+    cache = kvq.KiviCache(cfg)
+    kvq.kvq_quantize_kivi(cfg, kvq.PER_TOKEN, torch.from_numpy(V).cuda(), cache.v_codes, cache.v_scale,
+                          cache.v_zero, tok_begin=8)
+    torch.cuda.synchronize()
+    vc = _layout.unpack_codes(cache.v_codes.cpu().numpy(), bits)
+    vs, vz = cache.v_scale.cpu().numpy(), cache.v_zero.cpu().numpy()
+    for b in range(B):
+        for h in range(H):
+            c, sc, z = okivi.quantize_values(V[b, h], bits=bits)
+            assert np.array_equal(vc[b, h, 8:8 + n], c)
+            assert np.array_equal(vs[b, h, 8:8 + n].view(np.uint16), sc.view(np.uint16))
+            assert np.array_equal(vz[b, h, 8:8 + n].view(np.uint16), z.view(np.uint16))
+    assert not vc[:, :, :8].any() and not vc[:, :, 8 + n:].any()
+    assert not vs[:, :, 8 + n:].view(np.uint16).any() and not vz[:, :, 8 + n:].view(np.uint16).any()
+
+
 def test_quantize_full_size_sampled():
     # prefill workload: K and V of 16 heads x 32768 tokens
     H, n = 16, 32768

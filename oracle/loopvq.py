@@ -146,7 +146,8 @@ def decode_attention(q, t: int, Tc: int, seq_len: int, n_pages: int,
     Keys are rebuilt by lookup (quantized) or read (bf16), every key and the query are
     RoPE-rotated at their positions (keys are cached pre-RoPE: background "RoPE" and
     method step 1), and one softmax with scale 1/sqrt(D) runs over all keys (method step 5
-    merges the two kernels' partials exactly, so the result is the full softmax).
+    merges the partials of the quantized pages and of the bf16 window exactly, so the result
+    is the full softmax).
     """
     beta, m = step_to_block(t, Tc)
     q = np.asarray(q, np.float64)

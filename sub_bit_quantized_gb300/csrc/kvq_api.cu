@@ -88,8 +88,8 @@ kvq_status check_vq_cfg(const kvq_vq_cfg* c, const char* fn) {
 
 int win_slots(const kvq_vq_cfg* c) { return c->sink + c->recent + kvq::kPage; }
 
-// Blocks of the LoopVQ page kernel: one per SM unless the caller names a count (every block
-// takes an equal contiguous share of the units, so any count is correct).
+// Blocks of the LoopVQ decode kernel: one per SM unless the caller names a count (every block
+// takes an equal contiguous share of the page positions, so any count is correct).
 int plan_vq_blocks(int n_splits) { return n_splits > 0 ? n_splits : sm_count(); }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }

@@ -116,7 +116,7 @@ def test_workspace_size_and_split_plan(L):
     auto = kvq.kvq_decode_auto_splits(c, 64)
     assert auto >= 1
     assert kvq.kvq_decode_workspace_size(c, 64, 0) == kvq.kvq_decode_workspace_size(c, 64, auto)
-    # the page kernel runs one block per SM by default, whatever the batch
+    # the decode kernel runs one block per SM by default, whatever the batch
     big = cfg2(max_pages=40000, max_ctx=400000)
     assert kvq.kvq_decode_auto_splits(big, 1) == auto
 

@@ -134,11 +134,15 @@ struct KiviPlan {
 // Token splits of the KIVI kernel per (request, KV head, head subgroup): split k takes
 // quantized tokens [k tps, (k + 1) tps), and the last split also attends the fp16 residual.
 // The residual's 512 B per token count as quantized tokens of the same bytes, so tps divides
-// the quantized tokens plus that share evenly. The blocks run in rounds of (resident blocks
-// per SM) x SMs; the plan minimises rounds x (tps + a per-block cost) over plans of at least
-// 1.5 rounds (a single, partly empty round leaves SMs idle while its longest blocks finish),
-// which on this GPU picked 7 splits for 4-bit GQA (74.9 us; 79.1 us with 9) and 2 for one
-// head at 2 bits (100.5 us; 103.0 us with 7).
+// the quantized tokens plus that share evenly. A block's time is taken as tps plus a per-block
+// cost. The GPU starts a block whenever a slot frees (slots = resident blocks per SM x SMs),
+// so the call lasts about blocks / slots block times plus a tail in which the last blocks
+// finish on a partly idle GPU, 0.83 of a block time. The plan minimises that over plans of at
+// least 1.5 rounds. Measured split sweeps on this GPU (us per call): one head at 2 bits,
+// batch 16 x 32 heads, 4K: 2: 97.2, 3: 94.4, 4: 93.6 (picked), 5: 94.2, 6: 98.1. 4-bit GQA,
+// 32 over 8 heads: 5: 82.4, 6: 79.1, 7: 75.0 (picked), 8: 81.4, 9: 78.8. Whole rounds (the
+// earlier model) picked 2 splits for the first; a tail of half a block time picked 6 for the
+// second. Tails between 0.78 and 0.875 pick both optima.
 KiviPlan plan_kivi(const kvq_kivi_cfg* c, int B, int n_splits) {
   const double q_bytes = (c->k_bits + c->v_bits) * 16.0 + 24.0;  // codes + per-token share of scales
   const double resid_cost = c->residual * (512.0 / q_bytes);
@@ -156,8 +160,7 @@ KiviPlan plan_kivi(const kvq_kivi_cfg* c, int B, int n_splits) {
     const int tps = tps_for(n);
     const long long blocks = (long long)B * (c->n_q_heads / rh) * n;
     if (2 * blocks < 3 * slots && n < std::min(64, c->max_tokens / c->group)) continue;  // under 1.5 rounds
-    const long long rounds = (blocks + slots - 1) / slots;
-    const double cost = (double)rounds * (tps + 200.0);
+    const double cost = ((double)blocks / (double)slots + 0.83) * (tps + 200.0);
     if (cost < best * 0.999) {
       best = cost;
       p = KiviPlan{n, tps};

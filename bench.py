@@ -578,7 +578,7 @@ def run_ours(args, wl, rank, world, dist, pool):
         # appended in bf16 and the step's decode attention runs; every 8 tokens the append of
         # the token's last (layer, step) also encodes the oldest recent page into index pages
         B, H, NL, T = wl["B"], wl["H"], wl["layers"], wl["T"]
-        n_tok = args.warmup + 2 * args.steps + 16
+        n_tok = args.warmup + 2 * args.steps + 32
         cfg, cache, _, _ = setup_loopvq(wl, dev, 1234 + rank, extra_tokens=n_tok)
         gen = torch.Generator(device=dev).manual_seed(77 + rank)
         kn = torch.randn((B, H, D), generator=gen, device=dev).to(torch.bfloat16)
@@ -604,18 +604,27 @@ def run_ours(args, wl, rank, world, dist, pool):
         # the same 96 attention calls without appends (the cache stops growing), then per-token
         # events over 16 more tokens: tokens whose first append rolls a page vs the others
         ms_attn = time_region(lambda: [c() for c in calls.values()], args.steps, stream, dist) / args.steps
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(17)]
+        # per-token events around the token's first append (the call that rolls when a page is
+        # due): the roll's cost is that call's time on a rolling token minus its time on the others
+        n_meas = 32
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_meas)]
         rolled = []
-        for i in range(16):
+        for i in range(n_meas):
             Lb = int(cache.seq_len[0].item())  # length before this token
             np_b = int(cache.n_pages[0].item())
             rolled.append(Lb + 1 - 8 - 8 * np_b == wl["recent"] + 8)  # the first append advances, then rolls
-            ev[i].record(stream)
-            token()
-        ev[16].record(stream)
+            ev[i][0].record(stream)
+            kvq.kvq_append_page(cfg, cache, 0, 1, kn, vn, stream)
+            ev[i][1].record(stream)
+            calls[(0, 1)]()
+            for l in range(NL):
+                for t in range(1, T + 1):
+                    if (l, t) != (0, 1):
+                        kvq.kvq_append_page(cfg, cache, l, t, kn, vn, stream)
+                        calls[(l, t)]()
         torch.cuda.synchronize()
         assert kvq.device_error() == 0
-        tms = [ev[i].elapsed_time(ev[i + 1]) for i in range(16)]
+        tms = [e0.elapsed_time(e1) for e0, e1 in ev]
         plain = statistics.median([t for t, r in zip(tms, rolled) if not r])
         roll_extra = statistics.mean([t - plain for t, r in zip(tms, rolled) if r]) if any(rolled) else 0.0
         L_end = int(cache.seq_len[0].item())

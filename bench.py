@@ -393,8 +393,8 @@ DTYPE_LABEL = {
 PROFILED_TRAFFIC = {
     "loopvq_b64_6k:vq_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_attn.cu",
-        "94fbcf3a76d649fa04215d39ada0fc0955fab3d88125fa4f2267c3903ae5ba44",
-        245752832 + 3388160),
+        "d99056bcba3b29ae4051816d6ac4d7a082ba6ca0347d320bf160af919a52ca69",
+        245814528 + 3427328),
     "kivi_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
         "f9a971efd8ea1d5d4c32f9fcda3c4b12e017e1e4b6780049d481c08c1c92b352",

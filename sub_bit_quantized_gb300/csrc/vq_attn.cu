@@ -9,7 +9,7 @@
 //
 // GB300 design (the page's kernel gives every (request, head, split) its own program and
 // rebuilds value rows token by token). Here a codeword lookup costs shared-memory bandwidth
-// and every key 6 FMAs per channel pair, so the work is bound on chip, not by HBM. One
+// and every key 4 FMAs per channel pair, so the work is bound on chip, not by HBM. One
 // persistent launch, one block per SM; block k takes the k-th of G equal contiguous shares
 // of all index pages (head-major segments of (head, request)). Warp roles:
 //
@@ -29,14 +29,16 @@
 //      weight p_j = exp2(s_j - M) <= 1 is added as a fixed-point integer (2^-20 units) into a
 //      per-(group, codeword) histogram with shared-memory integer atomics (native on this
 //      GPU; float atomics are not), laid out [256][32 columns] so that the 32 lanes of every
-//      atomic hit 32 different banks. No value row is read per token.
+//      atomic hit 32 different banks. A page's 8 weights reach its lanes through the score
+//      buffer (two broadcast loads, not shuffles). No value row is read per token.
 //  * 4 aux warps: for each sub-piece, w . B_V (the fp16 value slice, read from L2) gives the
 //    sub-piece's partial (M, l, o); they attend the bf16 window of every segment whose first
-//    page this block holds (rotated query from the table, online softmax), merge, and write
-//    the output. A segment shared with other blocks is merged by the last block to finish
+//    page this block holds (two tokens per warp step, rotated query from the table, online
+//    softmax), merge, and write the output. A segment shared with other blocks is merged by the last block to finish
 //    its part (a per-segment counter in the workspace).
 //  * 1 producer warp (one lane): TMA bulk copies of each unit's index pages (and the query)
-//    into a ring of stages, and of the key slice whenever the share enters a new head.
+//    into a ring of stages, and of the key slice whenever the share enters a new head; an L2
+//    prefetch of each owned window's bf16 rows when the share reaches that segment.
 //
 // Every wait is an mbarrier wait with a time limit (the waiting warp suspends between polls);
 // a timeout sets the device error word and a block-wide flag, after which every role leaves
@@ -562,8 +564,9 @@ __device__ __forceinline__ void merge_part(float& M, float& l, float& o, float M
   M = Mn;
 }
 
-// bf16 sink and recent tokens of segment (h, b): 4 warps take every 4th token, lane l holds
-// channels 2l, 2l+1 and their RoPE partners; returns the window's partial for channel `at`.
+// bf16 sink and recent tokens of segment (h, b): 4 warps take every 4th token, two tokens per
+// step with their loads issued together; lane l holds channels 2l, 2l+1 and their RoPE
+// partners. Returns the window's partial for channel `at`.
 __device__ void aux_window(const VqAttnArgs& a, int h, int b, int L, int NP, float scale_log2, float* wp, int at,
                            float& Mo, float& lo_, float& oo) {
   const int aw = at >> 5, lane = at & 31;

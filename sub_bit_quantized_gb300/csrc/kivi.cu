@@ -588,7 +588,12 @@ struct AttnLayout {
   // float l [8 warps][RH], float M [8 warps][RH], int flag, int released [stages], int issued
   static constexpr int kOffRed = kOffBias + RH * 8 * 4;
   static constexpr int kOffBar = kOffRed + ((2 * kAWarps * RH + 2 + kAStages) * 4 + 15) / 16 * 16;  // mbarriers + failed
-  static constexpr int kSmem = kOffBar + 64;
+  // four query heads over 4-bit keys: the scores are a tensor-core product (score_mma), its
+  // q' operand in the q' area in fragment order, and each warp's [16 tokens][4 heads] scores
+  // pass through kOffS to the lanes that own the tokens
+  static constexpr bool kMma = (RH == 4 && KB == 4);
+  static constexpr int kOffS = kOffBar + 64;
+  static constexpr int kSmem = kOffS + (kMma ? kAWarps * 16 * RH * 4 : 0);
   // value phase: a lane takes kLW code words of one token, all in one value group (with one
   // query head the whole group, so its scale and zero-point are read once); a warp-step
   // covers kTS tokens
@@ -686,6 +691,23 @@ __device__ __forceinline__ int qpair_index(int c, int& j) {
   const int k = c / kCPW, p = c % kCPW;
   j = p % kP;
   return 2 * (k * kP + j) + p / kP;
+}
+
+// D += A B for one m16n8k16 tile: fp16 A (16 x 16, row-major) and B (16 x 8, column-major)
+// fragments, fp32 accumulators (the warp-wide tensor-core product of this architecture's
+// instruction set; a 16-token x 8-head tile is below the smallest tcgen05 shape)
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Byte t of a word of 4-bit key codes (channels 2t and 2t + 1 of the word) as an fp16 pair:
+// the low code as the bit pattern c0 (the fp16 subnormal c0 2^-24), the high one as 16 c1
+// (16 c1 2^-24; the 16 is folded into the q' of odd channels). Exact, two instructions.
+__device__ __forceinline__ uint32_t code_byte_f16x2(uint32_t w, uint32_t sel) {
+  return __byte_perm(w, 0u, sel) & 0x00F0000Fu;
 }
 
 __device__ __forceinline__ bool kivi_wait(uint64_t* bar, uint32_t parity, volatile int* failed, int* err) {
@@ -838,9 +860,22 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
 #pragma unroll
           for (int r = 0; r < RH; ++r) {
             const float qa = qs[r * kD + ch] * sa, qb = qs[r * kD + ch + 1] * sb;
-            float* qr = qf + (r * 4 + g) * kD + 64 * hf;
-            qr[ia] = qa * pow2_neg(KB * ja);
-            qr[ib] = qb * pow2_neg(KB * jb);
+            if constexpr (L::kMma) {
+              // B fragment of k-step ch / 16 for head r: channels (ch, ch + 1) are one fp16 pair
+              // of thread (r, (ch % 8) / 2), register (ch % 16) / 8; q' = hi + lo in fp16, the odd
+              // channel's q' over 16
+              const float qo = qb * 0.0625f;
+              const __half he = __float2half_rn(qa), ho = __float2half_rn(qo);
+              const __half le = __float2half_rn(qa - __half2float(he)), lo = __float2half_rn(qo - __half2float(ho));
+              const int kk = ch >> 4, thr = r * 4 + ((ch & 7) >> 1), reg = (ch >> 3) & 1;
+              uint32_t* qbf = reinterpret_cast<uint32_t*>(qf) + g * (2 * 8 * 16 * 2);
+              qbf[((0 * 8 + kk) * 16 + thr) * 2 + reg] = (uint32_t)__half_as_ushort(he) | ((uint32_t)__half_as_ushort(ho) << 16);
+              qbf[((1 * 8 + kk) * 16 + thr) * 2 + reg] = (uint32_t)__half_as_ushort(le) | ((uint32_t)__half_as_ushort(lo) << 16);
+            } else {
+              float* qr = qf + (r * 4 + g) * kD + 64 * hf;
+              qr[ia] = qa * pow2_neg(KB * ja);
+              qr[ib] = qb * pow2_neg(KB * jb);
+            }
             float pb = -(qa * za + qb * zb);
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) pb += __shfl_xor_sync(0xFFFFFFFFu, pb, off);
@@ -850,7 +885,62 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
         pair_sync(g);  // both halves written
         // ---- scores: lanes 0-15 channels 0-63 of token tb + lane, lanes 16-31 channels 64-127 ----
         float pk[RH];
-        {
+        if constexpr (L::kMma) {
+          // scores[16 tokens][4 heads] = codes[16 x 128] . q'[128 x 4] on the tensor cores: the
+          // A fragments come straight from the code bytes (tokens tb + g8 and tb + g8 + 8, byte
+          // t4 of every code word), the B fragments from the q' area; heads 4..7 of the n = 8
+          // tile are zero. Scores reach the lanes of their tokens through the warp's kOffS area.
+          const int g8 = lane >> 2, t4 = lane & 3;
+          const uint32_t sel = (uint32_t)t4 * 0x101u + 0x4040u;
+          const unsigned char* rowa = stage + L::kCKc + (tb + g8) * L::kKRow;
+          const unsigned char* rowb = rowa + 8 * L::kKRow;
+          const uint32_t* qbf = reinterpret_cast<const uint32_t*>(qf) + g * (2 * 8 * 16 * 2);
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int w4 = 0; w4 < 4; ++w4) {  // words 4 w4 .. 4 w4 + 3 of both rows: k-steps 2 w4, 2 w4 + 1
+            const uint4 ua = *reinterpret_cast<const uint4*>(rowa + 16 * w4);
+            const uint4 ub = *reinterpret_cast<const uint4*>(rowb + 16 * w4);
+            const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int kk = 2 * w4 + h;
+              const uint32_t af[4] = {code_byte_f16x2(wa[2 * h], sel), code_byte_f16x2(wb[2 * h], sel),
+                                      code_byte_f16x2(wa[2 * h + 1], sel), code_byte_f16x2(wb[2 * h + 1], sel)};
+              uint32_t bh0 = 0, bh1 = 0, bl0 = 0, bl1 = 0;
+              if (g8 < 4) {
+                const uint2 h2 = *reinterpret_cast<const uint2*>(qbf + ((0 * 8 + kk) * 16 + g8 * 4 + t4) * 2);
+                const uint2 l2 = *reinterpret_cast<const uint2*>(qbf + ((1 * 8 + kk) * 16 + g8 * 4 + t4) * 2);
+                bh0 = h2.x; bh1 = h2.y; bl0 = l2.x; bl1 = l2.y;
+              }
+              mma_16816(acc, af, bh0, bh1);
+              mma_16816(acc, af, bl0, bl1);
+            }
+          }
+          float* ss = reinterpret_cast<float*>(sma + L::kOffS) + warp * 16 * RH;
+          if (t4 < 2) {  // heads 2 t4, 2 t4 + 1 of tokens g8, g8 + 8 (x 2^24: the codes' fp16 scale)
+            ss[g8 * RH + 2 * t4] = acc[0] * 16777216.f;
+            ss[g8 * RH + 2 * t4 + 1] = acc[1] * 16777216.f;
+            ss[(g8 + 8) * RH + 2 * t4] = acc[2] * 16777216.f;
+            ss[(g8 + 8) * RH + 2 * t4 + 1] = acc[3] * 16777216.f;
+          }
+          __syncwarp();
+          const float4 sv4 = *reinterpret_cast<const float4*>(ss + (lane & 15) * RH);
+          const float raw[4] = {sv4.x, sv4.y, sv4.z, sv4.w};
+          __syncwarp();  // read before the next chunk overwrites it
+#pragma unroll
+          for (int r = 0; r < RH; ++r) {
+            const float sc_r = (raw[r] + bias[(r * 4 + g) * 2] + bias[(r * 4 + g) * 2 + 1]) * scale_log2;
+            float mx = sc_r;
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+            if (mx > M[r] + 8.f) rescale_to(r, mx);
+            pk[r] = exp2f(sc_r - M[r]);
+            float ls = pk[r];
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, off);
+            l[r] += ls;
+          }
+        } else {
           uint32_t wds[L::kKW];
 #pragma unroll
           for (int k4 = 0; k4 < L::kKW / 4; ++k4) {

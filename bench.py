@@ -397,8 +397,8 @@ PROFILED_TRAFFIC = {
         245814528 + 3427328),
     "kivi_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "f9a971efd8ea1d5d4c32f9fcda3c4b12e017e1e4b6780049d481c08c1c92b352",
-        228799232 + 3666176),
+        "521339451b682f8cc3bc58471609fe7e93c5b2478920cf6a70150ff11db57d06",
+        228778496 + 3532800),
     "encode_32k:encode_tc_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_encode_tc.cu",
         "42e194feda74fa6a5e78177d6a39c04b4785de3db0db60096413109cc4b1cd1a",
@@ -406,12 +406,12 @@ PROFILED_TRAFFIC = {
     # both quantize launches (keys per channel, values per token) of one step
     "kivi_quant_32k:kivi_quant_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "f9a971efd8ea1d5d4c32f9fcda3c4b12e017e1e4b6780049d481c08c1c92b352",
-        135000064 + 14761728 + 134275328 + 12550912),
+        "521339451b682f8cc3bc58471609fe7e93c5b2478920cf6a70150ff11db57d06",
+        134274560 + 9310720 + 134305792 + 6611456),
     "kivi4_gqa_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "f9a971efd8ea1d5d4c32f9fcda3c4b12e017e1e4b6780049d481c08c1c92b352",
-        89879040 + 2842624),
+        "521339451b682f8cc3bc58471609fe7e93c5b2478920cf6a70150ff11db57d06",
+        89872896 + 2462464),
 }
 
 

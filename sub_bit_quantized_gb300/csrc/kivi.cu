@@ -555,8 +555,10 @@ __global__ void __launch_bounds__(128) kivi_append_kernel(const KiviAppendArgs a
 // subgroups are adjacent in launch order so their code reads meet in L2. A quantized split
 // streams its tokens through a 3- or 4-stage shared-memory ring of 128-token chunks (TMA bulk
 // copies of the chunk's key codes, key scales and zeros, value codes, value scales and
-// zeros); each warp keeps its own online softmax per query head over its 16 tokens of every
-// chunk, and the block merges the warps at the end. Tokens whose key is quantized but whose
+// zeros); each warp takes 16 tokens of every chunk, computes their scores (for RH > 1 heads
+// as a tensor-core product per key group: fp16 code fragments against q' = q s split into
+// fp16 high and low parts; for one head on the CUDA cores), keeps its own online softmax per
+// query head, and sums the values on the CUDA cores; the block merges the warps at the end. Tokens whose key is quantized but whose
 // value is still in the fp16 window (the streaming cache's tail) take the value from the
 // window. Partials of all splits merge exactly in the last block of a (request, subgroup) to
 // finish (arrival counter, no spin-wait).
@@ -583,15 +585,22 @@ struct AttnLayout {
   static constexpr int kCVz = kCVs + kAChunk * 4 * 2;
   static constexpr int kStage = kCVz + kAChunk * 4 * 2;
   static constexpr int kOffQ = kAStages * kStage;         // float q [RH][128]
-  static constexpr int kOffQf = kOffQ + RH * kD * 4;      // float q' [RH][4 groups][128]
+  static constexpr int kOffQf = kOffQ + RH * kD * 4;      // q' B fragments, 4 groups x kQfWords
   static constexpr int kOffBias = kOffQf + RH * 4 * kD * 4;  // float [RH][4 groups][2 halves]
   // float l [8 warps][RH], float M [8 warps][RH], int flag, int released [stages], int issued
   static constexpr int kOffRed = kOffBias + RH * 8 * 4;
   static constexpr int kOffBar = kOffRed + ((2 * kAWarps * RH + 2 + kAStages) * 4 + 15) / 16 * 16;  // mbarriers + failed
-  // four query heads over 4-bit keys: the scores are a tensor-core product (score_mma), its
-  // q' operand in the q' area in fragment order, and each warp's [16 tokens][4 heads] scores
-  // pass through kOffS to the lanes that own the tokens
-  static constexpr bool kMma = (RH == 4 && KB == 4);
+  // With grouped heads the scores are a tensor-core product (with one head the CUDA-core
+  // path, below, measured faster): the q' area holds each key group's B fragments
+  // ([k-step pair][kNC columns][4 threads][k-step parity][2 registers] words, so a thread
+  // loads two k-steps with one 16-byte read; head r's high q' parts in column 2 r, its low
+  // parts in 2 r + 1), and each warp's [16 tokens][RH heads] scores pass through
+  // kOffS to the lanes that own the tokens
+  static constexpr int kNC = 2 * RH;                      // B columns in use (of 8)
+  static constexpr int kQfWords = 8 * kNC * 4 * 2;        // per key group (= RH 128 floats)
+  static_assert(KB == 2 || KB == 4, "2- or 4-bit keys");
+  static constexpr int kWPS = 16 * KB / 32;               // code words per 16-channel k-step
+  static constexpr bool kMma = RH > 1;
   static constexpr int kOffS = kOffBar + 64;
   static constexpr int kSmem = kOffS + (kMma ? kAWarps * 16 * RH * 4 : 0);
   // value phase: a lane takes kLW code words of one token, all in one value group (with one
@@ -605,7 +614,7 @@ struct AttnLayout {
   static constexpr int kLPT = kVW / kLW;                  // lanes per token
   static constexpr int kTS = 32 / kLPT;                   // tokens per warp-step
   static constexpr int kOV = kLW * kCPWv;                 // value accumulators per lane and head
-  // score phase: a lane covers 64 channels of one token
+  // one-head score phase: a lane covers 64 channels of one token
   static constexpr int kKW = kKRow / 8;                   // key code words per half token
   static constexpr int kPK = 16 / KB;                     // channel pairs per key word
   static_assert(kStage % 128 == 0 && kOffBar % 8 == 0, "alignment");
@@ -703,11 +712,30 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// Byte t of a word of 4-bit key codes (channels 2t and 2t + 1 of the word) as an fp16 pair:
-// the low code as the bit pattern c0 (the fp16 subnormal c0 2^-24), the high one as 16 c1
-// (16 c1 2^-24; the 16 is folded into the q' of odd channels). Exact, two instructions.
-__device__ __forceinline__ uint32_t code_byte_f16x2(uint32_t w, uint32_t sel) {
-  return __byte_perm(w, 0u, sel) & 0x00F0000Fu;
+// The A fragments of one 16-channel k-step from the code words of two token rows (wa: row
+// g8, wb: row g8 + 8; kWPS words each), thread t4 taking byte t4 of each word. A code c at
+// bit k of a 16-bit half reads as the fp16 subnormal c 2^(k-24), exact, so every register is
+// one byte permute (sel puts byte t4 under both halves) and one AND; the 2^k is folded into
+// that channel's q'.
+//   4-bit: byte t4 of word 0 (1) holds channels 2 t4, 2 t4 + 1 (+ 8) as (c, 16 c): k-step
+//          columns 2 t4, 2 t4 + 1 (+ 8) are the channels in order.
+//   2-bit: byte t4 of the word holds channels 4 t4 .. 4 t4 + 3 as (c, 4 c) and (16 c, 64 c):
+//          columns 2 t4, 2 t4 + 1 are channels 4 t4, 4 t4 + 1, columns 2 t4 + 8, 2 t4 + 9
+//          channels 4 t4 + 2, 4 t4 + 3.
+template <int KB>
+__device__ __forceinline__ void code_frag(const uint32_t* wa, const uint32_t* wb, uint32_t sel, uint32_t (&af)[4]) {
+  if constexpr (KB == 4) {
+    af[0] = __byte_perm(wa[0], 0u, sel) & 0x00F0000Fu;
+    af[1] = __byte_perm(wb[0], 0u, sel) & 0x00F0000Fu;
+    af[2] = __byte_perm(wa[1], 0u, sel) & 0x00F0000Fu;
+    af[3] = __byte_perm(wb[1], 0u, sel) & 0x00F0000Fu;
+  } else {
+    const uint32_t pa = __byte_perm(wa[0], 0u, sel), pb = __byte_perm(wb[0], 0u, sel);
+    af[0] = pa & 0x000C0003u;
+    af[1] = pb & 0x000C0003u;
+    af[2] = pa & 0x00C00030u;
+    af[3] = pb & 0x00C00030u;
+  }
 }
 
 __device__ __forceinline__ bool kivi_wait(uint64_t* bar, uint32_t parity, volatile int* failed, int* err) {
@@ -855,22 +883,30 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
           const uint32_t s2 = *reinterpret_cast<const uint32_t*>(stage + L::kCKs + (g * kD + ch) * 2);
           const uint32_t z2 = *reinterpret_cast<const uint32_t*>(stage + L::kCKz + (g * kD + ch) * 2);
           const float sa = h2f(s2 & 0xFFFFu), sb = h2f(s2 >> 16), za = h2f(z2 & 0xFFFFu), zb = h2f(z2 >> 16);
+          // tensor-core scores: channels (ch, ch + 1) are one fp16 pair of the B fragments of
+          // k-step ch / 16 (thread t4, register reg), each channel's q' divided by the power of
+          // two its code carries in the A fragment (code_frag); CUDA-core scores: q' in the
+          // code-pair order of a 64-channel half, divided by 2^(b j)
+          int t4 = 0, reg = 0;
+          float fa = 1.f, fb = 1.f;
+          if constexpr (L::kMma && KB == 4) {
+            t4 = (ch & 7) >> 1, reg = (ch >> 3) & 1, fb = 0.0625f;
+          } else if constexpr (L::kMma) {
+            t4 = (ch & 15) >> 2, reg = (ch >> 1) & 1, fa = reg ? 0.0625f : 1.f, fb = reg ? 0.015625f : 0.25f;
+          }
+          const int kk = ch >> 4;
+          uint32_t* qbf = reinterpret_cast<uint32_t*>(qf) + g * L::kQfWords + ((kk >> 1) * L::kNC * 4 + t4) * 4 + (kk & 1) * 2 + reg;
           int ja, jb;
           const int ia = qpair_index<KB>(ch & 63, ja), ib = qpair_index<KB>((ch + 1) & 63, jb);
 #pragma unroll
           for (int r = 0; r < RH; ++r) {
             const float qa = qs[r * kD + ch] * sa, qb = qs[r * kD + ch + 1] * sb;
-            if constexpr (L::kMma) {
-              // B fragment of k-step ch / 16 for head r: channels (ch, ch + 1) are one fp16 pair
-              // of thread (r, (ch % 8) / 2), register (ch % 16) / 8; q' = hi + lo in fp16, the odd
-              // channel's q' over 16
-              const float qo = qb * 0.0625f;
-              const __half he = __float2half_rn(qa), ho = __float2half_rn(qo);
-              const __half le = __float2half_rn(qa - __half2float(he)), lo = __float2half_rn(qo - __half2float(ho));
-              const int kk = ch >> 4, thr = r * 4 + ((ch & 7) >> 1), reg = (ch >> 3) & 1;
-              uint32_t* qbf = reinterpret_cast<uint32_t*>(qf) + g * (2 * 8 * 16 * 2);
-              qbf[((0 * 8 + kk) * 16 + thr) * 2 + reg] = (uint32_t)__half_as_ushort(he) | ((uint32_t)__half_as_ushort(ho) << 16);
-              qbf[((1 * 8 + kk) * 16 + thr) * 2 + reg] = (uint32_t)__half_as_ushort(le) | ((uint32_t)__half_as_ushort(lo) << 16);
+            if constexpr (L::kMma) {  // q' = hi + lo in fp16: column 2 r holds the high parts, 2 r + 1 the low
+              const float qe = qa * fa, qo = qb * fb;
+              const __half he = __float2half_rn(qe), ho = __float2half_rn(qo);
+              const __half le = __float2half_rn(qe - __half2float(he)), lo = __float2half_rn(qo - __half2float(ho));
+              qbf[(2 * r) * 4 * 4] = (uint32_t)__half_as_ushort(he) | ((uint32_t)__half_as_ushort(ho) << 16);
+              qbf[(2 * r + 1) * 4 * 4] = (uint32_t)__half_as_ushort(le) | ((uint32_t)__half_as_ushort(lo) << 16);
             } else {
               float* qr = qf + (r * 4 + g) * kD + 64 * hf;
               qr[ia] = qa * pow2_neg(KB * ja);
@@ -885,62 +921,50 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
         pair_sync(g);  // both halves written
         // ---- scores: lanes 0-15 channels 0-63 of token tb + lane, lanes 16-31 channels 64-127 ----
         float pk[RH];
+        float raw[RH];  // the 16 tokens' dot products q' . codes, lanes l and l + 16 holding token l
         if constexpr (L::kMma) {
-          // scores[16 tokens][4 heads] = codes[16 x 128] . q'[128 x 4] on the tensor cores: the
-          // A fragments come straight from the code bytes (tokens tb + g8 and tb + g8 + 8, byte
-          // t4 of every code word), the B fragments from the q' area; heads 4..7 of the n = 8
-          // tile are zero. Scores reach the lanes of their tokens through the warp's kOffS area.
+          // scores[16 tokens][RH heads] = codes[16 x 128] . q'[128 x RH] on the tensor cores, one
+          // m16n8k16 product per 16 channels: the A fragments come straight from the code bytes
+          // (tokens tb + g8 and tb + g8 + 8, byte t4 of the k-step's words), the B fragments from
+          // the q' area; column 2 r holds head r's high q' parts and 2 r + 1 its low parts, so
+          // thread (g8, t4 < RH) ends with head t4's two partial sums of both tokens. Scores reach
+          // the lanes of their tokens through the warp's kOffS area.
           const int g8 = lane >> 2, t4 = lane & 3;
           const uint32_t sel = (uint32_t)t4 * 0x101u + 0x4040u;
           const unsigned char* rowa = stage + L::kCKc + (tb + g8) * L::kKRow;
           const unsigned char* rowb = rowa + 8 * L::kKRow;
-          const uint32_t* qbf = reinterpret_cast<const uint32_t*>(qf) + g * (2 * 8 * 16 * 2);
+          const uint32_t* qbf = reinterpret_cast<const uint32_t*>(qf) + g * L::kQfWords + (g8 * 4 + t4) * 4;
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int w4 = 0; w4 < 4; ++w4) {  // words 4 w4 .. 4 w4 + 3 of both rows: k-steps 2 w4, 2 w4 + 1
+          for (int w4 = 0; w4 < L::kKRow / 16; ++w4) {  // 4 code words of both rows
             const uint4 ua = *reinterpret_cast<const uint4*>(rowa + 16 * w4);
             const uint4 ub = *reinterpret_cast<const uint4*>(rowb + 16 * w4);
             const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int kk = 2 * w4 + h;
-              const uint32_t af[4] = {code_byte_f16x2(wa[2 * h], sel), code_byte_f16x2(wb[2 * h], sel),
-                                      code_byte_f16x2(wa[2 * h + 1], sel), code_byte_f16x2(wb[2 * h + 1], sel)};
-              uint32_t bh0 = 0, bh1 = 0, bl0 = 0, bl1 = 0;
-              if (g8 < 4) {
-                const uint2 h2 = *reinterpret_cast<const uint2*>(qbf + ((0 * 8 + kk) * 16 + g8 * 4 + t4) * 2);
-                const uint2 l2 = *reinterpret_cast<const uint2*>(qbf + ((1 * 8 + kk) * 16 + g8 * 4 + t4) * 2);
-                bh0 = h2.x; bh1 = h2.y; bl0 = l2.x; bl1 = l2.y;
-              }
-              mma_16816(acc, af, bh0, bh1);
-              mma_16816(acc, af, bl0, bl1);
+            for (int h2 = 0; h2 < 2 / L::kWPS; ++h2) {  // k-steps kk, kk + 1: one B load
+              const int kk = (4 / L::kWPS) * w4 + 2 * h2;
+              uint4 bq = make_uint4(0u, 0u, 0u, 0u);
+              if (g8 < L::kNC) bq = *reinterpret_cast<const uint4*>(qbf + (kk >> 1) * L::kNC * 4 * 4);
+              uint32_t af[4];
+              code_frag<KB>(wa + L::kWPS * 2 * h2, wb + L::kWPS * 2 * h2, sel, af);
+              mma_16816(acc, af, bq.x, bq.y);
+              code_frag<KB>(wa + L::kWPS * (2 * h2 + 1), wb + L::kWPS * (2 * h2 + 1), sel, af);
+              mma_16816(acc, af, bq.z, bq.w);
             }
           }
           float* ss = reinterpret_cast<float*>(sma + L::kOffS) + warp * 16 * RH;
-          if (t4 < 2) {  // heads 2 t4, 2 t4 + 1 of tokens g8, g8 + 8 (x 2^24: the codes' fp16 scale)
-            ss[g8 * RH + 2 * t4] = acc[0] * 16777216.f;
-            ss[g8 * RH + 2 * t4 + 1] = acc[1] * 16777216.f;
-            ss[(g8 + 8) * RH + 2 * t4] = acc[2] * 16777216.f;
-            ss[(g8 + 8) * RH + 2 * t4 + 1] = acc[3] * 16777216.f;
+          if (t4 < RH) {  // head t4 of tokens g8, g8 + 8 (x 2^24: the codes' fp16 scale)
+            ss[g8 * RH + t4] = (acc[0] + acc[1]) * 16777216.f;
+            ss[(g8 + 8) * RH + t4] = (acc[2] + acc[3]) * 16777216.f;
           }
           __syncwarp();
-          const float4 sv4 = *reinterpret_cast<const float4*>(ss + (lane & 15) * RH);
-          const float raw[4] = {sv4.x, sv4.y, sv4.z, sv4.w};
+#pragma unroll
+          for (int r = 0; r < RH; ++r) raw[r] = ss[(lane & 15) * RH + r];
           __syncwarp();  // read before the next chunk overwrites it
-#pragma unroll
-          for (int r = 0; r < RH; ++r) {
-            const float sc_r = (raw[r] + bias[(r * 4 + g) * 2] + bias[(r * 4 + g) * 2 + 1]) * scale_log2;
-            float mx = sc_r;
-#pragma unroll
-            for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-            if (mx > M[r] + 8.f) rescale_to(r, mx);
-            pk[r] = exp2f(sc_r - M[r]);
-            float ls = pk[r];
-#pragma unroll
-            for (int off = 8; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, off);
-            l[r] += ls;
-          }
         } else {
+          // one head: lanes 0-15 take channels 0-63 of token tb + lane, lanes 16-31 channels
+          // 64-127; a byte permute per code word puts the codes under the exponent of 2^23, then
+          // one AND per code, one packed add and one packed FMA per code pair
           uint32_t wds[L::kKW];
 #pragma unroll
           for (int k4 = 0; k4 < L::kKW / 4; ++k4) {
@@ -966,25 +990,28 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
               }
             }
           }
-          // ---- warp-local online softmax over the 16 tokens (lanes l and l + 16 share one) ----
 #pragma unroll
           for (int r = 0; r < RH; ++r) {
-            float sc_r = acc2[r].x + acc2[r].y;
-            sc_r += __shfl_xor_sync(0xFFFFFFFFu, sc_r, 16);
-            sc_r = (sc_r + bias[(r * 4 + g) * 2] + bias[(r * 4 + g) * 2 + 1]) * scale_log2;
-            float mx = sc_r;
-#pragma unroll
-            for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-            // the running maximum is raised only when a score passes it by more than 2^8 (or on
-            // the first chunk): weights stay below 256, the sums exact relative to M, and most
-            // chunks skip the rescale (warp-uniform)
-            if (mx > M[r] + 8.f) rescale_to(r, mx);
-            pk[r] = exp2f(sc_r - M[r]);
-            float ls = pk[r];
-#pragma unroll
-            for (int off = 8; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, off);
-            l[r] += ls;
+            raw[r] = acc2[r].x + acc2[r].y;
+            raw[r] += __shfl_xor_sync(0xFFFFFFFFu, raw[r], 16);
           }
+        }
+        // ---- warp-local online softmax over the 16 tokens (lanes l and l + 16 share one) ----
+#pragma unroll
+        for (int r = 0; r < RH; ++r) {
+          const float sc_r = (raw[r] + bias[(r * 4 + g) * 2] + bias[(r * 4 + g) * 2 + 1]) * scale_log2;
+          float mx = sc_r;
+#pragma unroll
+          for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+          // the running maximum is raised only when a score passes it by more than 2^8 (or on
+          // the first chunk): weights stay below 256, the sums exact relative to M, and most
+          // chunks skip the rescale (warp-uniform)
+          if (mx > M[r] + 8.f) rescale_to(r, mx);
+          pk[r] = exp2f(sc_r - M[r]);
+          float ls = pk[r];
+#pragma unroll
+          for (int off = 8; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, off);
+          l[r] += ls;
         }
         // ---- values: kTS tokens of the warp per step ----
         // kFull: every token of the warp has a quantized value, so the steps need no per-token

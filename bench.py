@@ -397,21 +397,21 @@ PROFILED_TRAFFIC = {
         245814528 + 3427328),
     "kivi_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "521339451b682f8cc3bc58471609fe7e93c5b2478920cf6a70150ff11db57d06",
-        228778496 + 3532800),
+        "72bbd6a23beb3d4ecbaed9f57fa2a03fe82b3992461aa8f74b8e5e7f5adcd620",
+        228777728 + 3210240),
     "encode_32k:encode_tc_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_encode_tc.cu",
-        "42e194feda74fa6a5e78177d6a39c04b4785de3db0db60096413109cc4b1cd1a",
-        287192064 + 14977024),
+        "8f4d7c4d56f8e4813997994084beadad628c36cd5447f2bd11be519377daa3e4",
+        287095296 + 14688512),
     # both quantize launches (keys per channel, values per token) of one step
     "kivi_quant_32k:kivi_quant_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "521339451b682f8cc3bc58471609fe7e93c5b2478920cf6a70150ff11db57d06",
-        134274560 + 9310720 + 134305792 + 6611456),
+        "72bbd6a23beb3d4ecbaed9f57fa2a03fe82b3992461aa8f74b8e5e7f5adcd620",
+        134274304 + 9315584 + 134291712 + 6603776),
     "kivi4_gqa_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "521339451b682f8cc3bc58471609fe7e93c5b2478920cf6a70150ff11db57d06",
-        89872896 + 2462464),
+        "72bbd6a23beb3d4ecbaed9f57fa2a03fe82b3992461aa8f74b8e5e7f5adcd620",
+        89870080 + 2205952),
 }
 
 

@@ -575,6 +575,10 @@ struct AttnLayout {
   // codes (64 registers), three otherwise, two for 2-bit values with four heads (64
   // accumulators a thread)
   static constexpr int kMinBlocks = (RH == 1) ? ((KB + VB == 4) ? 4 : 3) : (VB == 2 && RH == 4) ? 2 : 3;
+  // log2 headroom of each warp's running maximum: weights p = exp2(s - M) stay below
+  // 2^kSlack. One head rounds its value weights p s_v to fp16, so p <= 4 keeps |p s_v| <=
+  // 4 (131008 / 15) < 65504 for any fp16 values; grouped heads keep their weights in fp32
+  static constexpr float kSlack = (RH == 1) ? 2.f : 8.f;
   static constexpr int kKRow = kD * KB / 8;               // key code bytes per token
   static constexpr int kVRow = kD * VB / 8;               // value code bytes per token
   static constexpr int kCKc = 0;                          // stage layout (bytes)
@@ -666,6 +670,17 @@ __device__ __forceinline__ void fma_f16x2(float& a0, float& a1, uint32_t m, uint
       "fma.rn.f32.f16 %1, h, p, %1;\n\t}"
       : "+f"(a0), "+f"(a1)
       : "r"(m), "r"(wh));
+}
+// a (low 16 bits, fp16) x b (low 16 bits, fp16) + c, product and sum in fp32
+__device__ __forceinline__ float fma_f16_f32(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 x, y;\n\t"
+      "cvt.u16.u32 x, %1;\n\t"
+      "cvt.u16.u32 y, %2;\n\t"
+      "fma.rn.f32.f16 %0, x, y, %3;\n\t}"
+      : "=f"(d)
+      : "r"(a), "r"(b), "f"(c));
+  return d;
 }
 template <bool B>
 struct BoolTag {
@@ -1003,10 +1018,10 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
           float mx = sc_r;
 #pragma unroll
           for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-          // the running maximum is raised only when a score passes it by more than 2^8 (or on
-          // the first chunk): weights stay below 256, the sums exact relative to M, and most
-          // chunks skip the rescale (warp-uniform)
-          if (mx > M[r] + 8.f) rescale_to(r, mx);
+          // the running maximum is raised only when a score passes it by more than kSlack (or
+          // on the first chunk): the sums stay exact relative to M, and most chunks skip the
+          // rescale (warp-uniform)
+          if (mx > M[r] + L::kSlack) rescale_to(r, mx);
           pk[r] = exp2f(sc_r - M[r]);
           float ls = pk[r];
 #pragma unroll
@@ -1027,13 +1042,14 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
             if (kFull || tc0 + tv < NQV) {
               uint32_t wv[L::kLW];
               load_words<L::kLW>(stage + L::kCVc + tv * L::kVRow + 4 * w0, wv);
-              const float sv = h2f(*reinterpret_cast<const uint16_t*>(stage + L::kCVs + (tv * 4 + gv) * 2));
-              const float zv = h2f(*reinterpret_cast<const uint16_t*>(stage + L::kCVz + (tv * 4 + gv) * 2));
+              const uint32_t svh = *reinterpret_cast<const uint16_t*>(stage + L::kCVs + (tv * 4 + gv) * 2);
+              const uint32_t zvh = *reinterpret_cast<const uint16_t*>(stage + L::kCVz + (tv * 4 + gv) * 2);
               if constexpr (RH == 1) {
-                // the zero-point term takes the same fp16-rounded weight as the codes
-                const __half wgt = __float2half_rn(p[0] * sv);
-                oz[0] = fmaf(__half2float(wgt), zv, oz[0]);
+                // the weight fp16(p) x s_v in one half multiply (p <= 2^kSlack); the zero-point
+                // term takes the same rounded weight, through the mixed-precision FMA
+                const __half wgt = __hmul(__float2half_rn(p[0]), __ushort_as_half((unsigned short)svh));
                 const uint32_t wh = __half_as_ushort(wgt);
+                oz[0] = fma_f16_f32(wh, zvh, oz[0]);
                 constexpr int kSp = HalfCodes<VB>::kSplit;
 #pragma unroll
                 for (int w = 0; w < L::kLW; ++w) {
@@ -1047,6 +1063,7 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
                   }
                 }
               } else {
+                const float sv = h2f(svh), zv = h2f(zvh);
                 float2 w2[RH];
 #pragma unroll
                 for (int r = 0; r < RH; ++r) {
@@ -1132,7 +1149,7 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
         float mx = sc_r;
 #pragma unroll
         for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-        if (mx > M[r] + 8.f) rescale_to(r, mx);  // warp-uniform; token tw is valid
+        if (mx > M[r] + L::kSlack) rescale_to(r, mx);  // warp-uniform; token tw is valid
         pk[r] = valid ? exp2f(sc_r - M[r]) : 0.f;
         float ls = pk[r];
 #pragma unroll

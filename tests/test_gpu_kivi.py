@@ -144,8 +144,8 @@ def test_attention_segments_and_splits(n_splits):
     check_all(case, run(case, C.fill_kivi_cache(case), n_splits).cpu().numpy())
 
 
-@pytest.mark.parametrize("k_bits,v_bits,rep", [(2, 2, 1), (4, 4, 1), (2, 4, 2), (4, 2, 4), (4, 4, 4), (2, 2, 8),
-                                               (4, 4, 3)])
+@pytest.mark.parametrize("k_bits,v_bits,rep", [(2, 2, 1), (4, 4, 1), (2, 4, 2), (4, 2, 2), (4, 2, 4), (4, 4, 4),
+                                               (2, 2, 8), (4, 4, 3)])
 def test_attention_bits_and_gqa(k_bits, v_bits, rep):
     # query head h reads KV head h // rep; one block serves up to four query heads
     case = C.make_kivi_case(313 + rep, B=3, H=2, Hq=2 * rep, k_bits=k_bits, v_bits=v_bits,

@@ -579,6 +579,12 @@ struct AttnLayout {
   // 2^kSlack. One head rounds its value weights p s_v to fp16, so p <= 4 keeps |p s_v| <=
   // 4 (131008 / 15) < 65504 for any fp16 values; grouped heads keep their weights in fp32
   static constexpr float kSlack = (RH == 1) ? 2.f : 8.f;
+  // tokens a warp takes of a chunk it works on: with one head a whole 32-token key group
+  // (warps 0-3 on even chunks, 4-7 on odd ones), so a warp builds its group's q' alone and
+  // no pair of warps meets; with grouped heads 16, the m16n8k16 tile's rows
+  static constexpr int kTPW = (RH == 1) ? 32 : 16;
+  static constexpr int kWPC = kAChunk / kTPW;             // warps per chunk
+  static constexpr int kNPar = kAThreads / 32 / kWPC;     // chunk parities
   static constexpr int kKRow = kD * KB / 8;               // key code bytes per token
   static constexpr int kVRow = kD * VB / 8;               // value code bytes per token
   static constexpr int kCKc = 0;                          // stage layout (bytes)
@@ -589,8 +595,10 @@ struct AttnLayout {
   static constexpr int kCVz = kCVs + kAChunk * 4 * 2;
   static constexpr int kStage = kCVz + kAChunk * 4 * 2;
   static constexpr int kOffQ = kAStages * kStage;         // float q [RH][128]
-  static constexpr int kOffQf = kOffQ + RH * kD * 4;      // q' B fragments, 4 groups x kQfWords
-  static constexpr int kOffBias = kOffQf + RH * 4 * kD * 4;  // float [RH][4 groups][2 halves]
+  // q': with grouped heads the B fragments of the 4 key groups (4 x kQfWords words); with one
+  // head a float [128] per warp (each warp takes a whole key group, below)
+  static constexpr int kOffQf = kOffQ + RH * kD * 4;
+  static constexpr int kOffBias = kOffQf + ((RH == 1) ? kAThreads / 32 : RH * 4) * kD * 4;  // float [RH][4 groups][2 halves]
   // float l [8 warps][RH], float M [8 warps][RH], int flag, int released [stages], int issued
   static constexpr int kOffRed = kOffBias + RH * 8 * 4;
   static constexpr int kOffBar = kOffRed + ((2 * kAWarps * RH + 2 + kAStages) * 4 + 15) / 16 * 16;  // mbarriers + failed
@@ -877,55 +885,73 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
       *issued = min(L::kAStages, n_chunks);
     }
 
-    // Every warp works on its 16 tokens of each chunk (half of one key group) with a
-    // warp-local online softmax; the two warps of a group share its q' and bias (each builds
-    // one channel half; a 64-thread named barrier per pair before and after), warps meet only
-    // at the end, and the last warp done with a stage refills it.
-    const int tb = 16 * warp, g = warp >> 1, hf = warp & 1;
-    const int tk = tb + (lane & 15), chh = lane >> 4;  // score phase: token, channel half
-    for (int c = 0; c < n_chunks; ++c) {
+    // Every warp works on its kTPW tokens of each chunk it takes with a warp-local online
+    // softmax, warps meet only at the end, and the last warp done with a stage refills it.
+    // Grouped heads: 16 tokens of every chunk (half of one key group); the two warps of a
+    // group share its q' fragments and bias (each builds one channel half; a 64-thread named
+    // barrier per pair before and after). One head: a whole key group of every other chunk,
+    // q' in the warp's own area and the bias in a register.
+    const int wc = warp % L::kWPC;                     // the warp's slot in its chunks
+    const int tb = L::kTPW * wc, g = (RH == 1) ? wc : warp >> 1, hf = warp & 1;
+    for (int c = warp / L::kWPC; c < n_chunks; c += L::kNPar) {
       const int st = c % L::kAStages;
       kivi_wait(&full[st], (c / L::kAStages) & 1, failed, a.err);  // a timeout leaves stale data: harmless, reported
       const unsigned char* stage = sma + st * L::kStage;
       const int tc0 = t0 + c * kAChunk;  // token of chunk row 0
-      const int n = min(kAChunk, t1 - tc0);  // a multiple of 32: both warps of a group have all 16 tokens or none
+      const int n = min(kAChunk, t1 - tc0);  // a multiple of 32: a key group's warps have all its tokens or none
+      float bias_w = 0.f;                    // one head: -sum q' z of the warp's key group
+      if (tb < n && RH == 1) {
+        // ---- one head: q' = q s of key group g (the scale folds into the query) in the code-
+        //      pair order of each 64-channel half, divided by 2^(b j); lane l builds channels
+        //      2 l, 2 l + 1 of both halves ----
+        float* qr = qf + warp * kD;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int ch = 64 * hh + 2 * lane;
+          const uint32_t s2 = *reinterpret_cast<const uint32_t*>(stage + L::kCKs + (g * kD + ch) * 2);
+          const uint32_t z2 = *reinterpret_cast<const uint32_t*>(stage + L::kCKz + (g * kD + ch) * 2);
+          const float qa = qs[ch] * h2f(s2 & 0xFFFFu), qb = qs[ch + 1] * h2f(s2 >> 16);
+          int ja, jb;
+          const int ia = qpair_index<KB>(2 * lane, ja), ib = qpair_index<KB>(2 * lane + 1, jb);
+          qr[64 * hh + ia] = qa * pow2_neg(KB * ja);
+          qr[64 * hh + ib] = qb * pow2_neg(KB * jb);
+          bias_w -= qa * h2f(z2 & 0xFFFFu) + qb * h2f(z2 >> 16);
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) bias_w += __shfl_xor_sync(0xFFFFFFFFu, bias_w, off);
+        __syncwarp();  // q' written before the lanes read it
+      }
       if (tb < n) {
-        // ---- q' = q s per key group (the scale folds into the query) and bias = -sum q' z:
-        //      warp hf builds channels 64 hf .. 64 hf + 63 ----
+        if constexpr (RH > 1) {
+        // ---- grouped heads: q' = q s per key group and bias = -sum q' z; warp hf builds
+        //      channels 64 hf .. 64 hf + 63 ----
         pair_sync(g);  // the partner is done reading the previous chunk's q'
         {
           const int ch = 64 * hf + 2 * lane;
           const uint32_t s2 = *reinterpret_cast<const uint32_t*>(stage + L::kCKs + (g * kD + ch) * 2);
           const uint32_t z2 = *reinterpret_cast<const uint32_t*>(stage + L::kCKz + (g * kD + ch) * 2);
           const float sa = h2f(s2 & 0xFFFFu), sb = h2f(s2 >> 16), za = h2f(z2 & 0xFFFFu), zb = h2f(z2 >> 16);
-          // tensor-core scores: channels (ch, ch + 1) are one fp16 pair of the B fragments of
-          // k-step ch / 16 (thread t4, register reg), each channel's q' divided by the power of
-          // two its code carries in the A fragment (code_frag); CUDA-core scores: q' in the
-          // code-pair order of a 64-channel half, divided by 2^(b j)
-          int t4 = 0, reg = 0;
-          float fa = 1.f, fb = 1.f;
-          if constexpr (L::kMma && KB == 4) {
+          // channels (ch, ch + 1) are one fp16 pair of the B fragments of k-step ch / 16 (thread
+          // t4, register reg), each channel's q' divided by the power of two its code carries in
+          // the A fragment (code_frag)
+          int t4, reg;
+          float fa = 1.f, fb;
+          if constexpr (KB == 4) {
             t4 = (ch & 7) >> 1, reg = (ch >> 3) & 1, fb = 0.0625f;
-          } else if constexpr (L::kMma) {
+          } else {
             t4 = (ch & 15) >> 2, reg = (ch >> 1) & 1, fa = reg ? 0.0625f : 1.f, fb = reg ? 0.015625f : 0.25f;
           }
           const int kk = ch >> 4;
           uint32_t* qbf = reinterpret_cast<uint32_t*>(qf) + g * L::kQfWords + ((kk >> 1) * L::kNC * 4 + t4) * 4 + (kk & 1) * 2 + reg;
-          int ja, jb;
-          const int ia = qpair_index<KB>(ch & 63, ja), ib = qpair_index<KB>((ch + 1) & 63, jb);
 #pragma unroll
           for (int r = 0; r < RH; ++r) {
             const float qa = qs[r * kD + ch] * sa, qb = qs[r * kD + ch + 1] * sb;
-            if constexpr (L::kMma) {  // q' = hi + lo in fp16: column 2 r holds the high parts, 2 r + 1 the low
+            {  // q' = hi + lo in fp16: column 2 r holds the high parts, 2 r + 1 the low
               const float qe = qa * fa, qo = qb * fb;
               const __half he = __float2half_rn(qe), ho = __float2half_rn(qo);
               const __half le = __float2half_rn(qe - __half2float(he)), lo = __float2half_rn(qo - __half2float(ho));
               qbf[(2 * r) * 4 * 4] = (uint32_t)__half_as_ushort(he) | ((uint32_t)__half_as_ushort(ho) << 16);
               qbf[(2 * r + 1) * 4 * 4] = (uint32_t)__half_as_ushort(le) | ((uint32_t)__half_as_ushort(lo) << 16);
-            } else {
-              float* qr = qf + (r * 4 + g) * kD + 64 * hf;
-              qr[ia] = qa * pow2_neg(KB * ja);
-              qr[ib] = qb * pow2_neg(KB * jb);
             }
             float pb = -(qa * za + qb * zb);
 #pragma unroll
@@ -934,9 +960,10 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
           }
         }
         pair_sync(g);  // both halves written
-        // ---- scores: lanes 0-15 channels 0-63 of token tb + lane, lanes 16-31 channels 64-127 ----
+        }
+        // ---- scores of the warp's kTPW tokens ----
         float pk[RH];
-        float raw[RH];  // the 16 tokens' dot products q' . codes, lanes l and l + 16 holding token l
+        float raw[RH];  // dot products q' . codes: lane l's token (grouped heads: l and l + 16 share token l)
         if constexpr (L::kMma) {
           // scores[16 tokens][RH heads] = codes[16 x 128] . q'[128 x RH] on the tensor cores, one
           // m16n8k16 product per 16 channels: the A fragments come straight from the code bytes
@@ -977,47 +1004,44 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
           for (int r = 0; r < RH; ++r) raw[r] = ss[(lane & 15) * RH + r];
           __syncwarp();  // read before the next chunk overwrites it
         } else {
-          // one head: lanes 0-15 take channels 0-63 of token tb + lane, lanes 16-31 channels
-          // 64-127; a byte permute per code word puts the codes under the exponent of 2^23, then
+          // one head: lane l takes all 128 channels of token tb + l, one 64-channel half at a
+          // time; a byte permute per code word puts the codes under the exponent of 2^23, then
           // one AND per code, one packed add and one packed FMA per code pair
-          uint32_t wds[L::kKW];
+          const float* qw = qf + warp * kD;
+          float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int k4 = 0; k4 < L::kKW / 4; ++k4) {
-            const uint4 cw = *reinterpret_cast<const uint4*>(stage + L::kCKc + tk * L::kKRow + chh * (L::kKRow / 2) + 16 * k4);
-            wds[4 * k4] = cw.x;
-            wds[4 * k4 + 1] = cw.y;
-            wds[4 * k4 + 2] = cw.z;
-            wds[4 * k4 + 3] = cw.w;
-          }
-          float2 acc2[RH];
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t wds[L::kKW];
 #pragma unroll
-          for (int r = 0; r < RH; ++r) acc2[r] = make_float2(0.f, 0.f);
+            for (int k4 = 0; k4 < L::kKW / 4; ++k4) {
+              const uint4 cw = *reinterpret_cast<const uint4*>(stage + L::kCKc + (tb + lane) * L::kKRow + hh * (L::kKRow / 2) + 16 * k4);
+              wds[4 * k4] = cw.x;
+              wds[4 * k4 + 1] = cw.y;
+              wds[4 * k4 + 2] = cw.z;
+              wds[4 * k4 + 3] = cw.w;
+            }
 #pragma unroll
-          for (int k = 0; k < L::kKW; ++k) {
-            const uint32_t ml = magic_lo(wds[k]), mh = magic_hi(wds[k]);
+            for (int k = 0; k < L::kKW; ++k) {
+              const uint32_t ml = magic_lo(wds[k]), mh = magic_hi(wds[k]);
 #pragma unroll
-            for (int j = 0; j < L::kPK; ++j) {
-              const float2 cp = code_pair<KB>(ml, mh, j);
-#pragma unroll
-              for (int r = 0; r < RH; ++r) {
-                const float2* q2 = reinterpret_cast<const float2*>(qf + (r * 4 + g) * kD + 64 * chh);
-                acc2[r] = __ffma2_rn(q2[k * L::kPK + j], cp, acc2[r]);
+              for (int j = 0; j < L::kPK; j += 2) {  // two code pairs per 16-byte q' load
+                const float4 q4 = *reinterpret_cast<const float4*>(qw + 64 * hh + 2 * (k * L::kPK + j));
+                acc2 = __ffma2_rn(make_float2(q4.x, q4.y), code_pair<KB>(ml, mh, j), acc2);
+                acc2 = __ffma2_rn(make_float2(q4.z, q4.w), code_pair<KB>(ml, mh, j + 1), acc2);
               }
             }
           }
-#pragma unroll
-          for (int r = 0; r < RH; ++r) {
-            raw[r] = acc2[r].x + acc2[r].y;
-            raw[r] += __shfl_xor_sync(0xFFFFFFFFu, raw[r], 16);
-          }
+          raw[0] = acc2.x + acc2.y;
         }
-        // ---- warp-local online softmax over the 16 tokens (lanes l and l + 16 share one) ----
+        // ---- warp-local online softmax over the warp's kTPW tokens ----
+        constexpr int kRed = L::kTPW / 2;  // first xor distance of the reductions over the tokens
 #pragma unroll
         for (int r = 0; r < RH; ++r) {
-          const float sc_r = (raw[r] + bias[(r * 4 + g) * 2] + bias[(r * 4 + g) * 2 + 1]) * scale_log2;
+          const float bsum = (RH == 1) ? bias_w : bias[(r * 4 + g) * 2] + bias[(r * 4 + g) * 2 + 1];
+          const float sc_r = (raw[r] + bsum) * scale_log2;
           float mx = sc_r;
 #pragma unroll
-          for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+          for (int off = kRed; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
           // the running maximum is raised only when a score passes it by more than kSlack (or
           // on the first chunk): the sums stay exact relative to M, and most chunks skip the
           // rescale (warp-uniform)
@@ -1025,7 +1049,7 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
           pk[r] = exp2f(sc_r - M[r]);
           float ls = pk[r];
 #pragma unroll
-          for (int off = 8; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, off);
+          for (int off = kRed; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, off);
           l[r] += ls;
         }
         // ---- values: kTS tokens of the warp per step ----
@@ -1034,7 +1058,7 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
         auto value_steps = [&](auto full_tag) {
           constexpr bool kFull = decltype(full_tag)::value;
 #pragma unroll
-          for (int step = 0; step < 16 / L::kTS; ++step) {
+          for (int step = 0; step < L::kTPW / L::kTS; ++step) {
             float p[RH];
 #pragma unroll
             for (int r = 0; r < RH; ++r) p[r] = __shfl_sync(0xFFFFFFFFu, pk[r], L::kTS * step + ts);
@@ -1092,12 +1116,12 @@ __global__ void __launch_bounds__(kAThreads, AttnLayout<KB, VB, RH>::kMinBlocks)
             }
           }
         };
-        if (tc0 + tb + 16 <= NQV) value_steps(BoolTag<true>{});
+        if (tc0 + tb + L::kTPW <= NQV) value_steps(BoolTag<true>{});
         else value_steps(BoolTag<false>{});
       }
       // ---- this warp is done with the stage; the last one refills it ----
       __syncwarp();
-      if (lane == 0 && atom_add_acq_rel_shared(&released[st], 1) == kAWarps - 1) {
+      if (lane == 0 && atom_add_acq_rel_shared(&released[st], 1) == L::kWPC - 1) {
         released[st] = 0;
         if (c + L::kAStages < n_chunks && !*failed) {
           fence_proxy_async_smem();

@@ -555,10 +555,11 @@ __global__ void __launch_bounds__(128) kivi_append_kernel(const KiviAppendArgs a
 // subgroups are adjacent in launch order so their code reads meet in L2. A quantized split
 // streams its tokens through a 3- or 4-stage shared-memory ring of 128-token chunks (TMA bulk
 // copies of the chunk's key codes, key scales and zeros, value codes, value scales and
-// zeros); each warp takes 16 tokens of every chunk, computes their scores (for RH > 1 heads
-// as a tensor-core product per key group: fp16 code fragments against q' = q s split into
-// fp16 high and low parts; for one head on the CUDA cores), keeps its own online softmax per
-// query head, and sums the values on the CUDA cores; the block merges the warps at the end. Tokens whose key is quantized but whose
+// zeros); each warp takes its tokens of a chunk (one head: a whole 32-token key group of
+// every other chunk; RH > 1 heads: 16 tokens of every chunk), computes their scores (RH > 1:
+// a tensor-core product per key group, fp16 code fragments against q' = q s split into fp16
+// high and low parts; one head: on the CUDA cores), keeps its own online softmax per query
+// head, and sums the values on the CUDA cores; the block merges the warps at the end. Tokens whose key is quantized but whose
 // value is still in the fp16 window (the streaming cache's tail) take the value from the
 // window. Partials of all splits merge exactly in the last block of a (request, subgroup) to
 // finish (arrival counter, no spin-wait).

@@ -397,8 +397,8 @@ PROFILED_TRAFFIC = {
         245814528 + 3427328),
     "kivi_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "3dd2eba2f7371cb8f823bc0bf7282482912431f1f5f0bf6df34ca6a394a8ddbf",
-        228793088 + 3563264),
+        "d9212bd30963454ad0bd578eb125492d04f4c19620162fddb05c762924a4ffbd",
+        228793344 + 3551488),
     "encode_32k:encode_tc_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_encode_tc.cu",
         "8f4d7c4d56f8e4813997994084beadad628c36cd5447f2bd11be519377daa3e4",
@@ -406,12 +406,12 @@ PROFILED_TRAFFIC = {
     # both quantize launches (keys per channel, values per token) of one step
     "kivi_quant_32k:kivi_quant_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "72bbd6a23beb3d4ecbaed9f57fa2a03fe82b3992461aa8f74b8e5e7f5adcd620",
-        134274304 + 9315584 + 134291712 + 6603776),
+        "d9212bd30963454ad0bd578eb125492d04f4c19620162fddb05c762924a4ffbd",
+        134273792 + 9351936 + 134293760 + 6658560),
     "kivi4_gqa_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
-        "72bbd6a23beb3d4ecbaed9f57fa2a03fe82b3992461aa8f74b8e5e7f5adcd620",
-        89870080 + 2205952),
+        "d9212bd30963454ad0bd578eb125492d04f4c19620162fddb05c762924a4ffbd",
+        89870592 + 2173440),
 }
 
 

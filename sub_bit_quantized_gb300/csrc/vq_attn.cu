@@ -33,7 +33,7 @@
 //      buffer (two broadcast loads, not shuffles). No value row is read per token.
 //  * 4 aux warps: for each sub-piece, w . B_V (the fp16 value slice, read from L2) gives the
 //    sub-piece's partial (M, l, o); they attend the bf16 window of every segment whose first
-//    page this block holds (two tokens per warp step, rotated query from the table, online
+//    page this block holds (three tokens per warp step, rotated query from the table, online
 //    softmax), merge, and write the output. A segment shared with other blocks is merged by the last block to finish
 //    its part (a per-segment counter in the workspace).
 //  * 1 producer warp (one lane): TMA bulk copies of each unit's index pages (and the query)
@@ -579,39 +579,59 @@ __device__ void aux_window(const VqAttnArgs& a, int h, int b, int L, int NP, flo
   const uint16_t* wk = a.win_k + bh * a.win_slots * kD;
   const uint16_t* wv = a.win_v + bh * a.win_slots * kD;
   float M = -INFINITY, l = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-  // two tokens per step (w, w + kAW), their loads issued together
-  constexpr int kTW = 2;
+  // kTW tokens per step (w, w + kAW, ...): their key and RoPE loads issued together, the
+  // value loads issued after the dot products (in flight during the interleaved reductions),
+  // one running-maximum update per step (four tokens no longer fit the 80 registers of the
+  // kernel's 672 threads)
+  constexpr int kTW = 3;
   for (int w = aw; w < nwin; w += kTW * kAW) {
-    uint32_t ka[kTW], kb[kTW], va[kTW], vb[kTW];
-    float2 c[kTW], sn[kTW];
+    int slot[kTW];
+    float sc[kTW];
+    {
+      uint32_t ka[kTW], kb[kTW];
+      float2 c[kTW], sn[kTW];
+#pragma unroll
+      for (int e = 0; e < kTW; ++e) {
+        const int we = min(w + e * kAW, nwin - 1);  // a missing token reloads the last one
+        const int p = (we < nsink) ? we : a.sink + kPage * NP + (we - nsink);
+        slot[e] = (p < a.sink) ? p : a.sink + (p - a.sink) % (a.recent + kPage);
+        ka[e] = __ldg(reinterpret_cast<const uint32_t*>(wk + (size_t)slot[e] * kD + 2 * lane));
+        kb[e] = __ldg(reinterpret_cast<const uint32_t*>(wk + (size_t)slot[e] * kD + 64 + 2 * lane));
+        const int d = L - 1 - p;
+        c[e] = __ldg(reinterpret_cast<const float2*>(a.rope_cos + (size_t)d * (kD / 2) + 2 * lane));
+        sn[e] = __ldg(reinterpret_cast<const float2*>(a.rope_sin + (size_t)d * (kD / 2) + 2 * lane));
+      }
+#pragma unroll
+      for (int e = 0; e < kTW; ++e) {
+        const float u0 = q0 * c[e].x - q2 * sn[e].x, u2 = q2 * c[e].x + q0 * sn[e].x;
+        const float u1 = q1 * c[e].y - q3 * sn[e].y, u3 = q3 * c[e].y + q1 * sn[e].y;
+        sc[e] = u0 * bf16_lo(ka[e]) + u1 * bf16_hi(ka[e]) + u2 * bf16_lo(kb[e]) + u3 * bf16_hi(kb[e]);
+      }
+    }
+    uint32_t va[kTW], vb[kTW];
 #pragma unroll
     for (int e = 0; e < kTW; ++e) {
-      const int we = min(w + e * kAW, nwin - 1);  // a missing token reloads the last one
-      const int p = (we < nsink) ? we : a.sink + kPage * NP + (we - nsink);
-      const int slot = (p < a.sink) ? p : a.sink + (p - a.sink) % (a.recent + kPage);
-      ka[e] = __ldg(reinterpret_cast<const uint32_t*>(wk + (size_t)slot * kD + 2 * lane));
-      kb[e] = __ldg(reinterpret_cast<const uint32_t*>(wk + (size_t)slot * kD + 64 + 2 * lane));
-      va[e] = __ldg(reinterpret_cast<const uint32_t*>(wv + (size_t)slot * kD + 2 * lane));
-      vb[e] = __ldg(reinterpret_cast<const uint32_t*>(wv + (size_t)slot * kD + 64 + 2 * lane));
-      const int d = L - 1 - p;
-      c[e] = __ldg(reinterpret_cast<const float2*>(a.rope_cos + (size_t)d * (kD / 2) + 2 * lane));
-      sn[e] = __ldg(reinterpret_cast<const float2*>(a.rope_sin + (size_t)d * (kD / 2) + 2 * lane));
+      va[e] = __ldg(reinterpret_cast<const uint32_t*>(wv + (size_t)slot[e] * kD + 2 * lane));
+      vb[e] = __ldg(reinterpret_cast<const uint32_t*>(wv + (size_t)slot[e] * kD + 64 + 2 * lane));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int e = 0; e < kTW; ++e) sc[e] += __shfl_xor_sync(0xFFFFFFFFu, sc[e], o);
+    float mx = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < kTW; ++e) {  // tokens past the window's end drop out (uniform across the warp)
+      sc[e] = (w + e * kAW < nwin) ? sc[e] * scale_log2 : -INFINITY;
+      mx = fmaxf(mx, sc[e]);
+    }
+    if (mx > M) {
+      const float f = (M == -INFINITY) ? 0.f : exp2f(M - mx);
+      l *= f; o0 *= f; o1 *= f; o2 *= f; o3 *= f;
+      M = mx;
     }
 #pragma unroll
     for (int e = 0; e < kTW; ++e) {
-      if (w + e * kAW >= nwin) break;  // uniform across the warp
-      const float u0 = q0 * c[e].x - q2 * sn[e].x, u2 = q2 * c[e].x + q0 * sn[e].x;
-      const float u1 = q1 * c[e].y - q3 * sn[e].y, u3 = q3 * c[e].y + q1 * sn[e].y;
-      float dot = u0 * bf16_lo(ka[e]) + u1 * bf16_hi(ka[e]) + u2 * bf16_lo(kb[e]) + u3 * bf16_hi(kb[e]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-      const float sc = dot * scale_log2;
-      if (sc > M) {
-        const float f = (M == -INFINITY) ? 0.f : exp2f(M - sc);
-        l *= f; o0 *= f; o1 *= f; o2 *= f; o3 *= f;
-        M = sc;
-      }
-      const float pw = exp2f(sc - M);
+      const float pw = exp2f(sc[e] - M);  // 0 for a dropped token
       l += pw;
       o0 += pw * bf16_lo(va[e]); o1 += pw * bf16_hi(va[e]); o2 += pw * bf16_lo(vb[e]); o3 += pw * bf16_hi(vb[e]);
     }

@@ -32,10 +32,15 @@
 //      atomic hit 32 different banks. A page's 8 weights reach its lanes through the score
 //      buffer (two broadcast loads, not shuffles). No value row is read per token.
 //  * 4 aux warps: for each sub-piece, w . B_V (the fp16 value slice, read from L2) gives the
-//    sub-piece's partial (M, l, o); they attend the bf16 window of every segment whose first
-//    page this block holds (three tokens per warp step, rotated query from the table, online
-//    softmax), merge, and write the output. A segment shared with other blocks is merged by the last block to finish
-//    its part (a per-segment counter in the workspace).
+//    sub-piece's partial (M, l, o); they merge it, and the window warps' partial of the
+//    segment's bf16 window when the piece starts the segment, and write the output. A segment
+//    shared with other blocks is merged by the last block to finish its part (a per-segment
+//    counter in the workspace). Segments without index pages are attended by the aux warps
+//    themselves, spread over the blocks.
+//  * 3 window warps: they walk the block's pieces like the aux warps and attend the bf16
+//    window (sink + recent tokens) of every segment whose first page this block holds, two
+//    tokens per warp step, rotated query from the table, online softmax, in parallel with the
+//    other roles; each window's rows go to the aux warps through a pair of mbarriers.
 //  * 1 producer warp (one lane): TMA bulk copies of each unit's index pages (and the query)
 //    into a ring of stages, and of the key slice whenever the share enters a new head; an L2
 //    prefetch of each owned window's bf16 rows when the share reaches that segment.
@@ -54,10 +59,12 @@ namespace {
 
 constexpr int kCW = kVqComputeWarps;                 // compute warps
 constexpr int kAW = 4;                               // aux warps
-constexpr int kThreads = (kCW + kAW + 1) * 32;       // + one producer warp
+constexpr int kWW = 3;                               // window warps
+constexpr int kThreads = (kCW + kAW + 1 + kWW) * 32; // + one producer warp and the window warps
 constexpr int kAuxT0 = kCW * 32;                     // first aux thread
 constexpr int kAuxN = kAW * 32;
 constexpr int kProdWarp = kCW + kAW;
+constexpr int kWinW0 = kProdWarp + 1;                // first window warp
 constexpr int kSubP = kVqSubPages;                   // pages per sub-piece
 constexpr int kFixBits = 20;                         // fixed-point weight resolution 2^-20
 // capacity: a bin sums at most kSubP * 8 weights of at most 2^20 each
@@ -94,11 +101,12 @@ struct Lay {
   static constexpr int kOffJ = kOffRing + kStg * kStageB;       // cos, sin(kJump theta), cos, sin(theta) [4][64]
   static constexpr int kOffWm = kOffJ + 4 * 64 * 4;            // sub-piece maxima [2 parities][kCW]
   static constexpr int kOffWp = kOffWm + 2 * kCW * 4;          // aux window partials [kAW][132]
-  static constexpr int kOffRed = kOffWp + kAW * 132 * 4;       // aux reduction [4][128] + [4] + flag
+  static constexpr int kOffWw = kOffWp + kAW * 132 * 4;        // window-warp partials [kWW][132]
+  static constexpr int kOffRed = kOffWw + kWW * 132 * 4;       // aux reduction [4][128] + [4] + flag
   static constexpr int kOffWalk = kOffRed + (4 * 128 + 8) * 4; // the share's first piece
   static constexpr int kOffBar = kOffWalk + 64;
-  // full[kStg], empty[kStg], kbar, ktfree, maxbar, hfull, hfree, then flags
-  static constexpr int kSmemBytes = kOffBar + (2 * kStg + 5) * 8 + 16;
+  // full[kStg], empty[kStg], kbar, ktfree, maxbar, hfull, hfree, wfull, wfree, then flags
+  static constexpr int kSmemBytes = kOffBar + (2 * kStg + 7) * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kOffRing % 128 == 0 && kStageB % 128 == 0 && kOffBar % 8 == 0 && kOffWalk % 16 == 0, "alignment");
 };
@@ -323,7 +331,7 @@ __device__ __forceinline__ void page_hist(const uint4 row, const uint32_t (&wt)[
 }
 
 struct Bars {
-  uint64_t *full, *empty, *kbar, *ktfree, *maxbar, *hfull, *hfree;
+  uint64_t *full, *empty, *kbar, *ktfree, *maxbar, *hfull, *hfree, *wfull, *wfree;
   volatile int* failed;
   int* flag;  // aux: last-contributor flag
 };
@@ -564,12 +572,13 @@ __device__ __forceinline__ void merge_part(float& M, float& l, float& o, float M
   M = Mn;
 }
 
-// bf16 sink and recent tokens of segment (h, b): 4 warps take every 4th token, two tokens per
-// step with their loads issued together; lane l holds channels 2l, 2l+1 and their RoPE
-// partners. Returns the window's partial for channel `at`.
-__device__ void aux_window(const VqAttnArgs& a, int h, int b, int L, int NP, float scale_log2, float* wp, int at,
-                           float& Mo, float& lo_, float& oo) {
-  const int aw = at >> 5, lane = at & 31;
+// bf16 sink and recent tokens of segment (h, b): NW warps, warp wi taking every NW-th token
+// from wi, kTW tokens per step; lane l holds channels 2l, 2l+1 and their RoPE partners.
+// Writes the warp's partial to its row of `rows` ([0] M, [1] l, [4 + ch] channel ch; 132
+// floats a row).
+template <int NW, int kTW>
+__device__ void win_attend(const VqAttnArgs& a, int h, int b, int L, int NP, float scale_log2, float* rows, int wi,
+                           int lane) {
   const int nsink = min(a.sink, L);
   const int nwin = (L > 0) ? nsink + max(0, L - a.sink - kPage * NP) : 0;
   const size_t bh = (size_t)b * a.H + h;
@@ -579,12 +588,10 @@ __device__ void aux_window(const VqAttnArgs& a, int h, int b, int L, int NP, flo
   const uint16_t* wk = a.win_k + bh * a.win_slots * kD;
   const uint16_t* wv = a.win_v + bh * a.win_slots * kD;
   float M = -INFINITY, l = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-  // kTW tokens per step (w, w + kAW, ...): their key and RoPE loads issued together, the
+  // kTW tokens per step (w, w + NW, ...): their key and RoPE loads issued together, the
   // value loads issued after the dot products (in flight during the interleaved reductions),
-  // one running-maximum update per step (four tokens no longer fit the 80 registers of the
-  // kernel's 672 threads)
-  constexpr int kTW = 3;
-  for (int w = aw; w < nwin; w += kTW * kAW) {
+  // one running-maximum update per step
+  for (int w = wi; w < nwin; w += kTW * NW) {
     int slot[kTW];
     float sc[kTW];
     {
@@ -592,7 +599,7 @@ __device__ void aux_window(const VqAttnArgs& a, int h, int b, int L, int NP, flo
       float2 c[kTW], sn[kTW];
 #pragma unroll
       for (int e = 0; e < kTW; ++e) {
-        const int we = min(w + e * kAW, nwin - 1);  // a missing token reloads the last one
+        const int we = min(w + e * NW, nwin - 1);  // a missing token reloads the last one
         const int p = (we < nsink) ? we : a.sink + kPage * NP + (we - nsink);
         slot[e] = (p < a.sink) ? p : a.sink + (p - a.sink) % (a.recent + kPage);
         ka[e] = __ldg(reinterpret_cast<const uint32_t*>(wk + (size_t)slot[e] * kD + 2 * lane));
@@ -621,7 +628,7 @@ __device__ void aux_window(const VqAttnArgs& a, int h, int b, int L, int NP, flo
     float mx = -INFINITY;
 #pragma unroll
     for (int e = 0; e < kTW; ++e) {  // tokens past the window's end drop out (uniform across the warp)
-      sc[e] = (w + e * kAW < nwin) ? sc[e] * scale_log2 : -INFINITY;
+      sc[e] = (w + e * NW < nwin) ? sc[e] * scale_log2 : -INFINITY;
       mx = fmaxf(mx, sc[e]);
     }
     if (mx > M) {
@@ -636,13 +643,25 @@ __device__ void aux_window(const VqAttnArgs& a, int h, int b, int L, int NP, flo
       o0 += pw * bf16_lo(va[e]); o1 += pw * bf16_hi(va[e]); o2 += pw * bf16_lo(vb[e]); o3 += pw * bf16_hi(vb[e]);
     }
   }
-  float* mine = wp + aw * 132;
+  float* mine = rows + wi * 132;
   mine[4 + 2 * lane] = o0; mine[5 + 2 * lane] = o1; mine[68 + 2 * lane] = o2; mine[69 + 2 * lane] = o3;
   if (lane == 0) { mine[0] = M; mine[1] = l; }
-  aux_sync();
+}
+
+// the NW rows' partials merged for channel ch
+template <int NW>
+__device__ __forceinline__ void win_merge(const float* rows, int ch, float& Mo, float& lo_, float& oo) {
   Mo = -INFINITY; lo_ = 0.f; oo = 0.f;
 #pragma unroll
-  for (int w = 0; w < kAW; ++w) merge_part(Mo, lo_, oo, wp[w * 132], wp[w * 132 + 1], wp[w * 132 + 4 + at]);
+  for (int w = 0; w < NW; ++w) merge_part(Mo, lo_, oo, rows[w * 132], rows[w * 132 + 1], rows[w * 132 + 4 + ch]);
+}
+
+// the window of a segment without index pages, attended by the 4 aux warps themselves
+__device__ void aux_window(const VqAttnArgs& a, int h, int b, int L, int NP, float scale_log2, float* wp, int at,
+                           float& Mo, float& lo_, float& oo) {
+  win_attend<kAW, 3>(a, h, b, L, NP, scale_log2, wp, at >> 5, at & 31);
+  aux_sync();
+  win_merge<kAW>(wp, at, Mo, lo_, oo);
   aux_sync();  // before the partial area is reused
 }
 
@@ -750,11 +769,10 @@ __device__ void aux_role(const VqAttnArgs& a, unsigned char* smem, const Bars& B
     aux_window(a, h, b, L, NP, scale_log2, wp, at, M, l, o);
     aux_emit(a, flag, h, b, 0, 0, Ptot, blk, at, M, l, o);
   }
-  uint32_t hfull_ph = 0;
+  uint32_t hfull_ph = 0, wfull_ph = 0;
   int par = 0;
   while (W.valid) {
     float M = -INFINITY, l = 0.f, o = 0.f;
-    if (W.pa == 0) aux_window(a, W.h, W.b, W.L, W.np, scale_log2, wp, at, M, l, o);
     for (int sa = W.pa; sa < W.pb; sa += kSubP) {
       if (aux_any(!wait_bar(B.hfull, hfull_ph, B.failed, a.err))) return;
       hfull_ph ^= 1u;
@@ -764,7 +782,40 @@ __device__ void aux_role(const VqAttnArgs& a, unsigned char* smem, const Bars& B
       merge_part(M, l, o, Ms, ls, os);
       par ^= 1;
     }
+    if (W.pa == 0) {  // the piece starts its segment: the window warps' partial of its window
+      if (aux_any(!wait_bar(B.wfull, wfull_ph, B.failed, a.err))) return;
+      wfull_ph ^= 1u;
+      float Mw, lw, ow;
+      win_merge<kWW>(reinterpret_cast<const float*>(smem + Ly::kOffWw), at, Mw, lw, ow);
+      __syncwarp();
+      if ((at & 31) == 0) mbar_arrive(B.wfree);  // this warp has read the rows
+      merge_part(M, l, o, Mw, lw, ow);
+    }
     aux_emit(a, flag, W.h, W.b, W.pos - W.pa, W.np, Ptot, blk, at, M, l, o);
+    walk_next(a, W, hi);
+  }
+}
+
+// ------------------------------------------------------------------ window warps
+// They walk the block's pieces like the aux warps and attend the bf16 window of every piece
+// that starts its segment, in parallel with the compute warps and the aux warps' sub-piece
+// sums, handing each window's rows to the aux warps: wfull (kWW arrivals) when written,
+// wfree (kAW arrivals) when read.
+template <int NG>
+__device__ void window_role(const VqAttnArgs& a, unsigned char* smem, const Bars& B, Walk W, const long long hi,
+                            const float scale_log2) {
+  using Ly = Lay<NG>;
+  const int wi = (threadIdx.x >> 5) - kWinW0, lane = threadIdx.x & 31;
+  float* rows = reinterpret_cast<float*>(smem + Ly::kOffWw);
+  uint32_t wfree_ph = 1;  // the rows start free
+  while (W.valid) {
+    if (W.pa == 0) {
+      if (!__all_sync(0xFFFFFFFFu, wait_bar(B.wfree, wfree_ph, B.failed, a.err))) return;
+      wfree_ph ^= 1u;
+      win_attend<kWW, 2>(a, W.h, W.b, W.L, W.np, scale_log2, rows, wi, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B.wfull);
+    }
     walk_next(a, W, hi);
   }
 }
@@ -785,7 +836,9 @@ __global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a
   B.maxbar = B.kbar + 2;
   B.hfull = B.kbar + 3;
   B.hfree = B.kbar + 4;
-  int* iflags = reinterpret_cast<int*>(B.kbar + 5);
+  B.wfull = B.kbar + 5;
+  B.wfree = B.kbar + 6;
+  int* iflags = reinterpret_cast<int*>(B.kbar + 7);
   B.failed = iflags;
   B.flag = iflags + 1;
   Walk* wstart = reinterpret_cast<Walk*>(smem + Ly::kOffWalk);
@@ -837,6 +890,8 @@ __global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a
     mbar_init(B.maxbar, kCW);
     mbar_init(B.hfull, kCW);
     mbar_init(B.hfree, kAuxN);
+    mbar_init(B.wfull, kWW);
+    mbar_init(B.wfree, kAW);
     *B.failed = 0;
     fence_mbar_init();
     Walk W;
@@ -883,8 +938,10 @@ __global__ void __launch_bounds__(kThreads, 1) vq_attn_kernel(const VqAttnArgs a
     compute_role<NG>(a, smem, B, scale_log2);
   } else if (warp < kCW + kAW) {
     aux_role<NG>(a, smem, B, *wstart, hi, Ptot, scale_log2);
-  } else if (lane == 0) {
-    producer_role<NG>(a, smem, B, *wstart, hi, issued, k_loads);
+  } else if (warp == kProdWarp) {
+    if (lane == 0) producer_role<NG>(a, smem, B, *wstart, hi, issued, k_loads);
+  } else {
+    window_role<NG>(a, smem, B, *wstart, hi, scale_log2);
   }
   __syncthreads();
   // after a timeout, let the block's own copies in flight land before it exits

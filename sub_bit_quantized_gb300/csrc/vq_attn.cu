@@ -38,7 +38,7 @@
 //    counter in the workspace). Segments without index pages are attended by the aux warps
 //    themselves, spread over the blocks.
 //  * 3 window warps: they walk the block's pieces like the aux warps and attend the bf16
-//    window (sink + recent tokens) of every segment whose first page this block holds, two
+//    window (sink + recent tokens) of every segment whose first page this block holds, three
 //    tokens per warp step, rotated query from the table, online softmax, in parallel with the
 //    other roles; each window's rows go to the aux warps through a pair of mbarriers.
 //  * 1 producer warp (one lane): TMA bulk copies of each unit's index pages (and the query)
@@ -812,7 +812,7 @@ __device__ void window_role(const VqAttnArgs& a, unsigned char* smem, const Bars
     if (W.pa == 0) {
       if (!__all_sync(0xFFFFFFFFu, wait_bar(B.wfree, wfree_ph, B.failed, a.err))) return;
       wfree_ph ^= 1u;
-      win_attend<kWW, 2>(a, W.h, W.b, W.L, W.np, scale_log2, rows, wi, lane);
+      win_attend<kWW, 3>(a, W.h, W.b, W.L, W.np, scale_log2, rows, wi, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(B.wfull);
     }

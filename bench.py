@@ -393,8 +393,8 @@ DTYPE_LABEL = {
 PROFILED_TRAFFIC = {
     "loopvq_b64_6k:vq_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/vq_attn.cu",
-        "d99056bcba3b29ae4051816d6ac4d7a082ba6ca0347d320bf160af919a52ca69",
-        245814528 + 3427328),
+        "0b5678e43e43cf1baab2d5ef0842ea12d8f8b3e2ba305d6d02da53b416c1be28",
+        245771008 + 3553280),
     "kivi_b16_4k:kivi_attn_kernel": (
         "sub_bit_quantized_gb300/csrc/kivi.cu",
         "d9212bd30963454ad0bd578eb125492d04f4c19620162fddb05c762924a4ffbd",

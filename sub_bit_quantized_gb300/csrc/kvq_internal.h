@@ -35,8 +35,9 @@ __host__ __device__ inline size_t page_byte(int g, int j, int NG) {
 // head-major, form one list of page positions; block k of G takes positions
 // [k P / G, (k + 1) P / G). Inside a block, 16 compute warps score the keys of up to
 // kVqSubPages pages (pass 1), then add the fixed-point softmax weights of the same pages into
-// a per-(group, codeword) histogram (pass 2); aux warps turn each histogram into value sums,
-// attend the bf16 window of every segment whose first page the block holds, and merge. A
+// a per-(group, codeword) histogram (pass 2); aux warps turn each histogram into value sums
+// and merge; window warps attend the bf16 window of every segment whose first page the block
+// holds, and the aux warps merge that in too. A
 // segment split over several blocks is merged by the last block to finish its part: each
 // writes a partial (M, l, o[128]) to a per-block slot and counts itself in cnt[segment]; the
 // last one merges the slots, writes the output and resets the counter to 0.
